@@ -1,0 +1,369 @@
+"""Pins of the CPU oracle against what the number formats and the mathematics fix.
+
+Each test checks the oracle against something other than itself: the OCP bit-field
+definitions, exact closed forms, brute force with numpy/scipy on tiny shapes, and special
+cases (k = E is the plain softmax, identical experts make the output independent of the
+routing, zero routed weights leave the shared expert alone, scaling w2 by two doubles the
+routed part).  A plausible slip in the oracle (a dropped term, a swapped nibble, a wrong
+sign or index, gate and up swapped, a missing renormalisation) fails at least one of them.
+"""
+import math
+import struct
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from helpers import (bf16_decode, e2m1_value_from_bits, is_nearest_bf16, np_mxfp4_dequant,
+                     quantize_to_nearest_bf16_bits, silu)
+from moe_layer_tail_gb300 import inputs as gen
+
+# ------------------------------------------------------------------ formats ----
+
+
+def test_e2m1_all_codes_match_bit_fields_and_ocp_table():
+    ocp_magnitudes = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for code in range(16):
+        v = oracle.e2m1(code)
+        assert v == e2m1_value_from_bits(code)
+        assert abs(v) == ocp_magnitudes[code & 7]
+        assert math.copysign(1.0, v) == (-1.0 if code & 8 else 1.0)
+
+
+def _e8m0_by_float_bits(s: int) -> float:
+    if s == 0:
+        return struct.unpack("<f", struct.pack("<I", 0x00400000))[0]  # 2^-127, subnormal
+    return struct.unpack("<f", struct.pack("<I", s << 23))[0]
+
+
+@pytest.mark.parametrize("s", [0, 1, 126, 127, 128, 254])
+def test_e8m0_times_e2m1_exhaustive(s):
+    assert oracle.e8m0(s) == _e8m0_by_float_bits(s)
+    # one 32-element block holding every code twice, decoded through the packed-row routine
+    codes = np.array([(c & 15) | (((c + 1) & 15) << 4) for c in range(0, 32, 2)], np.uint8)
+    row = oracle.mxfp4_dequant_row(codes, np.array([s], np.uint8), 32)
+    expect = [e2m1_value_from_bits(k & 15) * math.ldexp(1.0, s - 127) for k in range(32)]
+    assert row.tolist() == expect
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 7, 30, 31, 32, 33, 62, 63])
+def test_nibble_order_single_nonzero(idx):
+    K = 64
+    codes = np.zeros(K // 2, np.uint8)
+    codes[idx // 2] = (0x3 << 4) if idx % 2 else 0x3  # code 3 = 1.5
+    scales = np.array([127, 128], np.uint8)           # block 0 x1, block 1 x2
+    row = oracle.mxfp4_dequant_row(codes, scales, K)
+    expect = np.zeros(K)
+    expect[idx] = 1.5 * (2.0 if idx >= 32 else 1.0)
+    assert np.array_equal(row, expect)
+
+
+def test_mxfp4_pack_roundtrip_and_numpy_decoder_agree():
+    rng = np.random.default_rng(11)
+    K = 256
+    codes_unpacked = rng.integers(0, 16, K)
+    scales = rng.integers(100, 150, K // 32).astype(np.uint8)
+    exact = np.array([e2m1_value_from_bits(int(c)) for c in codes_unpacked]) * \
+        np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32)
+    packed = (codes_unpacked[0::2] | (codes_unpacked[1::2] << 4)).astype(np.uint8)
+    assert np.array_equal(oracle.mxfp4_dequant_row(packed, scales, K), exact)
+    assert np.array_equal(np_mxfp4_dequant(packed, scales), exact)
+
+
+def test_bf16_round_hand_cases():
+    u = 2.0 ** -8
+    cases = [
+        (1.0, 0x3F80), (1.0 + u, 0x3F80),               # tie -> even (down)
+        (1.0 + 3 * u, 0x3F82),                          # tie -> even (up)
+        (1.0 + u + 2.0 ** -30, 0x3F81),                 # just above the tie
+        (-1.0 - u - 2.0 ** -30, 0xBF81),
+        (0.0, 0x0000), (-0.0, 0x8000),
+        (2.0 ** -133, 0x0001), (2.0 ** -134, 0x0000),   # smallest subnormal; tie to zero
+        (3 * 2.0 ** -134, 0x0002),                      # 1.5 quanta -> 2 (even)
+        ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),         # largest finite
+        (2.0 ** 128, 0x7F80), (-2.0 ** 130, 0xFF80),    # overflow -> inf
+        (float("inf"), 0x7F80),
+    ]
+    for v, bits in cases:
+        assert oracle.bf16_round(v) == bits, (v, hex(oracle.bf16_round(v)), hex(bits))
+    assert (oracle.bf16_round(float("nan")) & 0x7FC0) == 0x7FC0
+
+
+def test_bf16_round_matches_torch_on_float32_inputs():
+    # float32 -> bf16 is a single rounding in torch; the oracle rounds the same value once.
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.standard_normal(3000).astype(np.float32) * 10,
+                        rng.standard_normal(1000).astype(np.float32) * 1e-38,
+                        (rng.standard_normal(1000) * 1e30).astype(np.float32)])
+    t = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_round(float(x)) for x in v], np.uint16)
+    assert np.array_equal(got, t)
+
+
+def test_bf16_round_is_nearest_on_float64_inputs():
+    rng = np.random.default_rng(6)
+    v = rng.standard_normal(2000) * np.exp(rng.uniform(-30, 30, 2000))
+    got = np.array([oracle.bf16_round(float(x)) for x in v], np.uint16)
+    assert is_nearest_bf16(got, v, slack=0).all()
+    assert np.array_equal(got, quantize_to_nearest_bf16_bits(v))
+
+
+def test_silu_special_values():
+    assert oracle.silu(0.0) == 0.0
+    assert oracle.silu(50.0) == pytest.approx(50.0, rel=1e-15)
+    assert abs(oracle.silu(-50.0)) < 1e-19
+    for z in (-3.0, -0.5, 0.7, 2.0):
+        assert oracle.silu(z) == pytest.approx(z * scipy.special.expit(z), rel=1e-15)
+
+
+# --------------------------------------------------------- residual add + RMSNorm ----
+
+
+def test_rmsnorm_constant_row_closed_form():
+    H, eps = 64, 1e-6
+    rng = np.random.default_rng(3)
+    gamma = gen.to_bf16_bits(1 + 0.1 * rng.standard_normal(H))
+    for c in (0.75, -2.5, 1e-3, 96.0):
+        x = np.full((1, H), gen.to_bf16_bits(np.array([c]))[0], np.uint16)
+        res = np.zeros((1, H), np.uint16)
+        r_new, n, rstd = oracle.add_rmsnorm(x, res, gamma, eps)
+        cb = float(bf16_decode(x[0, 0]))
+        assert np.array_equal(r_new, x)
+        assert rstd[0] == pytest.approx(1.0 / math.sqrt(cb * cb + eps), rel=1e-15)
+        exact = np.sign(cb) * bf16_decode(gamma) * abs(cb) / math.sqrt(cb * cb + eps)
+        assert is_nearest_bf16(n[0], exact, slack=1e-12).all()
+
+
+def test_residual_add_rounds_once_and_rows_are_independent():
+    rng = np.random.default_rng(4)
+    R, H = 3, 96
+    x = gen.to_bf16_bits(rng.standard_normal((R, H)))
+    res = gen.to_bf16_bits(rng.standard_normal((R, H)) * 300)
+    gamma = gen.to_bf16_bits(np.ones(H))
+    r_new, n, rstd = oracle.add_rmsnorm(x, res, gamma, 1e-6)
+    exact = bf16_decode(x) + bf16_decode(res)
+    assert is_nearest_bf16(r_new, exact, slack=0).all()
+    # each row alone gives the same result
+    for r in range(R):
+        r1, n1, _ = oracle.add_rmsnorm(x[r:r + 1], res[r:r + 1], gamma, 1e-6)
+        assert np.array_equal(r1[0], r_new[r]) and np.array_equal(n1[0], n[r])
+    # the norm uses the rounded sum: rms of gamma=1 output is ~1
+    nv = bf16_decode(n)
+    assert np.allclose(np.sqrt((nv ** 2).mean(axis=1)), 1.0, rtol=2e-3)
+    rv = bf16_decode(r_new)
+    want = rv / np.sqrt((rv ** 2).mean(axis=1, keepdims=True) + 1e-6)
+    assert is_nearest_bf16(n, want, slack=1e-12).all()
+
+
+# --------------------------------------------------------------- router + top-k ----
+
+
+def test_router_matches_numpy_dot():
+    rng = np.random.default_rng(7)
+    R, H, E = 3, 64, 6
+    n = gen.to_bf16_bits(rng.standard_normal((R, H)))
+    w = gen.to_bf16_bits(rng.standard_normal((E, H)) / 8)
+    got = oracle.router(n, w)
+    want = bf16_decode(n) @ bf16_decode(w).T
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-13)
+    assert not np.allclose(got, bf16_decode(n) @ bf16_decode(w)[::-1].T)
+
+
+def _brute_topk(l, k):
+    order = sorted(range(len(l)), key=lambda e: (-np.float32(l[e]), e))
+    return order[:k]
+
+
+def test_topk_bruteforce_order_and_weights():
+    rng = np.random.default_rng(8)
+    R, E, k = 6, 12, 4
+    logits = rng.standard_normal((R, E))
+    ids, wts = oracle.topk(logits, k)
+    for r in range(R):
+        assert ids[r].tolist() == _brute_topk(logits[r], k)
+        p = scipy.special.softmax(logits[r])
+        want = p[ids[r]] / p[ids[r]].sum()
+        assert np.allclose(wts[r], want, rtol=1e-13)
+        assert np.allclose(wts[r], scipy.special.softmax(logits[r][ids[r]]), rtol=1e-13)
+        assert abs(wts[r].sum() - 1.0) < 1e-12
+        assert np.all(np.diff(wts[r]) <= 0)  # pick order = descending weight
+
+
+def test_topk_k_equals_E_is_plain_softmax():
+    rng = np.random.default_rng(9)
+    logits = rng.standard_normal((2, 9)) * 3
+    ids, wts = oracle.topk(logits, 9)
+    for r in range(2):
+        assert sorted(ids[r].tolist()) == list(range(9))
+        assert np.allclose(wts[r], scipy.special.softmax(logits[r])[ids[r]], rtol=1e-13)
+
+
+def test_topk_exact_ties_pick_lowest_id_in_order():
+    logits = np.array([[0.5, 2.0, 1.0, 2.0, 1.0, -1.0, 1.0]])
+    ids, wts = oracle.topk(logits, 4)
+    assert ids[0].tolist() == [1, 3, 2, 4]
+    assert wts[0][0] == wts[0][1] and wts[0][2] == wts[0][3]
+    # the rank key is the fp32 logit: values equal in fp32 tie even if they differ in fp64
+    a = 1.0
+    b = 1.0 + 2.0 ** -40
+    ids, _ = oracle.topk(np.array([[a, 0.0, b]]), 1)
+    assert ids[0, 0] == 0
+
+
+def test_router_identical_rows_tie_to_lowest_id():
+    rng = np.random.default_rng(10)
+    H, E = 64, 8
+    n = gen.to_bf16_bits(rng.standard_normal((1, H)))
+    w = gen.to_bf16_bits(rng.standard_normal((E, H)) / 8)
+    l0 = oracle.router(n, w)[0]
+    top = int(np.argmax(l0))
+    w[5] = w[top] if top != 5 else w[2]
+    twin = top if top != 5 else 2
+    ids, _ = oracle.topk(oracle.router(n, w), 2)
+    assert ids[0].tolist() == [min(twin, 5), max(twin, 5)]
+
+
+# ------------------------------------------------------------------- experts ----
+
+
+def _tiny_weights(seed, H=64, I=32, E=3, Is=32):
+    return gen.make_weights(gen.TailShape(1, H, E, 2, I, Is), seed)
+
+
+def test_routed_expert_bruteforce():
+    w = _tiny_weights(12)
+    H = w["w13_codes"].shape[2] * 2
+    I = w["w2_codes"].shape[2] * 2
+    rng = np.random.default_rng(12)
+    n = gen.to_bf16_bits(rng.standard_normal(H))
+    for e in range(3):
+        y, mid = oracle.expert(n, e, w["w13_codes"], w["w13_scales"], w["w2_codes"],
+                               w["w2_scales"])
+        W13 = np_mxfp4_dequant(w["w13_codes"][e], w["w13_scales"][e])
+        W2 = np_mxfp4_dequant(w["w2_codes"][e], w["w2_scales"][e])
+        nv = bf16_decode(n)
+        g, u = W13[:I] @ nv, W13[I:] @ nv
+        assert is_nearest_bf16(mid, silu(g) * u, slack=1e-12).all()
+        # gate and up are not interchangeable: swapping them changes mid
+        assert not np.array_equal(quantize_to_nearest_bf16_bits(silu(u) * g), mid)
+        assert np.allclose(y, W2 @ bf16_decode(mid), rtol=1e-12, atol=1e-12)
+
+
+def test_shared_expert_bruteforce():
+    w = _tiny_weights(13)
+    H, Is = w["ws2"].shape
+    rng = np.random.default_rng(13)
+    n = gen.to_bf16_bits(rng.standard_normal(H))
+    ys, ms = oracle.shared(n, w["ws13"], w["ws2"])
+    W13 = bf16_decode(w["ws13"])
+    nv = bf16_decode(n)
+    g, u = W13[:Is] @ nv, W13[Is:] @ nv
+    assert is_nearest_bf16(ms, silu(g) * u, slack=1e-12).all()
+    assert np.allclose(ys, bf16_decode(w["ws2"]) @ bf16_decode(ms), rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------- the whole tail ----
+
+
+def _tail_inputs(seed, R=3, H=64, E=6, k=2, I=32, Is=32):
+    shape = gen.TailShape(R, H, E, k, I, Is)
+    d = gen.make_weights(shape, seed)
+    d.update(gen.make_activations(shape, seed))
+    return shape, d
+
+
+def _numpy_tail(d, k, eps):
+    """Whole tail by brute force with numpy, independent of the oracle's code."""
+    x, res = bf16_decode(d["x"]), bf16_decode(d["residual"])
+    r_new = quantize_to_nearest_bf16_bits(x + res).reshape(x.shape)
+    rv = bf16_decode(r_new)
+    rstd = 1.0 / np.sqrt((rv ** 2).mean(axis=1, keepdims=True) + eps)
+    n = bf16_decode(quantize_to_nearest_bf16_bits(rv * rstd * bf16_decode(d["gamma"])))
+    n = n.reshape(x.shape)
+    logits = n @ bf16_decode(d["w_r"]).T
+    E = logits.shape[1]
+    I = d["w2_codes"].shape[2] * 2
+    Is = d["ws2"].shape[1]
+    out = np.zeros_like(x)
+    W13s, W2s = bf16_decode(d["ws13"]), bf16_decode(d["ws2"])
+    for r in range(x.shape[0]):
+        ids = _brute_topk(logits[r], k)
+        p = scipy.special.softmax(logits[r])
+        wts = p[ids] / p[ids].sum()
+        acc = np.zeros(x.shape[1])
+        for i, e in enumerate(ids):
+            W13 = np_mxfp4_dequant(d["w13_codes"][e], d["w13_scales"][e])
+            W2 = np_mxfp4_dequant(d["w2_codes"][e], d["w2_scales"][e])
+            g, u = W13[:I] @ n[r], W13[I:] @ n[r]
+            mid = bf16_decode(quantize_to_nearest_bf16_bits(silu(g) * u))
+            acc += wts[i] * (W2 @ mid)
+        g, u = W13s[:Is] @ n[r], W13s[Is:] @ n[r]
+        ms = bf16_decode(quantize_to_nearest_bf16_bits(silu(g) * u))
+        acc += W2s @ ms
+        out[r] = acc
+    return r_new, out
+
+
+def test_whole_tail_matches_numpy_bruteforce():
+    shape, d = _tail_inputs(21)
+    got = oracle.moe_tail(d, shape.k, shape.eps)
+    r_new, out_exact = _numpy_tail(d, shape.k, shape.eps)
+    assert np.array_equal(got["residual"], r_new)
+    assert is_nearest_bf16(got["out"], out_exact, slack=1e-9).all()
+    assert abs(got["wts"].sum(axis=1) - 1).max() < 1e-12
+
+
+def test_identical_experts_make_output_routing_independent():
+    shape, d = _tail_inputs(22, R=4, E=5, k=3)
+    for key in ("w13_codes", "w13_scales", "w2_codes", "w2_scales"):
+        d[key] = np.repeat(d[key][:1], shape.E, axis=0)
+    got = oracle.moe_tail(d, shape.k, shape.eps)
+    _, n, _ = oracle.add_rmsnorm(d["x"], d["residual"], d["gamma"], shape.eps)
+    for r in range(shape.R):
+        y, _ = oracle.expert(n[r], 0, d["w13_codes"], d["w13_scales"], d["w2_codes"],
+                             d["w2_scales"])
+        ys, _ = oracle.shared(n[r], d["ws13"], d["ws2"])
+        assert is_nearest_bf16(got["out"][r], y + ys, slack=1e-12).all()
+
+
+def test_zero_routed_weights_leave_shared_expert():
+    shape, d = _tail_inputs(23)
+    d["w13_codes"][:] = 0
+    d["w2_codes"][:] = 0
+    got = oracle.moe_tail(d, shape.k, shape.eps)
+    r_new, out_exact = _numpy_tail(d, shape.k, shape.eps)
+    assert is_nearest_bf16(got["out"], out_exact, slack=1e-9).all()
+    assert np.count_nonzero(got["out"]) > 0
+
+
+def test_doubling_w2_scales_doubles_routed_part_exactly():
+    shape, d = _tail_inputs(24)
+    d["ws2"][:] = 0  # remove the shared expert's contribution
+    base = oracle.moe_tail(d, shape.k, shape.eps)
+    d2 = dict(d)
+    d2["w2_scales"] = (d["w2_scales"].astype(np.int32) + 1).astype(np.uint8)
+    twice = oracle.moe_tail(d2, shape.k, shape.eps)
+    assert np.array_equal(bf16_decode(twice["out"]), 2 * bf16_decode(base["out"]))
+    assert np.array_equal(twice["ids"], base["ids"])
+
+
+def test_oracle_is_deterministic_and_thread_count_invariant():
+    shape, d = _tail_inputs(25, R=4, E=8, k=3)
+    a = oracle.moe_tail(d, shape.k, shape.eps, nthreads=1)
+    b = oracle.moe_tail(d, shape.k, shape.eps, nthreads=1)
+    c = oracle.moe_tail(d, shape.k, shape.eps, nthreads=5)
+    for key in ("out", "residual", "ids", "wts", "logits"):
+        assert np.array_equal(a[key], b[key]) and np.array_equal(a[key], c[key])
+
+
+def test_tiny_workload_runs_and_inputs_are_reproducible():
+    d1 = gen.make_inputs("tiny")
+    d2 = gen.make_inputs("tiny")
+    for key in d1:
+        assert np.array_equal(d1[key], d2[key])
+    wl = gen.WORKLOADS["tiny"]
+    got = oracle.moe_tail(d1, wl.shape.k, wl.shape.eps)
+    assert got["out"].shape == (1, 256)
+    assert np.isfinite(bf16_decode(got["out"])).all()
