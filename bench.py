@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the decode-step MoE layer tail on GB300: microseconds per call and achieved
+HBM GB/s, for the 8-row, 256-expert top-8 workload with ~40% repeated picks
+(r8_h7168_e256k8_similar: H 7168, I 2048, shared inter 2048).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one full call of the tail (add+RMSNorm, router, top-k, dedup, routed MXFP4
+experts, bf16 shared expert, combine) on its own 8-row input set.  Each step streams
+~1 GB of weights, larger than the 126 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are independent replicas: the
+path has no cross-GPU exchange; value = all ranks' calls / max-over-ranks time.
+
+--impl reference times the CPU oracle (plain C, fp64) on the host cores instead, each step
+one bounded sample (one row of a call), scaled to microseconds per call.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from moe_layer_tail_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "us_per_call"
+UNIT = "us/call"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=gen.BENCH_WORKLOAD)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stage_bytes(shape, D, R):
+    """Algorithmic bytes of the gate/up and down launches (weights once + activations)."""
+    H, I, Is = shape.H, shape.I, shape.Is
+    gu = D * 2 * I * (H // 2 + H // 32) + 2 * Is * H * 2 + R * H * 2 * 2
+    dn = D * H * (I // 2 + I // 32) + H * Is * 2 + D * I * 2
+    return gu, dn
+
+
+def ncu_traffic(kernel_tag, src_hash):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it was taken on
+    the current source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(kernel_tag)
+    if not rec or rec.get("source_hash") != src_hash:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------- our arm ----
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import moe_layer_tail_gb300 as mt
+
+    torch.cuda.set_device(local_rank)
+    wl = gen.WORKLOADS[args.workload]
+    shape = wl.shape
+    R = shape.R
+    K, W = args.steps, args.warmup
+    nsets = K + W
+    host_w = gen.make_weights(shape, wl.seed)
+    dev_w = mt.weights_to_device(host_w)
+    # one input set per step: correlated rows (~40% repeated picks), seeds wl.seed + 1000*i
+    xs, rs = [], []
+    c = gen.similar_c() if wl.kind == "similar" else None
+    for i in range(nsets):
+        a = gen.make_activations(shape, wl.seed + 1000 * i, wl.kind, c)
+        xs.append(a["x"])
+        rs.append(a["residual"])
+    x_all = mt.acts_to_device(np.stack(xs))
+    res0 = mt.acts_to_device(np.stack(rs))
+    res = res0.clone()
+    out = torch.empty_like(x_all)
+    tail = mt.MoeTail(shape, dev_w, max_rows=R)
+    nst = tail.launches_per_run(R)
+    stream = torch.cuda.current_stream()
+
+    # warm-up
+    for i in range(W):
+        tail.run(x_all[i], res[i], out[i])
+    torch.cuda.synchronize()
+
+    # per-step stage events (recorded by the library around each launch, on our stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(K)]
+    # torch creates events lazily: record once so each handle exists
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    ev_handles = [[e.cuda_event for e in row] for row in evs]
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        tail.set_stage_events(ev_handles[i])
+        tail.run(x_all[W + i], res[W + i], out[W + i], stream=stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    tail.set_stage_events(None)
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    status = tail.status()
+
+    stage_ms = np.array([[row[2 * s].elapsed_time(row[2 * s + 1]) for s in range(nst)]
+                         for row in evs])  # [K, stages]
+
+    # distinct experts of every timed set (replayed untimed from pristine residuals)
+    Ds = []
+    res_chk = res0.clone()
+    for i in range(K):
+        tail.run(x_all[W + i], res_chk[W + i], out[W + i])
+        _, _, nd = tail.routing(R)
+        Ds.append(nd)
+    Ds = np.array(Ds)
+    bytes_per = np.array([gen.algorithmic_bytes(shape, int(d)) for d in Ds])
+    total_bytes = float(bytes_per.sum())
+    us_per_call = elapsed_ms * 1000.0 / (K * world)
+    gbps = total_bytes * world / (elapsed_ms * 1e-3) / 1e9
+
+    # dominant kernel: the stage with the largest total time
+    names = ["add_rmsnorm", "router", "topk_dedup", "stream_gate_up", "stream_down", "combine"]
+    if nst != len(names):
+        names = ["stage%d" % s for s in range(nst)]
+    tot = stage_ms.sum(axis=0)
+    dom = int(np.argmax(tot))
+    gu_b, dn_b = zip(*[stage_bytes(shape, int(d), R) for d in Ds])
+    dom_bytes = {"stream_gate_up": np.mean(gu_b), "stream_down": np.mean(dn_b)}.get(names[dom])
+    peak, peak_kind = peaks()
+    roof = None
+    if dom_bytes is not None:
+        dur_s = tot[dom] / K * 1e-3
+        achieved = dom_bytes / dur_s / 1e9
+        src = source_hash(["moe_layer_tail_gb300/csrc/k_stream.cu",
+                           "moe_layer_tail_gb300/csrc/moe_tail_internal.cuh"])
+        tr = ncu_traffic(names[dom], src)
+        roof = {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": tr,
+                "algorithmic_bytes_per_launch": int(dom_bytes),
+                "launch_us": round(tot[dom] / K * 1000, 2)}
+
+    result = {
+        "metric": METRIC, "value": round(us_per_call, 3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(elapsed_ms / K, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "rows": R, "hidden": shape.H, "experts": shape.E,
+                   "top_k": shape.k, "expert_inter": shape.I, "shared_inter": shape.Is,
+                   "weights": "MXFP4 routed experts, bf16 router and shared expert",
+                   "distinct_experts_mean": round(float(Ds.mean()), 2),
+                   "repeat_fraction_mean": round(float(1 - Ds.mean() / (R * shape.k)), 3),
+                   "bytes_per_call_mean": int(bytes_per.mean()),
+                   "input_sets": nsets,
+                   "l2": "no flush: each step streams ~%.0f MB of weights, larger than the "
+                         "126 MB L2" % (bytes_per.mean() / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "gbps": round(gbps, 1),
+        "hbm_frac_of_%s_peak" % peak_kind: round(gbps / peak, 4),
+        "stages_us": {n: round(float(tot[i] / K * 1000), 2) for i, n in enumerate(names)},
+        "roofline": roof,
+        "clocks": clk,
+        "gpu_launches": int(K * nst),
+        "device_status": status,
+    }
+
+    # end to end through the C ABI with host buffers (H2D/D2H inside the timed region)
+    if not args.no_e2e:
+        import torch as _t
+        ke = min(K, 200)
+        hx = [_t.from_numpy(xs[W + i].view(np.int16)).view(_t.bfloat16).pin_memory()
+              for i in range(ke)]
+        hr = [_t.from_numpy(rs[W + i].view(np.int16).copy()).view(_t.bfloat16).pin_memory()
+              for i in range(ke)]
+        ho = _t.empty((R, shape.H), dtype=_t.bfloat16).pin_memory()
+        tail.run_host(hx[0], hr[0].clone().pin_memory(), ho)  # warm the staging path
+        _t.cuda.synchronize()
+        ts = time.perf_counter()
+        for i in range(ke):
+            tail.run_host(hx[i], hr[i], ho)
+        te = time.perf_counter()
+        e2e_us = (te - ts) * 1e6 / ke
+        result["e2e"] = {"value": round(e2e_us / world, 3), "unit": UNIT,
+                         "h2d_bytes_per_step": 2 * R * shape.H * 2,
+                         "d2h_bytes_per_step": 2 * R * shape.H * 2, "steps": ke,
+                         "api": "moe_tail_run_host (pinned host x/residual in, out/residual back)"}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(shape, host_w, xs[W], rs[W])
+    tail.close()
+    return result
+
+
+def cpu_baseline(shape, host_w, x, r, budget_s=20.0):
+    """The oracle, as it stands, on the host cores: whole calls of the workload until the
+    budget is used (at least one)."""
+    import oracle
+    cores = oracle.host_cores()
+    d = dict(host_w)
+    d["x"] = x
+    d["residual"] = r
+    times = []
+    t_start = time.perf_counter()
+    while not times or (time.perf_counter() - t_start < budget_s and len(times) < 5):
+        t = time.perf_counter()
+        oracle.moe_tail(d, shape.k, shape.eps, nthreads=cores)
+        times.append(time.perf_counter() - t)
+    us = statistics.median(times) * 1e6
+    return {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d whole call(s) of the same workload (8 rows), median" % len(times)}
+
+
+# --------------------------------------------------------------- reference arm ----
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores, each step one row of the workload through the whole
+    tail (routing, its k experts, shared expert, combine); microseconds per call = per-row
+    time x rows."""
+    import oracle
+    wl = gen.WORKLOADS[args.workload]
+    shape = wl.shape
+    R = shape.R
+    cores = oracle.host_cores()
+    host_w = gen.make_weights(shape, wl.seed)
+    c = gen.similar_c() if wl.kind == "similar" else None
+    K, W = args.steps, args.warmup
+    a = gen.make_activations(shape, wl.seed, wl.kind, c)
+    samples = []
+    for i in range(W + K):
+        rr = i % R
+        d = dict(host_w)
+        d["x"] = a["x"][rr:rr + 1]
+        d["residual"] = a["residual"][rr:rr + 1]
+        t = time.perf_counter()
+        oracle.moe_tail(d, shape.k, shape.eps, nthreads=cores)
+        if i >= W:
+            samples.append(time.perf_counter() - t)
+    step_s = float(np.mean(samples))
+    us_per_call = step_s * R * 1e6
+    return {"impl": "reference", "metric": METRIC, "value": round(us_per_call, 1), "unit": UNIT,
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(step_s * 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "rows": R, "hidden": shape.H, "experts": shape.E,
+                       "top_k": shape.k, "expert_inter": shape.I, "shared_inter": shape.Is},
+            "cpu_baseline": {"value": round(us_per_call, 1), "unit": UNIT, "cores": cores,
+                             "kind": "oracle",
+                             "sample": "each step: one row of the workload through the whole "
+                                       "tail; us per call = mean row time x %d rows" % R},
+            "e2e": {"value": round(us_per_call, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        res = run_reference(args, rank, world)
+        print(json.dumps(res), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,158 @@
+/*
+ * moe_tail.h -- C ABI of the single-GPU decode-step MoE layer tail (libmoe_tail.so, sm_103a).
+ *
+ * The operation (one call, 1..max_rows token rows):
+ *   1. residual add + RMSNorm:  s = x + residual;  r_new = bf16(s);
+ *      n = bf16(r_new * rstd * gamma),  rstd = 1/sqrt(mean(r_new^2) + eps)
+ *      -- "[AMD] integrate kimi k3 monokernel", Kernel Replacement table, row "The
+ *         post-attention norm" (a fused add + RMSNorm kernel).
+ *   2. router GEMV:  logits[r, e] = n[r, :] . W_r[e, :]  (bf16 inputs, fp32 accumulation)
+ *      -- same table, row "The router".
+ *   3. softmax + top-k + renormalisation (norm_topk_prob): the k experts with the largest
+ *      logits, exact ties to the lowest expert id, in that pick order; weight of pick i =
+ *      softmax restricted to the picked logits
+ *      -- same table, row "The top-k"; section Refusals (norm_topk_prob is required);
+ *         "glm53: Long-context indexer ..." page, Modifications table row 9 (top-8 tie
+ *         shortcut: only an exact tie runs the id reduction, the pick order is unchanged).
+ *   4. routed MXFP4 experts, each distinct expert streamed once per call:
+ *      mid = bf16(SiLU(n . gate_j) * (n . up_j)),  y = mid . down
+ *      -- Kernel Replacement row "The routed experts" (g1u1 = gate and up, SiLU);
+ *         GLM-5.3 page, Modifications rows 16, 17, 20 (each expert once in up/gate and down).
+ *   5. bf16 shared expert: ms = bf16(SiLU(n . Wg_j) * (n . Wu_j)),  ys = ms . Ws2
+ *      -- Kernel Replacement rows "The shared expert gate_up / SiLU and mul / down".
+ *   6. combine + residual update: out = bf16(sum over picks, in pick order, of
+ *      w_i * y_i + ys);  residual <- r_new
+ *      -- Kernel checks table (`out` and `res_out`).
+ *
+ * Storage formats (all row-major, contiguous, device memory, 16-byte aligned):
+ *   bf16 values are IEEE bfloat16 bit patterns (uint16).
+ *   MXFP4 (OCP): a row of K elements is K/2 code bytes (byte j: element 2j in the low
+ *   nibble, 2j+1 in the high nibble; E2M1 codes) plus K/32 E8M0 scale bytes (2^(s-127)),
+ *   scale b covering elements [32b, 32b+32).
+ *
+ * Return codes: 0 on success, a negative MOE_TAIL_ERR_* otherwise (moe_tail_strerror).
+ * No entry point throws, aborts or prints.
+ */
+#ifndef MOE_TAIL_H
+#define MOE_TAIL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_TAIL_OK = 0,
+  MOE_TAIL_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, rows outside [1, max_rows] */
+  MOE_TAIL_ERR_UNSUPPORTED = -2,   /* shape or option the library does not build */
+  MOE_TAIL_ERR_CUDA = -3,          /* a CUDA call failed; moe_tail_last_cuda_error() */
+  MOE_TAIL_ERR_TIMEOUT = -4,       /* a device-side wait ran past its budget */
+  MOE_TAIL_ERR_NOT_CORESIDENT = -5,/* persistent mode cannot keep its whole grid resident */
+  MOE_TAIL_ERR_DEVICE = -6         /* a device-side check failed (see moe_tail_get_status) */
+};
+
+/* Execution modes. */
+enum {
+  MOE_TAIL_MODE_MULTI_KERNEL = 0,  /* one launch per stage, stream-ordered */
+  MOE_TAIL_MODE_PERSISTENT = 1     /* reserved: one resident launch with in-kernel flags */
+};
+
+/* debug_flags bits. */
+enum {
+  /* Run the expert stages with the warp-per-row CUDA-core kernels instead of the
+   * TMA-streaming kernels (same results within the parity rule; for cross-checking). */
+  MOE_TAIL_DEBUG_SIMPLE_KERNELS = 1
+};
+
+typedef struct moe_tail moe_tail_t; /* opaque handle */
+
+typedef struct {
+  int32_t max_rows;       /* 1..16: the largest `rows` any run will pass */
+  int32_t hidden;         /* H: multiple of 128 */
+  int32_t n_experts;      /* E: 1..1024 */
+  int32_t top_k;          /* k: 1..min(E, 32) */
+  int32_t expert_inter;   /* I: multiple of 128 */
+  int32_t shared_inter;   /* Is: multiple of 64 */
+  float rms_eps;          /* RMSNorm epsilon (> 0) */
+  int32_t norm_topk_prob; /* must be 1: the picked weights are renormalised to sum to 1 */
+  int32_t mode;           /* MOE_TAIL_MODE_* */
+  uint32_t wait_budget_us;/* budget of any device-side wait, microseconds; 0 = 100000 */
+  uint32_t debug_flags;   /* 0 in production */
+} moe_tail_config_t;
+
+/* Weights are BORROWED device pointers: the caller keeps them alive and unmodified until
+ * moe_tail_destroy.  The library never copies or writes them. */
+typedef struct {
+  const void* gamma;       /* bf16 [H] */
+  const void* router_w;    /* bf16 [E, H] */
+  const void* w13_codes;   /* u8 [E, 2I, H/2]  rows [0, I) gate, [I, 2I) up */
+  const void* w13_scales;  /* u8 E8M0 [E, 2I, H/32] */
+  const void* w2_codes;    /* u8 [E, H, I/2] */
+  const void* w2_scales;   /* u8 E8M0 [E, H, I/32] */
+  const void* shared_w13;  /* bf16 [2Is, H]  rows [0, Is) gate, [Is, 2Is) up */
+  const void* shared_w2;   /* bf16 [H, Is] */
+} moe_tail_weights_t;
+
+/* Validate the configuration and weights, allocate every scratch buffer the runs need on
+ * the current CUDA device, and return a handle in *out.  Unsupported configurations are
+ * refused here (MOE_TAIL_ERR_UNSUPPORTED), never at run time.  On error *out is NULL and
+ * nothing is left allocated. */
+int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weights_t* w,
+                    moe_tail_t** out);
+
+/* Enqueue one call on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   x        bf16 [rows, H] device, read only
+ *   residual bf16 [rows, H] device, read and overwritten with bf16(x + residual)
+ *   out      bf16 [rows, H] device, written with the MoE output
+ * x, residual and out must not overlap.  The call allocates nothing, never synchronises
+ * and is valid inside CUDA graph capture.  One stream at a time per handle: the handle's
+ * scratch is reused by every call, so two calls on the same handle must be stream-ordered.
+ * Device-side failures are reported by moe_tail_get_status, not by this return value. */
+int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* out, int32_t rows,
+                 void* stream);
+
+/* The same call on HOST buffers: copies x and residual to the handle's device staging
+ * buffers, runs, copies residual and out back, and synchronises `stream` before returning.
+ * Pinned host memory gives asynchronous copies; pageable memory works too. */
+int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host, void* out_host,
+                      int32_t rows, void* stream);
+
+/* Synchronise the device and read the handle's device status word (0 = no failure).  A
+ * nonzero word is sticky until moe_tail_clear_status. Returns MOE_TAIL_ERR_DEVICE when the
+ * word is nonzero, MOE_TAIL_OK otherwise. */
+int moe_tail_get_status(moe_tail_t* h, int32_t* device_status);
+int moe_tail_clear_status(moe_tail_t* h);
+
+/* Copy the routing of the last run on `stream` (stream-ordered, synchronises it):
+ * ids int32 [rows, k] and wts float [rows, k] in pick order, and the number of distinct
+ * experts the call streamed.  Any output pointer may be NULL.  Host pointers. */
+int moe_tail_debug_routing(moe_tail_t* h, int32_t* ids, float* wts, int32_t* n_distinct,
+                           void* stream);
+
+/* Optional per-stage timing.  When `events` is non-NULL, every later moe_tail_run records
+ * events[2*i] before and events[2*i+1] after its stage i on the call's stream (stages in
+ * launch order: add+RMSNorm, router, top-k+dedup, expert launches..., combine; see
+ * moe_tail_launches_per_run).  The events are cudaEvent_t handles owned by the caller and
+ * must outlive the runs that record them; n_events must be at least twice the launch
+ * count.  NULL (or n_events = 0) turns the recording off.  The array is copied. */
+int moe_tail_set_stage_events(moe_tail_t* h, void* const* events, int32_t n_events);
+
+/* Number of kernels one moe_tail_run enqueues for `rows` rows (for launch accounting). */
+int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows);
+
+/* Free the handle and its scratch (synchronises the device first).  NULL is a no-op. */
+void moe_tail_destroy(moe_tail_t* h);
+
+/* Static text for a return code. */
+const char* moe_tail_strerror(int code);
+
+/* Text of the last CUDA error seen by any entry point on this thread ("" if none). */
+const char* moe_tail_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_TAIL_H */

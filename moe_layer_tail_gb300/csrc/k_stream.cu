@@ -1,0 +1,646 @@
+// k_stream.cu -- the weight-streaming expert kernels: every distinct routed expert and the
+// shared expert stream their weights from HBM exactly once per call.
+//
+// Work: the gate/up launch (PHASE 0) runs the shared expert's gate/up tiles and, for each
+// distinct routed expert d and each group of 32 intermediate columns, the 32 gate + 32 up
+// MXFP4 rows against every row that picked d.  The down launch (PHASE 1) runs the shared
+// down tiles and, for each distinct expert and 64 hidden outputs, the 64 MXFP4 w2 rows
+// against each pick's SiLU*up vector.  A row's result never depends on which other rows
+// share its expert: each output column of the contraction belongs to one user.
+//
+// Sources: "[AMD] integrate kimi k3 monokernel" page, Kernel Replacement rows "The routed
+// experts" and "The shared expert gate_up / SiLU and mul / down"; "glm53: Long-context
+// indexer ..." page, Modifications rows 16 (each expert once in up/gate and down, every
+// using row as a column of one multi-column product), 17 (no work for experts nobody
+// picked), 18 (wide weight loads) and 21 (weights read once per call bypass the caches).
+//
+// Machine mapping (sm_103a):
+//   * one CTA per SM, one producer warp + 8 consumer warps, items taken from a global
+//     atomic counter (dynamic balance across the 152 SMs);
+//   * the producer streams 8 KB weight tiles with 2D TMA loads (64-byte swizzle) and the
+//     users' activation slices with 1D bulk copies into an 8-stage shared-memory ring
+//     guarded by mbarriers (transaction counts), and copies the E8M0 / activation scales
+//     with cp.async that arrive on the same mbarriers;
+//   * consumer warp w owns 32 K-elements of every stage: it decodes MXFP4 pairs with
+//     cvt.rn.f16x2.e2m1x2 straight into mma.m16n8k16 A fragments (weights = M rows, users =
+//     N columns), applies the per-block weight x activation scale to each block's fp32
+//     product, and accumulates in fp32; the 8 warps' partial sums are added in warp order.
+//   * activations enter the routed contractions as f16 with a power-of-two scale per
+//     32-element block (exact for bf16 values in range); the shared expert runs bf16 x bf16.
+//   * every mbarrier wait is bounded by a %globaltimer budget; on expiry the kernel sets
+//     the status word and leaves.
+#include "moe_tail_internal.cuh"
+
+namespace mtail {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 8;
+constexpr int kKChunk = 256;             // K elements per stage
+constexpr int kStageW = 8192;            // weight bytes per stage
+constexpr int kActStride = 576;          // bytes per user row per stage (512 + 64 pad)
+constexpr int kStageA = kMaxRows * kActStride;
+constexpr int kStageWS = 512;            // weight scales: 64 rows x 8 blocks
+constexpr int kStageAS = kMaxRows * 32;  // activation scales: 16 users x 8 floats
+constexpr int kStageBytes = kStageW + kStageA + kStageWS + kStageAS;
+constexpr int kRedBytes = kConsumerWarps * 4 * 2 * 512;  // [warp][tile][nt][lane] float4
+constexpr int kStreamSmem = 1024 + kStages * kStageBytes + kRedBytes + 256;
+
+static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+
+enum : int { kSharedGU = 0, kRoutedGU = 1, kSharedDN = 2, kRoutedDN = 3 };
+
+struct Item {
+  int kind;
+  int e, d;
+  int row0, row1;  // tensor-map rows: gate/single half, up half
+  int out0;        // first output index (j for gate/up, h for down)
+  int K, nst;
+  int U, u0;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
+                                            const Scratch& s, int D) {
+  Item it;
+  it.d = 0;
+  it.e = 0;
+  it.u0 = 0;
+  if (phase == 0) {
+    const int ns = dm.Is / 8;
+    it.K = dm.H;
+    if (item < ns) {
+      it.kind = kSharedGU;
+      it.out0 = item * 8;
+      it.row0 = it.out0;
+      it.row1 = dm.Is + it.out0;
+      it.U = dm.R;
+    } else {
+      const int q = item - ns, per = dm.I / 32;
+      it.kind = kRoutedGU;
+      it.d = min(q / per, D - 1);
+      const int jg = q % per;
+      it.e = s.uniq[it.d];
+      it.out0 = jg * 32;
+      it.row0 = it.e * 2 * dm.I + it.out0;
+      it.row1 = it.row0 + dm.I;
+      it.u0 = s.user_off[it.d];
+      it.U = s.user_off[it.d + 1] - it.u0;
+    }
+  } else {
+    const int ns = dm.H / 16;
+    if (item < ns) {
+      it.kind = kSharedDN;
+      it.K = dm.Is;
+      it.out0 = item * 16;
+      it.row0 = it.out0;
+      it.row1 = 0;
+      it.U = dm.R;
+    } else {
+      const int q = item - ns, per = dm.H / 64;
+      it.kind = kRoutedDN;
+      it.K = dm.I;
+      it.d = min(q / per, D - 1);
+      const int hg = q % per;
+      it.e = s.uniq[it.d];
+      it.out0 = hg * 64;
+      it.row0 = it.e * dm.H + it.out0;
+      it.row1 = 0;
+      it.u0 = s.user_off[it.d];
+      it.U = s.user_off[it.d + 1] - it.u0;
+    }
+  }
+  it.U = max(0, min(it.U, kMaxRows));
+  it.nst = (it.K + kKChunk - 1) / kKChunk;
+  return it;
+}
+
+// ------------------------------------------------------------------ PTX wrappers ----
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+               "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* b) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(b))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: false when the budget ran out (the caller records the timeout).
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint64_t budget_ns) {
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((i & 63) == 0 && globaltimer() - t0 > budget_ns) return false;
+  }
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
+                                       uint32_t& d) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void cvt_e2m1x4(uint32_t w, uint32_t* h) {
+  e2m1x8_to_f16x2(w, h[0], h[1], h[2], h[3]);
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Byte address of 16-byte chunk c of row r in a box of 64-byte rows written by TMA with
+// the 64-byte swizzle (chunk index XOR bits 1..2 of the row; box base 512-byte aligned).
+__device__ __forceinline__ uint32_t swz64(uint32_t base, int r, int c) {
+  return base + (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+// ------------------------------------------------------------------------ kernel ----
+
+template <int PHASE>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
+         uint64_t budget_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* stages = smem;
+  float4* red = (float4*)(smem + kStages * kStageBytes);
+  uint64_t* full = (uint64_t*)(smem + kStages * kStageBytes + kRedBytes);
+  uint64_t* empty = full + kStages;
+  int* info = (int*)(empty + kStages);  // [kStages][2]: item, k-chunk
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int D = *s.n_distinct;
+  const int n_items = (PHASE == 0) ? dm.Is / 8 + D * (dm.I / 32) : dm.H / 16 + D * (dm.H / 64);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1 + 32);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer ----
+    const uint64_t pol = policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (;;) {
+      int item = 0;
+      if (lane == 0) item = (int)atomicAdd(&s.counters[PHASE], 1u);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (item >= n_items) break;
+      const Item it = decode_item(PHASE, item, dm, s, D);
+      for (int kc = 0; kc < it.nst && ok; ++kc) {
+        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, budget_ns);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        uint8_t* st = stages + stage * kStageBytes;
+        uint8_t* sw = st;
+        uint8_t* sa = st + kStageW;
+        uint8_t* sws = sa + kStageA;
+        uint8_t* sas = sws + kStageWS;
+        const int k0 = kc * kKChunk;
+        const int kval = min(kKChunk, it.K - k0);  // multiple of 128 (routed) / 64 (shared)
+        if (lane == 0) {
+          info[stage * 2] = item;
+          info[stage * 2 + 1] = kc;
+          uint32_t bytes = 0;
+          if (it.kind == kRoutedGU) bytes = (uint32_t)(kval / 128) * 2 * 2048;
+          else if (it.kind == kRoutedDN) bytes = (uint32_t)(kval / 128) * 4096;
+          else if (it.kind == kSharedGU) bytes = (uint32_t)(kval / 32) * 1024;
+          else bytes = (uint32_t)(kval / 32) * 1024;
+          bytes += (uint32_t)it.U * (uint32_t)kval * 2u;
+          mbar_expect_tx(&full[stage], bytes);
+          if (it.kind == kRoutedGU) {
+            for (int b = 0; b < kval / 128; ++b) {
+              tma_load_2d(sw + b * 2048, &maps.w13, (k0 >> 1) + b * 64, it.row0, &full[stage], pol);
+              tma_load_2d(sw + 4096 + b * 2048, &maps.w13, (k0 >> 1) + b * 64, it.row1,
+                          &full[stage], pol);
+            }
+          } else if (it.kind == kRoutedDN) {
+            for (int b = 0; b < kval / 128; ++b)
+              tma_load_2d(sw + b * 4096, &maps.w2, (k0 >> 1) + b * 64, it.row0, &full[stage], pol);
+          } else if (it.kind == kSharedGU) {
+            for (int q = 0; q < kval / 32; ++q) {
+              tma_load_2d(sw + q * 1024, &maps.ws13, k0 + q * 32, it.row0, &full[stage], pol);
+              tma_load_2d(sw + q * 1024 + 512, &maps.ws13, k0 + q * 32, it.row1, &full[stage], pol);
+            }
+          } else {
+            for (int q = 0; q < kval / 32; ++q)
+              tma_load_2d(sw + q * 1024, &maps.ws2, k0 + q * 32, it.row0, &full[stage], pol);
+          }
+          // activation slices of the users (f16 scaled for routed, bf16 for shared)
+          for (int u = 0; u < it.U; ++u) {
+            const void* src;
+            if (it.kind == kSharedGU) src = s.n + (size_t)u * dm.H + k0;
+            else if (it.kind == kSharedDN) src = s.ms + (size_t)u * dm.Is + k0;
+            else if (it.kind == kRoutedGU) src = s.n16 + (size_t)(s.user_list[it.u0 + u] / dm.k) * dm.H + k0;
+            else src = s.mid16 + (size_t)s.user_list[it.u0 + u] * dm.I + k0;
+            bulk_load(sa + u * kActStride, src, (uint32_t)kval * 2u, &full[stage]);
+          }
+        }
+        // scales (routed only), copied by all producer lanes with cp.async
+        if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
+          const int kb = it.K / 32;           // scale bytes per weight row
+          const int words = kval / 128;       // 4-byte words per row in this stage (1 or 2)
+          for (int c = lane; c < 64 * 2; c += 32) {
+            const int row = c >> 1, wd = c & 1;
+            if (wd >= words) continue;
+            size_t grow;
+            const uint8_t* base;
+            if (it.kind == kRoutedGU) {
+              grow = (row < 32) ? (size_t)it.row0 + row : (size_t)it.row1 + (row - 32);
+              base = w.w13s;
+            } else {
+              grow = (size_t)it.row0 + row;
+              base = w.w2s;
+            }
+            cp_async4(sws + row * 8 + wd * 4, base + grow * kb + (k0 / 32) + wd * 4);
+          }
+          for (int c = lane; c < it.U * 2; c += 32) {
+            const int u = c >> 1, half = c & 1;
+            if (half >= words) continue;
+            const float* src;
+            if (it.kind == kRoutedGU)
+              src = s.n16s + (size_t)(s.user_list[it.u0 + u] / dm.k) * (dm.H / 32) + k0 / 32 + half * 4;
+            else
+              src = s.mid16s + (size_t)s.user_list[it.u0 + u] * (dm.I / 32) + k0 / 32 + half * 4;
+            cp_async16(sas + u * 32 + half * 16, src);
+          }
+        }
+        cp_async_arrive_noinc(&full[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+    }
+    if (ok) {
+      // end-of-work marker
+      if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, budget_ns);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (ok) {
+        if (lane == 0) {
+          info[stage * 2] = -1;
+          info[stage * 2 + 1] = 0;
+          mbar_arrive(&full[stage]);
+        }
+        cp_async_arrive_noinc(&full[stage]);
+      }
+    }
+    if (!ok && lane == 0) set_status(s.status, kStatusTimeout);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers ----
+  const int cw = warp - 1;            // K-slot of every stage this warp owns
+  const int g = lane >> 2, t = lane & 3;
+  int stage = 0;
+  uint32_t phase = 0;
+  int cur = -1;
+  Item it;
+  it.kind = 0; it.nst = 0; it.U = 0; it.K = 0; it.out0 = 0; it.u0 = 0; it.row0 = 0; it.row1 = 0;
+  it.e = 0; it.d = 0;
+  float acc[4][2][4];
+  const uint32_t sbase = smem_u32(stages);
+  for (;;) {
+    if (!mbar_wait(&full[stage], phase, budget_ns)) {
+      if (lane == 0) set_status(s.status, kStatusTimeout);
+      break;
+    }
+    const int item = info[stage * 2], kc = info[stage * 2 + 1];
+    if (item < 0) break;
+    if (item != cur) {
+      cur = item;
+      it = decode_item(PHASE, item, dm, s, D);
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[m][nt][q] = 0.f;
+    }
+    const int k0 = kc * kKChunk;
+    const uint32_t sw = sbase + stage * kStageBytes;
+    const uint32_t sa = sw + kStageW;
+    const uint8_t* sws = stages + stage * kStageBytes + kStageW + kStageA;
+    const float* sas = (const float*)(sws + kStageWS);
+    const int NT = it.U > 8 ? 2 : 1;
+    if (k0 + 32 * cw < it.K) {
+      // B fragments: user (nt*8 + g), elements [32cw + 8t, +8) of this stage
+      uint32_t b[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+        if (nt < NT)
+          lds128(sa + (nt * 8 + g) * kActStride + cw * 64 + t * 16, b[nt][0], b[nt][1],
+                 b[nt][2], b[nt][3]);
+      if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
+        float as[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) as[nt][q] = sas[(nt * 8 + 2 * t + q) * 8 + cw];
+        const int bx = cw >> 2, ch = cw & 3;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          int ra, rb, sra, srb;
+          uint32_t boxa, boxb;
+          if (it.kind == kRoutedGU) {
+            ra = 8 * m + g; rb = ra;                       // gate row, up row (same j)
+            boxa = sw + bx * 2048; boxb = sw + 4096 + bx * 2048;
+            sra = ra; srb = 32 + rb;
+          } else {
+            ra = 16 * m + g; rb = ra + 8;
+            boxa = sw + bx * 4096; boxb = boxa;
+            sra = ra; srb = rb;
+          }
+          const uint32_t wa = lds32(swz64(boxa, ra, ch) + 4 * t);
+          const uint32_t wb = lds32(swz64(boxb, rb, ch) + 4 * t);
+          uint32_t ha[4], hb[4];
+          cvt_e2m1x4(wa, ha);
+          cvt_e2m1x4(wb, hb);
+          const float sa_ = e8m0_to_float(sws[sra * 8 + cw]);
+          const float sb_ = e8m0_to_float(sws[srb * 8 + cw]);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            if (nt < NT) {
+              float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_f16(tmp, ha[0], hb[0], ha[1], hb[1], b[nt][0], b[nt][1]);
+              mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b[nt][2], b[nt][3]);
+              acc[m][nt][0] += tmp[0] * (sa_ * as[nt][0]);
+              acc[m][nt][1] += tmp[1] * (sa_ * as[nt][1]);
+              acc[m][nt][2] += tmp[2] * (sb_ * as[nt][0]);
+              acc[m][nt][3] += tmp[3] * (sb_ * as[nt][1]);
+            }
+          }
+        }
+      } else {
+        // shared expert: bf16 weights, one 16-row tile, K-slot cw = box cw
+        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+        const uint32_t box = sw + cw * 1024;
+        if (it.kind == kSharedGU) {
+          lds128(swz64(box, g, t), a0, a1, a2, a3);          // gate row g
+          lds128(swz64(box + 512, g, t), c0, c1, c2, c3);    // up row g
+        } else {
+          lds128(swz64(box, g, t), a0, a1, a2, a3);          // row g
+          lds128(swz64(box, g + 8, t), c0, c1, c2, c3);      // row g + 8
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          if (nt < NT) {
+            mma_bf16(acc[0][nt], a0, c0, a1, c1, b[nt][0], b[nt][1]);
+            mma_bf16(acc[0][nt], a2, c2, a3, c3, b[nt][2], b[nt][3]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == kStages) { stage = 0; phase ^= 1; }
+
+    if (kc == it.nst - 1) {
+      // ------------------------------------------------------ item epilogue ----
+      const int ntiles = (it.kind == kRoutedGU || it.kind == kRoutedDN) ? 4 : 1;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          if (m < ntiles && nt < NT)
+            red[((cw * 4 + m) * 2 + nt) * 32 + lane] =
+                make_float4(acc[m][nt][0], acc[m][nt][1], acc[m][nt][2], acc[m][nt][3]);
+      named_bar_sync(1, kConsumerWarps * 32);
+      if (cw == 0) {
+        float c[4][2][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            if (m >= ntiles || nt >= NT) {
+              c[m][nt][0] = c[m][nt][1] = c[m][nt][2] = c[m][nt][3] = 0.f;
+              continue;
+            }
+            float4 sum = red[((0 * 4 + m) * 2 + nt) * 32 + lane];
+            for (int w2 = 1; w2 < kConsumerWarps; ++w2) {
+              const float4 v = red[((w2 * 4 + m) * 2 + nt) * 32 + lane];
+              sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            }
+            c[m][nt][0] = sum.x; c[m][nt][1] = sum.y; c[m][nt][2] = sum.z; c[m][nt][3] = sum.w;
+          }
+        if (it.kind == kSharedGU) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int r = nt * 8 + 2 * t + q;
+              if (nt < NT && r < it.U)
+                s.ms[(size_t)r * dm.Is + it.out0 + g] =
+                    __float2bfloat16_rn(silu_f(c[0][nt][q]) * c[0][nt][2 + q]);
+            }
+        } else if (it.kind == kSharedDN) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int r = nt * 8 + 2 * t + q;
+              if (nt < NT && r < it.U) {
+                s.ys[(size_t)r * dm.H + it.out0 + g] = c[0][nt][q];
+                s.ys[(size_t)r * dm.H + it.out0 + g + 8] = c[0][nt][2 + q];
+              }
+            }
+        } else if (it.kind == kRoutedDN) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int u = nt * 8 + 2 * t + q;
+              if (nt < NT && u < it.U) {
+                const int pick = s.user_list[it.u0 + u];
+                float* yrow = s.y + (size_t)pick * dm.H + it.out0;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                  yrow[16 * m + g] = c[m][nt][q];
+                  yrow[16 * m + g + 8] = c[m][nt][2 + q];
+                }
+              }
+            }
+        } else {
+          // routed gate/up: mid = bf16(SiLU(gate) * up), then the f16 copy with one
+          // power-of-two scale per (pick, 32 columns)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              if (nt >= NT) continue;
+              const int u = nt * 8 + 2 * t + q;
+              float mv[4];
+              float amax = 0.f;
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                mv[m] = __bfloat162float(
+                    __float2bfloat16_rn(silu_f(c[m][nt][q]) * c[m][nt][2 + q]));
+                amax = fmaxf(amax, fabsf(mv[m]));
+              }
+              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+              int p = 0;
+              if (amax > 0.f) {
+                const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+                p = max(-100, min(100, ex - 14));
+              }
+              const float down = __uint_as_float((uint32_t)(127 - p) << 23);
+              if (u < it.U) {
+                const int pick = s.user_list[it.u0 + u];
+                __half* mrow = s.mid16 + (size_t)pick * dm.I + it.out0;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) mrow[8 * m + g] = __float2half_rn(mv[m] * down);
+                if (g == 0)
+                  s.mid16s[(size_t)pick * (dm.I / 32) + it.out0 / 32] =
+                      __uint_as_float((uint32_t)(127 + p) << 23);
+              }
+            }
+        }
+      }
+      named_bar_sync(1, kConsumerWarps * 32);
+    }
+  }
+}
+
+// Opt the streaming kernels in to their shared-memory size (once per process and device
+// before the first launch; called at create time, outside any graph capture).
+cudaError_t prepare_stream_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(k_stream<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kStreamSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_stream<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStreamSmem);
+  return e;
+}
+
+cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
+                          const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st) {
+  if (phase == 0)
+    k_stream<0><<<num_sms, kStreamThreads, kStreamSmem, st>>>(maps, d, w, s, budget_ns);
+  else
+    k_stream<1><<<num_sms, kStreamThreads, kStreamSmem, st>>>(maps, d, w, s, budget_ns);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------- tensor-map encoding ----
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static int encode_2d(EncodeTiledFn fn, CUtensorMap* m, CUtensorMapDataType dt, const void* base,
+                     uint64_t inner, uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
+                     uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+// Returns 0 on success, -1 if the driver has no tensor-map encoder, -2 if encoding failed.
+int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess || fn == nullptr)
+    return -1;
+  EncodeTiledFn enc = (EncodeTiledFn)fn;
+  const uint64_t H = d.H, E = d.E, I = d.I, Is = d.Is;
+  if (encode_2d(enc, &out->w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.w13c, H / 2, E * 2 * I, H / 2, 64, 32))
+    return -2;
+  if (encode_2d(enc, &out->w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.w2c, I / 2, E * H, I / 2, 64, 64))
+    return -2;
+  if (encode_2d(enc, &out->ws13, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w.ws13, H, 2 * Is, H * 2, 32, 8))
+    return -2;
+  if (encode_2d(enc, &out->ws2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w.ws2, Is, H, Is * 2, 32, 16))
+    return -2;
+  return 0;
+}
+
+size_t stream_maps_size() { return sizeof(StreamMaps); }
+
+}  // namespace mtail

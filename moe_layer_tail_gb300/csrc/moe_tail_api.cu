@@ -1,0 +1,287 @@
+// moe_tail_api.cu -- the C ABI of libmoe_tail.so: configuration checks, scratch
+// ownership, and the stream-ordered sequence of kernel launches of one call.
+//
+// The refusal of unsupported configurations at creation follows the Refusals section of
+// the "[AMD] integrate kimi k3 monokernel" page (the layer stops at startup, never at run
+// time); the borrowed weights follow its remark that the kernels read the weights in
+// place and copy none; scratch is owned per handle and reused by every call.
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/moe_tail.h"
+#include "moe_tail_internal.cuh"
+
+using namespace mtail;
+
+struct moe_tail {
+  moe_tail_config_t cfg;
+  Weights w;
+  StreamMaps maps;     // TMA descriptors of the streamed weights
+  Scratch s;
+  void* slab;          // one device allocation holding every scratch buffer
+  size_t slab_bytes;
+  void* stage;         // device staging for moe_tail_run_host: x, residual, out
+  int device;
+  int num_sms;
+  int last_rows;
+  cudaEvent_t ev[2 * 16];  // optional stage events (moe_tail_set_stage_events)
+  int n_ev;
+};
+
+static thread_local char g_cuda_err[256];
+
+static int cuda_fail(cudaError_t e) {
+  snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return MOE_TAIL_ERR_CUDA;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+extern "C" const char* moe_tail_strerror(int code) {
+  switch (code) {
+    case MOE_TAIL_OK: return "ok";
+    case MOE_TAIL_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, rows out of range)";
+    case MOE_TAIL_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_TAIL_ERR_CUDA: return "CUDA error";
+    case MOE_TAIL_ERR_TIMEOUT: return "device-side wait exceeded its budget";
+    case MOE_TAIL_ERR_NOT_CORESIDENT: return "persistent grid cannot be co-resident";
+    case MOE_TAIL_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown error";
+  }
+}
+
+extern "C" const char* moe_tail_last_cuda_error(void) { return g_cuda_err; }
+
+static int check_config(const moe_tail_config_t* c) {
+  if (c->max_rows < 1 || c->max_rows > kMaxRows) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->hidden < 128 || c->hidden % 128) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->hidden > (1 << 16)) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->n_experts < 1 || c->n_experts > kMaxExperts) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->top_k < 1 || c->top_k > kMaxTopK || c->top_k > c->n_experts)
+    return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->expert_inter < 128 || c->expert_inter % 128 || c->expert_inter > (1 << 16))
+    return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->shared_inter < 64 || c->shared_inter % 64 || c->shared_inter > (1 << 16))
+    return MOE_TAIL_ERR_UNSUPPORTED;
+  if (!(c->rms_eps > 0.f)) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->norm_topk_prob != 1) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->mode != MOE_TAIL_MODE_MULTI_KERNEL) return MOE_TAIL_ERR_UNSUPPORTED;
+  return MOE_TAIL_OK;
+}
+
+// Carve the scratch buffers out of one slab (256-byte aligned pieces).
+static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
+  const size_t R = c->max_rows, H = c->hidden, E = c->n_experts, k = c->top_k,
+               I = c->expert_inter, Is = c->shared_inter, P = R * k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    char* p = base ? base + off : nullptr;
+    off += (bytes + 255) & ~(size_t)255;
+    return p;
+  };
+  s->n = (__nv_bfloat16*)take(R * H * 2);
+  s->n16 = (__half*)take(R * H * 2);
+  s->n16s = (float*)take(R * (H / 32) * 4);
+  s->logits = (float*)take(R * E * 4);
+  s->ids = (int32_t*)take(P * 4);
+  s->wts = (float*)take(P * 4);
+  s->n_distinct = (int32_t*)take(4);
+  s->uniq = (int32_t*)take(P * 4);
+  s->user_off = (int32_t*)take((P + 1) * 4);
+  s->user_list = (int32_t*)take(P * 4);
+  s->mid = (__nv_bfloat16*)take(P * I * 2);
+  s->mid16 = (__half*)take(P * I * 2);
+  s->mid16s = (float*)take(P * (I / 32) * 4);
+  s->ms = (__nv_bfloat16*)take(R * Is * 2);
+  s->y = (float*)take(P * H * 4);
+  s->ys = (float*)take(R * H * 4);
+  s->status = (int32_t*)take(4);
+  s->counters = (uint32_t*)take(64 * 4);
+  return off;
+}
+
+extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weights_t* w,
+                               moe_tail_t** out) {
+  if (!out) return MOE_TAIL_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !w) return MOE_TAIL_ERR_INVALID_ARG;
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  const void* ptrs[8] = {w->gamma, w->router_w, w->w13_codes, w->w13_scales,
+                         w->w2_codes, w->w2_scales, w->shared_w13, w->shared_w2};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MOE_TAIL_ERR_INVALID_ARG;
+
+  moe_tail_t* h = new (std::nothrow) moe_tail_t;
+  if (!h) return MOE_TAIL_ERR_CUDA;
+  memset(h, 0, sizeof(*h));
+  h->cfg = *cfg;
+  h->w.gamma = (const __nv_bfloat16*)w->gamma;
+  h->w.w_r = (const __nv_bfloat16*)w->router_w;
+  h->w.w13c = (const uint8_t*)w->w13_codes;
+  h->w.w13s = (const uint8_t*)w->w13_scales;
+  h->w.w2c = (const uint8_t*)w->w2_codes;
+  h->w.w2s = (const uint8_t*)w->w2_scales;
+  h->w.ws13 = (const __nv_bfloat16*)w->shared_w13;
+  h->w.ws2 = (const __nv_bfloat16*)w->shared_w2;
+
+  {
+    Dims d0;
+    d0.R = cfg->max_rows; d0.H = cfg->hidden; d0.E = cfg->n_experts; d0.k = cfg->top_k;
+    d0.I = cfg->expert_inter; d0.Is = cfg->shared_inter; d0.eps = cfg->rms_eps;
+    const int mrc = make_stream_maps(&h->maps, d0, h->w);
+    if (mrc == -1) { delete h; snprintf(g_cuda_err, sizeof(g_cuda_err), "no cuTensorMapEncodeTiled"); return MOE_TAIL_ERR_CUDA; }
+    if (mrc != 0) { delete h; return MOE_TAIL_ERR_UNSUPPORTED; }
+  }
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = prepare_stream_kernels();
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) { delete h; return cuda_fail(e); }
+  h->slab_bytes = carve(cfg, nullptr, &h->s);
+  e = cudaMalloc(&h->slab, h->slab_bytes);
+  if (e != cudaSuccess) { delete h; return cuda_fail(e); }
+  carve(cfg, (char*)h->slab, &h->s);
+  const size_t act = (size_t)cfg->max_rows * cfg->hidden * 2;
+  e = cudaMalloc(&h->stage, 3 * act);
+  if (e == cudaSuccess) e = cudaMemset(h->slab, 0, h->slab_bytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(h->slab);
+    if (h->stage) cudaFree(h->stage);
+    delete h;
+    return cuda_fail(e);
+  }
+  *out = h;
+  return MOE_TAIL_OK;
+}
+
+extern "C" int moe_tail_set_stage_events(moe_tail_t* h, void* const* events, int32_t n_events) {
+  if (!h || n_events < 0) return MOE_TAIL_ERR_INVALID_ARG;
+  if (!events || n_events == 0) { h->n_ev = 0; return MOE_TAIL_OK; }
+  if (n_events > 2 * 16) n_events = 2 * 16;
+  for (int i = 0; i < n_events; ++i) {
+    if (!events[i]) return MOE_TAIL_ERR_INVALID_ARG;
+    h->ev[i] = (cudaEvent_t)events[i];
+  }
+  h->n_ev = n_events;
+  return MOE_TAIL_OK;
+}
+
+extern "C" int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows) {
+  (void)rows;
+  if (!h) return 0;
+  return (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) ? 8 : 6;
+}
+
+extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* out,
+                            int32_t rows, void* stream) {
+  if (!h || !x || !residual || !out) return MOE_TAIL_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(out)) return MOE_TAIL_ERR_INVALID_ARG;
+  if (rows < 1 || rows > h->cfg.max_rows) return MOE_TAIL_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  Dims d;
+  d.R = rows;
+  d.H = h->cfg.hidden;
+  d.E = h->cfg.n_experts;
+  d.k = h->cfg.top_k;
+  d.I = h->cfg.expert_inter;
+  d.Is = h->cfg.shared_inter;
+  d.eps = h->cfg.rms_eps;
+  cudaError_t e;
+  int stage_i = 0;
+  auto mark = [&](int which) -> cudaError_t {
+    const int idx = 2 * stage_i + which;
+    if (idx < h->n_ev) return cudaEventRecord(h->ev[idx], st);
+    return cudaSuccess;
+  };
+#define MT_STAGE(call)                                  \
+  do {                                                  \
+    if ((e = mark(0))) return cuda_fail(e);             \
+    if ((e = (call))) return cuda_fail(e);              \
+    if ((e = mark(1))) return cuda_fail(e);             \
+    ++stage_i;                                          \
+  } while (0)
+  MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (__nv_bfloat16*)residual, h->w, h->s, st));
+  MT_STAGE(launch_router(d, h->w, h->s, st));
+  MT_STAGE(launch_topk_dedup(d, h->s, st));
+  if (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) {
+    MT_STAGE(launch_experts_simple(d, h->w, h->s, h->num_sms, st));
+  } else {
+    const uint64_t budget_ns =
+        (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
+    MT_STAGE(launch_stream(0, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st));
+    MT_STAGE(launch_stream(1, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st));
+  }
+  MT_STAGE(launch_combine(d, h->s, (__nv_bfloat16*)out, st));
+#undef MT_STAGE
+  h->last_rows = rows;
+  return MOE_TAIL_OK;
+}
+
+extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host,
+                                 void* out_host, int32_t rows, void* stream) {
+  if (!h || !x_host || !residual_host || !out_host) return MOE_TAIL_ERR_INVALID_ARG;
+  if (rows < 1 || rows > h->cfg.max_rows) return MOE_TAIL_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t act = (size_t)h->cfg.max_rows * h->cfg.hidden * 2;
+  const size_t bytes = (size_t)rows * h->cfg.hidden * 2;
+  char* dx = (char*)h->stage;
+  char* dres = dx + act;
+  char* dout = dres + act;
+  cudaError_t e = cudaMemcpyAsync(dx, x_host, bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dres, residual_host, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int rc = moe_tail_run(h, dx, dres, dout, rows, stream);
+  if (rc) return rc;
+  e = cudaMemcpyAsync(residual_host, dres, bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, dout, bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
+}
+
+extern "C" int moe_tail_get_status(moe_tail_t* h, int32_t* device_status) {
+  if (!h) return MOE_TAIL_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  int32_t v = 0;
+  e = cudaMemcpy(&v, h->s.status, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (device_status) *device_status = v;
+  if (v & kStatusTimeout) return MOE_TAIL_ERR_TIMEOUT;
+  return v ? MOE_TAIL_ERR_DEVICE : MOE_TAIL_OK;
+}
+
+extern "C" int moe_tail_clear_status(moe_tail_t* h) {
+  if (!h) return MOE_TAIL_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemset(h->s.status, 0, 4);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
+}
+
+extern "C" int moe_tail_debug_routing(moe_tail_t* h, int32_t* ids, float* wts,
+                                      int32_t* n_distinct, void* stream) {
+  if (!h) return MOE_TAIL_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t P = (size_t)(h->last_rows > 0 ? h->last_rows : 0) * h->cfg.top_k;
+  cudaError_t e = cudaSuccess;
+  if (ids && P) e = cudaMemcpyAsync(ids, h->s.ids, P * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && wts && P) e = cudaMemcpyAsync(wts, h->s.wts, P * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && n_distinct)
+    e = cudaMemcpyAsync(n_distinct, h->s.n_distinct, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
+}
+
+extern "C" void moe_tail_destroy(moe_tail_t* h) {
+  if (!h) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != h->device) cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->slab);
+  cudaFree(h->stage);
+  if (cur >= 0 && cur != h->device) cudaSetDevice(cur);
+  delete h;
+}

@@ -1,0 +1,122 @@
+// moe_tail_internal.cuh -- device helpers, scratch layout and launcher declarations shared
+// by the kernels of libmoe_tail.so.  Nothing here is part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mtail {
+
+// Hard limits (checked at create time).
+constexpr int kMaxRows = 16;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxPicks = kMaxRows * kMaxTopK;  // (row, slot) pairs of one call
+
+// Device status word bits (sticky; read by moe_tail_get_status).
+enum : int32_t {
+  kStatusBadRouting = 1 << 0,   // top-k found no finite candidate (NaN logits)
+  kStatusBadDistinct = 1 << 1,  // distinct-expert count out of range
+  kStatusTimeout = 1 << 2,      // a bounded wait expired
+  kStatusBadTile = 1 << 3,      // a work item outside its matrix was skipped
+};
+
+struct Dims {
+  int R;        // rows of this call
+  int H, E, k, I, Is;
+  float eps;
+};
+
+struct Weights {
+  const __nv_bfloat16* gamma;
+  const __nv_bfloat16* w_r;
+  const uint8_t* w13c;
+  const uint8_t* w13s;
+  const uint8_t* w2c;
+  const uint8_t* w2s;
+  const __nv_bfloat16* ws13;
+  const __nv_bfloat16* ws2;
+};
+
+// Every buffer a call needs, carved from one allocation made at create time.
+struct Scratch {
+  __nv_bfloat16* n;      // [Rmax, H] normalised activations (bf16)
+  __half* n16;           // [Rmax, H] n as f16, scaled by 2^-p per 32-element block
+  float* n16s;           // [Rmax, H/32] the 2^p of each block
+  float* logits;         // [Rmax, E]
+  int32_t* ids;          // [Rmax, k] picks in pick order
+  float* wts;            // [Rmax, k]
+  int32_t* n_distinct;   // [1]
+  int32_t* uniq;         // [Rmax*k] distinct expert ids, ascending
+  int32_t* user_off;     // [Rmax*k + 1] CSR offsets into user_list
+  int32_t* user_list;    // [Rmax*k] pick indices r*k + slot, in (r, slot) order
+  __nv_bfloat16* mid;    // [Rmax*k, I] SiLU(gate)*up of each pick (bf16)
+  __half* mid16;         // [Rmax*k, I] mid as f16, scaled by 2^-p per 32-element block
+  float* mid16s;         // [Rmax*k, I/32]
+  __nv_bfloat16* ms;     // [Rmax, Is] shared-expert intermediate (bf16)
+  float* y;              // [Rmax*k, H] routed expert outputs
+  float* ys;             // [Rmax, H] shared expert output
+  int32_t* status;       // [1] sticky device status word
+  uint32_t* counters;    // [64] work counters and tickets (zero between calls)
+};
+
+// ------------------------------------------------------------------ device helpers ----
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Four bytes of packed E2M1 pairs -> four f16x2 registers (element 2j in the low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& h0, uint32_t& h1,
+                                                uint32_t& h2, uint32_t& h3) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+}
+
+// E8M0 scale byte -> float 2^(s-127) (s = 0 gives the subnormal 2^-127; 255 is not used).
+__device__ __forceinline__ float e8m0_to_float(uint32_t s) {
+  return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ void set_status(int32_t* status, int32_t bit) {
+  atomicOr(reinterpret_cast<int*>(status), bit);
+}
+
+// TMA descriptors of the streamed weight matrices (built once at create time).
+struct StreamMaps {
+  CUtensorMap w13;   // u8  [E*2I, H/2], box {64 B, 32 rows}, 64-byte swizzle
+  CUtensorMap w2;    // u8  [E*H, I/2],  box {64 B, 64 rows}
+  CUtensorMap ws13;  // bf16 [2Is, H],   box {32, 8}
+  CUtensorMap ws2;   // bf16 [H, Is],    box {32, 16}
+};
+
+// ------------------------------------------------------------------ launchers ----
+// Each returns the cudaError_t of its launch.
+
+cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x, __nv_bfloat16* residual,
+                               const Weights& w, const Scratch& s, cudaStream_t st);
+cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cudaStream_t st);
+cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st);
+cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch& s,
+                                  int num_sms, cudaStream_t st);
+int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w);
+cudaError_t prepare_stream_kernels();
+cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
+                          const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st);
+cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
+                           cudaStream_t st);
+
+}  // namespace mtail

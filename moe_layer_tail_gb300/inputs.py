@@ -104,7 +104,10 @@ def _e8m0_scales(rng, shape, K):
 
 
 def _codes(rng, shape):
-    return rng.integers(0, 256, size=shape, dtype=np.uint8)
+    """Uniform random bytes: the raw 64-bit outputs of the seeded PCG64 stream, little-endian."""
+    n = int(np.prod(shape))
+    raw = rng.bit_generator.random_raw((n + 7) // 8)
+    return raw.astype("<u8", copy=False).view(np.uint8)[:n].reshape(shape)
 
 
 _WEIGHT_STREAMS = ("gamma", "w_r", "w13_codes", "w13_scales", "w2_codes", "w2_scales", "ws13",

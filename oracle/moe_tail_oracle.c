@@ -13,10 +13,10 @@
  *     down) -> combine; section "Refusals": norm_topk_prob is required, norm/router/shared
  *     expert are bf16, routed experts are MXFP4; section "Kernel checks": the outputs are
  *     `out` and `res_out` (the updated residual).
- *   - "glm53: Long-context indexer ..." (sgl-amd-mono #86, quoting #85), commit 9 "top-8 tie
- *     shortcut": only an exact tie of the maximum runs the expert-id reduction, ties go to
- *     the lowest id and the pick order is unchanged; commit 10: the router activations are
- *     stored as bf16 before the GEMV.
+ *   - "glm53: Long-context indexer ..." (sgl-amd-mono #86, quoting #85), Modifications table
+ *     row 9 (top-8 tie shortcut): only an exact tie of the maximum runs the expert-id
+ *     reduction, ties go to the lowest id and the pick order is unchanged; row 10: the
+ *     router activations are stored as bf16 before the GEMV.
  *   - OCP MXFP4: 32-element blocks of E2M1 codes that share one E8M0 scale 2^(s-127).
  *
  * Arithmetic: every sum and product is in double precision.  The only roundings are the
@@ -95,10 +95,18 @@ double oracle_mxfp4_elem(const uint8_t* codes, const uint8_t* scales, int64_t k)
   return oracle_e2m1(code) * oracle_e8m0(scales[k / 32]);
 }
 
-/* Decode a whole packed row of K elements into doubles. */
+/* Decode a whole packed row of K elements into doubles: block b's scale 2^(s_b - 127)
+ * times the E2M1 value of each of its 32 elements (same values as oracle_mxfp4_elem). */
 void oracle_mxfp4_dequant_row(const uint8_t* codes, const uint8_t* scales, int64_t K,
                               double* out) {
-  for (int64_t k = 0; k < K; ++k) out[k] = oracle_mxfp4_elem(codes, scales, k);
+  for (int64_t b = 0; b * 32 < K; ++b) {
+    const double sc = oracle_e8m0(scales[b]);
+    for (int64_t k = b * 32; k < b * 32 + 32 && k < K; ++k) {
+      uint8_t byte = codes[k / 2];
+      int code = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+      out[k] = oracle_e2m1(code) * sc;
+    }
+  }
 }
 
 double oracle_silu(double z) { return z / (1.0 + exp(-z)); }

@@ -1,0 +1,82 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every entry point
+that include/moe_tail.h declares, and answers argument errors before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_layer_tail_gb300 as mt
+from moe_layer_tail_gb300 import build as mt_build
+from moe_layer_tail_gb300 import inputs as gen
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mt_build.build()
+    return mt.load_library()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(moe_tail_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10, names
+    for n in names:
+        assert hasattr(lib, n), "missing export " + n
+
+
+def test_strerror_covers_codes(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = lib.moe_tail_strerror(code).decode()
+        assert s and s != "unknown error"
+    assert lib.moe_tail_strerror(-99).decode() == "unknown error"
+
+
+def test_null_arguments_rejected_without_device(lib):
+    h = ctypes.c_void_p()
+    assert lib.moe_tail_create(None, None, ctypes.byref(h)) == mt.ERR_INVALID_ARG
+    assert h.value is None
+    assert lib.moe_tail_run(None, None, None, None, 1, None) == mt.ERR_INVALID_ARG
+    assert lib.moe_tail_run_host(None, None, None, None, 1, None) == mt.ERR_INVALID_ARG
+    assert lib.moe_tail_get_status(None, None) == mt.ERR_INVALID_ARG
+    lib.moe_tail_destroy(None)
+    assert lib.moe_tail_launches_per_run(None, 1) == 0
+
+
+@pytest.mark.parametrize("field,value", [("max_rows", 0), ("max_rows", 17), ("hidden", 200),
+                                         ("top_k", 9), ("expert_inter", 96),
+                                         ("shared_inter", 100), ("norm_topk_prob", 0),
+                                         ("n_experts", 2000), ("rms_eps", 0.0)])
+def test_unsupported_configs_refused_before_device(lib, field, value):
+    cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128))
+    setattr(cfg, field, value)
+    w = mt.WeightPtrs(*([16] * 8))  # never dereferenced: refusal comes first
+    h = ctypes.c_void_p()
+    assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
+        mt.ERR_UNSUPPORTED
+    assert h.value is None
+
+
+def test_misaligned_weight_pointer_refused(lib):
+    cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128))
+    w = mt.WeightPtrs(*([16] * 7 + [24]))
+    h = ctypes.c_void_p()
+    assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
+        mt.ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(mt, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        mt.load_library(str(tmp_path / "nope.so"))
