@@ -63,7 +63,10 @@ enum {
 enum {
   /* Run the expert stages with the warp-per-row CUDA-core kernels instead of the
    * TMA-streaming kernels (same results within the parity rule; for cross-checking). */
-  MOE_TAIL_DEBUG_SIMPLE_KERNELS = 1
+  MOE_TAIL_DEBUG_SIMPLE_KERNELS = 1,
+  /* Launch every kernel as a plain stream-ordered launch (no programmatic dependent
+   * launch overlap between consecutive kernels). */
+  MOE_TAIL_DEBUG_NO_PDL = 2
 };
 
 typedef struct moe_tail moe_tail_t; /* opaque handle */

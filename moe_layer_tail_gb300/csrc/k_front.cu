@@ -5,42 +5,87 @@
 // post-attention norm", "The router" and "The top-k"; "glm53: Long-context indexer ..."
 // page, Modifications table rows 9 (ties run the id reduction only when the maximum is
 // shared), 10 (bf16 activations before the router), 16 and 20 (each distinct expert once,
-// users in row order).
+// users in row order), and its reviewer note that every CTA routes all rows, so no
+// cross-CTA hand-off of the routing is needed.
+//
+// Two forms: k_front_fused (one launch: every CTA recomputes the row norms it needs, runs
+// its slice of the router, and the last CTA to finish runs top-k and the dedup), and the
+// three single-purpose kernels k_add_rmsnorm / k_router / k_topk_dedup used by the
+// cross-checking path.  bf16(x + residual) goes to scratch; the residual itself is
+// rewritten by the combine, after every reader is done.
 #include "moe_tail_internal.cuh"
 
 namespace mtail {
 
+// 2 bf16 in a word -> 2 bf16(a + b) in a word (fp32 add, round to nearest even).
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+  __nv_bfloat16 lo = __float2bfloat16_rn(bf16_lo(a) + bf16_lo(b));
+  __nv_bfloat16 hi = __float2bfloat16_rn(bf16_hi(a) + bf16_hi(b));
+  return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+}
+// 2 bf16 r, 2 bf16 gamma -> 2 bf16(r * rstd * gamma)
+__device__ __forceinline__ uint32_t norm_bf16x2(uint32_t r, uint32_t g, float rstd) {
+  __nv_bfloat16 lo = __float2bfloat16_rn(bf16_lo(r) * rstd * bf16_lo(g));
+  __nv_bfloat16 hi = __float2bfloat16_rn(bf16_hi(r) * rstd * bf16_hi(g));
+  return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+}
+
+// Power-of-two exponent p such that amax * 2^-p lies in [2^14, 2^15) (0 for amax == 0).
+__device__ __forceinline__ int f16_block_exp(float amax) {
+  if (!(amax > 0.f)) return 0;
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+  return max(-100, min(100, e - 14));
+}
+
+// 8 bf16 n values (one 16-byte group) -> f16 scaled by `down` (a power of two).
+__device__ __forceinline__ uint4 f16_group(uint4 nv, float down) {
+  const uint32_t w[4] = {nv.x, nv.y, nv.z, nv.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __half2 h2 = __floats2half2_rn(bf16_lo(w[q]) * down, bf16_hi(w[q]) * down);
+    o[q] = *reinterpret_cast<uint32_t*>(&h2);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float group_amax(uint4 nv) {
+  const uint32_t w[4] = {nv.x, nv.y, nv.z, nv.w};
+  float m = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+  return m;
+}
+
 // ---------------------------------------------------------------- add + RMSNorm ----
-// One CTA per row.  Each thread owns whole 32-element blocks, so the per-block f16 scale
-// of the routed experts' activation copy is thread-local.  The residual is rewritten in
-// place by the thread that read it.
+// One CTA per row; each thread owns whole 32-element blocks.
 constexpr int kNormThreads = 256;
 
 __global__ void __launch_bounds__(kNormThreads)
-k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ residual,
-              const __nv_bfloat16* __restrict__ gamma, __nv_bfloat16* __restrict__ n_out,
-              __half* __restrict__ n16, float* __restrict__ n16s, uint32_t* __restrict__ counters,
-              int H, float eps) {
+k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ residual,
+              const __nv_bfloat16* __restrict__ gamma, __nv_bfloat16* __restrict__ rnew,
+              __nv_bfloat16* __restrict__ n_out, __half* __restrict__ n16,
+              float* __restrict__ n16s, uint32_t* __restrict__ counters, int H, float eps) {
   const int r = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (r == 0 && threadIdx.x < 8) counters[threadIdx.x] = 0u;  // work counters of this call
   const int nblk = H / 32;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * H);
-  uint4* rr = reinterpret_cast<uint4*>(residual + (size_t)r * H);
+  const uint4* rr = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
+  uint4* rn = reinterpret_cast<uint4*>(rnew + (size_t)r * H);
   float ss = 0.f;
   for (int b = threadIdx.x; b < nblk; b += kNormThreads) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint4 xv = xr[b * 4 + c], rv = rr[b * 4 + c];
-      uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, rw[4] = {rv.x, rv.y, rv.z, rv.w}, ow[4];
+      const uint4 xv = xr[b * 4 + c], rv = rr[b * 4 + c];
+      const uint4 o = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
+                                 add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w));
+      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        __nv_bfloat16 lo = __float2bfloat16_rn(bf16_lo(xw[q]) + bf16_lo(rw[q]));
-        __nv_bfloat16 hi = __float2bfloat16_rn(bf16_hi(xw[q]) + bf16_hi(rw[q]));
-        float flo = __bfloat162float(lo), fhi = __bfloat162float(hi);
-        ss += flo * flo + fhi * fhi;
-        ow[q] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-      }
-      rr[b * 4 + c] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      for (int q = 0; q < 4; ++q)
+        ss += bf16_lo(ow[q]) * bf16_lo(ow[q]) + bf16_hi(ow[q]) * bf16_hi(ow[q]);
+      rn[b * 4 + c] = o;
     }
   }
   // deterministic block reduction: butterfly in each warp, then warp partials in order
@@ -60,50 +105,29 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ r
   uint4* no = reinterpret_cast<uint4*>(n_out + (size_t)r * H);
   uint4* n16o = reinterpret_cast<uint4*>(n16 + (size_t)r * H);
   for (int b = threadIdx.x; b < nblk; b += kNormThreads) {
-    float v[32];
+    uint4 nv[4];
     float amax = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint4 rv = rr[b * 4 + c], gv = g4[b * 4 + c];
-      uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w}, ow[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        __nv_bfloat16 lo = __float2bfloat16_rn(bf16_lo(rw[q]) * rstd * bf16_lo(gw[q]));
-        __nv_bfloat16 hi = __float2bfloat16_rn(bf16_hi(rw[q]) * rstd * bf16_hi(gw[q]));
-        v[c * 8 + q * 2] = __bfloat162float(lo);
-        v[c * 8 + q * 2 + 1] = __bfloat162float(hi);
-        amax = fmaxf(amax, fmaxf(fabsf(v[c * 8 + q * 2]), fabsf(v[c * 8 + q * 2 + 1])));
-        ow[q] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-      }
-      no[b * 4 + c] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      const uint4 rv = rn[b * 4 + c], gv = g4[b * 4 + c];
+      nv[c] = make_uint4(norm_bf16x2(rv.x, gv.x, rstd), norm_bf16x2(rv.y, gv.y, rstd),
+                         norm_bf16x2(rv.z, gv.z, rstd), norm_bf16x2(rv.w, gv.w, rstd));
+      no[b * 4 + c] = nv[c];
+      amax = fmaxf(amax, group_amax(nv[c]));
     }
-    // f16 copy scaled by 2^-p so that the block maximum lies in [2^14, 2^15): exact for
-    // every bf16 value down to 2^-29 of the block maximum.
-    int p = 0;
-    if (amax > 0.f) {
-      int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-      p = max(-100, min(100, e - 14));
-    }
+    const int p = f16_block_exp(amax);
     const float down = __uint_as_float((uint32_t)(127 - p) << 23);
     n16s[(size_t)r * nblk + b] = __uint_as_float((uint32_t)(127 + p) << 23);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t hw[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        __half2 h2 = __floats2half2_rn(v[c * 8 + q * 2] * down, v[c * 8 + q * 2 + 1] * down);
-        hw[q] = *reinterpret_cast<uint32_t*>(&h2);
-      }
-      n16o[b * 4 + c] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    }
+    for (int c = 0; c < 4; ++c) n16o[b * 4 + c] = f16_group(nv[c], down);
   }
 }
 
-cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x, __nv_bfloat16* residual,
-                               const Weights& w, const Scratch& s, cudaStream_t st) {
-  k_add_rmsnorm<<<d.R, kNormThreads, 0, st>>>(x, residual, w.gamma, s.n, s.n16, s.n16s,
-                                              s.counters, d.H, d.eps);
-  return cudaGetLastError();
+cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
+                               const __nv_bfloat16* residual, const Weights& w,
+                               const Scratch& s, cudaStream_t st, bool pdl) {
+  return launch_k(k_add_rmsnorm, dim3(d.R), dim3(kNormThreads), 0, st, pdl, x, residual,
+                  w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps);
 }
 
 // ------------------------------------------------------------------- router GEMV ----
@@ -116,6 +140,8 @@ k_router(const __nv_bfloat16* __restrict__ n, const __nv_bfloat16* __restrict__ 
          float* __restrict__ logits, int R, int H, int E) {
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_trigger();
   if (e >= E) return;
   float acc[kMaxRows];
 #pragma unroll
@@ -148,100 +174,97 @@ k_router(const __nv_bfloat16* __restrict__ n, const __nv_bfloat16* __restrict__ 
   }
 }
 
-cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cudaStream_t st) {
+cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cudaStream_t st,
+                          bool pdl) {
   dim3 grid((d.E + kRouterWarps - 1) / kRouterWarps);
-  k_router<<<grid, kRouterWarps * 32, 0, st>>>(s.n, w.w_r, s.logits, d.R, d.H, d.E);
-  return cudaGetLastError();
+  return launch_k(k_router, grid, dim3(kRouterWarps * 32), 0, st, pdl,
+                  (const __nv_bfloat16*)s.n, w.w_r, s.logits, d.R, d.H, d.E);
 }
 
 // ----------------------------------------------------------------- top-k + dedup ----
-// One CTA.  Warp r ranks row r: each round every lane takes its best untaken candidate
-// (larger logit, then lower id) and a butterfly over (value, id) pairs finds the round's
-// pick; an exact tie of the value resolves to the lower id, so the pick order is the
-// order of (logit desc, id asc).  The weights are the softmax of the picked logits.
-// Then the distinct experts of the call are listed in ascending id, with their users in
-// ascending row order (an expert appears at most once in a row's picks).
-constexpr int kTopkThreads = 512;
+// Run by one whole CTA.  Warp w ranks rows w, w + nwarps, ...: each round every lane takes
+// its best untaken candidate (larger logit, then lower id) and a butterfly over
+// (value, id) pairs finds the round's pick; an exact tie of the value resolves to the
+// lower id, so the pick order is (logit desc, id asc).  The weights are the softmax of the
+// picked logits.  Then the distinct experts of the call are listed in ascending id, with
+// their users in ascending row order (an expert appears at most once in a row's picks).
 
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
   return v > bv || (v == bv && e < be);
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
-k_topk_dedup(const float* __restrict__ logits, int32_t* __restrict__ ids,
-             float* __restrict__ wts, int32_t* __restrict__ n_distinct,
-             int32_t* __restrict__ uniq, int32_t* __restrict__ user_off,
-             int32_t* __restrict__ user_list, int32_t* __restrict__ status, int R, int E,
-             int k) {
+__device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
+                                 int32_t* n_distinct, int32_t* uniq, int32_t* user_off,
+                                 int32_t* user_list, int32_t* status, int R, int E, int k) {
   __shared__ uint32_t taken[kMaxRows][kMaxExperts / 32];
   __shared__ float pickv[kMaxRows][kMaxTopK];
   __shared__ int32_t s_ids[kMaxPicks];
   __shared__ uint32_t rowmask[kMaxExperts];
-  __shared__ int32_t eoff[kMaxExperts];   // first user slot of expert e
-  __shared__ int32_t wsum_d[kTopkThreads / 32], wsum_u[kTopkThreads / 32];
+  __shared__ int32_t eoff[kMaxExperts];  // first user slot of expert e
+  __shared__ int32_t wsum_d[32], wsum_u[32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kMaxRows * (kMaxExperts / 32); i += kTopkThreads)
-    (&taken[0][0])[i] = 0u;
-  for (int e = tid; e < kMaxExperts; e += kTopkThreads) rowmask[e] = 0u;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  for (int i = tid; i < kMaxRows * (kMaxExperts / 32); i += nthreads) (&taken[0][0])[i] = 0u;
+  for (int e = tid; e < kMaxExperts; e += nthreads) rowmask[e] = 0u;
   __syncthreads();
 
-  if (warp < R) {
-    const float* l = logits + (size_t)warp * E;
+  for (int row = warp; row < R; row += nwarps) {
+    const float* l = logits + (size_t)row * E;
     for (int i = 0; i < k; ++i) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
       for (int e = lane; e < E; e += 32) {
-        if (taken[warp][e >> 5] & (1u << (e & 31))) continue;
-        float v = l[e];
+        if (taken[row][e >> 5] & (1u << (e & 31))) continue;
+        const float v = __ldcg(l + e);
         if (better(v, e, bv, be)) { bv = v; be = e; }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
         if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
       }
       if (be >= E) {  // only NaN candidates left: take the lowest untaken id, flag it
-        be = E - 1;  // unreachable fallback: some id is always untaken while i < k <= E
+        be = E - 1;
         for (int e = 0; e < E; ++e)
-          if (!(taken[warp][e >> 5] & (1u << (e & 31)))) { be = e; break; }
-        bv = -INFINITY;
+          if (!(taken[row][e >> 5] & (1u << (e & 31)))) { be = e; break; }
         if (lane == 0) set_status(status, kStatusBadRouting);
       }
       if (lane == 0) {
-        taken[warp][be >> 5] |= 1u << (be & 31);
-        pickv[warp][i] = l[be];
-        s_ids[warp * k + i] = be;
+        taken[row][be >> 5] |= 1u << (be & 31);
+        pickv[row][i] = __ldcg(l + be);
+        s_ids[row * k + i] = be;
       }
       __syncwarp();
     }
     if (lane == 0) {
-      float m = pickv[warp][0], z = 0.f;
-      for (int i = 0; i < k; ++i) z += expf(pickv[warp][i] - m);
+      const float m = pickv[row][0];
+      float z = 0.f;
+      for (int i = 0; i < k; ++i) z += expf(pickv[row][i] - m);
       for (int i = 0; i < k; ++i) {
-        wts[warp * k + i] = expf(pickv[warp][i] - m) / z;
-        ids[warp * k + i] = s_ids[warp * k + i];
+        wts[row * k + i] = expf(pickv[row][i] - m) / z;
+        ids[row * k + i] = s_ids[row * k + i];
       }
     }
   }
   __syncthreads();
-  // rows using each expert
-  for (int p = tid; p < R * k; p += kTopkThreads)
-    atomicOr(&rowmask[s_ids[p]], 1u << (p / k));
+  for (int p = tid; p < R * k; p += nthreads) atomicOr(&rowmask[s_ids[p]], 1u << (p / k));
   __syncthreads();
-  // exclusive scans over experts of (used ? 1 : 0) and popc(rowmask): block of 512
-  // threads, two experts per thread, scan of warp totals in warp order.
-  const int e0 = tid * 2;
+  // exclusive scans over experts of (used ? 1 : 0) and popc(rowmask): each thread owns
+  // `per` consecutive experts; warp scan, then warp totals in warp order
+  const int per = (kMaxExperts + nthreads - 1) / nthreads;
+  const int e0 = tid * per;
   int cd = 0, cu = 0;
-  for (int q = 0; q < 2; ++q) {
-    int e = e0 + q;
+  for (int q = 0; q < per; ++q) {
+    const int e = e0 + q;
     if (e < E && rowmask[e]) { cd += 1; cu += __popc(rowmask[e]); }
   }
   int id_ = cd, iu = cu;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int td = __shfl_up_sync(0xffffffffu, id_, o), tu = __shfl_up_sync(0xffffffffu, iu, o);
+    const int td = __shfl_up_sync(0xffffffffu, id_, o);
+    const int tu = __shfl_up_sync(0xffffffffu, iu, o);
     if (lane >= o) { id_ += td; iu += tu; }
   }
   if (lane == 31) { wsum_d[warp] = id_; wsum_u[warp] = iu; }
@@ -249,8 +272,8 @@ k_topk_dedup(const float* __restrict__ logits, int32_t* __restrict__ ids,
   int bd = 0, bu = 0;
   for (int w2 = 0; w2 < warp; ++w2) { bd += wsum_d[w2]; bu += wsum_u[w2]; }
   int xd = bd + id_ - cd, xu = bu + iu - cu;  // exclusive prefixes at e0
-  for (int q = 0; q < 2; ++q) {
-    int e = e0 + q;
+  for (int q = 0; q < per; ++q) {
+    const int e = e0 + q;
     if (e < E && rowmask[e]) {
       eoff[e] = xu;
       uniq[xd] = e;
@@ -259,25 +282,184 @@ k_topk_dedup(const float* __restrict__ logits, int32_t* __restrict__ ids,
       xu += __popc(rowmask[e]);
     }
   }
-  if (tid == kTopkThreads - 1) {
-    int D = bd + id_, U = bu + iu;
+  if (tid == nthreads - 1) {
+    const int D = bd + id_, U = bu + iu;
     if (D < 1 || D > R * k || U != R * k) set_status(status, kStatusBadDistinct);
     *n_distinct = D;
     user_off[D] = U;
   }
   __syncthreads();
   // place each pick at its expert's slot: users of an expert are in ascending row order
-  for (int p = tid; p < R * k; p += kTopkThreads) {
-    int e = s_ids[p], r = p / k;
-    int rank = __popc(rowmask[e] & ((1u << r) - 1u));
+  for (int p = tid; p < R * k; p += nthreads) {
+    const int e = s_ids[p], r = p / k;
+    const int rank = __popc(rowmask[e] & ((1u << r) - 1u));
     user_list[eoff[e] + rank] = p;
   }
 }
 
-cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st) {
-  k_topk_dedup<<<1, kTopkThreads, 0, st>>>(s.logits, s.ids, s.wts, s.n_distinct, s.uniq,
-                                           s.user_off, s.user_list, s.status, d.R, d.E, d.k);
-  return cudaGetLastError();
+constexpr int kTopkThreads = 512;
+
+__global__ void __launch_bounds__(kTopkThreads)
+k_topk_dedup(const float* __restrict__ logits, int32_t* __restrict__ ids,
+             float* __restrict__ wts, int32_t* __restrict__ n_distinct,
+             int32_t* __restrict__ uniq, int32_t* __restrict__ user_off,
+             int32_t* __restrict__ user_list, int32_t* __restrict__ status, int R, int E,
+             int k) {
+  pdl_wait();
+  pdl_trigger();
+  topk_dedup_block(logits, ids, wts, n_distinct, uniq, user_off, user_list, status, R, E, k);
+}
+
+cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, bool pdl) {
+  return launch_k(k_topk_dedup, dim3(1), dim3(kTopkThreads), 0, st, pdl,
+                  (const float*)s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
+                  s.user_list, s.status, d.R, d.E, d.k);
+}
+
+// ------------------------------------------------------------------- fused front ----
+// One launch of ceil(E / 8) CTAs x 8 warps.  Every CTA computes rstd of every row (same
+// code and order in every CTA, so all agree bitwise), then walks H in chunks: the CTA
+// builds n = bf16(bf16(x + res) * rstd * gamma) for the chunk in shared memory and its
+// 8 warps (one expert each) accumulate their router dot products.  Chunk c's values are
+// also stored to scratch (r_new, n, and n's f16 copy) by CTA c % grid only.  The last CTA
+// to finish (atomic ticket after a fence) runs top-k and the dedup, and clears the
+// counters of the expert launches.
+constexpr int kFrontWarps = 8;
+constexpr int kFrontThreads = kFrontWarps * 32;
+constexpr int kFrontChunk = 1024;
+
+__global__ void __launch_bounds__(kFrontThreads)
+k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ residual,
+              const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ w_r,
+              Scratch s, int R, int H, int E, int k, float eps) {
+  __shared__ float s_rstd[kMaxRows];
+  __shared__ uint4 s_n[kMaxRows][kFrontChunk / 8];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x;
+  pdl_wait();
+  pdl_trigger();
+
+  // 1. rstd of every row: warp w sums rows w, w + 8 in a fixed order
+  for (int r = warp; r < R; r += kFrontWarps) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * H);
+    const uint4* rr = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
+    float ss = 0.f;
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 xv = __ldg(xr + c), rv = __ldg(rr + c);
+      const uint32_t o[4] = {add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
+                             add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w)};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        ss += bf16_lo(o[q]) * bf16_lo(o[q]) + bf16_hi(o[q]) * bf16_hi(o[q]);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) s_rstd[r] = 1.0f / sqrtf(ss / (float)H + eps);
+  }
+  __syncthreads();
+
+  // 2. router over H in chunks
+  const int e = blockIdx.x * kFrontWarps + warp;
+  float acc[kMaxRows];
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+  for (int h0 = 0, ci = 0; h0 < H; h0 += kFrontChunk, ++ci) {
+    const int cw = min(kFrontChunk, H - h0);  // multiple of 128
+    const int ng = cw / 8;                     // 16-byte groups per row in this chunk
+    const bool owner = (ci % G) == (int)blockIdx.x;
+    // the loop runs warp-uniformly (all 32 lanes take every trip) because of the shuffles;
+    // R * ng is a multiple of 16, so each aligned group of 4 lanes is valid or not as a whole
+    for (int base = warp * 32; base < R * ng; base += kFrontThreads) {
+      const int idx = base + lane;
+      const bool valid = idx < R * ng;
+      const int r = valid ? idx / ng : 0, gidx = valid ? idx % ng : 0;
+      const size_t off = ((size_t)r * H + h0) / 8 + gidx;
+      uint4 rn = make_uint4(0u, 0u, 0u, 0u), nv = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x) + off);
+        const uint4 rv = __ldg(reinterpret_cast<const uint4*>(residual) + off);
+        const uint4 gv = __ldg(g4 + h0 / 8 + gidx);
+        rn = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y), add_bf16x2(xv.z, rv.z),
+                        add_bf16x2(xv.w, rv.w));
+        const float rs = s_rstd[r];
+        nv = make_uint4(norm_bf16x2(rn.x, gv.x, rs), norm_bf16x2(rn.y, gv.y, rs),
+                        norm_bf16x2(rn.z, gv.z, rs), norm_bf16x2(rn.w, gv.w, rs));
+        s_n[r][gidx] = nv;
+      }
+      // groups idx..idx+3 (4 consecutive lanes) form one 32-element block
+      float amax = group_amax(nv);
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      if (valid && owner) {
+        reinterpret_cast<uint4*>(s.rnew)[off] = rn;
+        reinterpret_cast<uint4*>(s.n)[off] = nv;
+        const int p = f16_block_exp(amax);
+        reinterpret_cast<uint4*>(s.n16)[off] =
+            f16_group(nv, __uint_as_float((uint32_t)(127 - p) << 23));
+        if ((gidx & 3) == 0)
+          s.n16s[(size_t)r * (H / 32) + (h0 + gidx * 8) / 32] =
+              __uint_as_float((uint32_t)(127 + p) << 23);
+      }
+    }
+    __syncthreads();
+    if (e < E) {
+      const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)e * H + h0);
+      for (int c = lane; c < ng; c += 32) {
+        const uint4 wv = __ldg(wrow + c);
+        const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                             bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          if (r < R) {
+            const uint4 nv = s_n[r][c];
+            float a = acc[r];
+            a += wf[0] * bf16_lo(nv.x); a += wf[1] * bf16_hi(nv.x);
+            a += wf[2] * bf16_lo(nv.y); a += wf[3] * bf16_hi(nv.y);
+            a += wf[4] * bf16_lo(nv.z); a += wf[5] * bf16_hi(nv.z);
+            a += wf[6] * bf16_lo(nv.w); a += wf[7] * bf16_hi(nv.w);
+            acc[r] = a;
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (e < E) {
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      if (r < R) {
+        const float v = warp_sum(acc[r]);
+        if (lane == 0) s.logits[(size_t)r * E + e] = v;
+      }
+    }
+  }
+
+  // 3. the last CTA to finish ranks the experts and builds the work list
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t t = atomicAdd(&s.counters[kCtrFrontTicket], 1u);
+    s_last = (t == (uint32_t)(G - 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  topk_dedup_block(s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off, s.user_list,
+                   s.status, R, E, k);
+  if (tid == 0) {
+    s.counters[kCtrFrontTicket] = 0u;
+    s.counters[kCtrGateUp] = 0u;
+    s.counters[kCtrDown] = 0u;
+  }
+}
+
+cudaError_t launch_front_fused(const Dims& d, const __nv_bfloat16* x,
+                               const __nv_bfloat16* residual, const Weights& w,
+                               const Scratch& s, cudaStream_t st, bool pdl) {
+  dim3 grid((d.E + kFrontWarps - 1) / kFrontWarps);
+  return launch_k(k_front_fused, grid, dim3(kFrontThreads), 0, st, pdl, x, residual, w.gamma,
+                  w.w_r, s, d.R, d.H, d.E, d.k, d.eps);
 }
 
 }  // namespace mtail

@@ -228,8 +228,12 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
 }
 
 // ------------------------------------------------------------------------ combine ----
-// out[r, h] = bf16(sum over slots in pick order of wts * y + ys): a fixed-order fp32 sum.
-__global__ void k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out) {
+// out[r, h] = bf16(sum over slots in pick order of wts * y + ys): a fixed-order fp32 sum;
+// the residual receives bf16(x + residual), now that every reader of the old value is done.
+__global__ void k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
+                          __nv_bfloat16* __restrict__ residual) {
+  pdl_wait();
+  pdl_trigger();
   const int H = dm.H, k = dm.k;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= dm.R * H) return;
@@ -239,13 +243,14 @@ __global__ void k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out) {
     acc += s.wts[r * k + i] * s.y[(size_t)(r * k + i) * H + h];
   acc += s.ys[(size_t)r * H + h];
   out[idx] = __float2bfloat16_rn(acc);
+  residual[idx] = s.rnew[idx];
 }
 
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
-                           cudaStream_t st) {
+                           __nv_bfloat16* residual, cudaStream_t st, bool pdl) {
   const int n = d.R * d.H;
-  k_combine<<<(n + 255) / 256, 256, 0, st>>>(d, s, out);
-  return cudaGetLastError();
+  return launch_k(k_combine, dim3((n + 255) / 256), dim3(256), 0, st, pdl, d, s, out,
+                  residual);
 }
 
 }  // namespace mtail

@@ -241,6 +241,20 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   int* info = (int*)(empty + kStages);  // [kStages][2]: item, k-chunk
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Before the routing is known: pull this CTA's share of the shared expert's weights into
+  // L2 (they do not depend on any earlier kernel), so their HBM reads overlap the front.
+  if (warp == 0) {
+    const uint8_t* base = (PHASE == 0) ? (const uint8_t*)w.ws13 : (const uint8_t*)w.ws2;
+    const size_t total = (size_t)dm.Is * dm.H * 2 * (PHASE == 0 ? 2 : 1);
+    const size_t per = ((total / gridDim.x) + 4095) & ~(size_t)4095;
+    const size_t beg = (size_t)blockIdx.x * per;
+    const size_t end = min(total, beg + per);
+    for (size_t o = beg + (size_t)lane * 16384; o < end; o += 32 * 16384) {
+      const uint32_t n = (uint32_t)min((size_t)16384, end - o);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(n) : "memory");
+    }
+  }
+  pdl_wait();
   const int D = *s.n_distinct;
   const int n_items = (PHASE == 0) ? dm.Is / 8 + D * (dm.I / 32) : dm.H / 16 + D * (dm.H / 64);
 
@@ -264,7 +278,10 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
       int item = 0;
       if (lane == 0) item = (int)atomicAdd(&s.counters[PHASE], 1u);
       item = __shfl_sync(0xffffffffu, item, 0);
-      if (item >= n_items) break;
+      if (item >= n_items) {
+        pdl_trigger();  // this CTA is in its tail: let the next launch take the SM
+        break;
+      }
       const Item it = decode_item(PHASE, item, dm, s, D);
       for (int kc = 0; kc < it.nst && ok; ++kc) {
         if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, budget_ns);
@@ -593,12 +610,13 @@ cudaError_t prepare_stream_kernels() {
 }
 
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
-                          const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st) {
+                          const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
+                          bool pdl) {
   if (phase == 0)
-    k_stream<0><<<num_sms, kStreamThreads, kStreamSmem, st>>>(maps, d, w, s, budget_ns);
-  else
-    k_stream<1><<<num_sms, kStreamThreads, kStreamSmem, st>>>(maps, d, w, s, budget_ns);
-  return cudaGetLastError();
+    return launch_k(k_stream<0>, dim3(num_sms), dim3(kStreamThreads), kStreamSmem, st, pdl,
+                    maps, d, w, s, budget_ns);
+  return launch_k(k_stream<1>, dim3(num_sms), dim3(kStreamThreads), kStreamSmem, st, pdl, maps,
+                  d, w, s, budget_ns);
 }
 
 // ----------------------------------------------------------- tensor-map encoding ----

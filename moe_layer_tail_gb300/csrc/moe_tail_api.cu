@@ -81,6 +81,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
     off += (bytes + 255) & ~(size_t)255;
     return p;
   };
+  s->rnew = (__nv_bfloat16*)take(R * H * 2);
   s->n = (__nv_bfloat16*)take(R * H * 2);
   s->n16 = (__half*)take(R * H * 2);
   s->n16s = (float*)take(R * (H / 32) * 4);
@@ -172,7 +173,7 @@ extern "C" int moe_tail_set_stage_events(moe_tail_t* h, void* const* events, int
 extern "C" int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows) {
   (void)rows;
   if (!h) return 0;
-  return (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) ? 8 : 6;
+  return (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) ? 8 : 4;
 }
 
 extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* out,
@@ -203,18 +204,22 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
     if ((e = mark(1))) return cuda_fail(e);             \
     ++stage_i;                                          \
   } while (0)
-  MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (__nv_bfloat16*)residual, h->w, h->s, st));
-  MT_STAGE(launch_router(d, h->w, h->s, st));
-  MT_STAGE(launch_topk_dedup(d, h->s, st));
+  const bool pdl = !(h->cfg.debug_flags & MOE_TAIL_DEBUG_NO_PDL);
   if (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) {
+    MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
+                                h->w, h->s, st, pdl));
+    MT_STAGE(launch_router(d, h->w, h->s, st, pdl));
+    MT_STAGE(launch_topk_dedup(d, h->s, st, pdl));
     MT_STAGE(launch_experts_simple(d, h->w, h->s, h->num_sms, st));
   } else {
+    MT_STAGE(launch_front_fused(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
+                                h->w, h->s, st, pdl));
     const uint64_t budget_ns =
         (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
-    MT_STAGE(launch_stream(0, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st));
-    MT_STAGE(launch_stream(1, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st));
+    MT_STAGE(launch_stream(0, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl));
+    MT_STAGE(launch_stream(1, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl));
   }
-  MT_STAGE(launch_combine(d, h->s, (__nv_bfloat16*)out, st));
+  MT_STAGE(launch_combine(d, h->s, (__nv_bfloat16*)out, (__nv_bfloat16*)residual, st, pdl));
 #undef MT_STAGE
   h->last_rows = rows;
   return MOE_TAIL_OK;

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace mtail {
 
 // Hard limits (checked at create time).
@@ -43,6 +45,7 @@ struct Weights {
 
 // Every buffer a call needs, carved from one allocation made at create time.
 struct Scratch {
+  __nv_bfloat16* rnew;   // [Rmax, H] bf16(x + residual), copied to the residual at the end
   __nv_bfloat16* n;      // [Rmax, H] normalised activations (bf16)
   __half* n16;           // [Rmax, H] n as f16, scaled by 2^-p per 32-element block
   float* n16s;           // [Rmax, H/32] the 2^p of each block
@@ -62,6 +65,9 @@ struct Scratch {
   int32_t* status;       // [1] sticky device status word
   uint32_t* counters;    // [64] work counters and tickets (zero between calls)
 };
+
+// counters[] slots
+enum : int { kCtrGateUp = 0, kCtrDown = 1, kCtrFrontTicket = 2 };
 
 // ------------------------------------------------------------------ device helpers ----
 
@@ -95,6 +101,31 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t bit) {
   atomicOr(reinterpret_cast<int*>(status), bit);
 }
 
+// Programmatic dependent launch: wait until the previous kernel in the stream has completed
+// and its writes are visible (a no-op when the launch was not programmatic), and let the
+// next kernel's CTAs start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` on `st`, optionally as a programmatic dependent launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // TMA descriptors of the streamed weight matrices (built once at create time).
 struct StreamMaps {
   CUtensorMap w13;   // u8  [E*2I, H/2], box {64 B, 32 rows}, 64-byte swizzle
@@ -106,17 +137,28 @@ struct StreamMaps {
 // ------------------------------------------------------------------ launchers ----
 // Each returns the cudaError_t of its launch.
 
-cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x, __nv_bfloat16* residual,
-                               const Weights& w, const Scratch& s, cudaStream_t st);
-cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cudaStream_t st);
-cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st);
+cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
+                               const __nv_bfloat16* residual, const Weights& w,
+                               const Scratch& s, cudaStream_t st, bool pdl);
+cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cudaStream_t st,
+                          bool pdl);
+cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, bool pdl);
+cudaError_t launch_front_fused(const Dims& d, const __nv_bfloat16* x,
+                               const __nv_bfloat16* residual, const Weights& w, const Scratch& s,
+                               cudaStream_t st, bool pdl);
 cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch& s,
                                   int num_sms, cudaStream_t st);
 int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w);
 cudaError_t prepare_stream_kernels();
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
-                          const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st);
+                          const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
+                          bool pdl);
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
-                           cudaStream_t st);
+                           __nv_bfloat16* residual, cudaStream_t st, bool pdl);
+
+// Shared device pieces of the front (k_front.cu).
+__device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
+                                 int32_t* n_distinct, int32_t* uniq, int32_t* user_off,
+                                 int32_t* user_list, int32_t* status, int R, int E, int k);
 
 }  // namespace mtail

@@ -81,6 +81,7 @@ def _small(seed, R=3, H=384, E=12, k=3, I=256, Is=192, kind="plain"):
 
 
 SIMPLE = 1  # debug flag: warp-per-row CUDA-core expert kernels instead of the streaming ones
+NO_PDL = 2  # debug flag: plain stream-ordered launches (no programmatic dependent launch)
 
 
 def _check_small(shape, d, max_rows=None, rows=None, flags=0):
@@ -93,7 +94,7 @@ def _check_small(shape, d, max_rows=None, rows=None, flags=0):
     return tail, dev, orc, (out, res, ids, wts, nd)
 
 
-@pytest.mark.parametrize("flags", [0, SIMPLE])
+@pytest.mark.parametrize("flags", [0, SIMPLE, NO_PDL])
 @pytest.mark.parametrize("R,H,E,k,I,Is", [
     (1, 128, 1, 1, 128, 64),       # a single expert, smallest shapes
     (2, 384, 12, 3, 256, 192),     # several tiles, ragged tails
