@@ -104,23 +104,30 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
   uint4* no = reinterpret_cast<uint4*>(n_out + (size_t)r * H);
   uint4* n16o = reinterpret_cast<uint4*>(n16 + (size_t)r * H);
-  for (int b = threadIdx.x; b < nblk; b += kNormThreads) {
-    uint4 nv[4];
-    float amax = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 rv = rn[b * 4 + c], gv = g4[b * 4 + c];
-      nv[c] = make_uint4(norm_bf16x2(rv.x, gv.x, rstd), norm_bf16x2(rv.y, gv.y, rstd),
-                         norm_bf16x2(rv.z, gv.z, rstd), norm_bf16x2(rv.w, gv.w, rstd));
-      no[b * 4 + c] = nv[c];
-      amax = fmaxf(amax, group_amax(nv[c]));
-    }
-    const int p = f16_block_exp(amax);
-    const float down = __uint_as_float((uint32_t)(127 - p) << 23);
-    n16s[(size_t)r * nblk + b] = __uint_as_float((uint32_t)(127 + p) << 23);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) n16o[b * 4 + c] = f16_group(nv[c], down);
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < H / 8; c += kNormThreads) {
+    const uint4 rv = rn[c], gv = g4[c];
+    const uint4 nv = make_uint4(norm_bf16x2(rv.x, gv.x, rstd), norm_bf16x2(rv.y, gv.y, rstd),
+                                norm_bf16x2(rv.z, gv.z, rstd), norm_bf16x2(rv.w, gv.w, rstd));
+    no[c] = nv;
+    amax = fmaxf(amax, group_amax(nv));
   }
+  __shared__ float s_amax;
+  amax = warp_max(amax);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = 0.f;
+    for (int i = 0; i < kNormThreads / 32; ++i) m = fmaxf(m, part[i]);
+    s_amax = m;
+  }
+  __syncthreads();
+  // f16 copy with one power-of-two scale per row (row maximum in [2^14, 2^15))
+  const int p = f16_block_exp(s_amax);
+  const float down = __uint_as_float((uint32_t)(127 - p) << 23);
+  if (threadIdx.x == 0) n16s[r] = __uint_as_float((uint32_t)(127 + p) << 23);
+  for (int c = threadIdx.x; c < H / 8; c += kNormThreads) n16o[c] = f16_group(no[c], down);
 }
 
 cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
@@ -333,6 +340,8 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
               const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ w_r,
               Scratch s, int R, int H, int E, int k, float eps) {
   __shared__ float s_rstd[kMaxRows];
+  __shared__ float s_down[kMaxRows];
+  __shared__ float s_gmax[kFrontWarps];
   __shared__ uint4 s_n[kMaxRows][kFrontChunk / 8];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -340,21 +349,42 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   pdl_wait();
   pdl_trigger();
 
-  // 1. rstd of every row: warp w sums rows w, w + 8 in a fixed order
+  // 1. rstd of every row (warp w sums rows w, w + 8 in a fixed order), the row maxima of
+  //    |r_new| and the maximum of |gamma|: their product bounds |n| and fixes the row's
+  //    power-of-two scale for the f16 copy (row maximum below 2^15).
+  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+  {
+    float gm = 0.f;
+    for (int c = tid; c < H / 8; c += kFrontThreads) gm = fmaxf(gm, group_amax(__ldg(g4 + c)));
+    gm = warp_max(gm);
+    if (lane == 0) s_gmax[warp] = gm;
+  }
+  __syncthreads();
+  float gmax = 0.f;
+  for (int i = 0; i < kFrontWarps; ++i) gmax = fmaxf(gmax, s_gmax[i]);
   for (int r = warp; r < R; r += kFrontWarps) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * H);
     const uint4* rr = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
-    float ss = 0.f;
+    float ss = 0.f, rmax = 0.f;
     for (int c = lane; c < H / 8; c += 32) {
       const uint4 xv = __ldg(xr + c), rv = __ldg(rr + c);
-      const uint32_t o[4] = {add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
-                             add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w)};
+      const uint4 o4 = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
+                                  add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w));
+      const uint32_t o[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         ss += bf16_lo(o[q]) * bf16_lo(o[q]) + bf16_hi(o[q]) * bf16_hi(o[q]);
+      rmax = fmaxf(rmax, group_amax(o4));
     }
     ss = warp_sum(ss);
-    if (lane == 0) s_rstd[r] = 1.0f / sqrtf(ss / (float)H + eps);
+    rmax = warp_max(rmax);
+    const float rstd = 1.0f / sqrtf(ss / (float)H + eps);
+    const int p = f16_block_exp(rmax * rstd * gmax * 1.0078125f);
+    if (lane == 0) {
+      s_rstd[r] = rstd;
+      s_down[r] = __uint_as_float((uint32_t)(127 - p) << 23);
+      if (blockIdx.x == 0) s.n16s[r] = __uint_as_float((uint32_t)(127 + p) << 23);
+    }
   }
   __syncthreads();
 
@@ -363,43 +393,26 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   float acc[kMaxRows];
 #pragma unroll
   for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
-  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
   for (int h0 = 0, ci = 0; h0 < H; h0 += kFrontChunk, ++ci) {
     const int cw = min(kFrontChunk, H - h0);  // multiple of 128
     const int ng = cw / 8;                     // 16-byte groups per row in this chunk
     const bool owner = (ci % G) == (int)blockIdx.x;
-    // the loop runs warp-uniformly (all 32 lanes take every trip) because of the shuffles;
-    // R * ng is a multiple of 16, so each aligned group of 4 lanes is valid or not as a whole
-    for (int base = warp * 32; base < R * ng; base += kFrontThreads) {
-      const int idx = base + lane;
-      const bool valid = idx < R * ng;
-      const int r = valid ? idx / ng : 0, gidx = valid ? idx % ng : 0;
+    for (int idx = tid; idx < R * ng; idx += kFrontThreads) {
+      const int r = idx / ng, gidx = idx % ng;
       const size_t off = ((size_t)r * H + h0) / 8 + gidx;
-      uint4 rn = make_uint4(0u, 0u, 0u, 0u), nv = make_uint4(0u, 0u, 0u, 0u);
-      if (valid) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x) + off);
-        const uint4 rv = __ldg(reinterpret_cast<const uint4*>(residual) + off);
-        const uint4 gv = __ldg(g4 + h0 / 8 + gidx);
-        rn = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y), add_bf16x2(xv.z, rv.z),
-                        add_bf16x2(xv.w, rv.w));
-        const float rs = s_rstd[r];
-        nv = make_uint4(norm_bf16x2(rn.x, gv.x, rs), norm_bf16x2(rn.y, gv.y, rs),
-                        norm_bf16x2(rn.z, gv.z, rs), norm_bf16x2(rn.w, gv.w, rs));
-        s_n[r][gidx] = nv;
-      }
-      // groups idx..idx+3 (4 consecutive lanes) form one 32-element block
-      float amax = group_amax(nv);
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      if (valid && owner) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x) + off);
+      const uint4 rv = __ldg(reinterpret_cast<const uint4*>(residual) + off);
+      const uint4 gv = __ldg(g4 + h0 / 8 + gidx);
+      const uint4 rn = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
+                                  add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w));
+      const float rs = s_rstd[r];
+      const uint4 nv = make_uint4(norm_bf16x2(rn.x, gv.x, rs), norm_bf16x2(rn.y, gv.y, rs),
+                                  norm_bf16x2(rn.z, gv.z, rs), norm_bf16x2(rn.w, gv.w, rs));
+      s_n[r][gidx] = nv;
+      if (owner) {
         reinterpret_cast<uint4*>(s.rnew)[off] = rn;
         reinterpret_cast<uint4*>(s.n)[off] = nv;
-        const int p = f16_block_exp(amax);
-        reinterpret_cast<uint4*>(s.n16)[off] =
-            f16_group(nv, __uint_as_float((uint32_t)(127 - p) << 23));
-        if ((gidx & 3) == 0)
-          s.n16s[(size_t)r * (H / 32) + (h0 + gidx * 8) / 32] =
-              __uint_as_float((uint32_t)(127 + p) << 23);
+        reinterpret_cast<uint4*>(s.n16)[off] = f16_group(nv, s_down[r]);
       }
     }
     __syncthreads();

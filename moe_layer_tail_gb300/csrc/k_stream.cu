@@ -25,8 +25,9 @@
 //     cvt.rn.f16x2.e2m1x2 straight into mma.m16n8k16 A fragments (weights = M rows, users =
 //     N columns), applies the per-block weight x activation scale to each block's fp32
 //     product, and accumulates in fp32; the 8 warps' partial sums are added in warp order.
-//   * activations enter the routed contractions as f16 with a power-of-two scale per
-//     32-element block (exact for bf16 values in range); the shared expert runs bf16 x bf16.
+//   * activations enter the routed contractions as f16 with power-of-two scales (one per row
+//     for gate/up, applied in the epilogue; one per 32-element block for down, applied per
+//     block), exact for bf16 values in range; the shared expert runs bf16 x bf16.
 //   * every mbarrier wait is bounded by a %globaltimer budget; on expiry the kernel sets
 //     the status word and leaves.
 #include "moe_tail_internal.cuh"
@@ -350,14 +351,13 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
             }
             cp_async4(sws + row * 8 + wd * 4, base + grow * kb + (k0 / 32) + wd * 4);
           }
-          for (int c = lane; c < it.U * 2; c += 32) {
+          // per-block activation scales (down only: the gate/up activations carry one
+          // scale per row, applied in the epilogue)
+          for (int c = lane; it.kind == kRoutedDN && c < it.U * 2; c += 32) {
             const int u = c >> 1, half = c & 1;
             if (half >= words) continue;
-            const float* src;
-            if (it.kind == kRoutedGU)
-              src = s.n16s + (size_t)(s.user_list[it.u0 + u] / dm.k) * (dm.H / 32) + k0 / 32 + half * 4;
-            else
-              src = s.mid16s + (size_t)s.user_list[it.u0 + u] * (dm.I / 32) + k0 / 32 + half * 4;
+            const float* src =
+                s.mid16s + (size_t)s.user_list[it.u0 + u] * (dm.I / 32) + k0 / 32 + half * 4;
             cp_async16(sas + u * 32 + half * 16, src);
           }
         }
@@ -431,7 +431,8 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int q = 0; q < 2; ++q) as[nt][q] = sas[(nt * 8 + 2 * t + q) * 8 + cw];
+          for (int q = 0; q < 2; ++q)
+            as[nt][q] = (PHASE == 1) ? sas[(nt * 8 + 2 * t + q) * 8 + cw] : 1.0f;
         const int bx = cw >> 2, ch = cw & 3;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -459,10 +460,17 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
               float tmp[4] = {0.f, 0.f, 0.f, 0.f};
               mma_f16(tmp, ha[0], hb[0], ha[1], hb[1], b[nt][0], b[nt][1]);
               mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b[nt][2], b[nt][3]);
-              acc[m][nt][0] += tmp[0] * (sa_ * as[nt][0]);
-              acc[m][nt][1] += tmp[1] * (sa_ * as[nt][1]);
-              acc[m][nt][2] += tmp[2] * (sb_ * as[nt][0]);
-              acc[m][nt][3] += tmp[3] * (sb_ * as[nt][1]);
+              if (PHASE == 1) {
+                acc[m][nt][0] += tmp[0] * (sa_ * as[nt][0]);
+                acc[m][nt][1] += tmp[1] * (sa_ * as[nt][1]);
+                acc[m][nt][2] += tmp[2] * (sb_ * as[nt][0]);
+                acc[m][nt][3] += tmp[3] * (sb_ * as[nt][1]);
+              } else {
+                acc[m][nt][0] += tmp[0] * sa_;
+                acc[m][nt][1] += tmp[1] * sa_;
+                acc[m][nt][2] += tmp[2] * sb_;
+                acc[m][nt][3] += tmp[3] * sb_;
+              }
             }
           }
         }
@@ -564,12 +572,14 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
             for (int q = 0; q < 2; ++q) {
               if (nt >= NT) continue;
               const int u = nt * 8 + 2 * t + q;
+              // the row's activation scale (one power of two per row)
+              const float rs = (u < it.U) ? s.n16s[s.user_list[it.u0 + u] / dm.k] : 0.f;
               float mv[4];
               float amax = 0.f;
 #pragma unroll
               for (int m = 0; m < 4; ++m) {
-                mv[m] = __bfloat162float(
-                    __float2bfloat16_rn(silu_f(c[m][nt][q]) * c[m][nt][2 + q]));
+                mv[m] = __bfloat162float(__float2bfloat16_rn(silu_f(c[m][nt][q] * rs) *
+                                                             (c[m][nt][2 + q] * rs)));
                 amax = fmaxf(amax, fabsf(mv[m]));
               }
               amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));

@@ -84,7 +84,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
   s->rnew = (__nv_bfloat16*)take(R * H * 2);
   s->n = (__nv_bfloat16*)take(R * H * 2);
   s->n16 = (__half*)take(R * H * 2);
-  s->n16s = (float*)take(R * (H / 32) * 4);
+  s->n16s = (float*)take(R * 4);
   s->logits = (float*)take(R * E * 4);
   s->ids = (int32_t*)take(P * 4);
   s->wts = (float*)take(P * 4);

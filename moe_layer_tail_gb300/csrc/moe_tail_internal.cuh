@@ -47,8 +47,8 @@ struct Weights {
 struct Scratch {
   __nv_bfloat16* rnew;   // [Rmax, H] bf16(x + residual), copied to the residual at the end
   __nv_bfloat16* n;      // [Rmax, H] normalised activations (bf16)
-  __half* n16;           // [Rmax, H] n as f16, scaled by 2^-p per 32-element block
-  float* n16s;           // [Rmax, H/32] the 2^p of each block
+  __half* n16;           // [Rmax, H] n as f16, scaled by 2^-p per row
+  float* n16s;           // [Rmax] the 2^p of each row
   float* logits;         // [Rmax, E]
   int32_t* ids;          // [Rmax, k] picks in pick order
   float* wts;            // [Rmax, k]
@@ -92,6 +92,12 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t s) {
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 

@@ -65,54 +65,67 @@ def _row_margin(x_row, res_row, gamma, w_r, eps, k):
     return float(np.float32(l[a])) - float(np.float32(l[b])), a, b
 
 
+def _nudge_once(xrow, m0, res_row, gamma, w_r, eps, k, g, target, tol, iters):
+    """One bracket-and-bisect pass along gamma * (W_r[a] - W_r[b]) for the row's current
+    k-th (a) and (k+1)-th (b) experts; returns the best row found and its margin."""
+    from moe_layer_tail_gb300.inputs import to_bf16_bits
+    _, a, b = _row_margin(xrow, res_row, gamma, w_r, eps, k)
+    x0 = bf16_decode(xrow)
+    v = g * (bf16_decode(w_r[a]) - bf16_decode(w_r[b]))
+    v /= np.abs(v).max()
+
+    def trial(alpha):
+        xr = to_bf16_bits((x0 + alpha * v)[None])[0]
+        return _row_margin(xr, res_row, gamma, w_r, eps, k)[0], xr
+
+    best = (abs(m0 - target), xrow.copy(), m0)
+    lo, hi = None, 0.0  # alpha with margin < target (lo) / > target (hi)
+    if m0 < target:
+        lo, hi = 0.0, None
+    step = 1e-4  # the logit gap moves ~20x the step: start far below the target change
+    for _ in range(40):  # bracket
+        probe = step if m0 < target else -step
+        m, xr = trial(probe)
+        if abs(m - target) < best[0]:
+            best = (abs(m - target), xr, m)
+        if (m - target) * (m0 - target) <= 0:
+            if m0 < target:
+                hi = probe
+            else:
+                lo = probe
+            break
+        step *= 2
+    if lo is not None and hi is not None:
+        for _ in range(iters):
+            mid = 0.5 * (lo + hi)
+            m, xr = trial(mid)
+            if abs(m - target) < best[0]:
+                best = (abs(m - target), xr, m)
+            if best[0] <= tol:
+                break
+            if m < target:
+                lo = mid
+            else:
+                hi = mid
+    return best[1], best[2]
+
+
 def inject_near_ties(x, residual, gamma, w_r, eps, k, target=1e-2, tol=1e-4, iters=40):
     """Nudge each row of x (bf16 bits) so that the oracle's fp32 k-th/(k+1)-th logit margin
     is target +- tol.  The nudge is along gamma * (W_r[a] - W_r[b]) for the row's current
     k-th and (k+1)-th experts, sized by bisection (bf16 rounding makes the margin a fine
     staircase in the step size).  Returns the new x and the achieved margins."""
-    from moe_layer_tail_gb300.inputs import to_bf16_bits
     x = np.array(x, dtype=np.uint16, copy=True)
     got = []
     g = bf16_decode(gamma)
     for r in range(x.shape[0]):
-        x0 = bf16_decode(x[r])
-        m0, a, b = _row_margin(x[r], residual[r], gamma, w_r, eps, k)
-        v = g * (bf16_decode(w_r[a]) - bf16_decode(w_r[b]))
-        v /= np.abs(v).max()
-
-        def trial(alpha):
-            xr = to_bf16_bits((x0 + alpha * v)[None])[0]
-            return _row_margin(xr, residual[r], gamma, w_r, eps, k)[0], xr
-
-        best = (abs(m0 - target), x[r].copy(), m0)
-        lo, hi = None, 0.0  # alpha with margin < target (lo) / > target (hi)
-        if m0 < target:
-            lo, hi = 0.0, None
-        step = 0.01
-        for _ in range(30):  # bracket
-            probe = (step if m0 < target else -step)
-            m, xr = trial(probe)
-            if abs(m - target) < best[0]:
-                best = (abs(m - target), xr, m)
-            if (m - target) * (m0 - target) <= 0:
-                if m0 < target:
-                    hi = probe
-                else:
-                    lo = probe
+        cur = x[r].copy()
+        m_cur = _row_margin(cur, residual[r], gamma, w_r, eps, k)[0]
+        for _outer in range(6):  # re-aim at the current k-th/(k+1)-th pair until within tol
+            if abs(m_cur - target) <= tol:
                 break
-            step *= 2
-        if lo is not None and hi is not None:
-            for _ in range(iters):
-                mid = 0.5 * (lo + hi)
-                m, xr = trial(mid)
-                if abs(m - target) < best[0]:
-                    best = (abs(m - target), xr, m)
-                if best[0] <= tol:
-                    break
-                if m < target:
-                    lo = mid
-                else:
-                    hi = mid
-        x[r] = best[1]
-        got.append(best[2])
+            cur, m_cur = _nudge_once(cur, m_cur, residual[r], gamma, w_r, eps, k, g, target,
+                                     tol, iters)
+        x[r] = cur
+        got.append(m_cur)
     return x, np.array(got)

@@ -45,7 +45,7 @@ def workload_inputs(name):
         if wl.kind == "neartie":
             d["x"], margins = inject_near_ties(d["x"], d["residual"], d["gamma"], d["w_r"],
                                                wl.shape.eps, wl.shape.k)
-            assert np.all(np.abs(margins - 1e-2) <= 2e-4), margins
+            assert np.all(np.abs(margins - 1e-2) <= 1.01e-4), margins
         dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
         orc = oracle.moe_tail(d, wl.shape.k, wl.shape.eps, nthreads=NTHREADS)
         _CACHE[name] = (wl, d, dev, orc)
@@ -56,7 +56,7 @@ def workload_inputs(name):
 def test_workload_parity_full_size(name):
     wl, d, dev, orc = workload_inputs(name)
     tail = MoeTail(wl.shape, dev, max_rows=wl.shape.R)
-    assert tail.launches_per_run(wl.shape.R) == 6
+    assert tail.launches_per_run(wl.shape.R) == 4
     out, res, ids, wts, nd = run_gpu(tail, d)
     figs = check_parity(out, res, ids, orc, wl.shape.k)
     assert nd == len(np.unique(orc["ids"]))
