@@ -66,7 +66,12 @@ enum {
   MOE_TAIL_DEBUG_SIMPLE_KERNELS = 1,
   /* Launch every kernel as a plain stream-ordered launch (no programmatic dependent
    * launch overlap between consecutive kernels). */
-  MOE_TAIL_DEBUG_NO_PDL = 2
+  MOE_TAIL_DEBUG_NO_PDL = 2,
+  /* Failure injection for tests: in the gate/up launch, the first CTA's producer leaves its
+   * first pipeline stage unpublished, so that the consumers' bounded wait expires; the
+   * kernel records MOE_TAIL_ERR_TIMEOUT in the status word and returns.  The output of
+   * such a call is not meaningful. */
+  MOE_TAIL_DEBUG_STALL_FIRST_STAGE = 4
 };
 
 typedef struct moe_tail moe_tail_t; /* opaque handle */

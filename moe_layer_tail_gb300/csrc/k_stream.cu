@@ -232,7 +232,7 @@ __device__ __forceinline__ uint32_t swz64(uint32_t base, int r, int c) {
 template <int PHASE>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
-         uint64_t budget_ns) {
+         uint64_t budget_ns, uint32_t debug) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stages = smem;
@@ -275,6 +275,11 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    // stages whose copies were issued and not yet seen consumed, with their phase parity
+    uint32_t pend = 0u, pend_par = 0u;
+    // failure-injection switch: CTA 0 leaves its first stage unpublished, so the consumers'
+    // bounded wait on it expires (tests the timeout path; never set in production)
+    bool skip_first = (debug & kDebugStallFirstStage) && blockIdx.x == 0;
     for (;;) {
       int item = 0;
       if (lane == 0) item = (int)atomicAdd(&s.counters[PHASE], 1u);
@@ -288,6 +293,14 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
         if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, budget_ns);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
+        pend &= ~(1u << stage);
+        if (skip_first) {
+          skip_first = false;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          continue;
+        }
+        pend |= 1u << stage;
+        pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
         uint8_t* st = stages + stage * kStageBytes;
         uint8_t* sw = st;
         uint8_t* sa = st + kStageW;
@@ -379,7 +392,16 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
         cp_async_arrive_noinc(&full[stage]);
       }
     }
-    if (!ok && lane == 0) set_status(s.status, kStatusTimeout);
+    if (!ok) {
+      // a wait expired: record it, then let every copy this CTA issued land (bounded)
+      // before the CTA's shared memory is released
+      if (lane == 0) {
+        set_status(s.status, kStatusTimeout);
+        for (int st2 = 0; st2 < kStages; ++st2)
+          if (pend & (1u << st2)) mbar_wait(&full[st2], (pend_par >> st2) & 1u, budget_ns);
+      }
+      __syncwarp();
+    }
     asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }
@@ -621,12 +643,12 @@ cudaError_t prepare_stream_kernels() {
 
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
                           const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
-                          bool pdl) {
+                          bool pdl, uint32_t debug) {
   if (phase == 0)
     return launch_k(k_stream<0>, dim3(num_sms), dim3(kStreamThreads), kStreamSmem, st, pdl,
-                    maps, d, w, s, budget_ns);
+                    maps, d, w, s, budget_ns, debug);
   return launch_k(k_stream<1>, dim3(num_sms), dim3(kStreamThreads), kStreamSmem, st, pdl, maps,
-                  d, w, s, budget_ns);
+                  d, w, s, budget_ns, debug);
 }
 
 // ----------------------------------------------------------- tensor-map encoding ----

@@ -54,6 +54,9 @@ extern "C" const char* moe_tail_strerror(int code) {
 
 extern "C" const char* moe_tail_last_cuda_error(void) { return g_cuda_err; }
 
+static_assert(MOE_TAIL_DEBUG_STALL_FIRST_STAGE == (int)kDebugStallFirstStage,
+              "debug bit values agree");
+
 static int check_config(const moe_tail_config_t* c) {
   if (c->max_rows < 1 || c->max_rows > kMaxRows) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->hidden < 128 || c->hidden % 128) return MOE_TAIL_ERR_UNSUPPORTED;
@@ -216,8 +219,9 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
                                 h->w, h->s, st, pdl));
     const uint64_t budget_ns =
         (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
-    MT_STAGE(launch_stream(0, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl));
-    MT_STAGE(launch_stream(1, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl));
+    const uint32_t dbg = h->cfg.debug_flags;
+    MT_STAGE(launch_stream(0, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
+    MT_STAGE(launch_stream(1, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
   }
   MT_STAGE(launch_combine(d, h->s, (__nv_bfloat16*)out, (__nv_bfloat16*)residual, st, pdl));
 #undef MT_STAGE

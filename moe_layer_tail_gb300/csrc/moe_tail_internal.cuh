@@ -66,6 +66,9 @@ struct Scratch {
   uint32_t* counters;    // [64] work counters and tickets (zero between calls)
 };
 
+// Debug bits the kernels read (same values as MOE_TAIL_DEBUG_* in moe_tail.h).
+constexpr uint32_t kDebugStallFirstStage = 4u;
+
 // counters[] slots
 enum : int { kCtrGateUp = 0, kCtrDown = 1, kCtrFrontTicket = 2 };
 
@@ -158,7 +161,7 @@ int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w);
 cudaError_t prepare_stream_kernels();
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
                           const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
-                          bool pdl);
+                          bool pdl, uint32_t debug);
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl);
 

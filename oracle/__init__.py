@@ -48,7 +48,7 @@ def _load():
         lib.oracle_expert.restype = None
         lib.oracle_shared.argtypes = [I, I, P, P, P, P, P]
         lib.oracle_shared.restype = None
-        lib.oracle_moe_tail.argtypes = [I, I, I, I, I, I, D] + [P] * 14 + [I]
+        lib.oracle_moe_tail.argtypes = [I, I, I, I, I, I, D] + [P] * 15 + [I]
         lib.oracle_moe_tail.restype = I
         _lib = lib
     return _lib
@@ -159,8 +159,9 @@ def shared(n_row, ws13, ws2):
 def moe_tail(inputs: dict, k: int, eps: float, nthreads: int = 1):
     """The whole tail.  `inputs` holds the arrays made by moe_layer_tail_gb300.inputs.
 
-    Returns dict(out [R,H] bf16 bits, residual [R,H] bf16 bits (r_new), ids [R,k],
-    wts [R,k] float64, logits [R,E] float64).  The caller's arrays are not modified.
+    Returns dict(out [R,H] bf16 bits, out_exact [R,H] float64 (before the bf16 rounding),
+    residual [R,H] bf16 bits (r_new), ids [R,k], wts [R,k] float64, logits [R,E] float64).
+    The caller's arrays are not modified.
     """
     x = _c(inputs["x"], np.uint16)
     res = np.array(inputs["residual"], dtype=np.uint16, copy=True, order="C")
@@ -180,12 +181,13 @@ def moe_tail(inputs: dict, k: int, eps: float, nthreads: int = 1):
     ids = np.empty((R, k), np.int32)
     wts = np.empty((R, k), np.float64)
     logits = np.empty((R, E), np.float64)
+    exact = np.empty((R, H), np.float64)
     rc = _load().oracle_moe_tail(R, H, E, int(k), I, Is, float(eps), _p(x), _p(res), _p(gamma),
                                  _p(w_r), _p(w13c), _p(w13s), _p(w2c), _p(w2s), _p(ws13), _p(ws2),
-                                 _p(out), _p(ids), _p(wts), _p(logits), int(nthreads))
+                                 _p(out), _p(ids), _p(wts), _p(logits), _p(exact), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_moe_tail rejected the shapes (rc=%d)" % rc)
-    return dict(out=out, residual=res, ids=ids, wts=wts, logits=logits)
+    return dict(out=out, out_exact=exact, residual=res, ids=ids, wts=wts, logits=logits)
 
 
 def bf16_bits_to_f64(a):

@@ -295,14 +295,15 @@ static void* oracle_worker(void* arg) {
 
 /* The whole layer tail for R rows.  Inputs are bf16 bits except the MXFP4 arrays (u8).
  * residual_io is read and then overwritten with r_new; out receives the MoE output.
- * ids_out [R, k], wts_out [R, k] and logits_out [R, E] may be NULL.
+ * ids_out [R, k], wts_out [R, k], logits_out [R, E] and out_exact [R, H] (the output
+ * before its bf16 rounding) may be NULL.
  * nthreads >= 1 splits the independent (row, pick) tasks over threads. */
 int oracle_moe_tail(int R, int H, int E, int k, int I, int Is, double eps,
                     const uint16_t* x, uint16_t* residual_io, const uint16_t* gamma,
                     const uint16_t* w_r, const uint8_t* w13_codes, const uint8_t* w13_scales,
                     const uint8_t* w2_codes, const uint8_t* w2_scales, const uint16_t* ws13,
                     const uint16_t* ws2, uint16_t* out, int32_t* ids_out, double* wts_out,
-                    double* logits_out, int nthreads) {
+                    double* logits_out, double* out_exact, int nthreads) {
   if (R < 1 || H < 32 || E < 1 || k < 1 || k > E || I < 32 || Is < 1 || H % 32 || I % 32)
     return -1;
   uint16_t* r_new = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)R * H);
@@ -344,6 +345,7 @@ int oracle_moe_tail(int R, int H, int E, int k, int I, int Is, double eps,
       for (int i = 0; i < k; ++i)
         acc += wts[(int64_t)r * k + i] * y[((int64_t)r * k + i) * H + h];
       acc += ys[(int64_t)r * H + h];
+      if (out_exact) out_exact[(int64_t)r * H + h] = acc;
       out[(int64_t)r * H + h] = oracle_bf16_round(acc);
     }
   memcpy(residual_io, r_new, sizeof(uint16_t) * (size_t)R * H);

@@ -6,7 +6,11 @@ Tolerances (from the method's acceptance rule for this layer tail):
   - the selected expert set equals the oracle's in every row whose fp32 k-th minus
     (k+1)-th logit margin exceeds 1e-3 (rows at or below that margin may pick either of
     the near-tied experts and are excluded from the output check when they differ);
-  - per row: cosine(out, oracle out) >= 0.9999 and max |out - oracle| <= 2e-2 * RMS(oracle row).
+  - per row: cosine(out, oracle out) >= 0.9999 and max |out - oracle| <= 2e-2 * RMS(oracle
+    row), where "oracle" is the oracle's exact fp64 output before its bf16 rounding and each
+    element may also carry the half-ulp rounding of its own bf16 storage (a fp32 sum and a
+    fp64 sum that straddle a rounding boundary land on different bf16 neighbours, which at
+    a large element is more than 2e-2 * RMS on its own).
 """
 import numpy as np
 
@@ -44,15 +48,18 @@ def check_parity(got_out, got_res, got_ids, orc, k, rows=None):
             skipped += 1
             continue
         a = bf16_decode(got_out[r])
-        b = bf16_decode(orc["out"][r])
+        b = np.asarray(orc["out_exact"][r], dtype=np.float64)
         assert np.isfinite(a).all(), "row %d: non-finite output" % r
         cos = float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
         rms = float(np.sqrt(np.mean(b * b)))
+        half_ulp = np.ldexp(1.0, np.floor(np.log2(np.maximum(np.abs(a), 1e-38))).astype(int) - 8)
+        excess = np.abs(a - b) - half_ulp
         err = float(np.max(np.abs(a - b)))
         worst_cos = min(worst_cos, cos)
-        worst_err = max(worst_err, err / max(rms, 1e-300))
+        worst_err = max(worst_err, float(np.max(excess)) / max(rms, 1e-300))
         assert cos >= COSINE_MIN, "row %d: cosine %.7f" % (r, cos)
-        assert err <= MAXERR_REL_RMS * rms, "row %d: max err %.4g > 2e-2 * rms %.4g" % (r, err, rms)
+        assert np.max(excess) <= MAXERR_REL_RMS * rms, \
+            "row %d: max err %.4g (beyond half an ulp) > 2e-2 * rms %.4g" % (r, err, rms)
     return {"worst_cosine": worst_cos, "worst_err_over_rms": worst_err, "skipped": skipped,
             "min_margin": float(np.min(margins))}
 

@@ -60,12 +60,14 @@ def test_workload_parity_full_size(name):
     out, res, ids, wts, nd = run_gpu(tail, d)
     figs = check_parity(out, res, ids, orc, wl.shape.k)
     assert nd == len(np.unique(orc["ids"]))
-    # weights: renormalised softmax of the picked logits, same pick order as the oracle
+    # weights: renormalised softmax of the picked logits.  The GPU's fp32 rstd can round a
+    # few elements of n to the other bf16 neighbour than the oracle's fp64 rstd, which moves
+    # a logit by ~1e-4 and a weight by up to ~1e-4: allow 5e-4.
     for r in range(wl.shape.R):
         if set(ids[r]) == set(orc["ids"][r]):
             o = {e: w for e, w in zip(orc["ids"][r], orc["wts"][r])}
             g = {e: w for e, w in zip(ids[r], wts[r])}
-            assert max(abs(o[e] - g[e]) for e in o) < 1e-5
+            assert max(abs(o[e] - g[e]) for e in o) < 5e-4
         assert abs(float(wts[r].sum()) - 1.0) < 1e-5
     assert tail.status() == 0
     if wl.kind == "similar":

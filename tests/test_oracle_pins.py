@@ -312,6 +312,9 @@ def test_whole_tail_matches_numpy_bruteforce():
     r_new, out_exact = _numpy_tail(d, shape.k, shape.eps)
     assert np.array_equal(got["residual"], r_new)
     assert is_nearest_bf16(got["out"], out_exact, slack=1e-9).all()
+    # the exact (pre-rounding) output agrees with the brute force, and rounds to `out`
+    assert np.allclose(got["out_exact"], out_exact, rtol=1e-10, atol=1e-12)
+    assert np.array_equal(got["out"], quantize_to_nearest_bf16_bits(got["out_exact"]).reshape(got["out"].shape))
     assert abs(got["wts"].sum(axis=1) - 1).max() < 1e-12
 
 
