@@ -218,13 +218,22 @@ __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
 
   for (int row = warp; row < R; row += nwarps) {
     const float* l = logits + (size_t)row * E;
+    // the row's logits, lane-strided, in registers (E <= 1024: up to 32 per lane)
+    float lv[kMaxExperts / 32];
+#pragma unroll
+    for (int q = 0; q < kMaxExperts / 32; ++q) {
+      const int e = lane + 32 * q;
+      lv[q] = (e < E) ? __ldcg(l + e) : -INFINITY;
+    }
     for (int i = 0; i < k; ++i) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
-      for (int e = lane; e < E; e += 32) {
+#pragma unroll
+      for (int q = 0; q < kMaxExperts / 32; ++q) {
+        const int e = lane + 32 * q;
+        if (e >= E) break;
         if (taken[row][e >> 5] & (1u << (e & 31))) continue;
-        const float v = __ldcg(l + e);
-        if (better(v, e, bv, be)) { bv = v; be = e; }
+        if (better(lv[q], e, bv, be)) { bv = lv[q]; be = e; }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -355,6 +364,7 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
   {
     float gm = 0.f;
+#pragma unroll 4
     for (int c = tid; c < H / 8; c += kFrontThreads) gm = fmaxf(gm, group_amax(__ldg(g4 + c)));
     gm = warp_max(gm);
     if (lane == 0) s_gmax[warp] = gm;
@@ -366,6 +376,7 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * H);
     const uint4* rr = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
     float ss = 0.f, rmax = 0.f;
+#pragma unroll 4
     for (int c = lane; c < H / 8; c += 32) {
       const uint4 xv = __ldg(xr + c), rv = __ldg(rr + c);
       const uint4 o4 = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
@@ -397,6 +408,17 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
     const int cw = min(kFrontChunk, H - h0);  // multiple of 128
     const int ng = cw / 8;                     // 16-byte groups per row in this chunk
     const bool owner = (ci % G) == (int)blockIdx.x;
+    // this warp's router weights for the chunk, loaded before n is built (up to 4 groups
+    // of 8 per lane: kFrontChunk / 8 / 32)
+    uint4 wreg[kFrontChunk / 8 / 32];
+#pragma unroll
+    for (int q = 0; q < kFrontChunk / 8 / 32; ++q) {
+      const int c = lane + 32 * q;
+      wreg[q] = (e < E && c < ng)
+                    ? __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)e * H + h0) + c)
+                    : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll 4
     for (int idx = tid; idx < R * ng; idx += kFrontThreads) {
       const int r = idx / ng, gidx = idx % ng;
       const size_t off = ((size_t)r * H + h0) / 8 + gidx;
@@ -417,9 +439,11 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
     }
     __syncthreads();
     if (e < E) {
-      const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)e * H + h0);
-      for (int c = lane; c < ng; c += 32) {
-        const uint4 wv = __ldg(wrow + c);
+#pragma unroll
+      for (int q = 0; q < kFrontChunk / 8 / 32; ++q) {
+        const int c = lane + 32 * q;
+        if (c >= ng) break;
+        const uint4 wv = wreg[q];
         const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
                              bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
 #pragma unroll

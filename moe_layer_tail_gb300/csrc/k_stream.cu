@@ -45,7 +45,8 @@ constexpr int kStageWS = 512;            // weight scales: 64 rows x 8 blocks
 constexpr int kStageAS = kMaxRows * 32;  // activation scales: 16 users x 8 floats
 constexpr int kStageBytes = kStageW + kStageA + kStageWS + kStageAS;
 constexpr int kRedBytes = kConsumerWarps * 4 * 2 * 512;  // [warp][tile][nt][lane] float4
-constexpr int kStreamSmem = 1024 + kStages * kStageBytes + kRedBytes + 256;
+constexpr int kTableBytes = (3 * kMaxPicks + 1 + kMaxRows) * 4;
+constexpr int kStreamSmem = 1024 + kStages * kStageBytes + kRedBytes + 256 + kTableBytes;
 
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 
@@ -64,8 +65,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// The call's dedup tables, copied to shared memory once per CTA.
+struct Tables {
+  const int* uniq;      // [D] distinct expert ids
+  const int* off;       // [D + 1] user offsets
+  const int* users;     // [R*k] pick indices r*k + slot
+  const float* rscale;  // [R] per-row scale of the f16 gate/up activations
+};
+
 __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
-                                            const Scratch& s, int D) {
+                                            const Tables& s, int D) {
   Item it;
   it.d = 0;
   it.e = 0;
@@ -88,8 +97,8 @@ __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
       it.out0 = jg * 32;
       it.row0 = it.e * 2 * dm.I + it.out0;
       it.row1 = it.row0 + dm.I;
-      it.u0 = s.user_off[it.d];
-      it.U = s.user_off[it.d + 1] - it.u0;
+      it.u0 = s.off[it.d];
+      it.U = s.off[it.d + 1] - it.u0;
     }
   } else {
     const int ns = dm.H / 16;
@@ -110,8 +119,8 @@ __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
       it.out0 = hg * 64;
       it.row0 = it.e * dm.H + it.out0;
       it.row1 = 0;
-      it.u0 = s.user_off[it.d];
-      it.U = s.user_off[it.d + 1] - it.u0;
+      it.u0 = s.off[it.d];
+      it.U = s.off[it.d + 1] - it.u0;
     }
   }
   it.U = max(0, min(it.U, kMaxRows));
@@ -240,6 +249,10 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   uint64_t* full = (uint64_t*)(smem + kStages * kStageBytes + kRedBytes);
   uint64_t* empty = full + kStages;
   int* info = (int*)(empty + kStages);  // [kStages][2]: item, k-chunk
+  int* t_uniq = (int*)(smem + kStages * kStageBytes + kRedBytes + 256);
+  int* t_off = t_uniq + kMaxPicks;
+  int* t_users = t_off + kMaxPicks + 1;
+  float* t_rscale = (float*)(t_users + kMaxPicks);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Before the routing is known: pull this CTA's share of the shared expert's weights into
@@ -256,8 +269,17 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     }
   }
   pdl_wait();
-  const int D = *s.n_distinct;
+  const int D = min(max(*s.n_distinct, 1), kMaxPicks);
   const int n_items = (PHASE == 0) ? dm.Is / 8 + D * (dm.I / 32) : dm.H / 16 + D * (dm.H / 64);
+  for (int i = threadIdx.x; i < D; i += kStreamThreads) t_uniq[i] = s.uniq[i];
+  for (int i = threadIdx.x; i <= D; i += kStreamThreads) t_off[i] = s.user_off[i];
+  for (int i = threadIdx.x; i < dm.R * dm.k; i += kStreamThreads) t_users[i] = s.user_list[i];
+  for (int i = threadIdx.x; i < dm.R; i += kStreamThreads) t_rscale[i] = s.n16s[i];
+  Tables tb;
+  tb.uniq = t_uniq;
+  tb.off = t_off;
+  tb.users = t_users;
+  tb.rscale = t_rscale;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -280,15 +302,36 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     // failure-injection switch: CTA 0 leaves its first stage unpublished, so the consumers'
     // bounded wait on it expires (tests the timeout path; never set in production)
     bool skip_first = (debug & kDebugStallFirstStage) && blockIdx.x == 0;
+    int item = 0;
+    if (lane == 0) item = (int)atomicAdd(&s.counters[PHASE], 1u);
     for (;;) {
-      int item = 0;
-      if (lane == 0) item = (int)atomicAdd(&s.counters[PHASE], 1u);
       item = __shfl_sync(0xffffffffu, item, 0);
       if (item >= n_items) {
         pdl_trigger();  // this CTA is in its tail: let the next launch take the SM
         break;
       }
-      const Item it = decode_item(PHASE, item, dm, s, D);
+      int next = 0;  // the following item, fetched while this one streams
+      if (lane == 0) next = (int)atomicAdd(&s.counters[PHASE], 1u);
+      const Item it = decode_item(PHASE, item, dm, tb, D);
+      // lane u < U: where user u's activations (and down's per-block scales) come from
+      const uint8_t* asrc = nullptr;
+      const float* ssrc = nullptr;
+      if (lane < it.U) {
+        if (it.kind == kSharedGU) {
+          asrc = (const uint8_t*)(s.n + (size_t)lane * dm.H);
+        } else if (it.kind == kSharedDN) {
+          asrc = (const uint8_t*)(s.ms + (size_t)lane * dm.Is);
+        } else if (it.kind == kRoutedGU) {
+          asrc = (const uint8_t*)(s.n16 + (size_t)(tb.users[it.u0 + lane] / dm.k) * dm.H);
+        } else {
+          const int pick = tb.users[it.u0 + lane];
+          asrc = (const uint8_t*)(s.mid16 + (size_t)pick * dm.I);
+          ssrc = s.mid16s + (size_t)pick * (dm.I / 32);
+        }
+      }
+      const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
+      const uint8_t* wsbase = (it.kind == kRoutedGU) ? w.w13s : w.w2s;
+      const int kb = it.K / 32;  // scale bytes per weight row
       for (int kc = 0; kc < it.nst && ok; ++kc) {
         if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, budget_ns);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -314,7 +357,6 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
           uint32_t bytes = 0;
           if (it.kind == kRoutedGU) bytes = (uint32_t)(kval / 128) * 2 * 2048;
           else if (it.kind == kRoutedDN) bytes = (uint32_t)(kval / 128) * 4096;
-          else if (it.kind == kSharedGU) bytes = (uint32_t)(kval / 32) * 1024;
           else bytes = (uint32_t)(kval / 32) * 1024;
           bytes += (uint32_t)it.U * (uint32_t)kval * 2u;
           mbar_expect_tx(&full[stage], bytes);
@@ -336,48 +378,37 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
             for (int q = 0; q < kval / 32; ++q)
               tma_load_2d(sw + q * 1024, &maps.ws2, k0 + q * 32, it.row0, &full[stage], pol);
           }
-          // activation slices of the users (f16 scaled for routed, bf16 for shared)
-          for (int u = 0; u < it.U; ++u) {
-            const void* src;
-            if (it.kind == kSharedGU) src = s.n + (size_t)u * dm.H + k0;
-            else if (it.kind == kSharedDN) src = s.ms + (size_t)u * dm.Is + k0;
-            else if (it.kind == kRoutedGU) src = s.n16 + (size_t)(s.user_list[it.u0 + u] / dm.k) * dm.H + k0;
-            else src = s.mid16 + (size_t)s.user_list[it.u0 + u] * dm.I + k0;
-            bulk_load(sa + u * kActStride, src, (uint32_t)kval * 2u, &full[stage]);
-          }
         }
-        // scales (routed only), copied by all producer lanes with cp.async
-        if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
-          const int kb = it.K / 32;           // scale bytes per weight row
-          const int words = kval / 128;       // 4-byte words per row in this stage (1 or 2)
-          for (int c = lane; c < 64 * 2; c += 32) {
+        __syncwarp();
+        // user u's activation slice (f16 scaled for routed, bf16 for shared), by lane u
+        if (lane < it.U)
+          bulk_load(sa + lane * kActStride, asrc + (size_t)k0 * 2, (uint32_t)kval * 2u, &full[stage]);
+        if (routed) {
+          // E8M0 scales of the 64 weight rows, 8 blocks each (4 bytes per copy)
+          const int words = kval / 128;  // 1 or 2 words per row in this stage
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = lane + 32 * q;
             const int row = c >> 1, wd = c & 1;
-            if (wd >= words) continue;
-            size_t grow;
-            const uint8_t* base;
-            if (it.kind == kRoutedGU) {
-              grow = (row < 32) ? (size_t)it.row0 + row : (size_t)it.row1 + (row - 32);
-              base = w.w13s;
-            } else {
-              grow = (size_t)it.row0 + row;
-              base = w.w2s;
+            if (wd < words) {
+              const size_t grow = (it.kind == kRoutedGU)
+                                      ? ((row < 32) ? (size_t)it.row0 + row : (size_t)it.row1 + (row - 32))
+                                      : (size_t)it.row0 + row;
+              cp_async4(sws + row * 8 + wd * 4, wsbase + grow * kb + (k0 / 32) + wd * 4);
             }
-            cp_async4(sws + row * 8 + wd * 4, base + grow * kb + (k0 / 32) + wd * 4);
           }
           // per-block activation scales (down only: the gate/up activations carry one
           // scale per row, applied in the epilogue)
-          for (int c = lane; it.kind == kRoutedDN && c < it.U * 2; c += 32) {
-            const int u = c >> 1, half = c & 1;
-            if (half >= words) continue;
-            const float* src =
-                s.mid16s + (size_t)s.user_list[it.u0 + u] * (dm.I / 32) + k0 / 32 + half * 4;
-            cp_async16(sas + u * 32 + half * 16, src);
+          if (ssrc != nullptr) {
+            for (int half = 0; half < words; ++half)
+              cp_async16(sas + lane * 32 + half * 16, ssrc + k0 / 32 + half * 4);
           }
         }
         cp_async_arrive_noinc(&full[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
+      item = next;
     }
     if (ok) {
       // end-of-work marker
@@ -426,7 +457,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     if (item < 0) break;
     if (item != cur) {
       cur = item;
-      it = decode_item(PHASE, item, dm, s, D);
+      it = decode_item(PHASE, item, dm, tb, D);
 #pragma unroll
       for (int m = 0; m < 4; ++m)
 #pragma unroll
@@ -576,7 +607,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
             for (int q = 0; q < 2; ++q) {
               const int u = nt * 8 + 2 * t + q;
               if (nt < NT && u < it.U) {
-                const int pick = s.user_list[it.u0 + u];
+                const int pick = tb.users[it.u0 + u];
                 float* yrow = s.y + (size_t)pick * dm.H + it.out0;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
@@ -595,7 +626,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
               if (nt >= NT) continue;
               const int u = nt * 8 + 2 * t + q;
               // the row's activation scale (one power of two per row)
-              const float rs = (u < it.U) ? s.n16s[s.user_list[it.u0 + u] / dm.k] : 0.f;
+              const float rs = (u < it.U) ? tb.rscale[tb.users[it.u0 + u] / dm.k] : 0.f;
               float mv[4];
               float amax = 0.f;
 #pragma unroll
@@ -614,7 +645,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
               }
               const float down = __uint_as_float((uint32_t)(127 - p) << 23);
               if (u < it.U) {
-                const int pick = s.user_list[it.u0 + u];
+                const int pick = tb.users[it.u0 + u];
                 __half* mrow = s.mid16 + (size_t)pick * dm.I + it.out0;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) mrow[8 * m + g] = __float2half_rn(mv[m] * down);

@@ -84,6 +84,8 @@ def _small(seed, R=3, H=384, E=12, k=3, I=256, Is=192, kind="plain"):
 
 SIMPLE = 1  # debug flag: warp-per-row CUDA-core expert kernels instead of the streaming ones
 NO_PDL = 2  # debug flag: plain stream-ordered launches (no programmatic dependent launch)
+STALL = 4   # debug flag: one producer leaves a stage unpublished (failure injection)
+STATUS_TIMEOUT = 4  # device status bit: a bounded wait expired
 
 
 def _check_small(shape, d, max_rows=None, rows=None, flags=0):
@@ -104,6 +106,7 @@ def _check_small(shape, d, max_rows=None, rows=None, flags=0):
     (16, 256, 16, 16, 128, 128),   # k = E: every expert, maximum rows
     (16, 512, 64, 1, 256, 64),     # k = 1, maximum rows
     (4, 1024, 40, 32, 128, 256),   # k at its maximum
+    (4, 256, 1024, 8, 128, 64),    # the maximum expert count
 ])
 def test_small_shapes(R, H, E, k, I, Is, flags):
     shape, d = _small(100 + R + E, R, H, E, k, I, Is)
@@ -222,3 +225,23 @@ def test_run_rejects_bad_arguments():
             MoeTail(bad, dev)
         assert ei.value.code == ERR_UNSUPPORTED
     assert tail.status() == 0
+
+
+def test_device_wait_timeout_is_reported_and_context_survives():
+    """Failure detection without a fault: a stage that is never published makes the
+    consumers' bounded wait (5 ms here) expire; the kernel records the timeout in the
+    status word and returns, and the next call on a healthy handle is correct."""
+    shape, d = _small(14, R=2, H=512, E=8, k=2, I=256, Is=128)
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    bad = MoeTail(shape, dev, wait_budget_us=5000, debug_flags=STALL)
+    x = acts_to_device(d["x"])
+    res = acts_to_device(d["residual"])
+    out = torch.empty_like(x)
+    bad.run(x, res, out)
+    torch.cuda.synchronize()
+    st = bad.status()
+    assert st & STATUS_TIMEOUT, st
+    bad.clear_status()
+    assert bad.status() == 0
+    bad.close()
+    _check_small(shape, d)  # the context is healthy: a normal handle matches the oracle
