@@ -44,9 +44,10 @@ constexpr int kStageA = kMaxRows * kActStride;
 constexpr int kStageWS = 512;            // weight scales: 64 rows x 8 blocks
 constexpr int kStageAS = kMaxRows * 32;  // activation scales: 16 users x 8 floats
 constexpr int kStageBytes = kStageW + kStageA + kStageWS + kStageAS;
-constexpr int kRedBytes = kConsumerWarps * 4 * 2 * 512;  // [warp][tile][nt][lane] float4
+constexpr int kRedBytes = 2 * kConsumerWarps * 4 * 2 * 512;  // 2 x [warp][tile][nt][lane] float4
 constexpr int kTableBytes = (3 * kMaxPicks + 1 + kMaxRows) * 4;
-constexpr int kStreamSmem = 1024 + kStages * kStageBytes + kRedBytes + 256 + kTableBytes;
+constexpr int kXmaxBytes = 2 * 4 * kMaxRows * 4;
+constexpr int kStreamSmem = kStages * kStageBytes + kRedBytes + 256 + kTableBytes + kXmaxBytes;
 
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 
@@ -204,7 +205,7 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, 
 }
 __device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -212,7 +213,7 @@ __device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint
 }
 __device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -236,14 +237,113 @@ __device__ __forceinline__ uint32_t swz64(uint32_t base, int r, int c) {
   return base + (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
 }
 
+// Byte offset of 16-byte chunk c of row r in a box of 64-byte rows written by TMA with the
+// 64-byte swizzle (chunk index XOR bits 1..2 of the row; box base 512-byte aligned).
+__device__ __forceinline__ int swz64_off(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
+
+// One stage of a routed MXFP4 item, K-slot cw (32 elements = one scale block) of the
+// stage, all 4 MMA tiles.  GATE_UP: tile m = gate rows 8m..8m+7 (A rows 0-7) and the up rows
+// of the same j (A rows 8-15), weight scales rows [0, 32) gate, [32, 64) up; else tile m =
+// down rows 16m..16m+15.  The activation scale is per row (gate/up, applied later) or per
+// block (down, here).
+template <bool GATE_UP>
+__device__ __forceinline__ void stage_routed(const uint8_t* st, int cw, int g, int t, int NT,
+                                             float (&acc)[4][2][4]) {
+  const uint8_t* sw = st;
+  const uint8_t* sa = st + kStageW;
+  const uint8_t* sws = sa + kStageA;
+  const float* sas = reinterpret_cast<const float*>(sws + kStageWS);
+  uint4 b[2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+    if (nt < NT)
+      b[nt] = *reinterpret_cast<const uint4*>(sa + (nt * 8 + g) * kActStride + cw * 64 + t * 16);
+  float as[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      as[nt][q] = GATE_UP ? 1.0f : ((nt < NT) ? sas[(nt * 8 + 2 * t + q) * 8 + cw] : 0.f);
+  const int bx = cw >> 2, ch = cw & 3;
+  uint32_t wa[4], wb[4];
+  float sa_[4], sb_[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    int ra, rb, sra, srb;
+    const uint8_t *boxa, *boxb;
+    if (GATE_UP) {
+      ra = 8 * m + g; rb = ra;
+      boxa = sw + bx * 2048; boxb = sw + 4096 + bx * 2048;
+      sra = ra; srb = 32 + rb;
+    } else {
+      ra = 16 * m + g; rb = ra + 8;
+      boxa = sw + bx * 4096; boxb = boxa;
+      sra = ra; srb = rb;
+    }
+    wa[m] = *reinterpret_cast<const uint32_t*>(boxa + swz64_off(ra, ch) + 4 * t);
+    wb[m] = *reinterpret_cast<const uint32_t*>(boxb + swz64_off(rb, ch) + 4 * t);
+    sa_[m] = e8m0_to_float(sws[sra * 8 + cw]);
+    sb_[m] = e8m0_to_float(sws[srb * 8 + cw]);
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    uint32_t ha[4], hb[4];
+    e2m1x8_to_f16x2(wa[m], ha[0], ha[1], ha[2], ha[3]);
+    e2m1x8_to_f16x2(wb[m], hb[0], hb[1], hb[2], hb[3]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      if (nt < NT) {
+        float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16(tmp, ha[0], hb[0], ha[1], hb[1], b[nt].x, b[nt].y);
+        mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b[nt].z, b[nt].w);
+        if (GATE_UP) {
+          acc[m][nt][0] += tmp[0] * sa_[m];
+          acc[m][nt][1] += tmp[1] * sa_[m];
+          acc[m][nt][2] += tmp[2] * sb_[m];
+          acc[m][nt][3] += tmp[3] * sb_[m];
+        } else {
+          acc[m][nt][0] += tmp[0] * (sa_[m] * as[nt][0]);
+          acc[m][nt][1] += tmp[1] * (sa_[m] * as[nt][1]);
+          acc[m][nt][2] += tmp[2] * (sb_[m] * as[nt][0]);
+          acc[m][nt][3] += tmp[3] * (sb_[m] * as[nt][1]);
+        }
+      }
+    }
+  }
+}
+
+// One stage of a shared-expert (bf16) item: K-slot cw is one 32-element box per half,
+// one 16-row tile (gate/up: 8 gate rows + the 8 up rows of the same j; down: 16 rows).
+__device__ __forceinline__ void stage_shared(const uint8_t* st, int cw, int g, int t, int NT,
+                                             bool gate_up, float (&acc)[4][2][4]) {
+  const uint8_t* box = st + cw * 1024;
+  const uint8_t* sa = st + kStageW;
+  const uint4 a = *reinterpret_cast<const uint4*>(box + swz64_off(g, t));
+  const uint4 c = gate_up ? *reinterpret_cast<const uint4*>(box + 512 + swz64_off(g, t))
+                          : *reinterpret_cast<const uint4*>(box + swz64_off(g + 8, t));
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    if (nt < NT) {
+      const uint4 b = *reinterpret_cast<const uint4*>(sa + (nt * 8 + g) * kActStride + cw * 64 + t * 16);
+      mma_bf16(acc[0][nt], a.x, c.x, a.y, c.y, b.x, b.y);
+      mma_bf16(acc[0][nt], a.z, c.z, a.w, c.w, b.z, b.w);
+    }
+  }
+}
+
 // ------------------------------------------------------------------------ kernel ----
 
 template <int PHASE>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
          uint64_t budget_ns, uint32_t debug) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // The dynamic shared memory starts 1024-byte aligned (nothing else is in shared memory),
+  // as the swizzled TMA boxes need; every pointer below stays in the shared space.
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) set_status(s.status, kStatusBadTile);
+    return;
+  }
   uint8_t* stages = smem;
   float4* red = (float4*)(smem + kStages * kStageBytes);
   uint64_t* full = (uint64_t*)(smem + kStages * kStageBytes + kRedBytes);
@@ -253,6 +353,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   int* t_off = t_uniq + kMaxPicks;
   int* t_users = t_off + kMaxPicks + 1;
   float* t_rscale = (float*)(t_users + kMaxPicks);
+  float* xmax = t_rscale + kMaxRows;  // [2][4 tiles][kMaxRows]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Before the routing is known: pull this CTA's share of the shared expert's weights into
@@ -438,16 +539,15 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   }
 
   // ------------------------------------------------------------------ consumers ----
-  const int cw = warp - 1;            // K-slot of every stage this warp owns
+  const int cw = warp - 1;  // K-slot of every stage this warp owns, and its epilogue share
   const int g = lane >> 2, t = lane & 3;
   int stage = 0;
   uint32_t phase = 0;
-  int cur = -1;
+  int cur = -1, nitems = 0;
   Item it;
   it.kind = 0; it.nst = 0; it.U = 0; it.K = 0; it.out0 = 0; it.u0 = 0; it.row0 = 0; it.row1 = 0;
   it.e = 0; it.d = 0;
   float acc[4][2][4];
-  const uint32_t sbase = smem_u32(stages);
   for (;;) {
     if (!mbar_wait(&full[stage], phase, budget_ns)) {
       if (lane == 0) set_status(s.status, kStatusTimeout);
@@ -465,87 +565,15 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
 #pragma unroll
           for (int q = 0; q < 4; ++q) acc[m][nt][q] = 0.f;
     }
-    const int k0 = kc * kKChunk;
-    const uint32_t sw = sbase + stage * kStageBytes;
-    const uint32_t sa = sw + kStageW;
-    const uint8_t* sws = stages + stage * kStageBytes + kStageW + kStageA;
-    const float* sas = (const float*)(sws + kStageWS);
+    const uint8_t* st = stages + stage * kStageBytes;
     const int NT = it.U > 8 ? 2 : 1;
-    if (k0 + 32 * cw < it.K) {
-      // B fragments: user (nt*8 + g), elements [32cw + 8t, +8) of this stage
-      uint32_t b[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-        if (nt < NT)
-          lds128(sa + (nt * 8 + g) * kActStride + cw * 64 + t * 16, b[nt][0], b[nt][1],
-                 b[nt][2], b[nt][3]);
-      if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
-        float as[2][2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            as[nt][q] = (PHASE == 1) ? sas[(nt * 8 + 2 * t + q) * 8 + cw] : 1.0f;
-        const int bx = cw >> 2, ch = cw & 3;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          int ra, rb, sra, srb;
-          uint32_t boxa, boxb;
-          if (it.kind == kRoutedGU) {
-            ra = 8 * m + g; rb = ra;                       // gate row, up row (same j)
-            boxa = sw + bx * 2048; boxb = sw + 4096 + bx * 2048;
-            sra = ra; srb = 32 + rb;
-          } else {
-            ra = 16 * m + g; rb = ra + 8;
-            boxa = sw + bx * 4096; boxb = boxa;
-            sra = ra; srb = rb;
-          }
-          const uint32_t wa = lds32(swz64(boxa, ra, ch) + 4 * t);
-          const uint32_t wb = lds32(swz64(boxb, rb, ch) + 4 * t);
-          uint32_t ha[4], hb[4];
-          cvt_e2m1x4(wa, ha);
-          cvt_e2m1x4(wb, hb);
-          const float sa_ = e8m0_to_float(sws[sra * 8 + cw]);
-          const float sb_ = e8m0_to_float(sws[srb * 8 + cw]);
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            if (nt < NT) {
-              float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_f16(tmp, ha[0], hb[0], ha[1], hb[1], b[nt][0], b[nt][1]);
-              mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b[nt][2], b[nt][3]);
-              if (PHASE == 1) {
-                acc[m][nt][0] += tmp[0] * (sa_ * as[nt][0]);
-                acc[m][nt][1] += tmp[1] * (sa_ * as[nt][1]);
-                acc[m][nt][2] += tmp[2] * (sb_ * as[nt][0]);
-                acc[m][nt][3] += tmp[3] * (sb_ * as[nt][1]);
-              } else {
-                acc[m][nt][0] += tmp[0] * sa_;
-                acc[m][nt][1] += tmp[1] * sa_;
-                acc[m][nt][2] += tmp[2] * sb_;
-                acc[m][nt][3] += tmp[3] * sb_;
-              }
-            }
-          }
-        }
-      } else {
-        // shared expert: bf16 weights, one 16-row tile, K-slot cw = box cw
-        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-        const uint32_t box = sw + cw * 1024;
-        if (it.kind == kSharedGU) {
-          lds128(swz64(box, g, t), a0, a1, a2, a3);          // gate row g
-          lds128(swz64(box + 512, g, t), c0, c1, c2, c3);    // up row g
-        } else {
-          lds128(swz64(box, g, t), a0, a1, a2, a3);          // row g
-          lds128(swz64(box, g + 8, t), c0, c1, c2, c3);      // row g + 8
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          if (nt < NT) {
-            mma_bf16(acc[0][nt], a0, c0, a1, c1, b[nt][0], b[nt][1]);
-            mma_bf16(acc[0][nt], a2, c2, a3, c3, b[nt][2], b[nt][3]);
-          }
-        }
-      }
+    if (kc * kKChunk + 32 * cw < it.K) {
+      if (it.kind == kRoutedGU)
+        stage_routed<true>(st, cw, g, t, NT, acc);
+      else if (it.kind == kRoutedDN)
+        stage_routed<false>(st, cw, g, t, NT, acc);
+      else
+        stage_shared(st, cw, g, t, NT, it.kind == kSharedGU, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
@@ -553,110 +581,104 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
 
     if (kc == it.nst - 1) {
       // ------------------------------------------------------ item epilogue ----
+      // partial sums of the 8 warps go to one of two reduction buffers (alternating by
+      // item, so no barrier is needed before the next item writes); warp cw then adds the
+      // 8 partials of tile (cw & 3), N-tile (cw >> 2) in warp order and stores them.
+      const int buf = nitems & 1;
+      ++nitems;
+      float4* rb = red + buf * (kConsumerWarps * 4 * 2 * 32);
       const int ntiles = (it.kind == kRoutedGU || it.kind == kRoutedDN) ? 4 : 1;
 #pragma unroll
       for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
           if (m < ntiles && nt < NT)
-            red[((cw * 4 + m) * 2 + nt) * 32 + lane] =
+            rb[((cw * 4 + m) * 2 + nt) * 32 + lane] =
                 make_float4(acc[m][nt][0], acc[m][nt][1], acc[m][nt][2], acc[m][nt][3]);
       named_bar_sync(1, kConsumerWarps * 32);
-      if (cw == 0) {
-        float c[4][2][4];
+      const int em = cw & 3, ent = cw >> 2;
+      const bool active = em < ntiles && ent < NT;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      if (active) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+          const float4 v = rb[((w2 * 4 + em) * 2 + ent) * 32 + lane];
+          c[0] += v.x; c[1] += v.y; c[2] += v.z; c[3] += v.w;
+        }
+      }
+      if (it.kind == kSharedGU) {
+        if (active) {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            if (m >= ntiles || nt >= NT) {
-              c[m][nt][0] = c[m][nt][1] = c[m][nt][2] = c[m][nt][3] = 0.f;
-              continue;
-            }
-            float4 sum = red[((0 * 4 + m) * 2 + nt) * 32 + lane];
-            for (int w2 = 1; w2 < kConsumerWarps; ++w2) {
-              const float4 v = red[((w2 * 4 + m) * 2 + nt) * 32 + lane];
-              sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-            }
-            c[m][nt][0] = sum.x; c[m][nt][1] = sum.y; c[m][nt][2] = sum.z; c[m][nt][3] = sum.w;
+          for (int q = 0; q < 2; ++q) {
+            const int r = ent * 8 + 2 * t + q;
+            if (r < it.U)
+              s.ms[(size_t)r * dm.Is + it.out0 + g] = __float2bfloat16_rn(silu_f(c[q]) * c[2 + q]);
           }
-        if (it.kind == kSharedGU) {
+        }
+      } else if (it.kind == kSharedDN) {
+        if (active) {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int r = nt * 8 + 2 * t + q;
-              if (nt < NT && r < it.U)
-                s.ms[(size_t)r * dm.Is + it.out0 + g] =
-                    __float2bfloat16_rn(silu_f(c[0][nt][q]) * c[0][nt][2 + q]);
+          for (int q = 0; q < 2; ++q) {
+            const int r = ent * 8 + 2 * t + q;
+            if (r < it.U) {
+              s.ys[(size_t)r * dm.H + it.out0 + g] = c[q];
+              s.ys[(size_t)r * dm.H + it.out0 + g + 8] = c[2 + q];
             }
-        } else if (it.kind == kSharedDN) {
+          }
+        }
+      } else if (it.kind == kRoutedDN) {
+        if (active) {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int r = nt * 8 + 2 * t + q;
-              if (nt < NT && r < it.U) {
-                s.ys[(size_t)r * dm.H + it.out0 + g] = c[0][nt][q];
-                s.ys[(size_t)r * dm.H + it.out0 + g + 8] = c[0][nt][2 + q];
-              }
+          for (int q = 0; q < 2; ++q) {
+            const int u = ent * 8 + 2 * t + q;
+            if (u < it.U) {
+              float* yrow = s.y + (size_t)tb.users[it.u0 + u] * dm.H + it.out0 + 16 * em;
+              yrow[g] = c[q];
+              yrow[g + 8] = c[2 + q];
             }
-        } else if (it.kind == kRoutedDN) {
+          }
+        }
+      } else {
+        // routed gate/up: mid = bf16(SiLU(gate) * up) with the row's activation scale
+        // restored; its f16 copy gets one power-of-two scale per (pick, 32 columns), from
+        // the maximum over the item's 4 tiles (exchanged through shared memory)
+        float* mx = xmax + buf * (4 * kMaxRows);
+        float mv[2];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+        for (int q = 0; q < 2; ++q) {
+          const int u = ent * 8 + 2 * t + q;
+          const float rs = (active && u < it.U) ? tb.rscale[tb.users[it.u0 + u] / dm.k] : 0.f;
+          mv[q] = __bfloat162float(__float2bfloat16_rn(silu_f(c[q] * rs) * (c[2 + q] * rs)));
+          float amax = fabsf(mv[q]);
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+          if (active && g == 0) mx[em * kMaxRows + u] = amax;
+        }
+        named_bar_sync(2, kConsumerWarps * 32);
+        if (active) {
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const int u = nt * 8 + 2 * t + q;
-              if (nt < NT && u < it.U) {
-                const int pick = tb.users[it.u0 + u];
-                float* yrow = s.y + (size_t)pick * dm.H + it.out0;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                  yrow[16 * m + g] = c[m][nt][q];
-                  yrow[16 * m + g + 8] = c[m][nt][2 + q];
-                }
-              }
-            }
-        } else {
-          // routed gate/up: mid = bf16(SiLU(gate) * up), then the f16 copy with one
-          // power-of-two scale per (pick, 32 columns)
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              if (nt >= NT) continue;
-              const int u = nt * 8 + 2 * t + q;
-              // the row's activation scale (one power of two per row)
-              const float rs = (u < it.U) ? tb.rscale[tb.users[it.u0 + u] / dm.k] : 0.f;
-              float mv[4];
+          for (int q = 0; q < 2; ++q) {
+            const int u = ent * 8 + 2 * t + q;
+            if (u < it.U) {
               float amax = 0.f;
 #pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                mv[m] = __bfloat162float(__float2bfloat16_rn(silu_f(c[m][nt][q] * rs) *
-                                                             (c[m][nt][2 + q] * rs)));
-                amax = fmaxf(amax, fabsf(mv[m]));
-              }
-              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
-              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+              for (int m2 = 0; m2 < 4; ++m2) amax = fmaxf(amax, mx[m2 * kMaxRows + u]);
               int p = 0;
               if (amax > 0.f) {
                 const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
                 p = max(-100, min(100, ex - 14));
               }
               const float down = __uint_as_float((uint32_t)(127 - p) << 23);
-              if (u < it.U) {
-                const int pick = tb.users[it.u0 + u];
-                __half* mrow = s.mid16 + (size_t)pick * dm.I + it.out0;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) mrow[8 * m + g] = __float2half_rn(mv[m] * down);
-                if (g == 0)
-                  s.mid16s[(size_t)pick * (dm.I / 32) + it.out0 / 32] =
-                      __uint_as_float((uint32_t)(127 + p) << 23);
-              }
+              const int pick = tb.users[it.u0 + u];
+              s.mid16[(size_t)pick * dm.I + it.out0 + 8 * em + g] = __float2half_rn(mv[q] * down);
+              if (em == 0 && g == 0)
+                s.mid16s[(size_t)pick * (dm.I / 32) + it.out0 / 32] =
+                    __uint_as_float((uint32_t)(127 + p) << 23);
             }
+          }
         }
       }
-      named_bar_sync(1, kConsumerWarps * 32);
     }
   }
 }
