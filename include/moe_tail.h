@@ -150,6 +150,29 @@ int moe_tail_set_stage_events(moe_tail_t* h, void* const* events, int32_t n_even
 /* Number of kernels one moe_tail_run enqueues for `rows` rows (for launch accounting). */
 int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows);
 
+/* Routing of one call with no device allocation at all, for callers that cannot call
+ * cudaMalloc: a host framework that owns every device allocation and hands a plugin only
+ * its input and output tensors, or a decode step replayed from a memory pool that is
+ * frozen once warm-up is over.  It runs add + RMSNorm, the router GEMV and the top-k with
+ * renormalised weights on `stream`, with the same arithmetic as the front of moe_tail_run:
+ *   x, residual  bf16 [rows, hidden] device (both only read here)
+ *   gamma bf16 [hidden], router_w bf16 [n_experts, hidden] device
+ *   ids int32 [rows, top_k], wts float [rows, top_k] device, written in pick order;
+ *   n_distinct int32 device, may be NULL: the number of distinct experts picked.
+ * Its scratch is one fixed 71,696-byte array in the library's own device memory (a
+ * file-scope variable that every GPU which loads the library keeps until the process
+ * exits).  The array bounds the call: rows <= 16, n_experts <= 1024, top_k <= 32 (and
+ * hidden a multiple of 128); anything larger returns MOE_TAIL_ERR_UNSUPPORTED.  The first
+ * call on a device looks up the array's device address with that device current, so make
+ * that first call before any stream capture.  Every call shares the array and it keeps the
+ * last call's contents (the call clears its own counter first): calls that overlap on the
+ * same GPU race, so issue them in one stream or otherwise ordered.  Nothing is allocated or
+ * freed.  The pages have no counterpart to this entry point. */
+int moe_tail_route_noalloc(const void* x, const void* residual, const void* gamma,
+                           const void* router_w, int32_t rows, int32_t hidden,
+                           int32_t n_experts, int32_t top_k, float rms_eps, int32_t* ids,
+                           float* wts, int32_t* n_distinct, void* stream);
+
 /* Free the handle and its scratch (synchronises the device first).  NULL is a no-op. */
 void moe_tail_destroy(moe_tail_t* h);
 

@@ -13,6 +13,7 @@
 // three single-purpose kernels k_add_rmsnorm / k_router / k_topk_dedup used by the
 // cross-checking path.  bf16(x + residual) goes to scratch; the residual itself is
 // rewritten by the combine, after every reader is done.
+#include "../../include/moe_tail.h"
 #include "moe_tail_internal.cuh"
 
 namespace mtail {
@@ -500,3 +501,164 @@ cudaError_t launch_front_fused(const Dims& d, const __nv_bfloat16* x,
 }
 
 }  // namespace mtail
+
+// ------------------------------------------- routing without any allocation ----
+// The routing of one call (add + RMSNorm, router GEMV, top-k with renormalised weights)
+// for callers that cannot allocate device memory: everything the launch needs besides its
+// inputs and outputs lives in the file-scope array below, which every GPU that loads this
+// library holds until the process exits.  Its size bounds the call: rows <= 16 and
+// n_experts <= 1024 (the fp32 logits), plus the dedup tables and the ticket counter.
+
+namespace mtail {
+
+struct RouteScratch {
+  float logits[kMaxRows * kMaxExperts];
+  int32_t n_distinct;
+  int32_t status;
+  int32_t uniq[kMaxPicks];
+  int32_t user_off[kMaxPicks + 1];
+  int32_t user_list[kMaxPicks];
+  uint32_t ticket;
+};
+
+static_assert(sizeof(RouteScratch) == 71696, "the size stated in moe_tail.h");
+static __device__ __align__(256) uint8_t g_route_scratch[sizeof(RouteScratch)];
+
+// Same arithmetic as k_front_fused (same rstd, n and logit order, same top-k), without the
+// stores the expert stages need; ids/wts/n_distinct go to the caller's buffers.
+__global__ void __launch_bounds__(kFrontThreads)
+k_route_static(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ residual,
+               const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ w_r,
+               RouteScratch* __restrict__ rs, int32_t* __restrict__ ids_out,
+               float* __restrict__ wts_out, int32_t* __restrict__ nd_out, int R, int H, int E,
+               int k, float eps) {
+  __shared__ float s_rstd[kMaxRows];
+  __shared__ uint4 s_n[kMaxRows][kFrontChunk / 8];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x;
+  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+  for (int r = warp; r < R; r += kFrontWarps) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * H);
+    const uint4* rr = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
+    float ss = 0.f;
+#pragma unroll 4
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 xv = __ldg(xr + c), rv = __ldg(rr + c);
+      const uint32_t o[4] = {add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
+                             add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w)};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        ss += bf16_lo(o[q]) * bf16_lo(o[q]) + bf16_hi(o[q]) * bf16_hi(o[q]);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) s_rstd[r] = 1.0f / sqrtf(ss / (float)H + eps);
+  }
+  __syncthreads();
+  const int e = blockIdx.x * kFrontWarps + warp;
+  float acc[kMaxRows];
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+  for (int h0 = 0; h0 < H; h0 += kFrontChunk) {
+    const int ng = min(kFrontChunk, H - h0) / 8;
+    for (int idx = tid; idx < R * ng; idx += kFrontThreads) {
+      const int r = idx / ng, gidx = idx % ng;
+      const size_t off = ((size_t)r * H + h0) / 8 + gidx;
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x) + off);
+      const uint4 rv = __ldg(reinterpret_cast<const uint4*>(residual) + off);
+      const uint4 gv = __ldg(g4 + h0 / 8 + gidx);
+      const uint4 rn = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
+                                  add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w));
+      const float rsd = s_rstd[r];
+      s_n[r][gidx] = make_uint4(norm_bf16x2(rn.x, gv.x, rsd), norm_bf16x2(rn.y, gv.y, rsd),
+                                norm_bf16x2(rn.z, gv.z, rsd), norm_bf16x2(rn.w, gv.w, rsd));
+    }
+    __syncthreads();
+    if (e < E) {
+      const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)e * H + h0);
+      for (int c = lane; c < ng; c += 32) {
+        const uint4 wv = __ldg(wrow + c);
+        const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                             bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          if (r < R) {
+            const uint4 nv = s_n[r][c];
+            float a = acc[r];
+            a += wf[0] * bf16_lo(nv.x); a += wf[1] * bf16_hi(nv.x);
+            a += wf[2] * bf16_lo(nv.y); a += wf[3] * bf16_hi(nv.y);
+            a += wf[4] * bf16_lo(nv.z); a += wf[5] * bf16_hi(nv.z);
+            a += wf[6] * bf16_lo(nv.w); a += wf[7] * bf16_hi(nv.w);
+            acc[r] = a;
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (e < E) {
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+      if (r < R) {
+        const float v = warp_sum(acc[r]);
+        if (lane == 0) rs->logits[(size_t)r * E + e] = v;
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&rs->ticket, 1u) == (uint32_t)(G - 1)) ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  topk_dedup_block(rs->logits, ids_out, wts_out, &rs->n_distinct, rs->uniq, rs->user_off,
+                   rs->user_list, &rs->status, R, E, k);
+  __syncthreads();
+  if (tid == 0) {
+    if (nd_out) *nd_out = rs->n_distinct;
+    rs->ticket = 0u;
+  }
+}
+
+// Device address of the scratch array, looked up once per device (with that device
+// current) the first time the entry point runs on it.
+static void* g_route_scratch_ptr[64];
+static int g_route_scratch_ready[64];
+
+}  // namespace mtail
+
+extern "C" int moe_tail_route_noalloc(const void* x, const void* residual, const void* gamma,
+                                      const void* router_w, int32_t rows, int32_t hidden,
+                                      int32_t n_experts, int32_t top_k, float rms_eps,
+                                      int32_t* ids, float* wts, int32_t* n_distinct,
+                                      void* stream) {
+  using namespace mtail;
+  if (!x || !residual || !gamma || !router_w || !ids || !wts) return MOE_TAIL_ERR_INVALID_ARG;
+  const void* ptrs[4] = {x, residual, gamma, router_w};
+  for (const void* p : ptrs)
+    if ((uintptr_t)p & 15u) return MOE_TAIL_ERR_INVALID_ARG;
+  if (rows < 1 || rows > kMaxRows || n_experts < 1 || n_experts > kMaxExperts || top_k < 1 ||
+      top_k > kMaxTopK || top_k > n_experts || hidden < 128 || hidden % 128 != 0 ||
+      !(rms_eps > 0.f))
+    return MOE_TAIL_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_TAIL_ERR_CUDA;
+  if (!g_route_scratch_ready[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+      return MOE_TAIL_ERR_CUDA;
+    g_route_scratch_ptr[dev] = p;
+    g_route_scratch_ready[dev] = 1;
+  }
+  RouteScratch* rs = (RouteScratch*)g_route_scratch_ptr[dev];
+  cudaStream_t st = (cudaStream_t)stream;
+  // the ticket must start at zero (a call that stopped part-way could have left it set)
+  if (cudaMemsetAsync(&rs->ticket, 0, sizeof(uint32_t), st) != cudaSuccess)
+    return MOE_TAIL_ERR_CUDA;
+  const int grid = (n_experts + kFrontWarps - 1) / kFrontWarps;
+  k_route_static<<<grid, kFrontThreads, 0, st>>>(
+      (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual, (const __nv_bfloat16*)gamma,
+      (const __nv_bfloat16*)router_w, rs, ids, wts, n_distinct, rows, hidden, n_experts, top_k,
+      rms_eps);
+  return cudaGetLastError() == cudaSuccess ? MOE_TAIL_OK : MOE_TAIL_ERR_CUDA;
+}
