@@ -256,7 +256,7 @@ def run_ours(args, rank, world, local_rank):
     gbps = total_bytes * world / (elapsed_ms * 1e-3) / 1e9
 
     # dominant kernel: the stage with the largest total time
-    names = ["front", "stream_gate_up", "stream_down", "combine"]
+    names = ["add_rmsnorm", "router_topk", "stream_gate_up", "stream_down", "combine"]
     if nst != len(names):
         names = ["stage%d" % s for s in range(nst)]
     tot = stage_ms.sum(axis=0)

@@ -71,14 +71,17 @@ enum {
    * first pipeline stage unpublished, so that the consumers' bounded wait expires; the
    * kernel records MOE_TAIL_ERR_TIMEOUT in the status word and returns.  The output of
    * such a call is not meaningful. */
-  MOE_TAIL_DEBUG_STALL_FIRST_STAGE = 4
+  MOE_TAIL_DEBUG_STALL_FIRST_STAGE = 4,
+  /* Run the front (add + RMSNorm, router, top-k, dedup) as one launch in which every CTA
+   * recomputes the row norms, instead of a norm launch followed by a router launch. */
+  MOE_TAIL_DEBUG_FUSED_FRONT = 8
 };
 
 typedef struct moe_tail moe_tail_t; /* opaque handle */
 
 typedef struct {
   int32_t max_rows;       /* 1..16: the largest `rows` any run will pass */
-  int32_t hidden;         /* H: multiple of 128 */
+  int32_t hidden;         /* H: multiple of 128, at most 32768 */
   int32_t n_experts;      /* E: 1..1024 */
   int32_t top_k;          /* k: 1..min(E, 32) */
   int32_t expert_inter;   /* I: multiple of 128 */

@@ -13,7 +13,7 @@
 // three single-purpose kernels k_add_rmsnorm / k_router / k_topk_dedup used by the
 // cross-checking path.  bf16(x + residual) goes to scratch; the residual itself is
 // rewritten by the combine, after every reader is done.
-#include "../../include/moe_tail.h"
+#include "moe_tail.h"
 #include "moe_tail_internal.cuh"
 
 namespace mtail {
@@ -59,83 +59,98 @@ __device__ __forceinline__ float group_amax(uint4 nv) {
 }
 
 // ---------------------------------------------------------------- add + RMSNorm ----
-// One CTA per row; each thread owns whole 32-element blocks.
-constexpr int kNormThreads = 256;
+// One CTA of 512 threads per row.  Thread i owns the 16-byte groups i, i + 512, ... of the
+// row (up to 8, H <= 32768) and keeps bf16(x + residual) in registers; gamma is staged in
+// shared memory before the wait on the previous launch (it depends on nothing).  Two block
+// reductions (sum of squares, then max |n|) in a fixed order; no value is re-read from
+// global memory.
+constexpr int kNormThreads = 512;
+constexpr int kNormGroups = 8;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = is_max ? warp_max(v) : warp_sum(v);
+  __syncthreads();  // part[] may still be read by the previous reduction
+  if (lane == 0) part[warp] = v;
+  __syncthreads();
+  float r = 0.f;
+  for (int i = 0; i < kNormThreads / 32; ++i) r = is_max ? fmaxf(r, part[i]) : r + part[i];
+  return r;
+}
 
 __global__ void __launch_bounds__(kNormThreads)
 k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ residual,
               const __nv_bfloat16* __restrict__ gamma, __nv_bfloat16* __restrict__ rnew,
               __nv_bfloat16* __restrict__ n_out, __half* __restrict__ n16,
               float* __restrict__ n16s, uint32_t* __restrict__ counters, int H, float eps) {
+  extern __shared__ uint4 s_gamma[];  // [H / 8]
+  __shared__ float part[kNormThreads / 32];
   const int r = blockIdx.x;
+  const int ng = H / 8;
+  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+  for (int c = threadIdx.x; c < ng; c += kNormThreads) s_gamma[c] = __ldg(g4 + c);
   pdl_wait();
   pdl_trigger();
   if (r == 0 && threadIdx.x < 8) counters[threadIdx.x] = 0u;  // work counters of this call
-  const int nblk = H / 32;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * H);
   const uint4* rr = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
-  uint4* rn = reinterpret_cast<uint4*>(rnew + (size_t)r * H);
+  uint4 rn[kNormGroups];
   float ss = 0.f;
-  for (int b = threadIdx.x; b < nblk; b += kNormThreads) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 xv = xr[b * 4 + c], rv = rr[b * 4 + c];
-      const uint4 o = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
-                                 add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w));
-      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        ss += bf16_lo(ow[q]) * bf16_lo(ow[q]) + bf16_hi(ow[q]) * bf16_hi(ow[q]);
-      rn[b * 4 + c] = o;
+  for (int q = 0; q < kNormGroups; ++q) {
+    const int c = threadIdx.x + q * kNormThreads;
+    if (c < ng) {
+      const uint4 xv = xr[c], rv = rr[c];
+      rn[q] = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y), add_bf16x2(xv.z, rv.z),
+                         add_bf16x2(xv.w, rv.w));
+    } else {
+      rn[q] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  // deterministic block reduction: butterfly in each warp, then warp partials in order
-  __shared__ float part[kNormThreads / 32];
-  __shared__ float s_rstd;
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int i = 0; i < kNormThreads / 32; ++i) t += part[i];
-    s_rstd = 1.0f / sqrtf(t / (float)H + eps);
+#pragma unroll
+  for (int q = 0; q < kNormGroups; ++q) {
+    const uint32_t o[4] = {rn[q].x, rn[q].y, rn[q].z, rn[q].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ss += bf16_lo(o[i]) * bf16_lo(o[i]) + bf16_hi(o[i]) * bf16_hi(o[i]);
   }
-  __syncthreads();
-  const float rstd = s_rstd;
-  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
-  uint4* no = reinterpret_cast<uint4*>(n_out + (size_t)r * H);
-  uint4* n16o = reinterpret_cast<uint4*>(n16 + (size_t)r * H);
+  const float rstd = 1.0f / sqrtf(block_reduce(ss, false, part) / (float)H + eps);
   float amax = 0.f;
-  for (int c = threadIdx.x; c < H / 8; c += kNormThreads) {
-    const uint4 rv = rn[c], gv = g4[c];
-    const uint4 nv = make_uint4(norm_bf16x2(rv.x, gv.x, rstd), norm_bf16x2(rv.y, gv.y, rstd),
-                                norm_bf16x2(rv.z, gv.z, rstd), norm_bf16x2(rv.w, gv.w, rstd));
-    no[c] = nv;
-    amax = fmaxf(amax, group_amax(nv));
+#pragma unroll
+  for (int q = 0; q < kNormGroups; ++q) {
+    const int c = threadIdx.x + q * kNormThreads;
+    if (c < ng) {
+      const uint4 gv = s_gamma[c];
+      const uint4 nv = make_uint4(norm_bf16x2(rn[q].x, gv.x, rstd), norm_bf16x2(rn[q].y, gv.y, rstd),
+                                  norm_bf16x2(rn[q].z, gv.z, rstd), norm_bf16x2(rn[q].w, gv.w, rstd));
+      amax = fmaxf(amax, group_amax(nv));
+    }
   }
-  __shared__ float s_amax;
-  amax = warp_max(amax);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = amax;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = 0.f;
-    for (int i = 0; i < kNormThreads / 32; ++i) m = fmaxf(m, part[i]);
-    s_amax = m;
-  }
-  __syncthreads();
   // f16 copy with one power-of-two scale per row (row maximum in [2^14, 2^15))
-  const int p = f16_block_exp(s_amax);
+  const int p = f16_block_exp(block_reduce(amax, true, part));
   const float down = __uint_as_float((uint32_t)(127 - p) << 23);
   if (threadIdx.x == 0) n16s[r] = __uint_as_float((uint32_t)(127 + p) << 23);
-  for (int c = threadIdx.x; c < H / 8; c += kNormThreads) n16o[c] = f16_group(no[c], down);
+  uint4* rno = reinterpret_cast<uint4*>(rnew + (size_t)r * H);
+  uint4* no = reinterpret_cast<uint4*>(n_out + (size_t)r * H);
+  uint4* n16o = reinterpret_cast<uint4*>(n16 + (size_t)r * H);
+#pragma unroll
+  for (int q = 0; q < kNormGroups; ++q) {
+    const int c = threadIdx.x + q * kNormThreads;
+    if (c < ng) {
+      const uint4 gv = s_gamma[c];
+      const uint4 nv = make_uint4(norm_bf16x2(rn[q].x, gv.x, rstd), norm_bf16x2(rn[q].y, gv.y, rstd),
+                                  norm_bf16x2(rn[q].z, gv.z, rstd), norm_bf16x2(rn[q].w, gv.w, rstd));
+      rno[c] = rn[q];
+      no[c] = nv;
+      n16o[c] = f16_group(nv, down);
+    }
+  }
 }
 
 cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
                                const __nv_bfloat16* residual, const Weights& w,
                                const Scratch& s, cudaStream_t st, bool pdl) {
-  return launch_k(k_add_rmsnorm, dim3(d.R), dim3(kNormThreads), 0, st, pdl, x, residual,
-                  w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps);
+  return launch_k(k_add_rmsnorm, dim3(d.R), dim3(kNormThreads), (size_t)d.H * 2, st, pdl, x,
+                  residual, w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps);
 }
 
 // ------------------------------------------------------------------- router GEMV ----
@@ -331,6 +346,116 @@ cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, 
   return launch_k(k_topk_dedup, dim3(1), dim3(kTopkThreads), 0, st, pdl,
                   (const float*)s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
                   s.user_list, s.status, d.R, d.E, d.k);
+}
+
+// --------------------------------------------------------------- router + top-k ----
+// Grid (ceil(E / 8), P): CTA (x, p) runs experts 8x .. 8x+7 (one per warp) over K part p
+// of H (P parts of at most 2048 elements).  Each warp's router weights for the part are
+// read into registers before the wait on the norm launch (they depend on nothing); the
+// rows' n for the part are loaded into shared memory with every load issued at once.  The
+// partial logits of each part go to scratch; the last CTA to finish (atomic ticket after a
+// fence) adds the parts in part order, then runs top-k and the dedup.
+constexpr int kRtWarps = 8;
+constexpr int kRtThreads = kRtWarps * 32;
+constexpr int kRtPart = 2048;                    // max K elements per part
+constexpr int kRtGroups = kRtPart / 8 / 32;      // 16-byte weight groups per lane (8)
+
+__host__ __device__ inline int router_parts(int H) { return (H + kRtPart - 1) / kRtPart; }
+// elements per part: a multiple of 128 (the last part may be shorter)
+__host__ __device__ inline int router_part_len(int H) {
+  const int P = router_parts(H);
+  return ((H + P - 1) / P + 127) / 128 * 128;
+}
+
+__global__ void __launch_bounds__(kRtThreads)
+k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, int E, int k) {
+  extern __shared__ uint4 s_n[];  // [R][kRtPart / 8] (dynamic: R * 4 KB)
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = gridDim.y, p = blockIdx.y;
+  const int plen = router_part_len(H);
+  const int k0 = p * plen;
+  const int len = min(plen, H - k0);   // elements of this part (> 0, multiple of 128)
+  const int ng = len / 8;               // 16-byte groups per row in this part
+  const int e = blockIdx.x * kRtWarps + warp;
+  const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)min(e, E - 1) * H + k0);
+  uint4 wreg[kRtGroups];
+#pragma unroll
+  for (int q = 0; q < kRtGroups; ++q) {
+    const int c = lane + 32 * q;
+    wreg[q] = (e < E && c < ng) ? __ldg(wrow + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  pdl_wait();
+  pdl_trigger();
+  // the part of n for every row, all loads in flight together
+  for (int i = tid; i < R * ng; i += kRtThreads) {
+    const int r = i / ng, c = i % ng;
+    s_n[r * (kRtPart / 8) + c] = __ldcg(reinterpret_cast<const uint4*>(s.n + (size_t)r * H + k0) + c);
+  }
+  __syncthreads();
+  float acc[kMaxRows];
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+#pragma unroll
+  for (int q = 0; q < kRtGroups; ++q) {
+    const int c = lane + 32 * q;
+    if (c < ng) {
+      const uint4 wv = wreg[q];
+      const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                           bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        if (r < R) {
+          const uint4 nv = s_n[r * (kRtPart / 8) + c];
+          float a = acc[r];
+          a += wf[0] * bf16_lo(nv.x); a += wf[1] * bf16_hi(nv.x);
+          a += wf[2] * bf16_lo(nv.y); a += wf[3] * bf16_hi(nv.y);
+          a += wf[4] * bf16_lo(nv.z); a += wf[5] * bf16_hi(nv.z);
+          a += wf[6] * bf16_lo(nv.w); a += wf[7] * bf16_hi(nv.w);
+          acc[r] = a;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) {
+    const float v = warp_sum(acc[r]);
+    if (lane == 0 && r < R && e < E) s.logit_parts[((size_t)p * R + r) * E + e] = v;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0)
+    s_last = (atomicAdd(&s.counters[kCtrFrontTicket], 1u) == gridDim.x * gridDim.y - 1) ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = tid; i < R * E; i += kRtThreads) {  // logits = parts added in part order
+    float v = __ldcg(s.logit_parts + i);
+    for (int pp = 1; pp < P; ++pp) v += __ldcg(s.logit_parts + (size_t)pp * R * E + i);
+    s.logits[i] = v;
+  }
+  __syncthreads();
+  topk_dedup_block(s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off, s.user_list,
+                   s.status, R, E, k);
+  if (tid == 0) s.counters[kCtrFrontTicket] = 0u;
+}
+
+cudaError_t launch_router_topk(const Dims& d, const Weights& w, const Scratch& s,
+                               cudaStream_t st, bool pdl) {
+  const dim3 grid((d.E + kRtWarps - 1) / kRtWarps, router_parts(d.H));
+  return launch_k(k_router_topk, grid, dim3(kRtThreads), (size_t)d.R * kRtPart * 2, st, pdl,
+                  w.w_r, s, d.R, d.H, d.E, d.k);
+}
+
+// The norm kernel stages gamma (up to 64 KB) and the router kernel a part of n (up to 64 KB)
+// in dynamic shared memory.
+cudaError_t prepare_front_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(k_add_rmsnorm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (1 << 15) * 2);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_router_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxRows * kRtPart * 2);
+  return e;
 }
 
 // ------------------------------------------------------------------- fused front ----

@@ -230,25 +230,59 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
 // ------------------------------------------------------------------------ combine ----
 // out[r, h] = bf16(sum over slots in pick order of wts * y + ys): a fixed-order fp32 sum;
 // the residual receives bf16(x + residual), now that every reader of the old value is done.
-__global__ void k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
-                          __nv_bfloat16* __restrict__ residual) {
+// One thread per 8 consecutive outputs of a row; the slots' loads are unrolled so that they
+// are in flight together.
+__global__ void __launch_bounds__(256)
+k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
+          __nv_bfloat16* __restrict__ residual) {
   pdl_wait();
   pdl_trigger();
   const int H = dm.H, k = dm.k;
+  const int ng = H / 8;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= dm.R * H) return;
-  const int r = idx / H, h = idx % H;
-  float acc = 0.f;
-  for (int i = 0; i < k; ++i)
-    acc += s.wts[r * k + i] * s.y[(size_t)(r * k + i) * H + h];
-  acc += s.ys[(size_t)r * H + h];
-  out[idx] = __float2bfloat16_rn(acc);
-  residual[idx] = s.rnew[idx];
+  if (idx >= dm.R * ng) return;
+  const int r = idx / ng, c = idx % ng;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int i0 = 0; i0 < k; i0 += 8) {
+    float4 ya[8], yb[8];
+    float wv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j;
+      if (i < k) {
+        const float4* yp = reinterpret_cast<const float4*>(s.y + (size_t)(r * k + i) * H) + 2 * c;
+        ya[j] = __ldcg(yp);
+        yb[j] = __ldcg(yp + 1);
+        wv[j] = s.wts[r * k + i];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (i0 + j < k) {
+        acc[0] += wv[j] * ya[j].x; acc[1] += wv[j] * ya[j].y;
+        acc[2] += wv[j] * ya[j].z; acc[3] += wv[j] * ya[j].w;
+        acc[4] += wv[j] * yb[j].x; acc[5] += wv[j] * yb[j].y;
+        acc[6] += wv[j] * yb[j].z; acc[7] += wv[j] * yb[j].w;
+      }
+    }
+  }
+  const float4* ysp = reinterpret_cast<const float4*>(s.ys + (size_t)r * H) + 2 * c;
+  const float4 s0 = __ldcg(ysp), s1 = __ldcg(ysp + 1);
+  acc[0] += s0.x; acc[1] += s0.y; acc[2] += s0.z; acc[3] += s0.w;
+  acc[4] += s1.x; acc[5] += s1.y; acc[6] += s1.z; acc[7] += s1.w;
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q])) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q + 1])) << 16);
+  reinterpret_cast<uint4*>(out + (size_t)r * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  reinterpret_cast<uint4*>(residual + (size_t)r * H)[c] =
+      __ldcg(reinterpret_cast<const uint4*>(s.rnew + (size_t)r * H) + c);
 }
 
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl) {
-  const int n = d.R * d.H;
+  const int n = d.R * d.H / 8;
   return launch_k(k_combine, dim3((n + 255) / 256), dim3(256), 0, st, pdl, d, s, out,
                   residual);
 }

@@ -36,7 +36,7 @@ namespace mtail {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 8;
+constexpr int kStages = 10;
 constexpr int kKChunk = 256;             // K elements per stage
 constexpr int kStageW = 8192;            // weight bytes per stage
 constexpr int kActStride = 576;          // bytes per user row per stage (512 + 64 pad)
@@ -44,7 +44,7 @@ constexpr int kStageA = kMaxRows * kActStride;
 constexpr int kStageWS = 512;            // weight scales: 64 rows x 8 blocks
 constexpr int kStageAS = kMaxRows * 32;  // activation scales: 16 users x 8 floats
 constexpr int kStageBytes = kStageW + kStageA + kStageWS + kStageAS;
-constexpr int kRedBytes = 2 * kConsumerWarps * 4 * 2 * 512;  // 2 x [warp][tile][nt][lane] float4
+constexpr int kRedBytes = 2 * kConsumerWarps * 2 * 512;  // 2 x [warp][nt][lane] float4
 constexpr int kTableBytes = (3 * kMaxPicks + 1 + kMaxRows) * 4;
 constexpr int kXmaxBytes = 2 * 4 * kMaxRows * 4;
 constexpr int kStreamSmem = kStages * kStageBytes + kRedBytes + 256 + kTableBytes + kXmaxBytes;
@@ -241,71 +241,100 @@ __device__ __forceinline__ uint32_t swz64(uint32_t base, int r, int c) {
 // 64-byte swizzle (chunk index XOR bits 1..2 of the row; box base 512-byte aligned).
 __device__ __forceinline__ int swz64_off(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
 
-// One stage of a routed MXFP4 item, K-slot cw (32 elements = one scale block) of the
-// stage, all 4 MMA tiles.  GATE_UP: tile m = gate rows 8m..8m+7 (A rows 0-7) and the up rows
-// of the same j (A rows 8-15), weight scales rows [0, 32) gate, [32, 64) up; else tile m =
-// down rows 16m..16m+15.  The activation scale is per row (gate/up, applied later) or per
-// block (down, here).
-template <bool GATE_UP>
-__device__ __forceinline__ void stage_routed(const uint8_t* st, int cw, int g, int t, int NT,
-                                             float (&acc)[4][2][4]) {
-  const uint8_t* sw = st;
-  const uint8_t* sa = st + kStageW;
-  const uint8_t* sws = sa + kStageA;
-  const float* sas = reinterpret_cast<const float*>(sws + kStageWS);
-  uint4 b[2];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-    if (nt < NT)
-      b[nt] = *reinterpret_cast<const uint4*>(sa + (nt * 8 + g) * kActStride + cw * 64 + t * 16);
-  float as[2][2];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-      as[nt][q] = GATE_UP ? 1.0f : ((nt < NT) ? sas[(nt * 8 + 2 * t + q) * 8 + cw] : 0.f);
-  const int bx = cw >> 2, ch = cw & 3;
-  uint32_t wa[4], wb[4];
-  float sa_[4], sb_[4];
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    int ra, rb, sra, srb;
-    const uint8_t *boxa, *boxb;
-    if (GATE_UP) {
-      ra = 8 * m + g; rb = ra;
-      boxa = sw + bx * 2048; boxb = sw + 4096 + bx * 2048;
-      sra = ra; srb = 32 + rb;
-    } else {
-      ra = 16 * m + g; rb = ra + 8;
-      boxa = sw + bx * 4096; boxb = boxa;
-      sra = ra; srb = rb;
-    }
-    wa[m] = *reinterpret_cast<const uint32_t*>(boxa + swz64_off(ra, ch) + 4 * t);
-    wb[m] = *reinterpret_cast<const uint32_t*>(boxb + swz64_off(rb, ch) + 4 * t);
-    sa_[m] = e8m0_to_float(sws[sra * 8 + cw]);
-    sb_[m] = e8m0_to_float(sws[srb * 8 + cw]);
+// d = A * B for one m16n8k16 f16 product (no accumulator input).
+__device__ __forceinline__ void mma_f16_z(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// E8M0 byte i of a little-endian word of four scales -> float 2^(s-127); the byte 0
+// (2^-127) flushes to 0.
+__device__ __forceinline__ float e8m0_byte(uint32_t w, int i) {
+  return __uint_as_float((i < 3 ? (w << (23 - 8 * i)) : (w >> 1)) & 0x7F800000u);
+}
+
+// Per-lane shared-memory offsets of a routed item, fixed for the whole item: warp cw works
+// on MMA tile m = cw & 3 and on the 4 scale blocks [4h, 4h + 4) of every stage, h = cw >> 2.
+struct RoutedLane {
+  int code_a[4], code_b[4];  // word t of block chunk c, A rows g and g + 8
+  int scale_a, scale_b;      // the 4 E8M0 bytes of those rows for blocks 4h..4h+3
+  int act;                   // user g's 16 bytes of block 4h (N-tile 0); +64 per block
+  int ascale;                // down: user 2t's scales of blocks 4h..4h+3 (N-tile 0)
+};
+
+__device__ __forceinline__ RoutedLane routed_lane(bool gate_up, int cw, int g, int t) {
+  RoutedLane L;
+  const int m = cw & 3, h = cw >> 2;
+  int ra, rb, boxa, boxb, sra, srb;
+  if (gate_up) {  // gate box rows 8m+g (A rows 0-7), up box rows 8m+g (A rows 8-15)
+    ra = 8 * m + g; rb = ra;
+    boxa = h * 2048; boxb = 4096 + h * 2048;
+    sra = ra; srb = 32 + rb;
+  } else {        // down box rows 16m+g and 16m+g+8
+    ra = 16 * m + g; rb = ra + 8;
+    boxa = h * 4096; boxb = boxa;
+    sra = ra; srb = rb;
   }
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    uint32_t ha[4], hb[4];
-    e2m1x8_to_f16x2(wa[m], ha[0], ha[1], ha[2], ha[3]);
-    e2m1x8_to_f16x2(wb[m], hb[0], hb[1], hb[2], hb[3]);
+  for (int c = 0; c < 4; ++c) {
+    L.code_a[c] = boxa + swz64_off(ra, c) + 4 * t;
+    L.code_b[c] = boxb + swz64_off(rb, c) + 4 * t;
+  }
+  L.scale_a = kStageW + kStageA + sra * 8 + 4 * h;
+  L.scale_b = kStageW + kStageA + srb * 8 + 4 * h;
+  L.act = kStageW + g * kActStride + (4 * h) * 64 + t * 16;
+  L.ascale = kStageW + kStageA + kStageWS + (2 * t) * 32 + 16 * h;
+  return L;
+}
+
+// One stage of a routed MXFP4 item: 4 scale blocks x 1 tile per warp.  Each block's two
+// k16 products are scaled by the row's E8M0 scale (and, for down, the user's block scale)
+// and added to the fp32 accumulators.
+template <bool GATE_UP>
+__device__ __forceinline__ void stage_routed(const uint8_t* st, const RoutedLane& L, int NT,
+                                             float (&acc)[2][4]) {
+  const uint32_t swa = *reinterpret_cast<const uint32_t*>(st + L.scale_a);
+  const uint32_t swb = *reinterpret_cast<const uint32_t*>(st + L.scale_b);
+  float4 as0[2], as1[2];  // down: scales of users (2t, 2t+1) for the 4 blocks, per N-tile
+  if (!GATE_UP) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       if (nt < NT) {
-        float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f16(tmp, ha[0], hb[0], ha[1], hb[1], b[nt].x, b[nt].y);
-        mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b[nt].z, b[nt].w);
+        as0[nt] = *reinterpret_cast<const float4*>(st + L.ascale + nt * 8 * 32);
+        as1[nt] = *reinterpret_cast<const float4*>(st + L.ascale + nt * 8 * 32 + 32);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t wa = *reinterpret_cast<const uint32_t*>(st + L.code_a[c]);
+    const uint32_t wb = *reinterpret_cast<const uint32_t*>(st + L.code_b[c]);
+    uint32_t ha[4], hb[4];
+    e2m1x8_to_f16x2(wa, ha[0], ha[1], ha[2], ha[3]);
+    e2m1x8_to_f16x2(wb, hb[0], hb[1], hb[2], hb[3]);
+    const float sa = e8m0_byte(swa, c), sb = e8m0_byte(swb, c);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      if (nt < NT) {
+        const uint4 b = *reinterpret_cast<const uint4*>(st + L.act + nt * 8 * kActStride + c * 64);
+        float tmp[4];
+        mma_f16_z(tmp, ha[0], hb[0], ha[1], hb[1], b.x, b.y);
+        mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b.z, b.w);
         if (GATE_UP) {
-          acc[m][nt][0] += tmp[0] * sa_[m];
-          acc[m][nt][1] += tmp[1] * sa_[m];
-          acc[m][nt][2] += tmp[2] * sb_[m];
-          acc[m][nt][3] += tmp[3] * sb_[m];
+          acc[nt][0] += tmp[0] * sa;
+          acc[nt][1] += tmp[1] * sa;
+          acc[nt][2] += tmp[2] * sb;
+          acc[nt][3] += tmp[3] * sb;
         } else {
-          acc[m][nt][0] += tmp[0] * (sa_[m] * as[nt][0]);
-          acc[m][nt][1] += tmp[1] * (sa_[m] * as[nt][1]);
-          acc[m][nt][2] += tmp[2] * (sb_[m] * as[nt][0]);
-          acc[m][nt][3] += tmp[3] * (sb_[m] * as[nt][1]);
+          const float u0 = (c == 0) ? as0[nt].x : (c == 1) ? as0[nt].y : (c == 2) ? as0[nt].z : as0[nt].w;
+          const float u1 = (c == 0) ? as1[nt].x : (c == 1) ? as1[nt].y : (c == 2) ? as1[nt].z : as1[nt].w;
+          acc[nt][0] += tmp[0] * (sa * u0);
+          acc[nt][1] += tmp[1] * (sa * u1);
+          acc[nt][2] += tmp[2] * (sb * u0);
+          acc[nt][3] += tmp[3] * (sb * u1);
         }
       }
     }
@@ -315,7 +344,7 @@ __device__ __forceinline__ void stage_routed(const uint8_t* st, int cw, int g, i
 // One stage of a shared-expert (bf16) item: K-slot cw is one 32-element box per half,
 // one 16-row tile (gate/up: 8 gate rows + the 8 up rows of the same j; down: 16 rows).
 __device__ __forceinline__ void stage_shared(const uint8_t* st, int cw, int g, int t, int NT,
-                                             bool gate_up, float (&acc)[4][2][4]) {
+                                             bool gate_up, float (&acc)[2][4]) {
   const uint8_t* box = st + cw * 1024;
   const uint8_t* sa = st + kStageW;
   const uint4 a = *reinterpret_cast<const uint4*>(box + swz64_off(g, t));
@@ -325,8 +354,8 @@ __device__ __forceinline__ void stage_shared(const uint8_t* st, int cw, int g, i
   for (int nt = 0; nt < 2; ++nt) {
     if (nt < NT) {
       const uint4 b = *reinterpret_cast<const uint4*>(sa + (nt * 8 + g) * kActStride + cw * 64 + t * 16);
-      mma_bf16(acc[0][nt], a.x, c.x, a.y, c.y, b.x, b.y);
-      mma_bf16(acc[0][nt], a.z, c.z, a.w, c.w, b.z, b.w);
+      mma_bf16(acc[nt], a.x, c.x, a.y, c.y, b.x, b.y);
+      mma_bf16(acc[nt], a.z, c.z, a.w, c.w, b.z, b.w);
     }
   }
 }
@@ -539,7 +568,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   }
 
   // ------------------------------------------------------------------ consumers ----
-  const int cw = warp - 1;  // K-slot of every stage this warp owns, and its epilogue share
+  const int cw = warp - 1;
   const int g = lane >> 2, t = lane & 3;
   int stage = 0;
   uint32_t phase = 0;
@@ -547,7 +576,8 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   Item it;
   it.kind = 0; it.nst = 0; it.U = 0; it.K = 0; it.out0 = 0; it.u0 = 0; it.row0 = 0; it.row1 = 0;
   it.e = 0; it.d = 0;
-  float acc[4][2][4];
+  RoutedLane L = routed_lane(PHASE == 0, cw, g, t);
+  float acc[2][4];
   for (;;) {
     if (!mbar_wait(&full[stage], phase, budget_ns)) {
       if (lane == 0) set_status(s.status, kStatusTimeout);
@@ -559,21 +589,20 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
       cur = item;
       it = decode_item(PHASE, item, dm, tb, D);
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[m][nt][q] = 0.f;
+        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
     }
     const uint8_t* st = stages + stage * kStageBytes;
     const int NT = it.U > 8 ? 2 : 1;
-    if (kc * kKChunk + 32 * cw < it.K) {
-      if (it.kind == kRoutedGU)
-        stage_routed<true>(st, cw, g, t, NT, acc);
-      else if (it.kind == kRoutedDN)
-        stage_routed<false>(st, cw, g, t, NT, acc);
-      else
-        stage_shared(st, cw, g, t, NT, it.kind == kSharedGU, acc);
+    if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
+      // this warp's 4 blocks start at K offset 128 * (cw >> 2) of the stage
+      if (kc * kKChunk + 128 * (cw >> 2) < it.K) {
+        if (PHASE == 0) stage_routed<true>(st, L, NT, acc);
+        else stage_routed<false>(st, L, NT, acc);
+      }
+    } else if (kc * kKChunk + 32 * cw < it.K) {
+      stage_shared(st, cw, g, t, NT, it.kind == kSharedGU, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
@@ -581,29 +610,33 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
 
     if (kc == it.nst - 1) {
       // ------------------------------------------------------ item epilogue ----
-      // partial sums of the 8 warps go to one of two reduction buffers (alternating by
-      // item, so no barrier is needed before the next item writes); warp cw then adds the
-      // 8 partials of tile (cw & 3), N-tile (cw >> 2) in warp order and stores them.
+      // partial sums go to one of two reduction buffers (alternating by item, so the next
+      // item's writes need no barrier).  Routed: tile m is the sum of warps m and m + 4
+      // (blocks 0-3 then 4-7 of every stage), finished by warp m + 4 * nt.  Shared: the
+      // single tile is the sum of the 8 warps in warp order, finished by warp 4 * nt.
       const int buf = nitems & 1;
       ++nitems;
-      float4* rb = red + buf * (kConsumerWarps * 4 * 2 * 32);
-      const int ntiles = (it.kind == kRoutedGU || it.kind == kRoutedDN) ? 4 : 1;
+      float4* rb = red + buf * (kConsumerWarps * 2 * 32);
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-          if (m < ntiles && nt < NT)
-            rb[((cw * 4 + m) * 2 + nt) * 32 + lane] =
-                make_float4(acc[m][nt][0], acc[m][nt][1], acc[m][nt][2], acc[m][nt][3]);
+      for (int nt = 0; nt < 2; ++nt)
+        if (nt < NT)
+          rb[(cw * 2 + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
       named_bar_sync(1, kConsumerWarps * 32);
+      const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
       const int em = cw & 3, ent = cw >> 2;
-      const bool active = em < ntiles && ent < NT;
+      const bool active = routed ? (ent < NT) : (em == 0 && ent < NT);
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       if (active) {
+        if (routed) {
+          const float4 v0 = rb[(em * 2 + ent) * 32 + lane];
+          const float4 v1 = rb[((em + 4) * 2 + ent) * 32 + lane];
+          c[0] = v0.x + v1.x; c[1] = v0.y + v1.y; c[2] = v0.z + v1.z; c[3] = v0.w + v1.w;
+        } else {
 #pragma unroll
-        for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
-          const float4 v = rb[((w2 * 4 + em) * 2 + ent) * 32 + lane];
-          c[0] += v.x; c[1] += v.y; c[2] += v.z; c[3] += v.w;
+          for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+            const float4 v = rb[(w2 * 2 + ent) * 32 + lane];
+            c[0] += v.x; c[1] += v.y; c[2] += v.z; c[3] += v.w;
+          }
         }
       }
       if (it.kind == kSharedGU) {

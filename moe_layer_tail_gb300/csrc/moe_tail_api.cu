@@ -10,7 +10,7 @@
 
 #include <new>
 
-#include "../../include/moe_tail.h"
+#include "moe_tail.h"
 #include "moe_tail_internal.cuh"
 
 using namespace mtail;
@@ -60,7 +60,7 @@ static_assert(MOE_TAIL_DEBUG_STALL_FIRST_STAGE == (int)kDebugStallFirstStage,
 static int check_config(const moe_tail_config_t* c) {
   if (c->max_rows < 1 || c->max_rows > kMaxRows) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->hidden < 128 || c->hidden % 128) return MOE_TAIL_ERR_UNSUPPORTED;
-  if (c->hidden > (1 << 16)) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->hidden > (1 << 15)) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->n_experts < 1 || c->n_experts > kMaxExperts) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->top_k < 1 || c->top_k > kMaxTopK || c->top_k > c->n_experts)
     return MOE_TAIL_ERR_UNSUPPORTED;
@@ -89,6 +89,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
   s->n16 = (__half*)take(R * H * 2);
   s->n16s = (float*)take(R * 4);
   s->logits = (float*)take(R * E * 4);
+  s->logit_parts = (float*)take(((H + 2047) / 2048) * R * E * 4);
   s->ids = (int32_t*)take(P * 4);
   s->wts = (float*)take(P * 4);
   s->n_distinct = (int32_t*)take(4);
@@ -141,6 +142,7 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   }
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = prepare_stream_kernels();
+  if (e == cudaSuccess) e = prepare_front_kernels();
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e != cudaSuccess) { delete h; return cuda_fail(e); }
   h->slab_bytes = carve(cfg, nullptr, &h->s);
@@ -176,7 +178,8 @@ extern "C" int moe_tail_set_stage_events(moe_tail_t* h, void* const* events, int
 extern "C" int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows) {
   (void)rows;
   if (!h) return 0;
-  return (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) ? 8 : 4;
+  if (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) return 8;
+  return (h->cfg.debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT) ? 4 : 5;
 }
 
 extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* out,
@@ -215,8 +218,14 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
     MT_STAGE(launch_topk_dedup(d, h->s, st, pdl));
     MT_STAGE(launch_experts_simple(d, h->w, h->s, h->num_sms, st));
   } else {
-    MT_STAGE(launch_front_fused(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
-                                h->w, h->s, st, pdl));
+    if (h->cfg.debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT) {
+      MT_STAGE(launch_front_fused(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
+                                  h->w, h->s, st, pdl));
+    } else {
+      MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
+                                  h->w, h->s, st, pdl));
+      MT_STAGE(launch_router_topk(d, h->w, h->s, st, pdl));
+    }
     const uint64_t budget_ns =
         (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
     const uint32_t dbg = h->cfg.debug_flags;

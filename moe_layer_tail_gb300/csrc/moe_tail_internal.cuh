@@ -50,6 +50,7 @@ struct Scratch {
   __half* n16;           // [Rmax, H] n as f16, scaled by 2^-p per row
   float* n16s;           // [Rmax] the 2^p of each row
   float* logits;         // [Rmax, E]
+  float* logit_parts;    // [ceil(H / 2048), Rmax, E] router partial sums over K parts
   int32_t* ids;          // [Rmax, k] picks in pick order
   float* wts;            // [Rmax, k]
   int32_t* n_distinct;   // [1]
@@ -152,6 +153,8 @@ cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
 cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cudaStream_t st,
                           bool pdl);
 cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, bool pdl);
+cudaError_t launch_router_topk(const Dims& d, const Weights& w, const Scratch& s,
+                               cudaStream_t st, bool pdl);
 cudaError_t launch_front_fused(const Dims& d, const __nv_bfloat16* x,
                                const __nv_bfloat16* residual, const Weights& w, const Scratch& s,
                                cudaStream_t st, bool pdl);
@@ -159,6 +162,7 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
                                   int num_sms, cudaStream_t st);
 int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w);
 cudaError_t prepare_stream_kernels();
+cudaError_t prepare_front_kernels();
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
                           const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                           bool pdl, uint32_t debug);

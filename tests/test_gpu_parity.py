@@ -56,7 +56,7 @@ def workload_inputs(name):
 def test_workload_parity_full_size(name):
     wl, d, dev, orc = workload_inputs(name)
     tail = MoeTail(wl.shape, dev, max_rows=wl.shape.R)
-    assert tail.launches_per_run(wl.shape.R) == 4
+    assert tail.launches_per_run(wl.shape.R) == 5
     out, res, ids, wts, nd = run_gpu(tail, d)
     figs = check_parity(out, res, ids, orc, wl.shape.k)
     assert nd == len(np.unique(orc["ids"]))
@@ -85,6 +85,7 @@ def _small(seed, R=3, H=384, E=12, k=3, I=256, Is=192, kind="plain"):
 SIMPLE = 1  # debug flag: warp-per-row CUDA-core expert kernels instead of the streaming ones
 NO_PDL = 2  # debug flag: plain stream-ordered launches (no programmatic dependent launch)
 STALL = 4   # debug flag: one producer leaves a stage unpublished (failure injection)
+FUSED_FRONT = 8  # debug flag: the single-launch front
 STATUS_TIMEOUT = 4  # device status bit: a bounded wait expired
 
 
@@ -98,7 +99,7 @@ def _check_small(shape, d, max_rows=None, rows=None, flags=0):
     return tail, dev, orc, (out, res, ids, wts, nd)
 
 
-@pytest.mark.parametrize("flags", [0, SIMPLE, NO_PDL])
+@pytest.mark.parametrize("flags", [0, SIMPLE, NO_PDL, FUSED_FRONT])
 @pytest.mark.parametrize("R,H,E,k,I,Is", [
     (1, 128, 1, 1, 128, 64),       # a single expert, smallest shapes
     (2, 384, 12, 3, 256, 192),     # several tiles, ragged tails
