@@ -1,12 +1,13 @@
 // k_stream.cu -- the weight-streaming expert kernels: every distinct routed expert and the
 // shared expert stream their weights from HBM exactly once per call.
 //
-// Work: the gate/up launch (PHASE 0) runs the shared expert's gate/up tiles and, for each
-// distinct routed expert d and each group of 32 intermediate columns, the 32 gate + 32 up
-// MXFP4 rows against every row that picked d.  The down launch (PHASE 1) runs the shared
-// down tiles and, for each distinct expert and 64 hidden outputs, the 64 MXFP4 w2 rows
-// against each pick's SiLU*up vector.  A row's result never depends on which other rows
-// share its expert: each output column of the contraction belongs to one user.
+// Work: the gate/up launch (PHASE 0) runs, for each group of 32 intermediate columns j,
+// the 32 gate + 32 up weight rows of the shared expert (bf16) and of every distinct routed
+// expert d (MXFP4) against every row that uses them.  The down launch (PHASE 1) runs, for
+// each group of 64 hidden outputs, the 64 w2 rows of the shared expert and of every
+// distinct routed expert against each user's SiLU*up vector.  A row's result never depends
+// on which other rows share its expert: each output column of the contraction belongs to
+// one user, and every sum runs in the same order whoever else is present.
 //
 // Sources: "[AMD] integrate kimi k3 monokernel" page, Kernel Replacement rows "The routed
 // experts" and "The shared expert gate_up / SiLU and mul / down"; "glm53: Long-context
@@ -16,18 +17,22 @@
 //
 // Machine mapping (sm_103a):
 //   * one CTA per SM, one producer warp + 8 consumer warps, items taken from a global
-//     atomic counter (dynamic balance across the 152 SMs);
-//   * the producer streams 8 KB weight tiles with 2D TMA loads (64-byte swizzle) and the
-//     users' activation slices with 1D bulk copies into an 8-stage shared-memory ring
-//     guarded by mbarriers (transaction counts), and copies the E8M0 / activation scales
-//     with cp.async that arrive on the same mbarriers;
-//   * consumer warp w owns 32 K-elements of every stage: it decodes MXFP4 pairs with
-//     cvt.rn.f16x2.e2m1x2 straight into mma.m16n8k16 A fragments (weights = M rows, users =
-//     N columns), applies the per-block weight x activation scale to each block's fp32
-//     product, and accumulates in fp32; the 8 warps' partial sums are added in warp order.
+//     atomic counter (shared-expert items first, they are the largest);
+//   * every pipeline stage holds one 64-row x 128-byte weight tile (256 MXFP4 or 64 bf16
+//     elements per row), written by one or two 2D TMA loads with the 128-byte swizzle --
+//     few, large TMA operations, since each one occupies the SM's TMA unit for a while;
+//     the users' activation slices come with 1D bulk copies (routed) or one 2D box of all
+//     rows (shared); the E8M0 and activation scales come with cp.async, all arriving on the
+//     stage's mbarrier (transaction bytes + arrivals); 10 stages in flight per SM;
+//   * consumer warp w works on MMA tile m = w & 3 (16 weight rows) and half h = w >> 2 of
+//     every stage's K range: MXFP4 bytes go through cvt.rn.f16x2.e2m1x2 straight into
+//     mma.m16n8k16 A fragments (weights = M rows, users = N columns), each 32-element
+//     block's product is scaled by its E8M0 scale (times the activation block scale for
+//     down) and accumulated in fp32; the shared expert is bf16 x bf16 into fp32;
+//   * at the end of an item, tile m = (half 0) + (half 1), stored by one warp;
 //   * activations enter the routed contractions as f16 with power-of-two scales (one per row
 //     for gate/up, applied in the epilogue; one per 32-element block for down, applied per
-//     block), exact for bf16 values in range; the shared expert runs bf16 x bf16.
+//     block), exact for bf16 values in range;
 //   * every mbarrier wait is bounded by a %globaltimer budget; on expiry the kernel sets
 //     the status word and leaves.
 #include "moe_tail_internal.cuh"
@@ -37,9 +42,10 @@ namespace mtail {
 constexpr int kConsumerWarps = 8;
 constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 10;
-constexpr int kKChunk = 256;             // K elements per stage
-constexpr int kStageW = 8192;            // weight bytes per stage
-constexpr int kActStride = 576;          // bytes per user row per stage (512 + 64 pad)
+constexpr int kChunkF4 = 256;            // MXFP4 elements per stage row (128 bytes)
+constexpr int kChunkBF = 64;             // bf16 elements per stage row (128 bytes)
+constexpr int kStageW = 8192;            // 64 weight rows x 128 bytes
+constexpr int kActStride = 576;          // routed: bytes per user (512 + 64 pad)
 constexpr int kStageA = kMaxRows * kActStride;
 constexpr int kStageWS = 512;            // weight scales: 64 rows x 8 blocks
 constexpr int kStageAS = kMaxRows * 32;  // activation scales: 16 users x 8 floats
@@ -56,9 +62,9 @@ enum : int { kSharedGU = 0, kRoutedGU = 1, kSharedDN = 2, kRoutedDN = 3 };
 struct Item {
   int kind;
   int e, d;
-  int row0, row1;  // tensor-map rows: gate/single half, up half
+  int row0, row1;  // tensor-map rows: gate (or single) box, up box
   int out0;        // first output index (j for gate/up, h for down)
-  int K, nst;
+  int K, nst, chunk;
   int U, u0;
 };
 
@@ -80,52 +86,53 @@ __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
   it.d = 0;
   it.e = 0;
   it.u0 = 0;
+  it.row1 = 0;
   if (phase == 0) {
-    const int ns = dm.Is / 8;
+    const int ns = dm.Is / 32;
     it.K = dm.H;
     if (item < ns) {
       it.kind = kSharedGU;
-      it.out0 = item * 8;
+      it.out0 = item * 32;
       it.row0 = it.out0;
       it.row1 = dm.Is + it.out0;
       it.U = dm.R;
+      it.chunk = kChunkBF;
     } else {
       const int q = item - ns, per = dm.I / 32;
       it.kind = kRoutedGU;
       it.d = min(q / per, D - 1);
-      const int jg = q % per;
       it.e = s.uniq[it.d];
-      it.out0 = jg * 32;
+      it.out0 = (q % per) * 32;
       it.row0 = it.e * 2 * dm.I + it.out0;
       it.row1 = it.row0 + dm.I;
       it.u0 = s.off[it.d];
       it.U = s.off[it.d + 1] - it.u0;
+      it.chunk = kChunkF4;
     }
   } else {
-    const int ns = dm.H / 16;
+    const int ns = dm.H / 64;
     if (item < ns) {
       it.kind = kSharedDN;
       it.K = dm.Is;
-      it.out0 = item * 16;
+      it.out0 = item * 64;
       it.row0 = it.out0;
-      it.row1 = 0;
       it.U = dm.R;
+      it.chunk = kChunkBF;
     } else {
       const int q = item - ns, per = dm.H / 64;
       it.kind = kRoutedDN;
       it.K = dm.I;
       it.d = min(q / per, D - 1);
-      const int hg = q % per;
       it.e = s.uniq[it.d];
-      it.out0 = hg * 64;
+      it.out0 = (q % per) * 64;
       it.row0 = it.e * dm.H + it.out0;
-      it.row1 = 0;
       it.u0 = s.off[it.d];
       it.U = s.off[it.d + 1] - it.u0;
+      it.chunk = kChunkF4;
     }
   }
   it.U = max(0, min(it.U, kMaxRows));
-  it.nst = (it.K + kKChunk - 1) / kKChunk;
+  it.nst = (it.K + it.chunk - 1) / it.chunk;
   return it;
 }
 
@@ -237,9 +244,9 @@ __device__ __forceinline__ uint32_t swz64(uint32_t base, int r, int c) {
   return base + (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
 }
 
-// Byte offset of 16-byte chunk c of row r in a box of 64-byte rows written by TMA with the
-// 64-byte swizzle (chunk index XOR bits 1..2 of the row; box base 512-byte aligned).
-__device__ __forceinline__ int swz64_off(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
+// Byte offset of 16-byte chunk c of row r in a box of 128-byte rows written by TMA with the
+// 128-byte swizzle (chunk index XOR the row's low 3 bits; box base 1024-byte aligned).
+__device__ __forceinline__ int swz128_off(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
 // d = A * B for one m16n8k16 f16 product (no accumulator input).
 __device__ __forceinline__ void mma_f16_z(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
@@ -256,37 +263,43 @@ __device__ __forceinline__ float e8m0_byte(uint32_t w, int i) {
   return __uint_as_float((i < 3 ? (w << (23 - 8 * i)) : (w >> 1)) & 0x7F800000u);
 }
 
-// Per-lane shared-memory offsets of a routed item, fixed for the whole item: warp cw works
-// on MMA tile m = cw & 3 and on the 4 scale blocks [4h, 4h + 4) of every stage, h = cw >> 2.
-struct RoutedLane {
-  int code_a[4], code_b[4];  // word t of block chunk c, A rows g and g + 8
-  int scale_a, scale_b;      // the 4 E8M0 bytes of those rows for blocks 4h..4h+3
-  int act;                   // user g's 16 bytes of block 4h (N-tile 0); +64 per block
-  int ascale;                // down: user 2t's scales of blocks 4h..4h+3 (N-tile 0)
+// Per-lane shared-memory offsets (within a stage), fixed for the kernel: warp cw works on
+// MMA tile m = cw & 3 and on half h = cw >> 2 of every stage's K range.
+struct Lane {
+  // routed (MXFP4): word t of block chunk 4h + c, A rows g and g + 8; the 4 E8M0 bytes of
+  // those rows for blocks 4h..4h+3; user g's 16 bytes of block 4h; down: user 2t's scales
+  int code_a[4], code_b[4];
+  int scale_a, scale_b;
+  int act, ascale;
+  // shared (bf16): chunk 2t + h of A rows g and g + 8; user g's matching 16 bytes
+  int bw_a, bw_b, bact;
 };
 
-__device__ __forceinline__ RoutedLane routed_lane(bool gate_up, int cw, int g, int t) {
-  RoutedLane L;
+__device__ __forceinline__ Lane make_lane(bool gate_up, int cw, int g, int t) {
+  Lane L;
   const int m = cw & 3, h = cw >> 2;
   int ra, rb, boxa, boxb, sra, srb;
   if (gate_up) {  // gate box rows 8m+g (A rows 0-7), up box rows 8m+g (A rows 8-15)
     ra = 8 * m + g; rb = ra;
-    boxa = h * 2048; boxb = 4096 + h * 2048;
+    boxa = 0; boxb = 4096;
     sra = ra; srb = 32 + rb;
-  } else {        // down box rows 16m+g and 16m+g+8
+  } else {        // one 64-row box: rows 16m+g and 16m+g+8
     ra = 16 * m + g; rb = ra + 8;
-    boxa = h * 4096; boxb = boxa;
+    boxa = 0; boxb = 0;
     sra = ra; srb = rb;
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    L.code_a[c] = boxa + swz64_off(ra, c) + 4 * t;
-    L.code_b[c] = boxb + swz64_off(rb, c) + 4 * t;
+    L.code_a[c] = boxa + swz128_off(ra, 4 * h + c) + 4 * t;
+    L.code_b[c] = boxb + swz128_off(rb, 4 * h + c) + 4 * t;
   }
   L.scale_a = kStageW + kStageA + sra * 8 + 4 * h;
   L.scale_b = kStageW + kStageA + srb * 8 + 4 * h;
   L.act = kStageW + g * kActStride + (4 * h) * 64 + t * 16;
   L.ascale = kStageW + kStageA + kStageWS + (2 * t) * 32 + 16 * h;
+  L.bw_a = boxa + swz128_off(ra, 2 * t + h);
+  L.bw_b = boxb + swz128_off(rb, 2 * t + h);
+  L.bact = kStageW + swz128_off(g, 2 * t + h);
   return L;
 }
 
@@ -294,7 +307,7 @@ __device__ __forceinline__ RoutedLane routed_lane(bool gate_up, int cw, int g, i
 // k16 products are scaled by the row's E8M0 scale (and, for down, the user's block scale)
 // and added to the fp32 accumulators.
 template <bool GATE_UP>
-__device__ __forceinline__ void stage_routed(const uint8_t* st, const RoutedLane& L, int NT,
+__device__ __forceinline__ void stage_routed(const uint8_t* st, const Lane& L, int NT,
                                              float (&acc)[2][4]) {
   const uint32_t swa = *reinterpret_cast<const uint32_t*>(st + L.scale_a);
   const uint32_t swb = *reinterpret_cast<const uint32_t*>(st + L.scale_b);
@@ -341,19 +354,18 @@ __device__ __forceinline__ void stage_routed(const uint8_t* st, const RoutedLane
   }
 }
 
-// One stage of a shared-expert (bf16) item: K-slot cw is one 32-element box per half,
-// one 16-row tile (gate/up: 8 gate rows + the 8 up rows of the same j; down: 16 rows).
-__device__ __forceinline__ void stage_shared(const uint8_t* st, int cw, int g, int t, int NT,
-                                             bool gate_up, float (&acc)[2][4]) {
-  const uint8_t* box = st + cw * 1024;
-  const uint8_t* sa = st + kStageW;
-  const uint4 a = *reinterpret_cast<const uint4*>(box + swz64_off(g, t));
-  const uint4 c = gate_up ? *reinterpret_cast<const uint4*>(box + 512 + swz64_off(g, t))
-                          : *reinterpret_cast<const uint4*>(box + swz64_off(g + 8, t));
+// One stage of a shared-expert (bf16) item: 32 K elements (half h) x 1 tile per warp.
+// Lane t takes elements [16t + 8h, +8) of the 64-element stage row, for its two A rows and
+// for user g (conflict-free under the 128-byte swizzle).
+__device__ __forceinline__ void stage_shared(const uint8_t* st, const Lane& L, int NT,
+                                             float (&acc)[2][4]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(st + L.bw_a);
+  const uint4 c = *reinterpret_cast<const uint4*>(st + L.bw_b);
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     if (nt < NT) {
-      const uint4 b = *reinterpret_cast<const uint4*>(sa + (nt * 8 + g) * kActStride + cw * 64 + t * 16);
+      // users 8..15 are rows 8..15 of the activation box: same swizzle phase as rows 0..7
+      const uint4 b = *reinterpret_cast<const uint4*>(st + L.bact + nt * 8 * 128);
       mma_bf16(acc[nt], a.x, c.x, a.y, c.y, b.x, b.y);
       mma_bf16(acc[nt], a.z, c.z, a.w, c.w, b.z, b.w);
     }
@@ -400,7 +412,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   }
   pdl_wait();
   const int D = min(max(*s.n_distinct, 1), kMaxPicks);
-  const int n_items = (PHASE == 0) ? dm.Is / 8 + D * (dm.I / 32) : dm.H / 16 + D * (dm.H / 64);
+  const int n_items = (PHASE == 0) ? dm.Is / 32 + D * (dm.I / 32) : dm.H / 64 + D * (dm.H / 64);
   for (int i = threadIdx.x; i < D; i += kStreamThreads) t_uniq[i] = s.uniq[i];
   for (int i = threadIdx.x; i <= D; i += kStreamThreads) t_off[i] = s.user_off[i];
   for (int i = threadIdx.x; i < dm.R * dm.k; i += kStreamThreads) t_users[i] = s.user_list[i];
@@ -443,15 +455,13 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
       int next = 0;  // the following item, fetched while this one streams
       if (lane == 0) next = (int)atomicAdd(&s.counters[PHASE], 1u);
       const Item it = decode_item(PHASE, item, dm, tb, D);
-      // lane u < U: where user u's activations (and down's per-block scales) come from
+      const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
+      // lane u < U of a routed item: where user u's activations (and down's per-block
+      // scales) come from
       const uint8_t* asrc = nullptr;
       const float* ssrc = nullptr;
-      if (lane < it.U) {
-        if (it.kind == kSharedGU) {
-          asrc = (const uint8_t*)(s.n + (size_t)lane * dm.H);
-        } else if (it.kind == kSharedDN) {
-          asrc = (const uint8_t*)(s.ms + (size_t)lane * dm.Is);
-        } else if (it.kind == kRoutedGU) {
+      if (routed && lane < it.U) {
+        if (it.kind == kRoutedGU) {
           asrc = (const uint8_t*)(s.n16 + (size_t)(tb.users[it.u0 + lane] / dm.k) * dm.H);
         } else {
           const int pick = tb.users[it.u0 + lane];
@@ -459,7 +469,6 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
           ssrc = s.mid16s + (size_t)pick * (dm.I / 32);
         }
       }
-      const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
       const uint8_t* wsbase = (it.kind == kRoutedGU) ? w.w13s : w.w2s;
       const int kb = it.K / 32;  // scale bytes per weight row
       for (int kc = 0; kc < it.nst && ok; ++kc) {
@@ -479,41 +488,35 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
         uint8_t* sa = st + kStageW;
         uint8_t* sws = sa + kStageA;
         uint8_t* sas = sws + kStageWS;
-        const int k0 = kc * kKChunk;
-        const int kval = min(kKChunk, it.K - k0);  // multiple of 128 (routed) / 64 (shared)
+        const int k0 = kc * it.chunk;
+        const int kval = min(it.chunk, it.K - k0);  // routed: 128 or 256; shared: 64
         if (lane == 0) {
           info[stage * 2] = item;
           info[stage * 2 + 1] = kc;
-          uint32_t bytes = 0;
-          if (it.kind == kRoutedGU) bytes = (uint32_t)(kval / 128) * 2 * 2048;
-          else if (it.kind == kRoutedDN) bytes = (uint32_t)(kval / 128) * 4096;
-          else bytes = (uint32_t)(kval / 32) * 1024;
-          bytes += (uint32_t)it.U * (uint32_t)kval * 2u;
+          uint32_t bytes = kStageW;  // full boxes, also when partly past K (zero filled)
+          if (routed) bytes += (uint32_t)it.U * (uint32_t)kval * 2u;
+          else bytes += (uint32_t)dm.Rmax * 128u;
           mbar_expect_tx(&full[stage], bytes);
           if (it.kind == kRoutedGU) {
-            for (int b = 0; b < kval / 128; ++b) {
-              tma_load_2d(sw + b * 2048, &maps.w13, (k0 >> 1) + b * 64, it.row0, &full[stage], pol);
-              tma_load_2d(sw + 4096 + b * 2048, &maps.w13, (k0 >> 1) + b * 64, it.row1,
-                          &full[stage], pol);
-            }
+            tma_load_2d(sw, &maps.w13, k0 >> 1, it.row0, &full[stage], pol);
+            tma_load_2d(sw + 4096, &maps.w13, k0 >> 1, it.row1, &full[stage], pol);
           } else if (it.kind == kRoutedDN) {
-            for (int b = 0; b < kval / 128; ++b)
-              tma_load_2d(sw + b * 4096, &maps.w2, (k0 >> 1) + b * 64, it.row0, &full[stage], pol);
+            tma_load_2d(sw, &maps.w2, k0 >> 1, it.row0, &full[stage], pol);
           } else if (it.kind == kSharedGU) {
-            for (int q = 0; q < kval / 32; ++q) {
-              tma_load_2d(sw + q * 1024, &maps.ws13, k0 + q * 32, it.row0, &full[stage], pol);
-              tma_load_2d(sw + q * 1024 + 512, &maps.ws13, k0 + q * 32, it.row1, &full[stage], pol);
-            }
+            tma_load_2d(sw, &maps.ws13, k0, it.row0, &full[stage], pol);
+            tma_load_2d(sw + 4096, &maps.ws13, k0, it.row1, &full[stage], pol);
+            tma_load_2d(sa, &maps.n, k0, 0, &full[stage], 0ull);
           } else {
-            for (int q = 0; q < kval / 32; ++q)
-              tma_load_2d(sw + q * 1024, &maps.ws2, k0 + q * 32, it.row0, &full[stage], pol);
+            tma_load_2d(sw, &maps.ws2, k0, it.row0, &full[stage], pol);
+            tma_load_2d(sa, &maps.ms, k0, 0, &full[stage], 0ull);
           }
         }
         __syncwarp();
-        // user u's activation slice (f16 scaled for routed, bf16 for shared), by lane u
-        if (lane < it.U)
-          bulk_load(sa + lane * kActStride, asrc + (size_t)k0 * 2, (uint32_t)kval * 2u, &full[stage]);
         if (routed) {
+          // user u's f16 activation slice, by lane u
+          if (lane < it.U)
+            bulk_load(sa + lane * kActStride, asrc + (size_t)k0 * 2, (uint32_t)kval * 2u,
+                      &full[stage]);
           // E8M0 scales of the 64 weight rows, 8 blocks each (4 bytes per copy)
           const int words = kval / 128;  // 1 or 2 words per row in this stage
 #pragma unroll
@@ -570,13 +573,14 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   // ------------------------------------------------------------------ consumers ----
   const int cw = warp - 1;
   const int g = lane >> 2, t = lane & 3;
+  const int em = cw & 3, eh = cw >> 2;  // this warp's tile and K half
   int stage = 0;
   uint32_t phase = 0;
   int cur = -1, nitems = 0;
   Item it;
   it.kind = 0; it.nst = 0; it.U = 0; it.K = 0; it.out0 = 0; it.u0 = 0; it.row0 = 0; it.row1 = 0;
-  it.e = 0; it.d = 0;
-  RoutedLane L = routed_lane(PHASE == 0, cw, g, t);
+  it.e = 0; it.d = 0; it.chunk = kChunkF4;
+  const Lane L = make_lane(PHASE == 0, cw, g, t);
   float acc[2][4];
   for (;;) {
     if (!mbar_wait(&full[stage], phase, budget_ns)) {
@@ -595,14 +599,14 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     }
     const uint8_t* st = stages + stage * kStageBytes;
     const int NT = it.U > 8 ? 2 : 1;
-    if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
-      // this warp's 4 blocks start at K offset 128 * (cw >> 2) of the stage
-      if (kc * kKChunk + 128 * (cw >> 2) < it.K) {
+    // this warp's half of the stage's K range starts at element (chunk / 2) * eh
+    if (kc * it.chunk + (it.chunk >> 1) * eh < it.K) {
+      if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
         if (PHASE == 0) stage_routed<true>(st, L, NT, acc);
         else stage_routed<false>(st, L, NT, acc);
+      } else {
+        stage_shared(st, L, NT, acc);
       }
-    } else if (kc * kKChunk + 32 * cw < it.K) {
-      stage_shared(st, cw, g, t, NT, it.kind == kSharedGU, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
@@ -611,9 +615,8 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     if (kc == it.nst - 1) {
       // ------------------------------------------------------ item epilogue ----
       // partial sums go to one of two reduction buffers (alternating by item, so the next
-      // item's writes need no barrier).  Routed: tile m is the sum of warps m and m + 4
-      // (blocks 0-3 then 4-7 of every stage), finished by warp m + 4 * nt.  Shared: the
-      // single tile is the sum of the 8 warps in warp order, finished by warp 4 * nt.
+      // item's writes need no barrier); tile m = (half 0) + (half 1), i.e. warps m and
+      // m + 4, finished by warp m + 4 * nt for N-tile nt.
       const int buf = nitems & 1;
       ++nitems;
       float4* rb = red + buf * (kConsumerWarps * 2 * 32);
@@ -622,22 +625,13 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
         if (nt < NT)
           rb[(cw * 2 + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
       named_bar_sync(1, kConsumerWarps * 32);
-      const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
-      const int em = cw & 3, ent = cw >> 2;
-      const bool active = routed ? (ent < NT) : (em == 0 && ent < NT);
+      const int ent = eh;  // N-tile this warp finishes
+      const bool active = ent < NT;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       if (active) {
-        if (routed) {
-          const float4 v0 = rb[(em * 2 + ent) * 32 + lane];
-          const float4 v1 = rb[((em + 4) * 2 + ent) * 32 + lane];
-          c[0] = v0.x + v1.x; c[1] = v0.y + v1.y; c[2] = v0.z + v1.z; c[3] = v0.w + v1.w;
-        } else {
-#pragma unroll
-          for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
-            const float4 v = rb[(w2 * 2 + ent) * 32 + lane];
-            c[0] += v.x; c[1] += v.y; c[2] += v.z; c[3] += v.w;
-          }
-        }
+        const float4 v0 = rb[(em * 2 + ent) * 32 + lane];
+        const float4 v1 = rb[((em + 4) * 2 + ent) * 32 + lane];
+        c[0] = v0.x + v1.x; c[1] = v0.y + v1.y; c[2] = v0.z + v1.z; c[3] = v0.w + v1.w;
       }
       if (it.kind == kSharedGU) {
         if (active) {
@@ -645,7 +639,8 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
           for (int q = 0; q < 2; ++q) {
             const int r = ent * 8 + 2 * t + q;
             if (r < it.U)
-              s.ms[(size_t)r * dm.Is + it.out0 + g] = __float2bfloat16_rn(silu_f(c[q]) * c[2 + q]);
+              s.ms[(size_t)r * dm.Is + it.out0 + 8 * em + g] =
+                  __float2bfloat16_rn(silu_f(c[q]) * c[2 + q]);
           }
         }
       } else if (it.kind == kSharedDN) {
@@ -654,8 +649,9 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
           for (int q = 0; q < 2; ++q) {
             const int r = ent * 8 + 2 * t + q;
             if (r < it.U) {
-              s.ys[(size_t)r * dm.H + it.out0 + g] = c[q];
-              s.ys[(size_t)r * dm.H + it.out0 + g + 8] = c[2 + q];
+              float* yrow = s.ys + (size_t)r * dm.H + it.out0 + 16 * em;
+              yrow[g] = c[q];
+              yrow[g + 8] = c[2 + q];
             }
           }
         }
@@ -752,31 +748,30 @@ static int encode_2d(EncodeTiledFn fn, CUtensorMap* m, CUtensorMapDataType dt, c
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
-// Returns 0 on success, -1 if the driver has no tensor-map encoder, -2 if encoding failed.
-int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w) {
+// Every box has 128-byte rows (the 128-byte swizzle span): 128 MXFP4 code bytes (256
+// elements) or 64 bf16 elements.  Returns 0 on success, -1 if the driver has no tensor-map
+// encoder, -2 if encoding failed.
+int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scratch& s) {
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                        &q) != cudaSuccess || fn == nullptr)
     return -1;
   EncodeTiledFn enc = (EncodeTiledFn)fn;
-  const uint64_t H = d.H, E = d.E, I = d.I, Is = d.Is;
-  if (encode_2d(enc, &out->w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.w13c, H / 2, E * 2 * I, H / 2, 64, 32))
-    return -2;
-  if (encode_2d(enc, &out->w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.w2c, I / 2, E * H, I / 2, 64, 64))
-    return -2;
-  if (encode_2d(enc, &out->ws13, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w.ws13, H, 2 * Is, H * 2, 32, 8))
-    return -2;
-  if (encode_2d(enc, &out->ws2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w.ws2, Is, H, Is * 2, 32, 16))
-    return -2;
+  const uint64_t H = d.H, E = d.E, I = d.I, Is = d.Is, R = d.Rmax;
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (encode_2d(enc, &out->w13, U8, w.w13c, H / 2, E * 2 * I, H / 2, 128, 32)) return -2;
+  if (encode_2d(enc, &out->w2, U8, w.w2c, I / 2, E * H, I / 2, 128, 64)) return -2;
+  if (encode_2d(enc, &out->ws13, BF, w.ws13, H, 2 * Is, H * 2, 64, 32)) return -2;
+  if (encode_2d(enc, &out->ws2, BF, w.ws2, Is, H, Is * 2, 64, 64)) return -2;
+  if (encode_2d(enc, &out->n, BF, s.n, H, R, H * 2, 64, (uint32_t)R)) return -2;
+  if (encode_2d(enc, &out->ms, BF, s.ms, Is, R, Is * 2, 64, (uint32_t)R)) return -2;
   return 0;
 }
-
-size_t stream_maps_size() { return sizeof(StreamMaps); }
 
 }  // namespace mtail

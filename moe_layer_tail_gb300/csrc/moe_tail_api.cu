@@ -132,14 +132,6 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   h->w.ws13 = (const __nv_bfloat16*)w->shared_w13;
   h->w.ws2 = (const __nv_bfloat16*)w->shared_w2;
 
-  {
-    Dims d0;
-    d0.R = cfg->max_rows; d0.H = cfg->hidden; d0.E = cfg->n_experts; d0.k = cfg->top_k;
-    d0.I = cfg->expert_inter; d0.Is = cfg->shared_inter; d0.eps = cfg->rms_eps;
-    const int mrc = make_stream_maps(&h->maps, d0, h->w);
-    if (mrc == -1) { delete h; snprintf(g_cuda_err, sizeof(g_cuda_err), "no cuTensorMapEncodeTiled"); return MOE_TAIL_ERR_CUDA; }
-    if (mrc != 0) { delete h; return MOE_TAIL_ERR_UNSUPPORTED; }
-  }
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = prepare_stream_kernels();
   if (e == cudaSuccess) e = prepare_front_kernels();
@@ -158,6 +150,22 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
     if (h->stage) cudaFree(h->stage);
     delete h;
     return cuda_fail(e);
+  }
+  {
+    Dims d0;
+    d0.R = cfg->max_rows; d0.Rmax = cfg->max_rows; d0.H = cfg->hidden; d0.E = cfg->n_experts;
+    d0.k = cfg->top_k; d0.I = cfg->expert_inter; d0.Is = cfg->shared_inter; d0.eps = cfg->rms_eps;
+    const int mrc = make_stream_maps(&h->maps, d0, h->w, h->s);
+    if (mrc != 0) {
+      cudaFree(h->slab);
+      cudaFree(h->stage);
+      delete h;
+      if (mrc == -1) {
+        snprintf(g_cuda_err, sizeof(g_cuda_err), "no cuTensorMapEncodeTiled");
+        return MOE_TAIL_ERR_CUDA;
+      }
+      return MOE_TAIL_ERR_UNSUPPORTED;
+    }
   }
   *out = h;
   return MOE_TAIL_OK;
@@ -190,6 +198,7 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
   cudaStream_t st = (cudaStream_t)stream;
   Dims d;
   d.R = rows;
+  d.Rmax = h->cfg.max_rows;
   d.H = h->cfg.hidden;
   d.E = h->cfg.n_experts;
   d.k = h->cfg.top_k;

@@ -28,6 +28,7 @@ enum : int32_t {
 
 struct Dims {
   int R;        // rows of this call
+  int Rmax;     // rows the handle was created for (height of the activation boxes)
   int H, E, k, I, Is;
   float eps;
 };
@@ -138,10 +139,12 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // TMA descriptors of the streamed weight matrices (built once at create time).
 struct StreamMaps {
-  CUtensorMap w13;   // u8  [E*2I, H/2], box {64 B, 32 rows}, 64-byte swizzle
-  CUtensorMap w2;    // u8  [E*H, I/2],  box {64 B, 64 rows}
-  CUtensorMap ws13;  // bf16 [2Is, H],   box {32, 8}
-  CUtensorMap ws2;   // bf16 [H, Is],    box {32, 16}
+  CUtensorMap w13;   // u8  [E*2I, H/2], box {128 B, 32 rows}, 128-byte swizzle
+  CUtensorMap w2;    // u8  [E*H, I/2],  box {128 B, 64 rows}
+  CUtensorMap ws13;  // bf16 [2Is, H],   box {64, 32}
+  CUtensorMap ws2;   // bf16 [H, Is],    box {64, 64}
+  CUtensorMap n;     // bf16 [Rmax, H] scratch n,   box {64, Rmax}
+  CUtensorMap ms;    // bf16 [Rmax, Is] scratch ms, box {64, Rmax}
 };
 
 // ------------------------------------------------------------------ launchers ----
@@ -160,7 +163,7 @@ cudaError_t launch_front_fused(const Dims& d, const __nv_bfloat16* x,
                                cudaStream_t st, bool pdl);
 cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch& s,
                                   int num_sms, cudaStream_t st);
-int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w);
+int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scratch& s);
 cudaError_t prepare_stream_kernels();
 cudaError_t prepare_front_kernels();
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
