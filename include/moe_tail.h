@@ -81,10 +81,10 @@ typedef struct moe_tail moe_tail_t; /* opaque handle */
 
 typedef struct {
   int32_t max_rows;       /* 1..16: the largest `rows` any run will pass */
-  int32_t hidden;         /* H: multiple of 128, at most 32768 */
+  int32_t hidden;         /* H: multiple of 256 (of 512 above 2048), at most 32768 */
   int32_t n_experts;      /* E: 1..1024 */
   int32_t top_k;          /* k: 1..min(E, 32) */
-  int32_t expert_inter;   /* I: multiple of 128 */
+  int32_t expert_inter;   /* I: multiple of 128 (of 512 above 2048) */
   int32_t shared_inter;   /* Is: multiple of 64 */
   float rms_eps;          /* RMSNorm epsilon (> 0) */
   int32_t norm_topk_prob; /* must be 1: the picked weights are renormalised to sum to 1 */

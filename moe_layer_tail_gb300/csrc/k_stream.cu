@@ -1,10 +1,10 @@
 // k_stream.cu -- the weight-streaming expert kernels: every distinct routed expert and the
 // shared expert stream their weights from HBM exactly once per call.
 //
-// Work: the gate/up launch (PHASE 0) runs, for each group of 32 intermediate columns j,
-// the 32 gate + 32 up weight rows of the shared expert (bf16) and of every distinct routed
+// Work: the gate/up launch (PHASE 0) runs, for each group of 64 intermediate columns j,
+// the 64 gate + 64 up weight rows of the shared expert (bf16) and of every distinct routed
 // expert d (MXFP4) against every row that uses them.  The down launch (PHASE 1) runs, for
-// each group of 64 hidden outputs, the 64 w2 rows of the shared expert and of every
+// each group of 128 hidden outputs, the 128 w2 rows of the shared expert and of every
 // distinct routed expert against each user's SiLU*up vector.  A row's result never depends
 // on which other rows share its expert: each output column of the contraction belongs to
 // one user, and every sum runs in the same order whoever else is present.
@@ -15,56 +15,52 @@
 // using row as a column of one multi-column product), 17 (no work for experts nobody
 // picked), 18 (wide weight loads) and 21 (weights read once per call bypass the caches).
 //
-// Machine mapping (sm_103a):
-//   * one CTA per SM, one producer warp + 8 consumer warps, items taken from a global
-//     atomic counter (shared-expert items first, they are the largest);
-//   * every pipeline stage holds one 64-row x 128-byte weight tile (256 MXFP4 or 64 bf16
-//     elements per row), written by one or two 2D TMA loads with the 128-byte swizzle --
-//     few, large TMA operations, since each one occupies the SM's TMA unit for a while;
-//     the users' activation slices come with 1D bulk copies (routed) or one 2D box of all
-//     rows (shared); the E8M0 and activation scales come with cp.async, all arriving on the
-//     stage's mbarrier (transaction bytes + arrivals); 10 stages in flight per SM;
-//   * consumer warp w works on MMA tile m = w & 3 (16 weight rows) and half h = w >> 2 of
-//     every stage's K range: MXFP4 bytes go through cvt.rn.f16x2.e2m1x2 straight into
-//     mma.m16n8k16 A fragments (weights = M rows, users = N columns), each 32-element
-//     block's product is scaled by its E8M0 scale (times the activation block scale for
-//     down) and accumulated in fp32; the shared expert is bf16 x bf16 into fp32;
-//   * at the end of an item, tile m = (half 0) + (half 1), stored by one warp;
+// Machine mapping (sm_103a), one CTA per SM, warp-specialised:
+//   * warp 0, lane 0 -- the producer: takes items from a global atomic counter (shared-expert
+//     items first, they are the largest) and, per pipeline stage, issues one or two 2D TMA
+//     loads of a 128-row x 128-byte weight tile (128-byte swizzle, L2 evict-first) plus one
+//     TMA load of the users' activation slice; every 8 stages of a routed item it adds the
+//     E8M0 weight scales (and, for down, the activation block scales) of the next 2048 K
+//     elements into a separate two-slot window ring.  Nothing but TMA issue and mbarrier
+//     bookkeeping runs on this thread, so a stage costs it a few hundred cycles at most;
+//   * warps 2..17 -- 16 consumer warps: warp c works on MMA tile m = c & 7 (16 weight rows)
+//     and half h = c >> 3 of every stage's K range.  MXFP4 bytes go through
+//     cvt.rn.f16x2.e2m1x2 straight into mma.m16n8k16 A fragments (weights = M rows, users =
+//     N columns), each 32-element block's product is scaled by its E8M0 scale (times the
+//     activation block scale for down) and accumulated in fp32; the shared expert is
+//     bf16 x bf16 into fp32.  At the end of an item each warp drops its partial sums into a
+//     reduction slot and moves on -- no consumer ever waits for another consumer;
+//   * warp 1 -- the epilogue: adds the two K halves of every tile in a fixed order and
+//     finishes the item (SiLU*up, the f16 copy of mid with its block scales, stores).
 //   * activations enter the routed contractions as f16 with power-of-two scales (one per row
 //     for gate/up, applied in the epilogue; one per 32-element block for down, applied per
 //     block), exact for bf16 values in range;
-//   * every mbarrier wait is bounded by a %globaltimer budget; on expiry the kernel sets
-//     the status word and leaves.
+//   * every wait is bounded by a %globaltimer budget; on expiry the kernel sets the status
+//     word, lets the copies it issued land, and leaves.
+#include <cstring>
+
 #include "moe_tail_internal.cuh"
 
 namespace mtail {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 10;
-constexpr int kChunkF4 = 256;            // MXFP4 elements per stage row (128 bytes)
-constexpr int kChunkBF = 64;             // bf16 elements per stage row (128 bytes)
-constexpr int kStageW = 8192;            // 64 weight rows x 128 bytes
-constexpr int kActStride = 576;          // routed: bytes per user (512 + 64 pad)
-constexpr int kStageA = kMaxRows * kActStride;
-constexpr int kStageWS = 512;            // weight scales: 64 rows x 8 blocks
-constexpr int kStageAS = kMaxRows * 32;  // activation scales: 16 users x 8 floats
-constexpr int kStageBytes = kStageW + kStageA + kStageWS + kStageAS;
-constexpr int kRedBytes = 2 * kConsumerWarps * 2 * 512;  // 2 x [warp][nt][lane] float4
-constexpr int kTableBytes = (3 * kMaxPicks + 1 + kMaxRows) * 4;
-constexpr int kXmaxBytes = 2 * 4 * kMaxRows * 4;
-constexpr int kStreamSmem = kStages * kStageBytes + kRedBytes + 256 + kTableBytes + kXmaxBytes;
-
-static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+constexpr int kConsumerWarps = 16;
+constexpr int kStreamThreads = (kConsumerWarps + 2) * 32;
+constexpr int kChunkF4 = 256;     // MXFP4 elements per stage row (128 bytes)
+constexpr int kChunkBF = 64;      // bf16 elements per stage row (128 bytes)
+constexpr int kStageW = 16384;    // 128 weight rows x 128 bytes
+constexpr int kActPitch = 512;    // routed activation rows: 256 f16 per stage
+constexpr int kWinK = 2048;       // K elements per scale window
+constexpr int kWinStages = kWinK / kChunkF4;
+constexpr int kWinW = 8192;       // weight scales of one window: 128 rows x 64 bytes
+constexpr int kSmemLimit = 232448;
 
 enum : int { kSharedGU = 0, kRoutedGU = 1, kSharedDN = 2, kRoutedDN = 3 };
 
 struct Item {
   int kind;
-  int e, d;
   int row0, row1;  // tensor-map rows: gate (or single) box, up box
   int out0;        // first output index (j for gate/up, h for down)
-  int K, nst, chunk;
+  int K, nst;
   int U, u0;
 };
 
@@ -80,59 +76,60 @@ struct Tables {
   const float* rscale;  // [R] per-row scale of the f16 gate/up activations
 };
 
+__device__ __forceinline__ int items_of(int phase, const Dims& dm, int D) {
+  return (phase == 0) ? dm.Is / 64 + D * (dm.I / 64) : dm.H / 128 + D * (dm.H / 128);
+}
+
 __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
                                             const Tables& s, int D) {
   Item it;
-  it.d = 0;
-  it.e = 0;
   it.u0 = 0;
   it.row1 = 0;
   if (phase == 0) {
-    const int ns = dm.Is / 32;
+    const int ns = dm.Is / 64;
     it.K = dm.H;
     if (item < ns) {
       it.kind = kSharedGU;
-      it.out0 = item * 32;
+      it.out0 = item * 64;
       it.row0 = it.out0;
       it.row1 = dm.Is + it.out0;
       it.U = dm.R;
-      it.chunk = kChunkBF;
+      it.nst = (dm.H + kChunkBF - 1) / kChunkBF;
     } else {
-      const int q = item - ns, per = dm.I / 32;
+      const int q = item - ns, per = dm.I / 64;
+      const int d = min(q / per, D - 1);
+      const int e = s.uniq[d];
       it.kind = kRoutedGU;
-      it.d = min(q / per, D - 1);
-      it.e = s.uniq[it.d];
-      it.out0 = (q % per) * 32;
-      it.row0 = it.e * 2 * dm.I + it.out0;
+      it.out0 = (q % per) * 64;
+      it.row0 = e * 2 * dm.I + it.out0;
       it.row1 = it.row0 + dm.I;
-      it.u0 = s.off[it.d];
-      it.U = s.off[it.d + 1] - it.u0;
-      it.chunk = kChunkF4;
+      it.u0 = s.off[d];
+      it.U = s.off[d + 1] - it.u0;
+      it.nst = (dm.H + kChunkF4 - 1) / kChunkF4;
     }
   } else {
-    const int ns = dm.H / 64;
+    const int ns = dm.H / 128;
     if (item < ns) {
       it.kind = kSharedDN;
       it.K = dm.Is;
-      it.out0 = item * 64;
+      it.out0 = item * 128;
       it.row0 = it.out0;
       it.U = dm.R;
-      it.chunk = kChunkBF;
+      it.nst = (dm.Is + kChunkBF - 1) / kChunkBF;
     } else {
-      const int q = item - ns, per = dm.H / 64;
+      const int q = item - ns, per = dm.H / 128;
+      const int d = min(q / per, D - 1);
+      const int e = s.uniq[d];
       it.kind = kRoutedDN;
       it.K = dm.I;
-      it.d = min(q / per, D - 1);
-      it.e = s.uniq[it.d];
-      it.out0 = (q % per) * 64;
-      it.row0 = it.e * dm.H + it.out0;
-      it.u0 = s.off[it.d];
-      it.U = s.off[it.d + 1] - it.u0;
-      it.chunk = kChunkF4;
+      it.out0 = (q % per) * 128;
+      it.row0 = e * dm.H + it.out0;
+      it.u0 = s.off[d];
+      it.U = s.off[d + 1] - it.u0;
+      it.nst = (dm.I + kChunkF4 - 1) / kChunkF4;
     }
   }
-  it.U = max(0, min(it.U, kMaxRows));
-  it.nst = (it.K + it.chunk - 1) / it.chunk;
+  it.U = max(1, min(it.U, kMaxRows));
   return it;
 }
 
@@ -147,10 +144,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* b) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(b))
-               : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
   uint32_t ok;
@@ -183,6 +176,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
@@ -191,63 +192,13 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
-                                       uint32_t& d) {
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-               : "r"(addr));
-}
 __device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void cvt_e2m1x4(uint32_t w, uint32_t* h) {
-  e2m1x8_to_f16x2(w, h[0], h[1], h[2], h[3]);
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Byte address of 16-byte chunk c of row r in a box of 64-byte rows written by TMA with
-// the 64-byte swizzle (chunk index XOR bits 1..2 of the row; box base 512-byte aligned).
-__device__ __forceinline__ uint32_t swz64(uint32_t base, int r, int c) {
-  return base + (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
-}
-
-// Byte offset of 16-byte chunk c of row r in a box of 128-byte rows written by TMA with the
-// 128-byte swizzle (chunk index XOR the row's low 3 bits; box base 1024-byte aligned).
-__device__ __forceinline__ int swz128_off(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
-
 // d = A * B for one m16n8k16 f16 product (no accumulator input).
 __device__ __forceinline__ void mma_f16_z(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -256,6 +207,22 @@ __device__ __forceinline__ void mma_f16_z(float* d, uint32_t a0, uint32_t a1, ui
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
+__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Byte offset of 16-byte chunk c of row r in a box of 128-byte rows written by TMA with the
+// 128-byte swizzle (chunk index XOR the row's low 3 bits; box base 1024-byte aligned).
+__device__ __forceinline__ int swz128_off(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
 // E8M0 byte i of a little-endian word of four scales -> float 2^(s-127); the byte 0
 // (2^-127) flushes to 0.
@@ -263,61 +230,108 @@ __device__ __forceinline__ float e8m0_byte(uint32_t w, int i) {
   return __uint_as_float((i < 3 ? (w << (23 - 8 * i)) : (w >> 1)) & 0x7F800000u);
 }
 
-// Per-lane shared-memory offsets (within a stage), fixed for the kernel: warp cw works on
-// MMA tile m = cw & 3 and on half h = cw >> 2 of every stage's K range.
-struct Lane {
-  // routed (MXFP4): word t of block chunk 4h + c, A rows g and g + 8; the 4 E8M0 bytes of
-  // those rows for blocks 4h..4h+3; user g's 16 bytes of block 4h; down: user 2t's scales
-  int code_a[4], code_b[4];
-  int scale_a, scale_b;
-  int act, ascale;
-  // shared (bf16): chunk 2t + h of A rows g and g + 8; user g's matching 16 bytes
-  int bw_a, bw_b, bact;
+// --------------------------------------------------------------- shared-memory plan ----
+
+struct SmemPtrs {
+  uint8_t* stages;
+  uint8_t* win;      // [2][win_bytes]
+  float4* red;       // [2][16 warps][nt_max][32 lanes]
+  int* t_uniq;
+  int* t_off;
+  int* t_users;
+  float* t_rscale;
+  uint64_t* full;    // [stages] producer -> consumers (transaction bytes)
+  uint64_t* empty;   // [stages] consumers -> producer (16 arrivals)
+  uint64_t* wempty;  // [2] consumers -> producer: scale window slot free
+  uint64_t* rfull;   // [2] consumers -> epilogue: partial sums written (16 arrivals)
+  uint64_t* rempty;  // [2] epilogue -> consumers: reduction slot read
+  int2* info;        // [stages] item, k-chunk of each stage
+  int* rinfo;        // [2] item of each reduction slot
 };
 
-__device__ __forceinline__ Lane make_lane(bool gate_up, int cw, int g, int t) {
+__device__ __forceinline__ SmemPtrs carve_smem(uint8_t* smem, const StreamLayout& L) {
+  SmemPtrs p;
+  p.stages = smem;
+  p.win = smem + L.off_win;
+  p.red = reinterpret_cast<float4*>(smem + L.off_red);
+  p.t_uniq = reinterpret_cast<int*>(smem + L.off_tab);
+  p.t_off = p.t_uniq + kMaxPicks;
+  p.t_users = p.t_off + kMaxPicks + 1;
+  p.t_rscale = reinterpret_cast<float*>(p.t_users + kMaxPicks);
+  p.full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
+  p.empty = p.full + kMaxStreamStages;
+  p.wempty = p.empty + kMaxStreamStages;
+  p.rfull = p.wempty + 2;
+  p.rempty = p.rfull + 2;
+  p.info = reinterpret_cast<int2*>(p.rempty + 2);
+  p.rinfo = reinterpret_cast<int*>(p.info + kMaxStreamStages);
+  return p;
+}
+
+// --------------------------------------------------------------------- consumers ----
+
+// Per-lane shared-memory offsets fixed for the kernel: warp c works on MMA tile m = c & 7
+// and on half h = c >> 3 of every stage's K range.
+struct Lane {
+  // routed (MXFP4): word t of block chunk 4h + c, A rows a (MMA rows 0-7) and b (8-15)
+  int code_a[4], code_b[4];
+  // routed: the rows' E8M0 bytes inside a scale window (add the block offset)
+  int scale_a, scale_b;
+  // shared (bf16): chunk 2t + h of A rows a and b
+  int bw_a, bw_b;
+};
+
+__device__ __forceinline__ Lane make_lane(bool gate_up, int cw, int g, int t, int spitch) {
   Lane L;
-  const int m = cw & 3, h = cw >> 2;
-  int ra, rb, boxa, boxb, sra, srb;
+  const int m = cw & 7, h = cw >> 3;
+  int ra, rb, boxb, sb0;
   if (gate_up) {  // gate box rows 8m+g (A rows 0-7), up box rows 8m+g (A rows 8-15)
-    ra = 8 * m + g; rb = ra;
-    boxa = 0; boxb = 4096;
-    sra = ra; srb = 32 + rb;
-  } else {        // one 64-row box: rows 16m+g and 16m+g+8
-    ra = 16 * m + g; rb = ra + 8;
-    boxa = 0; boxb = 0;
-    sra = ra; srb = rb;
+    ra = 8 * m + g;
+    rb = ra;
+    boxb = 8192;
+    sb0 = 4096;
+  } else {        // one 128-row box: rows 16m+g and 16m+g+8
+    ra = 16 * m + g;
+    rb = ra + 8;
+    boxb = 0;
+    sb0 = 0;
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    L.code_a[c] = boxa + swz128_off(ra, 4 * h + c) + 4 * t;
+    L.code_a[c] = swz128_off(ra, 4 * h + c) + 4 * t;
     L.code_b[c] = boxb + swz128_off(rb, 4 * h + c) + 4 * t;
   }
-  L.scale_a = kStageW + kStageA + sra * 8 + 4 * h;
-  L.scale_b = kStageW + kStageA + srb * 8 + 4 * h;
-  L.act = kStageW + g * kActStride + (4 * h) * 64 + t * 16;
-  L.ascale = kStageW + kStageA + kStageWS + (2 * t) * 32 + 16 * h;
-  L.bw_a = boxa + swz128_off(ra, 2 * t + h);
+  L.scale_a = ra * spitch + 4 * h;
+  L.scale_b = sb0 + rb * spitch + 4 * h;
+  L.bw_a = swz128_off(ra, 2 * t + h);
   L.bw_b = boxb + swz128_off(rb, 2 * t + h);
-  L.bact = kStageW + swz128_off(g, 2 * t + h);
   return L;
 }
 
+// Per-item offsets of this lane's users (N columns 8nt + g for the B fragments; columns
+// 8nt + 2t and 8nt + 2t + 1 for the down activation scales).
+struct UserOffs {
+  int act[2];
+  int as0[2], as1[2];
+};
+
 // One stage of a routed MXFP4 item: 4 scale blocks x 1 tile per warp.  Each block's two
 // k16 products are scaled by the row's E8M0 scale (and, for down, the user's block scale)
-// and added to the fp32 accumulators.
+// and added to the fp32 accumulators.  `sblk` = byte offset of this warp's first block in
+// the window rows; `wsb` = the window slot.
 template <bool GATE_UP>
-__device__ __forceinline__ void stage_routed(const uint8_t* st, const Lane& L, int NT,
-                                             float (&acc)[2][4]) {
-  const uint32_t swa = *reinterpret_cast<const uint32_t*>(st + L.scale_a);
-  const uint32_t swb = *reinterpret_cast<const uint32_t*>(st + L.scale_b);
-  float4 as0[2], as1[2];  // down: scales of users (2t, 2t+1) for the 4 blocks, per N-tile
+__device__ __forceinline__ void stage_routed(const uint8_t* st, const uint8_t* wsb,
+                                             const Lane& L, const UserOffs& uo, int NT,
+                                             int sblk, float (&acc)[2][4]) {
+  const uint32_t swa = *reinterpret_cast<const uint32_t*>(wsb + L.scale_a + sblk);
+  const uint32_t swb = *reinterpret_cast<const uint32_t*>(wsb + L.scale_b + sblk);
+  float4 as0[2], as1[2];  // down: block scales of users (2t, 2t+1), per N-tile
   if (!GATE_UP) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       if (nt < NT) {
-        as0[nt] = *reinterpret_cast<const float4*>(st + L.ascale + nt * 8 * 32);
-        as1[nt] = *reinterpret_cast<const float4*>(st + L.ascale + nt * 8 * 32 + 32);
+        as0[nt] = *reinterpret_cast<const float4*>(wsb + uo.as0[nt] + 4 * sblk);
+        as1[nt] = *reinterpret_cast<const float4*>(wsb + uo.as1[nt] + 4 * sblk);
       }
     }
   }
@@ -332,7 +346,7 @@ __device__ __forceinline__ void stage_routed(const uint8_t* st, const Lane& L, i
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       if (nt < NT) {
-        const uint4 b = *reinterpret_cast<const uint4*>(st + L.act + nt * 8 * kActStride + c * 64);
+        const uint4 b = *reinterpret_cast<const uint4*>(st + uo.act[nt] + c * 64);
         float tmp[4];
         mma_f16_z(tmp, ha[0], hb[0], ha[1], hb[1], b.x, b.y);
         mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b.z, b.w);
@@ -357,17 +371,119 @@ __device__ __forceinline__ void stage_routed(const uint8_t* st, const Lane& L, i
 // One stage of a shared-expert (bf16) item: 32 K elements (half h) x 1 tile per warp.
 // Lane t takes elements [16t + 8h, +8) of the 64-element stage row, for its two A rows and
 // for user g (conflict-free under the 128-byte swizzle).
-__device__ __forceinline__ void stage_shared(const uint8_t* st, const Lane& L, int NT,
-                                             float (&acc)[2][4]) {
+__device__ __forceinline__ void stage_shared(const uint8_t* st, const Lane& L,
+                                             const UserOffs& uo, int NT, float (&acc)[2][4]) {
   const uint4 a = *reinterpret_cast<const uint4*>(st + L.bw_a);
   const uint4 c = *reinterpret_cast<const uint4*>(st + L.bw_b);
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     if (nt < NT) {
-      // users 8..15 are rows 8..15 of the activation box: same swizzle phase as rows 0..7
-      const uint4 b = *reinterpret_cast<const uint4*>(st + L.bact + nt * 8 * 128);
+      const uint4 b = *reinterpret_cast<const uint4*>(st + uo.act[nt]);
       mma_bf16(acc[nt], a.x, c.x, a.y, c.y, b.x, b.y);
       mma_bf16(acc[nt], a.z, c.z, a.w, c.w, b.z, b.w);
+    }
+  }
+}
+
+// --------------------------------------------------------------------- epilogue ----
+
+// Tile m's sums for N-tile nt: (half 0) + (half 1), in that order.
+__device__ __forceinline__ void tile_sum(const float4* rb, int nt_max, int m, int nt, int lane,
+                                         float (&c)[4]) {
+  const float4 v0 = rb[(m * nt_max + nt) * 32 + lane];
+  const float4 v1 = rb[((m + 8) * nt_max + nt) * 32 + lane];
+  c[0] = v0.x + v1.x;
+  c[1] = v0.y + v1.y;
+  c[2] = v0.z + v1.z;
+  c[3] = v0.w + v1.w;
+}
+
+__device__ __forceinline__ void finish_item(const Item& it, const float4* rb, int nt_max,
+                                         const Dims& dm, const Tables& tb, const Scratch& s,
+                                         int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const int NT = it.U > 8 ? 2 : 1;
+  for (int nt = 0; nt < NT; ++nt) {
+    if (it.kind == kSharedGU) {
+      for (int m = 0; m < 8; ++m) {
+        float c[4];
+        tile_sum(rb, nt_max, m, nt, lane, c);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int r = nt * 8 + 2 * t + q;
+          if (r < it.U)
+            s.ms[(size_t)r * dm.Is + it.out0 + 8 * m + g] =
+                __float2bfloat16_rn(silu_f(c[q]) * c[2 + q]);
+        }
+      }
+    } else if (it.kind == kSharedDN || it.kind == kRoutedDN) {
+      float* rows[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int u = nt * 8 + 2 * t + q;
+        rows[q] = nullptr;
+        if (u < it.U)
+          rows[q] = (it.kind == kSharedDN) ? s.ys + (size_t)u * dm.H + it.out0
+                                           : s.y + (size_t)tb.users[it.u0 + u] * dm.H + it.out0;
+      }
+      for (int m = 0; m < 8; ++m) {
+        float c[4];
+        tile_sum(rb, nt_max, m, nt, lane, c);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          if (rows[q] != nullptr) {
+            rows[q][16 * m + g] = c[q];
+            rows[q][16 * m + g + 8] = c[2 + q];
+          }
+        }
+      }
+    } else {
+      // routed gate/up: mid = bf16(SiLU(gate) * up) with the row's activation scale
+      // restored; its f16 copy gets one power-of-two scale per (user, 32 columns)
+      float rs[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int u = nt * 8 + 2 * t + q;
+        rs[q] = (u < it.U) ? tb.rscale[tb.users[it.u0 + u] / dm.k] : 0.f;
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float mv[4][2];
+        float amax[2] = {0.f, 0.f};
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+          float c[4];
+          tile_sum(rb, nt_max, 4 * half + mm, nt, lane, c);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            mv[mm][q] = __bfloat162float(
+                __float2bfloat16_rn(silu_f(c[q] * rs[q]) * (c[2 + q] * rs[q])));
+            amax[q] = fmaxf(amax[q], fabsf(mv[mm][q]));
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          amax[q] = fmaxf(amax[q], __shfl_xor_sync(0xffffffffu, amax[q], 4));
+          amax[q] = fmaxf(amax[q], __shfl_xor_sync(0xffffffffu, amax[q], 8));
+          amax[q] = fmaxf(amax[q], __shfl_xor_sync(0xffffffffu, amax[q], 16));
+          const int u = nt * 8 + 2 * t + q;
+          if (u < it.U) {
+            int p = 0;
+            if (amax[q] > 0.f) {
+              const int ex = (int)((__float_as_uint(amax[q]) >> 23) & 0xFF) - 127;
+              p = max(-100, min(100, ex - 14));
+            }
+            const float down = __uint_as_float((uint32_t)(127 - p) << 23);
+            const size_t slot = (size_t)(it.u0 + u);
+            __half* mrow = s.mid16 + slot * dm.I + it.out0 + 32 * half;
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) mrow[8 * mm + g] = __float2half_rn(mv[mm][q] * down);
+            if (g == 0)
+              s.mid16s[slot * (dm.I / 32) + it.out0 / 32 + half] =
+                  __uint_as_float((uint32_t)(127 + p) << 23);
+          }
+        }
+      }
     }
   }
 }
@@ -381,22 +497,15 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   // The dynamic shared memory starts 1024-byte aligned (nothing else is in shared memory),
   // as the swizzled TMA boxes need; every pointer below stays in the shared space.
   extern __shared__ __align__(1024) uint8_t smem[];
+  const StreamLayout& lay = maps.lay;
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) set_status(s.status, kStatusBadTile);
     return;
   }
-  uint8_t* stages = smem;
-  float4* red = (float4*)(smem + kStages * kStageBytes);
-  uint64_t* full = (uint64_t*)(smem + kStages * kStageBytes + kRedBytes);
-  uint64_t* empty = full + kStages;
-  int* info = (int*)(empty + kStages);  // [kStages][2]: item, k-chunk
-  int* t_uniq = (int*)(smem + kStages * kStageBytes + kRedBytes + 256);
-  int* t_off = t_uniq + kMaxPicks;
-  int* t_users = t_off + kMaxPicks + 1;
-  float* t_rscale = (float*)(t_users + kMaxPicks);
-  float* xmax = t_rscale + kMaxRows;  // [2][4 tiles][kMaxRows]
-
+  const SmemPtrs sp = carve_smem(smem, lay);
+  const int S = lay.stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
   // Before the routing is known: pull this CTA's share of the shared expert's weights into
   // L2 (they do not depend on any earlier kernel), so their HBM reads overlap the front.
   if (warp == 0) {
@@ -412,325 +521,283 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   }
   pdl_wait();
   const int D = min(max(*s.n_distinct, 1), kMaxPicks);
-  const int n_items = (PHASE == 0) ? dm.Is / 32 + D * (dm.I / 32) : dm.H / 64 + D * (dm.H / 64);
-  for (int i = threadIdx.x; i < D; i += kStreamThreads) t_uniq[i] = s.uniq[i];
-  for (int i = threadIdx.x; i <= D; i += kStreamThreads) t_off[i] = s.user_off[i];
-  for (int i = threadIdx.x; i < dm.R * dm.k; i += kStreamThreads) t_users[i] = s.user_list[i];
-  for (int i = threadIdx.x; i < dm.R; i += kStreamThreads) t_rscale[i] = s.n16s[i];
+  const int n_items = items_of(PHASE, dm, D);
+  for (int i = threadIdx.x; i < D; i += kStreamThreads) sp.t_uniq[i] = s.uniq[i];
+  for (int i = threadIdx.x; i <= D; i += kStreamThreads) sp.t_off[i] = s.user_off[i];
+  for (int i = threadIdx.x; i < dm.R * dm.k; i += kStreamThreads) sp.t_users[i] = s.user_list[i];
+  for (int i = threadIdx.x; i < dm.R; i += kStreamThreads) sp.t_rscale[i] = s.n16s[i];
   Tables tb;
-  tb.uniq = t_uniq;
-  tb.off = t_off;
-  tb.users = t_users;
-  tb.rscale = t_rscale;
+  tb.uniq = sp.t_uniq;
+  tb.off = sp.t_off;
+  tb.users = sp.t_users;
+  tb.rscale = sp.t_rscale;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full[i], 1 + 32);
-      mbar_init(&empty[i], kConsumerWarps);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&sp.full[i], 1);
+      mbar_init(&sp.empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sp.wempty[i], kConsumerWarps);
+      mbar_init(&sp.rfull[i], kConsumerWarps);
+      mbar_init(&sp.rempty[i], 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
 
+  // K length of the routed contraction and the byte pitch of its scale-window rows
+  const int Kr = (PHASE == 0) ? dm.H : dm.I;
+  const int spitch = (Kr > kWinK) ? 64 : Kr / 32;
+  const int apitch = 4 * min(64, dm.I / 32);  // down: activation-scale window rows
+
   if (warp == 0) {
     // ---------------------------------------------------------------- producer ----
+    if (lane != 0) return;
     const uint64_t pol = policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
+    uint32_t wcnt = 0;  // scale windows issued so far
     bool ok = true;
     // stages whose copies were issued and not yet seen consumed, with their phase parity
     uint32_t pend = 0u, pend_par = 0u;
     // failure-injection switch: CTA 0 leaves its first stage unpublished, so the consumers'
     // bounded wait on it expires (tests the timeout path; never set in production)
     bool skip_first = (debug & kDebugStallFirstStage) && blockIdx.x == 0;
-    int item = 0;
-    if (lane == 0) item = (int)atomicAdd(&s.counters[PHASE], 1u);
-    for (;;) {
-      item = __shfl_sync(0xffffffffu, item, 0);
-      if (item >= n_items) {
-        pdl_trigger();  // this CTA is in its tail: let the next launch take the SM
-        break;
-      }
-      int next = 0;  // the following item, fetched while this one streams
-      if (lane == 0) next = (int)atomicAdd(&s.counters[PHASE], 1u);
+    int item = (int)atomicAdd(&s.counters[PHASE], 1u);
+    while (ok && item < n_items) {
+      const int next = (int)atomicAdd(&s.counters[PHASE], 1u);  // lands while this streams
       const Item it = decode_item(PHASE, item, dm, tb, D);
       const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
-      // lane u < U of a routed item: where user u's activations (and down's per-block
-      // scales) come from
-      const uint8_t* asrc = nullptr;
-      const float* ssrc = nullptr;
-      if (routed && lane < it.U) {
-        if (it.kind == kRoutedGU) {
-          asrc = (const uint8_t*)(s.n16 + (size_t)(tb.users[it.u0 + lane] / dm.k) * dm.H);
-        } else {
-          const int pick = tb.users[it.u0 + lane];
-          asrc = (const uint8_t*)(s.mid16 + (size_t)pick * dm.I);
-          ssrc = s.mid16s + (size_t)pick * (dm.I / 32);
-        }
-      }
-      const uint8_t* wsbase = (it.kind == kRoutedGU) ? w.w13s : w.w2s;
-      const int kb = it.K / 32;  // scale bytes per weight row
-      for (int kc = 0; kc < it.nst && ok; ++kc) {
-        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, budget_ns);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+      const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;  // down activation box height
+      uint32_t act_bytes;
+      if (it.kind == kRoutedGU) act_bytes = (uint32_t)dm.Rmax * kActPitch;
+      else if (it.kind == kRoutedDN) act_bytes = (4u << hsel) * kActPitch;
+      else act_bytes = (uint32_t)dm.Rmax * 128u;
+      for (int kc = 0; kc < it.nst; ++kc) {
+        if (!mbar_wait(&sp.empty[stage], phase ^ 1, budget_ns)) { ok = false; break; }
         pend &= ~(1u << stage);
         if (skip_first) {
           skip_first = false;
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (++stage == S) { stage = 0; phase ^= 1; }
           continue;
+        }
+        uint8_t* st = sp.stages + stage * lay.stage_bytes;
+        uint32_t bytes = kStageW + act_bytes;
+        const bool wstart = routed && (kc % kWinStages) == 0;
+        uint8_t* ws = sp.win + (wcnt & 1u) * lay.win_bytes;
+        uint32_t wbytes = 0;
+        if (wstart) {
+          if (!mbar_wait(&sp.wempty[wcnt & 1u], ((wcnt >> 1) & 1u) ^ 1u, budget_ns)) {
+            ok = false;
+            break;
+          }
+          if (PHASE == 0) wbytes = (Kr > kWinK) ? 8192u : 4u * (uint32_t)Kr;
+          else wbytes = ((Kr > kWinK) ? 8192u : 4u * (uint32_t)Kr) + (4u << hsel) * (uint32_t)apitch;
+          bytes += wbytes;
         }
         pend |= 1u << stage;
         pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-        uint8_t* st = stages + stage * kStageBytes;
-        uint8_t* sw = st;
+        sp.info[stage] = make_int2(item, kc);
+        mbar_expect_tx(&sp.full[stage], bytes);
         uint8_t* sa = st + kStageW;
-        uint8_t* sws = sa + kStageA;
-        uint8_t* sas = sws + kStageWS;
-        const int k0 = kc * it.chunk;
-        const int kval = min(it.chunk, it.K - k0);  // routed: 128 or 256; shared: 64
-        if (lane == 0) {
-          info[stage * 2] = item;
-          info[stage * 2 + 1] = kc;
-          uint32_t bytes = kStageW;  // full boxes, also when partly past K (zero filled)
-          if (routed) bytes += (uint32_t)it.U * (uint32_t)kval * 2u;
-          else bytes += (uint32_t)dm.Rmax * 128u;
-          mbar_expect_tx(&full[stage], bytes);
-          if (it.kind == kRoutedGU) {
-            tma_load_2d(sw, &maps.w13, k0 >> 1, it.row0, &full[stage], pol);
-            tma_load_2d(sw + 4096, &maps.w13, k0 >> 1, it.row1, &full[stage], pol);
-          } else if (it.kind == kRoutedDN) {
-            tma_load_2d(sw, &maps.w2, k0 >> 1, it.row0, &full[stage], pol);
-          } else if (it.kind == kSharedGU) {
-            tma_load_2d(sw, &maps.ws13, k0, it.row0, &full[stage], pol);
-            tma_load_2d(sw + 4096, &maps.ws13, k0, it.row1, &full[stage], pol);
-            tma_load_2d(sa, &maps.n, k0, 0, &full[stage], 0ull);
-          } else {
-            tma_load_2d(sw, &maps.ws2, k0, it.row0, &full[stage], pol);
-            tma_load_2d(sa, &maps.ms, k0, 0, &full[stage], 0ull);
-          }
+        if (it.kind == kRoutedGU) {
+          const int x = kc * (kChunkF4 / 2);
+          tma_load_2d(st, &maps.w13, x, it.row0, &sp.full[stage], pol);
+          tma_load_2d(st + 8192, &maps.w13, x, it.row1, &sp.full[stage], pol);
+          tma_load_2d(sa, &maps.n16, kc * kChunkF4, 0, &sp.full[stage]);
+        } else if (it.kind == kRoutedDN) {
+          tma_load_2d(st, &maps.w2, kc * (kChunkF4 / 2), it.row0, &sp.full[stage], pol);
+          tma_load_2d(sa, &maps.mid16[hsel], kc * kChunkF4, it.u0, &sp.full[stage]);
+        } else if (it.kind == kSharedGU) {
+          tma_load_2d(st, &maps.ws13, kc * kChunkBF, it.row0, &sp.full[stage], pol);
+          tma_load_2d(st + 8192, &maps.ws13, kc * kChunkBF, it.row1, &sp.full[stage], pol);
+          tma_load_2d(sa, &maps.n, kc * kChunkBF, 0, &sp.full[stage]);
+        } else {
+          tma_load_2d(st, &maps.ws2, kc * kChunkBF, it.row0, &sp.full[stage], pol);
+          tma_load_2d(sa, &maps.ms, kc * kChunkBF, 0, &sp.full[stage]);
         }
-        __syncwarp();
-        if (routed) {
-          // user u's f16 activation slice, by lane u
-          if (lane < it.U)
-            bulk_load(sa + lane * kActStride, asrc + (size_t)k0 * 2, (uint32_t)kval * 2u,
-                      &full[stage]);
-          // E8M0 scales of the 64 weight rows, 8 blocks each (4 bytes per copy)
-          const int words = kval / 128;  // 1 or 2 words per row in this stage
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c = lane + 32 * q;
-            const int row = c >> 1, wd = c & 1;
-            if (wd < words) {
-              const size_t grow = (it.kind == kRoutedGU)
-                                      ? ((row < 32) ? (size_t)it.row0 + row : (size_t)it.row1 + (row - 32))
-                                      : (size_t)it.row0 + row;
-              cp_async4(sws + row * 8 + wd * 4, wsbase + grow * kb + (k0 / 32) + wd * 4);
+        if (wstart) {
+          const int win = kc / kWinStages;
+          if (PHASE == 0) {
+            if (Kr > kWinK) {
+              tma_load_2d(ws, &maps.w13s, win * 64, it.row0, &sp.full[stage]);
+              tma_load_2d(ws + 4096, &maps.w13s, win * 64, it.row1, &sp.full[stage]);
+            } else {  // the whole K of the 64 gate and 64 up rows: two contiguous runs
+              const size_t rb = (size_t)(Kr / 32);
+              bulk_load(ws, w.w13s + (size_t)it.row0 * rb, 2u * (uint32_t)Kr, &sp.full[stage]);
+              bulk_load(ws + 4096, w.w13s + (size_t)it.row1 * rb, 2u * (uint32_t)Kr,
+                        &sp.full[stage]);
             }
+          } else {
+            if (Kr > kWinK) {
+              tma_load_2d(ws, &maps.w2s, win * 64, it.row0, &sp.full[stage]);
+            } else {
+              const size_t rb = (size_t)(Kr / 32);
+              bulk_load(ws, w.w2s + (size_t)it.row0 * rb, 4u * (uint32_t)Kr, &sp.full[stage]);
+            }
+            tma_load_2d(ws + kWinW, &maps.mid16s[hsel], win * 64, it.u0, &sp.full[stage]);
           }
-          // per-block activation scales (down only: the gate/up activations carry one
-          // scale per row, applied in the epilogue)
-          if (ssrc != nullptr) {
-            for (int half = 0; half < words; ++half)
-              cp_async16(sas + lane * 32 + half * 16, ssrc + k0 / 32 + half * 4);
-          }
+          ++wcnt;
         }
-        cp_async_arrive_noinc(&full[stage]);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++stage == S) { stage = 0; phase ^= 1; }
       }
-      if (!ok) break;
       item = next;
     }
+    pdl_trigger();  // this CTA is in its tail: let the next launch take the SM
     if (ok) {
-      // end-of-work marker
-      if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, budget_ns);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (ok) {
-        if (lane == 0) {
-          info[stage * 2] = -1;
-          info[stage * 2 + 1] = 0;
-          mbar_arrive(&full[stage]);
-        }
-        cp_async_arrive_noinc(&full[stage]);
+      // end-of-work marker (withheld too by the failure injection, when this CTA got no
+      // item to stall on)
+      ok = mbar_wait(&sp.empty[stage], phase ^ 1, budget_ns);
+      if (ok && !skip_first) {
+        sp.info[stage] = make_int2(-1, 0);
+        mbar_arrive(&sp.full[stage]);
       }
     }
     if (!ok) {
       // a wait expired: record it, then let every copy this CTA issued land (bounded)
       // before the CTA's shared memory is released
-      if (lane == 0) {
-        set_status(s.status, kStatusTimeout);
-        for (int st2 = 0; st2 < kStages; ++st2)
-          if (pend & (1u << st2)) mbar_wait(&full[st2], (pend_par >> st2) & 1u, budget_ns);
-      }
-      __syncwarp();
+      set_status(s.status, kStatusTimeout);
+      for (int st2 = 0; st2 < S; ++st2)
+        if (pend & (1u << st2)) mbar_wait(&sp.full[st2], (pend_par >> st2) & 1u, budget_ns);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+
+  if (warp == 1) {
+    // ---------------------------------------------------------------- epilogue ----
+    for (uint32_t rc = 0;; ++rc) {
+      const uint32_t rb = rc & 1u;
+      if (!mbar_wait(&sp.rfull[rb], (rc >> 1) & 1u, budget_ns)) {
+        if (lane == 0) set_status(s.status, kStatusTimeout);
+        break;
+      }
+      const int item = sp.rinfo[rb];
+      if (item < 0) break;
+      const Item it = decode_item(PHASE, item, dm, tb, D);
+      finish_item(it, sp.red + rb * (kConsumerWarps * lay.nt_max * 32), lay.nt_max, dm, tb, s,
+                  lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sp.rempty[rb]);
+    }
     return;
   }
 
   // ------------------------------------------------------------------ consumers ----
-  const int cw = warp - 1;
+  const int cw = warp - 2;
   const int g = lane >> 2, t = lane & 3;
-  const int em = cw & 3, eh = cw >> 2;  // this warp's tile and K half
+  const int eh = cw >> 3;  // this warp's K half
+  const Lane L = make_lane(PHASE == 0, cw, g, t, spitch);
   int stage = 0;
   uint32_t phase = 0;
-  int cur = -1, nitems = 0;
+  uint32_t wcnt = 0, rc = 0;
+  int cur = -1;
   Item it;
-  it.kind = 0; it.nst = 0; it.U = 0; it.K = 0; it.out0 = 0; it.u0 = 0; it.row0 = 0; it.row1 = 0;
-  it.e = 0; it.d = 0; it.chunk = kChunkF4;
-  const Lane L = make_lane(PHASE == 0, cw, g, t);
+  it.kind = 0; it.nst = 1; it.U = 1; it.K = 0; it.out0 = 0; it.u0 = 0; it.row0 = 0; it.row1 = 0;
+  UserOffs uo;
+  int NT = 1;
+  bool routed = false;
   float acc[2][4];
   for (;;) {
-    if (!mbar_wait(&full[stage], phase, budget_ns)) {
+    if (!mbar_wait(&sp.full[stage], phase, budget_ns)) {
       if (lane == 0) set_status(s.status, kStatusTimeout);
       break;
     }
-    const int item = info[stage * 2], kc = info[stage * 2 + 1];
-    if (item < 0) break;
+    const int2 inf = sp.info[stage];
+    const int item = inf.x, kc = inf.y;
+    if (item < 0) {
+      // end of work: hand the epilogue the end marker through the next reduction slot
+      const uint32_t rb = rc & 1u;
+      if (mbar_wait(&sp.rempty[rb], ((rc >> 1) & 1u) ^ 1u, budget_ns)) {
+        if (cw == 0 && lane == 0) sp.rinfo[rb] = -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sp.rfull[rb]);
+      } else if (lane == 0) {
+        set_status(s.status, kStatusTimeout);
+      }
+      break;
+    }
     if (item != cur) {
       cur = item;
       it = decode_item(PHASE, item, dm, tb, D);
+      routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
+      NT = it.U > 8 ? 2 : 1;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt) {
+        const int n = min(nt * 8 + g, it.U - 1);  // B column of this lane (clamped)
+        if (it.kind == kRoutedGU)
+          uo.act[nt] = kStageW + (tb.users[it.u0 + n] / dm.k) * kActPitch + eh * 256 + 16 * t;
+        else if (it.kind == kRoutedDN)
+          uo.act[nt] = kStageW + n * kActPitch + eh * 256 + 16 * t;
+        else
+          uo.act[nt] = kStageW + swz128_off(n, 2 * t + eh);
+        const int u0c = min(nt * 8 + 2 * t, it.U - 1), u1c = min(nt * 8 + 2 * t + 1, it.U - 1);
+        uo.as0[nt] = kWinW + u0c * apitch + 16 * eh;
+        uo.as1[nt] = kWinW + u1c * apitch + 16 * eh;
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-    }
-    const uint8_t* st = stages + stage * kStageBytes;
-    const int NT = it.U > 8 ? 2 : 1;
-    // this warp's half of the stage's K range starts at element (chunk / 2) * eh
-    if (kc * it.chunk + (it.chunk >> 1) * eh < it.K) {
-      if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
-        if (PHASE == 0) stage_routed<true>(st, L, NT, acc);
-        else stage_routed<false>(st, L, NT, acc);
-      } else {
-        stage_shared(st, L, NT, acc);
       }
     }
+    const uint8_t* st = sp.stages + stage * lay.stage_bytes;
+    if (routed) {
+      const uint8_t* wsb = sp.win + (wcnt & 1u) * lay.win_bytes;
+      if (kc * kChunkF4 + (kChunkF4 / 2) * eh < it.K) {
+        const int sblk = (kc % kWinStages) * 8;
+        if (PHASE == 0) stage_routed<true>(st, wsb, L, uo, NT, sblk, acc);
+        else stage_routed<false>(st, wsb, L, uo, NT, sblk, acc);
+      }
+    } else if (kc * kChunkBF + (kChunkBF / 2) * eh < it.K) {
+      stage_shared(st, L, uo, NT, acc);
+    }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == kStages) { stage = 0; phase ^= 1; }
-
+    if (lane == 0) mbar_arrive(&sp.empty[stage]);
+    if (++stage == S) { stage = 0; phase ^= 1; }
+    if (routed && ((kc % kWinStages) == kWinStages - 1 || kc == it.nst - 1)) {
+      if (lane == 0) mbar_arrive(&sp.wempty[wcnt & 1u]);
+      ++wcnt;
+    }
     if (kc == it.nst - 1) {
-      // ------------------------------------------------------ item epilogue ----
-      // partial sums go to one of two reduction buffers (alternating by item, so the next
-      // item's writes need no barrier); tile m = (half 0) + (half 1), i.e. warps m and
-      // m + 4, finished by warp m + 4 * nt for N-tile nt.
-      const int buf = nitems & 1;
-      ++nitems;
-      float4* rb = red + buf * (kConsumerWarps * 2 * 32);
+      // item end: partial sums to the next reduction slot, then on to the next item
+      const uint32_t rb = rc & 1u;
+      if (!mbar_wait(&sp.rempty[rb], ((rc >> 1) & 1u) ^ 1u, budget_ns)) {
+        if (lane == 0) set_status(s.status, kStatusTimeout);
+        break;
+      }
+      float4* red = sp.red + rb * (kConsumerWarps * lay.nt_max * 32);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
         if (nt < NT)
-          rb[(cw * 2 + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-      named_bar_sync(1, kConsumerWarps * 32);
-      const int ent = eh;  // N-tile this warp finishes
-      const bool active = ent < NT;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      if (active) {
-        const float4 v0 = rb[(em * 2 + ent) * 32 + lane];
-        const float4 v1 = rb[((em + 4) * 2 + ent) * 32 + lane];
-        c[0] = v0.x + v1.x; c[1] = v0.y + v1.y; c[2] = v0.z + v1.z; c[3] = v0.w + v1.w;
-      }
-      if (it.kind == kSharedGU) {
-        if (active) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int r = ent * 8 + 2 * t + q;
-            if (r < it.U)
-              s.ms[(size_t)r * dm.Is + it.out0 + 8 * em + g] =
-                  __float2bfloat16_rn(silu_f(c[q]) * c[2 + q]);
-          }
-        }
-      } else if (it.kind == kSharedDN) {
-        if (active) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int r = ent * 8 + 2 * t + q;
-            if (r < it.U) {
-              float* yrow = s.ys + (size_t)r * dm.H + it.out0 + 16 * em;
-              yrow[g] = c[q];
-              yrow[g + 8] = c[2 + q];
-            }
-          }
-        }
-      } else if (it.kind == kRoutedDN) {
-        if (active) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int u = ent * 8 + 2 * t + q;
-            if (u < it.U) {
-              float* yrow = s.y + (size_t)tb.users[it.u0 + u] * dm.H + it.out0 + 16 * em;
-              yrow[g] = c[q];
-              yrow[g + 8] = c[2 + q];
-            }
-          }
-        }
-      } else {
-        // routed gate/up: mid = bf16(SiLU(gate) * up) with the row's activation scale
-        // restored; its f16 copy gets one power-of-two scale per (pick, 32 columns), from
-        // the maximum over the item's 4 tiles (exchanged through shared memory)
-        float* mx = xmax + buf * (4 * kMaxRows);
-        float mv[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int u = ent * 8 + 2 * t + q;
-          const float rs = (active && u < it.U) ? tb.rscale[tb.users[it.u0 + u] / dm.k] : 0.f;
-          mv[q] = __bfloat162float(__float2bfloat16_rn(silu_f(c[q] * rs) * (c[2 + q] * rs)));
-          float amax = fabsf(mv[q]);
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-          if (active && g == 0) mx[em * kMaxRows + u] = amax;
-        }
-        named_bar_sync(2, kConsumerWarps * 32);
-        if (active) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int u = ent * 8 + 2 * t + q;
-            if (u < it.U) {
-              float amax = 0.f;
-#pragma unroll
-              for (int m2 = 0; m2 < 4; ++m2) amax = fmaxf(amax, mx[m2 * kMaxRows + u]);
-              int p = 0;
-              if (amax > 0.f) {
-                const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-                p = max(-100, min(100, ex - 14));
-              }
-              const float down = __uint_as_float((uint32_t)(127 - p) << 23);
-              const int pick = tb.users[it.u0 + u];
-              s.mid16[(size_t)pick * dm.I + it.out0 + 8 * em + g] = __float2half_rn(mv[q] * down);
-              if (em == 0 && g == 0)
-                s.mid16s[(size_t)pick * (dm.I / 32) + it.out0 / 32] =
-                    __uint_as_float((uint32_t)(127 + p) << 23);
-            }
-          }
-        }
-      }
+          red[(cw * lay.nt_max + nt) * 32 + lane] =
+              make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+      if (cw == 0 && lane == 0) sp.rinfo[rb] = item;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sp.rfull[rb]);
+      ++rc;
     }
   }
 }
 
-// Opt the streaming kernels in to their shared-memory size (once per process and device
-// before the first launch; called at create time, outside any graph capture).
+// Opt the streaming kernels in to the largest shared-memory size (once per process and
+// device before the first launch; called at create time, outside any graph capture).
 cudaError_t prepare_stream_kernels() {
   cudaError_t e = cudaFuncSetAttribute(k_stream<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kStreamSmem);
+                                       kSmemLimit);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_stream<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStreamSmem);
+                             kSmemLimit);
   return e;
 }
 
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
                           const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                           bool pdl, uint32_t debug) {
+  const size_t smem = (size_t)maps.lay.smem_bytes;
   if (phase == 0)
-    return launch_k(k_stream<0>, dim3(num_sms), dim3(kStreamThreads), kStreamSmem, st, pdl,
-                    maps, d, w, s, budget_ns, debug);
-  return launch_k(k_stream<1>, dim3(num_sms), dim3(kStreamThreads), kStreamSmem, st, pdl, maps,
-                  d, w, s, budget_ns, debug);
+    return launch_k(k_stream<0>, dim3(num_sms), dim3(kStreamThreads), smem, st, pdl, maps, d, w,
+                    s, budget_ns, debug);
+  return launch_k(k_stream<1>, dim3(num_sms), dim3(kStreamThreads), smem, st, pdl, maps, d, w, s,
+                  budget_ns, debug);
 }
 
 // ----------------------------------------------------------- tensor-map encoding ----
@@ -742,18 +809,38 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 static int encode_2d(EncodeTiledFn fn, CUtensorMap* m, CUtensorMapDataType dt, const void* base,
                      uint64_t inner, uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
-                     uint32_t box_rows) {
+                     uint32_t box_rows, CUtensorMapSwizzle swz) {
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
-// Every box has 128-byte rows (the 128-byte swizzle span): 128 MXFP4 code bytes (256
+// Shared-memory plan for a handle created for `Rmax` rows (stages as many as fit, up to 8).
+StreamLayout make_stream_layout(int Rmax) {
+  StreamLayout L;
+  L.act_rows = (Rmax <= 4) ? 4 : (Rmax <= 8) ? 8 : 16;
+  L.stage_bytes = kStageW + L.act_rows * kActPitch;
+  L.win_bytes = kWinW + L.act_rows * 256;
+  L.nt_max = (Rmax > 8) ? 2 : 1;
+  const int red_bytes = 2 * kConsumerWarps * L.nt_max * 512;
+  const int tab_bytes = ((3 * kMaxPicks + 1 + kMaxRows) * 4 + 127) & ~127;
+  const int bar_bytes = (2 * kMaxStreamStages + 6) * 8 + kMaxStreamStages * 8 + 2 * 4;
+  const int fixed = 2 * L.win_bytes + red_bytes + tab_bytes + ((bar_bytes + 127) & ~127);
+  L.stages = min(kMaxStreamStages, (kSmemLimit - fixed) / L.stage_bytes);
+  L.off_win = L.stages * L.stage_bytes;
+  L.off_red = L.off_win + 2 * L.win_bytes;
+  L.off_tab = L.off_red + red_bytes;
+  L.off_bar = L.off_tab + tab_bytes;
+  L.smem_bytes = L.off_bar + ((bar_bytes + 127) & ~127);
+  return L;
+}
+
+// Every weight box has 128-byte rows (the 128-byte swizzle span): 128 MXFP4 code bytes (256
 // elements) or 64 bf16 elements.  Returns 0 on success, -1 if the driver has no tensor-map
 // encoder, -2 if encoding failed.
 int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scratch& s) {
@@ -763,14 +850,35 @@ int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scr
                                        &q) != cudaSuccess || fn == nullptr)
     return -1;
   EncodeTiledFn enc = (EncodeTiledFn)fn;
-  const uint64_t H = d.H, E = d.E, I = d.I, Is = d.Is, R = d.Rmax;
-  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (encode_2d(enc, &out->w13, U8, w.w13c, H / 2, E * 2 * I, H / 2, 128, 32)) return -2;
-  if (encode_2d(enc, &out->w2, U8, w.w2c, I / 2, E * H, I / 2, 128, 64)) return -2;
-  if (encode_2d(enc, &out->ws13, BF, w.ws13, H, 2 * Is, H * 2, 64, 32)) return -2;
-  if (encode_2d(enc, &out->ws2, BF, w.ws2, Is, H, Is * 2, 64, 64)) return -2;
-  if (encode_2d(enc, &out->n, BF, s.n, H, R, H * 2, 64, (uint32_t)R)) return -2;
-  if (encode_2d(enc, &out->ms, BF, s.ms, Is, R, Is * 2, 64, (uint32_t)R)) return -2;
+  const uint64_t H = d.H, E = d.E, I = d.I, Is = d.Is, R = d.Rmax, P = (uint64_t)d.Rmax * d.k;
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
+  memset(out, 0, sizeof(*out));
+  if (encode_2d(enc, &out->w13, U8, w.w13c, H / 2, E * 2 * I, H / 2, 128, 64, SW)) return -2;
+  if (encode_2d(enc, &out->w2, U8, w.w2c, I / 2, E * H, I / 2, 128, 128, SW)) return -2;
+  if (encode_2d(enc, &out->ws13, BF, w.ws13, H, 2 * Is, H * 2, 64, 64, SW)) return -2;
+  if (encode_2d(enc, &out->ws2, BF, w.ws2, Is, H, Is * 2, 64, 128, SW)) return -2;
+  if (encode_2d(enc, &out->n, BF, s.n, H, R, H * 2, 64, (uint32_t)R, SW)) return -2;
+  if (encode_2d(enc, &out->ms, BF, s.ms, Is, R, Is * 2, 64, (uint32_t)R, SW)) return -2;
+  if (encode_2d(enc, &out->n16, F16, s.n16, H, R, H * 2, 256, (uint32_t)R, NS)) return -2;
+  for (int i = 0; i < 3; ++i) {
+    const uint32_t rows = 4u << i;
+    if (encode_2d(enc, &out->mid16[i], F16, s.mid16, I, P, I * 2, 256, rows, NS)) return -2;
+    if (encode_2d(enc, &out->mid16s[i], F32, s.mid16s, I / 32, P, (I / 32) * 4,
+                  (uint32_t)(I / 32 < 64 ? I / 32 : 64), rows, NS))
+      return -2;
+  }
+  // scale windows of 64 bytes per row, only where a row holds more than one window
+  if (H > (uint64_t)kWinK &&
+      encode_2d(enc, &out->w13s, U8, w.w13s, H / 32, E * 2 * I, H / 32, 64, 64, NS))
+    return -2;
+  if (I > (uint64_t)kWinK &&
+      encode_2d(enc, &out->w2s, U8, w.w2s, I / 32, E * H, I / 32, 64, 128, NS))
+    return -2;
+  out->lay = make_stream_layout(d.Rmax);
   return 0;
 }
 

@@ -59,13 +59,17 @@ static_assert(MOE_TAIL_DEBUG_STALL_FIRST_STAGE == (int)kDebugStallFirstStage,
 
 static int check_config(const moe_tail_config_t* c) {
   if (c->max_rows < 1 || c->max_rows > kMaxRows) return MOE_TAIL_ERR_UNSUPPORTED;
-  if (c->hidden < 128 || c->hidden % 128) return MOE_TAIL_ERR_UNSUPPORTED;
+  // hidden: whole 256-element stages; above 2048 the E8M0 rows (hidden/32 bytes) must be
+  // whole 16-byte units for the scale-window tensor maps
+  if (c->hidden < 256 || c->hidden % 256) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->hidden > 2048 && c->hidden % 512) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->hidden > (1 << 15)) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->n_experts < 1 || c->n_experts > kMaxExperts) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->top_k < 1 || c->top_k > kMaxTopK || c->top_k > c->n_experts)
     return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->expert_inter < 128 || c->expert_inter % 128 || c->expert_inter > (1 << 16))
     return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->expert_inter > 2048 && c->expert_inter % 512) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->shared_inter < 64 || c->shared_inter % 64 || c->shared_inter > (1 << 16))
     return MOE_TAIL_ERR_UNSUPPORTED;
   if (!(c->rms_eps > 0.f)) return MOE_TAIL_ERR_UNSUPPORTED;

@@ -59,8 +59,9 @@ struct Scratch {
   int32_t* user_off;     // [Rmax*k + 1] CSR offsets into user_list
   int32_t* user_list;    // [Rmax*k] pick indices r*k + slot, in (r, slot) order
   __nv_bfloat16* mid;    // [Rmax*k, I] SiLU(gate)*up of each pick (bf16)
-  __half* mid16;         // [Rmax*k, I] mid as f16, scaled by 2^-p per 32-element block
-  float* mid16s;         // [Rmax*k, I/32]
+  __half* mid16;         // [Rmax*k, I] mid as f16, scaled by 2^-p per 32-element block;
+                         // row = the pick's position in user_list (users of an expert adjacent)
+  float* mid16s;         // [Rmax*k, I/32] the 2^p of each block, same rows
   __nv_bfloat16* ms;     // [Rmax, Is] shared-expert intermediate (bf16)
   float* y;              // [Rmax*k, H] routed expert outputs
   float* ys;             // [Rmax, H] shared expert output
@@ -137,14 +138,32 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// TMA descriptors of the streamed weight matrices (built once at create time).
+// Shared-memory plan of the streaming kernels for one handle (depends on its row count).
+constexpr int kMaxStreamStages = 8;
+struct StreamLayout {
+  int stages;       // pipeline stages (<= kMaxStreamStages)
+  int stage_bytes;  // 16 KB weight tile + act_rows x 512 B of activations
+  int act_rows;     // activation rows a stage holds: 4, 8 or 16
+  int win_bytes;    // one scale window: 8 KB weight scales + act_rows x 256 B
+  int nt_max;       // N-tiles of 8 users (1 or 2)
+  int off_win, off_red, off_tab, off_bar;  // byte offsets of the regions after the stages
+  int smem_bytes;   // dynamic shared memory of a launch
+};
+
+// TMA descriptors of the streamed matrices (built once at create time) and the plan.
 struct StreamMaps {
-  CUtensorMap w13;   // u8  [E*2I, H/2], box {128 B, 32 rows}, 128-byte swizzle
-  CUtensorMap w2;    // u8  [E*H, I/2],  box {128 B, 64 rows}
-  CUtensorMap ws13;  // bf16 [2Is, H],   box {64, 32}
-  CUtensorMap ws2;   // bf16 [H, Is],    box {64, 64}
-  CUtensorMap n;     // bf16 [Rmax, H] scratch n,   box {64, Rmax}
-  CUtensorMap ms;    // bf16 [Rmax, Is] scratch ms, box {64, Rmax}
+  CUtensorMap w13;        // u8 [E*2I, H/2], box {128 B, 64 rows}, 128-byte swizzle
+  CUtensorMap w2;         // u8 [E*H, I/2], box {128 B, 128 rows}, 128-byte swizzle
+  CUtensorMap ws13;       // bf16 [2Is, H], box {64, 64}, 128-byte swizzle
+  CUtensorMap ws2;        // bf16 [H, Is], box {64, 128}, 128-byte swizzle
+  CUtensorMap n;          // bf16 [Rmax, H] scratch n, box {64, Rmax}, 128-byte swizzle
+  CUtensorMap ms;         // bf16 [Rmax, Is] scratch ms, box {64, Rmax}, 128-byte swizzle
+  CUtensorMap n16;        // f16 [Rmax, H] scratch n16, box {256, Rmax}
+  CUtensorMap mid16[3];   // f16 [Rmax*k, I] scratch mid16, box {256, 4 / 8 / 16 rows}
+  CUtensorMap mid16s[3];  // f32 [Rmax*k, I/32], box {min(64, I/32), 4 / 8 / 16 rows}
+  CUtensorMap w13s;       // u8 [E*2I, H/32], box {64 B, 64 rows} (H > 2048 only)
+  CUtensorMap w2s;        // u8 [E*H, I/32], box {64 B, 128 rows} (I > 2048 only)
+  StreamLayout lay;
 };
 
 // ------------------------------------------------------------------ launchers ----
@@ -164,6 +183,7 @@ cudaError_t launch_front_fused(const Dims& d, const __nv_bfloat16* x,
 cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch& s,
                                   int num_sms, cudaStream_t st);
 int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scratch& s);
+StreamLayout make_stream_layout(int Rmax);
 cudaError_t prepare_stream_kernels();
 cudaError_t prepare_front_kernels();
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,

@@ -55,7 +55,9 @@ def test_null_arguments_rejected_without_device(lib):
 
 
 @pytest.mark.parametrize("field,value", [("max_rows", 0), ("max_rows", 17), ("hidden", 200),
+                                         ("hidden", 384), ("hidden", 2304),
                                          ("top_k", 9), ("expert_inter", 96),
+                                         ("expert_inter", 2176),
                                          ("shared_inter", 100), ("norm_topk_prob", 0),
                                          ("n_experts", 2000), ("rms_eps", 0.0)])
 def test_unsupported_configs_refused_before_device(lib, field, value):

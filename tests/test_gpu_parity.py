@@ -75,7 +75,7 @@ def test_workload_parity_full_size(name):
     print(name, figs)
 
 
-def _small(seed, R=3, H=384, E=12, k=3, I=256, Is=192, kind="plain"):
+def _small(seed, R=3, H=512, E=12, k=3, I=256, Is=192, kind="plain"):
     shape = gen.TailShape(R, H, E, k, I, Is)
     d = gen.make_weights(shape, seed)
     d.update(gen.make_activations(shape, seed, kind, c=0.8))
@@ -101,9 +101,10 @@ def _check_small(shape, d, max_rows=None, rows=None, flags=0):
 
 @pytest.mark.parametrize("flags", [0, SIMPLE, NO_PDL, FUSED_FRONT])
 @pytest.mark.parametrize("R,H,E,k,I,Is", [
-    (1, 128, 1, 1, 128, 64),       # a single expert, smallest shapes
-    (2, 384, 12, 3, 256, 192),     # several tiles, ragged tails
-    (5, 640, 33, 7, 384, 320),     # odd expert count, k not a power of two
+    (1, 256, 1, 1, 128, 64),       # a single expert, smallest shapes
+    (2, 512, 12, 3, 256, 192),     # several tiles, ragged tails
+    (5, 768, 33, 7, 384, 320),     # odd expert count, k not a power of two
+    (3, 2560, 6, 2, 2560, 192),    # several E8M0 windows per row, the last one ragged
     (16, 256, 16, 16, 128, 128),   # k = E: every expert, maximum rows
     (16, 512, 64, 1, 256, 64),     # k = 1, maximum rows
     (4, 1024, 40, 32, 128, 256),   # k at its maximum
@@ -220,8 +221,8 @@ def test_run_rejects_bad_arguments():
         tail.run(mis, res, out)
     assert ei.value.code == ERR_INVALID_ARG
     # unsupported shapes are refused at creation
-    for bad in (gen.TailShape(2, 200, 12, 3, 256, 192), gen.TailShape(2, 384, 12, 13, 256, 192),
-                gen.TailShape(2, 384, 12, 3, 100, 192)):
+    for bad in (gen.TailShape(2, 200, 12, 3, 256, 192), gen.TailShape(2, 512, 12, 13, 256, 192),
+                gen.TailShape(2, 512, 12, 3, 100, 192), gen.TailShape(2, 2304, 12, 3, 256, 192)):
         with pytest.raises(MoeTailError) as ei:
             MoeTail(bad, dev)
         assert ei.value.code == ERR_UNSUPPORTED
