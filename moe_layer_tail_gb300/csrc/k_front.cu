@@ -216,11 +216,18 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
   return v > bv || (v == bv && e < be);
 }
 
+// kSmem: the logits are in this CTA's shared memory (else in global memory, written by an
+// earlier launch or by other CTAs of this one before a fence).
+template <bool kSmem>
+__device__ __forceinline__ float load_logit(const float* l) {
+  if constexpr (kSmem) return *l;
+  else return __ldcg(l);
+}
+
+template <bool kSmem>
 __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
                                  int32_t* n_distinct, int32_t* uniq, int32_t* user_off,
                                  int32_t* user_list, int32_t* status, int R, int E, int k) {
-  __shared__ uint32_t taken[kMaxRows][kMaxExperts / 32];
-  __shared__ float pickv[kMaxRows][kMaxTopK];
   __shared__ int32_t s_ids[kMaxPicks];
   __shared__ uint32_t rowmask[kMaxExperts];
   __shared__ int32_t eoff[kMaxExperts];  // first user slot of expert e
@@ -228,29 +235,28 @@ __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
-  for (int i = tid; i < kMaxRows * (kMaxExperts / 32); i += nthreads) (&taken[0][0])[i] = 0u;
   for (int e = tid; e < kMaxExperts; e += nthreads) rowmask[e] = 0u;
-  __syncthreads();
 
   for (int row = warp; row < R; row += nwarps) {
     const float* l = logits + (size_t)row * E;
-    // the row's logits, lane-strided, in registers (E <= 1024: up to 32 per lane)
+    // the row's logits, lane-strided, in registers (E <= 1024: up to 32 per lane); bit q of
+    // `tk` marks candidate lane + 32 q as taken (or past E)
     float lv[kMaxExperts / 32];
+    uint32_t tk = 0u;
 #pragma unroll
     for (int q = 0; q < kMaxExperts / 32; ++q) {
       const int e = lane + 32 * q;
-      lv[q] = (e < E) ? __ldcg(l + e) : -INFINITY;
+      lv[q] = (e < E) ? load_logit<kSmem>(l + e) : -INFINITY;
+      if (e >= E) tk |= 1u << q;
     }
+    float pv = 0.f;  // lane i < k keeps pick i
+    int pe = 0;
     for (int i = 0; i < k; ++i) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
 #pragma unroll
-      for (int q = 0; q < kMaxExperts / 32; ++q) {
-        const int e = lane + 32 * q;
-        if (e >= E) break;
-        if (taken[row][e >> 5] & (1u << (e & 31))) continue;
-        if (better(lv[q], e, bv, be)) { bv = lv[q]; be = e; }
-      }
+      for (int q = 0; q < kMaxExperts / 32; ++q)
+        if (!((tk >> q) & 1u) && better(lv[q], lane + 32 * q, bv, be)) { bv = lv[q]; be = lane + 32 * q; }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -258,26 +264,31 @@ __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
         if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
       }
       if (be >= E) {  // only NaN candidates left: take the lowest untaken id, flag it
-        be = E - 1;
-        for (int e = 0; e < E; ++e)
-          if (!(taken[row][e >> 5] & (1u << (e & 31)))) { be = e; break; }
+        int fe = 0x7fffffff;
+#pragma unroll
+        for (int q = kMaxExperts / 32 - 1; q >= 0; --q)
+          if (!((tk >> q) & 1u)) fe = lane + 32 * q;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) fe = min(fe, __shfl_xor_sync(0xffffffffu, fe, o));
+        be = min(fe, E - 1);
+        float mine = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMaxExperts / 32; ++q)
+          if (q == (be >> 5)) mine = lv[q];
+        bv = __shfl_sync(0xffffffffu, mine, be & 31);
         if (lane == 0) set_status(status, kStatusBadRouting);
       }
-      if (lane == 0) {
-        taken[row][be >> 5] |= 1u << (be & 31);
-        pickv[row][i] = __ldcg(l + be);
-        s_ids[row * k + i] = be;
-      }
-      __syncwarp();
+      if ((be & 31) == lane) tk |= 1u << (be >> 5);
+      if (lane == i) { pv = bv; pe = be; }
     }
-    if (lane == 0) {
-      const float m = pickv[row][0];
-      float z = 0.f;
-      for (int i = 0; i < k; ++i) z += expf(pickv[row][i] - m);
-      for (int i = 0; i < k; ++i) {
-        wts[row * k + i] = expf(pickv[row][i] - m) / z;
-        ids[row * k + i] = s_ids[row * k + i];
-      }
+    // weights: softmax of the picked logits (lane i holds pick i; pick 0 is the largest)
+    const float m = __shfl_sync(0xffffffffu, pv, 0);
+    const float ex = (lane < k) ? expf(pv - m) : 0.f;
+    const float z = warp_sum(ex);
+    if (lane < k) {
+      wts[row * k + lane] = ex / z;
+      ids[row * k + lane] = pe;
+      s_ids[row * k + lane] = pe;
     }
   }
   __syncthreads();
@@ -339,7 +350,8 @@ k_topk_dedup(const float* __restrict__ logits, int32_t* __restrict__ ids,
              int k) {
   pdl_wait();
   pdl_trigger();
-  topk_dedup_block(logits, ids, wts, n_distinct, uniq, user_off, user_list, status, R, E, k);
+  topk_dedup_block<false>(logits, ids, wts, n_distinct, uniq, user_off, user_list, status, R, E,
+                          k);
 }
 
 cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, bool pdl) {
@@ -429,14 +441,33 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int i = tid; i < R * E; i += kRtThreads) {  // logits = parts added in part order
-    float v = __ldcg(s.logit_parts + i);
-    for (int pp = 1; pp < P; ++pp) v += __ldcg(s.logit_parts + (size_t)pp * R * E + i);
-    s.logits[i] = v;
+  // logits = the parts added in part order, into shared memory (the part of n is no longer
+  // needed: R * E floats fit in its R * kRtPart bf16); eight sums in flight per thread
+  float* s_logits = reinterpret_cast<float*>(s_n);
+  const int RE = R * E;
+  for (int base = 0; base < RE; base += 8 * kRtThreads) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + tid + j * kRtThreads;
+      v[j] = (i < RE) ? __ldcg(s.logit_parts + i) : 0.f;
+    }
+    for (int pp = 1; pp < P; ++pp) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + tid + j * kRtThreads;
+        if (i < RE) v[j] += __ldcg(s.logit_parts + (size_t)pp * RE + i);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + tid + j * kRtThreads;
+      if (i < RE) s_logits[i] = v[j];
+    }
   }
   __syncthreads();
-  topk_dedup_block(s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off, s.user_list,
-                   s.status, R, E, k);
+  topk_dedup_block<true>(s_logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
+                         s.user_list, s.status, R, E, k);
   if (tid == 0) s.counters[kCtrFrontTicket] = 0u;
 }
 
@@ -608,8 +639,8 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  topk_dedup_block(s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off, s.user_list,
-                   s.status, R, E, k);
+  topk_dedup_block<false>(s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
+                          s.user_list, s.status, R, E, k);
   if (tid == 0) {
     s.counters[kCtrFrontTicket] = 0u;
     s.counters[kCtrGateUp] = 0u;
@@ -736,7 +767,7 @@ k_route_static(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restr
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  topk_dedup_block(rs->logits, ids_out, wts_out, &rs->n_distinct, rs->uniq, rs->user_off,
+  topk_dedup_block<false>(rs->logits, ids_out, wts_out, &rs->n_distinct, rs->uniq, rs->user_off,
                    rs->user_list, &rs->status, R, E, k);
   __syncthreads();
   if (tid == 0) {

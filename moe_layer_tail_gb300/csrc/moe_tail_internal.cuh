@@ -192,9 +192,4 @@ cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, cons
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl);
 
-// Shared device pieces of the front (k_front.cu).
-__device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
-                                 int32_t* n_distinct, int32_t* uniq, int32_t* user_off,
-                                 int32_t* user_list, int32_t* status, int R, int E, int k);
-
 }  // namespace mtail
