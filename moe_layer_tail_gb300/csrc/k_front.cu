@@ -13,6 +13,8 @@
 // three single-purpose kernels k_add_rmsnorm / k_router / k_topk_dedup used by the
 // cross-checking path.  bf16(x + residual) goes to scratch; the residual itself is
 // rewritten by the combine, after every reader is done.
+#include <algorithm>
+
 #include "moe_tail.h"
 #include "moe_tail_internal.cuh"
 
@@ -271,11 +273,7 @@ __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) fe = min(fe, __shfl_xor_sync(0xffffffffu, fe, o));
         be = min(fe, E - 1);
-        float mine = 0.f;
-#pragma unroll
-        for (int q = 0; q < kMaxExperts / 32; ++q)
-          if (q == (be >> 5)) mine = lv[q];
-        bv = __shfl_sync(0xffffffffu, mine, be & 31);
+        bv = load_logit<kSmem>(l + be);
         if (lane == 0) set_status(status, kStatusBadRouting);
       }
       if ((be & 31) == lane) tk |= 1u << (be >> 5);
@@ -361,78 +359,127 @@ cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, 
 }
 
 // --------------------------------------------------------------- router + top-k ----
-// Grid (ceil(E / 8), P): CTA (x, p) runs experts 8x .. 8x+7 (one per warp) over K part p
-// of H (P parts of at most 2048 elements).  Each warp's router weights for the part are
-// read into registers before the wait on the norm launch (they depend on nothing); the
-// rows' n for the part are loaded into shared memory with every load issued at once.  The
+// Grid (ceil(E / 16), P): CTA (x, p) computes the logits of experts 16x .. 16x+15 for every
+// row over K part p of H, on the tensor cores (mma.m16n8k16, bf16 x bf16 into fp32; the 16
+// experts are the M rows, the call's rows the N columns).  The CTA's router weights are
+// copied into shared memory with cp.async before the wait on the norm launch (they depend
+// on nothing), then the rows' n for the part; each of the 8 warps takes a slice of the
+// part's 32-element K steps and the warps' partial tiles are added in warp order.  The
 // partial logits of each part go to scratch; the last CTA to finish (atomic ticket after a
-// fence) adds the parts in part order, then runs top-k and the dedup.
+// fence) adds the parts in part order into shared memory, then runs top-k and the dedup.
+// Loops stay rolled: every CTA runs this code once, so its size, not its instruction
+// count, sets the time an SM waits for instructions.
 constexpr int kRtWarps = 8;
 constexpr int kRtThreads = kRtWarps * 32;
-constexpr int kRtPart = 2048;                    // max K elements per part
-constexpr int kRtGroups = kRtPart / 8 / 32;      // 16-byte weight groups per lane (8)
+constexpr int kRtTile = 16;      // experts per CTA
+constexpr int kRtMaxPart = 2048; // K elements per part at most
+constexpr int kRtMaxParts = 16;
 
-__host__ __device__ inline int router_parts(int H) { return (H + kRtPart - 1) / kRtPart; }
-// elements per part: a multiple of 128 (the last part may be shorter)
-__host__ __device__ inline int router_part_len(int H) {
-  const int P = router_parts(H);
-  return ((H + P - 1) / P + 127) / 128 * 128;
+struct RouterPlan {
+  int tiles, parts, plen;
+  size_t smem;
+};
+
+// Parts: enough CTAs to spread the router weights over the SMs (about 128), parts of at
+// most 2048 elements, each a multiple of 32.
+static RouterPlan router_plan(int R, int H, int E) {
+  RouterPlan p;
+  p.tiles = (E + kRtTile - 1) / kRtTile;
+  int P = (128 + p.tiles - 1) / p.tiles;
+  P = std::max(P, (H + kRtMaxPart - 1) / kRtMaxPart);
+  P = std::min(P, kRtMaxParts);
+  p.plen = ((H + P - 1) / P + 31) / 32 * 32;
+  p.parts = (H + p.plen - 1) / p.plen;
+  const size_t pitch = (size_t)p.plen * 2 + 16;
+  const size_t tiles_bytes = (kRtTile + (size_t)R) * pitch;
+  const size_t logit_bytes = (size_t)R * E * 4;
+  const size_t nt = (R + 7) / 8;
+  p.smem = ((std::max(tiles_bytes, logit_bytes) + 15) / 16) * 16 + kRtWarps * nt * 32 * 16;
+  return p;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __global__ void __launch_bounds__(kRtThreads)
-k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, int E, int k) {
-  extern __shared__ uint4 s_n[];  // [R][kRtPart / 8] (dynamic: R * 4 KB)
+k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, int E, int k,
+              int plen, int red_off) {
+  extern __shared__ __align__(16) uint8_t sm[];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
   const int P = gridDim.y, p = blockIdx.y;
-  const int plen = router_part_len(H);
   const int k0 = p * plen;
-  const int len = min(plen, H - k0);   // elements of this part (> 0, multiple of 128)
-  const int ng = len / 8;               // 16-byte groups per row in this part
-  const int e = blockIdx.x * kRtWarps + warp;
-  const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)min(e, E - 1) * H + k0);
-  uint4 wreg[kRtGroups];
-#pragma unroll
-  for (int q = 0; q < kRtGroups; ++q) {
-    const int c = lane + 32 * q;
-    wreg[q] = (e < E && c < ng) ? __ldg(wrow + c) : make_uint4(0u, 0u, 0u, 0u);
+  const int len = min(plen, H - k0);  // elements of this part (> 0, multiple of 32)
+  const int cpr = len / 8;            // 16-byte chunks per row in this part
+  const int pitch = plen * 2 + 16;    // bytes per staged row (16-byte pad: no bank conflicts)
+  const int e0 = blockIdx.x * kRtTile;
+  uint8_t* sw = sm;                             // [16][pitch] router weights
+  uint8_t* sn = sm + kRtTile * pitch;           // [R][pitch] n
+  float4* red = reinterpret_cast<float4*>(sm + red_off);  // [8 warps][NT][32 lanes]
+  for (int i = tid; i < kRtTile * cpr; i += kRtThreads) {
+    const int r = i / cpr, c = i % cpr;
+    cp_async16(sw + r * pitch + c * 16, w_r + (size_t)min(e0 + r, E - 1) * H + k0 + c * 8);
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   pdl_wait();
   pdl_trigger();
-  // the part of n for every row, all loads in flight together
-  for (int i = tid; i < R * ng; i += kRtThreads) {
-    const int r = i / ng, c = i % ng;
-    s_n[r * (kRtPart / 8) + c] = __ldcg(reinterpret_cast<const uint4*>(s.n + (size_t)r * H + k0) + c);
+  for (int i = tid; i < R * cpr; i += kRtThreads) {
+    const int r = i / cpr, c = i % cpr;
+    cp_async16(sn + r * pitch + c * 16, s.n + (size_t)r * H + k0 + c * 8);
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  float acc[kMaxRows];
-#pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
-#pragma unroll
-  for (int q = 0; q < kRtGroups; ++q) {
-    const int c = lane + 32 * q;
-    if (c < ng) {
-      const uint4 wv = wreg[q];
-      const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
-                           bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
-        if (r < R) {
-          const uint4 nv = s_n[r * (kRtPart / 8) + c];
-          float a = acc[r];
-          a += wf[0] * bf16_lo(nv.x); a += wf[1] * bf16_hi(nv.x);
-          a += wf[2] * bf16_lo(nv.y); a += wf[3] * bf16_hi(nv.y);
-          a += wf[4] * bf16_lo(nv.z); a += wf[5] * bf16_hi(nv.z);
-          a += wf[6] * bf16_lo(nv.w); a += wf[7] * bf16_hi(nv.w);
-          acc[r] = a;
-        }
-      }
+  // warp w: K steps [w * spw, ...) of 32 elements; lane (g, t) takes elements 8t .. 8t+7 of
+  // a step for weight rows g and g + 8 and for activation row g (+ 8 for the second tile)
+  const int NT = (R + 7) / 8;
+  const int S = len / 32, spw = (S + kRtWarps - 1) / kRtWarps;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  const uint8_t* wa = sw + g * pitch + 16 * t;
+  const uint8_t* wc = sw + (g + 8) * pitch + 16 * t;
+  const uint8_t* nb0 = sn + min(g, R - 1) * pitch + 16 * t;
+  const uint8_t* nb1 = sn + min(8 + g, R - 1) * pitch + 16 * t;
+#pragma unroll 1
+  for (int st = warp * spw; st < min(S, (warp + 1) * spw); ++st) {
+    const uint4 a = *reinterpret_cast<const uint4*>(wa + st * 64);
+    const uint4 c = *reinterpret_cast<const uint4*>(wc + st * 64);
+    const uint4 b = *reinterpret_cast<const uint4*>(nb0 + st * 64);
+    mma_bf16_16816(acc[0], a.x, c.x, a.y, c.y, b.x, b.y);
+    mma_bf16_16816(acc[0], a.z, c.z, a.w, c.w, b.z, b.w);
+    if (NT > 1) {
+      const uint4 b2 = *reinterpret_cast<const uint4*>(nb1 + st * 64);
+      mma_bf16_16816(acc[1], a.x, c.x, a.y, c.y, b2.x, b2.y);
+      mma_bf16_16816(acc[1], a.z, c.z, a.w, c.w, b2.z, b2.w);
     }
   }
-#pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) {
-    const float v = warp_sum(acc[r]);
-    if (lane == 0 && r < R && e < E) s.logit_parts[((size_t)p * R + r) * E + e] = v;
+  for (int nt = 0; nt < NT; ++nt)
+    red[(warp * NT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+  __syncthreads();
+  if (warp == 0) {
+    // lane (g, t): experts g and g + 8, rows 8 nt + 2t and 8 nt + 2t + 1
+    for (int nt = 0; nt < NT; ++nt) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int w2 = 0; w2 < kRtWarps; ++w2) {
+        const float4 x = red[(w2 * NT + nt) * 32 + lane];
+        v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+      }
+      for (int q = 0; q < 4; ++q) {
+        const int e = e0 + g + 8 * (q >> 1), r = 8 * nt + 2 * t + (q & 1);
+        if (e < E && r < R) s.logit_parts[((size_t)p * R + r) * E + e] = v[q];
+      }
+    }
   }
   __threadfence();
   __syncthreads();
@@ -441,9 +488,9 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // logits = the parts added in part order, into shared memory (the part of n is no longer
-  // needed: R * E floats fit in its R * kRtPart bf16); eight sums in flight per thread
-  float* s_logits = reinterpret_cast<float*>(s_n);
+  // logits = the parts added in part order, into shared memory (the staged tiles are no
+  // longer needed); eight sums in flight per thread
+  float* s_logits = reinterpret_cast<float*>(sm);
   const int RE = R * E;
   for (int base = 0; base < RE; base += 8 * kRtThreads) {
     float v[8];
@@ -473,19 +520,24 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
 
 cudaError_t launch_router_topk(const Dims& d, const Weights& w, const Scratch& s,
                                cudaStream_t st, bool pdl) {
-  const dim3 grid((d.E + kRtWarps - 1) / kRtWarps, router_parts(d.H));
-  return launch_k(k_router_topk, grid, dim3(kRtThreads), (size_t)d.R * kRtPart * 2, st, pdl,
-                  w.w_r, s, d.R, d.H, d.E, d.k);
+  const RouterPlan rp = router_plan(d.R, d.H, d.E);
+  const size_t nt = (d.R + 7) / 8;
+  const int red_off = (int)(rp.smem - kRtWarps * nt * 32 * 16);
+  return launch_k(k_router_topk, dim3(rp.tiles, rp.parts), dim3(kRtThreads), rp.smem, st, pdl,
+                  w.w_r, s, d.R, d.H, d.E, d.k, rp.plen, red_off);
 }
 
-// The norm kernel stages gamma (up to 64 KB) and the router kernel a part of n (up to 64 KB)
-// in dynamic shared memory.
+// Parts of the router's K at most: sizes the scratch of the partial logits.
+int router_max_parts() { return kRtMaxParts; }
+
+// The norm kernel stages gamma (up to 64 KB) and the router kernel its weight tile and n
+// (up to 2 x 16 rows of 2048 bf16 plus the reduction tiles) in dynamic shared memory.
 cudaError_t prepare_front_kernels() {
   cudaError_t e = cudaFuncSetAttribute(k_add_rmsnorm, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (1 << 15) * 2);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_router_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxRows * kRtPart * 2);
+                             (int)router_plan(kMaxRows, 1 << 15, kMaxExperts).smem + 4096);
   return e;
 }
 

@@ -93,7 +93,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
   s->n16 = (__half*)take(R * H * 2);
   s->n16s = (float*)take(R * 4);
   s->logits = (float*)take(R * E * 4);
-  s->logit_parts = (float*)take(((H + 2047) / 2048) * R * E * 4);
+  s->logit_parts = (float*)take((size_t)router_max_parts() * R * E * 4);
   s->ids = (int32_t*)take(P * 4);
   s->wts = (float*)take(P * 4);
   s->n_distinct = (int32_t*)take(4);

@@ -51,7 +51,7 @@ struct Scratch {
   __half* n16;           // [Rmax, H] n as f16, scaled by 2^-p per row
   float* n16s;           // [Rmax] the 2^p of each row
   float* logits;         // [Rmax, E]
-  float* logit_parts;    // [ceil(H / 2048), Rmax, E] router partial sums over K parts
+  float* logit_parts;    // [16, Rmax, E] router partial sums over K parts
   int32_t* ids;          // [Rmax, k] picks in pick order
   float* wts;            // [Rmax, k]
   int32_t* n_distinct;   // [1]
@@ -186,6 +186,7 @@ int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scr
 StreamLayout make_stream_layout(int Rmax);
 cudaError_t prepare_stream_kernels();
 cudaError_t prepare_front_kernels();
+int router_max_parts();
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
                           const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                           bool pdl, uint32_t debug);
