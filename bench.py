@@ -148,9 +148,11 @@ def stage_bytes(shape, D, R):
     return gu, dn
 
 
-def ncu_traffic(kernel_tag, src_hash):
-    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it was taken on
-    the current source (else None)."""
+def ncu_traffic(kernel_tag, src_hash, algorithmic_bytes):
+    """Per-launch DRAM bytes of a kernel, from the committed ncu summary if it was taken on
+    the current source (else None).  The capture runs a smaller case of the same kernel; its
+    measured DRAM bytes over its algorithmic bytes (traffic grows with the weight bytes
+    streamed) scale this launch's algorithmic bytes."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -159,7 +161,7 @@ def ncu_traffic(kernel_tag, src_hash):
     rec = d.get(kernel_tag)
     if not rec or rec.get("source_hash") != src_hash:
         return None
-    return rec.get("dram_bytes_per_launch")
+    return int(rec["dram_over_algorithmic"] * algorithmic_bytes)
 
 
 # --------------------------------------------------------------------- our arm ----
@@ -270,7 +272,7 @@ def run_ours(args, rank, world, local_rank):
         achieved = dom_bytes / dur_s / 1e9
         src = source_hash(["moe_layer_tail_gb300/csrc/k_stream.cu",
                            "moe_layer_tail_gb300/csrc/moe_tail_internal.cuh"])
-        tr = ncu_traffic(names[dom], src)
+        tr = ncu_traffic(names[dom], src, dom_bytes)
         roof = {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
                 "measured": "CUDA events around each launch on its stream, second pass of the "
                             "same %d calls (events serialise the launches: %.1f us/call)"
