@@ -16,6 +16,7 @@ path has no cross-GPU exchange; value = all ranks' calls / max-over-ranks time.
 one bounded sample (one row of a call), scaled to microseconds per call.
 """
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -46,6 +47,10 @@ def parse_args():
     p.add_argument("--workload", default=gen.BENCH_WORKLOAD)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--experts", type=int, default=0,
+                   help="profiling aid: the workload with this many experts instead (a "
+                        "smaller case of the same kernels, e.g. for an ncu capture); the "
+                        "line's config says so")
     return p.parse_args()
 
 
@@ -173,6 +178,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     wl = gen.WORKLOADS[args.workload]
     shape = wl.shape
+    if args.experts:
+        shape = dataclasses.replace(shape, E=args.experts)
     R = shape.R
     K, W = args.steps, args.warmup
     nsets = K + W
@@ -287,7 +294,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": K, "warmup": W, "ms_per_step": round(elapsed_ms / K, 5),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl.name, "rows": R, "hidden": shape.H, "experts": shape.E,
+        "config": {"workload": wl.name + ("" if not args.experts else " with %d experts" % shape.E),
+                   "rows": R, "hidden": shape.H, "experts": shape.E,
                    "top_k": shape.k, "expert_inter": shape.I, "shared_inter": shape.Is,
                    "weights": "MXFP4 routed experts, bf16 router and shared expert",
                    "distinct_experts_mean": round(float(Ds.mean()), 2),
@@ -361,6 +369,8 @@ def run_reference(args, rank, world):
     import oracle
     wl = gen.WORKLOADS[args.workload]
     shape = wl.shape
+    if args.experts:
+        shape = dataclasses.replace(shape, E=args.experts)
     R = shape.R
     cores = oracle.host_cores()
     host_w = gen.make_weights(shape, wl.seed)
