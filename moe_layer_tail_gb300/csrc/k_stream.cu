@@ -319,20 +319,18 @@ struct UserOffs {
 // k16 products are scaled by the row's E8M0 scale (and, for down, the user's block scale)
 // and added to the fp32 accumulators.  `sblk` = byte offset of this warp's first block in
 // the window rows; `wsb` = the window slot.
-template <bool GATE_UP>
+template <bool GATE_UP, int NT>
 __device__ __forceinline__ void stage_routed(const uint8_t* st, const uint8_t* wsb,
-                                             const Lane& L, const UserOffs& uo, int NT,
-                                             int sblk, float (&acc)[2][4]) {
+                                             const Lane& L, const UserOffs& uo, int sblk,
+                                             float (&acc)[2][4]) {
   const uint32_t swa = *reinterpret_cast<const uint32_t*>(wsb + L.scale_a + sblk);
   const uint32_t swb = *reinterpret_cast<const uint32_t*>(wsb + L.scale_b + sblk);
-  float4 as0[2], as1[2];  // down: block scales of users (2t, 2t+1), per N-tile
+  float4 as0[NT], as1[NT];  // down: block scales of users (2t, 2t+1), per N-tile
   if (!GATE_UP) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      if (nt < NT) {
-        as0[nt] = *reinterpret_cast<const float4*>(wsb + uo.as0[nt] + 4 * sblk);
-        as1[nt] = *reinterpret_cast<const float4*>(wsb + uo.as1[nt] + 4 * sblk);
-      }
+    for (int nt = 0; nt < NT; ++nt) {
+      as0[nt] = *reinterpret_cast<const float4*>(wsb + uo.as0[nt] + 4 * sblk);
+      as1[nt] = *reinterpret_cast<const float4*>(wsb + uo.as1[nt] + 4 * sblk);
     }
   }
 #pragma unroll
@@ -344,25 +342,23 @@ __device__ __forceinline__ void stage_routed(const uint8_t* st, const uint8_t* w
     e2m1x8_to_f16x2(wb, hb[0], hb[1], hb[2], hb[3]);
     const float sa = e8m0_byte(swa, c), sb = e8m0_byte(swb, c);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      if (nt < NT) {
-        const uint4 b = *reinterpret_cast<const uint4*>(st + uo.act[nt] + c * 64);
-        float tmp[4];
-        mma_f16_z(tmp, ha[0], hb[0], ha[1], hb[1], b.x, b.y);
-        mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b.z, b.w);
-        if (GATE_UP) {
-          acc[nt][0] += tmp[0] * sa;
-          acc[nt][1] += tmp[1] * sa;
-          acc[nt][2] += tmp[2] * sb;
-          acc[nt][3] += tmp[3] * sb;
-        } else {
-          const float u0 = (c == 0) ? as0[nt].x : (c == 1) ? as0[nt].y : (c == 2) ? as0[nt].z : as0[nt].w;
-          const float u1 = (c == 0) ? as1[nt].x : (c == 1) ? as1[nt].y : (c == 2) ? as1[nt].z : as1[nt].w;
-          acc[nt][0] += tmp[0] * (sa * u0);
-          acc[nt][1] += tmp[1] * (sa * u1);
-          acc[nt][2] += tmp[2] * (sb * u0);
-          acc[nt][3] += tmp[3] * (sb * u1);
-        }
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint4 b = *reinterpret_cast<const uint4*>(st + uo.act[nt] + c * 64);
+      float tmp[4];
+      mma_f16_z(tmp, ha[0], hb[0], ha[1], hb[1], b.x, b.y);
+      mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b.z, b.w);
+      if (GATE_UP) {
+        acc[nt][0] += tmp[0] * sa;
+        acc[nt][1] += tmp[1] * sa;
+        acc[nt][2] += tmp[2] * sb;
+        acc[nt][3] += tmp[3] * sb;
+      } else {
+        const float u0 = (c == 0) ? as0[nt].x : (c == 1) ? as0[nt].y : (c == 2) ? as0[nt].z : as0[nt].w;
+        const float u1 = (c == 0) ? as1[nt].x : (c == 1) ? as1[nt].y : (c == 2) ? as1[nt].z : as1[nt].w;
+        acc[nt][0] += tmp[0] * (sa * u0);
+        acc[nt][1] += tmp[1] * (sa * u1);
+        acc[nt][2] += tmp[2] * (sb * u0);
+        acc[nt][3] += tmp[3] * (sb * u1);
       }
     }
   }
@@ -371,18 +367,67 @@ __device__ __forceinline__ void stage_routed(const uint8_t* st, const uint8_t* w
 // One stage of a shared-expert (bf16) item: 32 K elements (half h) x 1 tile per warp.
 // Lane t takes elements [16t + 8h, +8) of the 64-element stage row, for its two A rows and
 // for user g (conflict-free under the 128-byte swizzle).
+template <int NT>
 __device__ __forceinline__ void stage_shared(const uint8_t* st, const Lane& L,
-                                             const UserOffs& uo, int NT, float (&acc)[2][4]) {
+                                             const UserOffs& uo, float (&acc)[2][4]) {
   const uint4 a = *reinterpret_cast<const uint4*>(st + L.bw_a);
   const uint4 c = *reinterpret_cast<const uint4*>(st + L.bw_b);
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    if (nt < NT) {
-      const uint4 b = *reinterpret_cast<const uint4*>(st + uo.act[nt]);
-      mma_bf16(acc[nt], a.x, c.x, a.y, c.y, b.x, b.y);
-      mma_bf16(acc[nt], a.z, c.z, a.w, c.w, b.z, b.w);
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint4 b = *reinterpret_cast<const uint4*>(st + uo.act[nt]);
+    mma_bf16(acc[nt], a.x, c.x, a.y, c.y, b.x, b.y);
+    mma_bf16(acc[nt], a.z, c.z, a.w, c.w, b.z, b.w);
+  }
+}
+
+// The ring position of a consumer warp: stage slot, its phase parity, scale windows seen.
+struct Ring {
+  int stage;
+  uint32_t phase, wcnt;
+};
+
+// All stages of one item for one consumer warp; the item's first stage has already been
+// waited for.  Returns false when a wait ran out of budget.
+template <bool GATE_UP, int NT>
+__device__ __forceinline__ bool run_routed(const SmemPtrs& sp, const StreamLayout& lay, Ring& rg,
+                                        const Item& it, const Lane& L, const UserOffs& uo,
+                                        int eh, uint64_t budget_ns, float (&acc)[2][4]) {
+  const int lane = threadIdx.x & 31;
+  const uint8_t* wsb = sp.win + (rg.wcnt & 1u) * lay.win_bytes;
+  // this warp's half of the last stage may lie past K
+  const bool last_has_k = (it.nst - 1) * kChunkF4 + (kChunkF4 / 2) * eh < it.K;
+  for (int kc = 0; kc < it.nst; ++kc) {
+    if (kc > 0 && !mbar_wait(&sp.full[rg.stage], rg.phase, budget_ns)) return false;
+    if (kc < it.nst - 1 || last_has_k)
+      stage_routed<GATE_UP, NT>(sp.stages + rg.stage * lay.stage_bytes, wsb, L, uo,
+                                (kc % kWinStages) * 8, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sp.empty[rg.stage]);
+    if (++rg.stage == lay.stages) { rg.stage = 0; rg.phase ^= 1; }
+    if ((kc % kWinStages) == kWinStages - 1 || kc == it.nst - 1) {
+      if (lane == 0) mbar_arrive(&sp.wempty[rg.wcnt & 1u]);
+      ++rg.wcnt;
+      wsb = sp.win + (rg.wcnt & 1u) * lay.win_bytes;
     }
   }
+  return true;
+}
+
+template <int NT>
+__device__ __forceinline__ bool run_shared(const SmemPtrs& sp, const StreamLayout& lay, Ring& rg,
+                                        const Item& it, const Lane& L, const UserOffs& uo,
+                                        int eh, uint64_t budget_ns, float (&acc)[2][4]) {
+  const int lane = threadIdx.x & 31;
+  const bool last_has_k = (it.nst - 1) * kChunkBF + (kChunkBF / 2) * eh < it.K;
+  for (int kc = 0; kc < it.nst; ++kc) {
+    if (kc > 0 && !mbar_wait(&sp.full[rg.stage], rg.phase, budget_ns)) return false;
+    if (kc < it.nst - 1 || last_has_k)
+      stage_shared<NT>(sp.stages + rg.stage * lay.stage_bytes, L, uo, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sp.empty[rg.stage]);
+    if (++rg.stage == lay.stages) { rg.stage = 0; rg.phase ^= 1; }
+  }
+  return true;
 }
 
 // --------------------------------------------------------------------- epilogue ----
@@ -689,23 +734,15 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   const int g = lane >> 2, t = lane & 3;
   const int eh = cw >> 3;  // this warp's K half
   const Lane L = make_lane(PHASE == 0, cw, g, t, spitch);
-  int stage = 0;
-  uint32_t phase = 0;
-  uint32_t wcnt = 0, rc = 0;
-  int cur = -1;
-  Item it;
-  it.kind = 0; it.nst = 1; it.U = 1; it.K = 0; it.out0 = 0; it.u0 = 0; it.row0 = 0; it.row1 = 0;
-  UserOffs uo;
-  int NT = 1;
-  bool routed = false;
-  float acc[2][4];
+  Ring rg;
+  rg.stage = 0;
+  rg.phase = 0;
+  rg.wcnt = 0;
+  uint32_t rc = 0;
+  bool ok = true;
   for (;;) {
-    if (!mbar_wait(&sp.full[stage], phase, budget_ns)) {
-      if (lane == 0) set_status(s.status, kStatusTimeout);
-      break;
-    }
-    const int2 inf = sp.info[stage];
-    const int item = inf.x, kc = inf.y;
+    if (!mbar_wait(&sp.full[rg.stage], rg.phase, budget_ns)) { ok = false; break; }
+    const int item = sp.info[rg.stage].x;
     if (item < 0) {
       // end of work: hand the epilogue the end marker through the next reduction slot
       const uint32_t rb = rc & 1u;
@@ -713,69 +750,51 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
         if (cw == 0 && lane == 0) sp.rinfo[rb] = -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sp.rfull[rb]);
-      } else if (lane == 0) {
-        set_status(s.status, kStatusTimeout);
+      } else {
+        ok = false;
       }
       break;
     }
-    if (item != cur) {
-      cur = item;
-      it = decode_item(PHASE, item, dm, tb, D);
-      routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
-      NT = it.U > 8 ? 2 : 1;
+    const Item it = decode_item(PHASE, item, dm, tb, D);
+    const int NT = it.U > 8 ? 2 : 1;
+    UserOffs uo;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int n = min(nt * 8 + g, it.U - 1);  // B column of this lane (clamped)
-        if (it.kind == kRoutedGU)
-          uo.act[nt] = kStageW + (tb.users[it.u0 + n] / dm.k) * kActPitch + eh * 256 + 16 * t;
-        else if (it.kind == kRoutedDN)
-          uo.act[nt] = kStageW + n * kActPitch + eh * 256 + 16 * t;
-        else
-          uo.act[nt] = kStageW + swz128_off(n, 2 * t + eh);
-        const int u0c = min(nt * 8 + 2 * t, it.U - 1), u1c = min(nt * 8 + 2 * t + 1, it.U - 1);
-        uo.as0[nt] = kWinW + u0c * apitch + 16 * eh;
-        uo.as1[nt] = kWinW + u1c * apitch + 16 * eh;
+    for (int nt = 0; nt < 2; ++nt) {
+      const int n = min(nt * 8 + g, it.U - 1);  // B column of this lane (clamped)
+      if (it.kind == kRoutedGU)
+        uo.act[nt] = kStageW + (tb.users[it.u0 + n] / dm.k) * kActPitch + eh * 256 + 16 * t;
+      else if (it.kind == kRoutedDN)
+        uo.act[nt] = kStageW + n * kActPitch + eh * 256 + 16 * t;
+      else
+        uo.act[nt] = kStageW + swz128_off(n, 2 * t + eh);
+      const int u0c = min(nt * 8 + 2 * t, it.U - 1), u1c = min(nt * 8 + 2 * t + 1, it.U - 1);
+      uo.as0[nt] = kWinW + u0c * apitch + 16 * eh;
+      uo.as1[nt] = kWinW + u1c * apitch + 16 * eh;
+    }
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
+      ok = (NT == 1) ? run_routed<PHASE == 0, 1>(sp, lay, rg, it, L, uo, eh, budget_ns, acc)
+                     : run_routed<PHASE == 0, 2>(sp, lay, rg, it, L, uo, eh, budget_ns, acc);
+    } else {
+      ok = (NT == 1) ? run_shared<1>(sp, lay, rg, it, L, uo, eh, budget_ns, acc)
+                     : run_shared<2>(sp, lay, rg, it, L, uo, eh, budget_ns, acc);
+    }
+    if (!ok) break;
+    // item end: partial sums to the next reduction slot, then on to the next item
+    const uint32_t rb = rc & 1u;
+    if (!mbar_wait(&sp.rempty[rb], ((rc >> 1) & 1u) ^ 1u, budget_ns)) { ok = false; break; }
+    float4* red = sp.red + rb * (kConsumerWarps * lay.nt_max * 32);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
-      }
-    }
-    const uint8_t* st = sp.stages + stage * lay.stage_bytes;
-    if (routed) {
-      const uint8_t* wsb = sp.win + (wcnt & 1u) * lay.win_bytes;
-      if (kc * kChunkF4 + (kChunkF4 / 2) * eh < it.K) {
-        const int sblk = (kc % kWinStages) * 8;
-        if (PHASE == 0) stage_routed<true>(st, wsb, L, uo, NT, sblk, acc);
-        else stage_routed<false>(st, wsb, L, uo, NT, sblk, acc);
-      }
-    } else if (kc * kChunkBF + (kChunkBF / 2) * eh < it.K) {
-      stage_shared(st, L, uo, NT, acc);
-    }
+    for (int nt = 0; nt < 2; ++nt)
+      if (nt < NT)
+        red[(cw * lay.nt_max + nt) * 32 + lane] =
+            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+    if (cw == 0 && lane == 0) sp.rinfo[rb] = item;
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sp.empty[stage]);
-    if (++stage == S) { stage = 0; phase ^= 1; }
-    if (routed && ((kc % kWinStages) == kWinStages - 1 || kc == it.nst - 1)) {
-      if (lane == 0) mbar_arrive(&sp.wempty[wcnt & 1u]);
-      ++wcnt;
-    }
-    if (kc == it.nst - 1) {
-      // item end: partial sums to the next reduction slot, then on to the next item
-      const uint32_t rb = rc & 1u;
-      if (!mbar_wait(&sp.rempty[rb], ((rc >> 1) & 1u) ^ 1u, budget_ns)) {
-        if (lane == 0) set_status(s.status, kStatusTimeout);
-        break;
-      }
-      float4* red = sp.red + rb * (kConsumerWarps * lay.nt_max * 32);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-        if (nt < NT)
-          red[(cw * lay.nt_max + nt) * 32 + lane] =
-              make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-      if (cw == 0 && lane == 0) sp.rinfo[rb] = item;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sp.rfull[rb]);
-      ++rc;
-    }
+    if (lane == 0) mbar_arrive(&sp.rfull[rb]);
+    ++rc;
   }
+  if (!ok && lane == 0) set_status(s.status, kStatusTimeout);
 }
 
 // Opt the streaming kernels in to the largest shared-memory size (once per process and
