@@ -697,6 +697,7 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
     s.counters[kCtrFrontTicket] = 0u;
     s.counters[kCtrGateUp] = 0u;
     s.counters[kCtrDown] = 0u;
+    s.counters[kCtrMidScaled] = 0u;
   }
 }
 

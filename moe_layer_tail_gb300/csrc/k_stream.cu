@@ -319,14 +319,14 @@ struct UserOffs {
 // k16 products are scaled by the row's E8M0 scale (and, for down, the user's block scale)
 // and added to the fp32 accumulators.  `sblk` = byte offset of this warp's first block in
 // the window rows; `wsb` = the window slot.
-template <bool GATE_UP, int NT>
+template <bool GATE_UP, int NT, bool ACT_SCALED>
 __device__ __forceinline__ void stage_routed(const uint8_t* st, const uint8_t* wsb,
                                              const Lane& L, const UserOffs& uo, int sblk,
                                              float (&acc)[2][4]) {
   const uint32_t swa = *reinterpret_cast<const uint32_t*>(wsb + L.scale_a + sblk);
   const uint32_t swb = *reinterpret_cast<const uint32_t*>(wsb + L.scale_b + sblk);
   float4 as0[NT], as1[NT];  // down: block scales of users (2t, 2t+1), per N-tile
-  if (!GATE_UP) {
+  if (!GATE_UP && ACT_SCALED) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       as0[nt] = *reinterpret_cast<const float4*>(wsb + uo.as0[nt] + 4 * sblk);
@@ -347,7 +347,7 @@ __device__ __forceinline__ void stage_routed(const uint8_t* st, const uint8_t* w
       float tmp[4];
       mma_f16_z(tmp, ha[0], hb[0], ha[1], hb[1], b.x, b.y);
       mma_f16(tmp, ha[2], hb[2], ha[3], hb[3], b.z, b.w);
-      if (GATE_UP) {
+      if (GATE_UP || !ACT_SCALED) {
         acc[nt][0] += tmp[0] * sa;
         acc[nt][1] += tmp[1] * sa;
         acc[nt][2] += tmp[2] * sb;
@@ -388,7 +388,7 @@ struct Ring {
 
 // All stages of one item for one consumer warp; the item's first stage has already been
 // waited for.  Returns false when a wait ran out of budget.
-template <bool GATE_UP, int NT>
+template <bool GATE_UP, int NT, bool ACT_SCALED>
 __device__ __forceinline__ bool run_routed(const SmemPtrs& sp, const StreamLayout& lay, Ring& rg,
                                         const Item& it, const Lane& L, const UserOffs& uo,
                                         int eh, uint64_t budget_ns, float (&acc)[2][4]) {
@@ -399,7 +399,7 @@ __device__ __forceinline__ bool run_routed(const SmemPtrs& sp, const StreamLayou
   for (int kc = 0; kc < it.nst; ++kc) {
     if (kc > 0 && !mbar_wait(&sp.full[rg.stage], rg.phase, budget_ns)) return false;
     if (kc < it.nst - 1 || last_has_k)
-      stage_routed<GATE_UP, NT>(sp.stages + rg.stage * lay.stage_bytes, wsb, L, uo,
+      stage_routed<GATE_UP, NT, ACT_SCALED>(sp.stages + rg.stage * lay.stage_bytes, wsb, L, uo,
                                 (kc % kWinStages) * 8, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sp.empty[rg.stage]);
@@ -513,10 +513,16 @@ __device__ __forceinline__ void finish_item(const Item& it, const float4* rb, in
           amax[q] = fmaxf(amax[q], __shfl_xor_sync(0xffffffffu, amax[q], 16));
           const int u = nt * 8 + 2 * t + q;
           if (u < it.U) {
+            // blocks whose largest magnitude lies in [2^-10, 2^15) are stored unscaled: f16
+            // holds their bf16 values exactly down to 2^-14 and the smaller ones within 2^-25;
+            // any other block gets a power of two and marks the call as scaled
             int p = 0;
             if (amax[q] > 0.f) {
               const int ex = (int)((__float_as_uint(amax[q]) >> 23) & 0xFF) - 127;
-              p = max(-100, min(100, ex - 14));
+              if (ex < -10 || ex > 14) {
+                p = max(-100, min(100, ex - 14));
+                if (g == 0) atomicOr(&s.counters[kCtrMidScaled], 1u);
+              }
             }
             const float down = __uint_as_float((uint32_t)(127 - p) << 23);
             const size_t slot = (size_t)(it.u0 + u);
@@ -566,6 +572,8 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   }
   pdl_wait();
   const int D = min(max(*s.n_distinct, 1), kMaxPicks);
+  // down: whether any block of mid carries a scale (else its f16 values are the values)
+  const bool mid_scaled = (PHASE == 1) && (*(volatile const uint32_t*)&s.counters[kCtrMidScaled] != 0u);
   const int n_items = items_of(PHASE, dm, D);
   for (int i = threadIdx.x; i < D; i += kStreamThreads) sp.t_uniq[i] = s.uniq[i];
   for (int i = threadIdx.x; i <= D; i += kStreamThreads) sp.t_off[i] = s.user_off[i];
@@ -773,8 +781,12 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
-      ok = (NT == 1) ? run_routed<PHASE == 0, 1>(sp, lay, rg, it, L, uo, eh, budget_ns, acc)
-                     : run_routed<PHASE == 0, 2>(sp, lay, rg, it, L, uo, eh, budget_ns, acc);
+      if (PHASE == 0 || !mid_scaled)
+        ok = (NT == 1) ? run_routed<PHASE == 0, 1, false>(sp, lay, rg, it, L, uo, eh, budget_ns, acc)
+                       : run_routed<PHASE == 0, 2, false>(sp, lay, rg, it, L, uo, eh, budget_ns, acc);
+      else
+        ok = (NT == 1) ? run_routed<false, 1, true>(sp, lay, rg, it, L, uo, eh, budget_ns, acc)
+                       : run_routed<false, 2, true>(sp, lay, rg, it, L, uo, eh, budget_ns, acc);
     } else {
       ok = (NT == 1) ? run_shared<1>(sp, lay, rg, it, L, uo, eh, budget_ns, acc)
                      : run_shared<2>(sp, lay, rg, it, L, uo, eh, budget_ns, acc);

@@ -59,7 +59,8 @@ struct Scratch {
   int32_t* user_off;     // [Rmax*k + 1] CSR offsets into user_list
   int32_t* user_list;    // [Rmax*k] pick indices r*k + slot, in (r, slot) order
   __nv_bfloat16* mid;    // [Rmax*k, I] SiLU(gate)*up of each pick (bf16)
-  __half* mid16;         // [Rmax*k, I] mid as f16, scaled by 2^-p per 32-element block;
+  __half* mid16;         // [Rmax*k, I] mid as f16 (unscaled, or scaled by 2^-p per 32-element
+                         // block where its largest magnitude leaves [2^-10, 2^15));
                          // row = the pick's position in user_list (users of an expert adjacent)
   float* mid16s;         // [Rmax*k, I/32] the 2^p of each block, same rows
   __nv_bfloat16* ms;     // [Rmax, Is] shared-expert intermediate (bf16)
@@ -73,7 +74,7 @@ struct Scratch {
 constexpr uint32_t kDebugStallFirstStage = 4u;
 
 // counters[] slots
-enum : int { kCtrGateUp = 0, kCtrDown = 1, kCtrFrontTicket = 2 };
+enum : int { kCtrGateUp = 0, kCtrDown = 1, kCtrFrontTicket = 2, kCtrMidScaled = 3 };
 
 // ------------------------------------------------------------------ device helpers ----
 

@@ -122,6 +122,16 @@ def test_repeated_experts_and_dedup_count(flags):
     assert nd == len(np.unique(orc["ids"])) < shape.R * shape.k
 
 
+@pytest.mark.parametrize("shift", [12, -16])
+def test_mid_outside_f16_range_takes_block_scales(shift):
+    """SiLU*up values far above (gate/up E8M0 scales x 2^12) or below (x 2^-16) the f16 range
+    make the gate/up epilogue store mid with per-block powers of two, and the down launch
+    apply them; the result still matches the oracle."""
+    shape, d = _small(15, R=4, H=512, E=10, k=3, I=256, Is=128)
+    d["w13_scales"] = (d["w13_scales"].astype(np.int32) + shift).astype(np.uint8)
+    _check_small(shape, d)
+
+
 def test_identical_experts_output_independent_of_routing():
     shape, d = _small(8, R=4, E=6, k=2)
     for key in ("w13_codes", "w13_scales", "w2_codes", "w2_scales"):
