@@ -199,6 +199,13 @@ __device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// Four 8x8 b16 matrices from shared memory: lane i gives the address of row i & 7 of matrix
+// i >> 3; lane l receives word l & 3 of row l >> 2 of each matrix.
+__device__ __forceinline__ void ldsm_x4(const void* p, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
 // d = A * B for one m16n8k16 f16 product (no accumulator input).
 __device__ __forceinline__ void mma_f16_z(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -273,33 +280,34 @@ __device__ __forceinline__ SmemPtrs carve_smem(uint8_t* smem, const StreamLayout
 // Per-lane shared-memory offsets fixed for the kernel: warp c works on MMA tile m = c & 7
 // and on half h = c >> 3 of every stage's K range.
 struct Lane {
-  // routed (MXFP4): word t of block chunk 4h + c, A rows a (MMA rows 0-7) and b (8-15)
-  int code_a[4], code_b[4];
+  // routed (MXFP4): this lane's row address for the two ldmatrix.x4 loads of a stage; load
+  // p returns word t of block chunks 4h + 2p and 4h + 2p + 1 of A rows a (MMA rows 0-7)
+  // and b (8-15) as {a, b, a', b'}
+  int ldsm[2];
   // routed: the rows' E8M0 bytes inside a scale window (add the block offset)
   int scale_a, scale_b;
   // shared (bf16): chunk 2t + h of A rows a and b
   int bw_a, bw_b;
 };
 
-__device__ __forceinline__ Lane make_lane(bool gate_up, int cw, int g, int t, int spitch) {
+__device__ __forceinline__ Lane make_lane(bool gate_up, int cw, int lane, int spitch) {
   Lane L;
   const int m = cw & 7, h = cw >> 3;
-  int ra, rb, boxb, sb0;
-  if (gate_up) {  // gate box rows 8m+g (A rows 0-7), up box rows 8m+g (A rows 8-15)
-    ra = 8 * m + g;
-    rb = ra;
-    boxb = 8192;
-    sb0 = 4096;
-  } else {        // one 128-row box: rows 16m+g and 16m+g+8
-    ra = 16 * m + g;
-    rb = ra + 8;
-    boxb = 0;
-    sb0 = 0;
-  }
+  const int g = lane >> 2, t = lane & 3;
+  // A rows a and b of MMA row r (0-7): gate/up -- gate box rows 8m+r and up box rows 8m+r;
+  // down -- one 128-row box, rows 16m+r and 16m+r+8
+  const int abase = gate_up ? 8 * m : 16 * m;
+  const int bbase = gate_up ? 8 * m : 16 * m + 8;
+  const int boxb = gate_up ? 8192 : 0;
+  const int sb0 = gate_up ? 4096 : 0;
+  const int ra = abase + g, rb = bbase + g;
+  {
+    // ldmatrix: lane i addresses row i & 7 of matrix i >> 3 (a, b, a', b')
+    const int j = lane >> 3, r = lane & 7;
+    const int row = (j & 1) ? bbase + r : abase + r;
+    const int box = (j & 1) ? boxb : 0;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    L.code_a[c] = swz128_off(ra, 4 * h + c) + 4 * t;
-    L.code_b[c] = boxb + swz128_off(rb, 4 * h + c) + 4 * t;
+    for (int p = 0; p < 2; ++p) L.ldsm[p] = box + swz128_off(row, 4 * h + 2 * p + (j >> 1));
   }
   L.scale_a = ra * spitch + 4 * h;
   L.scale_b = sb0 + rb * spitch + 4 * h;
@@ -333,10 +341,13 @@ __device__ __forceinline__ void stage_routed(const uint8_t* st, const uint8_t* w
       as1[nt] = *reinterpret_cast<const float4*>(wsb + uo.as1[nt] + 4 * sblk);
     }
   }
+  uint32_t code[2][4];
+#pragma unroll
+  for (int p = 0; p < 2; ++p) ldsm_x4(st + L.ldsm[p], code[p]);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const uint32_t wa = *reinterpret_cast<const uint32_t*>(st + L.code_a[c]);
-    const uint32_t wb = *reinterpret_cast<const uint32_t*>(st + L.code_b[c]);
+    const uint32_t wa = code[c >> 1][2 * (c & 1)];
+    const uint32_t wb = code[c >> 1][2 * (c & 1) + 1];
     uint32_t ha[4], hb[4];
     e2m1x8_to_f16x2(wa, ha[0], ha[1], ha[2], ha[3]);
     e2m1x8_to_f16x2(wb, hb[0], hb[1], hb[2], hb[3]);
@@ -741,7 +752,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   const int cw = warp - 2;
   const int g = lane >> 2, t = lane & 3;
   const int eh = cw >> 3;  // this warp's K half
-  const Lane L = make_lane(PHASE == 0, cw, g, t, spitch);
+  const Lane L = make_lane(PHASE == 0, cw, lane, spitch);
   Ring rg;
   rg.stage = 0;
   rg.phase = 0;

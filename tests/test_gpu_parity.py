@@ -105,6 +105,7 @@ def _check_small(shape, d, max_rows=None, rows=None, flags=0):
     (2, 512, 12, 3, 256, 192),     # several tiles, ragged tails
     (5, 768, 33, 7, 384, 320),     # odd expert count, k not a power of two
     (3, 2560, 6, 2, 2560, 192),    # several E8M0 windows per row, the last one ragged
+    (16, 3072, 2, 2, 128, 64),     # 16 users of each expert (two N-tiles), long K
     (16, 256, 16, 16, 128, 128),   # k = E: every expert, maximum rows
     (16, 512, 64, 1, 256, 64),     # k = 1, maximum rows
     (4, 1024, 40, 32, 128, 256),   # k at its maximum
