@@ -226,6 +226,62 @@ __device__ __forceinline__ float load_logit(const float* l) {
   else return __ldcg(l);
 }
 
+// The k largest logits of one row, for one warp: lane i < k returns pick i (value, id), in
+// descending order, ties to the lower id.  The row's logits sit lane-strided in registers
+// (Q slots per lane, Q * 32 >= E); each lane keeps its best untaken candidate, so after a
+// pick only the lane that owned it looks at its slots again.  If only NaN candidates are
+// left, the lowest untaken id is taken and the status flags the routing.
+template <bool kSmem, int Q>
+__device__ __forceinline__ void topk_row(const float* l, int E, int k, int32_t* status,
+                                         float& pv, int& pe) {
+  const int lane = threadIdx.x & 31;
+  float lv[Q];
+  uint32_t tk = 0u;  // bit q: slot q taken (or past E)
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    const int e = lane + 32 * q;
+    lv[q] = (e < E) ? load_logit<kSmem>(l + e) : -INFINITY;
+    if (e >= E) tk |= 1u << q;
+  }
+  float bv = -INFINITY;  // this lane's best untaken candidate
+  int be = 0x7fffffff;
+#pragma unroll
+  for (int q = 0; q < Q; ++q)
+    if (!((tk >> q) & 1u) && better(lv[q], lane + 32 * q, bv, be)) { bv = lv[q]; be = lane + 32 * q; }
+  pv = 0.f;
+  pe = 0;
+  for (int i = 0; i < k; ++i) {
+    float wv = bv;
+    int we = be;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, we, o);
+      if (better(ov, oe, wv, we)) { wv = ov; we = oe; }
+    }
+    if (we >= E) {  // only NaN candidates left: take the lowest untaken id, flag it
+      int fe = 0x7fffffff;
+#pragma unroll
+      for (int q = Q - 1; q >= 0; --q)
+        if (!((tk >> q) & 1u)) fe = lane + 32 * q;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) fe = min(fe, __shfl_xor_sync(0xffffffffu, fe, o));
+      we = min(fe, E - 1);
+      wv = load_logit<kSmem>(l + we);
+      if (lane == 0) set_status(status, kStatusBadRouting);
+    }
+    if ((we & 31) == lane) {
+      tk |= 1u << (we >> 5);
+      bv = -INFINITY;
+      be = 0x7fffffff;
+#pragma unroll
+      for (int q = 0; q < Q; ++q)
+        if (!((tk >> q) & 1u) && better(lv[q], lane + 32 * q, bv, be)) { bv = lv[q]; be = lane + 32 * q; }
+    }
+    if (lane == i) { pv = wv; pe = we; }
+  }
+}
+
 template <bool kSmem>
 __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
                                  int32_t* n_distinct, int32_t* uniq, int32_t* user_off,
@@ -237,48 +293,18 @@ __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
-  for (int e = tid; e < kMaxExperts; e += nthreads) rowmask[e] = 0u;
+  for (int e = tid; e < E; e += nthreads) rowmask[e] = 0u;
 
   for (int row = warp; row < R; row += nwarps) {
     const float* l = logits + (size_t)row * E;
-    // the row's logits, lane-strided, in registers (E <= 1024: up to 32 per lane); bit q of
-    // `tk` marks candidate lane + 32 q as taken (or past E)
-    float lv[kMaxExperts / 32];
-    uint32_t tk = 0u;
-#pragma unroll
-    for (int q = 0; q < kMaxExperts / 32; ++q) {
-      const int e = lane + 32 * q;
-      lv[q] = (e < E) ? load_logit<kSmem>(l + e) : -INFINITY;
-      if (e >= E) tk |= 1u << q;
-    }
-    float pv = 0.f;  // lane i < k keeps pick i
-    int pe = 0;
-    for (int i = 0; i < k; ++i) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int q = 0; q < kMaxExperts / 32; ++q)
-        if (!((tk >> q) & 1u) && better(lv[q], lane + 32 * q, bv, be)) { bv = lv[q]; be = lane + 32 * q; }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
-      }
-      if (be >= E) {  // only NaN candidates left: take the lowest untaken id, flag it
-        int fe = 0x7fffffff;
-#pragma unroll
-        for (int q = kMaxExperts / 32 - 1; q >= 0; --q)
-          if (!((tk >> q) & 1u)) fe = lane + 32 * q;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) fe = min(fe, __shfl_xor_sync(0xffffffffu, fe, o));
-        be = min(fe, E - 1);
-        bv = load_logit<kSmem>(l + be);
-        if (lane == 0) set_status(status, kStatusBadRouting);
-      }
-      if ((be & 31) == lane) tk |= 1u << (be >> 5);
-      if (lane == i) { pv = bv; pe = be; }
-    }
+    float pv;  // lane i < k keeps pick i
+    int pe;
+    if (E <= 32) topk_row<kSmem, 1>(l, E, k, status, pv, pe);
+    else if (E <= 64) topk_row<kSmem, 2>(l, E, k, status, pv, pe);
+    else if (E <= 128) topk_row<kSmem, 4>(l, E, k, status, pv, pe);
+    else if (E <= 256) topk_row<kSmem, 8>(l, E, k, status, pv, pe);
+    else if (E <= 512) topk_row<kSmem, 16>(l, E, k, status, pv, pe);
+    else topk_row<kSmem, kMaxExperts / 32>(l, E, k, status, pv, pe);
     // weights: softmax of the picked logits (lane i holds pick i; pick 0 is the largest)
     const float m = __shfl_sync(0xffffffffu, pv, 0);
     const float ex = (lane < k) ? expf(pv - m) : 0.f;
@@ -294,7 +320,7 @@ __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
   __syncthreads();
   // exclusive scans over experts of (used ? 1 : 0) and popc(rowmask): each thread owns
   // `per` consecutive experts; warp scan, then warp totals in warp order
-  const int per = (kMaxExperts + nthreads - 1) / nthreads;
+  const int per = (E + nthreads - 1) / nthreads;
   const int e0 = tid * per;
   int cd = 0, cu = 0;
   for (int q = 0; q < per; ++q) {
@@ -489,27 +515,27 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   if (!s_last) return;
   __threadfence();
   // logits = the parts added in part order, into shared memory (the staged tiles are no
-  // longer needed); eight sums in flight per thread
+  // longer needed); every part of four logits per thread is loaded before any is added
   float* s_logits = reinterpret_cast<float*>(sm);
   const int RE = R * E;
-  for (int base = 0; base < RE; base += 8 * kRtThreads) {
-    float v[8];
+  constexpr int kJ = 4;
+  for (int base = 0; base < RE; base += kJ * kRtThreads) {
+    float v[kRtMaxParts][kJ];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = base + tid + j * kRtThreads;
-      v[j] = (i < RE) ? __ldcg(s.logit_parts + i) : 0.f;
-    }
-    for (int pp = 1; pp < P; ++pp) {
+    for (int pp = 0; pp < kRtMaxParts; ++pp)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kJ; ++j) {
         const int i = base + tid + j * kRtThreads;
-        if (i < RE) v[j] += __ldcg(s.logit_parts + (size_t)pp * RE + i);
+        v[pp][j] = (pp < P && i < RE) ? __ldcg(s.logit_parts + (size_t)pp * RE + i) : 0.f;
       }
-    }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kJ; ++j) {
+      float sum = v[0][j];
+#pragma unroll
+      for (int pp = 1; pp < kRtMaxParts; ++pp)
+        if (pp < P) sum += v[pp][j];
       const int i = base + tid + j * kRtThreads;
-      if (i < RE) s_logits[i] = v[j];
+      if (i < RE) s_logits[i] = sum;
     }
   }
   __syncthreads();

@@ -23,15 +23,16 @@
 //     E8M0 weight scales (and, for down, the activation block scales) of the next 2048 K
 //     elements into a separate two-slot window ring.  Nothing but TMA issue and mbarrier
 //     bookkeeping runs on this thread, so a stage costs it a few hundred cycles at most;
-//   * warps 2..17 -- 16 consumer warps: warp c works on MMA tile m = c & 7 (16 weight rows)
+//   * warps 3..18 -- 16 consumer warps: warp c works on MMA tile m = c & 7 (16 weight rows)
 //     and half h = c >> 3 of every stage's K range.  MXFP4 bytes go through
 //     cvt.rn.f16x2.e2m1x2 straight into mma.m16n8k16 A fragments (weights = M rows, users =
 //     N columns), each 32-element block's product is scaled by its E8M0 scale (times the
 //     activation block scale for down) and accumulated in fp32; the shared expert is
 //     bf16 x bf16 into fp32.  At the end of an item each warp drops its partial sums into a
 //     reduction slot and moves on -- no consumer ever waits for another consumer;
-//   * warp 1 -- the epilogue: adds the two K halves of every tile in a fixed order and
-//     finishes the item (SiLU*up, the f16 copy of mid with its block scales, stores).
+//   * warps 1 and 2 -- the epilogue, taking items in turn: adds the two K halves of every
+//     tile in a fixed order and finishes the item (SiLU*up, the f16 copy of mid with its
+//     block scales, stores).
 //   * activations enter the routed contractions as f16 with power-of-two scales (one per row
 //     for gate/up, applied in the epilogue; one per 32-element block for down, applied per
 //     block), exact for bf16 values in range;
@@ -44,7 +45,8 @@
 namespace mtail {
 
 constexpr int kConsumerWarps = 16;
-constexpr int kStreamThreads = (kConsumerWarps + 2) * 32;
+constexpr int kEpilogueWarps = 2;  // one per reduction slot
+constexpr int kStreamThreads = (1 + kEpilogueWarps + kConsumerWarps) * 32;
 constexpr int kChunkF4 = 256;     // MXFP4 elements per stage row (128 bytes)
 constexpr int kChunkBF = 64;      // bf16 elements per stage row (128 bytes)
 constexpr int kStageW = 16384;    // 128 weight rows x 128 bytes
@@ -729,9 +731,10 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     return;
   }
 
-  if (warp == 1) {
+  if (warp <= kEpilogueWarps) {
     // ---------------------------------------------------------------- epilogue ----
-    for (uint32_t rc = 0;; ++rc) {
+    // epilogue warp w finishes the items of reduction slot w - 1 (every other item)
+    for (uint32_t rc = (uint32_t)(warp - 1);; rc += kEpilogueWarps) {
       const uint32_t rb = rc & 1u;
       if (!mbar_wait(&sp.rfull[rb], (rc >> 1) & 1u, budget_ns)) {
         if (lane == 0) set_status(s.status, kStatusTimeout);
@@ -749,7 +752,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   }
 
   // ------------------------------------------------------------------ consumers ----
-  const int cw = warp - 2;
+  const int cw = warp - 1 - kEpilogueWarps;
   const int g = lane >> 2, t = lane & 3;
   const int eh = cw >> 3;  // this warp's K half
   const Lane L = make_lane(PHASE == 0, cw, lane, spitch);
@@ -763,14 +766,16 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     if (!mbar_wait(&sp.full[rg.stage], rg.phase, budget_ns)) { ok = false; break; }
     const int item = sp.info[rg.stage].x;
     if (item < 0) {
-      // end of work: hand the epilogue the end marker through the next reduction slot
-      const uint32_t rb = rc & 1u;
-      if (mbar_wait(&sp.rempty[rb], ((rc >> 1) & 1u) ^ 1u, budget_ns)) {
-        if (cw == 0 && lane == 0) sp.rinfo[rb] = -1;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sp.rfull[rb]);
-      } else {
-        ok = false;
+      // end of work: hand each epilogue warp the end marker through its next reduction slot
+      for (int q = 0; q < kEpilogueWarps && ok; ++q, ++rc) {
+        const uint32_t rb = rc & 1u;
+        if (mbar_wait(&sp.rempty[rb], ((rc >> 1) & 1u) ^ 1u, budget_ns)) {
+          if (cw == 0 && lane == 0) sp.rinfo[rb] = -1;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sp.rfull[rb]);
+        } else {
+          ok = false;
+        }
       }
       break;
     }

@@ -108,7 +108,9 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+// SiLU in fp32 with the fast exponential and division (a few ulp; mid is rounded to bf16
+// right after).
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bit) {
   atomicOr(reinterpret_cast<int*>(status), bit);
