@@ -59,6 +59,19 @@ enum {
   MOE_TAIL_MODE_PERSISTENT = 1     /* reserved: one resident launch with in-kernel flags */
 };
 
+/* Bits of the device status word read by moe_tail_get_status (sticky until cleared). */
+enum {
+  /* A row's top-k found no number among its remaining logits (NaN router output): the
+   * lowest untaken expert ids were picked for it. */
+  MOE_TAIL_STATUS_BAD_ROUTING = 1,
+  /* The distinct-expert count of a call fell outside [1, rows * top_k]. */
+  MOE_TAIL_STATUS_BAD_DISTINCT = 2,
+  /* A device-side wait ran past its budget; the kernel let its copies land and returned. */
+  MOE_TAIL_STATUS_TIMEOUT = 4,
+  /* A work item outside its matrix (or a misaligned shared-memory base) was skipped. */
+  MOE_TAIL_STATUS_BAD_TILE = 8
+};
+
 /* debug_flags bits. */
 enum {
   /* Run the expert stages with the warp-per-row CUDA-core kernels instead of the
@@ -69,7 +82,7 @@ enum {
   MOE_TAIL_DEBUG_NO_PDL = 2,
   /* Failure injection for tests: in the gate/up launch, the first CTA's producer leaves its
    * first pipeline stage unpublished, so that the consumers' bounded wait expires; the
-   * kernel records MOE_TAIL_ERR_TIMEOUT in the status word and returns.  The output of
+   * kernel sets MOE_TAIL_STATUS_TIMEOUT in the status word and returns.  The output of
    * such a call is not meaningful. */
   MOE_TAIL_DEBUG_STALL_FIRST_STAGE = 4,
   /* Run the front (add + RMSNorm, router, top-k, dedup) as one launch in which every CTA

@@ -23,6 +23,12 @@ ERR_TIMEOUT = -4
 ERR_NOT_CORESIDENT = -5
 ERR_DEVICE = -6
 
+# bits of the device status word (moe_tail_get_status)
+STATUS_BAD_ROUTING = 1
+STATUS_BAD_DISTINCT = 2
+STATUS_TIMEOUT = 4
+STATUS_BAD_TILE = 8
+
 MODE_MULTI_KERNEL = 0
 MODE_PERSISTENT = 1
 

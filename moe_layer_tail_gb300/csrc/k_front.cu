@@ -226,59 +226,55 @@ __device__ __forceinline__ float load_logit(const float* l) {
   else return __ldcg(l);
 }
 
+// Order-preserving 32-bit key of a logit: larger value <=> larger key, +0 and -0 equal; 0
+// marks NaN (below every number, -inf included).  key_value inverts it (0 -> NaN).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (v != v) return 0u;
+  const uint32_t b = __float_as_uint(v + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 // The k largest logits of one row, for one warp: lane i < k returns pick i (value, id), in
-// descending order, ties to the lower id.  The row's logits sit lane-strided in registers
-// (Q slots per lane, Q * 32 >= E); each lane keeps its best untaken candidate, so after a
-// pick only the lane that owned it looks at its slots again.  If only NaN candidates are
-// left, the lowest untaken id is taken and the status flags the routing.
+// descending order, ties to the lower id.  The row's keys sit lane-strided in registers (Q
+// slots per lane, Q * 32 >= E); each lane keeps its best untaken candidate, a pick is one
+// warp max over the lanes' best keys and one warp min over the ids holding it, and only the
+// lane that owned the pick looks at its slots again.  If only NaN candidates are left the
+// lowest untaken id is taken and the status flags the routing.
 template <bool kSmem, int Q>
 __device__ __forceinline__ void topk_row(const float* l, int E, int k, int32_t* status,
                                          float& pv, int& pe) {
   const int lane = threadIdx.x & 31;
-  float lv[Q];
+  uint32_t key[Q];
   uint32_t tk = 0u;  // bit q: slot q taken (or past E)
 #pragma unroll
   for (int q = 0; q < Q; ++q) {
     const int e = lane + 32 * q;
-    lv[q] = (e < E) ? load_logit<kSmem>(l + e) : -INFINITY;
+    key[q] = (e < E) ? order_key(load_logit<kSmem>(l + e)) : 0u;
     if (e >= E) tk |= 1u << q;
   }
-  float bv = -INFINITY;  // this lane's best untaken candidate
-  int be = 0x7fffffff;
+  uint32_t bk = 0u;  // this lane's best untaken candidate (key, id)
+  uint32_t be = 0xffffffffu;
 #pragma unroll
   for (int q = 0; q < Q; ++q)
-    if (!((tk >> q) & 1u) && better(lv[q], lane + 32 * q, bv, be)) { bv = lv[q]; be = lane + 32 * q; }
+    if (!((tk >> q) & 1u) && (key[q] > bk || be == 0xffffffffu)) { bk = key[q]; be = lane + 32 * q; }
   pv = 0.f;
   pe = 0;
   for (int i = 0; i < k; ++i) {
-    float wv = bv;
-    int we = be;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, we, o);
-      if (better(ov, oe, wv, we)) { wv = ov; we = oe; }
-    }
-    if (we >= E) {  // only NaN candidates left: take the lowest untaken id, flag it
-      int fe = 0x7fffffff;
-#pragma unroll
-      for (int q = Q - 1; q >= 0; --q)
-        if (!((tk >> q) & 1u)) fe = lane + 32 * q;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) fe = min(fe, __shfl_xor_sync(0xffffffffu, fe, o));
-      we = min(fe, E - 1);
-      wv = load_logit<kSmem>(l + we);
-      if (lane == 0) set_status(status, kStatusBadRouting);
-    }
-    if ((we & 31) == lane) {
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t we = __reduce_min_sync(0xffffffffu, bk == mk ? be : 0xffffffffu);
+    if (mk == 0u && lane == 0) set_status(status, kStatusBadRouting);
+    if ((int)(we & 31u) == lane) {
       tk |= 1u << (we >> 5);
-      bv = -INFINITY;
-      be = 0x7fffffff;
+      bk = 0u;
+      be = 0xffffffffu;
 #pragma unroll
       for (int q = 0; q < Q; ++q)
-        if (!((tk >> q) & 1u) && better(lv[q], lane + 32 * q, bv, be)) { bv = lv[q]; be = lane + 32 * q; }
+        if (!((tk >> q) & 1u) && (key[q] > bk || be == 0xffffffffu)) { bk = key[q]; be = lane + 32 * q; }
     }
-    if (lane == i) { pv = wv; pe = we; }
+    if (lane == i) { pv = key_value(mk); pe = (int)we; }
   }
 }
 
@@ -460,7 +456,6 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
   pdl_wait();
-  pdl_trigger();
   for (int i = tid; i < R * cpr; i += kRtThreads) {
     const int r = i / cpr, c = i % cpr;
     cp_async16(sn + r * pitch + c * 16, s.n + (size_t)r * H + k0 + c * 8);
@@ -542,6 +537,8 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   topk_dedup_block<true>(s_logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
                          s.user_list, s.status, R, E, k);
   if (tid == 0) s.counters[kCtrFrontTicket] = 0u;
+  pdl_trigger();  // the other CTAs have exited: the expert launch may start (launched any
+                  // earlier, its CTAs would share the SMs with this one's top-k)
 }
 
 cudaError_t launch_router_topk(const Dims& d, const Weights& w, const Scratch& s,

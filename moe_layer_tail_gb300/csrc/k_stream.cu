@@ -570,19 +570,6 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   const int S = lay.stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Before the routing is known: pull this CTA's share of the shared expert's weights into
-  // L2 (they do not depend on any earlier kernel), so their HBM reads overlap the front.
-  if (warp == 0) {
-    const uint8_t* base = (PHASE == 0) ? (const uint8_t*)w.ws13 : (const uint8_t*)w.ws2;
-    const size_t total = (size_t)dm.Is * dm.H * 2 * (PHASE == 0 ? 2 : 1);
-    const size_t per = ((total / gridDim.x) + 4095) & ~(size_t)4095;
-    const size_t beg = (size_t)blockIdx.x * per;
-    const size_t end = min(total, beg + per);
-    for (size_t o = beg + (size_t)lane * 16384; o < end; o += 32 * 16384) {
-      const uint32_t n = (uint32_t)min((size_t)16384, end - o);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(n) : "memory");
-    }
-  }
   pdl_wait();
   const int D = min(max(*s.n_distinct, 1), kMaxPicks);
   // down: whether any block of mid carries a scale (else its f16 values are the values)

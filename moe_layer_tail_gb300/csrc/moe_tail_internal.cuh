@@ -18,9 +18,10 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxPicks = kMaxRows * kMaxTopK;  // (row, slot) pairs of one call
 
-// Device status word bits (sticky; read by moe_tail_get_status).
+// Device status word bits (sticky; read by moe_tail_get_status; the same values as
+// MOE_TAIL_STATUS_* in moe_tail.h).
 enum : int32_t {
-  kStatusBadRouting = 1 << 0,   // top-k found no finite candidate (NaN logits)
+  kStatusBadRouting = 1 << 0,   // top-k found only NaN logits left for a pick
   kStatusBadDistinct = 1 << 1,  // distinct-expert count out of range
   kStatusTimeout = 1 << 2,      // a bounded wait expired
   kStatusBadTile = 1 << 3,      // a work item outside its matrix was skipped

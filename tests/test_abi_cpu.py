@@ -36,6 +36,23 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), "missing export " + n
 
 
+def header_enum_values():
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "moe_tail.h")).read(),
+                 flags=re.S)
+    return {k: int(v) for k, v in re.findall(r"\b(MOE_TAIL_[A-Z0-9_]+)\s*=\s*(-?\d+)", src)}
+
+
+def test_binding_constants_match_header():
+    vals = header_enum_values()
+    for name, v in vals.items():
+        short = name[len("MOE_TAIL_"):]
+        if short.startswith(("ERR_", "STATUS_", "MODE_")) or short == "OK":
+            assert getattr(mt, short) == v, name
+    assert {k for k in vals if k.startswith("MOE_TAIL_STATUS_")} == {
+        "MOE_TAIL_STATUS_BAD_ROUTING", "MOE_TAIL_STATUS_BAD_DISTINCT", "MOE_TAIL_STATUS_TIMEOUT",
+        "MOE_TAIL_STATUS_BAD_TILE"}
+
+
 def test_strerror_covers_codes(lib):
     for code in (0, -1, -2, -3, -4, -5, -6):
         s = lib.moe_tail_strerror(code).decode()

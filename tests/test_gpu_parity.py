@@ -12,8 +12,9 @@ import numpy as np
 import pytest
 
 import oracle
-from moe_layer_tail_gb300 import (ERR_INVALID_ARG, ERR_UNSUPPORTED, MoeTail, MoeTailError,
-                                  acts_to_device, bf16_tensor_to_bits, weights_to_device)
+from moe_layer_tail_gb300 import (ERR_INVALID_ARG, ERR_UNSUPPORTED, STATUS_BAD_ROUTING, MoeTail,
+                                  MoeTailError, acts_to_device, bf16_tensor_to_bits,
+                                  weights_to_device)
 from moe_layer_tail_gb300 import inputs as gen
 from parity import check_parity, inject_near_ties
 
@@ -151,6 +152,26 @@ def test_exact_router_tie_picks_lowest_id():
     tail, dev, orc, (out, res, ids, wts, nd) = _check_small(shape, d)
     assert lo in ids[0] and hi not in ids[0]
     assert lo in orc["ids"][0] and hi not in orc["ids"][0]
+
+
+def test_nan_router_logits_flag_routing():
+    # experts 2..9 get NaN router rows: each row picks the two finite experts by value, then
+    # the lowest NaN id, and the status word records the bad routing
+    shape, d = _small(16, R=2, H=256, E=10, k=3, I=128, Is=64)
+    d["w_r"][2:] = 0x7FC0  # bf16 quiet NaN
+    _, n, _ = oracle.add_rmsnorm(d["x"], d["residual"], d["gamma"], shape.eps)
+    l = oracle.router(n, d["w_r"])
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    tail = MoeTail(shape, dev, max_rows=shape.R)
+    _, _, ids, _, nd = run_gpu(tail, d)
+    for r in range(shape.R):
+        assert sorted(ids[r][:2]) == [0, 1] and ids[r][2] == 2, (r, ids[r])
+        if abs(l[r, 0] - l[r, 1]) > 1e-3:
+            assert ids[r][0] == (0 if l[r, 0] > l[r, 1] else 1), (r, ids[r], l[r, :2])
+    assert nd == 3
+    assert tail.status() & STATUS_BAD_ROUTING
+    tail.clear_status()
+    assert tail.status() == 0
 
 
 def test_rows_below_max_and_batch_invariance():
