@@ -93,7 +93,8 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   for (int c = threadIdx.x; c < ng; c += kNormThreads) s_gamma[c] = __ldg(g4 + c);
   pdl_wait();
   pdl_trigger();
-  if (r == 0 && threadIdx.x < 8) counters[threadIdx.x] = 0u;  // work counters of this call
+  if (r == 0)  // work counters, tickets and per-expert progress of this call
+    for (int i = threadIdx.x; i < kCtrWords; i += kNormThreads) counters[i] = 0u;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * H);
   const uint4* rr = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
   uint4 rn[kNormGroups];
@@ -716,12 +717,8 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   __threadfence();
   topk_dedup_block<false>(s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
                           s.user_list, s.status, R, E, k);
-  if (tid == 0) {
-    s.counters[kCtrFrontTicket] = 0u;
-    s.counters[kCtrGateUp] = 0u;
-    s.counters[kCtrDown] = 0u;
-    s.counters[kCtrMidScaled] = 0u;
-  }
+  // the ticket and the expert launch's counters for this call (every other CTA is done)
+  for (int i = tid; i < kCtrWords; i += kFrontThreads) s.counters[i] = 0u;
 }
 
 cudaError_t launch_front_fused(const Dims& d, const __nv_bfloat16* x,

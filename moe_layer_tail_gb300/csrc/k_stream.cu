@@ -60,6 +60,7 @@ enum : int { kSharedGU = 0, kRoutedGU = 1, kSharedDN = 2, kRoutedDN = 3 };
 
 struct Item {
   int kind;
+  int d;           // routed: the expert's distinct slot (else -1)
   int row0, row1;  // tensor-map rows: gate (or single) box, up box
   int out0;        // first output index (j for gate/up, h for down)
   int K, nst;
@@ -87,6 +88,7 @@ __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
   Item it;
   it.u0 = 0;
   it.row1 = 0;
+  it.d = -1;
   if (phase == 0) {
     const int ns = dm.Is / 64;
     it.K = dm.H;
@@ -102,6 +104,7 @@ __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
       const int d = min(q / per, D - 1);
       const int e = s.uniq[d];
       it.kind = kRoutedGU;
+      it.d = d;
       it.out0 = (q % per) * 64;
       it.row0 = e * 2 * dm.I + it.out0;
       it.row1 = it.row0 + dm.I;
@@ -123,6 +126,7 @@ __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
       const int d = min(q / per, D - 1);
       const int e = s.uniq[d];
       it.kind = kRoutedDN;
+      it.d = d;
       it.K = dm.I;
       it.out0 = (q % per) * 128;
       it.row0 = e * dm.H + it.out0;
@@ -534,7 +538,7 @@ __device__ __forceinline__ void finish_item(const Item& it, const float4* rb, in
               const int ex = (int)((__float_as_uint(amax[q]) >> 23) & 0xFF) - 127;
               if (ex < -10 || ex > 14) {
                 p = max(-100, min(100, ex - 14));
-                if (g == 0) atomicOr(&s.counters[kCtrMidScaled], 1u);
+                if (g == 0) atomicOr(&s.counters[kCtrMidFlag + it.d], 1u);
               }
             }
             const float down = __uint_as_float((uint32_t)(127 - p) << 23);
@@ -554,6 +558,20 @@ __device__ __forceinline__ void finish_item(const Item& it, const float4* rb, in
 
 // ------------------------------------------------------------------------ kernel ----
 
+// Bounded wait until *p >= need (acquire at GPU scope): false when the budget ran out.
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t need, uint64_t budget_ns) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  if (v >= need) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= need) return true;
+    if ((i & 15) == 0 && globaltimer() - t0 > budget_ns) return false;
+  }
+}
+
 template <int PHASE>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
@@ -570,10 +588,12 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   const int S = lay.stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  pdl_wait();
+  // Gate/up waits for the routing.  Down does not wait for the gate/up grid as a whole: it is
+  // launched once every gate/up CTA has passed that wait (so the routing is complete), its
+  // CTAs take the SMs the gate/up CTAs leave, and each down item waits, in its producer,
+  // for the gate/up items whose output it reads (counted by their epilogues).
+  if (PHASE == 0) pdl_wait();
   const int D = min(max(*s.n_distinct, 1), kMaxPicks);
-  // down: whether any block of mid carries a scale (else its f16 values are the values)
-  const bool mid_scaled = (PHASE == 1) && (*(volatile const uint32_t*)&s.counters[kCtrMidScaled] != 0u);
   const int n_items = items_of(PHASE, dm, D);
   for (int i = threadIdx.x; i < D; i += kStreamThreads) sp.t_uniq[i] = s.uniq[i];
   for (int i = threadIdx.x; i <= D; i += kStreamThreads) sp.t_off[i] = s.user_off[i];
@@ -597,6 +617,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (PHASE == 0) pdl_trigger();  // the down launch may queue for SMs from now on
   }
   __syncthreads();
 
@@ -624,6 +645,19 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
       const Item it = decode_item(PHASE, item, dm, tb, D);
       const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
       const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;  // down activation box height
+      int scaled = 0;  // routed down: some block of the expert's mid carries a scale
+      if (PHASE == 1) {
+        // the gate/up items this one reads must be finished (their epilogues' stores made
+        // visible to this thread, then to the copy engine)
+        const bool sh = (it.kind == kSharedDN);
+        if (!wait_count(&s.counters[sh ? kCtrSharedGUDone : kCtrGUDone + it.d],
+                        (uint32_t)(sh ? dm.Is / 64 : dm.I / 64), budget_ns)) {
+          ok = false;
+          break;
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        if (!sh) scaled = *(volatile const uint32_t*)&s.counters[kCtrMidFlag + it.d] != 0u;
+      }
       uint32_t act_bytes;
       if (it.kind == kRoutedGU) act_bytes = (uint32_t)dm.Rmax * kActPitch;
       else if (it.kind == kRoutedDN) act_bytes = (4u << hsel) * kActPitch;
@@ -652,7 +686,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
         }
         pend |= 1u << stage;
         pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-        sp.info[stage] = make_int2(item, kc);
+        sp.info[stage] = make_int2(item, scaled);
         mbar_expect_tx(&sp.full[stage], bytes);
         uint8_t* sa = st + kStageW;
         if (it.kind == kRoutedGU) {
@@ -698,7 +732,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
       }
       item = next;
     }
-    pdl_trigger();  // this CTA is in its tail: let the next launch take the SM
+    if (PHASE == 1) pdl_trigger();  // this CTA is in its tail: the combine may launch
     if (ok) {
       // end-of-work marker (withheld too by the failure injection, when this CTA got no
       // item to stall on)
@@ -732,6 +766,15 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
       const Item it = decode_item(PHASE, item, dm, tb, D);
       finish_item(it, sp.red + rb * (kConsumerWarps * lay.nt_max * 32), lay.nt_max, dm, tb, s,
                   lane);
+      if (PHASE == 0) {
+        // count the item for the down items that read its output
+        __threadfence();  // this item's stores (every lane), before the count
+        __syncwarp();
+        if (lane == 0) {
+          uint32_t* c = &s.counters[it.kind == kSharedGU ? kCtrSharedGUDone : kCtrGUDone + it.d];
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sp.rempty[rb]);
     }
@@ -751,7 +794,8 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   bool ok = true;
   for (;;) {
     if (!mbar_wait(&sp.full[rg.stage], rg.phase, budget_ns)) { ok = false; break; }
-    const int item = sp.info[rg.stage].x;
+    const int2 info = sp.info[rg.stage];
+    const int item = info.x;
     if (item < 0) {
       // end of work: hand each epilogue warp the end marker through its next reduction slot
       for (int q = 0; q < kEpilogueWarps && ok; ++q, ++rc) {
@@ -784,7 +828,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     if (it.kind == kRoutedGU || it.kind == kRoutedDN) {
-      if (PHASE == 0 || !mid_scaled)
+      if (PHASE == 0 || info.y == 0)
         ok = (NT == 1) ? run_routed<PHASE == 0, 1, false>(sp, lay, rg, it, L, uo, eh, budget_ns, acc)
                        : run_routed<PHASE == 0, 2, false>(sp, lay, rg, it, L, uo, eh, budget_ns, acc);
       else

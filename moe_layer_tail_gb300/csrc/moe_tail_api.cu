@@ -107,7 +107,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
   s->y = (float*)take(P * H * 4);
   s->ys = (float*)take(R * H * 4);
   s->status = (int32_t*)take(4);
-  s->counters = (uint32_t*)take(64 * 4);
+  s->counters = (uint32_t*)take(kCtrWords * 4);
   return off;
 }
 

@@ -68,14 +68,23 @@ struct Scratch {
   float* y;              // [Rmax*k, H] routed expert outputs
   float* ys;             // [Rmax, H] shared expert output
   int32_t* status;       // [1] sticky device status word
-  uint32_t* counters;    // [64] work counters and tickets (zero between calls)
+  uint32_t* counters;    // [kCtrWords] work counters, tickets and per-expert progress
 };
 
 // Debug bits the kernels read (same values as MOE_TAIL_DEBUG_* in moe_tail.h).
 constexpr uint32_t kDebugStallFirstStage = 4u;
 
-// counters[] slots
-enum : int { kCtrGateUp = 0, kCtrDown = 1, kCtrFrontTicket = 2, kCtrMidScaled = 3 };
+// counters[] words (all zeroed at the start of every call by the front)
+enum : int {
+  kCtrGateUp = 0,        // next work item of the gate/up launch
+  kCtrDown = 1,          // next work item of the down launch
+  kCtrFrontTicket = 2,   // router CTAs done (the last one ranks the experts)
+  kCtrSharedGUDone = 4,  // shared-expert gate/up items finished
+  kCtrGUDone = 16,       // [kMaxPicks] routed gate/up items finished, per distinct expert
+  kCtrMidFlag = 16 + kMaxPicks,  // [kMaxPicks] nonzero: some 32-block of the expert's mid
+                                 // carries a power-of-two scale
+  kCtrWords = 16 + 2 * kMaxPicks
+};
 
 // ------------------------------------------------------------------ device helpers ----
 
