@@ -279,6 +279,59 @@ __device__ __forceinline__ void topk_row(const float* l, int E, int k, int32_t* 
   }
 }
 
+// Compare-exchange of two (key, id) candidates so that the better one (larger key, then
+// lower id) comes first.
+__device__ __forceinline__ void cas_desc(uint32_t& ka, uint32_t& ia, uint32_t& kb, uint32_t& ib) {
+  const bool sw = kb > ka || (kb == ka && ib < ia);
+  const uint32_t k0 = sw ? kb : ka, i0 = sw ? ib : ia;
+  kb = sw ? ka : kb;
+  ib = sw ? ia : ib;
+  ka = k0;
+  ia = i0;
+}
+
+// topk_row for E <= 256: each lane first sorts its 8 candidates (best first) with Batcher's
+// 19-comparator network, so that handing over a pick costs its owner a shift of the list
+// instead of a rescan.  Slots past E are (key 0, id ~0): after every expert, NaN ones
+// included, and never picked.
+template <bool kSmem>
+__device__ __forceinline__ void topk_row_sorted(const float* l, int E, int k, int32_t* status,
+                                                float& pv, int& pe) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[8], id[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = lane + 32 * q;
+    key[q] = (e < E) ? order_key(load_logit<kSmem>(l + e)) : 0u;
+    id[q] = (e < E) ? (uint32_t)e : 0xffffffffu;
+  }
+#define MT_CAS(a, b) cas_desc(key[a], id[a], key[b], id[b])
+  MT_CAS(0, 1); MT_CAS(2, 3); MT_CAS(4, 5); MT_CAS(6, 7);
+  MT_CAS(0, 2); MT_CAS(1, 3); MT_CAS(4, 6); MT_CAS(5, 7);
+  MT_CAS(1, 2); MT_CAS(5, 6);
+  MT_CAS(0, 4); MT_CAS(1, 5); MT_CAS(2, 6); MT_CAS(3, 7);
+  MT_CAS(2, 4); MT_CAS(3, 5);
+  MT_CAS(1, 2); MT_CAS(3, 4); MT_CAS(5, 6);
+#undef MT_CAS
+  pv = 0.f;
+  pe = 0;
+  for (int i = 0; i < k; ++i) {
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, key[0]);
+    const uint32_t we = __reduce_min_sync(0xffffffffu, key[0] == mk ? id[0] : 0xffffffffu);
+    if (mk == 0u && lane == 0) set_status(status, kStatusBadRouting);
+    if (id[0] == we) {  // this lane owned the pick: the next candidate moves up
+#pragma unroll
+      for (int q = 0; q < 7; ++q) {
+        key[q] = key[q + 1];
+        id[q] = id[q + 1];
+      }
+      key[7] = 0u;
+      id[7] = 0xffffffffu;
+    }
+    if (lane == i) { pv = key_value(mk); pe = (int)we; }
+  }
+}
+
 template <bool kSmem>
 __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
                                  int32_t* n_distinct, int32_t* uniq, int32_t* user_off,
@@ -296,10 +349,7 @@ __device__ void topk_dedup_block(const float* logits, int32_t* ids, float* wts,
     const float* l = logits + (size_t)row * E;
     float pv;  // lane i < k keeps pick i
     int pe;
-    if (E <= 32) topk_row<kSmem, 1>(l, E, k, status, pv, pe);
-    else if (E <= 64) topk_row<kSmem, 2>(l, E, k, status, pv, pe);
-    else if (E <= 128) topk_row<kSmem, 4>(l, E, k, status, pv, pe);
-    else if (E <= 256) topk_row<kSmem, 8>(l, E, k, status, pv, pe);
+    if (E <= 256) topk_row_sorted<kSmem>(l, E, k, status, pv, pe);
     else if (E <= 512) topk_row<kSmem, 16>(l, E, k, status, pv, pe);
     else topk_row<kSmem, kMaxExperts / 32>(l, E, k, status, pv, pe);
     // weights: softmax of the picked logits (lane i holds pick i; pick 0 is the largest)

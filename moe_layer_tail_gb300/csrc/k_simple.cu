@@ -231,17 +231,30 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
 // out[r, h] = bf16(sum over slots in pick order of wts * y + ys): a fixed-order fp32 sum;
 // the residual receives bf16(x + residual), now that every reader of the old value is done.
 // One thread per 8 consecutive outputs of a row; the slots' loads are unrolled so that they
-// are in flight together.
+// are in flight together.  wait_tiles: instead of waiting for the previous launch as a
+// whole, each warp waits (bounded, acquire) until the down items of the two 128-output
+// tiles it covers (the shared expert's and one per distinct expert) are counted done.
 __global__ void __launch_bounds__(256)
 k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
-          __nv_bfloat16* __restrict__ residual) {
-  pdl_wait();
+          __nv_bfloat16* __restrict__ residual, bool wait_tiles, uint64_t budget_ns) {
+  if (!wait_tiles) pdl_wait();
   pdl_trigger();
   const int H = dm.H, k = dm.k;
-  const int ng = H / 8;
+  const int ng = H / 8;  // a multiple of 32: whole warps lie in one row
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= dm.R * ng) return;
   const int r = idx / ng, c = idx % ng;
+  if (wait_tiles) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t need = (uint32_t)min(max(*s.n_distinct, 1), kMaxPicks) + 1u;
+    bool ok = true;
+    if ((lane & 15) == 0) ok = wait_count(&s.counters[kCtrTileDone + c / 16], need, budget_ns);
+    if (__any_sync(0xffffffffu, !ok)) {
+      if (lane == 0) set_status(s.status, kStatusTimeout);
+      return;
+    }
+    __syncwarp();  // orders the other lanes' loads after lanes 0 and 16's acquires
+  }
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int i0 = 0; i0 < k; i0 += 8) {
     float4 ya[8], yb[8];
@@ -281,10 +294,11 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
 }
 
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
-                           __nv_bfloat16* residual, cudaStream_t st, bool pdl) {
+                           __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
+                           uint64_t budget_ns) {
   const int n = d.R * d.H / 8;
   return launch_k(k_combine, dim3((n + 255) / 256), dim3(256), 0, st, pdl, d, s, out,
-                  residual);
+                  residual, wait_tiles, budget_ns);
 }
 
 }  // namespace mtail

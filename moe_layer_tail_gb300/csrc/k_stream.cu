@@ -160,11 +160,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 // Bounded wait: false when the budget ran out (the caller records the timeout).
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint64_t budget_ns) {
   if (mbar_try_wait(b, parity)) return true;
@@ -558,19 +553,6 @@ __device__ __forceinline__ void finish_item(const Item& it, const float4* rb, in
 
 // ------------------------------------------------------------------------ kernel ----
 
-// Bounded wait until *p >= need (acquire at GPU scope): false when the budget ran out.
-__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t need, uint64_t budget_ns) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  if (v >= need) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    __nanosleep(64);
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    if (v >= need) return true;
-    if ((i & 15) == 0 && globaltimer() - t0 > budget_ns) return false;
-  }
-}
 
 template <int PHASE>
 __global__ void __launch_bounds__(kStreamThreads, 1)
@@ -617,7 +599,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    if (PHASE == 0) pdl_trigger();  // the down launch may queue for SMs from now on
+    pdl_trigger();  // the next launch may queue for SMs from now on (it waits on counts)
   }
   __syncthreads();
 
@@ -732,7 +714,6 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
       }
       item = next;
     }
-    if (PHASE == 1) pdl_trigger();  // this CTA is in its tail: the combine may launch
     if (ok) {
       // end-of-work marker (withheld too by the failure injection, when this CTA got no
       // item to stall on)
@@ -766,14 +747,14 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
       const Item it = decode_item(PHASE, item, dm, tb, D);
       finish_item(it, sp.red + rb * (kConsumerWarps * lay.nt_max * 32), lay.nt_max, dm, tb, s,
                   lane);
-      if (PHASE == 0) {
-        // count the item for the down items that read its output
-        __threadfence();  // this item's stores (every lane), before the count
-        __syncwarp();
-        if (lane == 0) {
-          uint32_t* c = &s.counters[it.kind == kSharedGU ? kCtrSharedGUDone : kCtrGUDone + it.d];
-          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
-        }
+      // count the item for its readers (the down items of the expert, or the combine of its
+      // 128 outputs): the warp barrier orders every lane's stores before lane 0's release
+      __syncwarp();
+      if (lane == 0) {
+        uint32_t* c = &s.counters[PHASE == 1 ? kCtrTileDone + it.out0 / 128
+                                  : it.kind == kSharedGU ? kCtrSharedGUDone
+                                                         : kCtrGUDone + it.d];
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sp.rempty[rb]);

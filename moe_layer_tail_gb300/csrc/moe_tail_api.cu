@@ -224,7 +224,10 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
     ++stage_i;                                          \
   } while (0)
   const bool pdl = !(h->cfg.debug_flags & MOE_TAIL_DEBUG_NO_PDL);
-  if (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) {
+  const bool simple = (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) != 0;
+  const uint64_t budget_ns =
+      (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
+  if (simple) {
     MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
                                 h->w, h->s, st, pdl));
     MT_STAGE(launch_router(d, h->w, h->s, st, pdl));
@@ -239,13 +242,14 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
                                   h->w, h->s, st, pdl));
       MT_STAGE(launch_router_topk(d, h->w, h->s, st, pdl));
     }
-    const uint64_t budget_ns =
-        (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
     const uint32_t dbg = h->cfg.debug_flags;
     MT_STAGE(launch_stream(0, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
     MT_STAGE(launch_stream(1, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
   }
-  MT_STAGE(launch_combine(d, h->s, (__nv_bfloat16*)out, (__nv_bfloat16*)residual, st, pdl));
+  // after the streaming kernels the combine waits per 128 outputs for the down items that
+  // write them; after the cross-checking kernels it waits for the previous launch
+  MT_STAGE(launch_combine(d, h->s, (__nv_bfloat16*)out, (__nv_bfloat16*)residual, st, pdl,
+                          !simple, budget_ns));
 #undef MT_STAGE
   h->last_rows = rows;
   return MOE_TAIL_OK;

@@ -83,7 +83,8 @@ enum : int {
   kCtrGUDone = 16,       // [kMaxPicks] routed gate/up items finished, per distinct expert
   kCtrMidFlag = 16 + kMaxPicks,  // [kMaxPicks] nonzero: some 32-block of the expert's mid
                                  // carries a power-of-two scale
-  kCtrWords = 16 + 2 * kMaxPicks
+  kCtrTileDone = 16 + 2 * kMaxPicks,  // [256] down items finished per 128 hidden outputs
+  kCtrWords = 16 + 2 * kMaxPicks + 256
 };
 
 // ------------------------------------------------------------------ device helpers ----
@@ -104,6 +105,26 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& h0, uint32
 // E8M0 scale byte -> float 2^(s-127) (s = 0 gives the subnormal 2^-127; 255 is not used).
 __device__ __forceinline__ float e8m0_to_float(uint32_t s) {
   return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait until *p >= need (acquire at GPU scope): false when the budget ran out.
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t need, uint64_t budget_ns) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  if (v >= need) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= need) return true;
+    if ((i & 15) == 0 && globaltimer() - t0 > budget_ns) return false;
+  }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -204,6 +225,7 @@ cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, cons
                           const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                           bool pdl, uint32_t debug);
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
-                           __nv_bfloat16* residual, cudaStream_t st, bool pdl);
+                           __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
+                           uint64_t budget_ns);
 
 }  // namespace mtail
