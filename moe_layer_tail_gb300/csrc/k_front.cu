@@ -208,16 +208,11 @@ cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cud
 }
 
 // ----------------------------------------------------------------- top-k + dedup ----
-// Run by one whole CTA.  Warp w ranks rows w, w + nwarps, ...: each round every lane takes
-// its best untaken candidate (larger logit, then lower id) and a butterfly over
-// (value, id) pairs finds the round's pick; an exact tie of the value resolves to the
-// lower id, so the pick order is (logit desc, id asc).  The weights are the softmax of the
-// picked logits.  Then the distinct experts of the call are listed in ascending id, with
-// their users in ascending row order (an expert appears at most once in a row's picks).
-
-__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
-  return v > bv || (v == bv && e < be);
-}
+// Run by one whole CTA.  Warp w ranks rows w, w + nwarps, ...: each round takes the best
+// untaken candidate of the row (larger logit, then lower id), so the pick order is (logit
+// desc, id asc).  The weights are the softmax of the picked logits.  Then the distinct
+// experts of the call are listed in ascending id, with their users in ascending row order
+// (an expert appears at most once in a row's picks).
 
 // kSmem: the logits are in this CTA's shared memory (else in global memory, written by an
 // earlier launch or by other CTAs of this one before a fence).
