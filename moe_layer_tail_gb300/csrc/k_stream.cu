@@ -32,10 +32,16 @@
 //     reduction slot and moves on -- no consumer ever waits for another consumer;
 //   * warps 1 and 2 -- the epilogue, taking items in turn: adds the two K halves of every
 //     tile in a fixed order and finishes the item (SiLU*up, the f16 copy of mid with its
-//     block scales, stores).
+//     block scales, stores), then counts it done for its readers;
 //   * activations enter the routed contractions as f16 with power-of-two scales (one per row
-//     for gate/up, applied in the epilogue; one per 32-element block for down, applied per
-//     block), exact for bf16 values in range;
+//     for gate/up, applied in the epilogue; for down, mid's 32-element blocks are unscaled
+//     unless one falls outside f16's exact range, which switches that expert's down items to
+//     per-block scales), exact for bf16 values in range;
+//   * the two launches synchronise through counts, not grids: gate/up waits for the router
+//     launch and then lets the down launch queue at once; down CTAs take the SMs gate/up
+//     CTAs leave, and a down item's producer waits for the gate/up items it reads (counted
+//     per distinct expert), so down overlaps the gate/up tail; down's epilogues count the
+//     items of every 128 outputs for the combine;
 //   * every wait is bounded by a %globaltimer budget; on expiry the kernel sets the status
 //     word, lets the copies it issued land, and leaves.
 #include <cstring>
