@@ -50,6 +50,10 @@ def _load():
         lib.oracle_shared.restype = None
         lib.oracle_moe_tail.argtypes = [I, I, I, I, I, I, D] + [P] * 15 + [I]
         lib.oracle_moe_tail.restype = I
+        lib.oracle_shared_gate.argtypes = [I, I, P, P, P]
+        lib.oracle_shared_gate.restype = None
+        lib.oracle_moe_tail_gated.argtypes = [I, I, I, I, I, I, D] + [P] * 16 + [I]
+        lib.oracle_moe_tail_gated.restype = I
         _lib = lib
     return _lib
 
@@ -156,8 +160,21 @@ def shared(n_row, ws13, ws2):
     return ys, ms
 
 
+def shared_gate(n, g):
+    """Per-row sigmoid gate of the shared expert: n [R,H] bf16 bits, g [H] bf16 bits ->
+    [R] float64."""
+    n = _c(n, np.uint16)
+    g = _c(g, np.uint16)
+    R, H = n.shape
+    assert g.shape == (H,)
+    gate = np.empty(R, np.float64)
+    _load().oracle_shared_gate(R, H, _p(n), _p(g), _p(gate))
+    return gate
+
+
 def moe_tail(inputs: dict, k: int, eps: float, nthreads: int = 1):
-    """The whole tail.  `inputs` holds the arrays made by moe_layer_tail_gb300.inputs.
+    """The whole tail.  `inputs` holds the arrays made by moe_layer_tail_gb300.inputs; an
+    optional "ws_gate" [H] (bf16 bits) gates the shared expert's output per row.
 
     Returns dict(out [R,H] bf16 bits, out_exact [R,H] float64 (before the bf16 rounding),
     residual [R,H] bf16 bits (r_new), ids [R,k], wts [R,k] float64, logits [R,E] float64).
@@ -173,6 +190,7 @@ def moe_tail(inputs: dict, k: int, eps: float, nthreads: int = 1):
     w2s = _c(inputs["w2_scales"], np.uint8)
     ws13 = _c(inputs["ws13"], np.uint16)
     ws2 = _c(inputs["ws2"], np.uint16)
+    wsg = _c(inputs["ws_gate"], np.uint16) if inputs.get("ws_gate") is not None else None
     R, H = x.shape
     E = w_r.shape[0]
     I = w2c.shape[2] * 2
@@ -182,9 +200,10 @@ def moe_tail(inputs: dict, k: int, eps: float, nthreads: int = 1):
     wts = np.empty((R, k), np.float64)
     logits = np.empty((R, E), np.float64)
     exact = np.empty((R, H), np.float64)
-    rc = _load().oracle_moe_tail(R, H, E, int(k), I, Is, float(eps), _p(x), _p(res), _p(gamma),
-                                 _p(w_r), _p(w13c), _p(w13s), _p(w2c), _p(w2s), _p(ws13), _p(ws2),
-                                 _p(out), _p(ids), _p(wts), _p(logits), _p(exact), int(nthreads))
+    rc = _load().oracle_moe_tail_gated(R, H, E, int(k), I, Is, float(eps), _p(x), _p(res),
+                                       _p(gamma), _p(w_r), _p(w13c), _p(w13s), _p(w2c),
+                                       _p(w2s), _p(ws13), _p(ws2), _p(wsg), _p(out), _p(ids),
+                                       _p(wts), _p(logits), _p(exact), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_moe_tail rejected the shapes (rc=%d)" % rc)
     return dict(out=out, out_exact=exact, residual=res, ids=ids, wts=wts, logits=logits)

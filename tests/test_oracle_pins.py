@@ -301,7 +301,10 @@ def _numpy_tail(d, k, eps):
             acc += wts[i] * (W2 @ mid)
         g, u = W13s[:Is] @ n[r], W13s[Is:] @ n[r]
         ms = bf16_decode(quantize_to_nearest_bf16_bits(silu(g) * u))
-        acc += W2s @ ms
+        gate = 1.0
+        if d.get("ws_gate") is not None:
+            gate = scipy.special.expit(n[r] @ bf16_decode(d["ws_gate"]))
+        acc += gate * (W2s @ ms)
         out[r] = acc
     return r_new, out
 
@@ -350,6 +353,67 @@ def test_doubling_w2_scales_doubles_routed_part_exactly():
     twice = oracle.moe_tail(d2, shape.k, shape.eps)
     assert np.array_equal(bf16_decode(twice["out"]), 2 * bf16_decode(base["out"]))
     assert np.array_equal(twice["ids"], base["ids"])
+
+
+# ------------------------------------------------------- shared-expert gate ----
+
+
+def _gate_vector(seed, H):
+    rng = np.random.default_rng(seed)
+    return gen.to_bf16_bits(rng.standard_normal(H) / np.sqrt(H))
+
+
+def test_shared_gate_matches_scipy_expit():
+    shape, d = _tail_inputs(26, R=5)
+    _, n, _ = oracle.add_rmsnorm(d["x"], d["residual"], d["gamma"], shape.eps)
+    g = _gate_vector(26, shape.H)
+    got = oracle.shared_gate(n, g)
+    want = scipy.special.expit(bf16_decode(n).reshape(shape.R, shape.H) @ bf16_decode(g))
+    assert np.allclose(got, want, rtol=1e-14, atol=0)
+    assert (got > 0).all() and (got < 1).all()
+
+
+def test_gated_tail_matches_numpy_bruteforce():
+    shape, d = _tail_inputs(27)
+    d["ws_gate"] = _gate_vector(27, shape.H)
+    got = oracle.moe_tail(d, shape.k, shape.eps)
+    _, out_exact = _numpy_tail(d, shape.k, shape.eps)
+    assert np.allclose(got["out_exact"], out_exact, rtol=1e-10, atol=1e-12)
+    ungated = oracle.moe_tail({k: v for k, v in d.items() if k != "ws_gate"}, shape.k, shape.eps)
+    assert not np.array_equal(got["out"], ungated["out"])
+    assert np.array_equal(got["ids"], ungated["ids"])  # the gate does not touch the routing
+
+
+def test_zero_gate_halves_the_shared_part_exactly():
+    # sigmoid(0) = 1/2, applied to the shared expert's output only: the same as halving every
+    # shared down weight (an exact exponent decrement for these normal bf16 values)
+    shape, d = _tail_inputs(28)
+    gated = dict(d)
+    gated["ws_gate"] = np.zeros(shape.H, np.uint16)
+    a = oracle.moe_tail(gated, shape.k, shape.eps)
+    half = dict(d)
+    ws2 = d["ws2"].astype(np.uint32)
+    exp = (ws2 >> 7) & 0xFF
+    assert ((exp > 1) | (ws2 & 0x7FFF == 0)).all()
+    half["ws2"] = np.where(ws2 & 0x7FFF, ws2 - 0x80, ws2).astype(np.uint16)
+    b = oracle.moe_tail(half, shape.k, shape.eps)
+    assert np.array_equal(a["out_exact"], b["out_exact"])
+    assert np.array_equal(a["out"], b["out"])
+
+
+def test_closed_gate_removes_the_shared_expert():
+    # a gate vector anti-parallel to the row's activations drives the logit far below -745,
+    # where e^-z overflows and the gate is exactly 0: the output is the routed part alone
+    shape, d = _tail_inputs(29, R=1)
+    _, n, _ = oracle.add_rmsnorm(d["x"], d["residual"], d["gamma"], shape.eps)
+    gated = dict(d)
+    gated["ws_gate"] = gen.to_bf16_bits(-64.0 * bf16_decode(n[0]))
+    assert oracle.shared_gate(n, gated["ws_gate"])[0] == 0.0
+    a = oracle.moe_tail(gated, shape.k, shape.eps)
+    no_shared = dict(d)
+    no_shared["ws2"] = np.zeros_like(d["ws2"])
+    b = oracle.moe_tail(no_shared, shape.k, shape.eps)
+    assert np.array_equal(a["out_exact"], b["out_exact"])
 
 
 def test_oracle_is_deterministic_and_thread_count_invariant():
