@@ -45,7 +45,7 @@ class Config(ctypes.Structure):
 class WeightPtrs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("gamma", "router_w", "w13_codes", "w13_scales", "w2_codes", "w2_scales",
-                 "shared_w13", "shared_w2")]
+                 "shared_w13", "shared_w2", "shared_gate")]
 
 
 class MoeTailError(RuntimeError):
@@ -126,7 +126,8 @@ def make_config(shape, max_rows=None, mode=MODE_MULTI_KERNEL, wait_budget_us=0,
 
 _WEIGHT_KEYS = {"gamma": "gamma", "router_w": "w_r", "w13_codes": "w13_codes",
                 "w13_scales": "w13_scales", "w2_codes": "w2_codes", "w2_scales": "w2_scales",
-                "shared_w13": "ws13", "shared_w2": "ws2"}
+                "shared_w13": "ws13", "shared_w2": "ws2", "shared_gate": "ws_gate"}
+_OPTIONAL_WEIGHTS = ("ws_gate",)  # absent: a null pointer
 
 
 class MoeTail:
@@ -138,7 +139,9 @@ class MoeTail:
         self.shape = shape
         self._weights = weights  # keep the borrowed tensors alive
         self.cfg = make_config(shape, max_rows, mode, wait_budget_us, debug_flags)
-        wp = WeightPtrs(**{f: weights[k].data_ptr() for f, k in _WEIGHT_KEYS.items()})
+        wp = WeightPtrs(**{f: (weights[k].data_ptr() if weights.get(k) is not None else None)
+                           for f, k in _WEIGHT_KEYS.items()
+                           if k in weights or k not in _OPTIONAL_WEIGHTS})
         h = ctypes.c_void_p()
         rc = lib.moe_tail_create(ctypes.byref(self.cfg), ctypes.byref(wp), ctypes.byref(h))
         if rc != OK:

@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(kNormThreads)
 k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ residual,
               const __nv_bfloat16* __restrict__ gamma, __nv_bfloat16* __restrict__ rnew,
               __nv_bfloat16* __restrict__ n_out, __half* __restrict__ n16,
-              float* __restrict__ n16s, uint32_t* __restrict__ counters, int H, float eps) {
+              float* __restrict__ n16s, uint32_t* __restrict__ counters, int H, float eps,
+              const __nv_bfloat16* __restrict__ wsg, float* __restrict__ sgate) {
   extern __shared__ uint4 s_gamma[];  // [H / 8]
   __shared__ float part[kNormThreads / 32];
   const int r = blockIdx.x;
@@ -135,6 +136,8 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   uint4* rno = reinterpret_cast<uint4*>(rnew + (size_t)r * H);
   uint4* no = reinterpret_cast<uint4*>(n_out + (size_t)r * H);
   uint4* n16o = reinterpret_cast<uint4*>(n16 + (size_t)r * H);
+  const uint4* wg4 = reinterpret_cast<const uint4*>(wsg);
+  float zg = 0.f;  // this thread's part of the shared-expert gate logit n . wsg
 #pragma unroll
   for (int q = 0; q < kNormGroups; ++q) {
     const int c = threadIdx.x + q * kNormThreads;
@@ -145,7 +148,18 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
       rno[c] = rn[q];
       no[c] = nv;
       n16o[c] = f16_group(nv, down);
+      if (wsg) {
+        const uint4 w = __ldg(wg4 + c);
+        const uint32_t nn[4] = {nv.x, nv.y, nv.z, nv.w}, ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          zg += bf16_lo(nn[i]) * bf16_lo(ww[i]) + bf16_hi(nn[i]) * bf16_hi(ww[i]);
+      }
     }
+  }
+  if (wsg) {  // the gate of this row: sigmoid of the block-reduced logit
+    const float z = block_reduce(zg, false, part);
+    if (threadIdx.x == 0) sgate[r] = 1.0f / (1.0f + expf(-z));
   }
 }
 
@@ -153,7 +167,8 @@ cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
                                const __nv_bfloat16* residual, const Weights& w,
                                const Scratch& s, cudaStream_t st, bool pdl) {
   return launch_k(k_add_rmsnorm, dim3(d.R), dim3(kNormThreads), (size_t)d.H * 2, st, pdl, x,
-                  residual, w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps);
+                  residual, w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps, w.wsg,
+                  s.sgate);
 }
 
 // ------------------------------------------------------------------- router GEMV ----

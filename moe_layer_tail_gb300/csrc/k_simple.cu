@@ -236,7 +236,8 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
 // tiles it covers (the shared expert's and one per distinct expert) are counted done.
 __global__ void __launch_bounds__(256)
 k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
-          __nv_bfloat16* __restrict__ residual, bool wait_tiles, uint64_t budget_ns) {
+          __nv_bfloat16* __restrict__ residual, bool wait_tiles, uint64_t budget_ns,
+          bool gated) {
   if (!wait_tiles) pdl_wait();
   pdl_trigger();
   const int H = dm.H, k = dm.k;
@@ -279,10 +280,14 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
       }
     }
   }
+  // + the shared expert's output, times its row's sigmoid gate when the layer has one
   const float4* ysp = reinterpret_cast<const float4*>(s.ys + (size_t)r * H) + 2 * c;
   const float4 s0 = __ldcg(ysp), s1 = __ldcg(ysp + 1);
-  acc[0] += s0.x; acc[1] += s0.y; acc[2] += s0.z; acc[3] += s0.w;
-  acc[4] += s1.x; acc[5] += s1.y; acc[6] += s1.z; acc[7] += s1.w;
+  const float gt = gated ? __ldcg(s.sgate + r) : 1.f;
+  acc[0] = fmaf(gt, s0.x, acc[0]); acc[1] = fmaf(gt, s0.y, acc[1]);
+  acc[2] = fmaf(gt, s0.z, acc[2]); acc[3] = fmaf(gt, s0.w, acc[3]);
+  acc[4] = fmaf(gt, s1.x, acc[4]); acc[5] = fmaf(gt, s1.y, acc[5]);
+  acc[6] = fmaf(gt, s1.z, acc[6]); acc[7] = fmaf(gt, s1.w, acc[7]);
   uint32_t o[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q)
@@ -295,10 +300,10 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
 
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
-                           uint64_t budget_ns) {
+                           uint64_t budget_ns, bool gated) {
   const int n = d.R * d.H / 8;
   return launch_k(k_combine, dim3((n + 255) / 256), dim3(256), 0, st, pdl, d, s, out,
-                  residual, wait_tiles, budget_ns);
+                  residual, wait_tiles, budget_ns, gated);
 }
 
 }  // namespace mtail

@@ -106,6 +106,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
   s->ms = (__nv_bfloat16*)take(R * Is * 2);
   s->y = (float*)take(P * H * 4);
   s->ys = (float*)take(R * H * 4);
+  s->sgate = (float*)take(R * 4);
   s->status = (int32_t*)take(4);
   s->counters = (uint32_t*)take(kCtrWords * 4);
   return off;
@@ -122,6 +123,10 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
                          w->w2_codes, w->w2_scales, w->shared_w13, w->shared_w2};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return MOE_TAIL_ERR_INVALID_ARG;
+  if (w->shared_gate && !aligned16(w->shared_gate)) return MOE_TAIL_ERR_INVALID_ARG;
+  // the fused front computes n chunk by chunk across CTAs: it has no row-wide gate reduction
+  if (w->shared_gate && (cfg->debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT))
+    return MOE_TAIL_ERR_UNSUPPORTED;
 
   moe_tail_t* h = new (std::nothrow) moe_tail_t;
   if (!h) return MOE_TAIL_ERR_CUDA;
@@ -135,6 +140,7 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   h->w.w2s = (const uint8_t*)w->w2_scales;
   h->w.ws13 = (const __nv_bfloat16*)w->shared_w13;
   h->w.ws2 = (const __nv_bfloat16*)w->shared_w2;
+  h->w.wsg = (const __nv_bfloat16*)w->shared_gate;
 
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = prepare_stream_kernels();
@@ -249,7 +255,7 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
   // after the streaming kernels the combine waits per 128 outputs for the down items that
   // write them; after the cross-checking kernels it waits for the previous launch
   MT_STAGE(launch_combine(d, h->s, (__nv_bfloat16*)out, (__nv_bfloat16*)residual, st, pdl,
-                          !simple, budget_ns));
+                          !simple, budget_ns, h->w.wsg != nullptr));
 #undef MT_STAGE
   h->last_rows = rows;
   return MOE_TAIL_OK;

@@ -43,6 +43,7 @@ struct Weights {
   const uint8_t* w2s;
   const __nv_bfloat16* ws13;
   const __nv_bfloat16* ws2;
+  const __nv_bfloat16* wsg;  // shared-expert gate [H], or null
 };
 
 // Every buffer a call needs, carved from one allocation made at create time.
@@ -67,6 +68,7 @@ struct Scratch {
   __nv_bfloat16* ms;     // [Rmax, Is] shared-expert intermediate (bf16)
   float* y;              // [Rmax*k, H] routed expert outputs
   float* ys;             // [Rmax, H] shared expert output
+  float* sgate;          // [Rmax] sigmoid gate of the shared output (when a gate is given)
   int32_t* status;       // [1] sticky device status word
   uint32_t* counters;    // [kCtrWords] work counters, tickets and per-expert progress
 };
@@ -226,6 +228,6 @@ cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, cons
                           bool pdl, uint32_t debug);
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
-                           uint64_t budget_ns);
+                           uint64_t budget_ns, bool gated);
 
 }  // namespace mtail

@@ -111,7 +111,8 @@ def _codes(rng, shape):
 
 
 _WEIGHT_STREAMS = ("gamma", "w_r", "w13_codes", "w13_scales", "w2_codes", "w2_scales", "ws13",
-                   "ws2")
+                   "ws2", "ws_gate")
+_LAYER_WEIGHTS = _WEIGHT_STREAMS[:-1]  # the shared-expert gate is optional
 
 
 def make_weight(shape: TailShape, seed: int, key: str) -> np.ndarray:
@@ -134,11 +135,14 @@ def make_weight(shape: TailShape, seed: int, key: str) -> np.ndarray:
         return _normal_bf16(rng, (2 * Is, H), 1.0 / math.sqrt(H))
     if key == "ws2":
         return _normal_bf16(rng, (H, Is), 1.0 / math.sqrt(Is))
+    if key == "ws_gate":  # logit n . g ~ N(0, 1) for normalised rows
+        return _normal_bf16(rng, (H,), 1.0 / math.sqrt(H))
     raise KeyError(key)
 
 
-def make_weights(shape: TailShape, seed: int, keys=_WEIGHT_STREAMS) -> dict:
-    """Weights of one layer: gamma, router, routed MXFP4 experts, shared bf16 expert."""
+def make_weights(shape: TailShape, seed: int, keys=_LAYER_WEIGHTS) -> dict:
+    """Weights of one layer: gamma, router, routed MXFP4 experts, shared bf16 expert (add
+    "ws_gate" to `keys` for the shared expert's sigmoid gate)."""
     return {key: make_weight(shape, seed, key) for key in keys}
 
 

@@ -53,6 +53,15 @@ def test_binding_constants_match_header():
         "MOE_TAIL_STATUS_BAD_TILE"}
 
 
+def test_weight_struct_fields_match_header():
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "moe_tail.h")).read(),
+                 flags=re.S)
+    body = re.search(r"typedef struct \{([^}]*)\} moe_tail_weights_t;", src).group(1)
+    fields = re.findall(r"const void\*\s+(\w+);", body)
+    assert [f for f, _ in mt.WeightPtrs._fields_] == fields
+    assert fields[-1] == "shared_gate"
+
+
 def test_strerror_covers_codes(lib):
     for code in (0, -1, -2, -3, -4, -5, -6):
         s = lib.moe_tail_strerror(code).decode()

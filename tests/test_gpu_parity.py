@@ -174,6 +174,31 @@ def test_nan_router_logits_flag_routing():
     assert tail.status() == 0
 
 
+@pytest.mark.parametrize("flags", [0, SIMPLE, NO_PDL])
+@pytest.mark.parametrize("R,H,E,k,I,Is", [
+    (3, 512, 12, 3, 256, 192),     # several tiles
+    (8, 2560, 20, 4, 512, 256),    # long K, repeated experts
+    (16, 256, 16, 16, 128, 128),   # maximum rows, every expert
+])
+def test_shared_expert_gate(R, H, E, k, I, Is, flags):
+    shape, d = _small(200 + R + E, R, H, E, k, I, Is)
+    d["ws_gate"] = gen.make_weight(shape, 200 + R + E, "ws_gate")
+    tail, dev, orc, (out, res, ids, wts, nd) = _check_small(shape, d, flags=flags)
+    # the gate moves the output: the ungated oracle does not match it
+    plain = oracle.moe_tail({kk: v for kk, v in d.items() if kk != "ws_gate"}, shape.k, shape.eps,
+                            nthreads=NTHREADS)
+    assert not np.array_equal(orc["out"], plain["out"])
+
+
+def test_shared_expert_gate_refused_with_fused_front():
+    shape, d = _small(210)
+    d["ws_gate"] = gen.make_weight(shape, 210, "ws_gate")
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    with pytest.raises(MoeTailError) as ei:
+        MoeTail(shape, dev, max_rows=shape.R, debug_flags=FUSED_FRONT)
+    assert ei.value.code == ERR_UNSUPPORTED
+
+
 def test_rows_below_max_and_batch_invariance():
     shape, d = _small(10, R=6, H=512, E=20, k=4, I=256, Is=128)
     dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
