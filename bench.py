@@ -51,6 +51,9 @@ def parse_args():
                    help="profiling aid: the workload with this many experts instead (a "
                         "smaller case of the same kernels, e.g. for an ncu capture); the "
                         "line's config says so")
+    p.add_argument("--shared-gate", action="store_true",
+                   help="the workload with the shared expert's sigmoid gate; the line's config "
+                        "says so")
     return p.parse_args()
 
 
@@ -184,6 +187,8 @@ def run_ours(args, rank, world, local_rank):
     K, W = args.steps, args.warmup
     nsets = K + W
     host_w = gen.make_weights(shape, wl.seed)
+    if args.shared_gate:
+        host_w["ws_gate"] = gen.make_weight(shape, wl.seed, "ws_gate")
     dev_w = mt.weights_to_device(host_w)
     # one input set per step: correlated rows (~40% repeated picks), seeds wl.seed + 1000*i
     xs, rs = [], []
@@ -259,7 +264,8 @@ def run_ours(args, rank, world, local_rank):
         _, _, nd = tail.routing(R)
         Ds.append(nd)
     Ds = np.array(Ds)
-    bytes_per = np.array([gen.algorithmic_bytes(shape, int(d)) for d in Ds])
+    bytes_per = np.array([gen.algorithmic_bytes(shape, int(d), gated=args.shared_gate)
+                          for d in Ds])
     total_bytes = float(bytes_per.sum())
     us_per_call = job_us_per_call(elapsed_ms, K, world)
     gbps = total_bytes * world / (elapsed_ms * 1e-3) / 1e9
@@ -294,7 +300,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": K, "warmup": W, "ms_per_step": round(elapsed_ms / K, 5),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl.name + ("" if not args.experts else " with %d experts" % shape.E),
+        "config": {"workload": wl.name + ("" if not args.experts else " with %d experts" % shape.E)
+                               + (" with shared-expert gate" if args.shared_gate else ""),
                    "rows": R, "hidden": shape.H, "experts": shape.E,
                    "top_k": shape.k, "expert_inter": shape.I, "shared_inter": shape.Is,
                    "weights": "MXFP4 routed experts, bf16 router and shared expert",
@@ -374,6 +381,8 @@ def run_reference(args, rank, world):
     R = shape.R
     cores = oracle.host_cores()
     host_w = gen.make_weights(shape, wl.seed)
+    if args.shared_gate:
+        host_w["ws_gate"] = gen.make_weight(shape, wl.seed, "ws_gate")
     c = gen.similar_c() if wl.kind == "similar" else None
     K, W = args.steps, args.warmup
     a = gen.make_activations(shape, wl.seed, wl.kind, c)

@@ -175,10 +175,13 @@ def make_inputs(name_or_wl, c: float = None) -> dict:
     return d
 
 
-def algorithmic_bytes(shape: TailShape, distinct: int, rows: int = None) -> int:
+def algorithmic_bytes(shape: TailShape, distinct: int, rows: int = None,
+                      gated: bool = False) -> int:
     """Bytes one call must move: each distinct expert's MXFP4 codes and scales once, the bf16
-    router, shared expert and gamma once, and x, residual (read and write) and out."""
+    router, shared expert (and its gate vector), gamma once, and x, residual (read and
+    write) and out."""
     R = shape.R if rows is None else rows
     H, E, I, Is = shape.H, shape.E, shape.I, shape.Is
     per_expert = 3 * I * H // 2 + 3 * I * H // 32
-    return (distinct * per_expert + E * H * 2 + 3 * Is * H * 2 + H * 2 + R * H * 2 * 4)
+    return (distinct * per_expert + E * H * 2 + 3 * Is * H * 2 + H * 2 + R * H * 2 * 4
+            + (H * 2 if gated else 0))
