@@ -52,6 +52,8 @@ def _load():
         lib.oracle_moe_tail.restype = I
         lib.oracle_shared_gate.argtypes = [I, I, P, P, P]
         lib.oracle_shared_gate.restype = None
+        lib.oracle_out_proj.argtypes = [I, I, I, P, P, P]
+        lib.oracle_out_proj.restype = None
         lib.oracle_moe_tail_gated.argtypes = [I, I, I, I, I, I, D] + [P] * 16 + [I]
         lib.oracle_moe_tail_gated.restype = I
         _lib = lib
@@ -160,6 +162,19 @@ def shared(n_row, ws13, ws2):
     return ys, ms
 
 
+def out_proj(attn, w_o):
+    """Attention output projection: attn [R,Ha] bf16 bits, w_o [H,Ha] bf16 bits -> x [R,H]
+    bf16 bits."""
+    attn = _c(attn, np.uint16)
+    w_o = _c(w_o, np.uint16)
+    R, Ha = attn.shape
+    H = w_o.shape[0]
+    assert w_o.shape == (H, Ha)
+    x = np.empty((R, H), np.uint16)
+    _load().oracle_out_proj(R, Ha, H, _p(attn), _p(w_o), _p(x))
+    return x
+
+
 def shared_gate(n, g):
     """Per-row sigmoid gate of the shared expert: n [R,H] bf16 bits, g [H] bf16 bits ->
     [R] float64."""
@@ -174,13 +189,17 @@ def shared_gate(n, g):
 
 def moe_tail(inputs: dict, k: int, eps: float, nthreads: int = 1):
     """The whole tail.  `inputs` holds the arrays made by moe_layer_tail_gb300.inputs; an
-    optional "ws_gate" [H] (bf16 bits) gates the shared expert's output per row.
+    optional "ws_gate" [H] (bf16 bits) gates the shared expert's output per row; with
+    "w_o" [H,Ha] and "attn" [R,Ha] the input x is the projection out_proj(attn, w_o).
 
     Returns dict(out [R,H] bf16 bits, out_exact [R,H] float64 (before the bf16 rounding),
     residual [R,H] bf16 bits (r_new), ids [R,k], wts [R,k] float64, logits [R,E] float64).
     The caller's arrays are not modified.
     """
-    x = _c(inputs["x"], np.uint16)
+    if inputs.get("w_o") is not None:
+        x = out_proj(inputs["attn"], inputs["w_o"])
+    else:
+        x = _c(inputs["x"], np.uint16)
     res = np.array(inputs["residual"], dtype=np.uint16, copy=True, order="C")
     gamma = _c(inputs["gamma"], np.uint16)
     w_r = _c(inputs["w_r"], np.uint16)

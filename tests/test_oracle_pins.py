@@ -416,6 +416,45 @@ def test_closed_gate_removes_the_shared_expert():
     assert np.array_equal(a["out_exact"], b["out_exact"])
 
 
+# --------------------------------------------------- attention out_proj ----
+
+
+def test_out_proj_matches_numpy_dot():
+    rng = np.random.default_rng(30)
+    R, Ha, H = 3, 96, 64
+    attn = gen.to_bf16_bits(rng.standard_normal((R, Ha)))
+    w_o = gen.to_bf16_bits(rng.standard_normal((H, Ha)) / np.sqrt(Ha))
+    x = oracle.out_proj(attn, w_o)
+    want = bf16_decode(attn).reshape(R, Ha) @ bf16_decode(w_o).reshape(H, Ha).T
+    assert is_nearest_bf16(x, want, slack=1e-12).all()
+
+
+def test_out_proj_with_a_selection_matrix_copies_its_input():
+    # w_o = [identity | 0]: x is the first H columns of attn, bit for bit
+    rng = np.random.default_rng(31)
+    R, Ha, H = 4, 96, 64
+    attn = gen.to_bf16_bits(rng.standard_normal((R, Ha)))
+    w_o = np.zeros((H, Ha), np.uint16)
+    w_o[np.arange(H), np.arange(H)] = 0x3F80  # bf16 1.0
+    assert np.array_equal(oracle.out_proj(attn, w_o), attn[:, :H])
+
+
+def test_tail_from_attention_output_projects_first():
+    shape, d = _tail_inputs(32)
+    rng = np.random.default_rng(32)
+    Ha = 96
+    d2 = {k: v for k, v in d.items() if k != "x"}
+    d2["attn"] = gen.to_bf16_bits(rng.standard_normal((shape.R, Ha)))
+    d2["w_o"] = gen.to_bf16_bits(rng.standard_normal((shape.H, Ha)) / np.sqrt(Ha))
+    got = oracle.moe_tail(d2, shape.k, shape.eps)
+    d3 = dict(d)
+    d3["x"] = quantize_to_nearest_bf16_bits(
+        bf16_decode(d2["attn"]).reshape(shape.R, Ha) @ bf16_decode(d2["w_o"]).reshape(shape.H, Ha).T
+    ).reshape(shape.R, shape.H)
+    _, out_exact = _numpy_tail(d3, shape.k, shape.eps)
+    assert np.allclose(got["out_exact"], out_exact, rtol=1e-10, atol=1e-12)
+
+
 def test_oracle_is_deterministic_and_thread_count_invariant():
     shape, d = _tail_inputs(25, R=4, E=8, k=3)
     a = oracle.moe_tail(d, shape.k, shape.eps, nthreads=1)
