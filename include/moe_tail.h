@@ -104,6 +104,8 @@ typedef struct {
   int32_t mode;           /* MOE_TAIL_MODE_* */
   uint32_t wait_budget_us;/* budget of any device-side wait, microseconds; 0 = 100000 */
   uint32_t debug_flags;   /* 0 in production */
+  int32_t attn_dim;       /* Ha: 0, or a multiple of 64 up to 65536 to put the attention
+                           * output projection in front of the tail (moe_tail_run_attn) */
 } moe_tail_config_t;
 
 /* Weights are BORROWED device pointers: the caller keeps them alive and unmodified until
@@ -122,6 +124,10 @@ typedef struct {
    * Kernel Replacement row "shared expert gate, sigmoid and add").  Not available with
    * MOE_TAIL_DEBUG_FUSED_FRONT (refused at create). */
   const void* shared_gate;
+  /* bf16 [H, Ha] when attn_dim > 0 (else NULL): the attention output projection of
+   * moe_tail_run_attn ("[AMD] integrate kimi k3 monokernel" page, Kernel Replacement row 1,
+   * a bf16 GEMM in front of the post-attention norm). */
+  const void* out_proj;
 } moe_tail_weights_t;
 
 /* Validate the configuration and weights, allocate every scratch buffer the runs need on
@@ -141,6 +147,14 @@ int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weights_t* w,
  * Device-side failures are reported by moe_tail_get_status, not by this return value. */
 int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* out, int32_t rows,
                  void* stream);
+
+/* The same call with the attention output projection in front (handles created with
+ * attn_dim > 0; MOE_TAIL_ERR_UNSUPPORTED otherwise):
+ *   attn     bf16 [rows, Ha] device, read-only, 16-byte aligned
+ * x = bf16(attn . out_proj^T) (fp32 sums) is computed into the handle's scratch and the
+ * tail runs on it exactly as moe_tail_run(x, residual, out) would. */
+int moe_tail_run_attn(moe_tail_t* h, const void* attn, void* residual, void* out, int32_t rows,
+                      void* stream);
 
 /* The same call on HOST buffers: copies x and residual to the handle's device staging
  * buffers, runs, copies residual and out back, and synchronises `stream` before returning.

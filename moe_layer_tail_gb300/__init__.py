@@ -39,13 +39,13 @@ class Config(ctypes.Structure):
                 ("expert_inter", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
                 ("rms_eps", ctypes.c_float), ("norm_topk_prob", ctypes.c_int32),
                 ("mode", ctypes.c_int32), ("wait_budget_us", ctypes.c_uint32),
-                ("debug_flags", ctypes.c_uint32)]
+                ("debug_flags", ctypes.c_uint32), ("attn_dim", ctypes.c_int32)]
 
 
 class WeightPtrs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("gamma", "router_w", "w13_codes", "w13_scales", "w2_codes", "w2_scales",
-                 "shared_w13", "shared_w2", "shared_gate")]
+                 "shared_w13", "shared_w2", "shared_gate", "out_proj")]
 
 
 class MoeTailError(RuntimeError):
@@ -84,6 +84,8 @@ def load_library(path: str = None):
     lib.moe_tail_run.restype = ctypes.c_int
     lib.moe_tail_run_host.argtypes = [P, P, P, P, i32, P]
     lib.moe_tail_run_host.restype = ctypes.c_int
+    lib.moe_tail_run_attn.argtypes = [P, P, P, P, i32, P]
+    lib.moe_tail_run_attn.restype = ctypes.c_int
     lib.moe_tail_get_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.moe_tail_get_status.restype = ctypes.c_int
     lib.moe_tail_clear_status.argtypes = [P]
@@ -121,13 +123,14 @@ def make_config(shape, max_rows=None, mode=MODE_MULTI_KERNEL, wait_budget_us=0,
                   hidden=shape.H, n_experts=shape.E, top_k=shape.k, expert_inter=shape.I,
                   shared_inter=shape.Is, rms_eps=float(shape.eps), norm_topk_prob=1,
                   mode=int(mode), wait_budget_us=int(wait_budget_us),
-                  debug_flags=int(debug_flags))
+                  debug_flags=int(debug_flags), attn_dim=int(getattr(shape, "Ha", 0)))
 
 
 _WEIGHT_KEYS = {"gamma": "gamma", "router_w": "w_r", "w13_codes": "w13_codes",
                 "w13_scales": "w13_scales", "w2_codes": "w2_codes", "w2_scales": "w2_scales",
-                "shared_w13": "ws13", "shared_w2": "ws2", "shared_gate": "ws_gate"}
-_OPTIONAL_WEIGHTS = ("ws_gate",)  # absent: a null pointer
+                "shared_w13": "ws13", "shared_w2": "ws2", "shared_gate": "ws_gate",
+                "out_proj": "w_o"}
+_OPTIONAL_WEIGHTS = ("ws_gate", "w_o")  # absent: a null pointer
 
 
 class MoeTail:
@@ -160,6 +163,15 @@ class MoeTail:
                                     _stream_handle(stream))
         if rc != OK:
             raise MoeTailError(rc, "moe_tail_run")
+
+    def run_attn(self, attn, residual, out, rows: int = None, stream=None) -> None:
+        """The call with the attention output projection in front: attn bf16 [>= rows, Ha]
+        (the handle's shape has Ha > 0 and its weights a "w_o" [H, Ha])."""
+        rows = int(attn.shape[0] if rows is None else rows)
+        rc = self._lib.moe_tail_run_attn(self._h, _ptr(attn), _ptr(residual), _ptr(out), rows,
+                                         _stream_handle(stream))
+        if rc != OK:
+            raise MoeTailError(rc, "moe_tail_run_attn")
 
     def run_host(self, x, residual, out, rows: int = None, stream=None) -> None:
         """Same call on host (CPU) tensors: copies in, runs, copies back, synchronises."""

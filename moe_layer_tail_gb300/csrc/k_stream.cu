@@ -62,7 +62,7 @@ constexpr int kWinStages = kWinK / kChunkF4;
 constexpr int kWinW = 8192;       // weight scales of one window: 128 rows x 64 bytes
 constexpr int kSmemLimit = 232448;
 
-enum : int { kSharedGU = 0, kRoutedGU = 1, kSharedDN = 2, kRoutedDN = 3 };
+enum : int { kSharedGU = 0, kRoutedGU = 1, kSharedDN = 2, kRoutedDN = 3, kOutProj = 4 };
 
 struct Item {
   int kind;
@@ -85,8 +85,15 @@ struct Tables {
   const float* rscale;  // [R] per-row scale of the f16 gate/up activations
 };
 
+// Launches: 0 = gate/up, 1 = down, 2 = the attention out_proj in front of the tail.
 __device__ __forceinline__ int items_of(int phase, const Dims& dm, int D) {
-  return (phase == 0) ? dm.Is / 64 + D * (dm.I / 64) : dm.H / 128 + D * (dm.H / 128);
+  return (phase == 0) ? dm.Is / 64 + D * (dm.I / 64)
+         : (phase == 1) ? dm.H / 128 + D * (dm.H / 128)
+                        : dm.H / 128;
+}
+
+__device__ __forceinline__ int work_counter(int phase) {
+  return (phase == 0) ? kCtrGateUp : (phase == 1) ? kCtrDown : kCtrOutProj;
 }
 
 __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
@@ -118,6 +125,14 @@ __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
       it.U = s.off[d + 1] - it.u0;
       it.nst = (dm.H + kChunkF4 - 1) / kChunkF4;
     }
+  } else if (phase == 2) {
+    // out_proj: 128 rows of W_o (hidden outputs) against every row's attention output
+    it.kind = kOutProj;
+    it.K = dm.Ha;
+    it.out0 = item * 128;
+    it.row0 = it.out0;
+    it.U = dm.R;
+    it.nst = dm.Ha / kChunkBF;
   } else {
     const int ns = dm.H / 128;
     if (item < ns) {
@@ -479,6 +494,21 @@ __device__ __forceinline__ void finish_item(const Item& it, const float4* rb, in
                 __float2bfloat16_rn(silu_f(c[q]) * c[2 + q]);
         }
       }
+    } else if (it.kind == kOutProj) {
+      // x = bf16(attn . W_o^T): rows 16m + g and 16m + g + 8 of the 128-output box
+      for (int m = 0; m < 8; ++m) {
+        float c[4];
+        tile_sum(rb, nt_max, m, nt, lane, c);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int u = nt * 8 + 2 * t + q;
+          if (u < it.U) {
+            __nv_bfloat16* xr = s.xproj + (size_t)u * dm.H + it.out0;
+            xr[16 * m + g] = __float2bfloat16_rn(c[q]);
+            xr[16 * m + g + 8] = __float2bfloat16_rn(c[2 + q]);
+          }
+        }
+      }
     } else if (it.kind == kSharedDN || it.kind == kRoutedDN) {
       float* rows[2];
 #pragma unroll
@@ -580,7 +610,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
   // launched once every gate/up CTA has passed that wait (so the routing is complete), its
   // CTAs take the SMs the gate/up CTAs leave, and each down item waits, in its producer,
   // for the gate/up items whose output it reads (counted by their epilogues).
-  if (PHASE == 0) pdl_wait();
+  if (PHASE != 1) pdl_wait();
   const int D = min(max(*s.n_distinct, 1), kMaxPicks);
   const int n_items = items_of(PHASE, dm, D);
   for (int i = threadIdx.x; i < D; i += kStreamThreads) sp.t_uniq[i] = s.uniq[i];
@@ -626,10 +656,10 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
     uint32_t pend = 0u, pend_par = 0u;
     // failure-injection switch: CTA 0 leaves its first stage unpublished, so the consumers'
     // bounded wait on it expires (tests the timeout path; never set in production)
-    bool skip_first = (debug & kDebugStallFirstStage) && blockIdx.x == 0;
-    int item = (int)atomicAdd(&s.counters[PHASE], 1u);
+    bool skip_first = PHASE == 0 && (debug & kDebugStallFirstStage) && blockIdx.x == 0;
+    int item = (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
     while (ok && item < n_items) {
-      const int next = (int)atomicAdd(&s.counters[PHASE], 1u);  // lands while this streams
+      const int next = (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);  // lands while this streams
       const Item it = decode_item(PHASE, item, dm, tb, D);
       const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
       const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;  // down activation box height
@@ -685,6 +715,9 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
         } else if (it.kind == kRoutedDN) {
           tma_load_2d(st, &maps.w2, kc * (kChunkF4 / 2), it.row0, &sp.full[stage], pol);
           tma_load_2d(sa, &maps.mid16[hsel], kc * kChunkF4, it.u0, &sp.full[stage]);
+        } else if (it.kind == kOutProj) {
+          tma_load_2d(st, &maps.wo, kc * kChunkBF, it.row0, &sp.full[stage], pol);
+          tma_load_2d(sa, &maps.attn, kc * kChunkBF, 0, &sp.full[stage]);
         } else if (it.kind == kSharedGU) {
           tma_load_2d(st, &maps.ws13, kc * kChunkBF, it.row0, &sp.full[stage], pol);
           tma_load_2d(st + 8192, &maps.ws13, kc * kChunkBF, it.row1, &sp.full[stage], pol);
@@ -756,7 +789,7 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
       // count the item for its readers (the down items of the expert, or the combine of its
       // 128 outputs): the warp barrier orders every lane's stores before lane 0's release
       __syncwarp();
-      if (lane == 0) {
+      if (PHASE != 2 && lane == 0) {  // (the norm launch waits for out_proj as a whole)
         uint32_t* c = &s.counters[PHASE == 1 ? kCtrTileDone + it.out0 / 128
                                   : it.kind == kSharedGU ? kCtrSharedGUDone
                                                          : kCtrGUDone + it.d];
@@ -851,6 +884,9 @@ cudaError_t prepare_stream_kernels() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_stream<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemLimit);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_stream<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemLimit);
   return e;
 }
 
@@ -861,7 +897,12 @@ cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, cons
   if (phase == 0)
     return launch_k(k_stream<0>, dim3(num_sms), dim3(kStreamThreads), smem, st, pdl, maps, d, w,
                     s, budget_ns, debug);
-  return launch_k(k_stream<1>, dim3(num_sms), dim3(kStreamThreads), smem, st, pdl, maps, d, w, s,
+  if (phase == 1)
+    return launch_k(k_stream<1>, dim3(num_sms), dim3(kStreamThreads), smem, st, pdl, maps, d,
+                    w, s, budget_ns, debug);
+  // out_proj: H / 128 items, at most one per SM
+  const int grid = d.H / 128 < num_sms ? d.H / 128 : num_sms;
+  return launch_k(k_stream<2>, dim3(grid), dim3(kStreamThreads), smem, st, pdl, maps, d, w, s,
                   budget_ns, debug);
 }
 
@@ -908,13 +949,32 @@ StreamLayout make_stream_layout(int Rmax) {
 // Every weight box has 128-byte rows (the 128-byte swizzle span): 128 MXFP4 code bytes (256
 // elements) or 64 bf16 elements.  Returns 0 on success, -1 if the driver has no tensor-map
 // encoder, -2 if encoding failed.
+static EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+int make_attn_map(StreamMaps* m, const void* attn, int rows, const Dims& d) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return -1;
+  // rows past the call's are filled with zeros by the copy engine (their outputs unused)
+  if (encode_2d(enc, &m->attn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, attn, (uint64_t)d.Ha,
+                (uint64_t)rows, (uint64_t)d.Ha * 2, 64, (uint32_t)d.Rmax,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+    return -2;
+  return 0;
+}
+
 int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scratch& s) {
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                       &q) != cudaSuccess || fn == nullptr)
-    return -1;
-  EncodeTiledFn enc = (EncodeTiledFn)fn;
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return -1;
   const uint64_t H = d.H, E = d.E, I = d.I, Is = d.Is, R = d.Rmax, P = (uint64_t)d.Rmax * d.k;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -942,6 +1002,9 @@ int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scr
     return -2;
   if (I > (uint64_t)kWinK &&
       encode_2d(enc, &out->w2s, U8, w.w2s, I / 32, E * H, I / 32, 64, 128, NS))
+    return -2;
+  if (d.Ha > 0 &&
+      encode_2d(enc, &out->wo, BF, w.wo, (uint64_t)d.Ha, H, (uint64_t)d.Ha * 2, 64, 128, SW))
     return -2;
   out->lay = make_stream_layout(d.Rmax);
   return 0;

@@ -73,6 +73,8 @@ static int check_config(const moe_tail_config_t* c) {
   if (c->shared_inter < 64 || c->shared_inter % 64 || c->shared_inter > (1 << 16))
     return MOE_TAIL_ERR_UNSUPPORTED;
   if (!(c->rms_eps > 0.f)) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->attn_dim < 0 || c->attn_dim > (1 << 16) || c->attn_dim % 64)
+    return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->norm_topk_prob != 1) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->mode != MOE_TAIL_MODE_MULTI_KERNEL) return MOE_TAIL_ERR_UNSUPPORTED;
   return MOE_TAIL_OK;
@@ -107,6 +109,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
   s->y = (float*)take(P * H * 4);
   s->ys = (float*)take(R * H * 4);
   s->sgate = (float*)take(R * 4);
+  s->xproj = (__nv_bfloat16*)take(R * H * 2);
   s->status = (int32_t*)take(4);
   s->counters = (uint32_t*)take(kCtrWords * 4);
   return off;
@@ -124,6 +127,9 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return MOE_TAIL_ERR_INVALID_ARG;
   if (w->shared_gate && !aligned16(w->shared_gate)) return MOE_TAIL_ERR_INVALID_ARG;
+  // out_proj exactly when the configuration asks for it
+  if ((cfg->attn_dim > 0) != (w->out_proj != nullptr)) return MOE_TAIL_ERR_INVALID_ARG;
+  if (w->out_proj && !aligned16(w->out_proj)) return MOE_TAIL_ERR_INVALID_ARG;
   // the fused front computes n chunk by chunk across CTAs: it has no row-wide gate reduction
   if (w->shared_gate && (cfg->debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT))
     return MOE_TAIL_ERR_UNSUPPORTED;
@@ -141,6 +147,7 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   h->w.ws13 = (const __nv_bfloat16*)w->shared_w13;
   h->w.ws2 = (const __nv_bfloat16*)w->shared_w2;
   h->w.wsg = (const __nv_bfloat16*)w->shared_gate;
+  h->w.wo = (const __nv_bfloat16*)w->out_proj;
 
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = prepare_stream_kernels();
@@ -165,6 +172,7 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
     Dims d0;
     d0.R = cfg->max_rows; d0.Rmax = cfg->max_rows; d0.H = cfg->hidden; d0.E = cfg->n_experts;
     d0.k = cfg->top_k; d0.I = cfg->expert_inter; d0.Is = cfg->shared_inter; d0.eps = cfg->rms_eps;
+    d0.Ha = cfg->attn_dim;
     const int mrc = make_stream_maps(&h->maps, d0, h->w, h->s);
     if (mrc != 0) {
       cudaFree(h->slab);
@@ -200,11 +208,9 @@ extern "C" int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows) {
   return (h->cfg.debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT) ? 4 : 5;
 }
 
-extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* out,
-                            int32_t rows, void* stream) {
-  if (!h || !x || !residual || !out) return MOE_TAIL_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(residual) || !aligned16(out)) return MOE_TAIL_ERR_INVALID_ARG;
-  if (rows < 1 || rows > h->cfg.max_rows) return MOE_TAIL_ERR_INVALID_ARG;
+// One call: x is the tail's input, or null with attn the attention output to project first.
+static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residual, void* out,
+                    int32_t rows, void* stream) {
   cudaStream_t st = (cudaStream_t)stream;
   Dims d;
   d.R = rows;
@@ -214,6 +220,7 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
   d.k = h->cfg.top_k;
   d.I = h->cfg.expert_inter;
   d.Is = h->cfg.shared_inter;
+  d.Ha = h->cfg.attn_dim;
   d.eps = h->cfg.rms_eps;
   cudaError_t e;
   int stage_i = 0;
@@ -233,6 +240,16 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
   const bool simple = (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) != 0;
   const uint64_t budget_ns =
       (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
+  if (attn) {
+    // the attention output projection into scratch; the call's map of attn travels with
+    // the launch's parameters (a graph replays it as captured)
+    StreamMaps m = h->maps;
+    const int mrc = make_attn_map(&m, attn, rows, d);
+    if (mrc) return mrc == -1 ? cuda_fail(cudaErrorNotSupported) : MOE_TAIL_ERR_INVALID_ARG;
+    MT_STAGE(launch_stream(2, m, d, h->w, h->s, h->num_sms, budget_ns, st, pdl,
+                           h->cfg.debug_flags));
+    x = h->s.xproj;
+  }
   if (simple) {
     MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
                                 h->w, h->s, st, pdl));
@@ -259,6 +276,24 @@ extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* 
 #undef MT_STAGE
   h->last_rows = rows;
   return MOE_TAIL_OK;
+}
+
+extern "C" int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* out,
+                            int32_t rows, void* stream) {
+  if (!h || !x || !residual || !out) return MOE_TAIL_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(out)) return MOE_TAIL_ERR_INVALID_ARG;
+  if (rows < 1 || rows > h->cfg.max_rows) return MOE_TAIL_ERR_INVALID_ARG;
+  return run_impl(h, x, nullptr, residual, out, rows, stream);
+}
+
+extern "C" int moe_tail_run_attn(moe_tail_t* h, const void* attn, void* residual, void* out,
+                                 int32_t rows, void* stream) {
+  if (!h || !attn || !residual || !out) return MOE_TAIL_ERR_INVALID_ARG;
+  if (!aligned16(attn) || !aligned16(residual) || !aligned16(out))
+    return MOE_TAIL_ERR_INVALID_ARG;
+  if (rows < 1 || rows > h->cfg.max_rows) return MOE_TAIL_ERR_INVALID_ARG;
+  if (h->cfg.attn_dim <= 0) return MOE_TAIL_ERR_UNSUPPORTED;
+  return run_impl(h, nullptr, attn, residual, out, rows, stream);
 }
 
 extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host,

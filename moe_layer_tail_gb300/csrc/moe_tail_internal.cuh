@@ -31,6 +31,7 @@ struct Dims {
   int R;        // rows of this call
   int Rmax;     // rows the handle was created for (height of the activation boxes)
   int H, E, k, I, Is;
+  int Ha;       // attention out_proj K (0: none)
   float eps;
 };
 
@@ -44,6 +45,7 @@ struct Weights {
   const __nv_bfloat16* ws13;
   const __nv_bfloat16* ws2;
   const __nv_bfloat16* wsg;  // shared-expert gate [H], or null
+  const __nv_bfloat16* wo;   // attention out_proj [H, Ha], or null
 };
 
 // Every buffer a call needs, carved from one allocation made at create time.
@@ -69,6 +71,7 @@ struct Scratch {
   float* y;              // [Rmax*k, H] routed expert outputs
   float* ys;             // [Rmax, H] shared expert output
   float* sgate;          // [Rmax] sigmoid gate of the shared output (when a gate is given)
+  __nv_bfloat16* xproj;  // [Rmax, H] x = out_proj(attn) for moe_tail_run_attn
   int32_t* status;       // [1] sticky device status word
   uint32_t* counters;    // [kCtrWords] work counters, tickets and per-expert progress
 };
@@ -85,6 +88,8 @@ enum : int {
   kCtrGUDone = 16,       // [kMaxPicks] routed gate/up items finished, per distinct expert
   kCtrMidFlag = 16 + kMaxPicks,  // [kMaxPicks] nonzero: some 32-block of the expert's mid
                                  // carries a power-of-two scale
+  kCtrOutProj = 6,       // next work item of the out_proj launch (runs before the norm
+                         // launch, which zeroes it with the rest for the next call)
   kCtrTileDone = 16 + 2 * kMaxPicks,  // [256] down items finished per 128 hidden outputs
   kCtrWords = 16 + 2 * kMaxPicks + 256
 };
@@ -199,6 +204,8 @@ struct StreamMaps {
   CUtensorMap mid16s[3];  // f32 [Rmax*k, I/32], box {min(64, I/32), 4 / 8 / 16 rows}
   CUtensorMap w13s;       // u8 [E*2I, H/32], box {64 B, 64 rows} (H > 2048 only)
   CUtensorMap w2s;        // u8 [E*H, I/32], box {64 B, 128 rows} (I > 2048 only)
+  CUtensorMap wo;         // bf16 [H, Ha], box {64, 128}, 128-byte swizzle (Ha > 0 only)
+  CUtensorMap attn;       // bf16 [rows, Ha] of the call, box {64, Rmax}, 128-byte swizzle
   StreamLayout lay;
 };
 
@@ -219,6 +226,8 @@ cudaError_t launch_front_fused(const Dims& d, const __nv_bfloat16* x,
 cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch& s,
                                   int num_sms, cudaStream_t st);
 int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scratch& s);
+// The call's attention-output map (bf16 [rows, Ha] at attn): 0, or -1/-2 as make_stream_maps.
+int make_attn_map(StreamMaps* m, const void* attn, int rows, const Dims& d);
 StreamLayout make_stream_layout(int Rmax);
 cudaError_t prepare_stream_kernels();
 cudaError_t prepare_front_kernels();

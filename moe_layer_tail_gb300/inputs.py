@@ -46,6 +46,7 @@ class TailShape:
     I: int
     Is: int
     eps: float = 1e-6
+    Ha: int = 0  # attention output width in front of the tail (0: none)
 
 
 @dataclass(frozen=True)
@@ -111,8 +112,8 @@ def _codes(rng, shape):
 
 
 _WEIGHT_STREAMS = ("gamma", "w_r", "w13_codes", "w13_scales", "w2_codes", "w2_scales", "ws13",
-                   "ws2", "ws_gate")
-_LAYER_WEIGHTS = _WEIGHT_STREAMS[:-1]  # the shared-expert gate is optional
+                   "ws2", "ws_gate", "w_o")
+_LAYER_WEIGHTS = _WEIGHT_STREAMS[:-2]  # the shared-expert gate and out_proj are optional
 
 
 def make_weight(shape: TailShape, seed: int, key: str) -> np.ndarray:
@@ -137,6 +138,8 @@ def make_weight(shape: TailShape, seed: int, key: str) -> np.ndarray:
         return _normal_bf16(rng, (H, Is), 1.0 / math.sqrt(Is))
     if key == "ws_gate":  # logit n . g ~ N(0, 1) for normalised rows
         return _normal_bf16(rng, (H,), 1.0 / math.sqrt(H))
+    if key == "w_o":  # attention output projection [H, Ha]
+        return _normal_bf16(rng, (H, shape.Ha), 1.0 / math.sqrt(shape.Ha))
     raise KeyError(key)
 
 
@@ -168,6 +171,13 @@ def make_activations(shape: TailShape, seed: int, kind: str = "plain", c: float 
     return {"x": to_bf16_bits(x), "residual": to_bf16_bits(res)}
 
 
+def make_attention_output(shape: TailShape, seed: int, rows: int = None) -> np.ndarray:
+    """attn [rows, Ha] bf16 bits, N(0, 1): the input of the attention output projection."""
+    R = shape.R if rows is None else rows
+    rng = np.random.default_rng([seed, 3])
+    return to_bf16_bits(rng.standard_normal(size=(R, shape.Ha), dtype=np.float32))
+
+
 def make_inputs(name_or_wl, c: float = None) -> dict:
     wl = WORKLOADS[name_or_wl] if isinstance(name_or_wl, str) else name_or_wl
     d = make_weights(wl.shape, wl.seed)
@@ -176,12 +186,16 @@ def make_inputs(name_or_wl, c: float = None) -> dict:
 
 
 def algorithmic_bytes(shape: TailShape, distinct: int, rows: int = None,
-                      gated: bool = False) -> int:
+                      gated: bool = False, out_proj: bool = False) -> int:
     """Bytes one call must move: each distinct expert's MXFP4 codes and scales once, the bf16
     router, shared expert (and its gate vector), gamma once, and x, residual (read and
-    write) and out."""
+    write) and out; with out_proj, its [H, Ha] weights and the attention output instead of
+    x."""
     R = shape.R if rows is None else rows
     H, E, I, Is = shape.H, shape.E, shape.I, shape.Is
     per_expert = 3 * I * H // 2 + 3 * I * H // 32
-    return (distinct * per_expert + E * H * 2 + 3 * Is * H * 2 + H * 2 + R * H * 2 * 4
-            + (H * 2 if gated else 0))
+    b = (distinct * per_expert + E * H * 2 + 3 * Is * H * 2 + H * 2 + R * H * 2 * 4
+         + (H * 2 if gated else 0))
+    if out_proj:
+        b += H * shape.Ha * 2 + R * shape.Ha * 2 - R * H * 2
+    return b

@@ -59,7 +59,16 @@ def test_weight_struct_fields_match_header():
     body = re.search(r"typedef struct \{([^}]*)\} moe_tail_weights_t;", src).group(1)
     fields = re.findall(r"const void\*\s+(\w+);", body)
     assert [f for f, _ in mt.WeightPtrs._fields_] == fields
-    assert fields[-1] == "shared_gate"
+    assert fields[-2:] == ["shared_gate", "out_proj"]
+
+
+def test_config_struct_fields_match_header():
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "moe_tail.h")).read(),
+                 flags=re.S)
+    body = re.search(r"typedef struct \{([^}]*)\} moe_tail_config_t;", src).group(1)
+    fields = re.findall(r"(?:int32_t|uint32_t|float)\s+(\w+);", body)
+    assert [f for f, _ in mt.Config._fields_] == fields
+    assert fields[-1] == "attn_dim"
 
 
 def test_strerror_covers_codes(lib):
@@ -75,6 +84,7 @@ def test_null_arguments_rejected_without_device(lib):
     assert h.value is None
     assert lib.moe_tail_run(None, None, None, None, 1, None) == mt.ERR_INVALID_ARG
     assert lib.moe_tail_run_host(None, None, None, None, 1, None) == mt.ERR_INVALID_ARG
+    assert lib.moe_tail_run_attn(None, None, None, None, 1, None) == mt.ERR_INVALID_ARG
     assert lib.moe_tail_get_status(None, None) == mt.ERR_INVALID_ARG
     lib.moe_tail_destroy(None)
     assert lib.moe_tail_launches_per_run(None, 1) == 0
@@ -85,7 +95,9 @@ def test_null_arguments_rejected_without_device(lib):
                                          ("top_k", 9), ("expert_inter", 96),
                                          ("expert_inter", 2176),
                                          ("shared_inter", 100), ("norm_topk_prob", 0),
-                                         ("n_experts", 2000), ("rms_eps", 0.0)])
+                                         ("n_experts", 2000), ("rms_eps", 0.0),
+                                         ("attn_dim", -64), ("attn_dim", 100),
+                                         ("attn_dim", 65600)])
 def test_unsupported_configs_refused_before_device(lib, field, value):
     cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128))
     setattr(cfg, field, value)
@@ -102,6 +114,19 @@ def test_misaligned_weight_pointer_refused(lib):
     h = ctypes.c_void_p()
     assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
         mt.ERR_INVALID_ARG
+
+
+def test_out_proj_pointer_must_match_attn_dim(lib):
+    h = ctypes.c_void_p()
+    cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128, Ha=128))
+    w = mt.WeightPtrs(*([16] * 8))  # attn_dim > 0 but no out_proj
+    assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
+        mt.ERR_INVALID_ARG
+    cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128))
+    w = mt.WeightPtrs(*([16] * 8 + [0, 16]))  # out_proj given with attn_dim 0
+    assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
+        mt.ERR_INVALID_ARG
+    assert h.value is None
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

@@ -16,7 +16,7 @@ from moe_layer_tail_gb300 import (ERR_INVALID_ARG, ERR_UNSUPPORTED, STATUS_BAD_R
                                   MoeTailError, acts_to_device, bf16_tensor_to_bits,
                                   weights_to_device)
 from moe_layer_tail_gb300 import inputs as gen
-from parity import check_parity, inject_near_ties
+from parity import bf16_step, check_parity, inject_near_ties
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -196,6 +196,51 @@ def test_shared_expert_gate_refused_with_fused_front():
     dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
     with pytest.raises(MoeTailError) as ei:
         MoeTail(shape, dev, max_rows=shape.R, debug_flags=FUSED_FRONT)
+    assert ei.value.code == ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("flags", [0, SIMPLE, NO_PDL, FUSED_FRONT])
+@pytest.mark.parametrize("R,H,E,k,I,Is,Ha", [
+    (3, 512, 12, 3, 256, 192, 768),      # several K stages and output boxes
+    (8, 2560, 20, 4, 512, 256, 4096),    # long K, repeated experts
+    (16, 256, 16, 16, 128, 128, 64),     # one stage, maximum rows
+])
+def test_attention_out_proj(R, H, E, k, I, Is, Ha, flags):
+    shape = gen.TailShape(R, H, E, k, I, Is, Ha=Ha)
+    seed = 300 + R + E
+    d = gen.make_weights(shape, seed, keys=gen._LAYER_WEIGHTS + ("w_o",))
+    d.update(gen.make_activations(shape, seed))
+    d["attn"] = gen.make_attention_output(shape, seed)
+    orc = oracle.moe_tail(d, shape.k, shape.eps, nthreads=NTHREADS)
+    dev = weights_to_device({kk: v for kk, v in d.items() if kk not in ("x", "residual", "attn")})
+    tail = MoeTail(shape, dev, max_rows=R, debug_flags=flags)
+    attn = acts_to_device(d["attn"])
+    res = acts_to_device(d["residual"])
+    out = torch.empty_like(res)
+    tail.run_attn(attn, res, out)
+    torch.cuda.synchronize()
+    ids, wts, nd = tail.routing(R)
+    # x = bf16(attn . W_o^T) sums in fp32 here and in fp64 in the oracle: an element may round
+    # to the neighbouring bf16 value, and r_new = bf16(x + residual) with it
+    x_orc = oracle.out_proj(d["attn"], d["w_o"])
+    tol = bf16_step(x_orc) + bf16_step(orc["residual"])
+    figs = check_parity(bf16_tensor_to_bits(out), bf16_tensor_to_bits(res), ids, orc, shape.k,
+                        residual_tol=tol)
+    assert tail.status() == 0
+    # the same handle still runs the plain call (x given directly)
+    plain = oracle.moe_tail({kk: v for kk, v in d.items() if kk not in ("attn", "w_o")}, shape.k,
+                            shape.eps, nthreads=NTHREADS)
+    got = run_gpu(tail, d)
+    check_parity(got[0], got[1], got[2], plain, shape.k)
+
+
+def test_run_attn_needs_attn_dim():
+    shape, d = _small(310)
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    tail = MoeTail(shape, dev, max_rows=shape.R)
+    x = acts_to_device(d["x"])
+    with pytest.raises(MoeTailError) as ei:
+        tail.run_attn(x, x.clone(), torch.empty_like(x))
     assert ei.value.code == ERR_UNSUPPORTED
 
 
