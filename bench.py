@@ -51,6 +51,9 @@ def parse_args():
                    help="profiling aid: the workload with this many experts instead (a "
                         "smaller case of the same kernels, e.g. for an ncu capture); the "
                         "line's config says so")
+    p.add_argument("--out-proj", type=int, default=0, metavar="HA",
+                   help="the workload with an attention output projection of width HA in "
+                        "front (moe_tail_run_attn); the line's config says so (no e2e leg)")
     p.add_argument("--shared-gate", action="store_true",
                    help="the workload with the shared expert's sigmoid gate; the line's config "
                         "says so")
@@ -183,31 +186,37 @@ def run_ours(args, rank, world, local_rank):
     shape = wl.shape
     if args.experts:
         shape = dataclasses.replace(shape, E=args.experts)
+    if args.out_proj:
+        shape = dataclasses.replace(shape, Ha=args.out_proj)
     R = shape.R
     K, W = args.steps, args.warmup
     nsets = K + W
     host_w = gen.make_weights(shape, wl.seed)
     if args.shared_gate:
         host_w["ws_gate"] = gen.make_weight(shape, wl.seed, "ws_gate")
+    if args.out_proj:
+        host_w["w_o"] = gen.make_weight(shape, wl.seed, "w_o")
     dev_w = mt.weights_to_device(host_w)
     # one input set per step: correlated rows (~40% repeated picks), seeds wl.seed + 1000*i
     xs, rs = [], []
     c = gen.similar_c() if wl.kind == "similar" else None
     for i in range(nsets):
         a = gen.make_activations(shape, wl.seed + 1000 * i, wl.kind, c)
-        xs.append(a["x"])
+        xs.append(gen.make_attention_output(shape, wl.seed + 1000 * i) if args.out_proj
+                  else a["x"])
         rs.append(a["residual"])
-    x_all = mt.acts_to_device(np.stack(xs))
+    x_all = mt.acts_to_device(np.stack(xs))  # the attention outputs with --out-proj
     res0 = mt.acts_to_device(np.stack(rs))
     res = res0.clone()
-    out = torch.empty_like(x_all)
+    out = torch.empty_like(res0)
     tail = mt.MoeTail(shape, dev_w, max_rows=R)
-    nst = tail.launches_per_run(R)
+    nst = tail.launches_per_run(R) + (1 if args.out_proj else 0)
     stream = torch.cuda.current_stream()
+    call = tail.run_attn if args.out_proj else tail.run
 
     # warm-up
     for i in range(W):
-        tail.run(x_all[i], res[i], out[i])
+        call(x_all[i], res[i], out[i])
     torch.cuda.synchronize()
 
     # per-step stage events (recorded by the library around each launch, on our stream)
@@ -229,7 +238,7 @@ def run_ours(args, rank, world, local_rank):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(K):
-        tail.run(x_all[W + i], res[W + i], out[W + i], stream=stream)
+        call(x_all[W + i], res[W + i], out[W + i], stream=stream)
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -246,7 +255,7 @@ def run_ours(args, rank, world, local_rank):
     s0.record(stream)
     for i in range(K):
         tail.set_stage_events(ev_handles[i])
-        tail.run(x_all[W + i], res[W + i], out[W + i], stream=stream)
+        call(x_all[W + i], res[W + i], out[W + i], stream=stream)
     s1.record(stream)
     torch.cuda.synchronize()
     tail.set_stage_events(None)
@@ -260,18 +269,19 @@ def run_ours(args, rank, world, local_rank):
     Ds = []
     res_chk = res0.clone()
     for i in range(K):
-        tail.run(x_all[W + i], res_chk[W + i], out[W + i])
+        call(x_all[W + i], res_chk[W + i], out[W + i])
         _, _, nd = tail.routing(R)
         Ds.append(nd)
     Ds = np.array(Ds)
-    bytes_per = np.array([gen.algorithmic_bytes(shape, int(d), gated=args.shared_gate)
-                          for d in Ds])
+    bytes_per = np.array([gen.algorithmic_bytes(shape, int(d), gated=args.shared_gate,
+                                                 out_proj=bool(args.out_proj)) for d in Ds])
     total_bytes = float(bytes_per.sum())
     us_per_call = job_us_per_call(elapsed_ms, K, world)
     gbps = total_bytes * world / (elapsed_ms * 1e-3) / 1e9
 
     # dominant kernel: the stage with the largest total time
-    names = ["add_rmsnorm", "router_topk", "stream_gate_up", "stream_down", "combine"]
+    names = (["out_proj"] if args.out_proj else []) + ["add_rmsnorm", "router_topk",
+                                                       "stream_gate_up", "stream_down", "combine"]
     if nst != len(names):
         names = ["stage%d" % s for s in range(nst)]
     tot = stage_ms.sum(axis=0)
@@ -301,7 +311,8 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": wl.name + ("" if not args.experts else " with %d experts" % shape.E)
-                               + (" with shared-expert gate" if args.shared_gate else ""),
+                               + (" with shared-expert gate" if args.shared_gate else "")
+                               + (" with out_proj from %d" % shape.Ha if args.out_proj else ""),
                    "rows": R, "hidden": shape.H, "experts": shape.E,
                    "top_k": shape.k, "expert_inter": shape.I, "shared_inter": shape.Is,
                    "weights": "MXFP4 routed experts, bf16 router and shared expert",
@@ -322,7 +333,7 @@ def run_ours(args, rank, world, local_rank):
     }
 
     # end to end through the C ABI with host buffers (H2D/D2H inside the timed region)
-    if not args.no_e2e:
+    if not args.no_e2e and not args.out_proj:
         import torch as _t
         ke = min(K, 200)
         hx = [_t.from_numpy(xs[W + i].view(np.int16)).view(_t.bfloat16).pin_memory()
@@ -343,18 +354,19 @@ def run_ours(args, rank, world, local_rank):
                          "api": "moe_tail_run_host (pinned host x/residual in, out/residual back)"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(shape, host_w, xs[W], rs[W])
+        result["cpu_baseline"] = cpu_baseline(shape, host_w, xs[W], rs[W],
+                                              attn=bool(args.out_proj))
     tail.close()
     return result
 
 
-def cpu_baseline(shape, host_w, x, r, budget_s=20.0):
+def cpu_baseline(shape, host_w, x, r, budget_s=20.0, attn=False):
     """The oracle, as it stands, on the host cores: whole calls of the workload until the
-    budget is used (at least one)."""
+    budget is used (at least one).  attn: x is the attention output to project first."""
     import oracle
     cores = oracle.host_cores()
     d = dict(host_w)
-    d["x"] = x
+    d["attn" if attn else "x"] = x
     d["residual"] = r
     times = []
     t_start = time.perf_counter()

@@ -20,6 +20,12 @@
 
 namespace mtail {
 
+// Two floats -> two bf16 (round to nearest even) in a word, a in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+}
+
 // 2 bf16 in a word -> 2 bf16(a + b) in a word (fp32 add, round to nearest even).
 __device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
   __nv_bfloat16 lo = __float2bfloat16_rn(bf16_lo(a) + bf16_lo(b));
@@ -85,7 +91,8 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
               const __nv_bfloat16* __restrict__ gamma, __nv_bfloat16* __restrict__ rnew,
               __nv_bfloat16* __restrict__ n_out, __half* __restrict__ n16,
               float* __restrict__ n16s, uint32_t* __restrict__ counters, int H, float eps,
-              const __nv_bfloat16* __restrict__ wsg, float* __restrict__ sgate) {
+              const __nv_bfloat16* __restrict__ wsg, float* __restrict__ sgate,
+              const float* __restrict__ xpart, int Pk, size_t part_stride) {
   extern __shared__ uint4 s_gamma[];  // [H / 8]
   __shared__ float part[kNormThreads / 32];
   const int r = blockIdx.x;
@@ -104,7 +111,23 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   for (int q = 0; q < kNormGroups; ++q) {
     const int c = threadIdx.x + q * kNormThreads;
     if (c < ng) {
-      const uint4 xv = xr[c], rv = rr[c];
+      uint4 xv;
+      if (xpart) {  // x = bf16(the out_proj K parts added in part order)
+        const float* p0 = xpart + (size_t)r * H + 8 * (size_t)c;
+        float4 a = __ldcg(reinterpret_cast<const float4*>(p0));
+        float4 b = __ldcg(reinterpret_cast<const float4*>(p0) + 1);
+        for (int pp = 1; pp < Pk; ++pp) {
+          const float4* pq = reinterpret_cast<const float4*>(p0 + pp * part_stride);
+          const float4 a2 = __ldcg(pq), b2 = __ldcg(pq + 1);
+          a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
+          b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
+        }
+        xv = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                        pack_bf16x2(b.z, b.w));
+      } else {
+        xv = xr[c];
+      }
+      const uint4 rv = rr[c];
       rn[q] = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y), add_bf16x2(xv.z, rv.z),
                          add_bf16x2(xv.w, rv.w));
     } else {
@@ -165,10 +188,10 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
 
 cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
                                const __nv_bfloat16* residual, const Weights& w,
-                               const Scratch& s, cudaStream_t st, bool pdl) {
+                               const Scratch& s, cudaStream_t st, bool pdl, const float* xpart) {
   return launch_k(k_add_rmsnorm, dim3(d.R), dim3(kNormThreads), (size_t)d.H * 2, st, pdl, x,
                   residual, w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps, w.wsg,
-                  s.sgate);
+                  s.sgate, xpart, d.Pk, (size_t)d.Rmax * d.H);
 }
 
 // ------------------------------------------------------------------- router GEMV ----

@@ -69,7 +69,8 @@ struct Item {
   int d;           // routed: the expert's distinct slot (else -1)
   int row0, row1;  // tensor-map rows: gate (or single) box, up box
   int out0;        // first output index (j for gate/up, h for down)
-  int K, nst;
+  int k0, K, nst;  // first K element (out_proj parts), K elements and stages of the item
+  int part;        // out_proj: K part of its 128-output box
   int U, u0;
 };
 
@@ -89,7 +90,7 @@ struct Tables {
 __device__ __forceinline__ int items_of(int phase, const Dims& dm, int D) {
   return (phase == 0) ? dm.Is / 64 + D * (dm.I / 64)
          : (phase == 1) ? dm.H / 128 + D * (dm.H / 128)
-                        : dm.H / 128;
+                        : (dm.H / 128) * dm.Pk;
 }
 
 __device__ __forceinline__ int work_counter(int phase) {
@@ -102,6 +103,8 @@ __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
   it.u0 = 0;
   it.row1 = 0;
   it.d = -1;
+  it.k0 = 0;
+  it.part = 0;
   if (phase == 0) {
     const int ns = dm.Is / 64;
     it.K = dm.H;
@@ -126,13 +129,16 @@ __device__ __forceinline__ Item decode_item(int phase, int item, const Dims& dm,
       it.nst = (dm.H + kChunkF4 - 1) / kChunkF4;
     }
   } else if (phase == 2) {
-    // out_proj: 128 rows of W_o (hidden outputs) against every row's attention output
+    // out_proj: 128 rows of W_o (hidden outputs), one of Pk K parts, against every row's
+    // attention output
     it.kind = kOutProj;
-    it.K = dm.Ha;
-    it.out0 = item * 128;
+    it.part = item % dm.Pk;
+    it.K = dm.Ha / dm.Pk;  // a multiple of 64
+    it.k0 = it.part * it.K;
+    it.out0 = (item / dm.Pk) * 128;
     it.row0 = it.out0;
     it.U = dm.R;
-    it.nst = dm.Ha / kChunkBF;
+    it.nst = it.K / kChunkBF;
   } else {
     const int ns = dm.H / 128;
     if (item < ns) {
@@ -495,7 +501,8 @@ __device__ __forceinline__ void finish_item(const Item& it, const float4* rb, in
         }
       }
     } else if (it.kind == kOutProj) {
-      // x = bf16(attn . W_o^T): rows 16m + g and 16m + g + 8 of the 128-output box
+      // rows 16m + g and 16m + g + 8 of the 128-output box: x = bf16(attn . W_o^T) when the
+      // box is one part, else this part's fp32 sums (the norm launch adds the parts in order)
       for (int m = 0; m < 8; ++m) {
         float c[4];
         tile_sum(rb, nt_max, m, nt, lane, c);
@@ -503,9 +510,15 @@ __device__ __forceinline__ void finish_item(const Item& it, const float4* rb, in
         for (int q = 0; q < 2; ++q) {
           const int u = nt * 8 + 2 * t + q;
           if (u < it.U) {
-            __nv_bfloat16* xr = s.xproj + (size_t)u * dm.H + it.out0;
-            xr[16 * m + g] = __float2bfloat16_rn(c[q]);
-            xr[16 * m + g + 8] = __float2bfloat16_rn(c[2 + q]);
+            if (dm.Pk == 1) {
+              __nv_bfloat16* xr = s.xproj + (size_t)u * dm.H + it.out0;
+              xr[16 * m + g] = __float2bfloat16_rn(c[q]);
+              xr[16 * m + g + 8] = __float2bfloat16_rn(c[2 + q]);
+            } else {
+              float* xr = s.xpart + ((size_t)it.part * dm.Rmax + u) * dm.H + it.out0;
+              xr[16 * m + g] = c[q];
+              xr[16 * m + g + 8] = c[2 + q];
+            }
           }
         }
       }
@@ -716,8 +729,9 @@ k_stream(const __grid_constant__ StreamMaps maps, Dims dm, Weights w, Scratch s,
           tma_load_2d(st, &maps.w2, kc * (kChunkF4 / 2), it.row0, &sp.full[stage], pol);
           tma_load_2d(sa, &maps.mid16[hsel], kc * kChunkF4, it.u0, &sp.full[stage]);
         } else if (it.kind == kOutProj) {
-          tma_load_2d(st, &maps.wo, kc * kChunkBF, it.row0, &sp.full[stage], pol);
-          tma_load_2d(sa, &maps.attn, kc * kChunkBF, 0, &sp.full[stage]);
+          const int x = it.k0 + kc * kChunkBF;
+          tma_load_2d(st, &maps.wo, x, it.row0, &sp.full[stage], pol);
+          tma_load_2d(sa, &maps.attn, x, 0, &sp.full[stage]);
         } else if (it.kind == kSharedGU) {
           tma_load_2d(st, &maps.ws13, kc * kChunkBF, it.row0, &sp.full[stage], pol);
           tma_load_2d(st + 8192, &maps.ws13, kc * kChunkBF, it.row1, &sp.full[stage], pol);

@@ -110,6 +110,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
   s->ys = (float*)take(R * H * 4);
   s->sgate = (float*)take(R * 4);
   s->xproj = (__nv_bfloat16*)take(R * H * 2);
+  s->xpart = (float*)take((size_t)kMaxOutProjParts * R * H * 4);
   s->status = (int32_t*)take(4);
   s->counters = (uint32_t*)take(kCtrWords * 4);
   return off;
@@ -173,6 +174,7 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
     d0.R = cfg->max_rows; d0.Rmax = cfg->max_rows; d0.H = cfg->hidden; d0.E = cfg->n_experts;
     d0.k = cfg->top_k; d0.I = cfg->expert_inter; d0.Is = cfg->shared_inter; d0.eps = cfg->rms_eps;
     d0.Ha = cfg->attn_dim;
+    d0.Pk = 1;
     const int mrc = make_stream_maps(&h->maps, d0, h->w, h->s);
     if (mrc != 0) {
       cudaFree(h->slab);
@@ -221,6 +223,7 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   d.I = h->cfg.expert_inter;
   d.Is = h->cfg.shared_inter;
   d.Ha = h->cfg.attn_dim;
+  d.Pk = 1;
   d.eps = h->cfg.rms_eps;
   cudaError_t e;
   int stage_i = 0;
@@ -240,19 +243,27 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   const bool simple = (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) != 0;
   const uint64_t budget_ns =
       (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
+  const float* xpart = nullptr;
   if (attn) {
     // the attention output projection into scratch; the call's map of attn travels with
-    // the launch's parameters (a graph replays it as captured)
+    // the launch's parameters (a graph replays it as captured).  Each 128-output box is
+    // split along K into up to 8 parts (while the items stay within two per SM), whose
+    // fp32 sums the norm launch adds in part order; the fused front reads x whole.
     StreamMaps m = h->maps;
     const int mrc = make_attn_map(&m, attn, rows, d);
     if (mrc) return mrc == -1 ? cuda_fail(cudaErrorNotSupported) : MOE_TAIL_ERR_INVALID_ARG;
+    int pk = kMaxOutProjParts;
+    while (pk > 1 && ((d.Ha / 64) % pk != 0 || (d.H / 128) * pk > 2 * h->num_sms)) pk >>= 1;
+    if (h->cfg.debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT) pk = 1;
+    d.Pk = pk;
     MT_STAGE(launch_stream(2, m, d, h->w, h->s, h->num_sms, budget_ns, st, pdl,
                            h->cfg.debug_flags));
     x = h->s.xproj;
+    if (pk > 1) xpart = h->s.xpart;
   }
   if (simple) {
     MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
-                                h->w, h->s, st, pdl));
+                                h->w, h->s, st, pdl, xpart));
     MT_STAGE(launch_router(d, h->w, h->s, st, pdl));
     MT_STAGE(launch_topk_dedup(d, h->s, st, pdl));
     MT_STAGE(launch_experts_simple(d, h->w, h->s, h->num_sms, st));
@@ -262,7 +273,7 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
                                   h->w, h->s, st, pdl));
     } else {
       MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
-                                  h->w, h->s, st, pdl));
+                                  h->w, h->s, st, pdl, xpart));
       MT_STAGE(launch_router_topk(d, h->w, h->s, st, pdl));
     }
     const uint32_t dbg = h->cfg.debug_flags;

@@ -17,6 +17,7 @@ constexpr int kMaxRows = 16;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxPicks = kMaxRows * kMaxTopK;  // (row, slot) pairs of one call
+constexpr int kMaxOutProjParts = 8;  // K parts of an out_proj box at most
 
 // Device status word bits (sticky; read by moe_tail_get_status; the same values as
 // MOE_TAIL_STATUS_* in moe_tail.h).
@@ -32,6 +33,7 @@ struct Dims {
   int Rmax;     // rows the handle was created for (height of the activation boxes)
   int H, E, k, I, Is;
   int Ha;       // attention out_proj K (0: none)
+  int Pk;       // K parts of an out_proj box (1: the launch writes x itself)
   float eps;
 };
 
@@ -71,7 +73,8 @@ struct Scratch {
   float* y;              // [Rmax*k, H] routed expert outputs
   float* ys;             // [Rmax, H] shared expert output
   float* sgate;          // [Rmax] sigmoid gate of the shared output (when a gate is given)
-  __nv_bfloat16* xproj;  // [Rmax, H] x = out_proj(attn) for moe_tail_run_attn
+  __nv_bfloat16* xproj;  // [Rmax, H] x = out_proj(attn) for moe_tail_run_attn (one K part)
+  float* xpart;          // [kMaxOutProjParts, Rmax, H] fp32 sums of each out_proj K part
   int32_t* status;       // [1] sticky device status word
   uint32_t* counters;    // [kCtrWords] work counters, tickets and per-expert progress
 };
@@ -214,7 +217,8 @@ struct StreamMaps {
 
 cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
                                const __nv_bfloat16* residual, const Weights& w,
-                               const Scratch& s, cudaStream_t st, bool pdl);
+                               const Scratch& s, cudaStream_t st, bool pdl,
+                               const float* xpart = nullptr);
 cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cudaStream_t st,
                           bool pdl);
 cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, bool pdl);
