@@ -914,8 +914,9 @@ cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, cons
   if (phase == 1)
     return launch_k(k_stream<1>, dim3(num_sms), dim3(kStreamThreads), smem, st, pdl, maps, d,
                     w, s, budget_ns, debug);
-  // out_proj: H / 128 items, at most one per SM
-  const int grid = d.H / 128 < num_sms ? d.H / 128 : num_sms;
+  // out_proj: (H / 128) x Pk items, one CTA per item up to one per SM
+  const int items = d.H / 128 * d.Pk;
+  const int grid = items < num_sms ? items : num_sms;
   return launch_k(k_stream<2>, dim3(grid), dim3(kStreamThreads), smem, st, pdl, maps, d, w, s,
                   budget_ns, debug);
 }

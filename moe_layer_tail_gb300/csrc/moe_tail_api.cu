@@ -247,14 +247,23 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   if (attn) {
     // the attention output projection into scratch; the call's map of attn travels with
     // the launch's parameters (a graph replays it as captured).  Each 128-output box is
-    // split along K into up to 8 parts (while the items stay within two per SM), whose
-    // fp32 sums the norm launch adds in part order; the fused front reads x whole.
+    // split along K into 1, 2, 4 or 8 parts, whose fp32 sums the norm launch adds in part
+    // order; the count taken is the one whose busiest CTA streams the fewest K columns
+    // (ceil(items / SMs) items of Ha / parts columns; ties keep the smaller count).  The
+    // fused front reads x whole, so it takes one part.
     StreamMaps m = h->maps;
     const int mrc = make_attn_map(&m, attn, rows, d);
     if (mrc) return mrc == -1 ? cuda_fail(cudaErrorNotSupported) : MOE_TAIL_ERR_INVALID_ARG;
-    int pk = kMaxOutProjParts;
-    while (pk > 1 && ((d.Ha / 64) % pk != 0 || (d.H / 128) * pk > 2 * h->num_sms)) pk >>= 1;
-    if (h->cfg.debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT) pk = 1;
+    int pk = 1;
+    if (!(h->cfg.debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT)) {
+      const long boxes = d.H / 128;
+      long best = -1;
+      for (int p = 1; p <= kMaxOutProjParts; p <<= 1) {
+        if ((d.Ha / 64) % p) continue;
+        const long cols = (boxes * p + h->num_sms - 1) / h->num_sms * (d.Ha / p);
+        if (best < 0 || cols < best) { best = cols; pk = p; }
+      }
+    }
     d.Pk = pk;
     MT_STAGE(launch_stream(2, m, d, h->w, h->s, h->num_sms, budget_ns, st, pdl,
                            h->cfg.debug_flags));

@@ -204,6 +204,8 @@ def test_shared_expert_gate_refused_with_fused_front():
     (3, 512, 12, 3, 256, 192, 768),      # several K stages and output boxes
     (8, 2560, 20, 4, 512, 256, 4096),    # long K, repeated experts
     (16, 256, 16, 16, 128, 128, 64),     # one stage, maximum rows
+    (4, 1024, 16, 4, 256, 128, 512),     # eight K parts per box
+    (2, 768, 8, 2, 128, 128, 128),       # two K parts per box
 ])
 def test_attention_out_proj(R, H, E, k, I, Is, Ha, flags):
     shape = gen.TailShape(R, H, E, k, I, Is, Ha=Ha)
