@@ -185,6 +185,68 @@ def make_inputs(name_or_wl, c: float = None) -> dict:
     return d
 
 
+# ------------------------------------------ second workload: the AttnRes residual mix ----
+#
+# A decoder runs the mix once per sublayer: L calls on the same R rows, each adding its
+# sublayer's output into the running sum of the current block (the prefix) and mixing the
+# committed blocks with that prefix.  Block 0 (the embedding) is committed before the first
+# call and the prefix starts at zero; every `block_calls` calls the last call of a block
+# commits its prefix as the next block.  Recipe per family:
+#   "unit"    sublayer outputs and the embedding N(0, 1)
+#   "scaled"  the same, each (call, row) scaled by 2^u, u uniform in {0, ..., 11}, so rows
+#             reach magnitudes of a few thousand
+#   both      query q_l [H] N(0, 1/sqrt(H)) (source scores ~ N(0, 1)), gamma_l 1 + N(0, 0.1)
+
+
+@dataclass(frozen=True)
+class MixSequence:
+    R: int
+    H: int = 7168
+    L: int = 187
+    block_calls: int = 24
+    eps: float = 1e-6
+
+    def n_blocks(self, call: int) -> int:
+        """Committed blocks before call `call` (0-based)."""
+        return 1 + call // self.block_calls
+
+    def commit(self, call: int) -> bool:
+        return (call + 1) % self.block_calls == 0
+
+    @property
+    def max_blocks(self) -> int:
+        """Blocks the buffer must hold: the committed ones plus the last call's commit."""
+        last = self.L - 1
+        return self.n_blocks(last) + (1 if self.commit(last) else 0)
+
+
+def make_mix_sequence(seq: MixSequence, seed: int, family: str = "unit") -> dict:
+    """sub [L,R,H], q [L,H], gamma [L,H], blocks [max_blocks,R,H] (block 0 the embedding,
+    the rest zero) and prefix [R,H] (zero), all bf16 bits."""
+    L, R, H = seq.L, seq.R, seq.H
+    rng = np.random.default_rng([seed, 4])
+    sub = rng.standard_normal(size=(L, R, H), dtype=np.float32)
+    emb = rng.standard_normal(size=(R, H), dtype=np.float32)
+    if family == "scaled":
+        u = rng.integers(0, 12, size=(L, R, 1))
+        sub = sub * np.exp2(u).astype(np.float32)
+    elif family != "unit":
+        raise ValueError(family)
+    q = rng.standard_normal(size=(L, H), dtype=np.float32) * np.float32(1.0 / math.sqrt(H))
+    gamma = np.float32(1.0) + rng.standard_normal(size=(L, H), dtype=np.float32) * np.float32(0.1)
+    blocks = np.zeros((seq.max_blocks, R, H), np.uint16)
+    blocks[0] = to_bf16_bits(emb)
+    return {"sub": to_bf16_bits(sub), "q": to_bf16_bits(q), "gamma": to_bf16_bits(gamma),
+            "blocks": blocks, "prefix": np.zeros((R, H), np.uint16)}
+
+
+def mix_call_bytes(R: int, H: int, n_blocks: int, commit: bool) -> int:
+    """Bytes one mix call must move: the committed sources, the prefix and the sublayer
+    output read, q and gamma read, the prefix (and on a commit the new block) written, the
+    mixture and the normalised output written."""
+    return 2 * (n_blocks * R * H + 2 * R * H + 2 * H + (2 if commit else 1) * R * H + 2 * R * H)
+
+
 def algorithmic_bytes(shape: TailShape, distinct: int, rows: int = None,
                       gated: bool = False, out_proj: bool = False) -> int:
     """Bytes one call must move: each distinct expert's MXFP4 codes and scales once, the bf16

@@ -56,6 +56,8 @@ def _load():
         lib.oracle_out_proj.restype = None
         lib.oracle_moe_tail_gated.argtypes = [I, I, I, I, I, I, D] + [P] * 16 + [I]
         lib.oracle_moe_tail_gated.restype = I
+        lib.oracle_attnres_mix.argtypes = [I, I, I, I, D] + [P] * 9
+        lib.oracle_attnres_mix.restype = I
         _lib = lib
     return _lib
 
@@ -226,6 +228,37 @@ def moe_tail(inputs: dict, k: int, eps: float, nthreads: int = 1):
     if rc != 0:
         raise ValueError("oracle_moe_tail rejected the shapes (rc=%d)" % rc)
     return dict(out=out, out_exact=exact, residual=res, ids=ids, wts=wts, logits=logits)
+
+
+def attnres_mix(sub, prefix, blocks, n_blocks: int, commit: bool, q, gamma, eps: float):
+    """One call of the AttnRes residual mix + RMSNorm for R rows.
+
+    sub, prefix [R,H] bf16 bits; blocks [B,R,H] bf16 bits with B > n_blocks when commit
+    (blocks 0 .. n_blocks-1 are the committed sources); q, gamma [H] bf16 bits.
+    Returns dict(prefix [R,H] (zero after a commit), blocks (block n_blocks holds the
+    committed prefix after a commit), mix [R,H], y [R,H], alpha [R,S], score [R,S]) with
+    S = n_blocks + 1; the caller's arrays are not modified.
+    """
+    sub = _c(sub, np.uint16)
+    pre = np.array(prefix, dtype=np.uint16, copy=True, order="C")
+    blk = np.array(blocks, dtype=np.uint16, copy=True, order="C")
+    q = _c(q, np.uint16)
+    gamma = _c(gamma, np.uint16)
+    R, H = sub.shape
+    assert pre.shape == (R, H) and q.shape == (H,) and gamma.shape == (H,)
+    assert blk.ndim == 3 and blk.shape[1:] == (R, H)
+    assert blk.shape[0] >= n_blocks + (1 if commit else 0)
+    S = n_blocks + 1
+    mix = np.empty((R, H), np.uint16)
+    y = np.empty((R, H), np.uint16)
+    alpha = np.empty((R, S), np.float64)
+    score = np.empty((R, S), np.float64)
+    rc = _load().oracle_attnres_mix(R, H, int(n_blocks), int(bool(commit)), float(eps),
+                                    _p(sub), _p(pre), _p(blk), _p(q), _p(gamma), _p(mix),
+                                    _p(y), _p(alpha), _p(score))
+    if rc != 0:
+        raise ValueError("oracle_attnres_mix rejected the shapes (rc=%d)" % rc)
+    return dict(prefix=pre, blocks=blk, mix=mix, y=y, alpha=alpha, score=score)
 
 
 def bf16_bits_to_f64(a):

@@ -18,6 +18,9 @@
  *     reduction, ties go to the lowest id and the pick order is unchanged; row 10: the
  *     router activations are stored as bf16 before the GEMV.
  *   - OCP MXFP4: 32-element blocks of E2M1 codes that share one E8M0 scale 2^(s-127).
+ *   - "Split the Kimi3 AttnRes mix across CTAs for decode rows" (voipmonitor/flare #11):
+ *     the second workload, one call of the AttnRes residual mix + RMSNorm
+ *     (oracle_attnres_mix at the end of this file, with its own readings).
  *
  * Arithmetic: every sum and product is in double precision.  The only roundings are the
  * bf16 storage points a real layer has (the new residual, the normalised activations, the
@@ -406,4 +409,94 @@ int oracle_moe_tail(int R, int H, int E, int k, int I, int Is, double eps,
   return oracle_moe_tail_gated(R, H, E, k, I, Is, eps, x, residual_io, gamma, w_r, w13_codes,
                                w13_scales, w2_codes, w2_scales, ws13, ws2, NULL, out, ids_out,
                                wts_out, logits_out, out_exact, nthreads);
+}
+
+/* ------------------------------ second workload: AttnRes residual mix + RMSNorm ---- */
+
+/* "Split the Kimi3 AttnRes mix across CTAs for decode rows" (voipmonitor/flare #11),
+ * Description and commit message: one call of the mix adds the sublayer output into the
+ * current block's running sum (the prefix), commits a finished block, mixes the block
+ * sources with softmax weights from per-source dot and square-sum reductions, and applies
+ * the RMSNorm to the mixture.  The page gives no formulas; the readings taken here are:
+ *   - prefix' = bf16(prefix + sub), one rounding of the exact sum;
+ *   - the sources of row r, in this order, are the committed blocks 0 .. n_blocks-1 of the
+ *     row and prefix';
+ *   - a commit stores prefix' as block n_blocks and leaves the prefix at zero; the mixture
+ *     of that call is over the same sources (the block just stored is prefix');
+ *   - score_i = (q . v_i) / sqrt(mean(v_i^2) + eps): one learned query vector q [H]
+ *     against each source RMS-normalised without a weight; alpha = softmax(score);
+ *   - mix = bf16(sum_i alpha_i v_i); y = bf16(mix * rstd(mix) * gamma) with
+ *     rstd(mix) = 1 / sqrt(mean(mix^2) + eps) of the bf16 mixture (the layer's input norm).
+ * Layouts (bf16 bits): sub, prefix_io, mix, y [R, H]; blocks [n_blocks + 1, R, H], block b
+ * of row r at (b * R + r) * H, block n_blocks written only on a commit; q, gamma [H].
+ * alpha_out [R, n_blocks + 1] and score_out [R, n_blocks + 1] may be NULL.
+ * Returns 0, or -1 for shapes it does not take. */
+int oracle_attnres_mix(int R, int H, int n_blocks, int commit, double eps,
+                       const uint16_t* sub, uint16_t* prefix_io, uint16_t* blocks,
+                       const uint16_t* q, const uint16_t* gamma, uint16_t* mix, uint16_t* y,
+                       double* alpha_out, double* score_out) {
+  if (R < 1 || H < 1 || n_blocks < 0) return -1;
+  const int S = n_blocks + 1;
+  uint16_t* pnew = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
+  double* score = (double*)malloc(sizeof(double) * (size_t)S);
+  double* alpha = (double*)malloc(sizeof(double) * (size_t)S);
+  double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+  for (int r = 0; r < R; ++r) {
+    const uint16_t* o = sub + (int64_t)r * H;
+    uint16_t* p = prefix_io + (int64_t)r * H;
+    /* residual add */
+    for (int h = 0; h < H; ++h)
+      pnew[h] = oracle_bf16_round(oracle_bf16_to_double(p[h]) + oracle_bf16_to_double(o[h]));
+    /* scores of the sources against q */
+    for (int i = 0; i < S; ++i) {
+      const uint16_t* v = i < n_blocks ? blocks + ((int64_t)i * R + r) * H : pnew;
+      double ss = 0.0, dot = 0.0;
+      for (int h = 0; h < H; ++h) {
+        const double vh = oracle_bf16_to_double(v[h]);
+        ss += vh * vh;
+        dot += oracle_bf16_to_double(q[h]) * vh;
+      }
+      score[i] = dot / sqrt(ss / H + eps);
+    }
+    /* softmax over the sources */
+    double mx = score[0];
+    for (int i = 1; i < S; ++i)
+      if (score[i] > mx) mx = score[i];
+    double den = 0.0;
+    for (int i = 0; i < S; ++i) {
+      alpha[i] = exp(score[i] - mx);
+      den += alpha[i];
+    }
+    for (int i = 0; i < S; ++i) alpha[i] /= den;
+    /* mixture of the sources, then the RMSNorm of the bf16 mixture */
+    for (int h = 0; h < H; ++h) acc[h] = 0.0;
+    for (int i = 0; i < S; ++i) {
+      const uint16_t* v = i < n_blocks ? blocks + ((int64_t)i * R + r) * H : pnew;
+      for (int h = 0; h < H; ++h) acc[h] += alpha[i] * oracle_bf16_to_double(v[h]);
+    }
+    double ssm = 0.0;
+    for (int h = 0; h < H; ++h) {
+      const uint16_t b = oracle_bf16_round(acc[h]);
+      mix[(int64_t)r * H + h] = b;
+      const double m = oracle_bf16_to_double(b);
+      ssm += m * m;
+    }
+    const double rstd = 1.0 / sqrt(ssm / H + eps);
+    for (int h = 0; h < H; ++h)
+      y[(int64_t)r * H + h] = oracle_bf16_round(
+          oracle_bf16_to_double(mix[(int64_t)r * H + h]) * rstd * oracle_bf16_to_double(gamma[h]));
+    /* commit, or keep the running sum */
+    if (commit) {
+      memcpy(blocks + ((int64_t)n_blocks * R + r) * H, pnew, sizeof(uint16_t) * (size_t)H);
+      memset(p, 0, sizeof(uint16_t) * (size_t)H);
+    } else {
+      memcpy(p, pnew, sizeof(uint16_t) * (size_t)H);
+    }
+    for (int i = 0; i < S; ++i) {
+      if (alpha_out) alpha_out[(int64_t)r * S + i] = alpha[i];
+      if (score_out) score_out[(int64_t)r * S + i] = score[i];
+    }
+  }
+  free(pnew); free(score); free(alpha); free(acc);
+  return 0;
 }

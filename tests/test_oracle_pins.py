@@ -473,3 +473,154 @@ def test_tiny_workload_runs_and_inputs_are_reproducible():
     got = oracle.moe_tail(d1, wl.shape.k, wl.shape.eps)
     assert got["out"].shape == (1, 256)
     assert np.isfinite(bf16_decode(got["out"])).all()
+
+
+# ------------------------------------------------ AttnRes residual mix (second workload) ----
+
+def _mix_inputs(R, H, n_blocks, seed, B=None):
+    rng = np.random.default_rng([seed, 77])
+
+    def bits(shape, std=1.0):
+        return gen.to_bf16_bits(rng.standard_normal(size=shape).astype(np.float32) * std)
+
+    B = n_blocks + 1 if B is None else B
+    blocks = np.zeros((B, R, H), np.uint16)
+    blocks[:n_blocks] = bits((n_blocks, R, H))
+    return dict(sub=bits((R, H)), prefix=bits((R, H)), blocks=blocks,
+                q=bits((H,), 1.0 / math.sqrt(H)),
+                gamma=gen.to_bf16_bits(1.0 + 0.1 * rng.standard_normal(size=H).astype(np.float32)))
+
+
+def _mix(d, n_blocks, commit=False, eps=1e-6):
+    return oracle.attnres_mix(d["sub"], d["prefix"], d["blocks"], n_blocks, commit, d["q"],
+                              d["gamma"], eps)
+
+
+def test_mix_with_no_committed_block_is_the_plain_add_rmsnorm():
+    d = _mix_inputs(3, 256, 0, 1)
+    m = _mix(d, 0)
+    r_new, n, _ = oracle.add_rmsnorm(d["sub"], d["prefix"], d["gamma"], 1e-6)
+    assert np.all(m["alpha"] == 1.0)
+    assert np.array_equal(m["prefix"], r_new)
+    assert np.array_equal(m["mix"], r_new)
+    assert np.array_equal(m["y"], n)
+
+
+def test_mix_residual_add_is_the_float32_sum_rounded_once():
+    d = _mix_inputs(4, 512, 2, 2)
+    m = _mix(d, 2)
+    t = (torch.from_numpy(bf16_decode(d["prefix"]).astype(np.float32))
+         + torch.from_numpy(bf16_decode(d["sub"]).astype(np.float32))).to(torch.bfloat16)
+    assert np.array_equal(m["prefix"], t.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(m["blocks"], d["blocks"])  # no commit: the blocks stay
+
+
+def test_mix_zero_query_gives_the_plain_mean():
+    R, H, nb = 2, 128, 3
+    d = _mix_inputs(R, H, nb, 3)
+    d["q"] = np.zeros(H, np.uint16)
+    m = _mix(d, nb)
+    assert np.all(m["alpha"] == 0.25)
+    pnew = bf16_decode(m["prefix"])
+    srcs = np.concatenate([bf16_decode(d["blocks"][:nb]), pnew[None]], axis=0)
+    mean = srcs.sum(axis=0) / 4.0  # exact: four bf16 values of N(0, 1) data
+    assert np.array_equal(m["mix"], quantize_to_nearest_bf16_bits(mean.ravel()).reshape(R, H))
+
+
+def test_mix_scores_and_weights_match_closed_forms():
+    # source i = c_i * (a pattern of +-1 with a_i plus signs), q = 1/8 everywhere:
+    # q . v_i = c_i (2 a_i - H) / 8 and mean(v_i^2) = c_i^2, so
+    # score_i = c_i (2 a_i - H) / 8 / sqrt(c_i^2 + eps) and alpha = softmax(score)
+    H, eps = 64, 1e-3
+    c = [1.0, 0.25, 2.0 ** -5, 4.0]
+    a = [40, 20, 64, 31]
+    nb = len(c) - 1
+    blocks = np.zeros((nb + 1, 1, H), np.uint16)
+    pats = []
+    for i in range(len(c)):
+        pat = -np.ones(H)
+        pat[:a[i]] = 1.0
+        np.random.default_rng(i).shuffle(pat)
+        pats.append(c[i] * pat)
+    for i in range(nb):
+        blocks[i, 0] = gen.to_bf16_bits(pats[i])
+    d = dict(sub=np.zeros((1, H), np.uint16), prefix=gen.to_bf16_bits(pats[nb])[None],
+             blocks=blocks, q=gen.to_bf16_bits(np.full(H, 0.125)),
+             gamma=gen.to_bf16_bits(np.ones(H)))
+    m = _mix(d, nb, eps=eps)
+    score = np.array([c[i] * (2 * a[i] - H) / 8.0 / math.sqrt(c[i] ** 2 + eps)
+                      for i in range(len(c))])
+    np.testing.assert_allclose(m["score"][0], score, rtol=1e-13, atol=0)
+    np.testing.assert_allclose(m["alpha"][0], scipy.special.softmax(score), rtol=1e-13, atol=0)
+
+
+def test_mix_scores_ignore_a_source_scale():
+    d = _mix_inputs(2, 256, 3, 4)
+    m = _mix(d, 3, eps=1e-30)  # eps far below ulp(mean(v^2)): the scores are exact ratios
+    d8 = dict(d)
+    d8["blocks"] = d["blocks"].copy()
+    d8["blocks"][1] = gen.to_bf16_bits(bf16_decode(d["blocks"][1]) * 8.0)  # exact
+    m8 = _mix(d8, 3, eps=1e-30)
+    np.testing.assert_allclose(m8["score"], m["score"], rtol=1e-15, atol=0)
+
+
+def test_mix_is_the_nearest_bf16_of_the_weighted_sum_and_y_its_rmsnorm():
+    R, H, nb = 3, 192, 4
+    d = _mix_inputs(R, H, nb, 5)
+    m = _mix(d, nb)
+    assert np.allclose(m["alpha"].sum(axis=1), 1.0, rtol=0, atol=1e-15)
+    srcs = np.concatenate([bf16_decode(d["blocks"][:nb]), bf16_decode(m["prefix"])[None]])
+    exact = np.einsum("rs,srh->rh", m["alpha"], srcs)
+    assert is_nearest_bf16(m["mix"].ravel(), exact.ravel(), slack=1e-13).all()
+    lo, hi = srcs.min(axis=0), srcs.max(axis=0)
+    mv = bf16_decode(m["mix"])
+    assert np.all(mv >= lo) and np.all(mv <= hi)  # a convex combination
+    rstd = 1.0 / np.sqrt((mv ** 2).mean(axis=1, keepdims=True) + 1e-6)
+    yx = mv * rstd * bf16_decode(d["gamma"])[None]
+    assert is_nearest_bf16(m["y"].ravel(), yx.ravel(), slack=1e-13).all()
+
+
+def test_mix_commit_stores_the_prefix_and_starts_a_new_block():
+    R, H, nb = 2, 128, 2
+    d = _mix_inputs(R, H, nb, 6, B=nb + 1)
+    plain = _mix(d, nb, commit=False)
+    com = _mix(d, nb, commit=True)
+    assert np.array_equal(com["blocks"][nb], plain["prefix"])
+    assert np.array_equal(com["blocks"][:nb], d["blocks"][:nb])
+    assert not com["prefix"].any()
+    for k in ("mix", "y", "alpha"):
+        assert np.array_equal(com[k], plain[k])
+
+
+def test_mix_sequence_blocks_are_running_bf16_sums_of_the_sublayer_outputs():
+    seq = gen.MixSequence(R=2, H=64, L=11, block_calls=4)
+    d = gen.make_mix_sequence(seq, 7)
+    pre, blk = d["prefix"], d["blocks"]
+    run = torch.zeros(seq.R, seq.H, dtype=torch.bfloat16)
+    committed = 1
+    for l in range(seq.L):
+        m = oracle.attnres_mix(d["sub"][l], pre, blk, seq.n_blocks(l), seq.commit(l), d["q"][l],
+                               d["gamma"][l], seq.eps)
+        pre, blk = m["prefix"], m["blocks"]
+        o = torch.from_numpy(bf16_decode(d["sub"][l]).astype(np.float32))
+        run = (run.float() + o).to(torch.bfloat16)
+        if seq.commit(l):
+            assert np.array_equal(blk[committed], run.view(torch.int16).numpy().view(np.uint16))
+            committed += 1
+            run.zero_()
+        assert np.array_equal(pre, run.view(torch.int16).numpy().view(np.uint16))
+    assert committed == seq.max_blocks
+
+
+def test_mix_permuting_the_committed_blocks_permutes_the_weights():
+    R, H, nb = 2, 256, 4
+    d = _mix_inputs(R, H, nb, 8)
+    m = _mix(d, nb)
+    perm = [2, 0, 3, 1]
+    dp = dict(d)
+    dp["blocks"] = d["blocks"].copy()
+    dp["blocks"][:nb] = d["blocks"][perm]
+    mp = _mix(dp, nb)
+    assert np.array_equal(mp["score"][:, :nb], m["score"][:, perm])
+    np.testing.assert_allclose(mp["alpha"][:, :nb], m["alpha"][:, perm], rtol=1e-14, atol=0)
+    assert np.abs(mp["mix"].astype(np.int32) - m["mix"].astype(np.int32)).max() <= 1
