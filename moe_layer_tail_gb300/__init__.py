@@ -32,6 +32,9 @@ STATUS_BAD_TILE = 8
 MODE_MULTI_KERNEL = 0
 MODE_PERSISTENT = 1
 
+# moe_attnres_mix launch flag (attnres_mix.h)
+ATTNRES_MIX_PDL = 1
+
 
 class Config(ctypes.Structure):
     _fields_ = [("max_rows", ctypes.c_int32), ("hidden", ctypes.c_int32),
@@ -102,6 +105,11 @@ def load_library(path: str = None):
     lib.moe_tail_strerror.restype = ctypes.c_char_p
     lib.moe_tail_last_cuda_error.argtypes = []
     lib.moe_tail_last_cuda_error.restype = ctypes.c_char_p
+    lib.moe_attnres_mix.argtypes = [i32, i32, i32, i32, ctypes.c_float] + [P] * 7 + \
+        [ctypes.c_uint, P]
+    lib.moe_attnres_mix.restype = ctypes.c_int
+    lib.moe_attnres_mix_ctas_per_row.argtypes = [i32, i32]
+    lib.moe_attnres_mix_ctas_per_row.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -231,6 +239,30 @@ class MoeTail:
             self.close()
         except Exception:
             pass
+
+
+def attnres_mix(sub, prefix, blocks, n_blocks: int, commit: bool, q, gamma, mix, y,
+                eps: float = 1e-6, rows: int = None, flags: int = 0, stream=None) -> None:
+    """One call of the AttnRes residual mix + RMSNorm (attnres_mix.h): bf16 CUDA tensors
+    sub, prefix, mix, y [rows, H], blocks [>= n_blocks (+1 on a commit), rows, H] (may be
+    None when n_blocks == 0 and there is no commit), q, gamma [H].  prefix is updated in
+    place; on a commit block n_blocks receives the new prefix and the prefix is zeroed."""
+    lib = load_library()
+    rows = int(sub.shape[0] if rows is None else rows)
+    H = int(sub.shape[-1])
+    rc = lib.moe_attnres_mix(rows, H, int(n_blocks), int(bool(commit)), float(eps), _ptr(sub),
+                             _ptr(prefix), _ptr(blocks), _ptr(q), _ptr(gamma), _ptr(mix),
+                             _ptr(y), int(flags), _stream_handle(stream))
+    if rc != OK:
+        raise MoeTailError(rc, "moe_attnres_mix")
+
+
+def attnres_mix_ctas_per_row(hidden: int, n_blocks: int) -> int:
+    """CTAs (one cluster) per row that attnres_mix launches for this shape (host only)."""
+    rc = load_library().moe_attnres_mix_ctas_per_row(int(hidden), int(n_blocks))
+    if rc < 0:
+        raise MoeTailError(rc, "moe_attnres_mix_ctas_per_row")
+    return rc
 
 
 def weights_to_device(weights: dict, device="cuda"):

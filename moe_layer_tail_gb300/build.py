@@ -26,7 +26,7 @@ def _sources():
 
 def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
-        [os.path.join(ROOT, "include", "moe_tail.h")]
+        sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def _stale():

@@ -1,0 +1,316 @@
+// k_mix.cu -- the AttnRes residual mix + RMSNorm of decode rows, one thread-block cluster
+// per row.
+//
+// What one call computes ("Split the Kimi3 AttnRes mix across CTAs for decode rows",
+// voipmonitor/flare #11, Description and commit message; the formulas are this library's
+// reading, stated in attnres_mix.h): the residual add of the sublayer output into the
+// block's running sum, the commit of a finished block, the softmax mixture of the row's
+// sources (the committed blocks and the running sum) by query scores over RMS-normalised
+// sources, and the RMSNorm of the bf16 mixture.
+//
+// The page splits a row over CTAs that exchange fp32 partials through global memory as
+// (value, call tag) words and spin until the row's other CTAs have published, with a
+// per-row epoch so that nothing is reset between calls.  Here the CTAs of a row form one
+// thread-block cluster: the hardware schedules them together, the partials travel through
+// distributed shared memory, and two cluster barriers replace the tagged words, the spins
+// and the epochs.  As on the page, every CTA adds the partials in the same fixed order
+// (its threads, then warps, then cluster ranks), so all CTAs of a row use bit-identical
+// scores and norms.
+//
+// Per CTA (row r = blockIdx.y, chunk c = cluster rank, W columns):
+//   1. cp.async stages the chunk of every source, the prefix, the sublayer output, q and
+//      gamma in shared memory (each thread copies exactly the 16-byte vectors it later
+//      uses, so no CTA barrier is needed before the arithmetic);
+//   2. prefix' = bf16(prefix + sub), kept in shared memory as the last source;
+//   3. per source: sum of squares and dot with q over the chunk (four sources at a time,
+//      so eight butterfly reductions are in flight together), added over warps;
+//   4. cluster barrier; each CTA adds the C chunks' partials in rank order; warp 0 forms
+//      the scores and their softmax;
+//   5. mixture h = bf16(sum_i alpha_i v_i) in source order (fp32 FMAs), stored; its
+//      sum of squares is reduced the same way through a second cluster barrier;
+//   6. y = bf16(h * rstd * gamma); prefix (or the new block and a zero prefix) stored.
+// A third barrier phase keeps every CTA alive until the others have read its partials.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "k_mix.cuh"
+#include "moe_tail_internal.cuh"
+
+namespace amix {
+
+using mtail::bf16_hi;
+using mtail::bf16_lo;
+using mtail::pdl_trigger;
+using mtail::pdl_wait;
+using mtail::warp_max;
+using mtail::warp_sum;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A float of CTA `rank`'s shared memory at the address of `p` in this CTA's.
+__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cp_async16(void* s, const void* g) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(s);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(a), "l"(g) : "memory");
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+__global__ void __launch_bounds__(kMaxThreads)
+k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
+  extern __shared__ uint4 sm[];
+  __shared__ float red[kMaxThreads / 32][2 * kMaxSources];
+  __shared__ float part1[2 * kMaxSources];
+  __shared__ float tot[2 * kMaxSources];
+  __shared__ float alpha[kMaxSources];
+  __shared__ float red2[kMaxThreads / 32];
+  __shared__ float part2;
+  __shared__ float rstd_s;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = blockDim.x, nwarps = T >> 5;
+  const int r = blockIdx.y;
+  const uint32_t c = cluster_rank();
+  const int S = a.n_blocks + 1;
+  const int nv = W >> 3;
+  uint4* src = sm;                  // [S][nv]; source S - 1 is prefix'
+  uint4* qv = sm + (size_t)S * nv;  // [nv]
+  uint4* gv = qv + nv;              // [nv]
+  uint4* pv = gv + nv;              // [nv] prefix as read, later the mixture h
+  uint4* ov = pv + nv;              // [nv] sublayer output
+
+  const size_t col0 = (size_t)c * W;
+  const size_t row_off = (size_t)r * a.H + col0;
+  const size_t blk_stride = (size_t)a.R * a.H;
+
+  pdl_wait();
+  pdl_trigger();
+
+  // 1. stage the chunk (each thread its own vectors)
+  for (int v = tid; v < nv; v += T) {
+    for (int i = 0; i < a.n_blocks; ++i)
+      cp_async16(&src[(size_t)i * nv + v], a.blocks + i * blk_stride + row_off + 8 * v);
+    cp_async16(&qv[v], a.q + col0 + 8 * v);
+    cp_async16(&gv[v], a.gamma + col0 + 8 * v);
+    cp_async16(&pv[v], a.prefix + row_off + 8 * v);
+    cp_async16(&ov[v], a.sub + row_off + 8 * v);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+  // 2. residual add (the fp32 sum of two bf16 values rounds to the same bf16 as the exact
+  //    sum: it is exact unless the exponents differ by more than 15, and then the smaller
+  //    term is far below half a bf16 step of the larger)
+  for (int v = tid; v < nv; v += T) {
+    float p[8], o[8];
+    unpack8(pv[v], p);
+    unpack8(ov[v], o);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) p[e] += o[e];
+    src[(size_t)(S - 1) * nv + v] = pack8(p);
+  }
+
+  // 3. per-source partials: sum of squares and dot with q
+  for (int i0 = 0; i0 < S; i0 += 4) {
+    float ss[4] = {0.f, 0.f, 0.f, 0.f}, dt[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int v = tid; v < nv; v += T) {
+      float qf[8];
+      unpack8(qv[v], qf);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (i0 + j < S) {
+          float x[8];
+          unpack8(src[(size_t)(i0 + j) * nv + v], x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            ss[j] = fmaf(x[e], x[e], ss[j]);
+            dt[j] = fmaf(qf[e], x[e], dt[j]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      ss[j] = warp_sum(ss[j]);
+      dt[j] = warp_sum(dt[j]);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (i0 + j < S) {
+          red[warp][2 * (i0 + j)] = ss[j];
+          red[warp][2 * (i0 + j) + 1] = dt[j];
+        }
+    }
+  }
+  __syncthreads();
+  if (tid < 2 * S) {
+    float s = 0.f;
+    for (int w = 0; w < nwarps; ++w) s += red[w][tid];
+    part1[tid] = s;
+  }
+
+  // 4. the row's totals in rank order, then the scores and their softmax
+  cluster_arrive();
+  cluster_wait();
+  if (tid < 2 * S) {
+    float s = 0.f;
+    for (int k = 0; k < C; ++k) s += ld_cluster(&part1[tid], (uint32_t)k);
+    tot[tid] = s;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const float invH = 1.0f / (float)a.H;
+    float sc = -INFINITY;
+    if (lane < S) sc = tot[2 * lane + 1] * rsqrtf(fmaf(tot[2 * lane], invH, a.eps));
+    const float m = warp_max(sc);
+    const float e = lane < S ? expf(sc - m) : 0.f;
+    const float den = __shfl_sync(0xffffffffu, warp_sum(e), 0);
+    if (lane < S) alpha[lane] = e / den;
+  }
+  __syncthreads();
+
+  // 5. the mixture, its sum of squares, and the prefix / commit stores
+  float hss = 0.f;
+  for (int v = tid; v < nv; v += T) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < S; ++i) {
+      const float al = alpha[i];
+      float x[8];
+      unpack8(src[(size_t)i * nv + v], x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(al, x[e], acc[e]);
+    }
+    const uint4 h = pack8(acc);
+    pv[v] = h;
+    *reinterpret_cast<uint4*>(a.mix + row_off + 8 * v) = h;
+    float hf[8];
+    unpack8(h, hf);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) hss = fmaf(hf[e], hf[e], hss);
+    const uint4 pn = src[(size_t)(S - 1) * nv + v];
+    if (a.commit) {
+      *reinterpret_cast<uint4*>(a.blocks + a.n_blocks * blk_stride + row_off + 8 * v) = pn;
+      *reinterpret_cast<uint4*>(a.prefix + row_off + 8 * v) = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      *reinterpret_cast<uint4*>(a.prefix + row_off + 8 * v) = pn;
+    }
+  }
+  hss = warp_sum(hss);
+  if (lane == 0) red2[warp] = hss;
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.f;
+    for (int w = 0; w < nwarps; ++w) s += red2[w];
+    part2 = s;
+  }
+  cluster_arrive();
+  cluster_wait();
+  if (tid == 0) {
+    float s = 0.f;
+    for (int k = 0; k < C; ++k) s += ld_cluster(&part2, (uint32_t)k);
+    rstd_s = rsqrtf(fmaf(s, 1.0f / (float)a.H, a.eps));
+  }
+  cluster_arrive();  // this CTA has read the others' partials
+  __syncthreads();
+
+  // 6. the RMSNorm of the mixture
+  const float rs = rstd_s;
+  for (int v = tid; v < nv; v += T) {
+    float hf[8], g[8];
+    unpack8(pv[v], hf);
+    unpack8(gv[v], g);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) hf[e] = hf[e] * rs * g[e];
+    *reinterpret_cast<uint4*>(a.y + row_off + 8 * v) = pack8(hf);
+  }
+  cluster_wait();  // and the others have read this CTA's
+}
+
+// Static shared memory of the kernel (the reduction arrays above), kept out of the
+// dynamic budget.
+constexpr size_t kStaticSmem = sizeof(float) * ((kMaxThreads / 32) * 2 * kMaxSources +
+                                                4 * kMaxSources + kMaxThreads / 32 + 2);
+constexpr size_t kDynSmemLimit = 227 * 1024 - kStaticSmem - 1024;
+
+bool mix_plan(int hidden, int S, MixPlan* p) {
+  if (hidden < 8 || hidden > kMaxHidden || hidden % 8) return false;
+  if (S < 1 || S > kMaxSources) return false;
+  int C = kMaxCluster;
+  while (C > 1 && (hidden % (8 * C) != 0 || hidden / C < 128)) C >>= 1;
+  const int W = hidden / C;
+  const int nv = W / 8;
+  int T = (nv + 31) / 32 * 32;
+  if (T < 64) T = 64;  // threads 0 .. 2S-1 add the per-source partials
+  if (T > kMaxThreads) T = kMaxThreads;
+  const size_t smem = (size_t)(S + 4) * W * 2;
+  if (smem > kDynSmemLimit) return false;
+  p->C = C;
+  p->W = W;
+  p->threads = T;
+  p->smem = smem;
+  return true;
+}
+
+cudaError_t launch_attnres_mix(const MixArgs& a, const MixPlan& p, cudaStream_t st, bool pdl) {
+  if (p.smem > 48 * 1024) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static int done[64];
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+      e = cudaFuncSetAttribute(k_attnres_mix, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kDynSmemLimit);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) done[dev] = 1;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.C, a.R);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeClusterDimension;
+  attr[n].val.clusterDim.x = p.C;
+  attr[n].val.clusterDim.y = 1;
+  attr[n].val.clusterDim.z = 1;
+  ++n;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k_attnres_mix, a, p.W, p.C);
+}
+
+}  // namespace amix

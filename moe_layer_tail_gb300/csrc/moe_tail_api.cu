@@ -10,6 +10,10 @@
 
 #include <new>
 
+#include <math.h>
+
+#include "attnres_mix.h"
+#include "k_mix.cuh"
 #include "moe_tail.h"
 #include "moe_tail_internal.cuh"
 
@@ -380,4 +384,43 @@ extern "C" void moe_tail_destroy(moe_tail_t* h) {
   cudaFree(h->stage);
   if (cur >= 0 && cur != h->device) cudaSetDevice(cur);
   delete h;
+}
+
+// ------------------------------------------- the AttnRes residual mix (attnres_mix.h) ----
+
+extern "C" int moe_attnres_mix_ctas_per_row(int hidden, int n_blocks) {
+  amix::MixPlan p;
+  if (n_blocks < 0 || !amix::mix_plan(hidden, n_blocks + 1, &p)) return MOE_TAIL_ERR_UNSUPPORTED;
+  return p.C;
+}
+
+extern "C" int moe_attnres_mix(int rows, int hidden, int n_blocks, int commit, float eps,
+                               const void* sub, void* prefix, void* blocks, const void* q,
+                               const void* gamma, void* mix, void* y, unsigned flags,
+                               void* stream) {
+  if (rows < 1 || rows > amix::kMaxRows || n_blocks < 0) return MOE_TAIL_ERR_INVALID_ARG;
+  if (!(eps > 0.f) || !isfinite(eps)) return MOE_TAIL_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)MOE_ATTNRES_MIX_PDL) return MOE_TAIL_ERR_INVALID_ARG;
+  const bool need_blocks = n_blocks > 0 || commit;
+  const void* ptrs[] = {sub, prefix, q, gamma, mix, y, need_blocks ? blocks : sub};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MOE_TAIL_ERR_INVALID_ARG;
+  amix::MixPlan plan;
+  if (!amix::mix_plan(hidden, n_blocks + 1, &plan)) return MOE_TAIL_ERR_UNSUPPORTED;
+  amix::MixArgs a;
+  a.sub = (const uint16_t*)sub;
+  a.prefix = (uint16_t*)prefix;
+  a.blocks = (uint16_t*)blocks;
+  a.q = (const uint16_t*)q;
+  a.gamma = (const uint16_t*)gamma;
+  a.mix = (uint16_t*)mix;
+  a.y = (uint16_t*)y;
+  a.R = rows;
+  a.H = hidden;
+  a.n_blocks = n_blocks;
+  a.commit = commit ? 1 : 0;
+  a.eps = eps;
+  const cudaError_t e = amix::launch_attnres_mix(a, plan, (cudaStream_t)stream,
+                                                 (flags & MOE_ATTNRES_MIX_PDL) != 0);
+  return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
 }

@@ -1,5 +1,6 @@
 """The C ABI without a GPU: the library builds for sm_103a, loads, exports every entry point
-that include/moe_tail.h declares, and answers argument errors before touching a device."""
+that include/*.h declares (moe_tail.h, attnres_mix.h), and answers argument errors before
+touching a device."""
 import ctypes
 import os
 import re
@@ -25,13 +26,14 @@ def declared_functions():
         if fn.endswith(".h"):
             src = open(os.path.join(ROOT, "include", fn)).read()
             src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-            names |= set(re.findall(r"\b(moe_tail_[a-z0-9_]+)\s*\(", src))
+            names |= set(re.findall(r"\b(moe_(?:tail|attnres)_[a-z0-9_]+)\s*\(", src))
     return sorted(names)
 
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) >= 10, names
+    assert len(names) >= 12, names
+    assert {"moe_attnres_mix", "moe_attnres_mix_ctas_per_row"} <= set(names)
     for n in names:
         assert hasattr(lib, n), "missing export " + n
 
@@ -133,3 +135,50 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(mt, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         mt.load_library(str(tmp_path / "nope.so"))
+
+
+# ------------------------------------------------------ the AttnRes mix (attnres_mix.h) ----
+
+def test_attnres_mix_flag_matches_header():
+    src = open(os.path.join(ROOT, "include", "attnres_mix.h")).read()
+    v = int(re.search(r"#define MOE_ATTNRES_MIX_PDL (\d+)u", src).group(1))
+    assert mt.ATTNRES_MIX_PDL == v
+
+
+@pytest.mark.parametrize("hidden,n_blocks,ctas", [
+    (7168, 8, 8), (8192, 31, 8), (256, 0, 2), (64, 0, 1), (1000, 3, 1), (1024, 5, 8),
+    (65536, 8, 8), (65536, 31, None), (7, 0, None), (65544, 0, None), (7168, 32, None),
+    (7168, -1, None)])
+def test_attnres_mix_plan(lib, hidden, n_blocks, ctas):
+    rc = lib.moe_attnres_mix_ctas_per_row(hidden, n_blocks)
+    assert rc == (ctas if ctas is not None else mt.ERR_UNSUPPORTED)
+
+
+def _mix_call(lib, **kw):
+    P = ctypes.c_void_p
+    args = dict(rows=8, hidden=7168, n_blocks=3, commit=0, eps=1e-6, sub=P(0x1000),
+                prefix=P(0x2000), blocks=P(0x3000), q=P(0x4000), gamma=P(0x5000),
+                mix=P(0x6000), y=P(0x7000), flags=0, stream=P(0))
+    args.update(kw)
+    return lib.moe_attnres_mix(*args.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(rows=0), mt.ERR_INVALID_ARG),
+    (dict(rows=4097), mt.ERR_INVALID_ARG),
+    (dict(n_blocks=-1), mt.ERR_INVALID_ARG),
+    (dict(eps=0.0), mt.ERR_INVALID_ARG),
+    (dict(eps=float("nan")), mt.ERR_INVALID_ARG),
+    (dict(eps=float("inf")), mt.ERR_INVALID_ARG),
+    (dict(flags=2), mt.ERR_INVALID_ARG),
+    (dict(sub=ctypes.c_void_p(0)), mt.ERR_INVALID_ARG),
+    (dict(y=ctypes.c_void_p(0x7008)), mt.ERR_INVALID_ARG),
+    (dict(blocks=ctypes.c_void_p(0)), mt.ERR_INVALID_ARG),
+    (dict(n_blocks=0, commit=1, blocks=ctypes.c_void_p(0)), mt.ERR_INVALID_ARG),
+    (dict(hidden=7164), mt.ERR_UNSUPPORTED),
+    (dict(hidden=1 << 17), mt.ERR_UNSUPPORTED),
+    (dict(n_blocks=32), mt.ERR_UNSUPPORTED),
+    (dict(hidden=65536, n_blocks=31), mt.ERR_UNSUPPORTED),
+])
+def test_attnres_mix_refuses_bad_arguments_before_any_launch(lib, kw, code):
+    assert _mix_call(lib, **kw) == code
