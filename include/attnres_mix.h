@@ -36,7 +36,9 @@ extern "C" {
 #endif
 
 /* Launch flag: the launch may start while the previous kernel on the stream finishes
- * (programmatic dependent launch); it reads nothing before that kernel has completed. */
+ * (programmatic dependent launch).  It then reads q and gamma at once, so the previous
+ * kernel must not write them; everything else it reads, and everything it writes, waits
+ * until the previous kernel has completed. */
 #define MOE_ATTNRES_MIX_PDL 1u
 
 /* One call of the mix for `rows` rows of `hidden` columns, enqueued on `stream` (a

@@ -11,25 +11,29 @@
 // The page splits a row over CTAs that exchange fp32 partials through global memory as
 // (value, call tag) words and spin until the row's other CTAs have published, with a
 // per-row epoch so that nothing is reset between calls.  Here the CTAs of a row form one
-// thread-block cluster: the hardware schedules them together, the partials travel through
-// distributed shared memory, and two cluster barriers replace the tagged words, the spins
-// and the epochs.  As on the page, every CTA adds the partials in the same fixed order
-// (its threads, then warps, then cluster ranks), so all CTAs of a row use bit-identical
-// scores and norms.
+// thread-block cluster: the hardware schedules them together, each CTA stores its
+// partials into a slot of every CTA's shared memory (distributed shared memory), and
+// cluster barriers replace the tagged words, the spins and the epochs.  As on the page,
+// every CTA adds the partials in the same fixed order (its threads, then warps, then
+// cluster ranks), so all CTAs of a row use bit-identical scores and norms.
 //
 // Per CTA (row r = blockIdx.y, chunk c = cluster rank, W columns):
 //   1. cp.async stages the chunk of every source, the prefix, the sublayer output, q and
 //      gamma in shared memory (each thread copies exactly the 16-byte vectors it later
-//      uses, so no CTA barrier is needed before the arithmetic);
+//      uses, so no CTA barrier is needed before the arithmetic); q and gamma, which the
+//      previous kernel does not write, are fetched before waiting for it, the rest is
+//      prefetched into L2 before the wait and copied after it;
 //   2. prefix' = bf16(prefix + sub), kept in shared memory as the last source;
-//   3. per source: sum of squares and dot with q over the chunk (four sources at a time,
-//      so eight butterfly reductions are in flight together), added over warps;
-//   4. cluster barrier; each CTA adds the C chunks' partials in rank order; warp 0 forms
-//      the scores and their softmax;
+//   3. per source: sum of squares and dot with q over the chunk (eight sources at a time,
+//      so sixteen butterfly reductions are in flight together), added over warps;
+//   4. the CTA's partials go to slot c of every CTA; after a cluster barrier each warp
+//      adds the slots in rank order and forms the scores and their softmax;
 //   5. mixture h = bf16(sum_i alpha_i v_i) in source order (fp32 FMAs), stored; its
-//      sum of squares is reduced the same way through a second cluster barrier;
+//      sum of squares travels the same way through a second barrier;
 //   6. y = bf16(h * rstd * gamma); prefix (or the new block and a zero prefix) stored.
-// A third barrier phase keeps every CTA alive until the others have read its partials.
+// A barrier arrival at the start, waited on before the first remote store, makes sure every
+// CTA of the cluster is running before another writes into its shared memory; after the
+// last barrier no CTA touches another's, so each may exit as soon as it is done.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -56,14 +60,15 @@ __device__ __forceinline__ void cluster_arrive() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// A float of CTA `rank`'s shared memory at the address of `p` in this CTA's.
-__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
+// Store a float into CTA `rank`'s shared memory at the address of `p` in this CTA's.
+__device__ __forceinline__ void st_cluster(float* p, uint32_t rank, float v) {
   const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
   uint32_t ra;
-  float v;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* g) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(g));
 }
 __device__ __forceinline__ void cp_async16(void* s, const void* g) {
   const uint32_t a = (uint32_t)__cvta_generic_to_shared(s);
@@ -86,12 +91,10 @@ __global__ void __launch_bounds__(kMaxThreads)
 k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   extern __shared__ uint4 sm[];
   __shared__ float red[kMaxThreads / 32][2 * kMaxSources];
-  __shared__ float part1[2 * kMaxSources];
-  __shared__ float tot[2 * kMaxSources];
-  __shared__ float alpha[kMaxSources];
+  __shared__ float part1[kMaxCluster][2 * kMaxSources];  // [rank][2 i + (0: v.v, 1: q.v)]
+  __shared__ float alpha_w[kMaxThreads / 32][kMaxSources];  // each warp's copy of alpha
   __shared__ float red2[kMaxThreads / 32];
-  __shared__ float part2;
-  __shared__ float rstd_s;
+  __shared__ float part2[kMaxCluster];                   // [rank] mixture square sums
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = blockDim.x, nwarps = T >> 5;
@@ -99,6 +102,7 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   const uint32_t c = cluster_rank();
   const int S = a.n_blocks + 1;
   const int nv = W >> 3;
+  const float invH = 1.0f / (float)a.H;
   uint4* src = sm;                  // [S][nv]; source S - 1 is prefix'
   uint4* qv = sm + (size_t)S * nv;  // [nv]
   uint4* gv = qv + nv;              // [nv]
@@ -109,15 +113,27 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   const size_t row_off = (size_t)r * a.H + col0;
   const size_t blk_stride = (size_t)a.R * a.H;
 
+  // Every CTA of the cluster must be running before another stores into its shared
+  // memory: arrive here, wait before the first remote store.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+  // 1. stage the chunk, each thread its own 16-byte vectors.  q and gamma are weights that
+  //    the previous kernel does not write, so they are fetched before waiting for it; the
+  //    rest is only prefetched into L2 (the point of coherence: a line fetched there early
+  //    cannot be stale when it is read after the wait) and copied after the wait.
+  for (int v = tid; v < nv; v += T) {
+    cp_async16(&qv[v], a.q + col0 + 8 * v);
+    cp_async16(&gv[v], a.gamma + col0 + 8 * v);
+    for (int i = 0; i < a.n_blocks; ++i)
+      prefetch_l2(a.blocks + i * blk_stride + row_off + 8 * v);
+    prefetch_l2(a.prefix + row_off + 8 * v);
+    prefetch_l2(a.sub + row_off + 8 * v);
+  }
   pdl_wait();
   pdl_trigger();
-
-  // 1. stage the chunk (each thread its own vectors)
   for (int v = tid; v < nv; v += T) {
     for (int i = 0; i < a.n_blocks; ++i)
       cp_async16(&src[(size_t)i * nv + v], a.blocks + i * blk_stride + row_off + 8 * v);
-    cp_async16(&qv[v], a.q + col0 + 8 * v);
-    cp_async16(&gv[v], a.gamma + col0 + 8 * v);
     cp_async16(&pv[v], a.prefix + row_off + 8 * v);
     cp_async16(&ov[v], a.sub + row_off + 8 * v);
   }
@@ -136,14 +152,17 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
     src[(size_t)(S - 1) * nv + v] = pack8(p);
   }
 
-  // 3. per-source partials: sum of squares and dot with q
-  for (int i0 = 0; i0 < S; i0 += 4) {
-    float ss[4] = {0.f, 0.f, 0.f, 0.f}, dt[4] = {0.f, 0.f, 0.f, 0.f};
+  // 3. per-source partials, eight sources at a time: sum of squares and dot with q over
+  //    this thread's vectors, then sixteen butterfly reductions interleaved level by level
+  for (int i0 = 0; i0 < S; i0 += 8) {
+    float ss[8], dt[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss[j] = dt[j] = 0.f;
     for (int v = tid; v < nv; v += T) {
       float qf[8];
       unpack8(qv[v], qf);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         if (i0 + j < S) {
           float x[8];
           unpack8(src[(size_t)(i0 + j) * nv + v], x);
@@ -156,13 +175,16 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
       }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      ss[j] = warp_sum(ss[j]);
-      dt[j] = warp_sum(dt[j]);
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], o);
+        dt[j] += __shfl_xor_sync(0xffffffffu, dt[j], o);
+      }
     }
     if (lane == 0) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < 8; ++j)
         if (i0 + j < S) {
           red[warp][2 * (i0 + j)] = ss[j];
           red[warp][2 * (i0 + j) + 1] = dt[j];
@@ -170,38 +192,41 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
     }
   }
   __syncthreads();
-  if (tid < 2 * S) {
-    float s = 0.f;
-    for (int w = 0; w < nwarps; ++w) s += red[w][tid];
-    part1[tid] = s;
-  }
 
-  // 4. the row's totals in rank order, then the scores and their softmax
-  cluster_arrive();
+  // 4. this CTA's partials (warps in order) into slot c of every CTA of the row; after the
+  //    barrier each CTA adds the slots in rank order
   cluster_wait();
   if (tid < 2 * S) {
     float s = 0.f;
-    for (int k = 0; k < C; ++k) s += ld_cluster(&part1[tid], (uint32_t)k);
-    tot[tid] = s;
+    for (int w = 0; w < nwarps; ++w) s += red[w][tid];
+    for (int k = 0; k < C; ++k) st_cluster(&part1[c][tid], (uint32_t)k, s);
   }
-  __syncthreads();
-  if (warp == 0) {
-    const float invH = 1.0f / (float)a.H;
+  cluster_arrive();
+  cluster_wait();
+  {
+    // the scores and their softmax, lane i for source i, the same in every warp and CTA
     float sc = -INFINITY;
-    if (lane < S) sc = tot[2 * lane + 1] * rsqrtf(fmaf(tot[2 * lane], invH, a.eps));
+    if (lane < S) {
+      float ssum = 0.f, dsum = 0.f;
+      for (int k = 0; k < C; ++k) {
+        ssum += part1[k][2 * lane];
+        dsum += part1[k][2 * lane + 1];
+      }
+      sc = dsum * rsqrtf(fmaf(ssum, invH, a.eps));
+    }
     const float m = warp_max(sc);
     const float e = lane < S ? expf(sc - m) : 0.f;
     const float den = __shfl_sync(0xffffffffu, warp_sum(e), 0);
-    if (lane < S) alpha[lane] = e / den;
+    if (lane < S) alpha_w[warp][lane] = e / den;
+    __syncwarp();
   }
-  __syncthreads();
 
   // 5. the mixture, its sum of squares, and the prefix / commit stores
   float hss = 0.f;
   for (int v = tid; v < nv; v += T) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int i = 0; i < S; ++i) {
-      const float al = alpha[i];
+      const float al = alpha_w[warp][i];
       float x[8];
       unpack8(src[(size_t)i * nv + v], x);
 #pragma unroll
@@ -225,23 +250,18 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   hss = warp_sum(hss);
   if (lane == 0) red2[warp] = hss;
   __syncthreads();
-  if (tid == 0) {
+  if (tid < C) {  // thread k sends this CTA's sum to rank k
     float s = 0.f;
     for (int w = 0; w < nwarps; ++w) s += red2[w];
-    part2 = s;
+    st_cluster(&part2[c], (uint32_t)tid, s);
   }
   cluster_arrive();
-  cluster_wait();
-  if (tid == 0) {
-    float s = 0.f;
-    for (int k = 0; k < C; ++k) s += ld_cluster(&part2, (uint32_t)k);
-    rstd_s = rsqrtf(fmaf(s, 1.0f / (float)a.H, a.eps));
-  }
-  cluster_arrive();  // this CTA has read the others' partials
-  __syncthreads();
+  cluster_wait();  // no CTA touches another's shared memory after this point
 
   // 6. the RMSNorm of the mixture
-  const float rs = rstd_s;
+  float tot = 0.f;
+  for (int k = 0; k < C; ++k) tot += part2[k];
+  const float rs = rsqrtf(fmaf(tot, invH, a.eps));
   for (int v = tid; v < nv; v += T) {
     float hf[8], g[8];
     unpack8(pv[v], hf);
@@ -250,13 +270,13 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
     for (int e = 0; e < 8; ++e) hf[e] = hf[e] * rs * g[e];
     *reinterpret_cast<uint4*>(a.y + row_off + 8 * v) = pack8(hf);
   }
-  cluster_wait();  // and the others have read this CTA's
 }
 
 // Static shared memory of the kernel (the reduction arrays above), kept out of the
 // dynamic budget.
-constexpr size_t kStaticSmem = sizeof(float) * ((kMaxThreads / 32) * 2 * kMaxSources +
-                                                4 * kMaxSources + kMaxThreads / 32 + 2);
+constexpr size_t kStaticSmem =
+    sizeof(float) * ((kMaxThreads / 32) * 2 * kMaxSources + kMaxCluster * 2 * kMaxSources +
+                     (kMaxThreads / 32) * kMaxSources + kMaxThreads / 32 + kMaxCluster);
 constexpr size_t kDynSmemLimit = 227 * 1024 - kStaticSmem - 1024;
 
 bool mix_plan(int hidden, int S, MixPlan* p) {
@@ -279,7 +299,9 @@ bool mix_plan(int hidden, int S, MixPlan* p) {
 }
 
 cudaError_t launch_attnres_mix(const MixArgs& a, const MixPlan& p, cudaStream_t st, bool pdl) {
-  if (p.smem > 48 * 1024) {
+  // the opt-in above 48 KB counts static and dynamic shared memory together, so it is set
+  // once per device whatever this launch's size
+  {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
