@@ -21,7 +21,9 @@
  * rounding of the exact sum); the CTAs of a row add their partials in one fixed order, so
  * a call's result does not depend on scheduling and a graph replay reproduces it bit for
  * bit.  Against an fp64 evaluation of the formulas the mixture may sit one bf16 step away
- * where the exact value is near a rounding boundary.
+ * where the exact value is near a rounding boundary.  The CTAs of a row exchange their
+ * partial sums through distributed shared memory; those waits are bounded and reported
+ * through moe_attnres_mix_get_status.
  *
  * Return codes are those of moe_tail.h (MOE_TAIL_OK, MOE_TAIL_ERR_*; moe_tail_strerror and
  * moe_tail_last_cuda_error apply).
@@ -40,6 +42,11 @@ extern "C" {
  * kernel must not write them; everything else it reads, and everything it writes, waits
  * until the previous kernel has completed. */
 #define MOE_ATTNRES_MIX_PDL 1u
+/* Launch flag for failure tests only: one CTA of row 0 waits for a partial sum that never
+ * comes.  Its wait gives up after the budget (50 ms), the device status word gets
+ * MOE_TAIL_STATUS_TIMEOUT, and the call completes (its results are still right: the
+ * awaited value is surplus). */
+#define MOE_ATTNRES_MIX_DEBUG_STALL 2u
 
 /* One call of the mix for `rows` rows of `hidden` columns, enqueued on `stream` (a
  * cudaStream_t; NULL is the legacy default stream).  Allocates nothing and never
@@ -58,7 +65,7 @@ extern "C" {
  *   q         device, bf16 [hidden], the query of the scores
  *   gamma     device, bf16 [hidden], the RMSNorm weight
  *   mix, y    device, bf16 [rows, hidden], written
- *   flags     0 or MOE_ATTNRES_MIX_PDL
+ *   flags     0 or MOE_ATTNRES_MIX_PDL (MOE_ATTNRES_MIX_DEBUG_STALL for failure tests)
  *
  * Every pointer is borrowed (the caller owns the memory) and must be 16-byte aligned.  The
  * outputs must not overlap q, gamma or blocks 0 .. n_blocks-1.
@@ -70,6 +77,14 @@ extern "C" {
 int moe_attnres_mix(int rows, int hidden, int n_blocks, int commit, float eps,
                     const void* sub, void* prefix, void* blocks, const void* q,
                     const void* gamma, void* mix, void* y, unsigned flags, void* stream);
+
+/* The device status word of the mix on the current device (MOE_TAIL_STATUS_* bits; the
+ * kernels OR MOE_TAIL_STATUS_TIMEOUT into it when an exchange between the CTAs of a row
+ * waited past its 50 ms budget).  Synchronous: waits for the device's pending work.  Writes
+ * the word to *status; clear != 0 zeroes it afterwards.  Returns MOE_TAIL_ERR_DEVICE when
+ * the word was nonzero, MOE_TAIL_ERR_INVALID_ARG for a NULL status, MOE_TAIL_ERR_CUDA when
+ * the copy fails, MOE_TAIL_OK otherwise. */
+int moe_attnres_mix_get_status(int* status, int clear);
 
 /* The CTAs (one thread-block cluster) that moe_attnres_mix gives each row for this shape:
  * 1, 2, 4 or 8; MOE_TAIL_ERR_UNSUPPORTED when the shape is not supported.  Host only. */

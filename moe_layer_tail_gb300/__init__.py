@@ -32,8 +32,9 @@ STATUS_BAD_TILE = 8
 MODE_MULTI_KERNEL = 0
 MODE_PERSISTENT = 1
 
-# moe_attnres_mix launch flag (attnres_mix.h)
+# moe_attnres_mix launch flags (attnres_mix.h)
 ATTNRES_MIX_PDL = 1
+ATTNRES_MIX_DEBUG_STALL = 2
 
 
 class Config(ctypes.Structure):
@@ -108,6 +109,8 @@ def load_library(path: str = None):
     lib.moe_attnres_mix.argtypes = [i32, i32, i32, i32, ctypes.c_float] + [P] * 7 + \
         [ctypes.c_uint, P]
     lib.moe_attnres_mix.restype = ctypes.c_int
+    lib.moe_attnres_mix_get_status.argtypes = [ctypes.POINTER(i32), i32]
+    lib.moe_attnres_mix_get_status.restype = ctypes.c_int
     lib.moe_attnres_mix_ctas_per_row.argtypes = [i32, i32]
     lib.moe_attnres_mix_ctas_per_row.restype = ctypes.c_int
     _lib = lib
@@ -255,6 +258,15 @@ def attnres_mix(sub, prefix, blocks, n_blocks: int, commit: bool, q, gamma, mix,
                              _ptr(y), int(flags), _stream_handle(stream))
     if rc != OK:
         raise MoeTailError(rc, "moe_attnres_mix")
+
+
+def attnres_mix_status(clear: bool = False) -> int:
+    """The mix's device status word (STATUS_* bits; synchronous); clear: zero it after."""
+    v = ctypes.c_int32(0)
+    rc = load_library().moe_attnres_mix_get_status(ctypes.byref(v), int(bool(clear)))
+    if rc not in (OK, ERR_DEVICE):
+        raise MoeTailError(rc, "moe_attnres_mix_get_status")
+    return int(v.value)
 
 
 def attnres_mix_ctas_per_row(hidden: int, n_blocks: int) -> int:

@@ -12,8 +12,9 @@
 // (value, call tag) words and spin until the row's other CTAs have published, with a
 // per-row epoch so that nothing is reset between calls.  Here the CTAs of a row form one
 // thread-block cluster: the hardware schedules them together, each CTA stores its
-// partials into a slot of every CTA's shared memory (distributed shared memory), and
-// cluster barriers replace the tagged words, the spins and the epochs.  As on the page,
+// partials into a slot of every CTA's shared memory (distributed shared memory), and the
+// receivers' mbarriers count the bytes in, which replaces the tagged words, the spins on
+// global memory and the epochs (an mbarrier is initialised afresh by every launch).  As on the page,
 // every CTA adds the partials in the same fixed order (its threads, then warps, then
 // cluster ranks), so all CTAs of a row use bit-identical scores and norms.
 //
@@ -24,23 +25,32 @@
 //      previous kernel does not write, are fetched before waiting for it, the rest is
 //      prefetched into L2 before the wait and copied after it;
 //   2. prefix' = bf16(prefix + sub), kept in shared memory as the last source;
-//   3. per source: sum of squares and dot with q over the chunk (eight sources at a time,
-//      so sixteen butterfly reductions are in flight together), added over warps;
-//   4. the CTA's partials go to slot c of every CTA; after a cluster barrier each warp
-//      adds the slots in rank order and forms the scores and their softmax;
+//   3. per source: sum of squares and dot with q over the chunk, eight sources (sixteen
+//      values) at a time reduced over the warp by a reduce-scatter butterfly (16 shuffles
+//      instead of 80, the same addition tree as a full butterfly), added over warps;
+//   4. the CTA's partials go to slot c of every CTA by asynchronous remote stores that
+//      complete a transaction on the receiver's mbarrier; once all ranks' values are in,
+//      each warp adds the slots in rank order and forms the scores and their softmax;
 //   5. mixture h = bf16(sum_i alpha_i v_i) in source order (fp32 FMAs), stored; its
-//      sum of squares travels the same way through a second barrier;
+//      sum of squares travels the same way to a second mbarrier;
 //   6. y = bf16(h * rstd * gamma); prefix (or the new block and a zero prefix) stored.
-// A barrier arrival at the start, waited on before the first remote store, makes sure every
-// CTA of the cluster is running before another writes into its shared memory; after the
-// last barrier no CTA touches another's, so each may exit as soon as it is done.
+// One cluster barrier, arrived at the start and waited on before the first remote store,
+// makes sure every CTA of the cluster is running (its mbarriers initialised) before another
+// writes into its shared memory; once a CTA's second mbarrier has completed nothing writes
+// into it any more, so each CTA exits as soon as it is done.  The mbarrier waits are
+// bounded (50 ms); on expiry the device status word reports MOE_TAIL_STATUS_TIMEOUT.
 #include <cuda_bf16.h>
 #include <math.h>
 
 #include "k_mix.cuh"
+#include "moe_tail.h"
 #include "moe_tail_internal.cuh"
 
 namespace amix {
+
+// The device's status word of the mix (MOE_TAIL_STATUS_* bits; moe_attnres_mix_get_status).
+__device__ int g_mix_status;
+constexpr uint64_t kWaitBudgetNs = 50ull * 1000 * 1000;
 
 using mtail::bf16_hi;
 using mtail::bf16_lo;
@@ -54,18 +64,44 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Store a float into CTA `rank`'s shared memory at the address of `p` in this CTA's.
-__device__ __forceinline__ void st_cluster(float* p, uint32_t rank, float v) {
-  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+// Asynchronous store of a float into CTA `rank`'s shared memory at the address of `p` in
+// this CTA's; its bytes count towards the transaction of that CTA's mbarrier `bar`.
+__device__ __forceinline__ void st_async(float* p, uint32_t rank, float v, uint64_t* bar) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+               "r"(__float_as_uint(v)), "r"(rb)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;"
+      " selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(b))
+      : "memory");
+  return ok != 0;
+}
+// Wait for the first phase of `b`, at most kWaitBudgetNs; on expiry the status word gets
+// MOE_TAIL_STATUS_TIMEOUT and the caller goes on with whatever has arrived.
+__device__ __forceinline__ void mbar_wait_bounded(uint64_t* b) {
+  if (mbar_try(b)) return;
+  const uint64_t t0 = mtail::globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(b)) return;
+    if ((i & 15) == 0 && mtail::globaltimer() - t0 > kWaitBudgetNs) {
+      atomicOr(&g_mix_status, (int)MOE_TAIL_STATUS_TIMEOUT);
+      return;
+    }
+  }
 }
 __device__ __forceinline__ void prefetch_l2(const void* g) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(g));
@@ -95,6 +131,7 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   __shared__ float alpha_w[kMaxThreads / 32][kMaxSources];  // each warp's copy of alpha
   __shared__ float red2[kMaxThreads / 32];
   __shared__ float part2[kMaxCluster];                   // [rank] mixture square sums
+  __shared__ __align__(8) uint64_t mbar[2];               // the two exchange rounds
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = blockDim.x, nwarps = T >> 5;
@@ -113,9 +150,26 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   const size_t row_off = (size_t)r * a.H + col0;
   const size_t blk_stride = (size_t)a.R * a.H;
 
-  // Every CTA of the cluster must be running before another stores into its shared
-  // memory: arrive here, wait before the first remote store.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  // The two exchange rounds land in this CTA's mbarriers, each expecting one fp32 value per
+  // rank and entry (2S entries, then 1).  Every CTA of the cluster must be running, with its
+  // mbarriers initialised, before another stores into its shared memory: arrive here, wait
+  // before the first remote store.
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[0])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[1])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the stall switch makes one CTA wait for a value that never comes (failure test)
+    const uint32_t extra = (a.debug_stall && r == 0 && c == 0) ? 4u : 0u;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(&mbar[0])),
+                 "r"((uint32_t)(C * 2 * S * 4))
+                 : "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(&mbar[1])),
+                 "r"((uint32_t)(C * 4) + extra)
+                 : "memory");
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // 1. stage the chunk, each thread its own 16-byte vectors.  q and gamma are weights that
   //    the previous kernel does not write, so they are fetched before waiting for it; the
@@ -153,7 +207,7 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   }
 
   // 3. per-source partials, eight sources at a time: sum of squares and dot with q over
-  //    this thread's vectors, then sixteen butterfly reductions interleaved level by level
+  //    this thread's vectors, then one reduce-scatter over the warp
   for (int i0 = 0; i0 < S; i0 += 8) {
     float ss[8], dt[8];
 #pragma unroll
@@ -174,21 +228,27 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
         }
       }
     }
+    // reduce-scatter butterfly: 16 values over 32 lanes in 8 + 4 + 2 + 1 + 1 shuffles;
+    // lane L ends with value 8 b4 + 4 b3 + 2 b2 + b1 (b the bits of L)
+    float vv[16];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int j = 0; j < 8; ++j) { vv[j] = ss[j]; vv[8 + j] = dt[j]; }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], o);
-        dt[j] += __shfl_xor_sync(0xffffffffu, dt[j], o);
+    for (int h = 8, o = 16; h >= 1; h >>= 1, o >>= 1) {
+      const bool b = (lane & o) != 0;
+#pragma unroll
+      for (int k = 0; k < h; ++k) {
+        const float send = b ? vv[k] : vv[k + h];
+        const float keep = b ? vv[k + h] : vv[k];
+        vv[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
       }
     }
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (i0 + j < S) {
-          red[warp][2 * (i0 + j)] = ss[j];
-          red[warp][2 * (i0 + j) + 1] = dt[j];
-        }
+    vv[0] += __shfl_xor_sync(0xffffffffu, vv[0], 1);
+    {
+      const int idx = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
+                      ((lane >> 1) & 1);
+      const int j = idx & 7;
+      if ((lane & 1) == 0 && i0 + j < S) red[warp][2 * (i0 + j) + (idx >> 3)] = vv[0];
     }
   }
   __syncthreads();
@@ -199,10 +259,9 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   if (tid < 2 * S) {
     float s = 0.f;
     for (int w = 0; w < nwarps; ++w) s += red[w][tid];
-    for (int k = 0; k < C; ++k) st_cluster(&part1[c][tid], (uint32_t)k, s);
+    for (int k = 0; k < C; ++k) st_async(&part1[c][tid], (uint32_t)k, s, &mbar[0]);
   }
-  cluster_arrive();
-  cluster_wait();
+  mbar_wait_bounded(&mbar[0]);
   {
     // the scores and their softmax, lane i for source i, the same in every warp and CTA
     float sc = -INFINITY;
@@ -253,10 +312,10 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   if (tid < C) {  // thread k sends this CTA's sum to rank k
     float s = 0.f;
     for (int w = 0; w < nwarps; ++w) s += red2[w];
-    st_cluster(&part2[c], (uint32_t)tid, s);
+    st_async(&part2[c], (uint32_t)tid, s, &mbar[1]);
   }
-  cluster_arrive();
-  cluster_wait();  // no CTA touches another's shared memory after this point
+  // once every rank's value has landed no CTA writes into this one any more
+  mbar_wait_bounded(&mbar[1]);
 
   // 6. the RMSNorm of the mixture
   float tot = 0.f;
@@ -333,6 +392,15 @@ cudaError_t launch_attnres_mix(const MixArgs& a, const MixPlan& p, cudaStream_t 
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, k_attnres_mix, a, p.W, p.C);
+}
+
+cudaError_t mix_status(int* out, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_mix_status, sizeof(int));
+  if (e == cudaSuccess && clear) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_mix_status, &zero, sizeof(int));
+  }
+  return e;
 }
 
 }  // namespace amix

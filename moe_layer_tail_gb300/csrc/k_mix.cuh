@@ -33,8 +33,12 @@ struct MixArgs {
   uint16_t* y;             // [R, H] bf16, out
   int R, H, n_blocks, commit;
   float eps;
+  int debug_stall;         // one CTA waits for a value that never comes (failure test)
 };
 
 cudaError_t launch_attnres_mix(const MixArgs& a, const MixPlan& p, cudaStream_t st, bool pdl);
+
+// The device status word of the mix (synchronous copy); clear: zero it afterwards.
+cudaError_t mix_status(int* out, bool clear);
 
 }  // namespace amix

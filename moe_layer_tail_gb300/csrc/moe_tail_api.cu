@@ -400,7 +400,8 @@ extern "C" int moe_attnres_mix(int rows, int hidden, int n_blocks, int commit, f
                                void* stream) {
   if (rows < 1 || rows > amix::kMaxRows || n_blocks < 0) return MOE_TAIL_ERR_INVALID_ARG;
   if (!(eps > 0.f) || !isfinite(eps)) return MOE_TAIL_ERR_INVALID_ARG;
-  if (flags & ~(unsigned)MOE_ATTNRES_MIX_PDL) return MOE_TAIL_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)(MOE_ATTNRES_MIX_PDL | MOE_ATTNRES_MIX_DEBUG_STALL))
+    return MOE_TAIL_ERR_INVALID_ARG;
   const bool need_blocks = n_blocks > 0 || commit;
   const void* ptrs[] = {sub, prefix, q, gamma, mix, y, need_blocks ? blocks : sub};
   for (const void* p : ptrs)
@@ -420,7 +421,17 @@ extern "C" int moe_attnres_mix(int rows, int hidden, int n_blocks, int commit, f
   a.n_blocks = n_blocks;
   a.commit = commit ? 1 : 0;
   a.eps = eps;
+  a.debug_stall = (flags & MOE_ATTNRES_MIX_DEBUG_STALL) ? 1 : 0;
   const cudaError_t e = amix::launch_attnres_mix(a, plan, (cudaStream_t)stream,
                                                  (flags & MOE_ATTNRES_MIX_PDL) != 0);
   return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
+}
+
+extern "C" int moe_attnres_mix_get_status(int* status, int clear) {
+  if (!status) return MOE_TAIL_ERR_INVALID_ARG;
+  int v = 0;
+  const cudaError_t e = amix::mix_status(&v, clear != 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *status = v;
+  return v ? MOE_TAIL_ERR_DEVICE : MOE_TAIL_OK;
 }

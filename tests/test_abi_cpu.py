@@ -33,7 +33,8 @@ def declared_functions():
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
     assert len(names) >= 12, names
-    assert {"moe_attnres_mix", "moe_attnres_mix_ctas_per_row"} <= set(names)
+    assert {"moe_attnres_mix", "moe_attnres_mix_ctas_per_row",
+            "moe_attnres_mix_get_status"} <= set(names)
     for n in names:
         assert hasattr(lib, n), "missing export " + n
 
@@ -139,10 +140,15 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
 
 # ------------------------------------------------------ the AttnRes mix (attnres_mix.h) ----
 
-def test_attnres_mix_flag_matches_header():
+def test_attnres_mix_flags_match_header():
     src = open(os.path.join(ROOT, "include", "attnres_mix.h")).read()
-    v = int(re.search(r"#define MOE_ATTNRES_MIX_PDL (\d+)u", src).group(1))
-    assert mt.ATTNRES_MIX_PDL == v
+    for name in ("PDL", "DEBUG_STALL"):
+        v = int(re.search(r"#define MOE_ATTNRES_MIX_%s (\d+)u" % name, src).group(1))
+        assert getattr(mt, "ATTNRES_MIX_" + name) == v
+
+
+def test_attnres_mix_status_refuses_null(lib):
+    assert lib.moe_attnres_mix_get_status(None, 0) == mt.ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("hidden,n_blocks,ctas", [
@@ -170,7 +176,8 @@ def _mix_call(lib, **kw):
     (dict(eps=0.0), mt.ERR_INVALID_ARG),
     (dict(eps=float("nan")), mt.ERR_INVALID_ARG),
     (dict(eps=float("inf")), mt.ERR_INVALID_ARG),
-    (dict(flags=2), mt.ERR_INVALID_ARG),
+    (dict(flags=4), mt.ERR_INVALID_ARG),
+    (dict(flags=0x80000000), mt.ERR_INVALID_ARG),
     (dict(sub=ctypes.c_void_p(0)), mt.ERR_INVALID_ARG),
     (dict(y=ctypes.c_void_p(0x7008)), mt.ERR_INVALID_ARG),
     (dict(blocks=ctypes.c_void_p(0)), mt.ERR_INVALID_ARG),

@@ -22,9 +22,10 @@ import numpy as np
 import pytest
 
 import oracle
-from moe_layer_tail_gb300 import (ATTNRES_MIX_PDL, ERR_INVALID_ARG, ERR_UNSUPPORTED,
-                                  MoeTailError, acts_to_device, attnres_mix,
-                                  attnres_mix_ctas_per_row, bf16_tensor_to_bits)
+from moe_layer_tail_gb300 import (ATTNRES_MIX_DEBUG_STALL, ATTNRES_MIX_PDL, ERR_INVALID_ARG,
+                                  ERR_UNSUPPORTED, STATUS_TIMEOUT, MoeTailError, acts_to_device,
+                                  attnres_mix, attnres_mix_ctas_per_row, attnres_mix_status,
+                                  bf16_tensor_to_bits)
 from moe_layer_tail_gb300 import inputs as gen
 from parity import bf16_step
 
@@ -181,6 +182,7 @@ def test_decoder_sequence_matches_oracle(R, family):
         pre, blk = orc["prefix"], orc["blocks"]
     assert np.array_equal(bf16_tensor_to_bits(dd["prefix"]), pre)
     assert np.array_equal(bf16_tensor_to_bits(dd["blocks"]), blk)
+    assert attnres_mix_status() == 0
 
 
 @pytest.mark.parametrize("flags", [0, ATTNRES_MIX_PDL])
@@ -228,3 +230,19 @@ def test_mix_refusals_on_device():
     assert e.value.code == ERR_INVALID_ARG
     # the inputs were not touched
     assert np.array_equal(bf16_tensor_to_bits(d["prefix"]), _inputs(2, 7168, 2, 9)["prefix"])
+
+
+def test_stalled_exchange_is_reported_and_the_device_stays_usable():
+    # one CTA waits for a partial sum that never comes: its bounded wait gives up, the
+    # status word says so, the call still completes with the right results (every real
+    # value had arrived), and the next call runs normally
+    R, H, nb = 4, 7168, 5
+    d = _inputs(R, H, nb, 21)
+    ref_m, ref_y = _run(_to_dev(d), nb, False)
+    assert attnres_mix_status(clear=True) == 0
+    gm, gy = _run(_to_dev(d), nb, False, flags=ATTNRES_MIX_DEBUG_STALL)
+    assert attnres_mix_status(clear=True) & STATUS_TIMEOUT
+    assert np.array_equal(gm, ref_m) and np.array_equal(gy, ref_y)
+    gm2, gy2 = _run(_to_dev(d), nb, False)
+    assert attnres_mix_status() == 0
+    assert np.array_equal(gm2, ref_m) and np.array_equal(gy2, ref_y)
