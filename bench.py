@@ -61,6 +61,9 @@ def parse_args():
     p.add_argument("--shared-gate", action="store_true",
                    help="the workload with the shared expert's sigmoid gate; the line's config "
                         "says so")
+    p.add_argument("--persistent", action="store_true",
+                   help="the workload in the single persistent launch (MOE_TAIL_MODE_PERSISTENT); "
+                        "the line's config says so")
     p.add_argument("--attnres-mix", type=int, default=0, metavar="ROWS",
                    help="the second workload instead: the AttnRes residual mix over a "
                         "187-call decoder sequence on ROWS rows (H 7168), one CUDA graph "
@@ -221,7 +224,8 @@ def run_ours(args, rank, world, local_rank):
     res0 = mt.acts_to_device(np.stack(rs))
     res = res0.clone()
     out = torch.empty_like(res0)
-    tail = mt.MoeTail(shape, dev_w, max_rows=R)
+    tail = mt.MoeTail(shape, dev_w, max_rows=R,
+                      mode=mt.MODE_PERSISTENT if args.persistent else mt.MODE_MULTI_KERNEL)
     nst = tail.launches_per_run(R) + (1 if args.out_proj else 0)
     stream = torch.cuda.current_stream()
     call = tail.run_attn if args.out_proj else tail.run
@@ -294,12 +298,15 @@ def run_ours(args, rank, world, local_rank):
     # dominant kernel: the stage with the largest total time
     names = (["out_proj"] if args.out_proj else []) + ["add_rmsnorm", "router_topk",
                                                        "stream_gate_up", "stream_down", "combine"]
+    if args.persistent:
+        names = ["tail_persistent"]
     if nst != len(names):
         names = ["stage%d" % s for s in range(nst)]
     tot = stage_ms.sum(axis=0)
     dom = int(np.argmax(tot))
     gu_b, dn_b = zip(*[stage_bytes(shape, int(d), R) for d in Ds])
-    dom_bytes = {"stream_gate_up": np.mean(gu_b), "stream_down": np.mean(dn_b)}.get(names[dom])
+    dom_bytes = {"stream_gate_up": np.mean(gu_b), "stream_down": np.mean(dn_b),
+                 "tail_persistent": float(bytes_per.mean())}.get(names[dom])
     peak, peak_kind = peaks()
     roof = None
     if dom_bytes is not None:
@@ -307,7 +314,7 @@ def run_ours(args, rank, world, local_rank):
         achieved = dom_bytes / dur_s / 1e9
         src = source_hash(["moe_layer_tail_gb300/csrc/k_stream.cu",
                            "moe_layer_tail_gb300/csrc/moe_tail_internal.cuh"])
-        tr = ncu_traffic(names[dom], src, dom_bytes)
+        tr = ncu_traffic(names[dom], src, dom_bytes) if not args.persistent else None
         roof = {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
                 "measured": "CUDA events around each launch on its stream, second pass of the "
                             "same %d calls (events serialise the launches: %.1f us/call)"
@@ -324,7 +331,8 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic",
         "config": {"workload": wl.name + ("" if not args.experts else " with %d experts" % shape.E)
                                + (" with shared-expert gate" if args.shared_gate else "")
-                               + (" with out_proj from %d" % shape.Ha if args.out_proj else ""),
+                               + (" with out_proj from %d" % shape.Ha if args.out_proj else "")
+                               + (" in one persistent launch" if args.persistent else ""),
                    "rows": R, "hidden": shape.H, "experts": shape.E,
                    "top_k": shape.k, "expert_inter": shape.I, "shared_inter": shape.Is,
                    "weights": "MXFP4 routed experts, bf16 router and shared expert",

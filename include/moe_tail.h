@@ -56,7 +56,18 @@ enum {
 /* Execution modes. */
 enum {
   MOE_TAIL_MODE_MULTI_KERNEL = 0,  /* one launch per stage, stream-ordered */
-  MOE_TAIL_MODE_PERSISTENT = 1     /* reserved: one resident launch with in-kernel flags */
+  MOE_TAIL_MODE_PERSISTENT = 1     /* the whole call in one cooperative launch, one CTA per
+                                      SM, its stages separated by grid-wide barriers whose
+                                      generation word tags every call (nothing is reset
+                                      between calls or graph replays); bounded waits report
+                                      MOE_TAIL_STATUS_TIMEOUT.  The stages are the
+                                      warp-per-row CUDA-core forms, so it is slower than the
+                                      multi-kernel mode; attn_dim must be 0 (else
+                                      MOE_TAIL_ERR_UNSUPPORTED at create) and the debug
+                                      flags do not apply.  moe_tail_create returns
+                                      MOE_TAIL_ERR_NOT_CORESIDENT when no CTA of it fits an
+                                      SM; a launch that cannot keep every CTA resident fails
+                                      with MOE_TAIL_ERR_CUDA instead of waiting. */
 };
 
 /* Bits of the device status word read by moe_tail_get_status (sticky until cleared). */
@@ -163,8 +174,9 @@ int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host, vo
                       int32_t rows, void* stream);
 
 /* Synchronise the device and read the handle's device status word (0 = no failure).  A
- * nonzero word is sticky until moe_tail_clear_status. Returns MOE_TAIL_ERR_DEVICE when the
- * word is nonzero, MOE_TAIL_OK otherwise. */
+ * nonzero word is sticky until moe_tail_clear_status (which, for a persistent-mode handle,
+ * also resets the grid barrier a call that gave up may have left half counted). Returns
+ * MOE_TAIL_ERR_DEVICE when the word is nonzero, MOE_TAIL_OK otherwise. */
 int moe_tail_get_status(moe_tail_t* h, int32_t* device_status);
 int moe_tail_clear_status(moe_tail_t* h);
 

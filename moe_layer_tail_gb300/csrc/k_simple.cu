@@ -8,6 +8,8 @@
 // routed experts" (bf16 activations x MXFP4 weights, gate and up, SiLU, down) and "The
 // shared expert gate_up / SiLU and mul / down"; "glm53: Long-context indexer ..." page,
 // Modifications rows 16 and 20 (each distinct expert once, every using row against it).
+#include "k_front.cuh"
+#include "k_persist.cuh"
 #include "moe_tail_internal.cuh"
 
 namespace mtail {
@@ -30,13 +32,16 @@ __device__ __forceinline__ void dequant32(uint4 c, float* v) {
   }
 }
 
-// dot of 32 floats with 32 bf16 values at p (64 bytes, 16-byte aligned)
+// dot of 32 floats with 32 bf16 activations at p (64 bytes, 16-byte aligned).  Activations
+// are read with ordinary loads, not the read-only path: in the persistent launch they were
+// written earlier in the same kernel by other CTAs, and ordinary loads after the grid
+// barrier's acquire see those writes (the CTA's warps still share them through L1).
 __device__ __forceinline__ float dot32_bf16(const float* v, const __nv_bfloat16* p) {
   const uint4* p4 = reinterpret_cast<const uint4*>(p);
   float a = 0.f;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    uint4 q = __ldg(p4 + c);
+    uint4 q = p4[c];
     uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -47,16 +52,49 @@ __device__ __forceinline__ float dot32_bf16(const float* v, const __nv_bfloat16*
   return a;
 }
 
+// Each stage below is a warp-level loop: warp gw of nw (this warp's index among all warps
+// of the grid, and their number) takes items gw, gw + nw, ...; the __global__ wrappers and
+// the single persistent launch call the same functions.
+
+// Ask L2 for a weight row's lines before the lanes walk it, so that a warp has the whole row
+// in flight rather than one 16-byte block per lane at a time.
+__device__ __forceinline__ void prefetch_row(const void* row, size_t bytes, int lane) {
+  const char* p = reinterpret_cast<const char*>(row);
+  for (size_t o = (size_t)lane * 128; o < bytes; o += 32 * 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
+}
+
+// The dots of 32 gate floats and 32 up floats with the same 32 bf16 activations at p, which
+// are loaded once for both.
+__device__ __forceinline__ void dot32x2_bf16(const float* g, const float* u,
+                                             const __nv_bfloat16* p, float& dg, float& du) {
+  const uint4* p4 = reinterpret_cast<const uint4*>(p);
+  float a = 0.f, b = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 q = p4[c];
+    uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      a += g[c * 8 + i * 2] * bf16_lo(w[i]);
+      a += g[c * 8 + i * 2 + 1] * bf16_hi(w[i]);
+      b += u[c * 8 + i * 2] * bf16_lo(w[i]);
+      b += u[c * 8 + i * 2 + 1] * bf16_hi(w[i]);
+    }
+  }
+  dg = a;
+  du = b;
+}
+
 // Routed gate/up: item (d, j) -> mid[pick, j] for every pick of distinct expert d.
-__global__ void __launch_bounds__(kSimpleWarps * 32)
-k_routed_gateup_simple(Dims dm, Weights w, Scratch s) {
+__device__ void routed_gateup_work(long long gw, long long nw, const Dims& dm, const Weights& w,
+                                   const Scratch& s) {
   const int lane = threadIdx.x & 31;
   const int D = *s.n_distinct;
   const int H = dm.H, I = dm.I, k = dm.k;
   const long long items = (long long)D * I;
   const int nblk = H / 32;
-  for (long long it = (long long)blockIdx.x * kSimpleWarps + (threadIdx.x >> 5); it < items;
-       it += (long long)gridDim.x * kSimpleWarps) {
+  for (long long it = gw; it < items; it += nw) {
     const int d = (int)(it / I), j = (int)(it % I);
     const int e = s.uniq[d];
     const int u0 = s.user_off[d], U = s.user_off[d + 1] - u0;
@@ -71,6 +109,10 @@ k_routed_gateup_simple(Dims dm, Weights w, Scratch s) {
     const uint4* uc = reinterpret_cast<const uint4*>(w.w13c + urow * (H / 2));
     const uint8_t* gs = w.w13s + grow * nblk;
     const uint8_t* us = w.w13s + urow * nblk;
+    prefetch_row(gc, (size_t)H / 2, lane);
+    prefetch_row(uc, (size_t)H / 2, lane);
+    prefetch_row(gs, (size_t)nblk, lane);
+    prefetch_row(us, (size_t)nblk, lane);
     for (int b = lane; b < nblk; b += 32) {
       float gv[32], uv[32];
       dequant32(__ldg(gc + b), gv);
@@ -79,9 +121,10 @@ k_routed_gateup_simple(Dims dm, Weights w, Scratch s) {
 #pragma unroll
       for (int u = 0; u < kMaxRows; ++u) {
         if (u < U) {
-          const __nv_bfloat16* np = s.n + (size_t)rows[u] * H + b * 32;
-          ag[u] += dot32_bf16(gv, np) * sg;
-          au[u] += dot32_bf16(uv, np) * su;
+          float dg, du;
+          dot32x2_bf16(gv, uv, s.n + (size_t)rows[u] * H + b * 32, dg, du);
+          ag[u] += dg * sg;
+          au[u] += du * su;
         }
       }
     }
@@ -99,15 +142,14 @@ k_routed_gateup_simple(Dims dm, Weights w, Scratch s) {
 }
 
 // Routed down: item (d, h) -> y[pick, h] for every pick of distinct expert d.
-__global__ void __launch_bounds__(kSimpleWarps * 32)
-k_routed_down_simple(Dims dm, Weights w, Scratch s) {
+__device__ void routed_down_work(long long gw, long long nw, const Dims& dm, const Weights& w,
+                                 const Scratch& s) {
   const int lane = threadIdx.x & 31;
   const int D = *s.n_distinct;
   const int H = dm.H, I = dm.I;
   const long long items = (long long)D * H;
   const int nblk = I / 32;
-  for (long long it = (long long)blockIdx.x * kSimpleWarps + (threadIdx.x >> 5); it < items;
-       it += (long long)gridDim.x * kSimpleWarps) {
+  for (long long it = gw; it < items; it += nw) {
     const int d = (int)(it / H), h = (int)(it % H);
     const int e = s.uniq[d];
     const int u0 = s.user_off[d], U = s.user_off[d + 1] - u0;
@@ -120,6 +162,8 @@ k_routed_down_simple(Dims dm, Weights w, Scratch s) {
     const size_t row = (size_t)e * H + h;
     const uint4* c4 = reinterpret_cast<const uint4*>(w.w2c + row * (I / 2));
     const uint8_t* sc = w.w2s + row * nblk;
+    prefetch_row(c4, (size_t)I / 2, lane);
+    prefetch_row(sc, (size_t)nblk, lane);
     for (int b = lane; b < nblk; b += 32) {
       float v[32];
       dequant32(__ldg(c4 + b), v);
@@ -139,24 +183,26 @@ k_routed_down_simple(Dims dm, Weights w, Scratch s) {
 }
 
 // Shared gate/up: item j -> ms[r, j] for every row.
-__global__ void __launch_bounds__(kSimpleWarps * 32)
-k_shared_gateup_simple(Dims dm, Weights w, Scratch s) {
+__device__ void shared_gateup_work(long long gw, long long nw, const Dims& dm, const Weights& w,
+                                   const Scratch& s) {
   const int lane = threadIdx.x & 31;
   const int H = dm.H, Is = dm.Is, R = dm.R;
-  for (int j = blockIdx.x * kSimpleWarps + (threadIdx.x >> 5); j < Is;
-       j += gridDim.x * kSimpleWarps) {
+  for (long long jj = gw; jj < Is; jj += nw) {
+    const int j = (int)jj;
     float ag[kMaxRows], au[kMaxRows];
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) { ag[r] = 0.f; au[r] = 0.f; }
     const uint4* g4 = reinterpret_cast<const uint4*>(w.ws13 + (size_t)j * H);
     const uint4* u4 = reinterpret_cast<const uint4*>(w.ws13 + (size_t)(Is + j) * H);
+    prefetch_row(g4, (size_t)H * 2, lane);
+    prefetch_row(u4, (size_t)H * 2, lane);
     for (int c = lane; c < H / 8; c += 32) {
       const uint4 gv = __ldg(g4 + c), uv = __ldg(u4 + c);
       const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r) {
         if (r < R) {
-          const uint4 nv = __ldg(reinterpret_cast<const uint4*>(s.n + (size_t)r * H) + c);
+          const uint4 nv = reinterpret_cast<const uint4*>(s.n + (size_t)r * H)[c];
           const uint32_t nw[4] = {nv.x, nv.y, nv.z, nv.w};
           float a = ag[r], b = au[r];
 #pragma unroll
@@ -179,23 +225,24 @@ k_shared_gateup_simple(Dims dm, Weights w, Scratch s) {
 }
 
 // Shared down: item h -> ys[r, h] for every row.
-__global__ void __launch_bounds__(kSimpleWarps * 32)
-k_shared_down_simple(Dims dm, Weights w, Scratch s) {
+__device__ void shared_down_work(long long gw, long long nw, const Dims& dm, const Weights& w,
+                                 const Scratch& s) {
   const int lane = threadIdx.x & 31;
   const int H = dm.H, Is = dm.Is, R = dm.R;
-  for (int h = blockIdx.x * kSimpleWarps + (threadIdx.x >> 5); h < H;
-       h += gridDim.x * kSimpleWarps) {
+  for (long long hh = gw; hh < H; hh += nw) {
+    const int h = (int)hh;
     float acc[kMaxRows];
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
     const uint4* w4 = reinterpret_cast<const uint4*>(w.ws2 + (size_t)h * Is);
+    prefetch_row(w4, (size_t)Is * 2, lane);
     for (int c = lane; c < Is / 8; c += 32) {
       const uint4 wv = __ldg(w4 + c);
       const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r) {
         if (r < R) {
-          const uint4 mv = __ldg(reinterpret_cast<const uint4*>(s.ms + (size_t)r * Is) + c);
+          const uint4 mv = reinterpret_cast<const uint4*>(s.ms + (size_t)r * Is)[c];
           const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
           float a = acc[r];
 #pragma unroll
@@ -217,6 +264,17 @@ k_shared_down_simple(Dims dm, Weights w, Scratch s) {
   }
 }
 
+#define MT_SIMPLE_KERNEL(name, work)                                                   \
+  __global__ void __launch_bounds__(kSimpleWarps * 32) name(Dims dm, Weights w, Scratch s) { \
+    work((long long)blockIdx.x * kSimpleWarps + (threadIdx.x >> 5),                      \
+         (long long)gridDim.x * kSimpleWarps, dm, w, s);                                 \
+  }
+MT_SIMPLE_KERNEL(k_shared_gateup_simple, shared_gateup_work)
+MT_SIMPLE_KERNEL(k_routed_gateup_simple, routed_gateup_work)
+MT_SIMPLE_KERNEL(k_shared_down_simple, shared_down_work)
+MT_SIMPLE_KERNEL(k_routed_down_simple, routed_down_work)
+#undef MT_SIMPLE_KERNEL
+
 cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch& s,
                                   int num_sms, cudaStream_t st) {
   const int grid = num_sms * 4;
@@ -234,13 +292,18 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
 // are in flight together.  wait_tiles: instead of waiting for the previous launch as a
 // whole, each warp waits (bounded, acquire) until the down items of the two 128-output
 // tiles it covers (the shared expert's and one per distinct expert) are counted done.
+// One thread's 8 outputs: row r, outputs 8c .. 8c + 7.
+__device__ __forceinline__ void combine_one(const Dims& dm, const Scratch& s, int r, int c,
+                                            __nv_bfloat16* __restrict__ out,
+                                            __nv_bfloat16* __restrict__ residual, bool gated);
+
 __global__ void __launch_bounds__(256)
 k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
           __nv_bfloat16* __restrict__ residual, bool wait_tiles, uint64_t budget_ns,
           bool gated) {
   if (!wait_tiles) pdl_wait();
   pdl_trigger();
-  const int H = dm.H, k = dm.k;
+  const int H = dm.H;
   const int ng = H / 8;  // a multiple of 32: whole warps lie in one row
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= dm.R * ng) return;
@@ -256,6 +319,13 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
     }
     __syncwarp();  // orders the other lanes' loads after lanes 0 and 16's acquires
   }
+  combine_one(dm, s, r, c, out, residual, gated);
+}
+
+__device__ __forceinline__ void combine_one(const Dims& dm, const Scratch& s, int r, int c,
+                                            __nv_bfloat16* __restrict__ out,
+                                            __nv_bfloat16* __restrict__ residual, bool gated) {
+  const int H = dm.H, k = dm.k;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int i0 = 0; i0 < k; i0 += 8) {
     float4 ya[8], yb[8];
@@ -304,6 +374,180 @@ cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
   const int n = d.R * d.H / 8;
   return launch_k(k_combine, dim3((n + 255) / 256), dim3(256), 0, st, pdl, d, s, out,
                   residual, wait_tiles, budget_ns, gated);
+}
+
+
+// ------------------------------------------------------- single persistent launch ----
+// The whole call in one launch whose CTAs are all resident (a cooperative launch): add +
+// RMSNorm (one warp per row), router logits (one warp per expert), top-k + dedup (CTA 0),
+// the shared and routed gate/up, the shared and routed down (the warp-level loops above),
+// and the combine with the residual update, separated by grid-wide barriers.  A barrier
+// is a count of arrivals and a generation word in the handle's counters: the last CTA to
+// arrive resets the count and advances the generation with a release store; the others
+// wait (bounded, acquire) until the generation differs from the one they read on arrival.
+// The generation only grows, so it tags every barrier of every call and nothing is reset
+// between calls or graph replays.  A CTA whose wait expires sets MOE_TAIL_STATUS_TIMEOUT
+// and leaves; the others then give up at the next barrier the same way.
+// Sources: "[AMD] integrate kimi k3 monokernel" page, Motivation and Kernel Replacement
+// (the layer tail as one resident launch whose stages hand over through in-kernel flags);
+// "Split the Kimi3 AttnRes mix across CTAs for decode rows" page (a tag per call instead of
+// a reset).
+constexpr int kPersistWarps = 8;
+constexpr int kCtrPersistArrive = 8;  // counters words outside every other use
+constexpr int kCtrPersistGen = 9;
+static_assert(kCtrOutProj < kCtrPersistArrive && kCtrPersistGen < kCtrGUDone &&
+                  kCtrPersistGen != kCtrSharedGUDone,
+              "the persistent launch's counter words are free");
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier; false when this CTA's wait expired (the status word says so).
+__device__ __forceinline__ bool grid_barrier(const Scratch& s, uint64_t budget_ns) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t* arrive = &s.counters[kCtrPersistArrive];
+    uint32_t* gen = &s.counters[kCtrPersistGen];
+    const uint32_t g0 = ld_acquire_u32(gen);
+    __threadfence();  // this CTA's writes (seen by thread 0 through the CTA barrier) first
+    int ok = 1;
+    if (atomicAdd(arrive, 1u) == gridDim.x - 1) {
+      atomicExch(arrive, 0u);
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(gen), "r"(g0 + 1u) : "memory");
+    } else {
+      const uint64_t t0 = globaltimer();
+      for (uint32_t i = 1; ld_acquire_u32(gen) == g0; ++i) {
+        __nanosleep(32);
+        if ((i & 15) == 0 && globaltimer() - t0 > budget_ns) {
+          set_status(s.status, kStatusTimeout);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// Add + RMSNorm of row r by one warp: r_new = bf16(x + residual) to scratch, rstd from the
+// fp32 sum of squares of r_new (lane-strided, butterfly, lane 0's value for every lane),
+// n = bf16(r_new * rstd * gamma); with a shared-expert gate, its sigmoid of n . g.
+__device__ __forceinline__ void norm_row_warp(int r, int lane, const Dims& dm,
+                                              const __nv_bfloat16* __restrict__ x,
+                                              const __nv_bfloat16* __restrict__ residual,
+                                              const Weights& w, const Scratch& s) {
+  const int H = dm.H;
+  const uint4* x4 = reinterpret_cast<const uint4*>(x + (size_t)r * H);
+  const uint4* r4 = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
+  const uint4* g4 = reinterpret_cast<const uint4*>(w.gamma);
+  uint4* rn4 = reinterpret_cast<uint4*>(s.rnew + (size_t)r * H);
+  uint4* n4 = reinterpret_cast<uint4*>(s.n + (size_t)r * H);
+  float ss = 0.f;
+  for (int c = lane; c < H / 8; c += 32) {
+    const uint4 xv = __ldg(x4 + c), rv = __ldcg(r4 + c);
+    const uint4 o = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
+                               add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w));
+    rn4[c] = o;
+    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ss = fmaf(bf16_lo(ow[i]), bf16_lo(ow[i]), ss);
+      ss = fmaf(bf16_hi(ow[i]), bf16_hi(ow[i]), ss);
+    }
+  }
+  ss = __shfl_sync(0xffffffffu, warp_sum(ss), 0);
+  const float rstd = 1.0f / sqrtf(ss / (float)H + dm.eps);
+  const uint4* wg4 = reinterpret_cast<const uint4*>(w.wsg);
+  float zg = 0.f;
+  for (int c = lane; c < H / 8; c += 32) {
+    const uint4 xv = __ldg(x4 + c), rv = __ldcg(r4 + c), gv = __ldg(g4 + c);
+    const uint4 o = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
+                               add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w));
+    const uint4 nv = make_uint4(norm_bf16x2(o.x, gv.x, rstd), norm_bf16x2(o.y, gv.y, rstd),
+                                norm_bf16x2(o.z, gv.z, rstd), norm_bf16x2(o.w, gv.w, rstd));
+    n4[c] = nv;
+    if (wg4) {
+      const uint4 wv = __ldg(wg4 + c);
+      const uint32_t nw[4] = {nv.x, nv.y, nv.z, nv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        zg = fmaf(bf16_lo(nw[i]), bf16_lo(ww[i]), zg);
+        zg = fmaf(bf16_hi(nw[i]), bf16_hi(ww[i]), zg);
+      }
+    }
+  }
+  if (wg4) {
+    const float z = __shfl_sync(0xffffffffu, warp_sum(zg), 0);
+    if (lane == 0) s.sgate[r] = 1.0f / (1.0f + expf(-z));
+  }
+}
+
+__global__ void __launch_bounds__(kPersistWarps * 32, 1)
+k_tail_persistent(Dims dm, Weights w, Scratch s, const __nv_bfloat16* __restrict__ x,
+                  const __nv_bfloat16* __restrict__ residual_in,
+                  __nv_bfloat16* __restrict__ residual, __nv_bfloat16* __restrict__ out,
+                  uint64_t budget_ns) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = (long long)blockIdx.x * kPersistWarps + (threadIdx.x >> 5);
+  const long long nw = (long long)gridDim.x * kPersistWarps;
+  // 1. add + RMSNorm
+  for (long long r = gw; r < dm.R; r += nw) norm_row_warp((int)r, lane, dm, x, residual_in, w, s);
+  if (!grid_barrier(s, budget_ns)) return;
+  // 2. router logits
+  for (long long e = gw; e < dm.E; e += nw)
+    router_warp(s.n, w.w_r, s.logits, dm.R, dm.H, dm.E, (int)e, lane);
+  if (!grid_barrier(s, budget_ns)) return;
+  // 3. top-k and the dedup
+  if (blockIdx.x == 0)
+    topk_dedup_block<false>(s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
+                            s.user_list, s.status, dm.R, dm.E, dm.k);
+  if (!grid_barrier(s, budget_ns)) return;
+  // 4. gate/up, 5. down
+  shared_gateup_work(gw, nw, dm, w, s);
+  routed_gateup_work(gw, nw, dm, w, s);
+  if (!grid_barrier(s, budget_ns)) return;
+  shared_down_work(gw, nw, dm, w, s);
+  routed_down_work(gw, nw, dm, w, s);
+  if (!grid_barrier(s, budget_ns)) return;
+  // 6. combine and the residual update
+  const int ng = dm.H / 8;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < (long long)dm.R * ng;
+       t += (long long)gridDim.x * blockDim.x)
+    combine_one(dm, s, (int)(t / ng), (int)(t % ng), out, residual, w.wsg != nullptr);
+}
+
+cudaError_t persistent_reset(const Scratch& s) {
+  return cudaMemset(s.counters + kCtrPersistArrive, 0, 2 * sizeof(uint32_t));
+}
+
+cudaError_t persistent_blocks_per_sm(int* blocks) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, k_tail_persistent,
+                                                       kPersistWarps * 32, 0);
+}
+
+cudaError_t launch_persistent(const Dims& d, const __nv_bfloat16* x,
+                              const __nv_bfloat16* residual_in, __nv_bfloat16* residual,
+                              __nv_bfloat16* out, const Weights& w, const Scratch& s, int grid,
+                              uint64_t budget_ns, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPersistWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_tail_persistent, d, w, s, x, residual_in, residual, out,
+                            budget_ns);
 }
 
 }  // namespace mtail

@@ -14,6 +14,7 @@
 
 #include "attnres_mix.h"
 #include "k_mix.cuh"
+#include "k_persist.cuh"
 #include "moe_tail.h"
 #include "moe_tail_internal.cuh"
 
@@ -29,6 +30,7 @@ struct moe_tail {
   void* stage;         // device staging for moe_tail_run_host: x, residual, out
   int device;
   int num_sms;
+  int persist_grid;    // CTAs of the single persistent launch (MOE_TAIL_MODE_PERSISTENT)
   int last_rows;
   cudaEvent_t ev[2 * 16];  // optional stage events (moe_tail_set_stage_events)
   int n_ev;
@@ -80,7 +82,10 @@ static int check_config(const moe_tail_config_t* c) {
   if (c->attn_dim < 0 || c->attn_dim > (1 << 16) || c->attn_dim % 64)
     return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->norm_topk_prob != 1) return MOE_TAIL_ERR_UNSUPPORTED;
-  if (c->mode != MOE_TAIL_MODE_MULTI_KERNEL) return MOE_TAIL_ERR_UNSUPPORTED;
+  if (c->mode != MOE_TAIL_MODE_MULTI_KERNEL && c->mode != MOE_TAIL_MODE_PERSISTENT)
+    return MOE_TAIL_ERR_UNSUPPORTED;
+  // the persistent launch covers the tail from x on (no out_proj stage in front of it)
+  if (c->mode == MOE_TAIL_MODE_PERSISTENT && c->attn_dim != 0) return MOE_TAIL_ERR_UNSUPPORTED;
   return MOE_TAIL_OK;
 }
 
@@ -158,6 +163,13 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   if (e == cudaSuccess) e = prepare_stream_kernels();
   if (e == cudaSuccess) e = prepare_front_kernels();
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e == cudaSuccess && cfg->mode == MOE_TAIL_MODE_PERSISTENT) {
+    // one CTA per SM at most; the cooperative launch checks at run time that all fit
+    int per_sm = 0;
+    e = persistent_blocks_per_sm(&per_sm);
+    if (e == cudaSuccess && per_sm < 1) { delete h; return MOE_TAIL_ERR_NOT_CORESIDENT; }
+    h->persist_grid = h->num_sms;
+  }
   if (e != cudaSuccess) { delete h; return cuda_fail(e); }
   h->slab_bytes = carve(cfg, nullptr, &h->s);
   e = cudaMalloc(&h->slab, h->slab_bytes);
@@ -210,6 +222,7 @@ extern "C" int moe_tail_set_stage_events(moe_tail_t* h, void* const* events, int
 extern "C" int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows) {
   (void)rows;
   if (!h) return 0;
+  if (h->cfg.mode == MOE_TAIL_MODE_PERSISTENT) return 1;
   if (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) return 8;
   return (h->cfg.debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT) ? 4 : 5;
 }
@@ -248,6 +261,14 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   const uint64_t budget_ns =
       (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
   const float* xpart = nullptr;
+  if (h->cfg.mode == MOE_TAIL_MODE_PERSISTENT) {
+    // the whole call in one cooperative launch (such a handle has no out_proj stage)
+    MT_STAGE(launch_persistent(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
+                               (__nv_bfloat16*)residual, (__nv_bfloat16*)out, h->w, h->s,
+                               h->persist_grid, budget_ns, st));
+    h->last_rows = rows;
+    return MOE_TAIL_OK;
+  }
   if (attn) {
     // the attention output projection into scratch; the call's map of attn travels with
     // the launch's parameters (a graph replays it as captured).  Each 128-output box is
@@ -356,6 +377,9 @@ extern "C" int moe_tail_get_status(moe_tail_t* h, int32_t* device_status) {
 extern "C" int moe_tail_clear_status(moe_tail_t* h) {
   if (!h) return MOE_TAIL_ERR_INVALID_ARG;
   cudaError_t e = cudaMemset(h->s.status, 0, 4);
+  // a persistent call that gave up may have left its barrier count behind
+  if (e == cudaSuccess && h->cfg.mode == MOE_TAIL_MODE_PERSISTENT)
+    e = persistent_reset(h->s);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
 }

@@ -351,3 +351,84 @@ def test_device_wait_timeout_is_reported_and_context_survives():
     assert bad.status() == 0
     bad.close()
     _check_small(shape, d)  # the context is healthy: a normal handle matches the oracle
+
+
+# ------------------------------------------------------------ single persistent launch ----
+
+from moe_layer_tail_gb300 import MODE_PERSISTENT  # noqa: E402
+
+
+@pytest.mark.parametrize("name", list(gen.WORKLOADS))
+def test_persistent_mode_parity_full_size(name):
+    wl, d, dev, orc = workload_inputs(name)
+    tail = MoeTail(wl.shape, dev, max_rows=wl.shape.R, mode=MODE_PERSISTENT)
+    assert tail.launches_per_run(wl.shape.R) == 1
+    got = run_gpu(tail, d)
+    check_parity(got[0], got[1], got[2], orc, wl.shape.k)
+    assert tail.status() == 0
+
+
+@pytest.mark.parametrize("R,H,E,k,I,Is,gated", [
+    (1, 256, 8, 2, 128, 128, False),
+    (5, 768, 20, 4, 384, 192, True),    # ragged rows, shared-expert gate
+    (16, 512, 12, 3, 256, 64, False),   # maximum rows, repeated experts
+    (3, 512, 4, 4, 256, 192, True),     # k = E
+])
+def test_persistent_mode_small_shapes(R, H, E, k, I, Is, gated):
+    shape = gen.TailShape(R, H, E, k, I, Is)
+    seed = 500 + R + E
+    keys = gen._LAYER_WEIGHTS + (("ws_gate",) if gated else ())
+    d = gen.make_weights(shape, seed, keys=keys)
+    d.update(gen.make_activations(shape, seed))
+    orc = oracle.moe_tail(d, k, shape.eps, nthreads=NTHREADS)
+    dev = weights_to_device({kk: v for kk, v in d.items() if kk not in ("x", "residual")})
+    tail = MoeTail(shape, dev, max_rows=R, mode=MODE_PERSISTENT)
+    got = run_gpu(tail, d)
+    check_parity(got[0], got[1], got[2], orc, k)
+    # fewer rows on the same handle
+    if R > 1:
+        d2 = dict(d)
+        d2["x"], d2["residual"] = d["x"][:R - 1], d["residual"][:R - 1]
+        orc2 = oracle.moe_tail(d2, k, shape.eps, nthreads=NTHREADS)
+        got2 = run_gpu(tail, d2)
+        check_parity(got2[0], got2[1], got2[2], orc2, k)
+    assert tail.status() == 0
+
+
+def test_persistent_mode_determinism_and_graph_replay():
+    shape, d = _small(13, R=4, H=512, E=24, k=4, I=256, Is=192)
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    tail = MoeTail(shape, dev, mode=MODE_PERSISTENT)
+    x = acts_to_device(d["x"])
+    res0 = acts_to_device(d["residual"])
+    eager = []
+    for _ in range(3):
+        res = res0.clone()
+        out = torch.empty_like(x)
+        tail.run(x, res, out)
+        torch.cuda.synchronize()
+        eager.append((bf16_tensor_to_bits(out), bf16_tensor_to_bits(res)))
+    assert all(np.array_equal(a, b) for a, b in zip(eager[0], eager[1]))
+    assert all(np.array_equal(a, b) for a, b in zip(eager[0], eager[2]))
+    res = res0.clone()
+    out = torch.empty_like(x)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        res.copy_(res0)
+        tail.run(x, res, out)
+    for i in range(100):
+        g.replay()
+        if i % 25 == 24:
+            torch.cuda.synchronize()
+            assert np.array_equal(bf16_tensor_to_bits(out), eager[0][0])
+            assert np.array_equal(bf16_tensor_to_bits(res), eager[0][1])
+    assert tail.status() == 0
+
+
+def test_persistent_mode_refuses_out_proj():
+    shape = gen.TailShape(2, 256, 8, 2, 128, 128, Ha=128)
+    d = gen.make_weights(shape, 7, keys=gen._LAYER_WEIGHTS + ("w_o",))
+    dev = weights_to_device(d)
+    with pytest.raises(MoeTailError) as e:
+        MoeTail(shape, dev, max_rows=2, mode=MODE_PERSISTENT)
+    assert e.value.code == ERR_UNSUPPORTED
