@@ -93,8 +93,9 @@ enum {
   MOE_TAIL_DEBUG_NO_PDL = 2,
   /* Failure injection for tests: in the gate/up launch, the first CTA's producer leaves its
    * first pipeline stage unpublished, so that the consumers' bounded wait expires; the
-   * kernel sets MOE_TAIL_STATUS_TIMEOUT in the status word and returns.  The output of
-   * such a call is not meaningful. */
+   * kernel sets MOE_TAIL_STATUS_TIMEOUT in the status word and returns.  In the persistent
+   * mode the first CTA never arrives at the grid barriers, so the others' waits expire the
+   * same way.  The output of such a call is not meaningful. */
   MOE_TAIL_DEBUG_STALL_FIRST_STAGE = 4,
   /* Run the front (add + RMSNorm, router, top-k, dedup) as one launch in which every CTA
    * recomputes the row norms, instead of a norm launch followed by a router launch. */

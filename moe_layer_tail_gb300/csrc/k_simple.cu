@@ -493,7 +493,10 @@ __global__ void __launch_bounds__(kPersistWarps * 32, 1)
 k_tail_persistent(Dims dm, Weights w, Scratch s, const __nv_bfloat16* __restrict__ x,
                   const __nv_bfloat16* __restrict__ residual_in,
                   __nv_bfloat16* __restrict__ residual, __nv_bfloat16* __restrict__ out,
-                  uint64_t budget_ns) {
+                  uint64_t budget_ns, int stall) {
+  // failure-injection switch: CTA 0 never arrives at a barrier, so the others' bounded
+  // waits expire (tests the timeout path; never set in production)
+  if (stall && blockIdx.x == 0) return;
   const int lane = threadIdx.x & 31;
   const long long gw = (long long)blockIdx.x * kPersistWarps + (threadIdx.x >> 5);
   const long long nw = (long long)gridDim.x * kPersistWarps;
@@ -535,7 +538,7 @@ cudaError_t persistent_blocks_per_sm(int* blocks) {
 cudaError_t launch_persistent(const Dims& d, const __nv_bfloat16* x,
                               const __nv_bfloat16* residual_in, __nv_bfloat16* residual,
                               __nv_bfloat16* out, const Weights& w, const Scratch& s, int grid,
-                              uint64_t budget_ns, cudaStream_t st) {
+                              uint64_t budget_ns, bool stall, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kPersistWarps * 32);
@@ -547,7 +550,7 @@ cudaError_t launch_persistent(const Dims& d, const __nv_bfloat16* x,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_tail_persistent, d, w, s, x, residual_in, residual, out,
-                            budget_ns);
+                            budget_ns, stall ? 1 : 0);
 }
 
 }  // namespace mtail

@@ -265,7 +265,8 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
     // the whole call in one cooperative launch (such a handle has no out_proj stage)
     MT_STAGE(launch_persistent(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
                                (__nv_bfloat16*)residual, (__nv_bfloat16*)out, h->w, h->s,
-                               h->persist_grid, budget_ns, st));
+                               h->persist_grid, budget_ns,
+                               (h->cfg.debug_flags & MOE_TAIL_DEBUG_STALL_FIRST_STAGE) != 0, st));
     h->last_rows = rows;
     return MOE_TAIL_OK;
   }

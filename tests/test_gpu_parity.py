@@ -432,3 +432,28 @@ def test_persistent_mode_refuses_out_proj():
     with pytest.raises(MoeTailError) as e:
         MoeTail(shape, dev, max_rows=2, mode=MODE_PERSISTENT)
     assert e.value.code == ERR_UNSUPPORTED
+
+
+def test_persistent_mode_barrier_timeout_is_reported_and_reset():
+    """A CTA that never arrives at the grid barrier makes the others' bounded waits (5 ms)
+    expire: the status reports the timeout, the call completes, clear_status resets the
+    barrier, the same stalled handle times out again the same way (no hang), and a healthy
+    persistent handle is correct afterwards."""
+    shape, d = _small(15, R=2, H=512, E=8, k=2, I=256, Is=128)
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    bad = MoeTail(shape, dev, mode=MODE_PERSISTENT, wait_budget_us=5000, debug_flags=STALL)
+    x = acts_to_device(d["x"])
+    for _ in range(2):
+        res = acts_to_device(d["residual"])
+        out = torch.empty_like(x)
+        bad.run(x, res, out)
+        torch.cuda.synchronize()
+        assert bad.status() & STATUS_TIMEOUT
+        bad.clear_status()
+        assert bad.status() == 0
+    bad.close()
+    good = MoeTail(shape, dev, mode=MODE_PERSISTENT)
+    orc = oracle.moe_tail(d, shape.k, shape.eps, nthreads=NTHREADS)
+    got = run_gpu(good, d)
+    check_parity(got[0], got[1], got[2], orc, shape.k)
+    assert good.status() == 0
