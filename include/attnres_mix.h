@@ -71,8 +71,9 @@ extern "C" {
  * outputs must not overlap q, gamma or blocks 0 .. n_blocks-1.
  * Errors (nothing is launched): MOE_TAIL_ERR_INVALID_ARG for rows, n_blocks or eps out of
  * range, a NULL or misaligned pointer, an unknown flag; MOE_TAIL_ERR_UNSUPPORTED for a
- * hidden size or source count outside the ranges above, or whose staging exceeds shared
- * memory ((n_blocks + 5) * hidden / ctas_per_row * 2 bytes must stay under ~220 KB);
+ * hidden size or source count outside the ranges above, or, for rows split into chunks
+ * wider than 2048 columns (staged in shared memory), whose staging exceeds it
+ * ((n_blocks + 5) * hidden / ctas_per_row * 2 bytes must stay under ~210 KB);
  * MOE_TAIL_ERR_CUDA when the launch fails. */
 int moe_attnres_mix(int rows, int hidden, int n_blocks, int commit, float eps,
                     const void* sub, void* prefix, void* blocks, const void* q,

@@ -18,6 +18,10 @@
 // every CTA adds the partials in the same fixed order (its threads, then warps, then
 // cluster ranks), so all CTAs of a row use bit-identical scores and norms.
 //
+// Two forms: k_attnres_mix_reg (chunks of at most 2048 columns, one thread per 16-byte vector,
+// every source in registers; H 7168 and most shapes) and k_attnres_mix below (any chunk,
+// operands staged in shared memory).  Both add in the same order.
+//
 // Per CTA (row r = blockIdx.y, chunk c = cluster rank, W columns):
 //   1. cp.async stages the chunk of every source, the prefix, the sublayer output, q and
 //      gamma in shared memory (each thread copies exactly the 16-byte vectors it later
@@ -331,6 +335,230 @@ k_attnres_mix(const __grid_constant__ MixArgs a, int W, int C) {
   }
 }
 
+
+// One level of the reduce-scatter butterfly: 2 HH values per lane become HH, summed with the
+// lane O apart (the lane with bit O set keeps the upper half).
+template <int HH, int O>
+__device__ __forceinline__ void rs_level(float* vv, int lane) {
+  const bool b = (lane & O) != 0;
+#pragma unroll
+  for (int k = 0; k < HH; ++k) {
+    const float send = b ? vv[k] : vv[k + HH];
+    const float keep = b ? vv[k + HH] : vv[k];
+    vv[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+  }
+}
+
+// Source i of a thread: block i from the registers, prefix' at i == nb (selected by value, so
+// that the register array is never indexed at run time).
+template <int SMAX>
+__device__ __forceinline__ uint4 source(const uint4 (&xs)[SMAX], int i, int nb, uint4 pn) {
+  const uint4 b = xs[i];
+  const bool p = (i == nb);
+  return make_uint4(p ? pn.x : b.x, p ? pn.y : b.y, p ? pn.z : b.z, p ? pn.w : b.w);
+}
+
+// Square sums and q dots of sources I0 .. I0 + 7 (zero beyond the row's sources), reduced
+// over the warp; the even lanes store the 16 totals into red_row.
+template <int SMAX, int I0>
+__device__ __forceinline__ void partials_group(const uint4 (&xs)[SMAX], uint4 pn, int nb,
+                                               const float* qf, int S, int lane,
+                                               float* red_row) {
+  float vv[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float x[8];
+    unpack8(source(xs, I0 + j, nb, pn), x);
+    float ss = 0.f, dt = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ss = fmaf(x[e], x[e], ss);
+      dt = fmaf(qf[e], x[e], dt);
+    }
+    vv[j] = ss;
+    vv[8 + j] = dt;
+  }
+  rs_level<8, 16>(vv, lane);
+  rs_level<4, 8>(vv, lane);
+  rs_level<2, 4>(vv, lane);
+  rs_level<1, 2>(vv, lane);
+  vv[0] += __shfl_xor_sync(0xffffffffu, vv[0], 1);
+  const int idx = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
+                  ((lane >> 1) & 1);
+  const int j = idx & 7;
+  if ((lane & 1) == 0 && I0 + j < S) red_row[2 * (I0 + j) + (idx >> 3)] = vv[0];
+}
+
+// The same computation with every operand in registers, for chunks of at most 256 vectors
+// (W <= 2048): one thread per 16-byte vector, up to SMAX sources held as uint4 registers.
+// The loads go straight to registers (no shared-memory staging and no copy wait beyond the
+// loads themselves), and both passes over the sources read registers.  Sources keep the
+// order of the staged kernel (blocks, then prefix'), so both give the same sums.
+constexpr int kRegThreads = 256;
+
+template <int SMAX>
+__global__ void __launch_bounds__(kRegThreads)
+k_attnres_mix_reg(const __grid_constant__ MixArgs a, int W, int C) {
+  __shared__ float red[kRegThreads / 32][2 * SMAX];
+  __shared__ float part1[kMaxCluster][2 * SMAX];        // [rank][2 i + (0: v.v, 1: q.v)]
+  __shared__ float alpha_w[kRegThreads / 32][SMAX];     // each warp's copy of alpha
+  __shared__ float red2[kRegThreads / 32];
+  __shared__ float part2[kMaxCluster];                  // [rank] mixture square sums
+  __shared__ __align__(8) uint64_t mbar[2];             // the two exchange rounds
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int r = blockIdx.y;
+  const uint32_t c = cluster_rank();
+  const int S = a.n_blocks + 1;
+  const int nv = W >> 3;
+  const int v = tid;
+  const bool own = v < nv;
+  const float invH = 1.0f / (float)a.H;
+  const size_t col0 = (size_t)c * W;
+  const size_t row_off = (size_t)r * a.H + col0 + 8 * (size_t)v;
+  const size_t blk_stride = (size_t)a.R * a.H;
+
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[0])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[1])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t extra = (a.debug_stall && r == 0 && c == 0) ? 4u : 0u;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(&mbar[0])),
+                 "r"((uint32_t)(C * 2 * S * 4))
+                 : "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(&mbar[1])),
+                 "r"((uint32_t)(C * 4) + extra)
+                 : "memory");
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+
+  // 1. q and gamma (weights the previous kernel does not write) before the wait; the rest
+  //    prefetched into L2 before it and loaded after it
+  uint4 qv4 = make_uint4(0u, 0u, 0u, 0u), gv4 = qv4, pv4 = qv4, ov4 = qv4;
+  uint4 xs[SMAX];
+#pragma unroll
+  for (int i = 0; i < SMAX; ++i) xs[i] = qv4;
+  if (own) {
+    qv4 = __ldg(reinterpret_cast<const uint4*>(a.q + col0) + v);
+    gv4 = __ldg(reinterpret_cast<const uint4*>(a.gamma + col0) + v);
+    for (int i = 0; i < a.n_blocks; ++i) prefetch_l2(a.blocks + i * blk_stride + row_off);
+    prefetch_l2(a.prefix + row_off);
+    prefetch_l2(a.sub + row_off);
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (own) {
+#pragma unroll
+    for (int i = 0; i < SMAX - 1; ++i)
+      if (i < a.n_blocks)
+        xs[i] = *reinterpret_cast<const uint4*>(a.blocks + i * blk_stride + row_off);
+    pv4 = *reinterpret_cast<const uint4*>(a.prefix + row_off);
+    ov4 = *reinterpret_cast<const uint4*>(a.sub + row_off);
+  }
+  // 2. residual add (exact, as in the staged kernel); prefix' becomes source S - 1
+  uint4 pn;
+  {
+    float p[8], o[8];
+    unpack8(pv4, p);
+    unpack8(ov4, o);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) p[e] += o[e];
+    pn = pack8(p);
+  }
+
+  // 3. per-source partials, eight sources at a time, reduce-scatter over the warp
+  {
+    float qf[8];
+    unpack8(qv4, qf);
+    partials_group<SMAX, 0>(xs, pn, a.n_blocks, qf, S, lane, red[warp]);
+    if constexpr (SMAX > 8) {
+      if (8 < S) partials_group<SMAX, 8>(xs, pn, a.n_blocks, qf, S, lane, red[warp]);
+    }
+    if constexpr (SMAX > 16) {
+      if (16 < S) partials_group<SMAX, 16>(xs, pn, a.n_blocks, qf, S, lane, red[warp]);
+      if (24 < S) partials_group<SMAX, 24>(xs, pn, a.n_blocks, qf, S, lane, red[warp]);
+    }
+  }
+  __syncthreads();
+
+  // 4. the exchange of the partials and the softmax, as in the staged kernel
+  cluster_wait();
+  if (tid < 2 * S) {
+    float sum = 0.f;
+    for (int w = 0; w < nwarps; ++w) sum += red[w][tid];
+    for (int k = 0; k < C; ++k) st_async(&part1[c][tid], (uint32_t)k, sum, &mbar[0]);
+  }
+  mbar_wait_bounded(&mbar[0]);
+  {
+    float sc = -INFINITY;
+    if (lane < S) {
+      float ssum = 0.f, dsum = 0.f;
+      for (int k = 0; k < C; ++k) {
+        ssum += part1[k][2 * lane];
+        dsum += part1[k][2 * lane + 1];
+      }
+      sc = dsum * rsqrtf(fmaf(ssum, invH, a.eps));
+    }
+    const float m = warp_max(sc);
+    const float e = lane < S ? expf(sc - m) : 0.f;
+    const float den = __shfl_sync(0xffffffffu, warp_sum(e), 0);
+    if (lane < S) alpha_w[warp][lane] = e / den;
+    __syncwarp();
+  }
+
+  // 5. the mixture from the registers, its sum of squares, the prefix / commit stores
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < SMAX; ++i) {
+    if (i < S) {
+      const float al = alpha_w[warp][i];
+      float x[8];
+      unpack8(source(xs, i, a.n_blocks, pn), x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(al, x[e], acc[e]);
+    }
+  }
+  const uint4 hv = pack8(acc);
+  float hf[8];
+  unpack8(hv, hf);
+  float hss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) hss = fmaf(hf[e], hf[e], hss);
+  if (own) {
+    *reinterpret_cast<uint4*>(a.mix + row_off) = hv;
+    if (a.commit) {
+      *reinterpret_cast<uint4*>(a.blocks + a.n_blocks * blk_stride + row_off) = pn;
+      *reinterpret_cast<uint4*>(a.prefix + row_off) = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      *reinterpret_cast<uint4*>(a.prefix + row_off) = pn;
+    }
+  }
+  hss = warp_sum(hss);
+  if (lane == 0) red2[warp] = hss;
+  __syncthreads();
+  if (tid < C) {
+    float sum = 0.f;
+    for (int w = 0; w < nwarps; ++w) sum += red2[w];
+    st_async(&part2[c], (uint32_t)tid, sum, &mbar[1]);
+  }
+  mbar_wait_bounded(&mbar[1]);
+
+  // 6. the RMSNorm of the mixture
+  float tot = 0.f;
+  for (int k = 0; k < C; ++k) tot += part2[k];
+  const float rs = rsqrtf(fmaf(tot, invH, a.eps));
+  if (own) {
+    float g[8];
+    unpack8(gv4, g);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) hf[e] = hf[e] * rs * g[e];
+    *reinterpret_cast<uint4*>(a.y + row_off) = pack8(hf);
+  }
+}
+
 // Static shared memory of the kernel (the reduction arrays above), kept out of the
 // dynamic budget.
 constexpr size_t kStaticSmem =
@@ -348,10 +576,17 @@ bool mix_plan(int hidden, int S, MixPlan* p) {
   int T = (nv + 31) / 32 * 32;
   if (T < 64) T = 64;  // threads 0 .. 2S-1 add the per-source partials
   if (T > kMaxThreads) T = kMaxThreads;
-  const size_t smem = (size_t)(S + 4) * W * 2;
-  if (smem > kDynSmemLimit) return false;
   p->C = C;
   p->W = W;
+  if (nv <= kRegThreads) {  // one thread per vector, every operand in registers
+    p->reg_smax = S <= 8 ? 8 : S <= 16 ? 16 : 32;
+    p->threads = T;
+    p->smem = 0;
+    return true;
+  }
+  const size_t smem = (size_t)(S + 4) * W * 2;
+  if (smem > kDynSmemLimit) return false;
+  p->reg_smax = 0;
   p->threads = T;
   p->smem = smem;
   return true;
@@ -391,7 +626,12 @@ cudaError_t launch_attnres_mix(const MixArgs& a, const MixPlan& p, cudaStream_t 
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, k_attnres_mix, a, p.W, p.C);
+  switch (p.reg_smax) {
+    case 8: return cudaLaunchKernelEx(&cfg, k_attnres_mix_reg<8>, a, p.W, p.C);
+    case 16: return cudaLaunchKernelEx(&cfg, k_attnres_mix_reg<16>, a, p.W, p.C);
+    case 32: return cudaLaunchKernelEx(&cfg, k_attnres_mix_reg<32>, a, p.W, p.C);
+    default: return cudaLaunchKernelEx(&cfg, k_attnres_mix, a, p.W, p.C);
+  }
 }
 
 cudaError_t mix_status(int* out, bool clear) {

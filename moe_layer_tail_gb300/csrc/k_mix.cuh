@@ -17,6 +17,7 @@ struct MixPlan {
   int W;         // columns per CTA (hidden / C, a multiple of 8)
   int threads;   // per CTA
   size_t smem;   // dynamic shared memory per CTA
+  int reg_smax;  // > 0: the register kernel for up to this many sources; 0: the staged one
 };
 
 // The plan for `hidden` columns and S sources; false when the shape is not supported

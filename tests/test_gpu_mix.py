@@ -108,11 +108,12 @@ def check_mix(gpu_mix, gpu_y, orc, srcs, alpha, gamma, eps):
     (16, 7168, 31, True, "unit"),     # the maximum source count
     (3, 256, 4, True, "unit"),        # two CTAs per row
     (4, 512, 6, False, "unit"),       # four CTAs per row
-    (3, 5408, 12, True, "scaled"),    # four CTAs, static + staging just above 48 KB
-    (2, 7168, 21, False, "unit"),     # eight CTAs, static + staging just above 48 KB
+    (3, 5408, 12, True, "scaled"),    # four CTAs of 169 vectors (register kernel)
+    (2, 7168, 21, False, "unit"),     # 22 sources (register kernel, up to 32)
+    (2, 17408, 6, True, "unit"),      # 272-vector chunks: staged kernel, just above 48 KB
     (2, 1000, 3, False, "scaled"),    # one CTA per row, hidden not a multiple of 64
     (5, 8192, 5, False, "unit"),
-    (2, 65536, 8, True, "unit"),      # the largest hidden size
+    (2, 65536, 8, True, "unit"),      # the largest hidden size (staged kernel)
     (4096, 64, 2, True, "unit"),      # the largest row count
 ])
 def test_mix_matches_oracle(R, H, n_blocks, commit, family):
@@ -130,7 +131,7 @@ def test_mix_matches_oracle(R, H, n_blocks, commit, family):
     check_mix(gm, gy, orc, srcs, orc["alpha"], d["gamma"], eps)
     if n_blocks == 0:
         assert np.array_equal(gm, pre_new)  # one source: alpha = 1, the mixture is prefix'
-    exp_ctas = {7168: 8, 256: 2, 512: 4, 5408: 4, 1000: 1, 8192: 8, 65536: 8, 64: 1}[H]
+    exp_ctas = {7168: 8, 256: 2, 512: 4, 5408: 4, 17408: 8, 1000: 1, 8192: 8, 65536: 8, 64: 1}[H]
     assert attnres_mix_ctas_per_row(H, n_blocks) == exp_ctas
 
 
