@@ -46,6 +46,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "k_mix.cuh"
 #include "moe_tail.h"
 #include "moe_tail_internal.cuh"
@@ -599,12 +601,13 @@ cudaError_t launch_attnres_mix(const MixArgs& a, const MixPlan& p, cudaStream_t 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static int done[64];
-    if (dev < 0 || dev >= 64 || !done[dev]) {
+    // (setting it twice from racing threads is harmless; the flag only saves the call)
+    static std::atomic<int> done[64];
+    if (dev < 0 || dev >= 64 || !done[dev].load(std::memory_order_acquire)) {
       e = cudaFuncSetAttribute(k_attnres_mix, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kDynSmemLimit);
       if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) done[dev] = 1;
+      if (dev >= 0 && dev < 64) done[dev].store(1, std::memory_order_release);
     }
   }
   cudaLaunchConfig_t cfg = {};

@@ -202,14 +202,16 @@ def test_decoder_sequence_graph_replays_match_eager(flags):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         mix_g, y_g = _sequence_on_gpu(seq, dd, flags)
-    for _ in range(50):
+    # 2,000 replays of the 187-call sequence, compared with the eager run every 500
+    for i in range(2000):
         dd["prefix"].copy_(pre0)
         dd["blocks"].copy_(blk0)
         g.replay()
-    torch.cuda.synchronize()
-    got = [bf16_tensor_to_bits(t) for t in (mix_g, y_g, dd["prefix"], dd["blocks"])]
-    for a, b in zip(ref, got):
-        assert np.array_equal(a, b)
+        if i % 500 == 499:
+            torch.cuda.synchronize()
+            got = [bf16_tensor_to_bits(t) for t in (mix_g, y_g, dd["prefix"], dd["blocks"])]
+            for a, b in zip(ref, got):
+                assert np.array_equal(a, b)
 
 
 def test_mix_refusals_on_device():
