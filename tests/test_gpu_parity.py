@@ -457,3 +457,37 @@ def test_persistent_mode_barrier_timeout_is_reported_and_reset():
     got = run_gpu(good, d)
     check_parity(got[0], got[1], got[2], orc, shape.k)
     assert good.status() == 0
+
+
+def test_graph_of_mixed_widths_replays_bitwise():
+    """Six calls of widths 8, 1, 3, 8, 2, 5 captured in one CUDA graph (each on its own
+    buffers) replay bitwise equal to the same calls run eagerly."""
+    shape, d = _small(16, R=8, H=512, E=24, k=4, I=256, Is=192)
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    tail = MoeTail(shape, dev, max_rows=8)
+    widths = [8, 1, 3, 8, 2, 5]
+    xs = [acts_to_device(gen.make_activations(shape, 700 + i, rows=w)["x"])
+          for i, w in enumerate(widths)]
+    r0 = [acts_to_device(gen.make_activations(shape, 700 + i, rows=w)["residual"])
+          for i, w in enumerate(widths)]
+    eager = []
+    for x, r in zip(xs, r0):
+        res, out = r.clone(), torch.empty_like(x)
+        tail.run(x, res, out)
+        torch.cuda.synchronize()
+        eager.append((bf16_tensor_to_bits(out), bf16_tensor_to_bits(res)))
+    res = [r.clone() for r in r0]
+    outs = [torch.empty_like(x) for x in xs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for x, rr, r, o in zip(xs, r0, res, outs):
+            r.copy_(rr)
+            tail.run(x, r, o)
+    for i in range(200):
+        g.replay()
+        if i % 100 == 99:
+            torch.cuda.synchronize()
+            for (eo, er), o, r in zip(eager, outs, res):
+                assert np.array_equal(bf16_tensor_to_bits(o), eo)
+                assert np.array_equal(bf16_tensor_to_bits(r), er)
+    assert tail.status() == 0
