@@ -179,6 +179,13 @@ int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host, vo
  * also resets the grid barrier a call that gave up may have left half counted). Returns
  * MOE_TAIL_ERR_DEVICE when the word is nonzero, MOE_TAIL_OK otherwise. */
 int moe_tail_get_status(moe_tail_t* h, int32_t* device_status);
+
+/* Guard check of the handle's scratch (for tests and debugging): every scratch buffer is
+ * followed by 256 bytes of a fixed pattern written at create; this synchronises the device
+ * and verifies them all.  Returns MOE_TAIL_OK, MOE_TAIL_ERR_DEVICE when a kernel wrote past
+ * the end of a buffer (moe_tail_last_cuda_error() names the guard), MOE_TAIL_ERR_CUDA when
+ * a copy fails, MOE_TAIL_ERR_INVALID_ARG for a NULL handle. */
+int moe_tail_check_scratch(moe_tail_t* h);
 int moe_tail_clear_status(moe_tail_t* h);
 
 /* Copy the routing of the last run on `stream` (stream-ordered, synchronises it):

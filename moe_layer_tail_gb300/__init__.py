@@ -92,6 +92,8 @@ def load_library(path: str = None):
     lib.moe_tail_run_attn.restype = ctypes.c_int
     lib.moe_tail_get_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.moe_tail_get_status.restype = ctypes.c_int
+    lib.moe_tail_check_scratch.argtypes = [P]
+    lib.moe_tail_check_scratch.restype = ctypes.c_int
     lib.moe_tail_clear_status.argtypes = [P]
     lib.moe_tail_clear_status.restype = ctypes.c_int
     lib.moe_tail_debug_routing.argtypes = [P, P, P, ctypes.POINTER(i32), P]
@@ -198,6 +200,12 @@ class MoeTail:
         if rc not in (OK, ERR_DEVICE, ERR_TIMEOUT):
             raise MoeTailError(rc, "moe_tail_get_status")
         return int(v.value)
+
+    def check_scratch(self) -> None:
+        """Raise if a kernel wrote past the end of a scratch buffer (guard words)."""
+        rc = self._lib.moe_tail_check_scratch(self._h)
+        if rc != OK:
+            raise MoeTailError(rc, "moe_tail_check_scratch")
 
     def clear_status(self) -> None:
         rc = self._lib.moe_tail_clear_status(self._h)

@@ -20,6 +20,12 @@
 
 using namespace mtail;
 
+// Every scratch buffer is followed by kCanaryBytes of a known pattern; a kernel that writes
+// past the end of a buffer changes them (moe_tail_check_scratch).
+constexpr int kMaxCanaries = 32;
+constexpr size_t kCanaryBytes = 256;
+constexpr unsigned char kCanaryByte = 0xA5;
+
 struct moe_tail {
   moe_tail_config_t cfg;
   Weights w;
@@ -34,6 +40,8 @@ struct moe_tail {
   int last_rows;
   cudaEvent_t ev[2 * 16];  // optional stage events (moe_tail_set_stage_events)
   int n_ev;
+  size_t canary_off[kMaxCanaries];  // slab offsets of the guard words after each buffer
+  int n_canary;
 };
 
 static thread_local char g_cuda_err[256];
@@ -89,14 +97,22 @@ static int check_config(const moe_tail_config_t* c) {
   return MOE_TAIL_OK;
 }
 
-// Carve the scratch buffers out of one slab (256-byte aligned pieces).
-static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
+// Carve the scratch buffers out of one slab (256-byte aligned pieces, each followed by a
+// guard region whose offset goes to canaries[]).
+static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s, size_t* canaries,
+                    int* n_canary) {
   const size_t R = c->max_rows, H = c->hidden, E = c->n_experts, k = c->top_k,
                I = c->expert_inter, Is = c->shared_inter, P = R * k;
   size_t off = 0;
+  int nc = 0;
   auto take = [&](size_t bytes) -> char* {
     char* p = base ? base + off : nullptr;
     off += (bytes + 255) & ~(size_t)255;
+    if (nc < kMaxCanaries) {
+      if (canaries) canaries[nc] = off;
+      ++nc;
+    }
+    off += kCanaryBytes;
     return p;
   };
   s->rnew = (__nv_bfloat16*)take(R * H * 2);
@@ -122,6 +138,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s) {
   s->xpart = (float*)take((size_t)kMaxOutProjParts * R * H * 4);
   s->status = (int32_t*)take(4);
   s->counters = (uint32_t*)take(kCtrWords * 4);
+  if (n_canary) *n_canary = nc < kMaxCanaries ? nc : kMaxCanaries;
   return off;
 }
 
@@ -171,13 +188,15 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
     h->persist_grid = h->num_sms;
   }
   if (e != cudaSuccess) { delete h; return cuda_fail(e); }
-  h->slab_bytes = carve(cfg, nullptr, &h->s);
+  h->slab_bytes = carve(cfg, nullptr, &h->s, nullptr, nullptr);
   e = cudaMalloc(&h->slab, h->slab_bytes);
   if (e != cudaSuccess) { delete h; return cuda_fail(e); }
-  carve(cfg, (char*)h->slab, &h->s);
+  carve(cfg, (char*)h->slab, &h->s, h->canary_off, &h->n_canary);
   const size_t act = (size_t)cfg->max_rows * cfg->hidden * 2;
   e = cudaMalloc(&h->stage, 3 * act);
   if (e == cudaSuccess) e = cudaMemset(h->slab, 0, h->slab_bytes);
+  for (int i = 0; e == cudaSuccess && i < h->n_canary; ++i)
+    e = cudaMemset((char*)h->slab + h->canary_off[i], kCanaryByte, kCanaryBytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cudaFree(h->slab);
@@ -459,4 +478,23 @@ extern "C" int moe_attnres_mix_get_status(int* status, int clear) {
   if (e != cudaSuccess) return cuda_fail(e);
   *status = v;
   return v ? MOE_TAIL_ERR_DEVICE : MOE_TAIL_OK;
+}
+
+extern "C" int moe_tail_check_scratch(moe_tail_t* h) {
+  if (!h) return MOE_TAIL_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned char buf[kCanaryBytes];
+  for (int i = 0; i < h->n_canary; ++i) {
+    e = cudaMemcpy(buf, (const char*)h->slab + h->canary_off[i], kCanaryBytes,
+                   cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    for (size_t b = 0; b < kCanaryBytes; ++b)
+      if (buf[b] != kCanaryByte) {
+        snprintf(g_cuda_err, sizeof(g_cuda_err), "scratch guard %d overwritten at byte %zu", i,
+                 b);
+        return MOE_TAIL_ERR_DEVICE;
+      }
+  }
+  return MOE_TAIL_OK;
 }

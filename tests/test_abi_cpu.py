@@ -189,3 +189,7 @@ def _mix_call(lib, **kw):
 ])
 def test_attnres_mix_refuses_bad_arguments_before_any_launch(lib, kw, code):
     assert _mix_call(lib, **kw) == code
+
+
+def test_check_scratch_refuses_null_handle(lib):
+    assert lib.moe_tail_check_scratch(None) == mt.ERR_INVALID_ARG

@@ -32,6 +32,7 @@ def run_gpu(tail, d, rows=None):
     tail.run(x, res, out, rows=R)
     torch.cuda.synchronize()
     ids, wts, nd = tail.routing(R)
+    tail.check_scratch()  # no kernel wrote past the end of a scratch buffer
     return bf16_tensor_to_bits(out[:R]), bf16_tensor_to_bits(res[:R]), ids, wts, nd
 
 
