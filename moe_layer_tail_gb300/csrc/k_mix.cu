@@ -19,8 +19,9 @@
 // cluster ranks), so all CTAs of a row use bit-identical scores and norms.
 //
 // Two forms: k_attnres_mix_reg (chunks of at most 2048 columns, one thread per 16-byte vector,
-// every source in registers; H 7168 and most shapes) and k_attnres_mix below (any chunk,
-// operands staged in shared memory).  Both add in the same order.
+// every source in registers; H 7168 and most shapes) and k_attnres_mix below (wider
+// chunks, operands staged in shared memory, threads looping over several vectors).  With one
+// vector per thread the two add in the same order.
 //
 // Per CTA (row r = blockIdx.y, chunk c = cluster rank, W columns):
 //   1. cp.async stages the chunk of every source, the prefix, the sublayer output, q and
@@ -395,7 +396,7 @@ __device__ __forceinline__ void partials_group(const uint4 (&xs)[SMAX], uint4 pn
 // (W <= 2048): one thread per 16-byte vector, up to SMAX sources held as uint4 registers.
 // The loads go straight to registers (no shared-memory staging and no copy wait beyond the
 // loads themselves), and both passes over the sources read registers.  Sources keep the
-// order of the staged kernel (blocks, then prefix'), so both give the same sums.
+// order of the staged kernel (blocks, then prefix').
 constexpr int kRegThreads = 256;
 
 template <int SMAX>
