@@ -6,8 +6,12 @@ HBM GB/s, for the 8-row, 256-expert top-8 workload with ~40% repeated picks
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one full call of the tail (add+RMSNorm, router, top-k, dedup, routed MXFP4
-experts, bf16 shared expert, combine) on its own 8-row input set.  Each step streams
-~1 GB of weights, larger than the 126 MB L2, so no flush is needed between steps.
+experts, bf16 shared expert, combine) on its own 8-row input set.  Consecutive steps run on
+different copies of the layer's weights (L = max(4, ceil(4 x L2 / bytes per call)) copies,
+one library handle each, like consecutive decoder layers), so no step finds its weights in
+L2 and no flush is needed.  Besides the K timed steps the line carries the protocol
+statistic: a CUDA graph of L calls replayed 7 trials x 50 replays in 2 rounds, median per
+call.  --workload picks another of the five workloads.
 
 Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are independent replicas: the
 path has no cross-GPU exchange; value = all ranks' calls / max-over-ranks time.
@@ -51,6 +55,9 @@ def parse_args():
     p.add_argument("--workload", default=gen.BENCH_WORKLOAD)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-protocol", action="store_true",
+                   help="skip the CUDA-graph protocol statistic (7 trials x 50 replays x 2 "
+                        "rounds)")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: the workload with this many experts instead (a "
                         "smaller case of the same kernels, e.g. for an ncu capture); the "
@@ -192,6 +199,17 @@ def ncu_traffic(kernel_tag, src_hash, algorithmic_bytes):
 
 # --------------------------------------------------------------------- our arm ----
 
+L2_BYTES = 126 * 1024 * 1024  # GB300 L2 as the driver reports it (cudaDevAttrL2CacheSize)
+PROTOCOL_TRIALS, PROTOCOL_REPLAYS, PROTOCOL_ROUNDS = 7, 50, 2
+MAX_COPIES = 1024
+
+
+def weight_copies(bytes_per_call: float) -> int:
+    """Layers (weight copies) a timed sequence rotates over: max(4, ceil(4 L2 / B)), so that
+    the weights streamed between two calls on the same copy exceed the L2 four times."""
+    return int(min(MAX_COPIES, max(4, -(-4 * L2_BYTES // max(1, int(bytes_per_call))))))
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import moe_layer_tail_gb300 as mt
@@ -211,7 +229,15 @@ def run_ours(args, rank, world, local_rank):
         host_w["ws_gate"] = gen.make_weight(shape, wl.seed, "ws_gate")
     if args.out_proj:
         host_w["w_o"] = gen.make_weight(shape, wl.seed, "w_o")
-    dev_w = mt.weights_to_device(host_w)
+    # L copies of the layer's weights (same bits, separate device memory), one handle each:
+    # consecutive calls run on different copies, like consecutive decoder layers, so no
+    # call finds its weights in L2 from the call before
+    est = gen.algorithmic_bytes(shape, min(shape.E, R * shape.k), gated=args.shared_gate,
+                                out_proj=bool(args.out_proj))
+    L = weight_copies(est)
+    dev_w = [mt.weights_to_device(host_w)]
+    for _ in range(L - 1):
+        dev_w.append({k: v.clone() for k, v in dev_w[0].items()})
     # one input set per step: correlated rows (~40% repeated picks), seeds wl.seed + 1000*i
     xs, rs = [], []
     c = gen.similar_c() if wl.kind == "similar" else None
@@ -224,15 +250,18 @@ def run_ours(args, rank, world, local_rank):
     res0 = mt.acts_to_device(np.stack(rs))
     res = res0.clone()
     out = torch.empty_like(res0)
-    tail = mt.MoeTail(shape, dev_w, max_rows=R,
-                      mode=mt.MODE_PERSISTENT if args.persistent else mt.MODE_MULTI_KERNEL)
-    nst = tail.launches_per_run(R) + (1 if args.out_proj else 0)
+    mode = mt.MODE_PERSISTENT if args.persistent else mt.MODE_MULTI_KERNEL
+    tails = [mt.MoeTail(shape, dw, max_rows=R, mode=mode) for dw in dev_w]
+    nst = tails[0].launches_per_run(R) + (1 if args.out_proj else 0)
     stream = torch.cuda.current_stream()
-    call = tail.run_attn if args.out_proj else tail.run
+
+    def call(i, stream=None):
+        t = tails[i % L]
+        (t.run_attn if args.out_proj else t.run)(x_all[i], res[i], out[i], stream=stream)
 
     # warm-up
     for i in range(W):
-        call(x_all[i], res[i], out[i])
+        call(i)
     torch.cuda.synchronize()
 
     # per-step stage events (recorded by the library around each launch, on our stream)
@@ -244,7 +273,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     ev_handles = [[e.cuda_event for e in row] for row in evs]
 
-    # timed region: K calls, nothing else on the stream
+    # timed region: K calls (step i on input set W + i and weight copy (W + i) mod L),
+    # nothing else on the stream
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -254,13 +284,62 @@ def run_ours(args, rank, world, local_rank):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(K):
-        call(x_all[W + i], res[W + i], out[W + i], stream=stream)
+        call(W + i, stream=stream)
     t1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1))
+
+    # the measurement protocol: a CUDA graph of L calls (one per weight copy, input sets
+    # 0..L-1), timed per replay with events on its stream; the residuals the calls update are
+    # restored before each replay, outside the events; 7 trials x 50 replays, two rounds
+    # (graph over the copies in order, then in reverse order, alternating)
+    proto = None
+    if not args.persistent and not args.no_protocol:
+        Lg = min(L, nsets)
+        graphs = []
+        cap = torch.cuda.Stream()
+        for order in (list(range(Lg)), list(range(Lg))[::-1]):
+            res.copy_(res0)
+            torch.cuda.synchronize()
+            cap.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                for j in order:
+                    t = tails[j]
+                    (t.run_attn if args.out_proj else t.run)(x_all[j], res[j], out[j],
+                                                             stream=cap)
+            graphs.append(g)
+        pristine = res0[:Lg].clone()
+        per_call = []
+        pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(PROTOCOL_REPLAYS)]
+        for rnd in range(PROTOCOL_ROUNDS):
+            for trial in range(PROTOCOL_TRIALS):
+                g = graphs[(rnd * PROTOCOL_TRIALS + trial) % 2]
+                for rep in range(PROTOCOL_REPLAYS):
+                    res[:Lg].copy_(pristine)
+                    pe[rep][0].record(stream)
+                    g.replay()
+                    pe[rep][1].record(stream)
+                torch.cuda.synchronize()
+                ms = sum(a.elapsed_time(b) for a, b in pe)
+                per_call.append(ms * 1000.0 / (PROTOCOL_REPLAYS * Lg))
+        res.copy_(res0)
+        torch.cuda.synchronize()
+        del graphs
+        proto = {"median_us_per_call": round(statistics.median(per_call), 3),
+                 "min_us": round(min(per_call), 3), "max_us": round(max(per_call), 3),
+                 "trials": len(per_call), "replays_per_trial": PROTOCOL_REPLAYS,
+                 "calls_per_replay": Lg,
+                 "how": "CUDA graph of %d calls on %d weight copies, events around each "
+                        "replay; residuals restored between replays outside the events; "
+                        "median of %d trials x %d replays in %d rounds, the graph's call "
+                        "order alternating between trials" % (Lg, Lg, PROTOCOL_TRIALS,
+                                                               PROTOCOL_REPLAYS,
+                                                               PROTOCOL_ROUNDS)}
+    clk = clocks.stop()
 
     # stage-timed pass: the same K calls again (residuals restored), with the library
     # recording an event pair around each launch on the launching stream
@@ -270,25 +349,27 @@ def run_ours(args, rank, world, local_rank):
     s1 = torch.cuda.Event(enable_timing=True)
     s0.record(stream)
     for i in range(K):
-        tail.set_stage_events(ev_handles[i])
-        call(x_all[W + i], res[W + i], out[W + i], stream=stream)
+        t = tails[(W + i) % L]
+        t.set_stage_events(ev_handles[i])
+        call(W + i, stream=stream)
+        t.set_stage_events(None)
     s1.record(stream)
     torch.cuda.synchronize()
-    tail.set_stage_events(None)
     staged_ms = s0.elapsed_time(s1)
-    status = tail.status()
+    status = max(t.status() for t in tails)
 
     stage_ms = np.array([[row[2 * s].elapsed_time(row[2 * s + 1]) for s in range(nst)]
                          for row in evs])  # [K, stages]
 
     # distinct experts of every timed set (replayed untimed from pristine residuals)
     Ds = []
-    res_chk = res0.clone()
+    res.copy_(res0)
     for i in range(K):
-        call(x_all[W + i], res_chk[W + i], out[W + i])
-        _, _, nd = tail.routing(R)
+        call(W + i)
+        _, _, nd = tails[(W + i) % L].routing(R)
         Ds.append(nd)
     Ds = np.array(Ds)
+    res.copy_(res0)
     bytes_per = np.array([gen.algorithmic_bytes(shape, int(d), gated=args.shared_gate,
                                                  out_proj=bool(args.out_proj)) for d in Ds])
     total_bytes = float(bytes_per.sum())
@@ -327,8 +408,8 @@ def run_ours(args, rank, world, local_rank):
     result = {
         "metric": METRIC, "value": round(us_per_call, 3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(elapsed_ms / K, 5),
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp4xbf16->f32", "data": "synthetic",
         "config": {"workload": wl.name + ("" if not args.experts else " with %d experts" % shape.E)
                                + (" with shared-expert gate" if args.shared_gate else "")
                                + (" with out_proj from %d" % shape.Ha if args.out_proj else "")
@@ -336,52 +417,62 @@ def run_ours(args, rank, world, local_rank):
                    "rows": R, "hidden": shape.H, "experts": shape.E,
                    "top_k": shape.k, "expert_inter": shape.I, "shared_inter": shape.Is,
                    "weights": "MXFP4 routed experts, bf16 router and shared expert",
+                   "arithmetic": "MXFP4 weights x bf16 activations (fed to the tensor cores "
+                                 "as f16 with power-of-two scales), fp32 accumulation",
                    "distinct_experts_mean": round(float(Ds.mean()), 2),
                    "repeat_fraction_mean": round(float(1 - Ds.mean() / (R * shape.k)), 3),
                    "bytes_per_call_mean": int(bytes_per.mean()),
                    "input_sets": nsets,
-                   "l2": "no flush: each step streams ~%.0f MB of weights, larger than the "
-                         "126 MB L2" % (bytes_per.mean() / 1e6),
+                   "weight_copies": L,
+                   "l2": "no flush: consecutive calls rotate over %d copies of the weights "
+                         "(one handle each), each call streaming ~%.0f MB of its own copy's "
+                         "weights, larger than the 126 MB L2" % (L, bytes_per.mean() / 1e6),
                    "parallelism": "replicas" if world > 1 else "single"},
         "gbps": round(gbps, 1),
         "hbm_frac_of_%s_peak" % peak_kind: round(gbps / peak, 4),
         "stages_us": {n: round(float(tot[i] / K * 1000), 2) for i, n in enumerate(names)},
         "roofline": roof,
+        "protocol": proto,
         "clocks": clk,
         "gpu_launches": int(K * nst),
         "device_status": status,
     }
 
-    # end to end through the C ABI with host buffers (H2D/D2H inside the timed region)
+    # end to end through the C ABI with host buffers (H2D/D2H inside the timed region): per
+    # step one pinned host block [x; residual; out], one copy in and one copy out
     if not args.no_e2e and not args.out_proj:
-        import torch as _t
         ke = min(K, 200)
-        hx = [_t.from_numpy(xs[W + i].view(np.int16)).view(_t.bfloat16).pin_memory()
-              for i in range(ke)]
-        hr = [_t.from_numpy(rs[W + i].view(np.int16).copy()).view(_t.bfloat16).pin_memory()
-              for i in range(ke)]
-        ho = _t.empty((R, shape.H), dtype=_t.bfloat16).pin_memory()
-        tail.run_host(hx[0], hr[0].clone().pin_memory(), ho)  # warm the staging path
-        _t.cuda.synchronize()
+        blocks = []
+        for i in range(ke):
+            hb = torch.empty((3, R, shape.H), dtype=torch.bfloat16).pin_memory()
+            hb[0].copy_(torch.from_numpy(xs[W + i].view(np.int16)).view(torch.bfloat16))
+            hb[1].copy_(torch.from_numpy(rs[W + i].view(np.int16)).view(torch.bfloat16))
+            blocks.append(hb)
+        warm = blocks[0].clone().pin_memory()
+        tails[0].run_host(warm[0], warm[1], warm[2])  # warm the staging path
+        torch.cuda.synchronize()
         ts = time.perf_counter()
         for i in range(ke):
-            tail.run_host(hx[i], hr[i], ho)
+            hb = blocks[i]
+            tails[(W + i) % L].run_host(hb[0], hb[1], hb[2])
         te = time.perf_counter()
         e2e_us = (te - ts) * 1e6 / ke
         result["e2e"] = {"value": round(e2e_us / world, 3), "unit": UNIT,
                          "h2d_bytes_per_step": 2 * R * shape.H * 2,
                          "d2h_bytes_per_step": 2 * R * shape.H * 2, "steps": ke,
-                         "api": "moe_tail_run_host (pinned host x/residual in, out/residual back)"}
+                         "api": "moe_tail_run_host on one pinned host block [x; residual; out] "
+                                "per step (one copy in, one copy out)"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shape, host_w, xs[W], rs[W],
                                               attn=bool(args.out_proj))
-    tail.close()
+    for t in tails:
+        t.close()
     return result
 
 
 # The pages' own per-call figures for their split mix over a 187-call decoder sequence in a
-# CUDA graph, by row count (RTX PRO 6000; another machine and kernel: context for the ratio).
+# CUDA graph, by row count (RTX PRO 6000; another machine and kernel: context only).
 PAGE_MIX_US = {1: 3.38, 8: 3.44, 16: 3.66}
 
 
@@ -456,8 +547,7 @@ def run_mix(args, rank, world, local_rank):
         "metric": METRIC, "value": round(us_per_call, 3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(elapsed_ms / K, 5),
         "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": (round(us_per_call / PAGE_MIX_US[R], 4) if R in PAGE_MIX_US else None),
-        "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16->f32", "data": "synthetic",
         "config": {"workload": "attnres_mix_h7168_187calls_r%d" % R, "rows": R, "hidden": H,
                    "calls_per_step": L, "block_calls": seq.block_calls,
                    "sources_per_call": "%d..%d" % (seq.n_blocks(0) + 1,
@@ -467,10 +557,9 @@ def run_mix(args, rank, world, local_rank):
                    "launch": "CUDA graph, " + ("plain launches" if args.no_pdl else
                                                "programmatic dependent launches"),
                    "l2": "flushed (256 MB write) between replays, outside the timed events",
-                   "context": "the pages quote 3.38 / 3.44 / 3.66 us per call at 1 / 8 / 16 "
-                              "rows for their split mix on an RTX PRO 6000 (another machine "
-                              "and another kernel: context, not a target); vs_baseline is "
-                              "this line's value over that figure (lower is better)",
+                   "context": "the pages quote %s us per call at %d rows for their split mix "
+                              "on an RTX PRO 6000 (another machine and another kernel: "
+                              "context, not a baseline)" % (PAGE_MIX_US.get(R, "no figure"), R),
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "kernel": "attnres_mix", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",

@@ -170,7 +170,10 @@ int moe_tail_run_attn(moe_tail_t* h, const void* attn, void* residual, void* out
 
 /* The same call on HOST buffers: copies x and residual to the handle's device staging
  * buffers, runs, copies residual and out back, and synchronises `stream` before returning.
- * Pinned host memory gives asynchronous copies; pageable memory works too. */
+ * Pinned host memory gives asynchronous copies; pageable memory works too.  When the three
+ * buffers are one block [x; residual; out] (residual_host = x_host + rows*H*2 bytes and
+ * out_host = residual_host + rows*H*2), x and residual go in one copy and residual and out
+ * come back in one copy. */
 int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host, void* out_host,
                       int32_t rows, void* stream);
 
@@ -209,24 +212,31 @@ int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows);
  * cudaMalloc: a host framework that owns every device allocation and hands a plugin only
  * its input and output tensors, or a decode step replayed from a memory pool that is
  * frozen once warm-up is over.  It runs add + RMSNorm, the router GEMV and the top-k with
- * renormalised weights on `stream`, with the same arithmetic as the front of moe_tail_run:
+ * renormalised weights on `stream`, with the arithmetic of the fused front
+ * (MOE_TAIL_DEBUG_FUSED_FRONT): its logits are summed in another order than the default
+ * front of moe_tail_run (which runs the router on the tensor cores), so they may differ in
+ * the last bits, and a pick can differ from moe_tail_run's where two logits are that close.
  *   x, residual  bf16 [rows, hidden] device (both only read here)
  *   gamma bf16 [hidden], router_w bf16 [n_experts, hidden] device
  *   ids int32 [rows, top_k], wts float [rows, top_k] device, written in pick order;
- *   n_distinct int32 device, may be NULL: the number of distinct experts picked.
+ *   n_distinct int32 device, may be NULL: the number of distinct experts picked;
+ *   status int32 device, may be NULL: this call's MOE_TAIL_STATUS_* bits (0 = clean;
+ *     MOE_TAIL_STATUS_BAD_ROUTING when a row ran out of numeric logits, its remaining picks
+ *     then being the lowest untaken ids), written when the call completes.
  * Its scratch is one fixed 71,696-byte array in the library's own device memory (a
  * file-scope variable that every GPU which loads the library keeps until the process
  * exits).  The array bounds the call: rows <= 16, n_experts <= 1024, top_k <= 32 (and
  * hidden a multiple of 128); anything larger returns MOE_TAIL_ERR_UNSUPPORTED.  The first
- * call on a device looks up the array's device address with that device current, so make
- * that first call before any stream capture.  Every call shares the array and it keeps the
- * last call's contents (the call clears its own counter first): calls that overlap on the
- * same GPU race, so issue them in one stream or otherwise ordered.  Nothing is allocated or
- * freed.  The pages have no counterpart to this entry point. */
+ * call on a device looks up the array's device address with that device current (once,
+ * safe from several host threads), so make that first call before any stream capture.
+ * Every call shares the array and it keeps the last call's contents (each call clears its
+ * status word and counter first): calls that overlap on the same GPU race, so issue them
+ * in one stream or otherwise ordered.  Nothing is allocated or freed.  The pages have no
+ * counterpart to this entry point. */
 int moe_tail_route_noalloc(const void* x, const void* residual, const void* gamma,
                            const void* router_w, int32_t rows, int32_t hidden,
                            int32_t n_experts, int32_t top_k, float rms_eps, int32_t* ids,
-                           float* wts, int32_t* n_distinct, void* stream);
+                           float* wts, int32_t* n_distinct, int32_t* status, void* stream);
 
 /* Free the handle and its scratch (synchronises the device first).  NULL is a no-op. */
 void moe_tail_destroy(moe_tail_t* h);

@@ -14,6 +14,8 @@
 // cross-checking path.  bf16(x + residual) goes to scratch; the residual itself is
 // rewritten by the combine, after every reader is done.
 #include <algorithm>
+#include <cstddef>
+#include <mutex>
 
 #include "k_front.cuh"
 #include "moe_tail.h"
@@ -583,24 +585,25 @@ namespace mtail {
 struct RouteScratch {
   float logits[kMaxRows * kMaxExperts];
   int32_t n_distinct;
-  int32_t status;
   int32_t uniq[kMaxPicks];
   int32_t user_off[kMaxPicks + 1];
   int32_t user_list[kMaxPicks];
-  uint32_t ticket;
+  int32_t status;   // status bits of the running call (cleared with the ticket)
+  uint32_t ticket;  // CTAs done with their logits (the last one ranks)
 };
 
 static_assert(sizeof(RouteScratch) == 71696, "the size stated in moe_tail.h");
 static __device__ __align__(256) uint8_t g_route_scratch[sizeof(RouteScratch)];
 
-// Same arithmetic as k_front_fused (same rstd, n and logit order, same top-k), without the
-// stores the expert stages need; ids/wts/n_distinct go to the caller's buffers.
+// Same arithmetic as k_front_fused, the fused-front form of moe_tail_run (same rstd, n
+// and logit order, same top-k), without the stores the expert stages need; ids, wts,
+// n_distinct and the call's status bits go to the caller's buffers.
 __global__ void __launch_bounds__(kFrontThreads)
 k_route_static(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ residual,
                const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ w_r,
                RouteScratch* __restrict__ rs, int32_t* __restrict__ ids_out,
-               float* __restrict__ wts_out, int32_t* __restrict__ nd_out, int R, int H, int E,
-               int k, float eps) {
+               float* __restrict__ wts_out, int32_t* __restrict__ nd_out,
+               int32_t* __restrict__ status_out, int R, int H, int E, int k, float eps) {
   __shared__ float s_rstd[kMaxRows];
   __shared__ uint4 s_n[kMaxRows][kFrontChunk / 8];
   __shared__ int s_last;
@@ -685,14 +688,18 @@ k_route_static(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restr
   __syncthreads();
   if (tid == 0) {
     if (nd_out) *nd_out = rs->n_distinct;
+    if (status_out) *status_out = *(volatile int32_t*)&rs->status;
     rs->ticket = 0u;
   }
 }
 
 // Device address of the scratch array, looked up once per device (with that device
-// current) the first time the entry point runs on it.
-static void* g_route_scratch_ptr[64];
-static int g_route_scratch_ready[64];
+// current) the first time the entry point runs on it; std::call_once makes the lookup
+// and its publication safe when several host threads make that first call together.
+constexpr int kRouteMaxDevices = 64;
+static std::once_flag g_route_once[kRouteMaxDevices];
+static void* g_route_scratch_ptr[kRouteMaxDevices];
+static cudaError_t g_route_scratch_err[kRouteMaxDevices];
 
 }  // namespace mtail
 
@@ -700,7 +707,7 @@ extern "C" int moe_tail_route_noalloc(const void* x, const void* residual, const
                                       const void* router_w, int32_t rows, int32_t hidden,
                                       int32_t n_experts, int32_t top_k, float rms_eps,
                                       int32_t* ids, float* wts, int32_t* n_distinct,
-                                      void* stream) {
+                                      int32_t* status, void* stream) {
   using namespace mtail;
   if (!x || !residual || !gamma || !router_w || !ids || !wts) return MOE_TAIL_ERR_INVALID_ARG;
   const void* ptrs[4] = {x, residual, gamma, router_w};
@@ -711,23 +718,28 @@ extern "C" int moe_tail_route_noalloc(const void* x, const void* residual, const
       !(rms_eps > 0.f))
     return MOE_TAIL_ERR_UNSUPPORTED;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_TAIL_ERR_CUDA;
-  if (!g_route_scratch_ready[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kRouteMaxDevices)
+    return MOE_TAIL_ERR_CUDA;
+  std::call_once(g_route_once[dev], [dev]() {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
-      return MOE_TAIL_ERR_CUDA;
-    g_route_scratch_ptr[dev] = p;
-    g_route_scratch_ready[dev] = 1;
-  }
+    cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e == cudaSuccess && p == nullptr) e = cudaErrorInvalidSymbol;
+    g_route_scratch_err[dev] = e;
+    g_route_scratch_ptr[dev] = (e == cudaSuccess) ? p : nullptr;
+  });
+  if (g_route_scratch_err[dev] != cudaSuccess) return MOE_TAIL_ERR_CUDA;
   RouteScratch* rs = (RouteScratch*)g_route_scratch_ptr[dev];
   cudaStream_t st = (cudaStream_t)stream;
-  // the ticket must start at zero (a call that stopped part-way could have left it set)
-  if (cudaMemsetAsync(&rs->ticket, 0, sizeof(uint32_t), st) != cudaSuccess)
-    return MOE_TAIL_ERR_CUDA;
+  // the status word and the ticket must start at zero (the status word holds the previous
+  // call's bits; a call that stopped part-way could have left the ticket set); they are
+  // adjacent in the array, so one memset clears both
+  static_assert(offsetof(RouteScratch, ticket) == offsetof(RouteScratch, status) + 4,
+                "status and ticket adjacent");
+  if (cudaMemsetAsync(&rs->status, 0, 8, st) != cudaSuccess) return MOE_TAIL_ERR_CUDA;
   const int grid = (n_experts + kFrontWarps - 1) / kFrontWarps;
   k_route_static<<<grid, kFrontThreads, 0, st>>>(
       (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual, (const __nv_bfloat16*)gamma,
-      (const __nv_bfloat16*)router_w, rs, ids, wts, n_distinct, rows, hidden, n_experts, top_k,
-      rms_eps);
+      (const __nv_bfloat16*)router_w, rs, ids, wts, n_distinct, status, rows, hidden, n_experts,
+      top_k, rms_eps);
   return cudaGetLastError() == cudaSuccess ? MOE_TAIL_OK : MOE_TAIL_ERR_CUDA;
 }

@@ -366,18 +366,28 @@ extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residu
   if (!h || !x_host || !residual_host || !out_host) return MOE_TAIL_ERR_INVALID_ARG;
   if (rows < 1 || rows > h->cfg.max_rows) return MOE_TAIL_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  const size_t act = (size_t)h->cfg.max_rows * h->cfg.hidden * 2;
   const size_t bytes = (size_t)rows * h->cfg.hidden * 2;
+  // device staging [x; residual; out], `bytes` apart, so that host buffers laid out the
+  // same way move in one copy each way
   char* dx = (char*)h->stage;
-  char* dres = dx + act;
-  char* dout = dres + act;
-  cudaError_t e = cudaMemcpyAsync(dx, x_host, bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(dres, residual_host, bytes, cudaMemcpyHostToDevice, st);
+  char* dres = dx + bytes;
+  char* dout = dres + bytes;
+  cudaError_t e;
+  if ((const char*)residual_host == (const char*)x_host + bytes) {
+    e = cudaMemcpyAsync(dx, x_host, 2 * bytes, cudaMemcpyHostToDevice, st);
+  } else {
+    e = cudaMemcpyAsync(dx, x_host, bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dres, residual_host, bytes, cudaMemcpyHostToDevice, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e);
   int rc = moe_tail_run(h, dx, dres, dout, rows, stream);
   if (rc) return rc;
-  e = cudaMemcpyAsync(residual_host, dres, bytes, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, dout, bytes, cudaMemcpyDeviceToHost, st);
+  if ((char*)out_host == (char*)residual_host + bytes) {
+    e = cudaMemcpyAsync(residual_host, dres, 2 * bytes, cudaMemcpyDeviceToHost, st);
+  } else {
+    e = cudaMemcpyAsync(residual_host, dres, bytes, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, dout, bytes, cudaMemcpyDeviceToHost, st);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
 }
