@@ -32,6 +32,13 @@ STATUS_BAD_TILE = 8
 MODE_MULTI_KERNEL = 0
 MODE_PERSISTENT = 1
 
+# debug_flags bits (moe_tail.h)
+DEBUG_SIMPLE_KERNELS = 1
+DEBUG_NO_PDL = 2
+DEBUG_STALL_FIRST_STAGE = 4
+DEBUG_FUSED_FRONT = 8
+DEBUG_TCGEN05 = 16
+
 # moe_attnres_mix launch flags (attnres_mix.h)
 ATTNRES_MIX_PDL = 1
 ATTNRES_MIX_DEBUG_STALL = 2

@@ -76,7 +76,8 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
               __nv_bfloat16* __restrict__ n_out, __half* __restrict__ n16,
               float* __restrict__ n16s, uint32_t* __restrict__ counters, int H, float eps,
               const __nv_bfloat16* __restrict__ wsg, float* __restrict__ sgate,
-              const float* __restrict__ xpart, int Pk, size_t part_stride) {
+              const float* __restrict__ xpart, int Pk, size_t part_stride,
+              uint8_t* __restrict__ np4, uint8_t* __restrict__ np4s) {
   extern __shared__ uint4 s_gamma[];  // [H / 8]
   __shared__ float part[kNormThreads / 32];
   const int r = blockIdx.x;
@@ -155,6 +156,43 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
       rno[c] = rn[q];
       no[c] = nv;
       n16o[c] = f16_group(nv, down);
+      if (np4) {
+        // the four E2M1 planes of n for the tensor-core experts: a 32-element block is the
+        // groups of four adjacent threads (H / 8 is a multiple of 32, so a warp is either
+        // wholly inside the row or wholly past it)
+        const uint32_t ww[4] = {nv.x, nv.y, nv.z, nv.w};
+        float rv[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          rv[2 * i] = bf16_lo(ww[i]);
+          rv[2 * i + 1] = bf16_hi(ww[i]);
+        }
+#pragma unroll
+        for (int pl = 0; pl < 4; ++pl) {
+          float am = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(rv[i]));
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+          const int e = e2m1_plane_exp(am);
+          const float inv = exp2_int(-e), sc = exp2_int(e);
+          float xs[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xs[i] = rv[i] * inv;
+          const uint32_t code = e2m1x8_pack(xs);
+          uint32_t h[4];
+          e2m1x8_to_f16x2(code, h[0], h[1], h[2], h[3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+            rv[2 * i] -= f.x * sc;
+            rv[2 * i + 1] -= f.y * sc;
+          }
+          const size_t prow = (size_t)(4 * r + pl);
+          reinterpret_cast<uint32_t*>(np4 + prow * (H / 2))[c] = code;
+          if ((c & 3) == 0) np4s[prow * (H / 32) + c / 4] = (uint8_t)(e + 127);
+        }
+      }
       if (wsg) {
         const uint4 w = __ldg(wg4 + c);
         const uint32_t nn[4] = {nv.x, nv.y, nv.z, nv.w}, ww[4] = {w.x, w.y, w.z, w.w};
@@ -172,10 +210,12 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
 
 cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
                                const __nv_bfloat16* residual, const Weights& w,
-                               const Scratch& s, cudaStream_t st, bool pdl, const float* xpart) {
+                               const Scratch& s, cudaStream_t st, bool pdl, const float* xpart,
+                               bool planes) {
   return launch_k(k_add_rmsnorm, dim3(d.R), dim3(kNormThreads), (size_t)d.H * 2, st, pdl, x,
                   residual, w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps, w.wsg,
-                  s.sgate, xpart, d.Pk, (size_t)d.Rmax * d.H);
+                  s.sgate, xpart, d.Pk, (size_t)d.Rmax * d.H, planes ? s.np4 : nullptr,
+                  planes ? s.np4s : nullptr);
 }
 
 // ------------------------------------------------------------------- router GEMV ----

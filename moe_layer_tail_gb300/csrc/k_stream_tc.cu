@@ -1,0 +1,757 @@
+// k_stream_tc.cu -- the weight-streaming expert kernels on the fifth-generation tensor cores:
+// each routed MXFP4 expert runs as tcgen05 block-scaled MMAs (kind::mxf4: E2M1 x E2M1 with
+// one E8M0 scale per 32 elements on both operands), the bf16 shared expert as tcgen05
+// kind::f16 MMAs; accumulators live in tensor memory.
+//
+// Work items, their order and the launch synchronisation are those of the CUDA-core form
+// (k_stream.cu): gate/up items of 64 gate + 64 up weight rows, down items of 128 weight
+// rows, each distinct routed expert streamed once per call, shared-expert items first;
+// down items wait (bounded) for the gate/up items of their expert, the combine for the down
+// items of its 128 outputs.
+//
+// Sources: "[AMD] integrate kimi k3 monokernel" page, Kernel Replacement rows "The routed
+// experts" and "The shared expert gate_up / SiLU and mul / down"; "glm53: Long-context
+// indexer ..." page, Modifications rows 16 (every using row a column of one multi-column
+// product per expert), 17, 18 and 21.
+//
+// Swap-AB: the weights are the MMA's A operand (M = 128 rows, K-major, exactly the
+// 128-byte-swizzled TMA boxes of the CUDA-core form); the activations are B (N columns).
+// The tensor core's block-scaled MXFP4 product needs E2M1 on both sides, so every bf16
+// activation row enters as four E2M1 planes with their own per-32 E8M0 scales: plane 0 is
+// the nearest E2M1 multiple of a power of two sized to the block maximum, each further plane
+// the same for what the planes before it left over.  Each plane gains about two bits; four
+// leave a remainder below ~1e-3 of the block maximum (the output error is far smaller, the
+// remainders being independent).  A row of activations is thus four B columns (plane-major
+// within the row), and the epilogue adds the four column sums in plane order.  The norm
+// launch writes the planes of n; the gate/up epilogue writes the planes of mid.
+//
+// Machine mapping (sm_103a), one CTA of 288 threads per SM.  A tcgen05.mma or tcgen05.cp
+// costs its issuing thread a fixed ~75 ns whatever N is (measured on GB300), while the
+// tensor core keeps up with several issuers at once; so two threads issue, each owning half
+// of every stage's K and an accumulator of its own, and nothing else runs on them:
+//   * warp 0, lane 0 -- the producer: per stage one or two TMA loads of a 128-row x 128-byte
+//     weight tile (L2 evict-first), one TMA load of the activation tile (planes, or bf16
+//     rows for the shared expert), and every 8 stages the E8M0 scales of the next 2048 K
+//     elements of weights and planes into a two-slot window ring;
+//   * warps 1, 2 (lane 0) -- the MMA issuers: issuer h copies scale-factor atom h of the
+//     stage's weights and activations into its own tensor-memory columns (tcgen05.cp) and
+//     issues the two MMAs of K steps 2h, 2h + 1 (K = 64 FP4 or 16 bf16 elements each; 32
+//     bytes of every operand row) into its accumulator, then commits the stage;
+//   * warps 3, 4 -- the scale warps: rearrange a stage's E8M0 bytes from the window into the
+//     atoms tcgen05.cp reads (32 rows x 16 bytes, row m of 128 at byte 16 (m mod 32) +
+//     4 (m / 32) + block), warp 3 for the weight rows, warp 4 for the activation planes;
+//   * warps 5..8 -- the epilogue: tcgen05.ld of both accumulators (TMEM lane = weight row)
+//     added in issuer order, plane sums, SiLU * up through a shared-memory exchange between
+//     the gate and up lane quadrants, planes of mid, stores, and the counts the next launch
+//     waits for;
+//   * tensor memory (512 columns): two accumulator slots x two issuers x N columns, and a
+//     ring of per-stage scale-factor slots (16 columns each); every wait is bounded, and a
+//     CTA that gives up lets its copies and MMAs finish before it frees its tensor memory.
+#include <cstring>
+
+#include "k_stream_common.cuh"
+
+namespace mtail {
+
+// warps: producer, two MMA issuers, two scale warps, four epilogue warps
+constexpr int kTcWarpMma = 1, kTcWarpScale = 3, kTcWarpEpi = 5;
+constexpr int kTcThreads = 9 * 32;
+constexpr int kTcSfBytes = 2048;    // per stage: A atoms 2 x 512 B, B atoms 2 x 512 B
+constexpr int kTcCols = 512;        // tensor-memory columns of a CTA
+constexpr int kTcSfCol = 256;       // first scale-factor column (accumulators below)
+constexpr uint32_t kNamedBarEpi = 1;
+
+// --------------------------------------------------------------------- PTX wrappers ----
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  // tcgen05 shared-memory matrix descriptor: start, leading and stride byte offsets (>> 4),
+  // descriptor version 1, layout type in bits 61..63 (2 = 128-byte swizzle, 0 = none)
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
+}
+// K-major operand rows of 128 bytes under the 128-byte swizzle (8-row atoms 1024 bytes apart)
+__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
+  return smem_desc(smem_u32(p), 16, 1024, 2);
+}
+// scale-factor atom: 32 rows x 16 bytes, contiguous (no swizzle; 8-row groups 128 bytes apart)
+__device__ __forceinline__ uint64_t sf_desc(const void* p) { return smem_desc(smem_u32(p), 128, 128, 0); }
+
+// Instruction descriptors.  kind::mxf4: E2M1 operands (format 1), K-major, N >> 3 at bit 17,
+// UE8M0 scales (bit 23), M >> 4 at bit 24; the scale-factor byte of A at bits 29..30 and of B
+// at bits 4..5.  kind::f16: fp32 accumulator (bit 4), bf16 operands (format 1).
+__device__ __forceinline__ uint32_t idesc_mxf4(int N, uint32_t sf_id) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | (8u << 24) |
+         (sf_id << 29) | (sf_id << 4);
+}
+__device__ __forceinline__ uint32_t idesc_bf16(int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (8u << 24);
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc));
+}
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], "
+      "[%6], p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+__device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+// arrive on `bar` once every tcgen05 operation this thread issued so far has completed
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void bar_epi() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kNamedBarEpi), "n"(128) : "memory");
+}
+
+// 32 lanes x 16/32/64 consecutive fp32 columns of the accumulator (lane = TMEM lane).
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]);
+
+#define MT_R4(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3])
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : MT_R4(0), MT_R4(4), MT_R4(8), MT_R4(12)
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : MT_R4(0), MT_R4(4), MT_R4(8), MT_R4(12), MT_R4(16), MT_R4(20), MT_R4(24), MT_R4(28)
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<64>(uint32_t taddr, float (&v)[64]) {
+  float a[32], b[32];
+  tmem_ld<32>(taddr, a);
+  tmem_ld<32>(taddr + 32, b);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = a[i];
+    v[32 + i] = b[i];
+  }
+}
+#undef MT_R4
+
+// ----------------------------------------------------------- E2M1 activation planes ----
+// (the norm launch makes the planes of n with the same two helpers, see k_front.cu)
+
+// --------------------------------------------------------------- shared-memory plan ----
+
+struct TcPtrs {
+  uint8_t* stages;
+  uint8_t* win;      // [2][win_bytes]: A scales [128][spitch] then B scales [nmax][spitch]
+  float* xch;        // [2][2][64][Rmax]: gate and up sums of a gate/up item, two buffers
+  int* t_uniq;
+  int* t_off;
+  int* t_users;
+  uint64_t* full;    // [stages] producer -> scale warps (transaction bytes)
+  uint64_t* ready;   // [stages] scale warps (2 arrivals) -> MMA issuers: atoms written
+  uint64_t* empty;   // [stages] MMA commits (2) -> producer
+  uint64_t* wempty;  // [2] scale warps (2) -> producer: scale window slot free
+  uint64_t* afull;   // [2] MMA commits (2) + item id (1) -> epilogue: accumulators ready
+  uint64_t* aempty;  // [2] epilogue (4 warps) -> MMA issuers: accumulators read
+  uint64_t* drain;   // [2] an issuer's own commit, only when its CTA gives up
+  int2* info;        // [stages] item of each stage
+  int* aitem;        // [2] item of each accumulator slot
+  uint32_t* tbase;   // tensor-memory base address of the CTA
+};
+
+__device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L) {
+  TcPtrs p;
+  p.stages = smem;
+  p.win = smem + L.off_win;
+  p.xch = reinterpret_cast<float*>(smem + L.off_x);
+  p.t_uniq = reinterpret_cast<int*>(smem + L.off_tab);
+  p.t_off = p.t_uniq + kMaxPicks;
+  p.t_users = p.t_off + kMaxPicks + 1;
+  p.full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
+  p.ready = p.full + kMaxStreamStages;
+  p.empty = p.ready + kMaxStreamStages;
+  p.wempty = p.empty + kMaxStreamStages;
+  p.afull = p.wempty + 2;
+  p.aempty = p.afull + 2;
+  p.drain = p.aempty + 2;
+  p.info = reinterpret_cast<int2*>(p.drain + 2);
+  p.aitem = reinterpret_cast<int*>(p.info + kMaxStreamStages);
+  p.tbase = reinterpret_cast<uint32_t*>(p.aitem + 2);
+  return p;
+}
+
+// ----------------------------------------------------------------------- epilogue ----
+
+// Sum of the four plane columns of activation column group c (plane order).
+template <int N>
+__device__ __forceinline__ float plane_sum(const float (&v)[N], int c) {
+  return ((v[4 * c] + v[4 * c + 1]) + v[4 * c + 2]) + v[4 * c + 3];
+}
+
+// The four E2M1 planes of one 32-element block of mid held one element per lane (lane =
+// element), stored as plane rows of the down launch's activations: 16 code bytes at
+// `codes + p * code_pitch` and one scale byte at `scales + p * scale_pitch`.
+__device__ __forceinline__ void store_planes_lane(float v, int lane, uint8_t* codes,
+                                                  size_t code_pitch, uint8_t* scales,
+                                                  size_t scale_pitch) {
+  float r = v;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    float am = fabsf(r);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const int e = e2m1_plane_exp(am);
+    const uint32_t code = e2m1_code(r * exp2_int(-e));
+    r -= e2m1_value(code) * exp2_int(e);
+    // eight codes per 32-bit word, element 2j in the low nibble of byte j
+    uint32_t w = code << (4 * (lane & 7));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    w |= __shfl_xor_sync(0xffffffffu, w, 4);
+    if ((lane & 7) == 0)
+      *reinterpret_cast<uint32_t*>(codes + p * code_pitch + (lane >> 1)) = w;
+    if (lane == 0) scales[p * scale_pitch] = (uint8_t)(e + 127);
+  }
+}
+
+// One finished item: its accumulator (N plane columns per TMEM lane) to outputs.
+// The sums of an item's columns: issuer 0's accumulator plus issuer 1's, in that order, when
+// issuer 1 took part (issuer 1 owns the second 128 K elements of every stage).
+template <int N>
+__device__ __forceinline__ void acc_ld(uint32_t acc0, uint32_t acc1, bool two, float (&v)[N]) {
+  tmem_ld<N>(acc0, v);
+  if (two) {
+    float w[N];
+    tmem_ld<N>(acc1, w);
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] += w[i];
+  }
+}
+
+template <int NMAX>
+__device__ __forceinline__ void tc_finish(const Item& it, uint32_t acc0, uint32_t acc1, float* xch,
+                                          int ew, int q, int lane, const Dims& dm,
+                                          const Tables& tb, const Scratch& s) {
+  // bf16 items have whole 64-element stages; an MXFP4 item's first stage reaches past 128
+  // elements unless K is 128
+  const bool two = (it.kind == kSharedGU || it.kind == kSharedDN) || it.K > 128;
+  const int m = 32 * q + lane;  // weight row of this thread within the item's 128
+  if (it.kind == kRoutedGU || it.kind == kSharedGU) {
+    const int R = dm.Rmax;
+    float* xg = xch;            // [64][R] gate sums
+    float* xu = xch + 64 * R;   // [64][R] up sums
+    float* dst = (m < 64) ? xg + m * R : xu + (m - 64) * R;
+    if (it.kind == kRoutedGU) {
+      float v[NMAX];
+      acc_ld<NMAX>(acc0, acc1, two, v);
+#pragma unroll
+      for (int c = 0; c < NMAX / 4; ++c)
+        if (c < R) dst[c] = plane_sum<NMAX>(v, c);
+    } else {
+      float v[16];
+      acc_ld<16>(acc0, acc1, two, v);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < R) dst[c] = v[c];
+    }
+    bar_epi();
+    if (it.kind == kRoutedGU) {
+      // (user, 32-column block) tasks, one per warp at a time; lane = column in the block
+      for (int t = ew; t < 2 * it.U; t += 4) {
+        const int u = t >> 1, blk = t & 1;
+        const int slot = it.u0 + u;
+        const int r = tb.users[slot] / dm.k;
+        const int j = 32 * blk + lane;
+        const float g = xg[j * R + r], up = xu[j * R + r];
+        const float mv = __bfloat162float(__float2bfloat16_rn(silu_f(g) * up));
+        const size_t cp = (size_t)dm.I / 2, spp = (size_t)dm.I / 32;
+        store_planes_lane(mv, lane, s.mid4 + (size_t)(4 * slot) * cp + (it.out0 + 32 * blk) / 2,
+                          cp, s.mid4s + (size_t)(4 * slot) * spp + (it.out0 + 32 * blk) / 32,
+                          spp);
+      }
+    } else {
+      for (int e = 32 * ew + lane; e < 64 * dm.R; e += 128) {
+        const int j = e & 63, r = e >> 6;
+        s.ms[(size_t)r * dm.Is + it.out0 + j] =
+            __float2bfloat16_rn(silu_f(xg[j * R + r]) * xu[j * R + r]);
+      }
+    }
+  } else if (it.kind == kRoutedDN) {
+    float v[NMAX];
+    acc_ld<NMAX>(acc0, acc1, two, v);
+#pragma unroll
+    for (int u = 0; u < NMAX / 4; ++u)
+      if (u < it.U)
+        s.y[(size_t)tb.users[it.u0 + u] * dm.H + it.out0 + m] = plane_sum<NMAX>(v, u);
+  } else {  // shared down
+    float v[16];
+    acc_ld<16>(acc0, acc1, two, v);
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      if (r < dm.R) s.ys[(size_t)r * dm.H + it.out0 + m] = v[r];
+  }
+}
+
+// ------------------------------------------------------------------------ kernel ----
+
+template <int PHASE, int NMAX>
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
+            uint64_t budget_ns, uint32_t debug) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const TcLayout& lay = maps.lay;
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) set_status(s.status, kStatusBadTile);
+    return;
+  }
+  const TcPtrs sp = tc_carve(smem, lay);
+  const int S = lay.stages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (PHASE == 0) pdl_wait();
+  const int D = min(max(*s.n_distinct, 1), kMaxPicks);
+  const int n_items = items_of(PHASE, dm, D);
+  for (int i = threadIdx.x; i < D; i += kTcThreads) sp.t_uniq[i] = s.uniq[i];
+  for (int i = threadIdx.x; i <= D; i += kTcThreads) sp.t_off[i] = s.user_off[i];
+  for (int i = threadIdx.x; i < dm.R * dm.k; i += kTcThreads) sp.t_users[i] = s.user_list[i];
+  Tables tb;
+  tb.uniq = sp.t_uniq;
+  tb.off = sp.t_off;
+  tb.users = sp.t_users;
+  tb.rscale = nullptr;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&sp.full[i], 1);
+      mbar_init(&sp.ready[i], 2);
+      mbar_init(&sp.empty[i], 2);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sp.wempty[i], 2);
+      mbar_init(&sp.afull[i], 3);
+      mbar_init(&sp.aempty[i], 4);
+      mbar_init(&sp.drain[i], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    pdl_trigger();  // the next launch may queue for SMs from now on (it waits on counts)
+  }
+  if (warp == kTcWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(sp.tbase)),
+                 "n"(kTcCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *sp.tbase;
+
+  const int Kr = (PHASE == 0) ? dm.H : dm.I;  // K of the routed contraction
+  const int spitch = (Kr > kWinK) ? 64 : Kr / 32;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer ----
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0, wcnt = 0;
+      uint32_t pend = 0u, pend_par = 0u;
+      bool skip_first = PHASE == 0 && (debug & kDebugStallFirstStage) && blockIdx.x == 0;
+      int item = (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
+      while (ok && item < n_items) {
+        const int next = (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
+        const Item it = decode_item(PHASE, item, dm, tb, D);
+        const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
+        const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;
+        const int nb = (it.kind == kRoutedGU) ? NMAX : (it.kind == kRoutedDN) ? (16 << hsel) : 0;
+        if (PHASE == 1) {
+          const bool sh = (it.kind == kSharedDN);
+          if (!wait_count(&s.counters[sh ? kCtrSharedGUDone : kCtrGUDone + it.d],
+                          (uint32_t)(sh ? dm.Is / 64 : dm.I / 64), budget_ns)) {
+            ok = false;
+            break;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        const uint32_t b_bytes = routed ? (uint32_t)nb * 128u : (uint32_t)dm.Rmax * 128u;
+        for (int kc = 0; kc < it.nst; ++kc) {
+          if (!mbar_wait(&sp.empty[stage], phase ^ 1, budget_ns)) { ok = false; break; }
+          pend &= ~(1u << stage);
+          if (skip_first) {
+            skip_first = false;
+            if (++stage == S) { stage = 0; phase ^= 1; }
+            continue;
+          }
+          uint8_t* st = sp.stages + stage * lay.stage_bytes;
+          uint8_t* sb = st + kStageW;
+          uint32_t bytes = kStageW + b_bytes;
+          const bool wstart = routed && (kc % kWinStages) == 0;
+          uint8_t* ws = sp.win + (wcnt & 1u) * lay.win_bytes;
+          if (wstart) {
+            if (!mbar_wait(&sp.wempty[wcnt & 1u], ((wcnt >> 1) & 1u) ^ 1u, budget_ns)) {
+              ok = false;
+              break;
+            }
+            const uint32_t rowb = (Kr > kWinK) ? 64u : (uint32_t)Kr / 32u;
+            bytes += 128u * rowb + (uint32_t)nb * rowb;
+          }
+          pend |= 1u << stage;
+          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+          sp.info[stage] = make_int2(item, 0);
+          mbar_expect_tx(&sp.full[stage], bytes);
+          if (it.kind == kRoutedGU) {
+            const int x = kc * (kChunkF4 / 2);
+            tma_load_2d(st, &maps.w13, x, it.row0, &sp.full[stage], pol);
+            tma_load_2d(st + 8192, &maps.w13, x, it.row1, &sp.full[stage], pol);
+            tma_load_2d(sb, &maps.np4, x, 0, &sp.full[stage]);
+          } else if (it.kind == kRoutedDN) {
+            const int x = kc * (kChunkF4 / 2);
+            tma_load_2d(st, &maps.w2, x, it.row0, &sp.full[stage], pol);
+            tma_load_2d(sb, &maps.mid4[hsel], x, 4 * it.u0, &sp.full[stage]);
+          } else if (it.kind == kSharedGU) {
+            tma_load_2d(st, &maps.ws13, kc * kChunkBF, it.row0, &sp.full[stage], pol);
+            tma_load_2d(st + 8192, &maps.ws13, kc * kChunkBF, it.row1, &sp.full[stage], pol);
+            tma_load_2d(sb, &maps.n, kc * kChunkBF, 0, &sp.full[stage]);
+          } else {
+            tma_load_2d(st, &maps.ws2, kc * kChunkBF, it.row0, &sp.full[stage], pol);
+            tma_load_2d(sb, &maps.ms, kc * kChunkBF, 0, &sp.full[stage]);
+          }
+          if (wstart) {
+            const int win = kc / kWinStages;
+            uint8_t* wb = ws + kWinW;  // B scales follow the 128 rows of A scales
+            if (PHASE == 0) {
+              if (Kr > kWinK) {
+                tma_load_2d(ws, &maps.w13s, win * 64, it.row0, &sp.full[stage]);
+                tma_load_2d(ws + 4096, &maps.w13s, win * 64, it.row1, &sp.full[stage]);
+                tma_load_2d(wb, &maps.np4s, win * 64, 0, &sp.full[stage]);
+              } else {
+                const size_t rb = (size_t)(Kr / 32);
+                bulk_load(ws, w.w13s + (size_t)it.row0 * rb, 2u * (uint32_t)Kr, &sp.full[stage]);
+                bulk_load(ws + 4096, w.w13s + (size_t)it.row1 * rb, 2u * (uint32_t)Kr,
+                          &sp.full[stage]);
+                bulk_load(wb, s.np4s, (uint32_t)nb * (uint32_t)rb, &sp.full[stage]);
+              }
+            } else {
+              if (Kr > kWinK) {
+                tma_load_2d(ws, &maps.w2s, win * 64, it.row0, &sp.full[stage]);
+                tma_load_2d(wb, &maps.mid4s[hsel], win * 64, 4 * it.u0, &sp.full[stage]);
+              } else {
+                const size_t rb = (size_t)(Kr / 32);
+                bulk_load(ws, w.w2s + (size_t)it.row0 * rb, 4u * (uint32_t)Kr, &sp.full[stage]);
+                bulk_load(wb, s.mid4s + (size_t)(4 * it.u0) * rb, (uint32_t)nb * (uint32_t)rb,
+                          &sp.full[stage]);
+              }
+            }
+            ++wcnt;
+          }
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+        item = next;
+      }
+      if (ok) {
+        ok = mbar_wait(&sp.empty[stage], phase ^ 1, budget_ns);
+        if (ok && !skip_first) {
+          sp.info[stage] = make_int2(-1, 0);
+          mbar_arrive(&sp.full[stage]);
+        }
+      }
+      if (!ok) {
+        set_status(s.status, kStatusTimeout);
+        for (int st2 = 0; st2 < S; ++st2)
+          if (pend & (1u << st2)) mbar_wait(&sp.full[st2], (pend_par >> st2) & 1u, budget_ns);
+      }
+    }
+  } else if (warp >= kTcWarpScale && warp < kTcWarpEpi) {
+    // ------------------------------------------------------------ scale warps ----
+    // warp 0 of the pair: the 128 weight rows' E8M0 bytes of a stage into the two A atoms;
+    // warp 1: the activation planes' bytes into the two B atoms
+    const bool arows = (warp == kTcWarpScale);
+    int stage = 0;
+    uint32_t phase = 0, wcnt = 0;
+    int kc = 0;
+    Item it;
+    it.nst = 0;
+    for (;;) {
+      if (!mbar_wait(&sp.full[stage], phase, budget_ns)) { ok = false; break; }
+      const int item = sp.info[stage].x;
+      if (kc == 0 && item >= 0) it = decode_item(PHASE, item, dm, tb, D);
+      if (item >= 0 && (it.kind == kRoutedGU || it.kind == kRoutedDN)) {
+        const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;
+        const int nb = (it.kind == kRoutedGU) ? NMAX : (16 << hsel);
+        const uint8_t* ws = sp.win + (wcnt & 1u) * lay.win_bytes;
+        uint8_t* atoms = sp.stages + stage * lay.stage_bytes + kStageW + lay.b_bytes;
+        const int boff = 8 * (kc % kWinStages);
+        const bool two = boff + 4 < spitch;  // blocks 4..7 lie inside the window row
+        if (arows) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int mr = lane + 32 * i;
+            const uint8_t* row = (PHASE == 0 && mr >= 64) ? ws + 4096 + (mr - 64) * spitch
+                                                          : ws + mr * spitch;
+            const uint32_t lo = *reinterpret_cast<const uint32_t*>(row + boff);
+            const uint32_t hi = two ? *reinterpret_cast<const uint32_t*>(row + boff + 4) : 0u;
+            *reinterpret_cast<uint32_t*>(atoms + 16 * lane + 4 * i) = lo;
+            *reinterpret_cast<uint32_t*>(atoms + 512 + 16 * lane + 4 * i) = hi;
+          }
+        } else {
+          const uint8_t* wb = ws + kWinW;
+#pragma unroll
+          for (int i = 0; i < (NMAX + 31) / 32; ++i) {
+            const int n = lane + 32 * i;
+            if (n < nb) {
+              const uint8_t* row = wb + n * spitch;
+              const uint32_t lo = *reinterpret_cast<const uint32_t*>(row + boff);
+              const uint32_t hi = two ? *reinterpret_cast<const uint32_t*>(row + boff + 4) : 0u;
+              *reinterpret_cast<uint32_t*>(atoms + 1024 + 16 * (n & 31) + 4 * (n >> 5)) = lo;
+              *reinterpret_cast<uint32_t*>(atoms + 1536 + 16 * (n & 31) + 4 * (n >> 5)) = hi;
+            }
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sp.ready[stage]);
+        if ((kc % kWinStages) == kWinStages - 1 || kc == it.nst - 1) {
+          if (lane == 0) mbar_arrive(&sp.wempty[wcnt & 1u]);
+          ++wcnt;
+        }
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sp.ready[stage]);  // bf16 stage, or the end marker
+      }
+      if (item < 0) break;
+      if (++stage == S) { stage = 0; phase ^= 1; }
+      if (++kc == it.nst) kc = 0;
+    }
+    if (!ok && lane == 0) set_status(s.status, kStatusTimeout);
+  } else if (warp >= kTcWarpMma && warp < kTcWarpScale) {
+    // ------------------------------------------------------------ MMA issuers ----
+    // issuer h owns K steps 2h and 2h + 1 of every stage (the second half of its 256 MXFP4
+    // or 64 bf16 elements for h = 1): its scale atoms, its MMAs, its own accumulator
+    const int h = warp - kTcWarpMma;
+    int stage = 0;
+    uint32_t phase = 0, acnt = 0;
+    int kc = 0;
+    Item it;
+    it.nst = 0;
+    for (;;) {
+      if (!mbar_wait(&sp.ready[stage], phase, budget_ns)) { ok = false; break; }
+      const int item = sp.info[stage].x;
+      if (item < 0) break;
+      if (kc == 0) {
+        it = decode_item(PHASE, item, dm, tb, D);
+        if (!mbar_wait(&sp.aempty[acnt & 1u], ((acnt >> 1) & 1u) ^ 1u, budget_ns)) {
+          ok = false;
+          break;
+        }
+      }
+      tc_fence_after();
+      const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
+      if (lane == 0) {
+        const uint8_t* st = sp.stages + stage * lay.stage_bytes;
+        const uint8_t* sb = st + kStageW;
+        const uint32_t acc = tbase + (2u * (acnt & 1u) + (uint32_t)h) * (uint32_t)NMAX;
+        if (routed) {
+          const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;
+          const int nb = (it.kind == kRoutedGU) ? NMAX : (16 << hsel);
+          const uint8_t* atoms = st + kStageW + lay.b_bytes;
+          const uint32_t sf = tbase + kTcSfCol + 16u * (uint32_t)stage + 8u * (uint32_t)h;
+          tc_cp_sf(sf, sf_desc(atoms + 512 * h));          // A atom h: blocks 4h..4h+3
+          tc_cp_sf(sf + 4, sf_desc(atoms + 1024 + 512 * h));  // B atom h
+          const int nk = min(4, (it.K - kc * kChunkF4 + 63) / 64);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int kk = 2 * h + j;
+            if (kk < nk)
+              tc_mma_mxf4(acc, sw128_desc(st + 32 * kk), sw128_desc(sb + 32 * kk),
+                          idesc_mxf4(nb, 2u * (uint32_t)j), sf, sf + 4,
+                          (kc > 0 || j > 0) ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int kk = 2 * h + j;
+            tc_mma_f16(acc, sw128_desc(st + 32 * kk), sw128_desc(sb + 32 * kk), idesc_bf16(16),
+                       (kc > 0 || j > 0) ? 1u : 0u);
+          }
+        }
+        tc_commit(&sp.empty[stage]);
+      }
+      __syncwarp();
+      if (++stage == S) { stage = 0; phase ^= 1; }
+      if (++kc == it.nst) {
+        // this issuer's accumulator is final once its MMAs complete; issuer 0 also
+        // publishes the item id (three arrivals in all)
+        if (lane == 0) {
+          if (h == 0) sp.aitem[acnt & 1u] = item;
+          tc_commit(&sp.afull[acnt & 1u]);
+          if (h == 0) mbar_arrive(&sp.afull[acnt & 1u]);
+        }
+        __syncwarp();
+        ++acnt;
+        kc = 0;
+      }
+    }
+    if (ok && h == 0) {
+      // end of work: an end marker in the next accumulator slot
+      if (mbar_wait(&sp.aempty[acnt & 1u], ((acnt >> 1) & 1u) ^ 1u, budget_ns)) {
+        if (lane == 0) {
+          sp.aitem[acnt & 1u] = -1;
+          mbar_arrive_n(&sp.afull[acnt & 1u], 3);
+        }
+      } else {
+        ok = false;
+      }
+    }
+    if (!ok) {
+      // let every MMA and copy this thread issued finish before the memory is released
+      if (lane == 0) {
+        set_status(s.status, kStatusTimeout);
+        tc_commit(&sp.drain[h]);
+        mbar_wait(&sp.drain[h], 0, budget_ns);
+      }
+      __syncwarp();
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue ----
+    const int q = warp & 3, ew = warp - kTcWarpEpi;
+    for (uint32_t ac = 0;; ++ac) {
+      const uint32_t as = ac & 1u;
+      if (!mbar_wait(&sp.afull[as], (ac >> 1) & 1u, budget_ns)) {
+        if (lane == 0) set_status(s.status, kStatusTimeout);
+        break;
+      }
+      tc_fence_after();
+      const int item = sp.aitem[as];
+      if (item < 0) break;
+      const Item it = decode_item(PHASE, item, dm, tb, D);
+      const uint32_t lq = (uint32_t)(32 * q) << 16;
+      const uint32_t acc0 = tbase + (2u * as) * (uint32_t)NMAX + lq;
+      const uint32_t acc1 = tbase + (2u * as + 1u) * (uint32_t)NMAX + lq;
+      float* xch = sp.xch + (size_t)(ac & 1u) * (2 * 64 * dm.Rmax);
+      tc_finish<NMAX>(it, acc0, acc1, xch, ew, q, lane, dm, tb, s);
+      // every epilogue thread's stores before the count the next launch waits for
+      __threadfence();
+      tc_fence_before();
+      bar_epi();
+      if (ew == 0 && lane == 0) {
+        uint32_t* c = &s.counters[PHASE == 1 ? kCtrTileDone + it.out0 / 128
+                                  : it.kind == kSharedGU ? kCtrSharedGUDone
+                                                         : kCtrGUDone + it.d];
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sp.aempty[as]);
+    }
+  }
+
+  // every role ends here: tensor memory is freed once all of them are done with it
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcWarpMma) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
+                 "n"(kTcCols));
+  }
+}
+
+// -------------------------------------------------------------------- host side ----
+
+template <int PHASE, int NMAX>
+static cudaError_t tc_prepare_one() {
+  return cudaFuncSetAttribute(k_stream_tc<PHASE, NMAX>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+}
+
+cudaError_t prepare_stream_tc_kernels() {
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = tc_prepare_one<0, 16>();
+  if (e == cudaSuccess) e = tc_prepare_one<0, 32>();
+  if (e == cudaSuccess) e = tc_prepare_one<0, 64>();
+  if (e == cudaSuccess) e = tc_prepare_one<1, 16>();
+  if (e == cudaSuccess) e = tc_prepare_one<1, 32>();
+  if (e == cudaSuccess) e = tc_prepare_one<1, 64>();
+  return e;
+}
+
+template <int PHASE, int NMAX>
+static cudaError_t tc_launch(const TcMaps& maps, const Dims& d, const Weights& w,
+                             const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
+                             bool pdl, uint32_t debug) {
+  return launch_k(k_stream_tc<PHASE, NMAX>, dim3(num_sms), dim3(kTcThreads),
+                  (size_t)maps.lay.smem_bytes, st, pdl, maps, d, w, s, budget_ns, debug);
+}
+
+cudaError_t launch_stream_tc(int phase, const TcMaps& maps, const Dims& d, const Weights& w,
+                             const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
+                             bool pdl, uint32_t debug) {
+  const int nmax = maps.lay.nmax;
+  if (phase == 0) {
+    if (nmax == 16) return tc_launch<0, 16>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+    if (nmax == 32) return tc_launch<0, 32>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+    return tc_launch<0, 64>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+  }
+  if (nmax == 16) return tc_launch<1, 16>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+  if (nmax == 32) return tc_launch<1, 32>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+  return tc_launch<1, 64>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+}
+
+// Shared-memory plan: stages of 16 KB weights + nmax x 128 B activations + 2 KB scale atoms,
+// as many as fit (up to 8, the tensor-memory scale ring), a two-slot scale window ring, the
+// epilogue exchange, the dedup tables and the barriers.
+TcLayout make_tc_layout(int Rmax) {
+  TcLayout L;
+  L.nmax = (Rmax <= 4) ? 16 : (Rmax <= 8) ? 32 : 64;
+  L.b_bytes = L.nmax * 128;
+  L.stage_bytes = kStageW + L.b_bytes + kTcSfBytes;
+  L.win_bytes = kWinW + L.nmax * 64;
+  const int x_bytes = 2 * 2 * 64 * Rmax * 4;
+  const int tab_bytes = ((3 * kMaxPicks + 1) * 4 + 127) & ~127;
+  const int bar_bytes = (3 * kMaxStreamStages + 8) * 8 + kMaxStreamStages * 8 + 2 * 4 + 4;
+  const int fixed = 2 * L.win_bytes + x_bytes + tab_bytes + ((bar_bytes + 127) & ~127);
+  L.stages = (kSmemLimit - fixed) / L.stage_bytes;
+  if (L.stages > kMaxStreamStages) L.stages = kMaxStreamStages;
+  L.off_win = L.stages * L.stage_bytes;
+  L.off_x = L.off_win + 2 * L.win_bytes;
+  L.off_tab = L.off_x + x_bytes;
+  L.off_bar = L.off_tab + tab_bytes;
+  L.smem_bytes = L.off_bar + ((bar_bytes + 127) & ~127);
+  return L;
+}
+
+}  // namespace mtail

@@ -30,6 +30,7 @@ struct moe_tail {
   moe_tail_config_t cfg;
   Weights w;
   StreamMaps maps;     // TMA descriptors of the streamed weights
+  TcMaps tcmaps;       // and of the tensor-core form (MOE_TAIL_DEBUG_TCGEN05)
   Scratch s;
   void* slab;          // one device allocation holding every scratch buffer
   size_t slab_bytes;
@@ -70,6 +71,7 @@ extern "C" const char* moe_tail_last_cuda_error(void) { return g_cuda_err; }
 
 static_assert(MOE_TAIL_DEBUG_STALL_FIRST_STAGE == (int)kDebugStallFirstStage,
               "debug bit values agree");
+static_assert(MOE_TAIL_DEBUG_TCGEN05 == (int)kDebugTcgen05, "debug bit values agree");
 
 static int check_config(const moe_tail_config_t* c) {
   if (c->max_rows < 1 || c->max_rows > kMaxRows) return MOE_TAIL_ERR_UNSUPPORTED;
@@ -94,6 +96,11 @@ static int check_config(const moe_tail_config_t* c) {
     return MOE_TAIL_ERR_UNSUPPORTED;
   // the persistent launch covers the tail from x on (no out_proj stage in front of it)
   if (c->mode == MOE_TAIL_MODE_PERSISTENT && c->attn_dim != 0) return MOE_TAIL_ERR_UNSUPPORTED;
+  // the tensor-core experts take their activation planes from the two-launch front, and
+  // replace the TMA-streaming CUDA-core kernels (not the cross-checking ones)
+  if ((c->debug_flags & MOE_TAIL_DEBUG_TCGEN05) &&
+      (c->debug_flags & (MOE_TAIL_DEBUG_FUSED_FRONT | MOE_TAIL_DEBUG_SIMPLE_KERNELS)))
+    return MOE_TAIL_ERR_UNSUPPORTED;
   return MOE_TAIL_OK;
 }
 
@@ -136,6 +143,10 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s, size_t* 
   s->sgate = (float*)take(R * 4);
   s->xproj = (__nv_bfloat16*)take(R * H * 2);
   s->xpart = (float*)take((size_t)kMaxOutProjParts * R * H * 4);
+  s->np4 = (uint8_t*)take(4 * R * H / 2);
+  s->np4s = (uint8_t*)take(64 * H / 32);
+  s->mid4 = (uint8_t*)take(4 * P * I / 2);
+  s->mid4s = (uint8_t*)take((4 * P + 64) * I / 32);
   s->status = (int32_t*)take(4);
   s->counters = (uint32_t*)take(kCtrWords * 4);
   if (n_canary) *n_canary = nc < kMaxCanaries ? nc : kMaxCanaries;
@@ -179,6 +190,8 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = prepare_stream_kernels();
   if (e == cudaSuccess) e = prepare_front_kernels();
+  if (e == cudaSuccess && (cfg->debug_flags & MOE_TAIL_DEBUG_TCGEN05))
+    e = prepare_stream_tc_kernels();
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess && cfg->mode == MOE_TAIL_MODE_PERSISTENT) {
     // one CTA per SM at most; the cooperative launch checks at run time that all fit
@@ -210,7 +223,9 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
     d0.k = cfg->top_k; d0.I = cfg->expert_inter; d0.Is = cfg->shared_inter; d0.eps = cfg->rms_eps;
     d0.Ha = cfg->attn_dim;
     d0.Pk = 1;
-    const int mrc = make_stream_maps(&h->maps, d0, h->w, h->s);
+    int mrc = make_stream_maps(&h->maps, d0, h->w, h->s);
+    if (mrc == 0 && (cfg->debug_flags & MOE_TAIL_DEBUG_TCGEN05))
+      mrc = make_tc_maps(&h->tcmaps, h->maps, d0, h->w, h->s);
     if (mrc != 0) {
       cudaFree(h->slab);
       cudaFree(h->stage);
@@ -277,6 +292,7 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   } while (0)
   const bool pdl = !(h->cfg.debug_flags & MOE_TAIL_DEBUG_NO_PDL);
   const bool simple = (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) != 0;
+  const bool tc = (h->cfg.debug_flags & MOE_TAIL_DEBUG_TCGEN05) != 0;
   const uint64_t budget_ns =
       (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
   const float* xpart = nullptr;
@@ -327,12 +343,17 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
                                   h->w, h->s, st, pdl));
     } else {
       MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
-                                  h->w, h->s, st, pdl, xpart));
+                                  h->w, h->s, st, pdl, xpart, tc));
       MT_STAGE(launch_router_topk(d, h->w, h->s, st, pdl));
     }
     const uint32_t dbg = h->cfg.debug_flags;
-    MT_STAGE(launch_stream(0, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
-    MT_STAGE(launch_stream(1, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
+    if (tc) {
+      MT_STAGE(launch_stream_tc(0, h->tcmaps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
+      MT_STAGE(launch_stream_tc(1, h->tcmaps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
+    } else {
+      MT_STAGE(launch_stream(0, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
+      MT_STAGE(launch_stream(1, h->maps, d, h->w, h->s, h->num_sms, budget_ns, st, pdl, dbg));
+    }
   }
   // after the streaming kernels the combine waits per 128 outputs for the down items that
   // write them; after the cross-checking kernels it waits for the previous launch

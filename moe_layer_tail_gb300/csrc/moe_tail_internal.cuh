@@ -75,12 +75,18 @@ struct Scratch {
   float* sgate;          // [Rmax] sigmoid gate of the shared output (when a gate is given)
   __nv_bfloat16* xproj;  // [Rmax, H] x = out_proj(attn) for moe_tail_run_attn (one K part)
   float* xpart;          // [kMaxOutProjParts, Rmax, H] fp32 sums of each out_proj K part
+  uint8_t* np4;          // [4 Rmax, H/2] E2M1 planes of n (row 4r + p = plane p of row r)
+  uint8_t* np4s;         // [64, H/32] their E8M0 scales (rows past 4 Rmax stay zero)
+  uint8_t* mid4;         // [4 Rmax k, I/2] E2M1 planes of mid (row 4 slot + p, slot = the
+                         // pick's position in user_list)
+  uint8_t* mid4s;        // [4 Rmax k + 64, I/32] their E8M0 scales (64 zero rows after)
   int32_t* status;       // [1] sticky device status word
   uint32_t* counters;    // [kCtrWords] work counters, tickets and per-expert progress
 };
 
 // Debug bits the kernels read (same values as MOE_TAIL_DEBUG_* in moe_tail.h).
 constexpr uint32_t kDebugStallFirstStage = 4u;
+constexpr uint32_t kDebugTcgen05 = 16u;
 
 // counters[] words (all zeroed at the start of every call by the front)
 enum : int {
@@ -153,6 +159,58 @@ __device__ __forceinline__ float warp_max(float v) {
 // right after).
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// 2^e as a float, exact for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float exp2_int(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// E2M1 activation planes (the tensor-core form of the routed experts).  A block of 32 values
+// becomes the sum of four planes, each an E2M1 code per value times one power of two 2^e per
+// plane: e is the smallest exponent with amax <= 6 * 2^e for the block's largest magnitude
+// amax of what the planes before it left over (-127 when that is zero), the codes are the
+// nearest E2M1 values (ties to even) of value / 2^e.
+__device__ __forceinline__ int e2m1_plane_exp(float amax) {
+  if (!(amax > 0.f)) return -127;
+  const uint32_t b = __float_as_uint(amax);
+  const int E = (int)((b >> 23) & 0xFF) - 127;
+  if (E < -126) return -127;  // subnormal: amax / 2^-127 < 2
+  const int e = E - 2 + ((b & 0x7FFFFFu) > 0x400000u ? 1 : 0);
+  return e > 127 ? 127 : e;
+}
+
+// Nearest E2M1 code of x (ties to even, saturating at 6), in the low nibble.
+__device__ __forceinline__ uint32_t e2m1_code(float x) {
+  uint32_t w;
+  asm("{ .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n mov.b32 %0, {t, t, t, t}; }"
+      : "=r"(w)
+      : "f"(0.f), "f"(x));
+  return w & 0xFu;
+}
+
+// Eight values -> eight E2M1 codes in one word (value 2j in the low nibble of byte j).
+__device__ __forceinline__ uint32_t e2m1x8_pack(const float (&x)[8]) {
+  uint32_t w;
+  asm("{ .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3}; }"
+      : "=r"(w)
+      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
+  return w;
+}
+
+// Value of the E2M1 code in the low nibble of `code`.
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  uint32_t h;
+  asm("{ .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0; }"
+      : "=r"(h)
+      : "r"(code & 0xFu));
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bit) {
   atomicOr(reinterpret_cast<int*>(status), bit);
 }
@@ -212,13 +270,34 @@ struct StreamMaps {
   StreamLayout lay;
 };
 
+// Shared-memory plan of the tensor-core streaming kernels (depends on the handle's rows).
+struct TcLayout {
+  int nmax;         // B columns of an item at most: 4 planes x rows (16, 32 or 64)
+  int b_bytes;      // activation tile of a stage: nmax rows x 128 bytes
+  int stage_bytes;  // 16 KB weights + b_bytes + 2 KB scale-factor atoms
+  int stages;
+  int win_bytes;    // one scale window: 8 KB weight scales + nmax x 64 B plane scales
+  int off_win, off_x, off_tab, off_bar, smem_bytes;
+};
+
+// TMA descriptors of the tensor-core streaming kernels.
+struct TcMaps {
+  CUtensorMap w13, w2, ws13, ws2, n, ms;  // as in StreamMaps
+  CUtensorMap w13s, w2s;                  // weight scale windows (K > 2048 only)
+  CUtensorMap np4;        // u8 [4 Rmax, H/2] planes of n, box {128 B, nmax}, 128-byte swizzle
+  CUtensorMap np4s;       // u8 [64, H/32], box {64 B, nmax} (H > 2048 only)
+  CUtensorMap mid4[3];    // u8 [4 P, I/2], box {128 B, 16 / 32 / 64 rows}, 128-byte swizzle
+  CUtensorMap mid4s[3];   // u8 [4 P + 64, I/32], box {64 B, 16 / 32 / 64} (I > 2048 only)
+  TcLayout lay;
+};
+
 // ------------------------------------------------------------------ launchers ----
 // Each returns the cudaError_t of its launch.
 
 cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
                                const __nv_bfloat16* residual, const Weights& w,
                                const Scratch& s, cudaStream_t st, bool pdl,
-                               const float* xpart = nullptr);
+                               const float* xpart = nullptr, bool planes = false);
 cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cudaStream_t st,
                           bool pdl);
 cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, bool pdl);
@@ -239,6 +318,13 @@ int router_max_parts();
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
                           const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                           bool pdl, uint32_t debug);
+TcLayout make_tc_layout(int Rmax);
+int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights& w,
+                 const Scratch& s);
+cudaError_t prepare_stream_tc_kernels();
+cudaError_t launch_stream_tc(int phase, const TcMaps& maps, const Dims& d, const Weights& w,
+                             const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
+                             bool pdl, uint32_t debug);
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
                            uint64_t budget_ns, bool gated);

@@ -49,7 +49,7 @@ def test_binding_constants_match_header():
     vals = header_enum_values()
     for name, v in vals.items():
         short = name[len("MOE_TAIL_"):]
-        if short.startswith(("ERR_", "STATUS_", "MODE_")) or short == "OK":
+        if short.startswith(("ERR_", "STATUS_", "MODE_", "DEBUG_")) or short == "OK":
             assert getattr(mt, short) == v, name
     assert {k for k in vals if k.startswith("MOE_TAIL_STATUS_")} == {
         "MOE_TAIL_STATUS_BAD_ROUTING", "MOE_TAIL_STATUS_BAD_DISTINCT", "MOE_TAIL_STATUS_TIMEOUT",
@@ -104,6 +104,16 @@ def test_null_arguments_rejected_without_device(lib):
 def test_unsupported_configs_refused_before_device(lib, field, value):
     cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128))
     setattr(cfg, field, value)
+    w = mt.WeightPtrs(*([16] * 8))  # never dereferenced: refusal comes first
+    h = ctypes.c_void_p()
+    assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
+        mt.ERR_UNSUPPORTED
+    assert h.value is None
+
+
+@pytest.mark.parametrize("flags", [16 | 8, 16 | 1])
+def test_tensor_core_form_refuses_the_fused_front_and_simple_kernels(lib, flags):
+    cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128), debug_flags=flags)
     w = mt.WeightPtrs(*([16] * 8))  # never dereferenced: refusal comes first
     h = ctypes.c_void_p()
     assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
