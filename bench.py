@@ -68,9 +68,10 @@ def parse_args():
     p.add_argument("--shared-gate", action="store_true",
                    help="the workload with the shared expert's sigmoid gate; the line's config "
                         "says so")
-    p.add_argument("--tcgen05", action="store_true",
-                   help="the expert stages on the tcgen05 tensor-core kernels "
-                        "(MOE_TAIL_DEBUG_TCGEN05); the line's config says so")
+    p.add_argument("--mma-sync", action="store_true",
+                   help="the expert stages on the CUDA-core dequantisation + mma.sync "
+                        "streaming kernels (MOE_TAIL_DEBUG_MMA_SYNC) instead of the default "
+                        "tcgen05 kernels; the line's config says so")
     p.add_argument("--persistent", action="store_true",
                    help="the workload in the single persistent launch (MOE_TAIL_MODE_PERSISTENT); "
                         "the line's config says so")
@@ -254,7 +255,7 @@ def run_ours(args, rank, world, local_rank):
     res = res0.clone()
     out = torch.empty_like(res0)
     mode = mt.MODE_PERSISTENT if args.persistent else mt.MODE_MULTI_KERNEL
-    flags = mt.DEBUG_TCGEN05 if args.tcgen05 else 0
+    flags = mt.DEBUG_MMA_SYNC if args.mma_sync else 0
     tails = [mt.MoeTail(shape, dw, max_rows=R, mode=mode, debug_flags=flags) for dw in dev_w]
     nst = tails[0].launches_per_run(R) + (1 if args.out_proj else 0)
     stream = torch.cuda.current_stream()
@@ -418,15 +419,16 @@ def run_ours(args, rank, world, local_rank):
                                + (" with shared-expert gate" if args.shared_gate else "")
                                + (" with out_proj from %d" % shape.Ha if args.out_proj else "")
                                + (" in one persistent launch" if args.persistent else "")
-                               + (" on the tcgen05 expert kernels" if args.tcgen05 else ""),
+                               + (" on the mma.sync expert kernels" if args.mma_sync else ""),
                    "rows": R, "hidden": shape.H, "experts": shape.E,
                    "top_k": shape.k, "expert_inter": shape.I, "shared_inter": shape.Is,
                    "weights": "MXFP4 routed experts, bf16 router and shared expert",
-                   "arithmetic": ("MXFP4 weights x bf16 activations as four E2M1 planes "
-                                  "(tcgen05 block-scaled MMAs), bf16 shared expert, fp32 "
-                                  "accumulation in tensor memory" if args.tcgen05 else
-                                  "MXFP4 weights x bf16 activations (fed to the tensor cores "
-                                  "as f16 with power-of-two scales), fp32 accumulation"),
+                   "arithmetic": ("MXFP4 weights x bf16 activations (fed to mma.sync as f16 "
+                                  "with power-of-two scales), fp32 accumulation"
+                                  if args.mma_sync or args.persistent else
+                                  "MXFP4 weights x bf16 activations as four E2M1 planes "
+                                  "(tcgen05 block-scaled MMAs), bf16 shared expert (tcgen05 "
+                                  "bf16 MMAs), fp32 accumulation in tensor memory"),
                    "distinct_experts_mean": round(float(Ds.mean()), 2),
                    "repeat_fraction_mean": round(float(1 - Ds.mean() / (R * shape.k)), 3),
                    "bytes_per_call_mean": int(bytes_per.mean()),

@@ -100,15 +100,17 @@ enum {
   /* Run the front (add + RMSNorm, router, top-k, dedup) as one launch in which every CTA
    * recomputes the row norms, instead of a norm launch followed by a router launch. */
   MOE_TAIL_DEBUG_FUSED_FRONT = 8,
-  /* Run the expert stages on the fifth-generation tensor cores (tcgen05): each routed
-   * MXFP4 expert as block-scaled E2M1 x E2M1 MMAs whose activations enter as four E2M1
-   * planes with per-32 E8M0 scales (their sum approximates the bf16 activation to ~1e-3 of
-   * its block maximum), the bf16 shared expert as bf16 MMAs; fp32 accumulation in tensor
-   * memory.  Results meet the same parity rule as the default form.  Not combinable with
-   * MOE_TAIL_DEBUG_FUSED_FRONT or MOE_TAIL_DEBUG_SIMPLE_KERNELS (MOE_TAIL_ERR_UNSUPPORTED
-   * at create); "glm53: Long-context indexer ..." page, Modifications row 16 (every using
-   * row a column of one multi-column product per expert). */
-  MOE_TAIL_DEBUG_TCGEN05 = 16
+  /* Run the expert stages on the TMA-streaming CUDA-core kernels (E2M1 weights converted to
+   * f16 and fed to mma.sync with fp32 accumulation, E8M0 scales applied per 32-element
+   * block) instead of the default tensor-core kernels.  The default form runs each routed
+   * MXFP4 expert as tcgen05 block-scaled E2M1 x E2M1 MMAs whose activations enter as four
+   * E2M1 planes with per-32 E8M0 scales (their sum approximates the bf16 activation to ~1e-3
+   * of its block maximum), and the bf16 shared expert as tcgen05 bf16 MMAs, accumulating in
+   * tensor memory ("glm53: Long-context indexer ..." page, Modifications row 16: every
+   * using row a column of one multi-column product per expert).  Both forms meet the same
+   * parity rule.  MOE_TAIL_DEBUG_FUSED_FRONT implies this form (the fused front writes no
+   * activation planes). */
+  MOE_TAIL_DEBUG_MMA_SYNC = 16
 };
 
 typedef struct moe_tail moe_tail_t; /* opaque handle */

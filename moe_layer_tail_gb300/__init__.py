@@ -37,7 +37,7 @@ DEBUG_SIMPLE_KERNELS = 1
 DEBUG_NO_PDL = 2
 DEBUG_STALL_FIRST_STAGE = 4
 DEBUG_FUSED_FRONT = 8
-DEBUG_TCGEN05 = 16
+DEBUG_MMA_SYNC = 16
 
 # moe_attnres_mix launch flags (attnres_mix.h)
 ATTNRES_MIX_PDL = 1

@@ -820,13 +820,10 @@ int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scr
 // -1 (no encoder) or -2 (encoding failed).
 int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights& w,
                  const Scratch& s) {
-  (void)w;
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return -1;
   memset(out, 0, sizeof(*out));
-  out->w13 = sm.w13;
   out->w2 = sm.w2;
-  out->ws13 = sm.ws13;
   out->ws2 = sm.ws2;
   out->n = sm.n;
   out->ms = sm.ms;
@@ -837,6 +834,26 @@ int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights
   const uint64_t H = d.H, I = d.I, R4 = 4ull * d.Rmax, P4 = 4ull * d.Rmax * d.k;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
+  {
+    // gate and up rows of a stage in one 3-D box each: w13 as [2E][I][H/2] bytes, the shared
+    // expert's ws13 as [2][Is][H] bf16
+    cuuint64_t dims[3] = {H / 2, I, 2ull * d.E};
+    cuuint64_t strides[2] = {H / 2, I * (H / 2)};
+    cuuint32_t box[3] = {128, 64, 2};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&out->w13, U8, 3, const_cast<uint8_t*>(w.w13c), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, SW, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return -2;
+    const uint64_t Is = d.Is;
+    cuuint64_t dims2[3] = {H, Is, 2};
+    cuuint64_t strides2[2] = {H * 2, Is * H * 2};
+    cuuint32_t box2[3] = {64, 64, 2};
+    if (enc(&out->ws13, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(w.ws13),
+            dims2, strides2, box2, es, CU_TENSOR_MAP_INTERLEAVE_NONE, SW,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return -2;
+  }
   // rows past 4 Rmax (planes) and 4 P (mid planes) read as zeros
   if (encode_2d(enc, &out->np4, U8, s.np4, H / 2, R4, H / 2, 128, nmax, SW)) return -2;
   if (H > (uint64_t)kWinK &&

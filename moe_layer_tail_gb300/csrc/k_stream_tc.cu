@@ -436,17 +436,17 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
           sp.info[stage] = make_int2(item, 0);
           mbar_expect_tx(&sp.full[stage], bytes);
           if (it.kind == kRoutedGU) {
+            // the 64 gate and 64 up rows in one copy (3-D box over [2E][I][H/2])
             const int x = kc * (kChunkF4 / 2);
-            tma_load_2d(st, &maps.w13, x, it.row0, &sp.full[stage], pol);
-            tma_load_2d(st + 8192, &maps.w13, x, it.row1, &sp.full[stage], pol);
+            tma_load_3d(st, &maps.w13, x, it.out0, 2 * (it.row0 / (2 * dm.I)), &sp.full[stage],
+                        pol);
             tma_load_2d(sb, &maps.np4, x, 0, &sp.full[stage]);
           } else if (it.kind == kRoutedDN) {
             const int x = kc * (kChunkF4 / 2);
             tma_load_2d(st, &maps.w2, x, it.row0, &sp.full[stage], pol);
             tma_load_2d(sb, &maps.mid4[hsel], x, 4 * it.u0, &sp.full[stage]);
           } else if (it.kind == kSharedGU) {
-            tma_load_2d(st, &maps.ws13, kc * kChunkBF, it.row0, &sp.full[stage], pol);
-            tma_load_2d(st + 8192, &maps.ws13, kc * kChunkBF, it.row1, &sp.full[stage], pol);
+            tma_load_3d(st, &maps.ws13, kc * kChunkBF, it.out0, 0, &sp.full[stage], pol);
             tma_load_2d(sb, &maps.n, kc * kChunkBF, 0, &sp.full[stage]);
           } else {
             tma_load_2d(st, &maps.ws2, kc * kChunkBF, it.row0, &sp.full[stage], pol);

@@ -30,7 +30,7 @@ struct moe_tail {
   moe_tail_config_t cfg;
   Weights w;
   StreamMaps maps;     // TMA descriptors of the streamed weights
-  TcMaps tcmaps;       // and of the tensor-core form (MOE_TAIL_DEBUG_TCGEN05)
+  TcMaps tcmaps;       // and of the tensor-core form (the default expert stages)
   Scratch s;
   void* slab;          // one device allocation holding every scratch buffer
   size_t slab_bytes;
@@ -71,7 +71,16 @@ extern "C" const char* moe_tail_last_cuda_error(void) { return g_cuda_err; }
 
 static_assert(MOE_TAIL_DEBUG_STALL_FIRST_STAGE == (int)kDebugStallFirstStage,
               "debug bit values agree");
-static_assert(MOE_TAIL_DEBUG_TCGEN05 == (int)kDebugTcgen05, "debug bit values agree");
+static_assert(MOE_TAIL_DEBUG_MMA_SYNC == (int)kDebugMmaSync, "debug bit values agree");
+
+// The expert stages run on the tcgen05 kernels unless a debug flag picks another form (the
+// mma.sync streaming kernels, the cross-checking CUDA-core kernels, or the fused front, which
+// writes no activation planes) or the handle is a persistent one.
+static bool uses_tc(const moe_tail_config_t* c) {
+  return c->mode == MOE_TAIL_MODE_MULTI_KERNEL &&
+         !(c->debug_flags & (MOE_TAIL_DEBUG_MMA_SYNC | MOE_TAIL_DEBUG_SIMPLE_KERNELS |
+                             MOE_TAIL_DEBUG_FUSED_FRONT));
+}
 
 static int check_config(const moe_tail_config_t* c) {
   if (c->max_rows < 1 || c->max_rows > kMaxRows) return MOE_TAIL_ERR_UNSUPPORTED;
@@ -96,11 +105,7 @@ static int check_config(const moe_tail_config_t* c) {
     return MOE_TAIL_ERR_UNSUPPORTED;
   // the persistent launch covers the tail from x on (no out_proj stage in front of it)
   if (c->mode == MOE_TAIL_MODE_PERSISTENT && c->attn_dim != 0) return MOE_TAIL_ERR_UNSUPPORTED;
-  // the tensor-core experts take their activation planes from the two-launch front, and
-  // replace the TMA-streaming CUDA-core kernels (not the cross-checking ones)
-  if ((c->debug_flags & MOE_TAIL_DEBUG_TCGEN05) &&
-      (c->debug_flags & (MOE_TAIL_DEBUG_FUSED_FRONT | MOE_TAIL_DEBUG_SIMPLE_KERNELS)))
-    return MOE_TAIL_ERR_UNSUPPORTED;
+
   return MOE_TAIL_OK;
 }
 
@@ -190,8 +195,7 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = prepare_stream_kernels();
   if (e == cudaSuccess) e = prepare_front_kernels();
-  if (e == cudaSuccess && (cfg->debug_flags & MOE_TAIL_DEBUG_TCGEN05))
-    e = prepare_stream_tc_kernels();
+  if (e == cudaSuccess && uses_tc(cfg)) e = prepare_stream_tc_kernels();
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess && cfg->mode == MOE_TAIL_MODE_PERSISTENT) {
     // one CTA per SM at most; the cooperative launch checks at run time that all fit
@@ -224,8 +228,7 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
     d0.Ha = cfg->attn_dim;
     d0.Pk = 1;
     int mrc = make_stream_maps(&h->maps, d0, h->w, h->s);
-    if (mrc == 0 && (cfg->debug_flags & MOE_TAIL_DEBUG_TCGEN05))
-      mrc = make_tc_maps(&h->tcmaps, h->maps, d0, h->w, h->s);
+    if (mrc == 0 && uses_tc(cfg)) mrc = make_tc_maps(&h->tcmaps, h->maps, d0, h->w, h->s);
     if (mrc != 0) {
       cudaFree(h->slab);
       cudaFree(h->stage);
@@ -292,7 +295,7 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   } while (0)
   const bool pdl = !(h->cfg.debug_flags & MOE_TAIL_DEBUG_NO_PDL);
   const bool simple = (h->cfg.debug_flags & MOE_TAIL_DEBUG_SIMPLE_KERNELS) != 0;
-  const bool tc = (h->cfg.debug_flags & MOE_TAIL_DEBUG_TCGEN05) != 0;
+  const bool tc = uses_tc(&h->cfg);
   const uint64_t budget_ns =
       (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
   const float* xpart = nullptr;

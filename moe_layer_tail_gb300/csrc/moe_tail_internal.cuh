@@ -86,7 +86,7 @@ struct Scratch {
 
 // Debug bits the kernels read (same values as MOE_TAIL_DEBUG_* in moe_tail.h).
 constexpr uint32_t kDebugStallFirstStage = 4u;
-constexpr uint32_t kDebugTcgen05 = 16u;
+constexpr uint32_t kDebugMmaSync = 16u;
 
 // counters[] words (all zeroed at the start of every call by the front)
 enum : int {
@@ -282,7 +282,10 @@ struct TcLayout {
 
 // TMA descriptors of the tensor-core streaming kernels.
 struct TcMaps {
-  CUtensorMap w13, w2, ws13, ws2, n, ms;  // as in StreamMaps
+  CUtensorMap w13;        // u8 [2E][I][H/2] (rows (2e + half) I + j), box {128 B, 64, 2}:
+                          // a stage's 64 gate and 64 up rows in one copy, 128-byte swizzle
+  CUtensorMap ws13;       // bf16 [2][Is][H], box {64, 64, 2}, 128-byte swizzle
+  CUtensorMap w2, ws2, n, ms;  // as in StreamMaps
   CUtensorMap w13s, w2s;                  // weight scale windows (K > 2048 only)
   CUtensorMap np4;        // u8 [4 Rmax, H/2] planes of n, box {128 B, nmax}, 128-byte swizzle
   CUtensorMap np4s;       // u8 [64, H/32], box {64 B, nmax} (H > 2048 only)

@@ -111,16 +111,6 @@ def test_unsupported_configs_refused_before_device(lib, field, value):
     assert h.value is None
 
 
-@pytest.mark.parametrize("flags", [16 | 8, 16 | 1])
-def test_tensor_core_form_refuses_the_fused_front_and_simple_kernels(lib, flags):
-    cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128), debug_flags=flags)
-    w = mt.WeightPtrs(*([16] * 8))  # never dereferenced: refusal comes first
-    h = ctypes.c_void_p()
-    assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
-        mt.ERR_UNSUPPORTED
-    assert h.value is None
-
-
 def test_misaligned_weight_pointer_refused(lib):
     cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128))
     w = mt.WeightPtrs(*([16] * 7 + [24]))

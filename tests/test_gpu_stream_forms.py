@@ -1,8 +1,9 @@
-"""The tensor-core form of the expert stages (MOE_TAIL_DEBUG_TCGEN05: tcgen05 block-scaled
-E2M1 x E2M1 MMAs for the routed MXFP4 experts, bf16 MMAs for the shared expert) against the
-oracle, element by element through the C ABI, under the same parity rule as the default
-form: every workload at full size, small shapes with ragged tails and the edge cases, graph
-replay, the launch modes and the bounded-wait failure path."""
+"""The two streaming forms of the expert stages side by side: the default tensor-core form
+(tcgen05 block-scaled E2M1 x E2M1 MMAs for the routed MXFP4 experts, bf16 MMAs for the shared
+expert) and the CUDA-core form (MOE_TAIL_DEBUG_MMA_SYNC: E2M1 -> f16 conversion into
+mma.sync), each against the oracle element by element through the C ABI under the same
+parity rule: every workload at full size, small shapes with ragged tails and the edge cases,
+graph replay, the launch modes and the bounded-wait failure path."""
 import numpy as np
 import pytest
 
@@ -15,7 +16,8 @@ from test_gpu_parity import NTHREADS, _small, run_gpu, workload_inputs
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-TC = 16      # debug flag: tcgen05 expert stages
+TC = 0       # the default (tcgen05) expert stages
+MMA_SYNC = 16  # debug flag: the CUDA-core mma.sync streaming kernels
 NO_PDL = 2   # plain stream-ordered launches
 STALL = 4    # failure injection: one producer leaves a stage unpublished
 STATUS_TIMEOUT = 4
@@ -38,10 +40,11 @@ def test_tiny_first():
     _check(wl.shape, d)
 
 
+@pytest.mark.parametrize("flags", [TC, MMA_SYNC])
 @pytest.mark.parametrize("name", list(gen.WORKLOADS))
-def test_workload_parity_full_size(name):
+def test_workload_parity_full_size(name, flags):
     wl, d, dev, orc = workload_inputs(name)
-    tail = MoeTail(wl.shape, dev, max_rows=wl.shape.R, debug_flags=TC)
+    tail = MoeTail(wl.shape, dev, max_rows=wl.shape.R, debug_flags=flags)
     out, res, ids, wts, nd = run_gpu(tail, d)
     figs = check_parity(out, res, ids, orc, wl.shape.k)
     assert nd == len(np.unique(orc["ids"]))
@@ -49,7 +52,7 @@ def test_workload_parity_full_size(name):
     print(name, figs)
 
 
-@pytest.mark.parametrize("flags", [TC, TC | NO_PDL])
+@pytest.mark.parametrize("flags", [TC, TC | NO_PDL, MMA_SYNC])
 @pytest.mark.parametrize("R,H,E,k,I,Is", [
     (1, 256, 1, 1, 128, 64),       # a single expert, smallest shapes
     (2, 512, 12, 3, 256, 192),     # several tiles, ragged tails
@@ -67,12 +70,13 @@ def test_small_shapes(R, H, E, k, I, Is, flags):
     _check(shape, d, flags=flags)
 
 
+@pytest.mark.parametrize("flags", [TC, MMA_SYNC])
 @pytest.mark.parametrize("shift", [12, -16])
-def test_mid_far_from_unit_scale(shift):
+def test_mid_far_from_unit_scale(shift, flags):
     """Gate/up weights scaled by 2^12 or 2^-16: the planes' own E8M0 scales follow mid."""
     shape, d = _small(15, R=4, H=512, E=10, k=3, I=256, Is=128)
     d["w13_scales"] = (d["w13_scales"].astype(np.int32) + shift).astype(np.uint8)
-    _check(shape, d)
+    _check(shape, d, flags=flags)
 
 
 def test_fewer_rows_than_the_handle():
@@ -80,12 +84,12 @@ def test_fewer_rows_than_the_handle():
     _check(shape, d, max_rows=16, rows=6)
 
 
-def test_matches_default_form_closely():
+def test_the_two_forms_agree_closely():
     """Both forms pass the rule against the oracle; here also against each other."""
     shape, d = _small(22, R=8, H=2048, E=32, k=4, I=512, Is=256, kind="similar")
     _, _, _, _, (out_tc, res_tc, ids_tc, _, _) = _check(shape, d)
     dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
-    ref = MoeTail(shape, dev, max_rows=shape.R)
+    ref = MoeTail(shape, dev, max_rows=shape.R, debug_flags=MMA_SYNC)
     out, res, ids, _, _ = run_gpu(ref, d)
     assert np.array_equal(res, res_tc) and np.array_equal(ids, ids_tc)
     a = (out.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
@@ -121,10 +125,11 @@ def test_graph_replay_bitwise_equal_to_eager():
     assert tail.status() == 0
 
 
-def test_device_wait_timeout_is_reported_and_context_survives():
+@pytest.mark.parametrize("flags", [TC, MMA_SYNC])
+def test_device_wait_timeout_is_reported_and_context_survives(flags):
     shape, d = _small(24, R=2, H=512, E=8, k=2, I=256, Is=128)
     dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
-    bad = MoeTail(shape, dev, max_rows=shape.R, debug_flags=TC | STALL, wait_budget_us=20000)
+    bad = MoeTail(shape, dev, max_rows=shape.R, debug_flags=flags | STALL, wait_budget_us=20000)
     x = acts_to_device(d["x"])
     res = acts_to_device(d["residual"])
     out = torch.empty_like(x)
@@ -133,4 +138,4 @@ def test_device_wait_timeout_is_reported_and_context_survives():
     assert bad.status() & STATUS_TIMEOUT
     bad.close()
     # a healthy handle on the same device still matches the oracle
-    _check(shape, d)
+    _check(shape, d, flags=flags)
