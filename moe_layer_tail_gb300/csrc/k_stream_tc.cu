@@ -191,6 +191,7 @@ struct TcPtrs {
   int2* info;        // [stages] item of each stage
   int* aitem;        // [2] item of each accumulator slot
   uint32_t* tbase;   // tensor-memory base address of the CTA
+  int* eflag;        // epilogue: this CTA completed a split shared item
 };
 
 __device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L) {
@@ -211,7 +212,41 @@ __device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L) {
   p.info = reinterpret_cast<int2*>(p.drain + 2);
   p.aitem = reinterpret_cast<int*>(p.info + kMaxStreamStages);
   p.tbase = reinterpret_cast<uint32_t*>(p.aitem + 2);
+  p.eflag = reinterpret_cast<int*>(p.tbase + 1);
   return p;
+}
+
+// K parts of every shared-expert gate/up item of this call: the fewest (1, 2 or 4, dividing
+// H / 64) that bring an item down to an SM's share of the launch's bytes, so that at one or a
+// few rows the shared items do not outlast the routed ones.  Every CTA computes the same.
+__device__ __forceinline__ int shared_parts(const Dims& dm, int D, int nsm) {
+  const int ns = dm.Is / 64;
+  if (ns > kMaxSharedSplitItems) return 1;
+  const uint64_t item_b = 128ull * (uint64_t)dm.H * 2;
+  const uint64_t routed_b = 128ull * (uint64_t)(dm.H / 2 + dm.H / 32);
+  const uint64_t total = (uint64_t)ns * item_b + (uint64_t)D * (uint64_t)(dm.I / 64) * routed_b;
+  const uint64_t share = total / (uint64_t)nsm;
+  int p = 1;
+  while (p < kMaxSharedParts && item_b / (uint64_t)p > share && (dm.H / 64) % (2 * p) == 0)
+    p *= 2;
+  return p;
+}
+
+// Items of a launch when the shared gate/up items are split into P K parts: the ns * P parts
+// first (part = item mod P, K elements [part H / P, (part + 1) H / P)), then the routed items.
+__device__ __forceinline__ Item decode_tc(int phase, int item, const Dims& dm, const Tables& tb,
+                                          int D, int P) {
+  if (phase != 0 || P == 1) return decode_item(phase, item, dm, tb, D);
+  const int ns = dm.Is / 64;
+  if (item < ns * P) {
+    Item it = decode_item(0, item / P, dm, tb, D);
+    it.part = item % P;
+    it.K = dm.H / P;
+    it.k0 = it.part * it.K;
+    it.nst = it.K / kChunkBF;
+    return it;
+  }
+  return decode_item(0, item - ns * (P - 1), dm, tb, D);
 }
 
 // ----------------------------------------------------------------------- epilogue ----
@@ -262,10 +297,13 @@ __device__ __forceinline__ void acc_ld(uint32_t acc0, uint32_t acc1, bool two, f
   }
 }
 
+// Returns false when the item is a K part of a split shared item that another part will
+// finish (nothing to count for the next launch yet).
 template <int NMAX>
-__device__ __forceinline__ void tc_finish(const Item& it, uint32_t acc0, uint32_t acc1, float* xch,
-                                          int ew, int q, int lane, const Dims& dm,
-                                          const Tables& tb, const Scratch& s) {
+__device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint32_t acc0,
+                                          uint32_t acc1, float* xch, int* eflag, int ew, int q,
+                                          int lane, const Dims& dm, const Tables& tb,
+                                          const Scratch& s) {
   // bf16 items have whole 64-element stages; an MXFP4 item's first stage reaches past 128
   // elements unless K is 128
   const bool two = (it.kind == kSharedGU || it.kind == kSharedDN) || it.K > 128;
@@ -275,7 +313,33 @@ __device__ __forceinline__ void tc_finish(const Item& it, uint32_t acc0, uint32_
     float* xg = xch;            // [64][R] gate sums
     float* xu = xch + 64 * R;   // [64][R] up sums
     float* dst = (m < 64) ? xg + m * R : xu + (m - 64) * R;
-    if (it.kind == kRoutedGU) {
+    if (it.kind == kSharedGU && P > 1) {
+      // one K part: its sums to scratch; the CTA whose part completes the item adds all parts
+      // in part order (whichever CTAs ran them) and finishes it
+      const int si = item / P;
+      float v[16];
+      acc_ld<16>(acc0, acc1, true, v);
+      float* gp = s.gpart + ((size_t)(si * kMaxSharedParts + it.part) * 128 + m) * R;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < R) gp[c] = v[c];
+      __threadfence();
+      bar_epi();
+      if (ew == 0 && lane == 0)
+        *eflag = (atomicAdd(&s.counters[kCtrSharedParts + si], 1u) == (uint32_t)(P - 1)) ? 1 : 0;
+      bar_epi();
+      if (!*eflag) return false;
+      __threadfence();
+      const float* g0 = s.gpart + ((size_t)(si * kMaxSharedParts) * 128 + m) * R;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        if (c < R) {
+          float a = __ldcg(g0 + c);
+          for (int pp = 1; pp < P; ++pp) a += __ldcg(g0 + (size_t)pp * 128 * R + c);
+          dst[c] = a;
+        }
+      }
+    } else if (it.kind == kRoutedGU) {
       float v[NMAX];
       acc_ld<NMAX>(acc0, acc1, two, v);
 #pragma unroll
@@ -324,6 +388,7 @@ __device__ __forceinline__ void tc_finish(const Item& it, uint32_t acc0, uint32_
     for (int r = 0; r < 16; ++r)
       if (r < dm.R) s.ys[(size_t)r * dm.H + it.out0 + m] = v[r];
   }
+  return true;
 }
 
 // ------------------------------------------------------------------------ kernel ----
@@ -344,7 +409,8 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
 
   if (PHASE == 0) pdl_wait();
   const int D = min(max(*s.n_distinct, 1), kMaxPicks);
-  const int n_items = items_of(PHASE, dm, D);
+  const int P = (PHASE == 0) ? shared_parts(dm, D, (int)gridDim.x) : 1;
+  const int n_items = items_of(PHASE, dm, D) + (dm.Is / 64) * (P - 1);
   for (int i = threadIdx.x; i < D; i += kTcThreads) sp.t_uniq[i] = s.uniq[i];
   for (int i = threadIdx.x; i <= D; i += kTcThreads) sp.t_off[i] = s.user_off[i];
   for (int i = threadIdx.x; i < dm.R * dm.k; i += kTcThreads) sp.t_users[i] = s.user_list[i];
@@ -396,7 +462,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       int item = (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
       while (ok && item < n_items) {
         const int next = (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
-        const Item it = decode_item(PHASE, item, dm, tb, D);
+        const Item it = decode_tc(PHASE, item, dm, tb, D, P);
         const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
         const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;
         const int nb = (it.kind == kRoutedGU) ? NMAX : (it.kind == kRoutedDN) ? (16 << hsel) : 0;
@@ -446,8 +512,9 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
             tma_load_2d(st, &maps.w2, x, it.row0, &sp.full[stage], pol);
             tma_load_2d(sb, &maps.mid4[hsel], x, 4 * it.u0, &sp.full[stage]);
           } else if (it.kind == kSharedGU) {
-            tma_load_3d(st, &maps.ws13, kc * kChunkBF, it.out0, 0, &sp.full[stage], pol);
-            tma_load_2d(sb, &maps.n, kc * kChunkBF, 0, &sp.full[stage]);
+            const int x = it.k0 + kc * kChunkBF;
+            tma_load_3d(st, &maps.ws13, x, it.out0, 0, &sp.full[stage], pol);
+            tma_load_2d(sb, &maps.n, x, 0, &sp.full[stage]);
           } else {
             tma_load_2d(st, &maps.ws2, kc * kChunkBF, it.row0, &sp.full[stage], pol);
             tma_load_2d(sb, &maps.ms, kc * kChunkBF, 0, &sp.full[stage]);
@@ -510,7 +577,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     for (;;) {
       if (!mbar_wait(&sp.full[stage], phase, budget_ns)) { ok = false; break; }
       const int item = sp.info[stage].x;
-      if (kc == 0 && item >= 0) it = decode_item(PHASE, item, dm, tb, D);
+      if (kc == 0 && item >= 0) it = decode_tc(PHASE, item, dm, tb, D, P);
       if (item >= 0 && (it.kind == kRoutedGU || it.kind == kRoutedDN)) {
         const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;
         const int nb = (it.kind == kRoutedGU) ? NMAX : (16 << hsel);
@@ -574,7 +641,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       const int item = sp.info[stage].x;
       if (item < 0) break;
       if (kc == 0) {
-        it = decode_item(PHASE, item, dm, tb, D);
+        it = decode_tc(PHASE, item, dm, tb, D, P);
         if (!mbar_wait(&sp.aempty[acnt & 1u], ((acnt >> 1) & 1u) ^ 1u, budget_ns)) {
           ok = false;
           break;
@@ -659,17 +726,18 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       tc_fence_after();
       const int item = sp.aitem[as];
       if (item < 0) break;
-      const Item it = decode_item(PHASE, item, dm, tb, D);
+      const Item it = decode_tc(PHASE, item, dm, tb, D, P);
       const uint32_t lq = (uint32_t)(32 * q) << 16;
       const uint32_t acc0 = tbase + (2u * as) * (uint32_t)NMAX + lq;
       const uint32_t acc1 = tbase + (2u * as + 1u) * (uint32_t)NMAX + lq;
       float* xch = sp.xch + (size_t)(ac & 1u) * (2 * 64 * dm.Rmax);
-      tc_finish<NMAX>(it, acc0, acc1, xch, ew, q, lane, dm, tb, s);
+      const bool done = tc_finish<NMAX>(it, item, P, acc0, acc1, xch, sp.eflag, ew, q, lane, dm,
+                                        tb, s);
       // every epilogue thread's stores before the count the next launch waits for
       __threadfence();
       tc_fence_before();
       bar_epi();
-      if (ew == 0 && lane == 0) {
+      if (done && ew == 0 && lane == 0) {
         uint32_t* c = &s.counters[PHASE == 1 ? kCtrTileDone + it.out0 / 128
                                   : it.kind == kSharedGU ? kCtrSharedGUDone
                                                          : kCtrGUDone + it.d];

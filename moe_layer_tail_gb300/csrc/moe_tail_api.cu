@@ -8,6 +8,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 
 #include <math.h>
@@ -148,6 +149,8 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s, size_t* 
   s->sgate = (float*)take(R * 4);
   s->xproj = (__nv_bfloat16*)take(R * H * 2);
   s->xpart = (float*)take((size_t)kMaxOutProjParts * R * H * 4);
+  s->gpart = (float*)take((size_t)std::min<size_t>(Is / 64, kMaxSharedSplitItems) *
+                          kMaxSharedParts * 128 * R * 4);
   s->np4 = (uint8_t*)take(4 * R * H / 2);
   s->np4s = (uint8_t*)take(64 * H / 32);
   s->mid4 = (uint8_t*)take(4 * P * I / 2);

@@ -18,6 +18,11 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxPicks = kMaxRows * kMaxTopK;  // (row, slot) pairs of one call
 constexpr int kMaxOutProjParts = 8;  // K parts of an out_proj box at most
+// A shared-expert gate/up item (64 gate + 64 up rows over all of H) may be split along K into
+// up to kMaxSharedParts parts when it is larger than an SM's share of the launch (the tensor-
+// core form), for shared experts of at most kMaxSharedSplitItems items.
+constexpr int kMaxSharedParts = 4;
+constexpr int kMaxSharedSplitItems = 256;
 
 // Device status word bits (sticky; read by moe_tail_get_status; the same values as
 // MOE_TAIL_STATUS_* in moe_tail.h).
@@ -75,6 +80,8 @@ struct Scratch {
   float* sgate;          // [Rmax] sigmoid gate of the shared output (when a gate is given)
   __nv_bfloat16* xproj;  // [Rmax, H] x = out_proj(attn) for moe_tail_run_attn (one K part)
   float* xpart;          // [kMaxOutProjParts, Rmax, H] fp32 sums of each out_proj K part
+  float* gpart;          // [kMaxSharedSplitItems, kMaxSharedParts, 128, Rmax] fp32 sums of the
+                         // K parts of split shared gate/up items (rows: 64 gate, 64 up)
   uint8_t* np4;          // [4 Rmax, H/2] E2M1 planes of n (row 4r + p = plane p of row r)
   uint8_t* np4s;         // [64, H/32] their E8M0 scales (rows past 4 Rmax stay zero)
   uint8_t* mid4;         // [4 Rmax k, I/2] E2M1 planes of mid (row 4 slot + p, slot = the
@@ -100,7 +107,9 @@ enum : int {
   kCtrOutProj = 6,       // next work item of the out_proj launch (runs before the norm
                          // launch, which zeroes it with the rest for the next call)
   kCtrTileDone = 16 + 2 * kMaxPicks,  // [256] down items finished per 128 hidden outputs
-  kCtrWords = 16 + 2 * kMaxPicks + 256
+  kCtrSharedParts = 16 + 2 * kMaxPicks + 256,  // [kMaxSharedSplitItems] K parts of a split
+                                               // shared gate/up item finished
+  kCtrWords = 16 + 2 * kMaxPicks + 256 + 256
 };
 
 // ------------------------------------------------------------------ device helpers ----
