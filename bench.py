@@ -62,6 +62,9 @@ def parse_args():
                    help="profiling aid: the workload with this many experts instead (a "
                         "smaller case of the same kernels, e.g. for an ncu capture); the "
                         "line's config says so")
+    p.add_argument("--weight-copies", type=int, default=0,
+                   help="profiling aid: rotate over this many weight copies instead of "
+                        "max(4, ceil(4 L2 / bytes per call)); the line's config says so")
     p.add_argument("--out-proj", type=int, default=0, metavar="HA",
                    help="the workload with an attention output projection of width HA in "
                         "front (moe_tail_run_attn); the line's config says so (no e2e leg)")
@@ -238,7 +241,7 @@ def run_ours(args, rank, world, local_rank):
     # call finds its weights in L2 from the call before
     est = gen.algorithmic_bytes(shape, min(shape.E, R * shape.k), gated=args.shared_gate,
                                 out_proj=bool(args.out_proj))
-    L = weight_copies(est)
+    L = args.weight_copies if args.weight_copies > 0 else weight_copies(est)
     dev_w = [mt.weights_to_device(host_w)]
     for _ in range(L - 1):
         dev_w.append({k: v.clone() for k, v in dev_w[0].items()})
@@ -398,9 +401,17 @@ def run_ours(args, rank, world, local_rank):
     if dom_bytes is not None:
         dur_s = tot[dom] / K * 1e-3
         achieved = dom_bytes / dur_s / 1e9
-        src = source_hash(["moe_layer_tail_gb300/csrc/k_stream.cu",
-                           "moe_layer_tail_gb300/csrc/moe_tail_internal.cuh"])
-        tr = ncu_traffic(names[dom], src, dom_bytes) if not args.persistent else None
+        if args.mma_sync:
+            src = source_hash(["moe_layer_tail_gb300/csrc/k_stream.cu",
+                               "moe_layer_tail_gb300/csrc/k_stream_common.cuh",
+                               "moe_layer_tail_gb300/csrc/moe_tail_internal.cuh"])
+            tag = names[dom] + "_mma_sync"
+        else:
+            src = source_hash(["moe_layer_tail_gb300/csrc/k_stream_tc.cu",
+                               "moe_layer_tail_gb300/csrc/k_stream_common.cuh",
+                               "moe_layer_tail_gb300/csrc/moe_tail_internal.cuh"])
+            tag = names[dom]
+        tr = ncu_traffic(tag, src, dom_bytes) if not args.persistent else None
         roof = {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
                 "measured": "CUDA events around each launch on its stream, second pass of the "
                             "same %d calls (events serialise the launches: %.1f us/call)"
