@@ -116,7 +116,9 @@ enum {
 typedef struct moe_tail moe_tail_t; /* opaque handle */
 
 typedef struct {
-  int32_t max_rows;       /* 1..16: the largest `rows` any run will pass */
+  int32_t max_rows;       /* 1..32: the largest `rows` any run will pass; above 16 only the
+                           * default expert form without attn_dim (the debug forms and the
+                           * persistent mode take 1..16; MOE_TAIL_ERR_UNSUPPORTED otherwise) */
   int32_t hidden;         /* H: multiple of 256 (of 512 above 2048), at most 32768 */
   int32_t n_experts;      /* E: 1..1024 */
   int32_t top_k;          /* k: 1..min(E, 32) */

@@ -268,8 +268,9 @@ cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, 
 // row over K part p of H, on the tensor cores (mma.m16n8k16, bf16 x bf16 into fp32; the 16
 // experts are the M rows, the call's rows the N columns).  The CTA's router weights are
 // copied into shared memory with cp.async before the wait on the norm launch (they depend
-// on nothing), then the rows' n for the part; each of the 8 warps takes a slice of the
-// part's 32-element K steps and the warps' partial tiles are added in warp order.  The
+// on nothing), then the rows' n for the part (up to 32 rows: four N-tiles of 8); each of
+// the 8 warps takes a slice of the part's 32-element K steps and the warps' partial tiles
+// are added in warp order.  The
 // partial logits of each part go to scratch; the last CTA to finish (atomic ticket after a
 // fence) adds the parts in part order into shared memory, then runs top-k and the dedup.
 // Loops stay rolled: every CTA runs this code once, so its size, not its instruction
@@ -293,13 +294,16 @@ static RouterPlan router_plan(int R, int H, int E) {
   int P = (128 + p.tiles - 1) / p.tiles;
   P = std::max(P, (H + kRtMaxPart - 1) / kRtMaxPart);
   P = std::min(P, kRtMaxParts);
-  p.plen = ((H + P - 1) / P + 31) / 32 * 32;
-  p.parts = (H + p.plen - 1) / p.plen;
-  const size_t pitch = (size_t)p.plen * 2 + 16;
-  const size_t tiles_bytes = (kRtTile + (size_t)R) * pitch;
-  const size_t logit_bytes = (size_t)R * E * 4;
-  const size_t nt = (R + 7) / 8;
-  p.smem = ((std::max(tiles_bytes, logit_bytes) + 15) / 16) * 16 + kRtWarps * nt * 32 * 16;
+  for (;; ++P) {  // more parts while the staged rows of many-row handles exceed 192 KB
+    p.plen = ((H + P - 1) / P + 31) / 32 * 32;
+    p.parts = (H + p.plen - 1) / p.plen;
+    const size_t pitch = (size_t)p.plen * 2 + 16;
+    const size_t tiles_bytes = (kRtTile + (size_t)R) * pitch;
+    const size_t logit_bytes = (size_t)R * E * 4;
+    const size_t nt = (R + 7) / 8;
+    p.smem = ((std::max(tiles_bytes, logit_bytes) + 15) / 16) * 16 + kRtWarps * nt * 32 * 16;
+    if (p.smem <= 192 * 1024 || P >= kRtMaxParts) break;
+  }
   return p;
 }
 
@@ -348,28 +352,33 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   __syncthreads();
   // warp w: K steps [w * spw, ...) of 32 elements; lane (g, t) takes elements 8t .. 8t+7 of
   // a step for weight rows g and g + 8 and for activation row g (+ 8 for the second tile)
-  const int NT = (R + 7) / 8;
+  const int NT = (R + 7) / 8;  // N-tiles of 8 rows (up to 4)
   const int S = len / 32, spw = (S + kRtWarps - 1) / kRtWarps;
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  float acc[kMaxRows / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < kMaxRows / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
   const uint8_t* wa = sw + g * pitch + 16 * t;
   const uint8_t* wc = sw + (g + 8) * pitch + 16 * t;
-  const uint8_t* nb0 = sn + min(g, R - 1) * pitch + 16 * t;
-  const uint8_t* nb1 = sn + min(8 + g, R - 1) * pitch + 16 * t;
+  const uint8_t* nb = sn + 16 * t;
 #pragma unroll 1
   for (int st = warp * spw; st < min(S, (warp + 1) * spw); ++st) {
     const uint4 a = *reinterpret_cast<const uint4*>(wa + st * 64);
     const uint4 c = *reinterpret_cast<const uint4*>(wc + st * 64);
-    const uint4 b = *reinterpret_cast<const uint4*>(nb0 + st * 64);
-    mma_bf16_16816(acc[0], a.x, c.x, a.y, c.y, b.x, b.y);
-    mma_bf16_16816(acc[0], a.z, c.z, a.w, c.w, b.z, b.w);
-    if (NT > 1) {
-      const uint4 b2 = *reinterpret_cast<const uint4*>(nb1 + st * 64);
-      mma_bf16_16816(acc[1], a.x, c.x, a.y, c.y, b2.x, b2.y);
-      mma_bf16_16816(acc[1], a.z, c.z, a.w, c.w, b2.z, b2.w);
+#pragma unroll
+    for (int nt = 0; nt < kMaxRows / 8; ++nt) {
+      if (nt < NT) {
+        const uint4 b =
+            *reinterpret_cast<const uint4*>(nb + min(8 * nt + g, R - 1) * pitch + st * 64);
+        mma_bf16_16816(acc[nt], a.x, c.x, a.y, c.y, b.x, b.y);
+        mma_bf16_16816(acc[nt], a.z, c.z, a.w, c.w, b.z, b.w);
+      }
     }
   }
-  for (int nt = 0; nt < NT; ++nt)
-    red[(warp * NT + nt) * 32 + lane] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+#pragma unroll
+  for (int nt = 0; nt < kMaxRows / 8; ++nt)
+    if (nt < NT)
+      red[(warp * NT + nt) * 32 + lane] =
+          make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
   __syncthreads();
   if (warp == 0) {
     // lane (g, t): experts g and g + 8, rows 8 nt + 2t and 8 nt + 2t + 1
@@ -463,10 +472,10 @@ __global__ void __launch_bounds__(kFrontThreads)
 k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ residual,
               const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ w_r,
               Scratch s, int R, int H, int E, int k, float eps) {
-  __shared__ float s_rstd[kMaxRows];
-  __shared__ float s_down[kMaxRows];
+  __shared__ float s_rstd[kMaxRowsOther];
+  __shared__ float s_down[kMaxRowsOther];
   __shared__ float s_gmax[kFrontWarps];
-  __shared__ uint4 s_n[kMaxRows][kFrontChunk / 8];
+  __shared__ uint4 s_n[kMaxRowsOther][kFrontChunk / 8];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x;
@@ -516,9 +525,9 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
 
   // 2. router over H in chunks
   const int e = blockIdx.x * kFrontWarps + warp;
-  float acc[kMaxRows];
+  float acc[kMaxRowsOther];
 #pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+  for (int r = 0; r < kMaxRowsOther; ++r) acc[r] = 0.f;
   for (int h0 = 0, ci = 0; h0 < H; h0 += kFrontChunk, ++ci) {
     const int cw = min(kFrontChunk, H - h0);  // multiple of 128
     const int ng = cw / 8;                     // 16-byte groups per row in this chunk
@@ -562,7 +571,7 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
         const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
                              bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
+        for (int r = 0; r < kMaxRowsOther; ++r) {
           if (r < R) {
             const uint4 nv = s_n[r][c];
             float a = acc[r];
@@ -579,7 +588,7 @@ k_front_fused(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   }
   if (e < E) {
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
+    for (int r = 0; r < kMaxRowsOther; ++r) {
       if (r < R) {
         const float v = warp_sum(acc[r]);
         if (lane == 0) s.logits[(size_t)r * E + e] = v;
@@ -623,11 +632,11 @@ cudaError_t launch_front_fused(const Dims& d, const __nv_bfloat16* x,
 namespace mtail {
 
 struct RouteScratch {
-  float logits[kMaxRows * kMaxExperts];
+  float logits[kMaxRowsOther * kMaxExperts];
   int32_t n_distinct;
-  int32_t uniq[kMaxPicks];
-  int32_t user_off[kMaxPicks + 1];
-  int32_t user_list[kMaxPicks];
+  int32_t uniq[kMaxRowsOther * kMaxTopK];
+  int32_t user_off[kMaxRowsOther * kMaxTopK + 1];
+  int32_t user_list[kMaxRowsOther * kMaxTopK];
   int32_t status;   // status bits of the running call (cleared with the ticket)
   uint32_t ticket;  // CTAs done with their logits (the last one ranks)
 };
@@ -644,8 +653,8 @@ k_route_static(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restr
                RouteScratch* __restrict__ rs, int32_t* __restrict__ ids_out,
                float* __restrict__ wts_out, int32_t* __restrict__ nd_out,
                int32_t* __restrict__ status_out, int R, int H, int E, int k, float eps) {
-  __shared__ float s_rstd[kMaxRows];
-  __shared__ uint4 s_n[kMaxRows][kFrontChunk / 8];
+  __shared__ float s_rstd[kMaxRowsOther];
+  __shared__ uint4 s_n[kMaxRowsOther][kFrontChunk / 8];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x;
@@ -668,9 +677,9 @@ k_route_static(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restr
   }
   __syncthreads();
   const int e = blockIdx.x * kFrontWarps + warp;
-  float acc[kMaxRows];
+  float acc[kMaxRowsOther];
 #pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+  for (int r = 0; r < kMaxRowsOther; ++r) acc[r] = 0.f;
   for (int h0 = 0; h0 < H; h0 += kFrontChunk) {
     const int ng = min(kFrontChunk, H - h0) / 8;
     for (int idx = tid; idx < R * ng; idx += kFrontThreads) {
@@ -693,7 +702,7 @@ k_route_static(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restr
         const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
                              bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
+        for (int r = 0; r < kMaxRowsOther; ++r) {
           if (r < R) {
             const uint4 nv = s_n[r][c];
             float a = acc[r];
@@ -710,7 +719,7 @@ k_route_static(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restr
   }
   if (e < E) {
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
+    for (int r = 0; r < kMaxRowsOther; ++r) {
       if (r < R) {
         const float v = warp_sum(acc[r]);
         if (lane == 0) rs->logits[(size_t)r * E + e] = v;
@@ -753,7 +762,7 @@ extern "C" int moe_tail_route_noalloc(const void* x, const void* residual, const
   const void* ptrs[4] = {x, residual, gamma, router_w};
   for (const void* p : ptrs)
     if ((uintptr_t)p & 15u) return MOE_TAIL_ERR_INVALID_ARG;
-  if (rows < 1 || rows > kMaxRows || n_experts < 1 || n_experts > kMaxExperts || top_k < 1 ||
+  if (rows < 1 || rows > kMaxRowsOther || n_experts < 1 || n_experts > kMaxExperts || top_k < 1 ||
       top_k > kMaxTopK || top_k > n_experts || hidden < 128 || hidden % 128 != 0 ||
       !(rms_eps > 0.f))
     return MOE_TAIL_ERR_UNSUPPORTED;

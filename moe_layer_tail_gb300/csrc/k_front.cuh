@@ -40,9 +40,9 @@ __device__ __forceinline__ void router_warp(const __nv_bfloat16* __restrict__ n,
                                             const __nv_bfloat16* __restrict__ w_r,
                                             float* __restrict__ logits, int R, int H, int E,
                                             int e, int lane) {
-  float acc[kMaxRows];
+  float acc[kMaxRowsOther];
 #pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+  for (int r = 0; r < kMaxRowsOther; ++r) acc[r] = 0.f;
   const uint4* wrow = reinterpret_cast<const uint4*>(w_r + (size_t)e * H);
   const int nch = H / 8;
   for (int c = lane; c < nch; c += 32) {
@@ -50,7 +50,7 @@ __device__ __forceinline__ void router_warp(const __nv_bfloat16* __restrict__ n,
     float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
                    bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
+    for (int r = 0; r < kMaxRowsOther; ++r) {
       if (r < R) {
         uint4 nv = reinterpret_cast<const uint4*>(n + (size_t)r * H)[c];
         float a = acc[r];
@@ -63,7 +63,7 @@ __device__ __forceinline__ void router_warp(const __nv_bfloat16* __restrict__ n,
     }
   }
 #pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) {
+  for (int r = 0; r < kMaxRowsOther; ++r) {
     if (r < R) {
       float v = warp_sum(acc[r]);
       if (lane == 0) logits[(size_t)r * E + e] = v;

@@ -98,12 +98,12 @@ __device__ void routed_gateup_work(long long gw, long long nw, const Dims& dm, c
     const int d = (int)(it / I), j = (int)(it % I);
     const int e = s.uniq[d];
     const int u0 = s.user_off[d], U = s.user_off[d + 1] - u0;
-    int rows[kMaxRows];
+    int rows[kMaxRowsOther];
 #pragma unroll
-    for (int u = 0; u < kMaxRows; ++u) rows[u] = (u < U) ? s.user_list[u0 + u] / k : 0;
-    float ag[kMaxRows], au[kMaxRows];
+    for (int u = 0; u < kMaxRowsOther; ++u) rows[u] = (u < U) ? s.user_list[u0 + u] / k : 0;
+    float ag[kMaxRowsOther], au[kMaxRowsOther];
 #pragma unroll
-    for (int u = 0; u < kMaxRows; ++u) { ag[u] = 0.f; au[u] = 0.f; }
+    for (int u = 0; u < kMaxRowsOther; ++u) { ag[u] = 0.f; au[u] = 0.f; }
     const size_t grow = (size_t)e * 2 * I + j, urow = grow + I;
     const uint4* gc = reinterpret_cast<const uint4*>(w.w13c + grow * (H / 2));
     const uint4* uc = reinterpret_cast<const uint4*>(w.w13c + urow * (H / 2));
@@ -119,7 +119,7 @@ __device__ void routed_gateup_work(long long gw, long long nw, const Dims& dm, c
       dequant32(__ldg(uc + b), uv);
       const float sg = e8m0_to_float(__ldg(gs + b)), su = e8m0_to_float(__ldg(us + b));
 #pragma unroll
-      for (int u = 0; u < kMaxRows; ++u) {
+      for (int u = 0; u < kMaxRowsOther; ++u) {
         if (u < U) {
           float dg, du;
           dot32x2_bf16(gv, uv, s.n + (size_t)rows[u] * H + b * 32, dg, du);
@@ -129,7 +129,7 @@ __device__ void routed_gateup_work(long long gw, long long nw, const Dims& dm, c
       }
     }
 #pragma unroll
-    for (int u = 0; u < kMaxRows; ++u) {
+    for (int u = 0; u < kMaxRowsOther; ++u) {
       if (u < U) {
         const float g = warp_sum(ag[u]), v = warp_sum(au[u]);
         if (lane == 0) {
@@ -153,12 +153,12 @@ __device__ void routed_down_work(long long gw, long long nw, const Dims& dm, con
     const int d = (int)(it / H), h = (int)(it % H);
     const int e = s.uniq[d];
     const int u0 = s.user_off[d], U = s.user_off[d + 1] - u0;
-    int picks[kMaxRows];
+    int picks[kMaxRowsOther];
 #pragma unroll
-    for (int u = 0; u < kMaxRows; ++u) picks[u] = (u < U) ? s.user_list[u0 + u] : 0;
-    float acc[kMaxRows];
+    for (int u = 0; u < kMaxRowsOther; ++u) picks[u] = (u < U) ? s.user_list[u0 + u] : 0;
+    float acc[kMaxRowsOther];
 #pragma unroll
-    for (int u = 0; u < kMaxRows; ++u) acc[u] = 0.f;
+    for (int u = 0; u < kMaxRowsOther; ++u) acc[u] = 0.f;
     const size_t row = (size_t)e * H + h;
     const uint4* c4 = reinterpret_cast<const uint4*>(w.w2c + row * (I / 2));
     const uint8_t* sc = w.w2s + row * nblk;
@@ -169,11 +169,11 @@ __device__ void routed_down_work(long long gw, long long nw, const Dims& dm, con
       dequant32(__ldg(c4 + b), v);
       const float sb = e8m0_to_float(__ldg(sc + b));
 #pragma unroll
-      for (int u = 0; u < kMaxRows; ++u)
+      for (int u = 0; u < kMaxRowsOther; ++u)
         if (u < U) acc[u] += dot32_bf16(v, s.mid + (size_t)picks[u] * I + b * 32) * sb;
     }
 #pragma unroll
-    for (int u = 0; u < kMaxRows; ++u) {
+    for (int u = 0; u < kMaxRowsOther; ++u) {
       if (u < U) {
         const float t = warp_sum(acc[u]);
         if (lane == 0) s.y[(size_t)picks[u] * H + h] = t;
@@ -189,9 +189,9 @@ __device__ void shared_gateup_work(long long gw, long long nw, const Dims& dm, c
   const int H = dm.H, Is = dm.Is, R = dm.R;
   for (long long jj = gw; jj < Is; jj += nw) {
     const int j = (int)jj;
-    float ag[kMaxRows], au[kMaxRows];
+    float ag[kMaxRowsOther], au[kMaxRowsOther];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) { ag[r] = 0.f; au[r] = 0.f; }
+    for (int r = 0; r < kMaxRowsOther; ++r) { ag[r] = 0.f; au[r] = 0.f; }
     const uint4* g4 = reinterpret_cast<const uint4*>(w.ws13 + (size_t)j * H);
     const uint4* u4 = reinterpret_cast<const uint4*>(w.ws13 + (size_t)(Is + j) * H);
     prefetch_row(g4, (size_t)H * 2, lane);
@@ -200,7 +200,7 @@ __device__ void shared_gateup_work(long long gw, long long nw, const Dims& dm, c
       const uint4 gv = __ldg(g4 + c), uv = __ldg(u4 + c);
       const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
+      for (int r = 0; r < kMaxRowsOther; ++r) {
         if (r < R) {
           const uint4 nv = reinterpret_cast<const uint4*>(s.n + (size_t)r * H)[c];
           const uint32_t nw[4] = {nv.x, nv.y, nv.z, nv.w};
@@ -215,7 +215,7 @@ __device__ void shared_gateup_work(long long gw, long long nw, const Dims& dm, c
       }
     }
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
+    for (int r = 0; r < kMaxRowsOther; ++r) {
       if (r < R) {
         const float g = warp_sum(ag[r]), v = warp_sum(au[r]);
         if (lane == 0) s.ms[(size_t)r * Is + j] = __float2bfloat16_rn(silu_f(g) * v);
@@ -231,16 +231,16 @@ __device__ void shared_down_work(long long gw, long long nw, const Dims& dm, con
   const int H = dm.H, Is = dm.Is, R = dm.R;
   for (long long hh = gw; hh < H; hh += nw) {
     const int h = (int)hh;
-    float acc[kMaxRows];
+    float acc[kMaxRowsOther];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+    for (int r = 0; r < kMaxRowsOther; ++r) acc[r] = 0.f;
     const uint4* w4 = reinterpret_cast<const uint4*>(w.ws2 + (size_t)h * Is);
     prefetch_row(w4, (size_t)Is * 2, lane);
     for (int c = lane; c < Is / 8; c += 32) {
       const uint4 wv = __ldg(w4 + c);
       const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
+      for (int r = 0; r < kMaxRowsOther; ++r) {
         if (r < R) {
           const uint4 mv = reinterpret_cast<const uint4*>(s.ms + (size_t)r * Is)[c];
           const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
@@ -255,7 +255,7 @@ __device__ void shared_down_work(long long gw, long long nw, const Dims& dm, con
       }
     }
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
+    for (int r = 0; r < kMaxRowsOther; ++r) {
       if (r < R) {
         const float t = warp_sum(acc[r]);
         if (lane == 0) s.ys[(size_t)r * H + h] = t;

@@ -80,9 +80,9 @@ __device__ __forceinline__ SmemPtrs carve_smem(uint8_t* smem, const StreamLayout
   p.win = smem + L.off_win;
   p.red = reinterpret_cast<float4*>(smem + L.off_red);
   p.t_uniq = reinterpret_cast<int*>(smem + L.off_tab);
-  p.t_off = p.t_uniq + kMaxPicks;
-  p.t_users = p.t_off + kMaxPicks + 1;
-  p.t_rscale = reinterpret_cast<float*>(p.t_users + kMaxPicks);
+  p.t_off = p.t_uniq + L.tab_picks;
+  p.t_users = p.t_off + L.tab_picks + 1;
+  p.t_rscale = reinterpret_cast<float*>(p.t_users + L.tab_picks);
   p.full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
   p.empty = p.full + kMaxStreamStages;
   p.wempty = p.empty + kMaxStreamStages;
@@ -732,14 +732,15 @@ static int encode_2d(EncodeTiledFn fn, CUtensorMap* m, CUtensorMapDataType dt, c
 }
 
 // Shared-memory plan for a handle created for `Rmax` rows (stages as many as fit, up to 8).
-StreamLayout make_stream_layout(int Rmax) {
+StreamLayout make_stream_layout(int Rmax, int k) {
   StreamLayout L;
+  L.tab_picks = Rmax * k;
   L.act_rows = (Rmax <= 4) ? 4 : (Rmax <= 8) ? 8 : 16;
   L.stage_bytes = kStageW + L.act_rows * kActPitch;
   L.win_bytes = kWinW + L.act_rows * 256;
   L.nt_max = (Rmax > 8) ? 2 : 1;
   const int red_bytes = 2 * kConsumerWarps * L.nt_max * 512;
-  const int tab_bytes = ((3 * kMaxPicks + 1 + kMaxRows) * 4 + 127) & ~127;
+  const int tab_bytes = ((3 * L.tab_picks + 1 + Rmax) * 4 + 127) & ~127;
   const int bar_bytes = (2 * kMaxStreamStages + 6) * 8 + kMaxStreamStages * 8 + 2 * 4;
   const int fixed = 2 * L.win_bytes + red_bytes + tab_bytes + ((bar_bytes + 127) & ~127);
   L.stages = min(kMaxStreamStages, (kSmemLimit - fixed) / L.stage_bytes);
@@ -811,7 +812,7 @@ int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scr
   if (d.Ha > 0 &&
       encode_2d(enc, &out->wo, BF, w.wo, (uint64_t)d.Ha, H, (uint64_t)d.Ha * 2, 64, 128, SW))
     return -2;
-  out->lay = make_stream_layout(d.Rmax);
+  out->lay = make_stream_layout(d.Rmax, d.k);
   return 0;
 }
 
@@ -829,7 +830,7 @@ int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights
   out->ms = sm.ms;
   out->w13s = sm.w13s;
   out->w2s = sm.w2s;
-  out->lay = make_tc_layout(d.Rmax);
+  out->lay = make_tc_layout(d.Rmax, d.k);
   const uint32_t nmax = (uint32_t)out->lay.nmax;
   const uint64_t H = d.H, I = d.I, R4 = 4ull * d.Rmax, P4 = 4ull * d.Rmax * d.k;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -857,13 +858,14 @@ int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights
   // rows past 4 Rmax (planes) and 4 P (mid planes) read as zeros
   if (encode_2d(enc, &out->np4, U8, s.np4, H / 2, R4, H / 2, 128, nmax, SW)) return -2;
   if (H > (uint64_t)kWinK &&
-      encode_2d(enc, &out->np4s, U8, s.np4s, H / 32, 64, H / 32, 64, nmax, NS))
+      encode_2d(enc, &out->np4s, U8, s.np4s, H / 32, 128, H / 32, 64, nmax, NS))
     return -2;
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < 4; ++i) {
     const uint32_t rows = 16u << i;
+    if (rows > nmax) break;
     if (encode_2d(enc, &out->mid4[i], U8, s.mid4, I / 2, P4, I / 2, 128, rows, SW)) return -2;
     if (I > (uint64_t)kWinK &&
-        encode_2d(enc, &out->mid4s[i], U8, s.mid4s, I / 32, P4 + 64, I / 32, 64, rows, NS))
+        encode_2d(enc, &out->mid4s[i], U8, s.mid4s, I / 32, P4 + 128, I / 32, 64, rows, NS))
       return -2;
   }
   return 0;

@@ -59,7 +59,15 @@ constexpr int kTcThreads = 9 * 32;
 constexpr int kTcSfBytes = 2048;    // per stage: A atoms 2 x 512 B, B atoms 2 x 512 B
 constexpr int kTcCols = 512;        // tensor-memory columns of a CTA
 constexpr int kTcSfCol = 256;       // first scale-factor column (accumulators below)
+constexpr int kTcMaxStages = 10;    // 16 scale-factor columns each: 256 + 160 <= 512
 constexpr uint32_t kNamedBarEpi = 1;
+// bf16 (shared-expert) MMA columns: the call's rows, 16 up to 16 rows, 32 above
+template <int NMAX>
+constexpr int kSharedCols = NMAX <= 64 ? 16 : 32;
+// accumulator slots: two (an item's MMAs overlap the previous item's epilogue), one at 128
+// columns (two issuers x 128 columns fill the half of tensor memory the slots may use)
+template <int NMAX>
+constexpr int kAccSlots = NMAX <= 64 ? 2 : 1;
 
 // --------------------------------------------------------------------- PTX wrappers ----
 
@@ -200,17 +208,17 @@ __device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L) {
   p.win = smem + L.off_win;
   p.xch = reinterpret_cast<float*>(smem + L.off_x);
   p.t_uniq = reinterpret_cast<int*>(smem + L.off_tab);
-  p.t_off = p.t_uniq + kMaxPicks;
-  p.t_users = p.t_off + kMaxPicks + 1;
+  p.t_off = p.t_uniq + L.tab_picks;
+  p.t_users = p.t_off + L.tab_picks + 1;
   p.full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
-  p.ready = p.full + kMaxStreamStages;
-  p.empty = p.ready + kMaxStreamStages;
-  p.wempty = p.empty + kMaxStreamStages;
+  p.ready = p.full + kTcMaxStages;
+  p.empty = p.ready + kTcMaxStages;
+  p.wempty = p.empty + kTcMaxStages;
   p.afull = p.wempty + 2;
   p.aempty = p.afull + 2;
   p.drain = p.aempty + 2;
   p.info = reinterpret_cast<int2*>(p.drain + 2);
-  p.aitem = reinterpret_cast<int*>(p.info + kMaxStreamStages);
+  p.aitem = reinterpret_cast<int*>(p.info + kTcMaxStages);
   p.tbase = reinterpret_cast<uint32_t*>(p.aitem + 2);
   p.eflag = reinterpret_cast<int*>(p.tbase + 1);
   return p;
@@ -284,21 +292,21 @@ __device__ __forceinline__ void store_planes_lane(float v, int lane, uint8_t* co
 }
 
 // One finished item: its accumulator (N plane columns per TMEM lane) to outputs.
-// The sums of an item's columns: issuer 0's accumulator plus issuer 1's, in that order, when
-// issuer 1 took part (issuer 1 owns the second 128 K elements of every stage).
-template <int N>
-__device__ __forceinline__ void acc_ld(uint32_t acc0, uint32_t acc1, bool two, float (&v)[N]) {
-  tmem_ld<N>(acc0, v);
+// C columns (16 or 32) of an item's sums from column c0: issuer 0's accumulator plus issuer
+// 1's, in that order, when issuer 1 took part (it owns the second 128 K elements of every
+// stage).  Loading 32 columns at most at a time bounds the registers at 128 columns.
+template <int C>
+__device__ __forceinline__ void acc_chunk(uint32_t acc0, uint32_t acc1, bool two, int c0,
+                                          float (&v)[C]) {
+  tmem_ld<C>(acc0 + (uint32_t)c0, v);
   if (two) {
-    float w[N];
-    tmem_ld<N>(acc1, w);
+    float w[C];
+    tmem_ld<C>(acc1 + (uint32_t)c0, w);
 #pragma unroll
-    for (int i = 0; i < N; ++i) v[i] += w[i];
+    for (int i = 0; i < C; ++i) v[i] += w[i];
   }
 }
 
-// Returns false when the item is a K part of a split shared item that another part will
-// finish (nothing to count for the next launch yet).
 template <int NMAX>
 __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint32_t acc0,
                                           uint32_t acc1, float* xch, int* eflag, int ew, int q,
@@ -308,6 +316,7 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
   // elements unless K is 128
   const bool two = (it.kind == kSharedGU || it.kind == kSharedDN) || it.K > 128;
   const int m = 32 * q + lane;  // weight row of this thread within the item's 128
+  constexpr int NSH = kSharedCols<NMAX>;  // bf16 (shared-expert) columns: the rows
   if (it.kind == kRoutedGU || it.kind == kSharedGU) {
     const int R = dm.Rmax;
     float* xg = xch;            // [64][R] gate sums
@@ -317,11 +326,11 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
       // one K part: its sums to scratch; the CTA whose part completes the item adds all parts
       // in part order (whichever CTAs ran them) and finishes it
       const int si = item / P;
-      float v[16];
-      acc_ld<16>(acc0, acc1, true, v);
+      float v[NSH];
+      acc_chunk<NSH>(acc0, acc1, true, 0, v);
       float* gp = s.gpart + ((size_t)(si * kMaxSharedParts + it.part) * 128 + m) * R;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < NSH; ++c)
         if (c < R) gp[c] = v[c];
       __threadfence();
       bar_epi();
@@ -332,7 +341,7 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
       __threadfence();
       const float* g0 = s.gpart + ((size_t)(si * kMaxSharedParts) * 128 + m) * R;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < NSH; ++c) {
         if (c < R) {
           float a = __ldcg(g0 + c);
           for (int pp = 1; pp < P; ++pp) a += __ldcg(g0 + (size_t)pp * 128 * R + c);
@@ -340,16 +349,23 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
         }
       }
     } else if (it.kind == kRoutedGU) {
-      float v[NMAX];
-      acc_ld<NMAX>(acc0, acc1, two, v);
+      // columns 4r + p: row r's planes, 32 columns (8 rows) at a time
+      constexpr int C = NMAX < 32 ? NMAX : 32;
 #pragma unroll
-      for (int c = 0; c < NMAX / 4; ++c)
-        if (c < R) dst[c] = plane_sum<NMAX>(v, c);
+      for (int c0 = 0; c0 < NMAX; c0 += C) {
+        if (c0 / 4 < R) {
+          float v[C];
+          acc_chunk<C>(acc0, acc1, two, c0, v);
+#pragma unroll
+          for (int c = 0; c < C / 4; ++c)
+            if (c0 / 4 + c < R) dst[c0 / 4 + c] = plane_sum<C>(v, c);
+        }
+      }
     } else {
-      float v[16];
-      acc_ld<16>(acc0, acc1, two, v);
+      float v[NSH];
+      acc_chunk<NSH>(acc0, acc1, two, 0, v);
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < NSH; ++c)
         if (c < R) dst[c] = v[c];
     }
     bar_epi();
@@ -375,17 +391,25 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
       }
     }
   } else if (it.kind == kRoutedDN) {
-    float v[NMAX];
-    acc_ld<NMAX>(acc0, acc1, two, v);
+    // columns 4u + p: user u's planes, 32 columns (8 users) at a time
+    constexpr int C = NMAX < 32 ? NMAX : 32;
 #pragma unroll
-    for (int u = 0; u < NMAX / 4; ++u)
-      if (u < it.U)
-        s.y[(size_t)tb.users[it.u0 + u] * dm.H + it.out0 + m] = plane_sum<NMAX>(v, u);
+    for (int c0 = 0; c0 < NMAX; c0 += C) {
+      if (c0 / 4 < it.U) {
+        float v[C];
+        acc_chunk<C>(acc0, acc1, two, c0, v);
+#pragma unroll
+        for (int c = 0; c < C / 4; ++c) {
+          const int u = c0 / 4 + c;
+          if (u < it.U) s.y[(size_t)tb.users[it.u0 + u] * dm.H + it.out0 + m] = plane_sum<C>(v, c);
+        }
+      }
+    }
   } else {  // shared down
-    float v[16];
-    acc_ld<16>(acc0, acc1, two, v);
+    float v[NSH];
+    acc_chunk<NSH>(acc0, acc1, two, 0, v);
 #pragma unroll
-    for (int r = 0; r < 16; ++r)
+    for (int r = 0; r < NSH; ++r)
       if (r < dm.R) s.ys[(size_t)r * dm.H + it.out0 + m] = v[r];
   }
   return true;
@@ -405,6 +429,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   }
   const TcPtrs sp = tc_carve(smem, lay);
   const int S = lay.stages;
+  constexpr uint32_t A = kAccSlots<NMAX>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (PHASE == 0) pdl_wait();
@@ -464,7 +489,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
         const int next = (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
         const Item it = decode_tc(PHASE, item, dm, tb, D, P);
         const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
-        const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;
+        const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : (it.U <= 16) ? 2 : 3;
         const int nb = (it.kind == kRoutedGU) ? NMAX : (it.kind == kRoutedDN) ? (16 << hsel) : 0;
         if (PHASE == 1) {
           const bool sh = (it.kind == kSharedDN);
@@ -579,7 +604,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       const int item = sp.info[stage].x;
       if (kc == 0 && item >= 0) it = decode_tc(PHASE, item, dm, tb, D, P);
       if (item >= 0 && (it.kind == kRoutedGU || it.kind == kRoutedDN)) {
-        const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;
+        const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : (it.U <= 16) ? 2 : 3;
         const int nb = (it.kind == kRoutedGU) ? NMAX : (16 << hsel);
         const uint8_t* ws = sp.win + (wcnt & 1u) * lay.win_bytes;
         uint8_t* atoms = sp.stages + stage * lay.stage_bytes + kStageW + lay.b_bytes;
@@ -642,7 +667,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       if (item < 0) break;
       if (kc == 0) {
         it = decode_tc(PHASE, item, dm, tb, D, P);
-        if (!mbar_wait(&sp.aempty[acnt & 1u], ((acnt >> 1) & 1u) ^ 1u, budget_ns)) {
+        if (!mbar_wait(&sp.aempty[acnt % A], ((acnt / A) & 1u) ^ 1u, budget_ns)) {
           ok = false;
           break;
         }
@@ -652,9 +677,9 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       if (lane == 0) {
         const uint8_t* st = sp.stages + stage * lay.stage_bytes;
         const uint8_t* sb = st + kStageW;
-        const uint32_t acc = tbase + (2u * (acnt & 1u) + (uint32_t)h) * (uint32_t)NMAX;
+        const uint32_t acc = tbase + (2u * (acnt % A) + (uint32_t)h) * (uint32_t)NMAX;
         if (routed) {
-          const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : 2;
+          const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : (it.U <= 16) ? 2 : 3;
           const int nb = (it.kind == kRoutedGU) ? NMAX : (16 << hsel);
           const uint8_t* atoms = st + kStageW + lay.b_bytes;
           const uint32_t sf = tbase + kTcSfCol + 16u * (uint32_t)stage + 8u * (uint32_t)h;
@@ -673,7 +698,8 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int kk = 2 * h + j;
-            tc_mma_f16(acc, sw128_desc(st + 32 * kk), sw128_desc(sb + 32 * kk), idesc_bf16(16),
+            tc_mma_f16(acc, sw128_desc(st + 32 * kk), sw128_desc(sb + 32 * kk),
+                       idesc_bf16(kSharedCols<NMAX>),
                        (kc > 0 || j > 0) ? 1u : 0u);
           }
         }
@@ -685,9 +711,9 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
         // this issuer's accumulator is final once its MMAs complete; issuer 0 also
         // publishes the item id (three arrivals in all)
         if (lane == 0) {
-          if (h == 0) sp.aitem[acnt & 1u] = item;
-          tc_commit(&sp.afull[acnt & 1u]);
-          if (h == 0) mbar_arrive(&sp.afull[acnt & 1u]);
+          if (h == 0) sp.aitem[acnt % A] = item;
+          tc_commit(&sp.afull[acnt % A]);
+          if (h == 0) mbar_arrive(&sp.afull[acnt % A]);
         }
         __syncwarp();
         ++acnt;
@@ -696,10 +722,10 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     }
     if (ok && h == 0) {
       // end of work: an end marker in the next accumulator slot
-      if (mbar_wait(&sp.aempty[acnt & 1u], ((acnt >> 1) & 1u) ^ 1u, budget_ns)) {
+      if (mbar_wait(&sp.aempty[acnt % A], ((acnt / A) & 1u) ^ 1u, budget_ns)) {
         if (lane == 0) {
-          sp.aitem[acnt & 1u] = -1;
-          mbar_arrive_n(&sp.afull[acnt & 1u], 3);
+          sp.aitem[acnt % A] = -1;
+          mbar_arrive_n(&sp.afull[acnt % A], 3);
         }
       } else {
         ok = false;
@@ -718,8 +744,8 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     // --------------------------------------------------------------- epilogue ----
     const int q = warp & 3, ew = warp - kTcWarpEpi;
     for (uint32_t ac = 0;; ++ac) {
-      const uint32_t as = ac & 1u;
-      if (!mbar_wait(&sp.afull[as], (ac >> 1) & 1u, budget_ns)) {
+      const uint32_t as = ac % A;
+      if (!mbar_wait(&sp.afull[as], (ac / A) & 1u, budget_ns)) {
         if (lane == 0) set_status(s.status, kStatusTimeout);
         break;
       }
@@ -730,7 +756,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       const uint32_t lq = (uint32_t)(32 * q) << 16;
       const uint32_t acc0 = tbase + (2u * as) * (uint32_t)NMAX + lq;
       const uint32_t acc1 = tbase + (2u * as + 1u) * (uint32_t)NMAX + lq;
-      float* xch = sp.xch + (size_t)(ac & 1u) * (2 * 64 * dm.Rmax);
+      float* xch = sp.xch;  // one buffer: the item-end barrier orders its reuse
       const bool done = tc_finish<NMAX>(it, item, P, acc0, acc1, xch, sp.eflag, ew, q, lane, dm,
                                         tb, s);
       // every epilogue thread's stores before the count the next launch waits for
@@ -771,9 +797,11 @@ cudaError_t prepare_stream_tc_kernels() {
   if (e == cudaSuccess) e = tc_prepare_one<0, 16>();
   if (e == cudaSuccess) e = tc_prepare_one<0, 32>();
   if (e == cudaSuccess) e = tc_prepare_one<0, 64>();
+  if (e == cudaSuccess) e = tc_prepare_one<0, 128>();
   if (e == cudaSuccess) e = tc_prepare_one<1, 16>();
   if (e == cudaSuccess) e = tc_prepare_one<1, 32>();
   if (e == cudaSuccess) e = tc_prepare_one<1, 64>();
+  if (e == cudaSuccess) e = tc_prepare_one<1, 128>();
   return e;
 }
 
@@ -792,28 +820,34 @@ cudaError_t launch_stream_tc(int phase, const TcMaps& maps, const Dims& d, const
   if (phase == 0) {
     if (nmax == 16) return tc_launch<0, 16>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
     if (nmax == 32) return tc_launch<0, 32>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
-    return tc_launch<0, 64>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+    if (nmax == 64) return tc_launch<0, 64>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+    return tc_launch<0, 128>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
   }
   if (nmax == 16) return tc_launch<1, 16>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
   if (nmax == 32) return tc_launch<1, 32>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
-  return tc_launch<1, 64>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+  if (nmax == 64) return tc_launch<1, 64>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+  return tc_launch<1, 128>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
 }
 
 // Shared-memory plan: stages of 16 KB weights + nmax x 128 B activations + 2 KB scale atoms,
 // as many as fit (up to 8, the tensor-memory scale ring), a two-slot scale window ring, the
 // epilogue exchange, the dedup tables and the barriers.
-TcLayout make_tc_layout(int Rmax) {
+TcLayout make_tc_layout(int Rmax, int k) {
   TcLayout L;
-  L.nmax = (Rmax <= 4) ? 16 : (Rmax <= 8) ? 32 : 64;
+  L.nmax = (Rmax <= 4) ? 16 : (Rmax <= 8) ? 32 : (Rmax <= 16) ? 64 : 128;
+  L.aslots = (L.nmax <= 64) ? 2 : 1;
+  L.tab_picks = Rmax * k;
   L.b_bytes = L.nmax * 128;
   L.stage_bytes = kStageW + L.b_bytes + kTcSfBytes;
   L.win_bytes = kWinW + L.nmax * 64;
-  const int x_bytes = 2 * 2 * 64 * Rmax * 4;
-  const int tab_bytes = ((3 * kMaxPicks + 1) * 4 + 127) & ~127;
-  const int bar_bytes = (3 * kMaxStreamStages + 8) * 8 + kMaxStreamStages * 8 + 2 * 4 + 4;
+  const int x_bytes = 2 * 64 * Rmax * 4;
+  const int tab_bytes = ((3 * L.tab_picks + 1) * 4 + 127) & ~127;
+  // mbarriers full, ready, empty per stage + wempty, afull, aempty, drain (2 each); the
+  // stages' item words; the accumulator slots' item words; tbase and eflag
+  const int bar_bytes = (3 * kTcMaxStages + 8) * 8 + kTcMaxStages * 8 + 2 * 4 + 4 + 4;
   const int fixed = 2 * L.win_bytes + x_bytes + tab_bytes + ((bar_bytes + 127) & ~127);
   L.stages = (kSmemLimit - fixed) / L.stage_bytes;
-  if (L.stages > kMaxStreamStages) L.stages = kMaxStreamStages;
+  if (L.stages > kTcMaxStages) L.stages = kTcMaxStages;
   L.off_win = L.stages * L.stage_bytes;
   L.off_x = L.off_win + 2 * L.win_bytes;
   L.off_tab = L.off_x + x_bytes;

@@ -85,6 +85,10 @@ static bool uses_tc(const moe_tail_config_t* c) {
 
 static int check_config(const moe_tail_config_t* c) {
   if (c->max_rows < 1 || c->max_rows > kMaxRows) return MOE_TAIL_ERR_UNSUPPORTED;
+  // more than 16 rows: the default expert form only, without the out_proj stage (whose
+  // streaming launch keeps 16-row register tiles)
+  if (c->max_rows > kMaxRowsOther && (!uses_tc(c) || c->attn_dim != 0))
+    return MOE_TAIL_ERR_UNSUPPORTED;
   // hidden: whole 256-element stages; above 2048 the E8M0 rows (hidden/32 bytes) must be
   // whole 16-byte units for the scale-window tensor maps
   if (c->hidden < 256 || c->hidden % 256) return MOE_TAIL_ERR_UNSUPPORTED;
@@ -152,9 +156,9 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s, size_t* 
   s->gpart = (float*)take((size_t)std::min<size_t>(Is / 64, kMaxSharedSplitItems) *
                           kMaxSharedParts * 128 * R * 4);
   s->np4 = (uint8_t*)take(4 * R * H / 2);
-  s->np4s = (uint8_t*)take(64 * H / 32);
+  s->np4s = (uint8_t*)take(128 * H / 32);
   s->mid4 = (uint8_t*)take(4 * P * I / 2);
-  s->mid4s = (uint8_t*)take((4 * P + 64) * I / 32);
+  s->mid4s = (uint8_t*)take((4 * P + 128) * I / 32);
   s->status = (int32_t*)take(4);
   s->counters = (uint32_t*)take(kCtrWords * 4);
   if (n_canary) *n_canary = nc < kMaxCanaries ? nc : kMaxCanaries;

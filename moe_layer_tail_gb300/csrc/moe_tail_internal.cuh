@@ -12,8 +12,12 @@
 
 namespace mtail {
 
-// Hard limits (checked at create time).
-constexpr int kMaxRows = 16;
+// Hard limits (checked at create time).  The default (tcgen05) form takes up to 32 rows (the
+// top-k dedup keeps each expert's users as a 32-bit row mask); the other expert forms, the
+// fused front, the persistent launch and the routing without allocation keep per-row
+// register arrays of 16.
+constexpr int kMaxRows = 32;
+constexpr int kMaxRowsOther = 16;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxPicks = kMaxRows * kMaxTopK;  // (row, slot) pairs of one call
@@ -83,10 +87,10 @@ struct Scratch {
   float* gpart;          // [kMaxSharedSplitItems, kMaxSharedParts, 128, Rmax] fp32 sums of the
                          // K parts of split shared gate/up items (rows: 64 gate, 64 up)
   uint8_t* np4;          // [4 Rmax, H/2] E2M1 planes of n (row 4r + p = plane p of row r)
-  uint8_t* np4s;         // [64, H/32] their E8M0 scales (rows past 4 Rmax stay zero)
+  uint8_t* np4s;         // [128, H/32] their E8M0 scales (rows past 4 Rmax stay zero)
   uint8_t* mid4;         // [4 Rmax k, I/2] E2M1 planes of mid (row 4 slot + p, slot = the
                          // pick's position in user_list)
-  uint8_t* mid4s;        // [4 Rmax k + 64, I/32] their E8M0 scales (64 zero rows after)
+  uint8_t* mid4s;        // [4 Rmax k + 128, I/32] their E8M0 scales (128 zero rows after)
   int32_t* status;       // [1] sticky device status word
   uint32_t* counters;    // [kCtrWords] work counters, tickets and per-expert progress
 };
@@ -259,6 +263,7 @@ struct StreamLayout {
   int nt_max;       // N-tiles of 8 users (1 or 2)
   int off_win, off_red, off_tab, off_bar;  // byte offsets of the regions after the stages
   int smem_bytes;   // dynamic shared memory of a launch
+  int tab_picks;    // entries of the dedup tables (rows x k of the handle)
 };
 
 // TMA descriptors of the streamed matrices (built once at create time) and the plan.
@@ -281,12 +286,14 @@ struct StreamMaps {
 
 // Shared-memory plan of the tensor-core streaming kernels (depends on the handle's rows).
 struct TcLayout {
-  int nmax;         // B columns of an item at most: 4 planes x rows (16, 32 or 64)
+  int nmax;         // B columns of an item at most: 4 planes x rows (16, 32, 64 or 128)
+  int aslots;       // accumulator slots (2, or 1 at 128 columns: tensor memory holds 512)
   int b_bytes;      // activation tile of a stage: nmax rows x 128 bytes
   int stage_bytes;  // 16 KB weights + b_bytes + 2 KB scale-factor atoms
   int stages;
   int win_bytes;    // one scale window: 8 KB weight scales + nmax x 64 B plane scales
   int off_win, off_x, off_tab, off_bar, smem_bytes;
+  int tab_picks;    // entries of the dedup tables (rows x k of the handle)
 };
 
 // TMA descriptors of the tensor-core streaming kernels.
@@ -298,8 +305,8 @@ struct TcMaps {
   CUtensorMap w13s, w2s;                  // weight scale windows (K > 2048 only)
   CUtensorMap np4;        // u8 [4 Rmax, H/2] planes of n, box {128 B, nmax}, 128-byte swizzle
   CUtensorMap np4s;       // u8 [64, H/32], box {64 B, nmax} (H > 2048 only)
-  CUtensorMap mid4[3];    // u8 [4 P, I/2], box {128 B, 16 / 32 / 64 rows}, 128-byte swizzle
-  CUtensorMap mid4s[3];   // u8 [4 P + 64, I/32], box {64 B, 16 / 32 / 64} (I > 2048 only)
+  CUtensorMap mid4[4];    // u8 [4 P, I/2], box {128 B, 16 / 32 / 64 / 128 rows}, 128-byte swizzle
+  CUtensorMap mid4s[4];   // u8 [4 P + 128, I/32], box {64 B, 16 / 32 / 64 / 128} (I > 2048 only)
   TcLayout lay;
 };
 
@@ -323,14 +330,14 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
 int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scratch& s);
 // The call's attention-output map (bf16 [rows, Ha] at attn): 0, or -1/-2 as make_stream_maps.
 int make_attn_map(StreamMaps* m, const void* attn, int rows, const Dims& d);
-StreamLayout make_stream_layout(int Rmax);
+StreamLayout make_stream_layout(int Rmax, int k);
 cudaError_t prepare_stream_kernels();
 cudaError_t prepare_front_kernels();
 int router_max_parts();
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
                           const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                           bool pdl, uint32_t debug);
-TcLayout make_tc_layout(int Rmax);
+TcLayout make_tc_layout(int Rmax, int k);
 int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights& w,
                  const Scratch& s);
 cudaError_t prepare_stream_tc_kernels();

@@ -13,6 +13,8 @@ measured on; R rows, hidden H, E experts top-k, expert inter I, shared inter Is)
   r4_h8192_e512k10           R 4,  H 8192, E 512, k 10, I 1024, Is 4096
   r16_h8192_e512k10_neartie  R 16, same shapes; the parity tests inject k-th/(k+1)-th
                              router-logit margins of 1e-2 into these rows
+  r32_h7168_e256k8_similar   R 32, the shapes of the 8-row workload: more than 16 rows per
+                             call (MTP verify / short prefill widths; the default expert form)
 
 Recipe (numpy PCG64 seeded by the workload's seed; bf16 values are float32 draws rounded
 to bf16 by torch):
@@ -66,6 +68,8 @@ WORKLOADS = {
         Workload("r4_h8192_e512k10", TailShape(4, 8192, 512, 10, 1024, 4096), 3, "plain"),
         Workload("r16_h8192_e512k10_neartie", TailShape(16, 8192, 512, 10, 1024, 4096), 4,
                  "neartie"),
+        Workload("r32_h7168_e256k8_similar", TailShape(32, 7168, 256, 8, 2048, 2048), 5,
+                 "similar"),
     ]
 }
 

@@ -93,7 +93,7 @@ def test_null_arguments_rejected_without_device(lib):
     assert lib.moe_tail_launches_per_run(None, 1) == 0
 
 
-@pytest.mark.parametrize("field,value", [("max_rows", 0), ("max_rows", 17), ("hidden", 200),
+@pytest.mark.parametrize("field,value", [("max_rows", 0), ("max_rows", 33), ("hidden", 200),
                                          ("hidden", 384), ("hidden", 2304),
                                          ("top_k", 9), ("expert_inter", 96),
                                          ("expert_inter", 2176),
@@ -105,6 +105,19 @@ def test_unsupported_configs_refused_before_device(lib, field, value):
     cfg = mt.make_config(gen.TailShape(2, 256, 8, 2, 128, 128))
     setattr(cfg, field, value)
     w = mt.WeightPtrs(*([16] * 8))  # never dereferenced: refusal comes first
+    h = ctypes.c_void_p()
+    assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
+        mt.ERR_UNSUPPORTED
+    assert h.value is None
+
+
+@pytest.mark.parametrize("flags,mode,attn", [(16, 0, 0), (1, 0, 0), (8, 0, 0), (0, 1, 0),
+                                             (0, 0, 64)])
+def test_more_than_16_rows_only_in_the_default_form(lib, flags, mode, attn):
+    # mma.sync, cross-checking kernels, fused front, persistent mode, out_proj: 16 rows at most
+    cfg = mt.make_config(gen.TailShape(24, 256, 8, 2, 128, 128, Ha=attn), debug_flags=flags,
+                         mode=mode)
+    w = mt.WeightPtrs(*([16] * 8 + ([0, 16] if attn else [])))  # never dereferenced
     h = ctypes.c_void_p()
     assert lib.moe_tail_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == \
         mt.ERR_UNSUPPORTED

@@ -72,7 +72,7 @@ def test_workload_parity_full_size(name):
             assert max(abs(o[e] - g[e]) for e in o) < 5e-4
         assert abs(float(wts[r].sum()) - 1.0) < 1e-5
     assert tail.status() == 0
-    if wl.kind == "similar":
+    if wl.kind == "similar" and wl.shape.R == 8:
         assert 0.3 <= 1 - nd / ids.size <= 0.5  # ~40% of the picks repeat
     print(name, figs)
 
@@ -362,6 +362,11 @@ from moe_layer_tail_gb300 import MODE_PERSISTENT  # noqa: E402
 @pytest.mark.parametrize("name", list(gen.WORKLOADS))
 def test_persistent_mode_parity_full_size(name):
     wl, d, dev, orc = workload_inputs(name)
+    if wl.shape.R > 16:  # the persistent launch takes 16 rows at most: refused at create
+        with pytest.raises(MoeTailError) as ei:
+            MoeTail(wl.shape, dev, max_rows=wl.shape.R, mode=MODE_PERSISTENT)
+        assert ei.value.code == ERR_UNSUPPORTED
+        return
     tail = MoeTail(wl.shape, dev, max_rows=wl.shape.R, mode=MODE_PERSISTENT)
     assert tail.launches_per_run(wl.shape.R) == 1
     got = run_gpu(tail, d)
