@@ -126,21 +126,25 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
     for (int i = 0; i < 4; ++i) ss += bf16_lo(o[i]) * bf16_lo(o[i]) + bf16_hi(o[i]) * bf16_hi(o[i]);
   }
   const float rstd = 1.0f / sqrtf(block_reduce(ss, false, part) / (float)H + eps);
-  float amax = 0.f;
+  float down = 1.f;
+  if (!np4) {
+    // the f16 copy of the CUDA-core expert form, with one power-of-two scale per row (row
+    // maximum in [2^14, 2^15)); the tensor-core form takes the E2M1 planes below instead
+    float amax = 0.f;
 #pragma unroll
-  for (int q = 0; q < kNormGroups; ++q) {
-    const int c = threadIdx.x + q * kNormThreads;
-    if (c < ng) {
-      const uint4 gv = s_gamma[c];
-      const uint4 nv = make_uint4(norm_bf16x2(rn[q].x, gv.x, rstd), norm_bf16x2(rn[q].y, gv.y, rstd),
-                                  norm_bf16x2(rn[q].z, gv.z, rstd), norm_bf16x2(rn[q].w, gv.w, rstd));
-      amax = fmaxf(amax, group_amax(nv));
+    for (int q = 0; q < kNormGroups; ++q) {
+      const int c = threadIdx.x + q * kNormThreads;
+      if (c < ng) {
+        const uint4 gv = s_gamma[c];
+        const uint4 nv = make_uint4(norm_bf16x2(rn[q].x, gv.x, rstd), norm_bf16x2(rn[q].y, gv.y, rstd),
+                                    norm_bf16x2(rn[q].z, gv.z, rstd), norm_bf16x2(rn[q].w, gv.w, rstd));
+        amax = fmaxf(amax, group_amax(nv));
+      }
     }
+    const int p = f16_block_exp(block_reduce(amax, true, part));
+    down = __uint_as_float((uint32_t)(127 - p) << 23);
+    if (threadIdx.x == 0) n16s[r] = __uint_as_float((uint32_t)(127 + p) << 23);
   }
-  // f16 copy with one power-of-two scale per row (row maximum in [2^14, 2^15))
-  const int p = f16_block_exp(block_reduce(amax, true, part));
-  const float down = __uint_as_float((uint32_t)(127 - p) << 23);
-  if (threadIdx.x == 0) n16s[r] = __uint_as_float((uint32_t)(127 + p) << 23);
   uint4* rno = reinterpret_cast<uint4*>(rnew + (size_t)r * H);
   uint4* no = reinterpret_cast<uint4*>(n_out + (size_t)r * H);
   uint4* n16o = reinterpret_cast<uint4*>(n16 + (size_t)r * H);
@@ -155,7 +159,7 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
                                   norm_bf16x2(rn[q].z, gv.z, rstd), norm_bf16x2(rn[q].w, gv.w, rstd));
       rno[c] = rn[q];
       no[c] = nv;
-      n16o[c] = f16_group(nv, down);
+      if (!np4) n16o[c] = f16_group(nv, down);
       if (np4) {
         // the four E2M1 planes of n for the tensor-core experts: a 32-element block is the
         // groups of four adjacent threads (H / 8 is a multiple of 32, so a warp is either
@@ -343,6 +347,10 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
   pdl_wait();
+  // the expert launch may start as soon as every router CTA is past its wait: its
+  // shared-expert items need only n (written by the norm launch, complete by now), and its
+  // routed items wait for the kCtrRouted word this launch's last CTA sets
+  pdl_trigger();
   for (int i = tid; i < R * cpr; i += kRtThreads) {
     const int r = i / cpr, c = i % cpr;
     cp_async16(sn + r * pitch + c * 16, s.n + (size_t)r * H + k0 + c * 8);
@@ -428,9 +436,15 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   __syncthreads();
   topk_dedup_block<true>(s_logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
                          s.user_list, s.status, R, E, k);
-  if (tid == 0) s.counters[kCtrFrontTicket] = 0u;
-  pdl_trigger();  // the other CTAs have exited: the expert launch may start (launched any
-                  // earlier, its CTAs would share the SMs with this one's top-k)
+  // publish the routing: every thread's table stores, then the word the expert launches
+  // wait for (release at GPU scope)
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    s.counters[kCtrFrontTicket] = 0u;
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&s.counters[kCtrRouted]), "r"(1u)
+                 : "memory");
+  }
 }
 
 cudaError_t launch_router_topk(const Dims& d, const Weights& w, const Scratch& s,

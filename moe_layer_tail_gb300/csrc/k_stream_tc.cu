@@ -200,6 +200,8 @@ struct TcPtrs {
   int* aitem;        // [2] item of each accumulator slot
   uint32_t* tbase;   // tensor-memory base address of the CTA
   int* eflag;        // epilogue: this CTA completed a split shared item
+  int* sD;           // the call's distinct-expert count once the tables are in shared memory
+  uint64_t* tables;  // [1] epilogue warps -> producer: routing tables copied (gate/up launch)
 };
 
 __device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L) {
@@ -217,10 +219,12 @@ __device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L) {
   p.afull = p.wempty + 2;
   p.aempty = p.afull + 2;
   p.drain = p.aempty + 2;
-  p.info = reinterpret_cast<int2*>(p.drain + 2);
+  p.tables = p.drain + 2;
+  p.info = reinterpret_cast<int2*>(p.tables + 1);
   p.aitem = reinterpret_cast<int*>(p.info + kTcMaxStages);
   p.tbase = reinterpret_cast<uint32_t*>(p.aitem + 2);
   p.eflag = reinterpret_cast<int*>(p.tbase + 1);
+  p.sD = p.eflag + 1;
   return p;
 }
 
@@ -432,13 +436,28 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   constexpr uint32_t A = kAccSlots<NMAX>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (PHASE == 0) pdl_wait();
-  const int D = min(max(*s.n_distinct, 1), kMaxPicks);
-  const int P = (PHASE == 0) ? shared_parts(dm, D, (int)gridDim.x) : 1;
-  const int n_items = items_of(PHASE, dm, D) + (dm.Is / 64) * (P - 1);
-  for (int i = threadIdx.x; i < D; i += kTcThreads) sp.t_uniq[i] = s.uniq[i];
-  for (int i = threadIdx.x; i <= D; i += kTcThreads) sp.t_off[i] = s.user_off[i];
-  for (int i = threadIdx.x; i < dm.R * dm.k; i += kTcThreads) sp.t_users[i] = s.user_list[i];
+  // The gate/up launch starts while the router still runs (its shared-expert items need only
+  // n, which the norm launch finished before the router's wait returned): it splits the
+  // shared items by the call's largest possible distinct count, and its routed items wait for
+  // the tables (copied to shared memory by the epilogue warps once the router's last CTA has
+  // published them).  The down launch starts after every gate/up CTA, and waits for the
+  // published routing once before it reads the tables.
+  const int Dmax = min(dm.E, dm.R * dm.k);
+  const int P = (PHASE == 0) ? shared_parts(dm, Dmax, (int)gridDim.x) : 1;
+  const int n_shared = (PHASE == 0) ? (dm.Is / 64) * P : 0;  // items that need no routing
+  int D = 1, n_items = 0;
+  if (PHASE == 1) {
+    if (threadIdx.x == 0 && !wait_count(&s.counters[kCtrRouted], 1u, budget_ns))
+      set_status(s.status, kStatusTimeout);
+    __syncthreads();
+    D = min(max(__ldcg(s.n_distinct), 1), kMaxPicks);
+    n_items = items_of(PHASE, dm, D);
+    for (int i = threadIdx.x; i < D; i += kTcThreads) sp.t_uniq[i] = __ldcg(s.uniq + i);
+    for (int i = threadIdx.x; i <= D; i += kTcThreads) sp.t_off[i] = __ldcg(s.user_off + i);
+    for (int i = threadIdx.x; i < dm.R * dm.k; i += kTcThreads)
+      sp.t_users[i] = __ldcg(s.user_list + i);
+    if (threadIdx.x == 0) *sp.sD = D;
+  }
   Tables tb;
   tb.uniq = sp.t_uniq;
   tb.off = sp.t_off;
@@ -457,6 +476,8 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       mbar_init(&sp.aempty[i], 4);
       mbar_init(&sp.drain[i], 1);
     }
+    mbar_init(sp.tables, 1);
+    if (PHASE == 0) *sp.sD = 1;  // until the routing is known (only routed items read it)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     pdl_trigger();  // the next launch may queue for SMs from now on (it waits on counts)
@@ -484,9 +505,19 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       uint32_t phase = 0, wcnt = 0;
       uint32_t pend = 0u, pend_par = 0u;
       bool skip_first = PHASE == 0 && (debug & kDebugStallFirstStage) && blockIdx.x == 0;
-      int item = (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
-      while (ok && item < n_items) {
-        const int next = (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
+      // a CTA's first item is its index; later ones come from the counter (from gridDim.x on)
+      int item = (int)blockIdx.x;
+      bool have_tables = (PHASE == 1);
+      while (ok) {
+        if (!have_tables && item >= n_shared) {
+          // the first routed item: the routing tables must be in shared memory
+          if (!mbar_wait(sp.tables, 0, budget_ns)) { ok = false; break; }
+          have_tables = true;
+          D = *sp.sD;
+          n_items = n_shared + D * (dm.I / 64);
+        }
+        if (have_tables && item >= n_items) break;
+        const int next = (int)gridDim.x + (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
         const Item it = decode_tc(PHASE, item, dm, tb, D, P);
         const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
         const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : (it.U <= 16) ? 2 : 3;
@@ -602,7 +633,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     for (;;) {
       if (!mbar_wait(&sp.full[stage], phase, budget_ns)) { ok = false; break; }
       const int item = sp.info[stage].x;
-      if (kc == 0 && item >= 0) it = decode_tc(PHASE, item, dm, tb, D, P);
+      if (kc == 0 && item >= 0) it = decode_tc(PHASE, item, dm, tb, *sp.sD, P);
       if (item >= 0 && (it.kind == kRoutedGU || it.kind == kRoutedDN)) {
         const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : (it.U <= 16) ? 2 : 3;
         const int nb = (it.kind == kRoutedGU) ? NMAX : (16 << hsel);
@@ -666,7 +697,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       const int item = sp.info[stage].x;
       if (item < 0) break;
       if (kc == 0) {
-        it = decode_tc(PHASE, item, dm, tb, D, P);
+        it = decode_tc(PHASE, item, dm, tb, *sp.sD, P);
         if (!mbar_wait(&sp.aempty[acnt % A], ((acnt / A) & 1u) ^ 1u, budget_ns)) {
           ok = false;
           break;
@@ -743,6 +774,31 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   } else {
     // --------------------------------------------------------------- epilogue ----
     const int q = warp & 3, ew = warp - kTcWarpEpi;
+    if (PHASE == 0) {
+      // the routing: wait for the tables the router's last CTA publishes, copy them into
+      // shared memory, and release the producer's routed items (none if the wait expired)
+      if (ew == 0 && lane == 0) {
+        int dv = 0;
+        if (wait_count(&s.counters[kCtrRouted], 1u, budget_ns))
+          dv = min(max(__ldcg(s.n_distinct), 1), kMaxPicks);
+        else
+          set_status(s.status, kStatusTimeout);
+        *sp.eflag = dv;
+      }
+      bar_epi();
+      const int dv = *sp.eflag;
+      const int et = 32 * ew + lane;
+      if (dv > 0) {
+        for (int i = et; i < dv; i += 128) sp.t_uniq[i] = __ldcg(s.uniq + i);
+        for (int i = et; i <= dv; i += 128) sp.t_off[i] = __ldcg(s.user_off + i);
+        for (int i = et; i < dm.R * dm.k; i += 128) sp.t_users[i] = __ldcg(s.user_list + i);
+      }
+      bar_epi();
+      if (et == 0) {
+        *sp.sD = dv;
+        mbar_arrive(sp.tables);
+      }
+    }
     for (uint32_t ac = 0;; ++ac) {
       const uint32_t as = ac % A;
       if (!mbar_wait(&sp.afull[as], (ac / A) & 1u, budget_ns)) {
@@ -752,7 +808,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       tc_fence_after();
       const int item = sp.aitem[as];
       if (item < 0) break;
-      const Item it = decode_tc(PHASE, item, dm, tb, D, P);
+      const Item it = decode_tc(PHASE, item, dm, tb, *sp.sD, P);
       const uint32_t lq = (uint32_t)(32 * q) << 16;
       const uint32_t acc0 = tbase + (2u * as) * (uint32_t)NMAX + lq;
       const uint32_t acc1 = tbase + (2u * as + 1u) * (uint32_t)NMAX + lq;
@@ -842,9 +898,9 @@ TcLayout make_tc_layout(int Rmax, int k) {
   L.win_bytes = kWinW + L.nmax * 64;
   const int x_bytes = 2 * 64 * Rmax * 4;
   const int tab_bytes = ((3 * L.tab_picks + 1) * 4 + 127) & ~127;
-  // mbarriers full, ready, empty per stage + wempty, afull, aempty, drain (2 each); the
-  // stages' item words; the accumulator slots' item words; tbase and eflag
-  const int bar_bytes = (3 * kTcMaxStages + 8) * 8 + kTcMaxStages * 8 + 2 * 4 + 4 + 4;
+  // mbarriers full, ready, empty per stage + wempty, afull, aempty, drain (2 each) + tables;
+  // the stages' item words; the accumulator slots' item words; tbase, eflag and sD
+  const int bar_bytes = (3 * kTcMaxStages + 9) * 8 + kTcMaxStages * 8 + 2 * 4 + 4 + 4 + 4;
   const int fixed = 2 * L.win_bytes + x_bytes + tab_bytes + ((bar_bytes + 127) & ~127);
   L.stages = (kSmemLimit - fixed) / L.stage_bytes;
   if (L.stages > kTcMaxStages) L.stages = kTcMaxStages;

@@ -104,6 +104,7 @@ enum : int {
   kCtrGateUp = 0,        // next work item of the gate/up launch
   kCtrDown = 1,          // next work item of the down launch
   kCtrFrontTicket = 2,   // router CTAs done (the last one ranks the experts)
+  kCtrRouted = 3,        // nonzero once the call's routing tables are written (release)
   kCtrSharedGUDone = 4,  // shared-expert gate/up items finished
   kCtrGUDone = 16,       // [kMaxPicks] routed gate/up items finished, per distinct expert
   kCtrMidFlag = 16 + kMaxPicks,  // [kMaxPicks] nonzero: some 32-block of the expert's mid
