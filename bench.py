@@ -71,6 +71,10 @@ def parse_args():
     p.add_argument("--shared-gate", action="store_true",
                    help="the workload with the shared expert's sigmoid gate; the line's config "
                         "says so")
+    p.add_argument("--timeline", action="store_true",
+                   help="also record the per-call milestone timeline (MOE_TAIL_DEBUG_TIMELINE "
+                        "on a separate handle, 20 calls after the timed region; medians in "
+                        "microseconds after the norm launch's start)")
     p.add_argument("--mma-sync", action="store_true",
                    help="the expert stages on the CUDA-core dequantisation + mma.sync "
                         "streaming kernels (MOE_TAIL_DEBUG_MMA_SYNC) instead of the default "
@@ -483,6 +487,23 @@ def run_ours(args, rank, world, local_rank):
                          "d2h_bytes_per_step": 2 * R * shape.H * 2, "steps": ke,
                          "api": "moe_tail_run_host on one pinned host block [x; residual; out] "
                                 "per step (one copy in, one copy out)"}
+
+    if args.timeline and not args.persistent:
+        tt = mt.MoeTail(shape, dev_w[0], max_rows=R, debug_flags=flags | mt.DEBUG_TIMELINE)
+        marks = []
+        for i in range(min(20, nsets)):
+            (tt.run_attn if args.out_proj else tt.run)(x_all[i], res[i], out[i])
+            marks.append(tt.timeline())
+        res.copy_(res0)
+        tt.close()
+        result["timeline_us"] = {
+            n: (round(float(np.median([m[n] for m in marks])), 2)
+                if all(m[n] is not None for m in marks) else None)
+            for n in mt.TL_NAMES}
+        result["timeline_us"]["how"] = ("%%globaltimer stamps of each launch's milestones, one "
+                                        "call at a time on a separate handle (its per-call "
+                                        "reset serialises the calls), median of %d calls"
+                                        % len(marks))
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shape, host_w, xs[W], rs[W],

@@ -110,7 +110,32 @@ enum {
    * using row a column of one multi-column product per expert).  Both forms meet the same
    * parity rule.  MOE_TAIL_DEBUG_FUSED_FRONT implies this form (the fused front writes no
    * activation planes). */
-  MOE_TAIL_DEBUG_MMA_SYNC = 16
+  MOE_TAIL_DEBUG_MMA_SYNC = 16,
+  /* Tracing: every run records %globaltimer readings (nanoseconds) of its launches'
+   * milestones into the handle (MOE_TAIL_TL_* slots below; zeroed by each run before its
+   * first launch, which also keeps consecutive runs from overlapping), for
+   * moe_tail_debug_timeline.  The stamps are recorded by the default expert form; slots of
+   * stages a run does not have stay zero. */
+  MOE_TAIL_DEBUG_TIMELINE = 32
+};
+
+/* Timeline slots: the first (or, for the ends, the last) reading of each milestone. */
+enum {
+  MOE_TAIL_TL_NORM_START = 0,        /* norm launch: first CTA past its wait on the previous */
+  MOE_TAIL_TL_NORM_END = 1,          /* norm launch: last CTA done */
+  MOE_TAIL_TL_ROUTER_START = 2,      /* router launch: first CTA past its wait */
+  MOE_TAIL_TL_TOPK_START = 3,        /* router launch: its last CTA starts top-k and dedup */
+  MOE_TAIL_TL_ROUTED = 4,            /* router launch: routing tables published */
+  MOE_TAIL_TL_GATE_UP_START = 5,     /* gate/up launch: first CTA entered */
+  MOE_TAIL_TL_GATE_UP_FIRST_COPY = 6,/* gate/up launch: first weight copy issued */
+  MOE_TAIL_TL_GATE_UP_ROUTED = 7,    /* gate/up launch: first routed expert's copy issued */
+  MOE_TAIL_TL_GATE_UP_END = 8,       /* gate/up launch: last CTA done */
+  MOE_TAIL_TL_DOWN_START = 9,        /* down launch: first CTA entered */
+  MOE_TAIL_TL_DOWN_FIRST_COPY = 10,  /* down launch: first weight copy issued */
+  MOE_TAIL_TL_DOWN_END = 11,         /* down launch: last CTA done */
+  MOE_TAIL_TL_COMBINE_START = 12,    /* combine launch: first CTA entered */
+  MOE_TAIL_TL_COMBINE_END = 13,      /* combine launch: last output written */
+  MOE_TAIL_TL_SLOTS = 14
 };
 
 typedef struct moe_tail moe_tail_t; /* opaque handle */
@@ -250,6 +275,13 @@ int moe_tail_route_noalloc(const void* x, const void* residual, const void* gamm
                            const void* router_w, int32_t rows, int32_t hidden,
                            int32_t n_experts, int32_t top_k, float rms_eps, int32_t* ids,
                            float* wts, int32_t* n_distinct, int32_t* status, void* stream);
+
+/* The last run's timeline (handles created with MOE_TAIL_DEBUG_TIMELINE; otherwise
+ * MOE_TAIL_ERR_UNSUPPORTED): synchronises the device and copies min(n, MOE_TAIL_TL_SLOTS)
+ * stamps (uint64 nanoseconds of the GPU's global timer, 0 = milestone not reached) to the host
+ * array `stamps`; returns the number copied, or a negative MOE_TAIL_ERR_*.  For tracing and
+ * tests; the pages have no counterpart. */
+int moe_tail_debug_timeline(moe_tail_t* h, uint64_t* stamps, int32_t n);
 
 /* Free the handle and its scratch (synchronises the device first).  NULL is a no-op. */
 void moe_tail_destroy(moe_tail_t* h);

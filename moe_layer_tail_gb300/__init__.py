@@ -38,6 +38,12 @@ DEBUG_NO_PDL = 2
 DEBUG_STALL_FIRST_STAGE = 4
 DEBUG_FUSED_FRONT = 8
 DEBUG_MMA_SYNC = 16
+DEBUG_TIMELINE = 32
+
+# timeline slots (moe_tail_debug_timeline)
+TL_NAMES = ("norm_start", "norm_end", "router_start", "topk_start", "routed", "gate_up_start",
+            "gate_up_first_copy", "gate_up_routed", "gate_up_end", "down_start",
+            "down_first_copy", "down_end", "combine_start", "combine_end")
 
 # moe_attnres_mix launch flags (attnres_mix.h)
 ATTNRES_MIX_PDL = 1
@@ -109,6 +115,8 @@ def load_library(path: str = None):
     lib.moe_tail_set_stage_events.restype = ctypes.c_int
     lib.moe_tail_launches_per_run.argtypes = [P, i32]
     lib.moe_tail_launches_per_run.restype = ctypes.c_int
+    lib.moe_tail_debug_timeline.argtypes = [P, P, i32]
+    lib.moe_tail_debug_timeline.restype = ctypes.c_int
     lib.moe_tail_destroy.argtypes = [P]
     lib.moe_tail_destroy.restype = None
     lib.moe_tail_strerror.argtypes = [ctypes.c_int]
@@ -243,6 +251,19 @@ class MoeTail:
             rc = self._lib.moe_tail_set_stage_events(self._h, arr, len(handles))
         if rc != OK:
             raise MoeTailError(rc, "moe_tail_set_stage_events")
+
+    def timeline(self) -> dict:
+        """The last run's milestone stamps (handles with DEBUG_TIMELINE): microseconds after
+        the norm launch passed its wait, None for a milestone not reached."""
+        import numpy as np
+        buf = np.zeros(len(TL_NAMES), np.uint64)
+        rc = self._lib.moe_tail_debug_timeline(self._h, buf.ctypes.data_as(ctypes.c_void_p),
+                                               len(TL_NAMES))
+        if rc < 0:
+            raise MoeTailError(rc, "moe_tail_debug_timeline")
+        t0 = int(buf[0])
+        return {n: (None if int(v) == 0 else (int(v) - t0) / 1000.0)
+                for n, v in zip(TL_NAMES, buf)}
 
     def launches_per_run(self, rows: int) -> int:
         return int(self._lib.moe_tail_launches_per_run(self._h, int(rows)))

@@ -77,7 +77,8 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
               float* __restrict__ n16s, uint32_t* __restrict__ counters, int H, float eps,
               const __nv_bfloat16* __restrict__ wsg, float* __restrict__ sgate,
               const float* __restrict__ xpart, int Pk, size_t part_stride,
-              uint8_t* __restrict__ np4, uint8_t* __restrict__ np4s) {
+              uint8_t* __restrict__ np4, uint8_t* __restrict__ np4s,
+              unsigned long long* __restrict__ tl) {
   extern __shared__ uint4 s_gamma[];  // [H / 8]
   __shared__ float part[kNormThreads / 32];
   const int r = blockIdx.x;
@@ -86,6 +87,7 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   for (int c = threadIdx.x; c < ng; c += kNormThreads) s_gamma[c] = __ldg(g4 + c);
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) tl_first(tl, kTlNormStart);
   if (r == 0)  // work counters, tickets and per-expert progress of this call
     for (int i = threadIdx.x; i < kCtrWords; i += kNormThreads) counters[i] = 0u;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * H);
@@ -210,6 +212,10 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
     const float z = block_reduce(zg, false, part);
     if (threadIdx.x == 0) sgate[r] = 1.0f / (1.0f + expf(-z));
   }
+  if (tl) {
+    __syncthreads();
+    if (threadIdx.x == 0) tl_last(tl, kTlNormEnd);
+  }
 }
 
 cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
@@ -219,7 +225,7 @@ cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
   return launch_k(k_add_rmsnorm, dim3(d.R), dim3(kNormThreads), (size_t)d.H * 2, st, pdl, x,
                   residual, w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps, w.wsg,
                   s.sgate, xpart, d.Pk, (size_t)d.Rmax * d.H, planes ? s.np4 : nullptr,
-                  planes ? s.np4s : nullptr);
+                  planes ? s.np4s : nullptr, s.tl);
 }
 
 // ------------------------------------------------------------------- router GEMV ----
@@ -347,6 +353,7 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
   pdl_wait();
+  if (tid == 0) tl_first(s.tl, kTlRouterStart);
   // the expert launch may start as soon as every router CTA is past its wait: its
   // shared-expert items need only n (written by the norm launch, complete by now), and its
   // routed items wait for the kCtrRouted word this launch's last CTA sets
@@ -434,6 +441,7 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
     }
   }
   __syncthreads();
+  if (tid == 0) tl_first(s.tl, kTlTopkStart);
   topk_dedup_block<true>(s_logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
                          s.user_list, s.status, R, E, k);
   // publish the routing: every thread's table stores, then the word the expert launches
@@ -444,6 +452,7 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
     s.counters[kCtrFrontTicket] = 0u;
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&s.counters[kCtrRouted]), "r"(1u)
                  : "memory");
+    tl_first(s.tl, kTlRouted);
   }
 }
 

@@ -303,6 +303,7 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
           bool gated) {
   if (!wait_tiles) pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) tl_first(s.tl, kTlCombineStart);
   const int H = dm.H;
   const int ng = H / 8;  // a multiple of 32: whole warps lie in one row
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -320,6 +321,7 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
     __syncwarp();  // orders the other lanes' loads after lanes 0 and 16's acquires
   }
   combine_one(dm, s, r, c, out, residual, gated);
+  if ((threadIdx.x & 31) == 0) tl_last(s.tl, kTlCombineEnd);
 }
 
 __device__ __forceinline__ void combine_one(const Dims& dm, const Scratch& s, int r, int c,

@@ -434,6 +434,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   const TcPtrs sp = tc_carve(smem, lay);
   const int S = lay.stages;
   constexpr uint32_t A = kAccSlots<NMAX>;
+  if (threadIdx.x == 0) tl_first(s.tl, PHASE == 0 ? kTlGateUpStart : kTlDownStart);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // The gate/up launch starts while the router still runs (its shared-expert items need only
@@ -557,6 +558,8 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
           sp.info[stage] = make_int2(item, 0);
           mbar_expect_tx(&sp.full[stage], bytes);
+          tl_first(s.tl, PHASE == 0 ? kTlGateUpFirstCopy : kTlDownFirstCopy);
+          if (PHASE == 0 && it.kind == kRoutedGU) tl_first(s.tl, kTlGateUpRouted);
           if (it.kind == kRoutedGU) {
             // the 64 gate and 64 up rows in one copy (3-D box over [2E][I][H/2])
             const int x = kc * (kChunkF4 / 2);
@@ -833,6 +836,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   // every role ends here: tensor memory is freed once all of them are done with it
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) tl_last(s.tl, PHASE == 0 ? kTlGateUpEnd : kTlDownEnd);
   if (warp == kTcWarpMma) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),

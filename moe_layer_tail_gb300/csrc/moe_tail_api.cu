@@ -73,6 +73,8 @@ extern "C" const char* moe_tail_last_cuda_error(void) { return g_cuda_err; }
 static_assert(MOE_TAIL_DEBUG_STALL_FIRST_STAGE == (int)kDebugStallFirstStage,
               "debug bit values agree");
 static_assert(MOE_TAIL_DEBUG_MMA_SYNC == (int)kDebugMmaSync, "debug bit values agree");
+static_assert(MOE_TAIL_DEBUG_TIMELINE == (int)kDebugTimeline, "debug bit values agree");
+static_assert(MOE_TAIL_TL_SLOTS == (int)kTlSlots, "timeline slots agree");
 
 // The expert stages run on the tcgen05 kernels unless a debug flag picks another form (the
 // mma.sync streaming kernels, the cross-checking CUDA-core kernels, or the fused front, which
@@ -159,6 +161,8 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s, size_t* 
   s->np4s = (uint8_t*)take(128 * H / 32);
   s->mid4 = (uint8_t*)take(4 * P * I / 2);
   s->mid4s = (uint8_t*)take((4 * P + 128) * I / 32);
+  s->tl = (c->debug_flags & MOE_TAIL_DEBUG_TIMELINE) ? (unsigned long long*)take(kTlSlots * 8)
+                                                     : nullptr;
   s->status = (int32_t*)take(4);
   s->counters = (uint32_t*)take(kCtrWords * 4);
   if (n_canary) *n_canary = nc < kMaxCanaries ? nc : kMaxCanaries;
@@ -306,6 +310,7 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   const uint64_t budget_ns =
       (uint64_t)(h->cfg.wait_budget_us ? h->cfg.wait_budget_us : 100000u) * 1000ull;
   const float* xpart = nullptr;
+  if (h->s.tl && (e = cudaMemsetAsync(h->s.tl, 0, kTlSlots * 8, st))) return cuda_fail(e);
   if (h->cfg.mode == MOE_TAIL_MODE_PERSISTENT) {
     // the whole call in one cooperative launch (such a handle has no out_proj stage)
     MT_STAGE(launch_persistent(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
@@ -457,6 +462,16 @@ extern "C" int moe_tail_debug_routing(moe_tail_t* h, int32_t* ids, float* wts,
     e = cudaMemcpyAsync(n_distinct, h->s.n_distinct, 4, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
+}
+
+extern "C" int moe_tail_debug_timeline(moe_tail_t* h, uint64_t* stamps, int32_t n) {
+  if (!h || !stamps || n < 0) return MOE_TAIL_ERR_INVALID_ARG;
+  if (!h->s.tl) return MOE_TAIL_ERR_UNSUPPORTED;
+  cudaError_t e = cudaDeviceSynchronize();
+  const int m = n < kTlSlots ? n : kTlSlots;
+  if (e == cudaSuccess && m > 0)
+    e = cudaMemcpy(stamps, h->s.tl, (size_t)m * 8, cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? m : cuda_fail(e);
 }
 
 extern "C" void moe_tail_destroy(moe_tail_t* h) {

@@ -91,6 +91,8 @@ struct Scratch {
   uint8_t* mid4;         // [4 Rmax k, I/2] E2M1 planes of mid (row 4 slot + p, slot = the
                          // pick's position in user_list)
   uint8_t* mid4s;        // [4 Rmax k + 128, I/32] their E8M0 scales (128 zero rows after)
+  unsigned long long* tl;  // [kTlSlots] %globaltimer stamps of the last run, or null (the
+                           // timeline debug flag off)
   int32_t* status;       // [1] sticky device status word
   uint32_t* counters;    // [kCtrWords] work counters, tickets and per-expert progress
 };
@@ -98,6 +100,27 @@ struct Scratch {
 // Debug bits the kernels read (same values as MOE_TAIL_DEBUG_* in moe_tail.h).
 constexpr uint32_t kDebugStallFirstStage = 4u;
 constexpr uint32_t kDebugMmaSync = 16u;
+constexpr uint32_t kDebugTimeline = 32u;
+
+// Timeline slots (same order as MOE_TAIL_TL_* in moe_tail.h): the first or last %globaltimer
+// reading of each milestone of a run, recorded when the handle has a timeline buffer.
+enum : int {
+  kTlNormStart = 0,   // norm launch: first CTA past its wait on the previous launch
+  kTlNormEnd,         // norm launch: last CTA done
+  kTlRouterStart,     // router launch: first CTA past its wait
+  kTlTopkStart,       // router launch: its last CTA starts top-k and the dedup
+  kTlRouted,          // router launch: routing published
+  kTlGateUpStart,     // gate/up launch: first CTA entered
+  kTlGateUpFirstCopy, // gate/up launch: first weight copy issued
+  kTlGateUpRouted,    // gate/up launch: first routed expert's weight copy issued
+  kTlGateUpEnd,       // gate/up launch: last CTA done
+  kTlDownStart,       // down launch: first CTA entered
+  kTlDownFirstCopy,   // down launch: first weight copy issued
+  kTlDownEnd,         // down launch: last CTA done
+  kTlCombineStart,    // combine launch: first CTA entered
+  kTlCombineEnd,      // combine launch: last output written
+  kTlSlots
+};
 
 // counters[] words (all zeroed at the start of every call by the front)
 enum : int {
@@ -223,6 +246,15 @@ __device__ __forceinline__ float e2m1_value(uint32_t code) {
       : "=r"(h)
       : "r"(code & 0xFu));
   return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
+// Timeline stamps (only when the handle records a timeline): the first reading of a slot
+// (the word is zero until then), or the latest.
+__device__ __forceinline__ void tl_first(unsigned long long* tl, int slot) {
+  if (tl) atomicCAS(tl + slot, 0ull, (unsigned long long)globaltimer());
+}
+__device__ __forceinline__ void tl_last(unsigned long long* tl, int slot) {
+  if (tl) atomicMax(tl + slot, (unsigned long long)globaltimer());
 }
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bit) {

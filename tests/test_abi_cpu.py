@@ -56,6 +56,20 @@ def test_binding_constants_match_header():
         "MOE_TAIL_STATUS_BAD_TILE"}
 
 
+def test_timeline_slots_match_header():
+    vals = header_enum_values()
+    slots = sorted((v, k) for k, v in vals.items()
+                   if k.startswith("MOE_TAIL_TL_") and k != "MOE_TAIL_TL_SLOTS")
+    assert [v for v, _ in slots] == list(range(vals["MOE_TAIL_TL_SLOTS"]))
+    assert [k[len("MOE_TAIL_TL_"):].lower() for _, k in slots] == list(mt.TL_NAMES)
+
+
+def test_timeline_refused_without_its_flag(lib):
+    import numpy as np
+    buf = np.zeros(14, np.uint64)
+    assert lib.moe_tail_debug_timeline(None, buf.ctypes.data, 14) == mt.ERR_INVALID_ARG
+
+
 def test_weight_struct_fields_match_header():
     src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "moe_tail.h")).read(),
                  flags=re.S)

@@ -157,3 +157,20 @@ def test_device_wait_timeout_is_reported_and_context_survives(flags):
     bad.close()
     # a healthy handle on the same device still matches the oracle
     _check(shape, d, flags=flags)
+
+
+def test_timeline_milestones_in_order():
+    """The tracing option: every milestone of a default-form call recorded, in causal order."""
+    from moe_layer_tail_gb300 import DEBUG_TIMELINE
+    shape, d = _small(25, R=8, H=1024, E=32, k=4, I=512, Is=256, kind="similar")
+    tail, _, _, _, _ = _check(shape, d, flags=DEBUG_TIMELINE)
+    t = tail.timeline()
+    assert all(v is not None for v in t.values()), t
+    assert t["norm_start"] == 0.0
+    for a, b in [("norm_start", "norm_end"), ("router_start", "topk_start"),
+                 ("topk_start", "routed"), ("gate_up_start", "gate_up_first_copy"),
+                 ("routed", "gate_up_routed"), ("gate_up_routed", "gate_up_end"),
+                 ("down_start", "down_first_copy"), ("down_first_copy", "down_end"),
+                 ("combine_start", "combine_end"), ("down_end", "combine_end")]:
+        assert t[a] <= t[b], (a, b, t)
+    assert t["combine_end"] < 1e4  # microseconds: one call
