@@ -473,20 +473,32 @@ def run_ours(args, rank, world, local_rank):
             hb[0].copy_(torch.from_numpy(xs[W + i].view(np.int16)).view(torch.bfloat16))
             hb[1].copy_(torch.from_numpy(rs[W + i].view(np.int16)).view(torch.bfloat16))
             blocks.append(hb)
+        # the C ABI called with prebuilt arguments (no Python tensor work inside the loop)
+        import ctypes
+        lib = mt.load_library()
+        st_e2e = torch.cuda.Stream()
+        sh = ctypes.c_void_p(st_e2e.cuda_stream)
+        act = R * shape.H * 2
+        calls = [(tails[(W + i) % L].handle, ctypes.c_void_p(hb.data_ptr()),
+                  ctypes.c_void_p(hb.data_ptr() + act), ctypes.c_void_p(hb.data_ptr() + 2 * act),
+                  R, sh) for i, hb in enumerate(blocks)]
         warm = blocks[0].clone().pin_memory()
-        tails[0].run_host(warm[0], warm[1], warm[2])  # warm the staging path
+        for t in tails:  # the first call on each handle captures its graph
+            t.run_host(warm[0], warm[1], warm[2], stream=st_e2e)
         torch.cuda.synchronize()
+        fn = lib.moe_tail_run_host
         ts = time.perf_counter()
-        for i in range(ke):
-            hb = blocks[i]
-            tails[(W + i) % L].run_host(hb[0], hb[1], hb[2])
+        for a in calls:
+            if fn(*a) != 0:
+                raise RuntimeError("moe_tail_run_host failed")
         te = time.perf_counter()
         e2e_us = (te - ts) * 1e6 / ke
         result["e2e"] = {"value": round(e2e_us / world, 3), "unit": UNIT,
                          "h2d_bytes_per_step": 2 * R * shape.H * 2,
                          "d2h_bytes_per_step": 2 * R * shape.H * 2, "steps": ke,
                          "api": "moe_tail_run_host on one pinned host block [x; residual; out] "
-                                "per step (one copy in, one copy out)"}
+                                "per step on a non-default stream (a replayed graph of copy in, "
+                                "the call's launches, copy out)"}
 
     if args.timeline and not args.persistent:
         tt = mt.MoeTail(shape, dev_w[0], max_rows=R, debug_flags=flags | mt.DEBUG_TIMELINE)

@@ -211,7 +211,10 @@ int moe_tail_run_attn(moe_tail_t* h, const void* attn, void* residual, void* out
  * Pinned host memory gives asynchronous copies; pageable memory works too.  When the three
  * buffers are one block [x; residual; out] (residual_host = x_host + rows*H*2 bytes and
  * out_host = residual_host + rows*H*2), x and residual go in one copy and residual and out
- * come back in one copy. */
+ * come back in one copy; if that block is page-locked and `stream` is not a default stream,
+ * the first such call for a row count captures [copy in, the call's launches, copy out] as a
+ * CUDA graph on `stream` and every later one replays it with its copies pointed at the
+ * call's block (so the first call must not run inside another capture). */
 int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host, void* out_host,
                       int32_t rows, void* stream);
 

@@ -44,6 +44,11 @@ struct moe_tail {
   int n_ev;
   size_t canary_off[kMaxCanaries];  // slab offsets of the guard words after each buffer
   int n_canary;
+  // moe_tail_run_host on page-locked buffers: one graph per row count of [copy in, the
+  // call's launches, copy out], its two copy nodes re-pointed at every run's buffers
+  cudaGraph_t hgraph[kMaxRows + 1];
+  cudaGraphExec_t hexec[kMaxRows + 1];
+  cudaGraphNode_t hin[kMaxRows + 1], hout[kMaxRows + 1];
 };
 
 static thread_local char g_cuda_err[256];
@@ -397,6 +402,62 @@ extern "C" int moe_tail_run_attn(moe_tail_t* h, const void* attn, void* residual
   return run_impl(h, nullptr, attn, residual, out, rows, stream);
 }
 
+static bool page_locked(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // pageable memory may report an error on some drivers: not sticky
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+// Capture [copy in, the call, copy out] on `st` for `rows` rows once, keeping the copy nodes.
+static cudaError_t build_host_graph(moe_tail_t* h, int rows, const void* in_host, void* out_host,
+                                    char* din, char* dout, size_t bytes2, cudaStream_t st) {
+  cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return e;
+  cudaError_t e1 = cudaMemcpyAsync(din, in_host, bytes2, cudaMemcpyHostToDevice, st);
+  const int rc = (e1 == cudaSuccess)
+                     ? run_impl(h, din, nullptr, din + bytes2 / 2, din + bytes2, rows, st)
+                     : MOE_TAIL_ERR_CUDA;
+  cudaError_t e2 = cudaMemcpyAsync(out_host, dout, bytes2, cudaMemcpyDeviceToHost, st);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(st, &g);
+  if (e == cudaSuccess && (e1 != cudaSuccess || rc != MOE_TAIL_OK || e2 != cudaSuccess))
+    e = cudaErrorUnknown;
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return e;
+  }
+  // the two copy nodes: the one that writes device memory and the one that reads it
+  size_t n = 0;
+  cudaGraphGetNodes(g, nullptr, &n);
+  cudaGraphNode_t nodes[64];
+  if (n > 64) n = 64;
+  e = cudaGraphGetNodes(g, nodes, &n);
+  cudaGraphNode_t gin = nullptr, gout = nullptr;
+  for (size_t i = 0; e == cudaSuccess && i < n; ++i) {
+    cudaGraphNodeType t;
+    if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess || t != cudaGraphNodeTypeMemcpy) continue;
+    cudaMemcpy3DParms p = {};
+    if (cudaGraphMemcpyNodeGetParams(nodes[i], &p) != cudaSuccess) continue;
+    if (p.kind == cudaMemcpyHostToDevice) gin = nodes[i];
+    else if (p.kind == cudaMemcpyDeviceToHost) gout = nodes[i];
+  }
+  cudaGraphExec_t ex = nullptr;
+  if (e == cudaSuccess && (!gin || !gout)) e = cudaErrorUnknown;
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&ex, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return e;
+  }
+  h->hgraph[rows] = g;
+  h->hexec[rows] = ex;
+  h->hin[rows] = gin;
+  h->hout[rows] = gout;
+  return cudaSuccess;
+}
+
 extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host,
                                  void* out_host, int32_t rows, void* stream) {
   if (!h || !x_host || !residual_host || !out_host) return MOE_TAIL_ERR_INVALID_ARG;
@@ -408,8 +469,27 @@ extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residu
   char* dx = (char*)h->stage;
   char* dres = dx + bytes;
   char* dout = dres + bytes;
+  const bool in_block = (const char*)residual_host == (const char*)x_host + bytes;
+  const bool out_block = (char*)out_host == (char*)residual_host + bytes;
   cudaError_t e;
-  if ((const char*)residual_host == (const char*)x_host + bytes) {
+  if (in_block && out_block && st != nullptr && st != cudaStreamLegacy && st != cudaStreamPerThread &&
+      h->n_ev == 0 && page_locked(x_host)) {
+    // one [x; residual; out] block in page-locked memory: replay this row count's graph
+    if (!h->hexec[rows]) {
+      e = build_host_graph(h, rows, x_host, residual_host, dx, dres, 2 * bytes, st);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = cudaGraphExecMemcpyNodeSetParams1D(h->hexec[rows], h->hin[rows], dx, x_host, 2 * bytes,
+                                           cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaGraphExecMemcpyNodeSetParams1D(h->hexec[rows], h->hout[rows], residual_host, dres,
+                                             2 * bytes, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaGraphLaunch(h->hexec[rows], st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) h->last_rows = rows;
+    return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
+  }
+  if (in_block) {
     e = cudaMemcpyAsync(dx, x_host, 2 * bytes, cudaMemcpyHostToDevice, st);
   } else {
     e = cudaMemcpyAsync(dx, x_host, bytes, cudaMemcpyHostToDevice, st);
@@ -418,7 +498,7 @@ extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residu
   if (e != cudaSuccess) return cuda_fail(e);
   int rc = moe_tail_run(h, dx, dres, dout, rows, stream);
   if (rc) return rc;
-  if ((char*)out_host == (char*)residual_host + bytes) {
+  if (out_block) {
     e = cudaMemcpyAsync(residual_host, dres, 2 * bytes, cudaMemcpyDeviceToHost, st);
   } else {
     e = cudaMemcpyAsync(residual_host, dres, bytes, cudaMemcpyDeviceToHost, st);
@@ -480,6 +560,10 @@ extern "C" void moe_tail_destroy(moe_tail_t* h) {
   cudaGetDevice(&cur);
   if (cur != h->device) cudaSetDevice(h->device);
   cudaDeviceSynchronize();
+  for (int r = 0; r <= kMaxRows; ++r) {
+    if (h->hexec[r]) cudaGraphExecDestroy(h->hexec[r]);
+    if (h->hgraph[r]) cudaGraphDestroy(h->hgraph[r]);
+  }
   cudaFree(h->slab);
   cudaFree(h->stage);
   if (cur >= 0 && cur != h->device) cudaSetDevice(cur);

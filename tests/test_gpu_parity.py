@@ -309,6 +309,31 @@ def test_run_host_matches_device_run():
     assert np.array_equal(bf16_tensor_to_bits(res), res_d)
 
 
+def test_run_host_block_graph_replays_match_device_runs():
+    """One page-locked [x; residual; out] block per call on a non-default stream: the entry
+    point replays a captured graph (one per row count) with its copies re-pointed at each
+    call's block; every call matches the device-buffer run bit for bit."""
+    shape, d = _small(14, R=4, H=512, E=12, k=3, I=256, Is=128)
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    tail = MoeTail(shape, dev, max_rows=4)
+    stream = torch.cuda.Stream()
+    H = shape.H
+    for rows, seed in ((4, 1), (4, 2), (2, 3), (4, 4), (2, 5)):
+        a = gen.make_activations(shape, 500 + seed, "plain", rows=rows)
+        dd = dict(d)
+        dd["x"], dd["residual"] = a["x"], a["residual"]
+        out_d, res_d, *_ = run_gpu(tail, dd, rows)
+        blk = torch.empty((3, rows, H), dtype=torch.bfloat16).pin_memory()
+        blk[0].copy_(torch.from_numpy(a["x"].view(np.int16)).view(torch.bfloat16))
+        blk[1].copy_(torch.from_numpy(a["residual"].view(np.int16)).view(torch.bfloat16))
+        tail.run_host(blk[0], blk[1], blk[2], rows=rows, stream=stream)
+        assert np.array_equal(bf16_tensor_to_bits(blk[2]), out_d), (rows, seed)
+        assert np.array_equal(bf16_tensor_to_bits(blk[1]), res_d), (rows, seed)
+    ids, _, _ = tail.routing(2)
+    assert ids.shape == (2, shape.k)
+    assert tail.status() == 0
+
+
 def test_run_rejects_bad_arguments():
     shape, d = _small(13, R=2)
     dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
