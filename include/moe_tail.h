@@ -159,7 +159,12 @@ typedef struct {
 } moe_tail_config_t;
 
 /* Weights are BORROWED device pointers: the caller keeps them alive and unmodified until
- * moe_tail_destroy.  The library never copies or writes them. */
+ * moe_tail_destroy.  The library never writes them.  One exception to reading them in place:
+ * the default (tensor-core) expert form reads the routed experts' E8M0 scales (w13_scales,
+ * w2_scales) from a copy made at create in the layout the block-scaled MMAs take them from
+ * (groups of 4 blocks x 128 rows per 512 bytes), owned by the handle: 1/16 of the MXFP4 code
+ * bytes, e.g. 352 MB for 256 experts at H 7168, I 2048.  A caller that changes those scales
+ * after create calls moe_tail_refresh_scales before the next run. */
 typedef struct {
   const void* gamma;       /* bf16 [H] */
   const void* router_w;    /* bf16 [E, H] */
@@ -285,6 +290,13 @@ int moe_tail_route_noalloc(const void* x, const void* residual, const void* gamm
  * array `stamps`; returns the number copied, or a negative MOE_TAIL_ERR_*.  For tracing and
  * tests; the pages have no counterpart. */
 int moe_tail_debug_timeline(moe_tail_t* h, uint64_t* stamps, int32_t n);
+
+/* Re-make the handle's copy of w13_scales and w2_scales (see moe_tail_weights_t) from the
+ * borrowed arrays, enqueued on `stream` (a cudaStream_t; NULL = legacy default stream):
+ * later runs on that stream read the new scales.  A no-op returning MOE_TAIL_OK for forms
+ * that read the scales in place (the debug forms, the persistent mode).  Returns
+ * MOE_TAIL_ERR_INVALID_ARG for a NULL handle, MOE_TAIL_ERR_CUDA if the launch fails. */
+int moe_tail_refresh_scales(moe_tail_t* h, void* stream);
 
 /* Free the handle and its scratch (synchronises the device first).  NULL is a no-op. */
 void moe_tail_destroy(moe_tail_t* h);

@@ -117,6 +117,8 @@ def load_library(path: str = None):
     lib.moe_tail_launches_per_run.restype = ctypes.c_int
     lib.moe_tail_debug_timeline.argtypes = [P, P, i32]
     lib.moe_tail_debug_timeline.restype = ctypes.c_int
+    lib.moe_tail_refresh_scales.argtypes = [P, P]
+    lib.moe_tail_refresh_scales.restype = ctypes.c_int
     lib.moe_tail_destroy.argtypes = [P]
     lib.moe_tail_destroy.restype = None
     lib.moe_tail_strerror.argtypes = [ctypes.c_int]
@@ -264,6 +266,13 @@ class MoeTail:
         t0 = int(buf[0])
         return {n: (None if int(v) == 0 else (int(v) - t0) / 1000.0)
                 for n, v in zip(TL_NAMES, buf)}
+
+    def refresh_scales(self, stream=None) -> None:
+        """Re-read w13s and w2s into the handle's copy in scale-factor atoms (after the
+        caller changed them in place); enqueued on `stream`."""
+        rc = self._lib.moe_tail_refresh_scales(self._h, _stream_handle(stream))
+        if rc != OK:
+            raise MoeTailError(rc, "moe_tail_refresh_scales")
 
     def launches_per_run(self, rows: int) -> int:
         return int(self._lib.moe_tail_launches_per_run(self._h, int(rows)))

@@ -77,7 +77,7 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
               float* __restrict__ n16s, uint32_t* __restrict__ counters, int H, float eps,
               const __nv_bfloat16* __restrict__ wsg, float* __restrict__ sgate,
               const float* __restrict__ xpart, int Pk, size_t part_stride,
-              uint8_t* __restrict__ np4, uint8_t* __restrict__ np4s,
+              uint8_t* __restrict__ np4, uint8_t* __restrict__ np4a,
               unsigned long long* __restrict__ tl) {
   extern __shared__ uint4 s_gamma[];  // [H / 8]
   __shared__ float part[kNormThreads / 32];
@@ -196,7 +196,7 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
           }
           const size_t prow = (size_t)(4 * r + pl);
           reinterpret_cast<uint32_t*>(np4 + prow * (H / 2))[c] = code;
-          if ((c & 3) == 0) np4s[prow * (H / 32) + c / 4] = (uint8_t)(e + 127);
+          if ((c & 3) == 0) np4a[sf_atom_offset((int)prow, c / 4)] = (uint8_t)(e + 127);
         }
       }
       if (wsg) {
@@ -225,7 +225,7 @@ cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
   return launch_k(k_add_rmsnorm, dim3(d.R), dim3(kNormThreads), (size_t)d.H * 2, st, pdl, x,
                   residual, w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps, w.wsg,
                   s.sgate, xpart, d.Pk, (size_t)d.Rmax * d.H, planes ? s.np4 : nullptr,
-                  planes ? s.np4s : nullptr, s.tl);
+                  planes ? s.np4a : nullptr, s.tl);
 }
 
 // ------------------------------------------------------------------- router GEMV ----

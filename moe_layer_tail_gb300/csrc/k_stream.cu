@@ -817,7 +817,8 @@ int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scr
 }
 
 // Tensor maps of the tensor-core streaming kernels: the weight and bf16 activation maps of
-// the CUDA-core form, plus the E2M1 planes of n and mid and their scale windows.  Returns 0,
+// the CUDA-core form, plus the E2M1 planes of n and mid (their scales, like the weights',
+// travel as scale-factor atoms by plain bulk copies).  Returns 0,
 // -1 (no encoder) or -2 (encoding failed).
 int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights& w,
                  const Scratch& s) {
@@ -828,13 +829,11 @@ int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights
   out->ws2 = sm.ws2;
   out->n = sm.n;
   out->ms = sm.ms;
-  out->w13s = sm.w13s;
-  out->w2s = sm.w2s;
   out->lay = make_tc_layout(d.Rmax, d.k);
   const uint32_t nmax = (uint32_t)out->lay.nmax;
   const uint64_t H = d.H, I = d.I, R4 = 4ull * d.Rmax, P4 = 4ull * d.Rmax * d.k;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
+  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
   {
     // gate and up rows of a stage in one 3-D box each: w13 as [2E][I][H/2] bytes, the shared
     // expert's ws13 as [2][Is][H] bf16
@@ -857,16 +856,10 @@ int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights
   }
   // rows past 4 Rmax (planes) and 4 P (mid planes) read as zeros
   if (encode_2d(enc, &out->np4, U8, s.np4, H / 2, R4, H / 2, 128, nmax, SW)) return -2;
-  if (H > (uint64_t)kWinK &&
-      encode_2d(enc, &out->np4s, U8, s.np4s, H / 32, 128, H / 32, 64, nmax, NS))
-    return -2;
   for (int i = 0; i < 4; ++i) {
     const uint32_t rows = 16u << i;
     if (rows > nmax) break;
     if (encode_2d(enc, &out->mid4[i], U8, s.mid4, I / 2, P4, I / 2, 128, rows, SW)) return -2;
-    if (I > (uint64_t)kWinK &&
-        encode_2d(enc, &out->mid4s[i], U8, s.mid4s, I / 32, P4 + 128, I / 32, 64, rows, NS))
-      return -2;
   }
   return 0;
 }

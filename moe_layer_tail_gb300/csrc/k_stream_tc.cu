@@ -25,22 +25,27 @@
 // within the row), and the epilogue adds the four column sums in plane order.  The norm
 // launch writes the planes of n; the gate/up epilogue writes the planes of mid.
 //
-// Machine mapping (sm_103a), one CTA of 288 threads per SM.  A tcgen05.mma or tcgen05.cp
+// Scales: the MMAs read E8M0 scales from tensor memory, brought there by tcgen05.cp from
+// scale-factor atoms in shared memory (512 bytes: 4 blocks of 128 rows, see sf_atom_offset).
+// Every scale a stage needs arrives as such atoms with the stage: the weights' from a copy of
+// w13s / w2s laid out in atoms once at create (1 KB of contiguous bytes per stage and weight
+// tile), the activation planes' as written in atoms by the launch that makes them (the norm for
+// n, the gate/up epilogue for mid, per distinct expert).  So no thread rearranges scales on the
+// way, and the scale bytes stream as whole kilobytes instead of 64-byte pieces of 128 rows.
+//
+// Machine mapping (sm_103a), one CTA of 224 threads per SM.  A tcgen05.mma or tcgen05.cp
 // costs its issuing thread a fixed ~75 ns whatever N is (measured on GB300), while the
 // tensor core keeps up with several issuers at once; so two threads issue, each owning half
 // of every stage's K and an accumulator of its own, and nothing else runs on them:
-//   * warp 0, lane 0 -- the producer: per stage one or two TMA loads of a 128-row x 128-byte
-//     weight tile (L2 evict-first), one TMA load of the activation tile (planes, or bf16
-//     rows for the shared expert), and every 8 stages the E8M0 scales of the next 2048 K
-//     elements of weights and planes into a two-slot window ring;
+//   * warp 0, lane 0 -- the producer: per stage one TMA load of a 128-row x 128-byte weight
+//     tile (L2 evict-first), one TMA load of the activation tile (planes, or bf16 rows for the
+//     shared expert), and for a routed item the stage's weight and activation scale atoms
+//     (two bulk copies of 1 KB);
 //   * warps 1, 2 (lane 0) -- the MMA issuers: issuer h copies scale-factor atom h of the
 //     stage's weights and activations into its own tensor-memory columns (tcgen05.cp) and
 //     issues the two MMAs of K steps 2h, 2h + 1 (K = 64 FP4 or 16 bf16 elements each; 32
 //     bytes of every operand row) into its accumulator, then commits the stage;
-//   * warps 3, 4 -- the scale warps: rearrange a stage's E8M0 bytes from the window into the
-//     atoms tcgen05.cp reads (32 rows x 16 bytes, row m of 128 at byte 16 (m mod 32) +
-//     4 (m / 32) + block), warp 3 for the weight rows, warp 4 for the activation planes;
-//   * warps 5..8 -- the epilogue: tcgen05.ld of both accumulators (TMEM lane = weight row)
+//   * warps 3..6 -- the epilogue: tcgen05.ld of both accumulators (TMEM lane = weight row)
 //     added in issuer order, plane sums, SiLU * up through a shared-memory exchange between
 //     the gate and up lane quadrants, planes of mid, stores, and the counts the next launch
 //     waits for;
@@ -53,13 +58,13 @@
 
 namespace mtail {
 
-// warps: producer, two MMA issuers, two scale warps, four epilogue warps
-constexpr int kTcWarpMma = 1, kTcWarpScale = 3, kTcWarpEpi = 5;
-constexpr int kTcThreads = 9 * 32;
+// warps: producer, two MMA issuers, four epilogue warps (warp mod 4 = their lane quadrant)
+constexpr int kTcWarpMma = 1, kTcWarpEpi = 3;
+constexpr int kTcThreads = 7 * 32;
 constexpr int kTcSfBytes = 2048;    // per stage: A atoms 2 x 512 B, B atoms 2 x 512 B
 constexpr int kTcCols = 512;        // tensor-memory columns of a CTA
 constexpr int kTcSfCol = 256;       // first scale-factor column (accumulators below)
-constexpr int kTcMaxStages = 10;    // 16 scale-factor columns each: 256 + 160 <= 512
+constexpr int kTcMaxStages = 12;    // 16 scale-factor columns each: 256 + 192 <= 512
 constexpr uint32_t kNamedBarEpi = 1;
 // bf16 (shared-expert) MMA columns: the call's rows, 16 up to 16 rows, 32 above
 template <int NMAX>
@@ -183,16 +188,13 @@ __device__ __forceinline__ void tmem_ld<64>(uint32_t taddr, float (&v)[64]) {
 // --------------------------------------------------------------- shared-memory plan ----
 
 struct TcPtrs {
-  uint8_t* stages;
-  uint8_t* win;      // [2][win_bytes]: A scales [128][spitch] then B scales [nmax][spitch]
+  uint8_t* stages;   // [stages][16 KB weights, b_bytes activations, 2 KB scale atoms]
   float* xch;        // [2][2][64][Rmax]: gate and up sums of a gate/up item, two buffers
   int* t_uniq;
   int* t_off;
   int* t_users;
-  uint64_t* full;    // [stages] producer -> scale warps (transaction bytes)
-  uint64_t* ready;   // [stages] scale warps (2 arrivals) -> MMA issuers: atoms written
+  uint64_t* full;    // [stages] producer -> MMA issuers (transaction bytes)
   uint64_t* empty;   // [stages] MMA commits (2) -> producer
-  uint64_t* wempty;  // [2] scale warps (2) -> producer: scale window slot free
   uint64_t* afull;   // [2] MMA commits (2) + item id (1) -> epilogue: accumulators ready
   uint64_t* aempty;  // [2] epilogue (4 warps) -> MMA issuers: accumulators read
   uint64_t* drain;   // [2] an issuer's own commit, only when its CTA gives up
@@ -207,16 +209,13 @@ struct TcPtrs {
 __device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L) {
   TcPtrs p;
   p.stages = smem;
-  p.win = smem + L.off_win;
   p.xch = reinterpret_cast<float*>(smem + L.off_x);
   p.t_uniq = reinterpret_cast<int*>(smem + L.off_tab);
   p.t_off = p.t_uniq + L.tab_picks;
   p.t_users = p.t_off + L.tab_picks + 1;
   p.full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
-  p.ready = p.full + kTcMaxStages;
-  p.empty = p.ready + kTcMaxStages;
-  p.wempty = p.empty + kTcMaxStages;
-  p.afull = p.wempty + 2;
+  p.empty = p.full + kTcMaxStages;
+  p.afull = p.empty + kTcMaxStages;
   p.aempty = p.afull + 2;
   p.drain = p.aempty + 2;
   p.tables = p.drain + 2;
@@ -382,10 +381,13 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
         const int j = 32 * blk + lane;
         const float g = xg[j * R + r], up = xu[j * R + r];
         const float mv = __bfloat162float(__float2bfloat16_rn(silu_f(g) * up));
-        const size_t cp = (size_t)dm.I / 2, spp = (size_t)dm.I / 32;
+        const size_t cp = (size_t)dm.I / 2;
+        // scales: atoms of this expert's down items, column 4 u + p (the planes of a user
+        // stay inside one 32-column group, so plane p is 16 bytes after plane 0)
+        uint8_t* sa = s.mid4a + (size_t)it.d * sf_atoms_per_tile(dm.I) * 512 +
+                      sf_atom_offset(4 * u, (it.out0 + 32 * blk) / 32);
         store_planes_lane(mv, lane, s.mid4 + (size_t)(4 * slot) * cp + (it.out0 + 32 * blk) / 2,
-                          cp, s.mid4s + (size_t)(4 * slot) * spp + (it.out0 + 32 * blk) / 32,
-                          spp);
+                          cp, sa, 16);
       }
     } else {
       for (int e = 32 * ew + lane; e < 64 * dm.R; e += 128) {
@@ -468,11 +470,9 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&sp.full[i], 1);
-      mbar_init(&sp.ready[i], 2);
       mbar_init(&sp.empty[i], 2);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sp.wempty[i], 2);
       mbar_init(&sp.afull[i], 3);
       mbar_init(&sp.aempty[i], 4);
       mbar_init(&sp.drain[i], 1);
@@ -493,17 +493,16 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *sp.tbase;
-
-  const int Kr = (PHASE == 0) ? dm.H : dm.I;  // K of the routed contraction
-  const int spitch = (Kr > kWinK) ? 64 : Kr / 32;
   bool ok = true;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer ----
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
+      // scale atoms per weight tile: over H (gate/up) or I (down), two per stage
+      const int ga = sf_atoms_per_tile(PHASE == 0 ? dm.H : dm.I);
       int stage = 0;
-      uint32_t phase = 0, wcnt = 0;
+      uint32_t phase = 0;
       uint32_t pend = 0u, pend_par = 0u;
       bool skip_first = PHASE == 0 && (debug & kDebugStallFirstStage) && blockIdx.x == 0;
       // a CTA's first item is its index; later ones come from the counter (from gridDim.x on)
@@ -532,7 +531,20 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
           }
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
+        // the item's scale atoms: its weight tile's (expert e, tile t) and its activations'
+        const uint8_t* a_sf = nullptr;
+        const uint8_t* b_sf = nullptr;
+        if (it.kind == kRoutedGU) {
+          const int e = it.row0 / (2 * dm.I), t = it.out0 / 64;
+          a_sf = w.w13a + (size_t)(e * (dm.I / 64) + t) * ga * 512;
+          b_sf = s.np4a;
+        } else if (it.kind == kRoutedDN) {
+          const int e = it.row0 / dm.H, t = it.out0 / 128;
+          a_sf = w.w2a + (size_t)(e * (dm.H / 128) + t) * ga * 512;
+          b_sf = s.mid4a + (size_t)it.d * ga * 512;
+        }
         const uint32_t b_bytes = routed ? (uint32_t)nb * 128u : (uint32_t)dm.Rmax * 128u;
+        const uint32_t bytes = kStageW + b_bytes + (routed ? (uint32_t)kTcSfBytes : 0u);
         for (int kc = 0; kc < it.nst; ++kc) {
           if (!mbar_wait(&sp.empty[stage], phase ^ 1, budget_ns)) { ok = false; break; }
           pend &= ~(1u << stage);
@@ -543,17 +555,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
           }
           uint8_t* st = sp.stages + stage * lay.stage_bytes;
           uint8_t* sb = st + kStageW;
-          uint32_t bytes = kStageW + b_bytes;
-          const bool wstart = routed && (kc % kWinStages) == 0;
-          uint8_t* ws = sp.win + (wcnt & 1u) * lay.win_bytes;
-          if (wstart) {
-            if (!mbar_wait(&sp.wempty[wcnt & 1u], ((wcnt >> 1) & 1u) ^ 1u, budget_ns)) {
-              ok = false;
-              break;
-            }
-            const uint32_t rowb = (Kr > kWinK) ? 64u : (uint32_t)Kr / 32u;
-            bytes += 128u * rowb + (uint32_t)nb * rowb;
-          }
+          uint8_t* sa = sb + lay.b_bytes;
           pend |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
           sp.info[stage] = make_int2(item, 0);
@@ -578,33 +580,10 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
             tma_load_2d(st, &maps.ws2, kc * kChunkBF, it.row0, &sp.full[stage], pol);
             tma_load_2d(sb, &maps.ms, kc * kChunkBF, 0, &sp.full[stage]);
           }
-          if (wstart) {
-            const int win = kc / kWinStages;
-            uint8_t* wb = ws + kWinW;  // B scales follow the 128 rows of A scales
-            if (PHASE == 0) {
-              if (Kr > kWinK) {
-                tma_load_2d(ws, &maps.w13s, win * 64, it.row0, &sp.full[stage]);
-                tma_load_2d(ws + 4096, &maps.w13s, win * 64, it.row1, &sp.full[stage]);
-                tma_load_2d(wb, &maps.np4s, win * 64, 0, &sp.full[stage]);
-              } else {
-                const size_t rb = (size_t)(Kr / 32);
-                bulk_load(ws, w.w13s + (size_t)it.row0 * rb, 2u * (uint32_t)Kr, &sp.full[stage]);
-                bulk_load(ws + 4096, w.w13s + (size_t)it.row1 * rb, 2u * (uint32_t)Kr,
-                          &sp.full[stage]);
-                bulk_load(wb, s.np4s, (uint32_t)nb * (uint32_t)rb, &sp.full[stage]);
-              }
-            } else {
-              if (Kr > kWinK) {
-                tma_load_2d(ws, &maps.w2s, win * 64, it.row0, &sp.full[stage]);
-                tma_load_2d(wb, &maps.mid4s[hsel], win * 64, 4 * it.u0, &sp.full[stage]);
-              } else {
-                const size_t rb = (size_t)(Kr / 32);
-                bulk_load(ws, w.w2s + (size_t)it.row0 * rb, 4u * (uint32_t)Kr, &sp.full[stage]);
-                bulk_load(wb, s.mid4s + (size_t)(4 * it.u0) * rb, (uint32_t)nb * (uint32_t)rb,
-                          &sp.full[stage]);
-              }
-            }
-            ++wcnt;
+          if (routed) {
+            // atoms 2 kc and 2 kc + 1 of the weights (A), then of the activations (B)
+            bulk_load(sa, a_sf + (size_t)kc * 1024, 1024u, &sp.full[stage], pol);
+            bulk_load(sa + 1024, b_sf + (size_t)kc * 1024, 1024u, &sp.full[stage]);
           }
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
@@ -623,69 +602,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
           if (pend & (1u << st2)) mbar_wait(&sp.full[st2], (pend_par >> st2) & 1u, budget_ns);
       }
     }
-  } else if (warp >= kTcWarpScale && warp < kTcWarpEpi) {
-    // ------------------------------------------------------------ scale warps ----
-    // warp 0 of the pair: the 128 weight rows' E8M0 bytes of a stage into the two A atoms;
-    // warp 1: the activation planes' bytes into the two B atoms
-    const bool arows = (warp == kTcWarpScale);
-    int stage = 0;
-    uint32_t phase = 0, wcnt = 0;
-    int kc = 0;
-    Item it;
-    it.nst = 0;
-    for (;;) {
-      if (!mbar_wait(&sp.full[stage], phase, budget_ns)) { ok = false; break; }
-      const int item = sp.info[stage].x;
-      if (kc == 0 && item >= 0) it = decode_tc(PHASE, item, dm, tb, *sp.sD, P);
-      if (item >= 0 && (it.kind == kRoutedGU || it.kind == kRoutedDN)) {
-        const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : (it.U <= 16) ? 2 : 3;
-        const int nb = (it.kind == kRoutedGU) ? NMAX : (16 << hsel);
-        const uint8_t* ws = sp.win + (wcnt & 1u) * lay.win_bytes;
-        uint8_t* atoms = sp.stages + stage * lay.stage_bytes + kStageW + lay.b_bytes;
-        const int boff = 8 * (kc % kWinStages);
-        const bool two = boff + 4 < spitch;  // blocks 4..7 lie inside the window row
-        if (arows) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int mr = lane + 32 * i;
-            const uint8_t* row = (PHASE == 0 && mr >= 64) ? ws + 4096 + (mr - 64) * spitch
-                                                          : ws + mr * spitch;
-            const uint32_t lo = *reinterpret_cast<const uint32_t*>(row + boff);
-            const uint32_t hi = two ? *reinterpret_cast<const uint32_t*>(row + boff + 4) : 0u;
-            *reinterpret_cast<uint32_t*>(atoms + 16 * lane + 4 * i) = lo;
-            *reinterpret_cast<uint32_t*>(atoms + 512 + 16 * lane + 4 * i) = hi;
-          }
-        } else {
-          const uint8_t* wb = ws + kWinW;
-#pragma unroll
-          for (int i = 0; i < (NMAX + 31) / 32; ++i) {
-            const int n = lane + 32 * i;
-            if (n < nb) {
-              const uint8_t* row = wb + n * spitch;
-              const uint32_t lo = *reinterpret_cast<const uint32_t*>(row + boff);
-              const uint32_t hi = two ? *reinterpret_cast<const uint32_t*>(row + boff + 4) : 0u;
-              *reinterpret_cast<uint32_t*>(atoms + 1024 + 16 * (n & 31) + 4 * (n >> 5)) = lo;
-              *reinterpret_cast<uint32_t*>(atoms + 1536 + 16 * (n & 31) + 4 * (n >> 5)) = hi;
-            }
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sp.ready[stage]);
-        if ((kc % kWinStages) == kWinStages - 1 || kc == it.nst - 1) {
-          if (lane == 0) mbar_arrive(&sp.wempty[wcnt & 1u]);
-          ++wcnt;
-        }
-      } else {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sp.ready[stage]);  // bf16 stage, or the end marker
-      }
-      if (item < 0) break;
-      if (++stage == S) { stage = 0; phase ^= 1; }
-      if (++kc == it.nst) kc = 0;
-    }
-    if (!ok && lane == 0) set_status(s.status, kStatusTimeout);
-  } else if (warp >= kTcWarpMma && warp < kTcWarpScale) {
+  } else if (warp >= kTcWarpMma && warp < kTcWarpEpi) {
     // ------------------------------------------------------------ MMA issuers ----
     // issuer h owns K steps 2h and 2h + 1 of every stage (the second half of its 256 MXFP4
     // or 64 bf16 elements for h = 1): its scale atoms, its MMAs, its own accumulator
@@ -696,7 +613,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     Item it;
     it.nst = 0;
     for (;;) {
-      if (!mbar_wait(&sp.ready[stage], phase, budget_ns)) { ok = false; break; }
+      if (!mbar_wait(&sp.full[stage], phase, budget_ns)) { ok = false; break; }
       const int item = sp.info[stage].x;
       if (item < 0) break;
       if (kc == 0) {
@@ -715,7 +632,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
         if (routed) {
           const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : (it.U <= 16) ? 2 : 3;
           const int nb = (it.kind == kRoutedGU) ? NMAX : (16 << hsel);
-          const uint8_t* atoms = st + kStageW + lay.b_bytes;
+          const uint8_t* atoms = sb + lay.b_bytes;
           const uint32_t sf = tbase + kTcSfCol + 16u * (uint32_t)stage + 8u * (uint32_t)h;
           tc_cp_sf(sf, sf_desc(atoms + 512 * h));          // A atom h: blocks 4h..4h+3
           tc_cp_sf(sf + 4, sf_desc(atoms + 1024 + 512 * h));  // B atom h
@@ -890,8 +807,8 @@ cudaError_t launch_stream_tc(int phase, const TcMaps& maps, const Dims& d, const
 }
 
 // Shared-memory plan: stages of 16 KB weights + nmax x 128 B activations + 2 KB scale atoms,
-// as many as fit (up to 8, the tensor-memory scale ring), a two-slot scale window ring, the
-// epilogue exchange, the dedup tables and the barriers.
+// as many as fit (up to kTcMaxStages, the tensor-memory scale ring), the epilogue exchange,
+// the dedup tables and the barriers.
 TcLayout make_tc_layout(int Rmax, int k) {
   TcLayout L;
   L.nmax = (Rmax <= 4) ? 16 : (Rmax <= 8) ? 32 : (Rmax <= 16) ? 64 : 128;
@@ -899,21 +816,70 @@ TcLayout make_tc_layout(int Rmax, int k) {
   L.tab_picks = Rmax * k;
   L.b_bytes = L.nmax * 128;
   L.stage_bytes = kStageW + L.b_bytes + kTcSfBytes;
-  L.win_bytes = kWinW + L.nmax * 64;
   const int x_bytes = 2 * 64 * Rmax * 4;
   const int tab_bytes = ((3 * L.tab_picks + 1) * 4 + 127) & ~127;
-  // mbarriers full, ready, empty per stage + wempty, afull, aempty, drain (2 each) + tables;
-  // the stages' item words; the accumulator slots' item words; tbase, eflag and sD
-  const int bar_bytes = (3 * kTcMaxStages + 9) * 8 + kTcMaxStages * 8 + 2 * 4 + 4 + 4 + 4;
-  const int fixed = 2 * L.win_bytes + x_bytes + tab_bytes + ((bar_bytes + 127) & ~127);
+  // mbarriers full, empty per stage + afull, aempty, drain (2 each) + tables; the stages'
+  // item words; the accumulator slots' item words; tbase, eflag and sD
+  const int bar_bytes = (2 * kTcMaxStages + 7) * 8 + kTcMaxStages * 8 + 2 * 4 + 4 + 4 + 4;
+  const int fixed = x_bytes + tab_bytes + ((bar_bytes + 127) & ~127);
   L.stages = (kSmemLimit - fixed) / L.stage_bytes;
   if (L.stages > kTcMaxStages) L.stages = kTcMaxStages;
-  L.off_win = L.stages * L.stage_bytes;
-  L.off_x = L.off_win + 2 * L.win_bytes;
+  L.off_x = L.stages * L.stage_bytes;
   L.off_tab = L.off_x + x_bytes;
   L.off_bar = L.off_tab + tab_bytes;
   L.smem_bytes = L.off_bar + ((bar_bytes + 127) & ~127);
   return L;
+}
+
+// ------------------------------------------------------- weight scales as atoms ----
+// w13s [E][2I][H/32] and w2s [E][H][I/32] (row-major E8M0, one byte per 32-element block)
+// into the atoms the producer copies per stage: for w13 the tile of a gate/up item (its 64
+// gate rows, then its 64 up rows), for w2 the 128 rows of a down item; blocks past the row
+// (the second atom of a last half stage) are zero.  One thread per 4-byte word of an atom:
+// the word of row m holds blocks 4g..4g+3, 4 bytes of the source row.
+__global__ void k_scale_atoms(const uint8_t* __restrict__ w13s, const uint8_t* __restrict__ w2s,
+                              uint8_t* __restrict__ w13a, uint8_t* __restrict__ w2a, int E, int H,
+                              int I) {
+  const int g13 = sf_atoms_per_tile(H), g2 = sf_atoms_per_tile(I);
+  const size_t n13 = (size_t)E * (I / 64) * g13 * 128, n2 = (size_t)E * (H / 128) * g2 * 128;
+  for (size_t wi = blockIdx.x * (size_t)blockDim.x + threadIdx.x; wi < n13 + n2;
+       wi += (size_t)gridDim.x * blockDim.x) {
+    const bool up13 = wi < n13;
+    const size_t v = up13 ? wi : wi - n13;
+    const int pos = (int)(v % 128);       // word within the atom
+    const int m = pos / 4 + 32 * (pos % 4);  // byte 4 pos = 16 (m mod 32) + 4 (m / 32)
+    const size_t a = v / 128;
+    const int ga = up13 ? g13 : g2;
+    const int g = (int)(a % ga);
+    const size_t tile = a / ga;
+    uint32_t word = 0u;
+    if (up13) {
+      const int t = (int)(tile % (I / 64)), e = (int)(tile / (I / 64));
+      const int row = (m < 64) ? 64 * t + m : I + 64 * t + (m - 64);
+      if (4 * g < H / 32)
+        word = *reinterpret_cast<const uint32_t*>(w13s + ((size_t)e * 2 * I + row) * (H / 32) +
+                                                  4 * g);
+      reinterpret_cast<uint32_t*>(w13a)[wi] = word;
+    } else {
+      const int t = (int)(tile % (H / 128)), e = (int)(tile / (H / 128));
+      const int row = 128 * t + m;
+      if (4 * g < I / 32)
+        word = *reinterpret_cast<const uint32_t*>(w2s + ((size_t)e * H + row) * (I / 32) + 4 * g);
+      reinterpret_cast<uint32_t*>(w2a)[v] = word;
+    }
+  }
+}
+
+size_t scale_atom_bytes(const Dims& d) {
+  return ((size_t)d.E * (d.I / 64) * sf_atoms_per_tile(d.H) +
+          (size_t)d.E * (d.H / 128) * sf_atoms_per_tile(d.I)) * 512;
+}
+
+cudaError_t launch_scale_atoms(const Dims& d, const Weights& w, uint8_t* atoms, cudaStream_t st) {
+  uint8_t* w13a = atoms;
+  uint8_t* w2a = atoms + (size_t)d.E * (d.I / 64) * sf_atoms_per_tile(d.H) * 512;
+  k_scale_atoms<<<1024, 256, 0, st>>>(w.w13s, w.w2s, w13a, w2a, d.E, d.H, d.I);
+  return cudaGetLastError();
 }
 
 }  // namespace mtail

@@ -36,6 +36,7 @@ struct moe_tail {
   void* slab;          // one device allocation holding every scratch buffer
   size_t slab_bytes;
   void* stage;         // device staging for moe_tail_run_host: x, residual, out
+  void* atoms;         // the tensor-core form's copy of w13s and w2s in scale-factor atoms
   int device;
   int num_sms;
   int persist_grid;    // CTAs of the single persistent launch (MOE_TAIL_MODE_PERSISTENT)
@@ -163,9 +164,9 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s, size_t* 
   s->gpart = (float*)take((size_t)std::min<size_t>(Is / 64, kMaxSharedSplitItems) *
                           kMaxSharedParts * 128 * R * 4);
   s->np4 = (uint8_t*)take(4 * R * H / 2);
-  s->np4s = (uint8_t*)take(128 * H / 32);
+  s->np4a = (uint8_t*)take((size_t)sf_atoms_per_tile((int)H) * 512);
   s->mid4 = (uint8_t*)take(4 * P * I / 2);
-  s->mid4s = (uint8_t*)take((4 * P + 128) * I / 32);
+  s->mid4a = (uint8_t*)take(std::min<size_t>(E, P) * sf_atoms_per_tile((int)I) * 512);
   s->tl = (c->debug_flags & MOE_TAIL_DEBUG_TIMELINE) ? (unsigned long long*)take(kTlSlots * 8)
                                                      : nullptr;
   s->status = (int32_t*)take(4);
@@ -243,11 +244,30 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
     d0.k = cfg->top_k; d0.I = cfg->expert_inter; d0.Is = cfg->shared_inter; d0.eps = cfg->rms_eps;
     d0.Ha = cfg->attn_dim;
     d0.Pk = 1;
+    if (uses_tc(cfg)) {
+      // the routed experts' E8M0 scales in the atoms the tensor-core kernels copy per stage
+      e = cudaMalloc(&h->atoms, scale_atom_bytes(d0));
+      if (e == cudaSuccess) {
+        h->w.w13a = (const uint8_t*)h->atoms;
+        h->w.w2a = (const uint8_t*)h->atoms +
+                   (size_t)d0.E * (d0.I / 64) * sf_atoms_per_tile(d0.H) * 512;
+        e = launch_scale_atoms(d0, h->w, (uint8_t*)h->atoms, 0);
+      }
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) {
+        cudaFree(h->slab);
+        cudaFree(h->stage);
+        if (h->atoms) cudaFree(h->atoms);
+        delete h;
+        return cuda_fail(e);
+      }
+    }
     int mrc = make_stream_maps(&h->maps, d0, h->w, h->s);
     if (mrc == 0 && uses_tc(cfg)) mrc = make_tc_maps(&h->tcmaps, h->maps, d0, h->w, h->s);
     if (mrc != 0) {
       cudaFree(h->slab);
       cudaFree(h->stage);
+      if (h->atoms) cudaFree(h->atoms);
       delete h;
       if (mrc == -1) {
         snprintf(g_cuda_err, sizeof(g_cuda_err), "no cuTensorMapEncodeTiled");
@@ -566,8 +586,20 @@ extern "C" void moe_tail_destroy(moe_tail_t* h) {
   }
   cudaFree(h->slab);
   cudaFree(h->stage);
+  if (h->atoms) cudaFree(h->atoms);
   if (cur >= 0 && cur != h->device) cudaSetDevice(cur);
   delete h;
+}
+
+extern "C" int moe_tail_refresh_scales(moe_tail_t* h, void* stream) {
+  if (!h) return MOE_TAIL_ERR_INVALID_ARG;
+  if (!h->atoms) return MOE_TAIL_OK;  // a form that reads w13s and w2s in place
+  Dims d0;
+  d0.R = h->cfg.max_rows; d0.Rmax = h->cfg.max_rows; d0.H = h->cfg.hidden;
+  d0.E = h->cfg.n_experts; d0.k = h->cfg.top_k; d0.I = h->cfg.expert_inter;
+  d0.Is = h->cfg.shared_inter; d0.eps = h->cfg.rms_eps; d0.Ha = h->cfg.attn_dim; d0.Pk = 1;
+  const cudaError_t e = launch_scale_atoms(d0, h->w, (uint8_t*)h->atoms, (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
 }
 
 // ------------------------------------------- the AttnRes residual mix (attnres_mix.h) ----

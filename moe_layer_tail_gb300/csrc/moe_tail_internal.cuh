@@ -57,6 +57,11 @@ struct Weights {
   const __nv_bfloat16* ws2;
   const __nv_bfloat16* wsg;  // shared-expert gate [H], or null
   const __nv_bfloat16* wo;   // attention out_proj [H, Ha], or null
+  // the tensor-core form's copies of w13s and w2s in scale-factor atoms (sf_atom_offset):
+  // w13a [E][I/64 items][H/128 atoms][512 B] (an item's 64 gate rows, then its 64 up rows),
+  // w2a [E][H/128 items][2 ceil(I/256) atoms][512 B]; null in the other forms
+  const uint8_t* w13a;
+  const uint8_t* w2a;
 };
 
 // Every buffer a call needs, carved from one allocation made at create time.
@@ -87,10 +92,11 @@ struct Scratch {
   float* gpart;          // [kMaxSharedSplitItems, kMaxSharedParts, 128, Rmax] fp32 sums of the
                          // K parts of split shared gate/up items (rows: 64 gate, 64 up)
   uint8_t* np4;          // [4 Rmax, H/2] E2M1 planes of n (row 4r + p = plane p of row r)
-  uint8_t* np4s;         // [128, H/32] their E8M0 scales (rows past 4 Rmax stay zero)
+  uint8_t* np4a;         // [H/128][512] their E8M0 scales in scale-factor atoms (row 4r + p)
   uint8_t* mid4;         // [4 Rmax k, I/2] E2M1 planes of mid (row 4 slot + p, slot = the
                          // pick's position in user_list)
-  uint8_t* mid4s;        // [4 Rmax k + 128, I/32] their E8M0 scales (128 zero rows after)
+  uint8_t* mid4a;        // [min(E, Rmax k)][2 ceil(I/256)][512] their E8M0 scales in
+                         // scale-factor atoms per distinct expert (row 4 (slot - u0) + p)
   unsigned long long* tl;  // [kTlSlots] %globaltimer stamps of the last run, or null (the
                            // timeline debug flag off)
   int32_t* status;       // [1] sticky device status word
@@ -238,6 +244,18 @@ __device__ __forceinline__ uint32_t e2m1x8_pack(const float (&x)[8]) {
   return w;
 }
 
+// Scale-factor atoms: the layout in which tcgen05.cp (32 rows x 128 bits, copied to all four
+// lane quadrants) brings E8M0 scales into tensor memory for the block-scaled MMAs.  One atom
+// of 512 bytes holds 4 consecutive 32-element blocks of 128 operand rows, row m's block b at
+// byte 16 (m mod 32) + 4 (m / 32) + b; consecutive atoms cover consecutive groups of 4
+// blocks.  Byte offset of (row, block) for a 128-row operand tile, block counted from 0:
+__host__ __device__ __forceinline__ uint32_t sf_atom_offset(int row, int block) {
+  return 512u * (uint32_t)(block >> 2) + 16u * (uint32_t)(row & 31) + 4u * (uint32_t)(row >> 5) +
+         (uint32_t)(block & 3);
+}
+// atoms of one operand tile over K elements (whole 256-element stages: two atoms each)
+__host__ __device__ __forceinline__ int sf_atoms_per_tile(int K) { return 2 * ((K + 255) / 256); }
+
 // Value of the E2M1 code in the low nibble of `code`.
 __device__ __forceinline__ float e2m1_value(uint32_t code) {
   uint32_t h;
@@ -324,8 +342,7 @@ struct TcLayout {
   int b_bytes;      // activation tile of a stage: nmax rows x 128 bytes
   int stage_bytes;  // 16 KB weights + b_bytes + 2 KB scale-factor atoms
   int stages;
-  int win_bytes;    // one scale window: 8 KB weight scales + nmax x 64 B plane scales
-  int off_win, off_x, off_tab, off_bar, smem_bytes;
+  int off_x, off_tab, off_bar, smem_bytes;
   int tab_picks;    // entries of the dedup tables (rows x k of the handle)
 };
 
@@ -335,11 +352,8 @@ struct TcMaps {
                           // a stage's 64 gate and 64 up rows in one copy, 128-byte swizzle
   CUtensorMap ws13;       // bf16 [2][Is][H], box {64, 64, 2}, 128-byte swizzle
   CUtensorMap w2, ws2, n, ms;  // as in StreamMaps
-  CUtensorMap w13s, w2s;                  // weight scale windows (K > 2048 only)
   CUtensorMap np4;        // u8 [4 Rmax, H/2] planes of n, box {128 B, nmax}, 128-byte swizzle
-  CUtensorMap np4s;       // u8 [64, H/32], box {64 B, nmax} (H > 2048 only)
   CUtensorMap mid4[4];    // u8 [4 P, I/2], box {128 B, 16 / 32 / 64 / 128 rows}, 128-byte swizzle
-  CUtensorMap mid4s[4];   // u8 [4 P + 128, I/32], box {64 B, 16 / 32 / 64 / 128} (I > 2048 only)
   TcLayout lay;
 };
 
@@ -377,6 +391,9 @@ cudaError_t prepare_stream_tc_kernels();
 cudaError_t launch_stream_tc(int phase, const TcMaps& maps, const Dims& d, const Weights& w,
                              const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                              bool pdl, uint32_t debug);
+// bytes of the two atom copies (w13a then w2a) and the launch that writes them from w13s, w2s
+size_t scale_atom_bytes(const Dims& d);
+cudaError_t launch_scale_atoms(const Dims& d, const Weights& w, uint8_t* atoms, cudaStream_t st);
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
                            uint64_t budget_ns, bool gated);

@@ -103,6 +103,7 @@ def test_null_arguments_rejected_without_device(lib):
     assert lib.moe_tail_run_host(None, None, None, None, 1, None) == mt.ERR_INVALID_ARG
     assert lib.moe_tail_run_attn(None, None, None, None, 1, None) == mt.ERR_INVALID_ARG
     assert lib.moe_tail_get_status(None, None) == mt.ERR_INVALID_ARG
+    assert lib.moe_tail_refresh_scales(None, None) == mt.ERR_INVALID_ARG
     lib.moe_tail_destroy(None)
     assert lib.moe_tail_launches_per_run(None, 1) == 0
 

@@ -106,7 +106,7 @@ def _check_small(shape, d, max_rows=None, rows=None, flags=0):
     (1, 256, 1, 1, 128, 64),       # a single expert, smallest shapes
     (2, 512, 12, 3, 256, 192),     # several tiles, ragged tails
     (5, 768, 33, 7, 384, 320),     # odd expert count, k not a power of two
-    (3, 2560, 6, 2, 2560, 192),    # several E8M0 windows per row, the last one ragged
+    (3, 2560, 6, 2, 2560, 192),    # several E8M0 windows per row (CUDA-core form), the last ragged
     (16, 3072, 2, 2, 128, 64),     # 16 users of each expert (two N-tiles), long K
     (16, 256, 16, 16, 128, 128),   # k = E: every expert, maximum rows
     (16, 512, 64, 1, 256, 64),     # k = 1, maximum rows
@@ -133,6 +133,27 @@ def test_mid_outside_f16_range_takes_block_scales(shift):
     shape, d = _small(15, R=4, H=512, E=10, k=3, I=256, Is=128)
     d["w13_scales"] = (d["w13_scales"].astype(np.int32) + shift).astype(np.uint8)
     _check_small(shape, d)
+
+
+def test_refresh_scales_follows_in_place_scale_changes():
+    """The default form reads the routed experts' E8M0 scales from a copy the handle makes at
+    create (scale-factor atoms).  After the caller rewrites w13_scales and w2_scales in place,
+    moe_tail_refresh_scales makes the next run follow the new scales: checked against the
+    oracle on the changed weights, with I = 384 (a half stage at the end of every down item)."""
+    shape, d = _small(23, R=5, H=768, E=9, k=3, I=384, Is=128)
+    tail, dev, _, _ = _check_small(shape, d)
+    rng = np.random.default_rng(231)
+    d2 = dict(d)
+    for key in ("w13_scales", "w2_scales"):
+        step = rng.integers(-1, 2, size=d[key].shape)
+        d2[key] = (d[key].astype(np.int32) + step).astype(np.uint8)
+        dev[key].copy_(torch.from_numpy(d2[key]))  # same device buffer, new values
+    tail.refresh_scales()
+    orc2 = oracle.moe_tail(d2, shape.k, shape.eps, nthreads=NTHREADS)
+    out, res, ids, _, _ = run_gpu(tail, d2)
+    check_parity(out, res, ids, orc2, shape.k)
+    assert tail.status() == 0
+    tail.close()
 
 
 def test_identical_experts_output_independent_of_routing():
