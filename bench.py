@@ -500,8 +500,9 @@ def run_ours(args, rank, world, local_rank):
                                 "per step on a non-default stream (a replayed graph of copy in, "
                                 "the call's launches, copy out)"}
 
-    if args.timeline and not args.persistent:
-        tt = mt.MoeTail(shape, dev_w[0], max_rows=R, debug_flags=flags | mt.DEBUG_TIMELINE)
+    if args.timeline:
+        tt = mt.MoeTail(shape, dev_w[0], max_rows=R, mode=mode,
+                        debug_flags=flags | mt.DEBUG_TIMELINE)
         marks = []
         for i in range(min(20, nsets)):
             (tt.run_attn if args.out_proj else tt.run)(x_all[i], res[i], out[i])

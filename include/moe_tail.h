@@ -57,17 +57,20 @@ enum {
 enum {
   MOE_TAIL_MODE_MULTI_KERNEL = 0,  /* one launch per stage, stream-ordered */
   MOE_TAIL_MODE_PERSISTENT = 1     /* the whole call in one cooperative launch, one CTA per
-                                      SM, its stages separated by grid-wide barriers whose
-                                      generation word tags every call (nothing is reset
-                                      between calls or graph replays); bounded waits report
-                                      MOE_TAIL_STATUS_TIMEOUT.  The stages are the
-                                      warp-per-row CUDA-core forms, so it is slower than the
-                                      multi-kernel mode; attn_dim must be 0 (else
-                                      MOE_TAIL_ERR_UNSUPPORTED at create) and the debug
-                                      flags do not apply.  moe_tail_create returns
-                                      MOE_TAIL_ERR_NOT_CORESIDENT when no CTA of it fits an
-                                      SM; a launch that cannot keep every CTA resident fails
-                                      with MOE_TAIL_ERR_CUDA instead of waiting. */
+                                      SM: add + RMSNorm, one grid-wide barrier (its
+                                      generation word tags every call: nothing is reset
+                                      between calls or graph replays), the router's parts
+                                      spread over the CTAs, then the tensor-core expert roles
+                                      of the multi-kernel form over the gate/up and then the
+                                      down items, then the combine, handing over through the
+                                      same per-expert and per-tile counts.  Bounded waits
+                                      report MOE_TAIL_STATUS_TIMEOUT.  attn_dim must be 0
+                                      (else MOE_TAIL_ERR_UNSUPPORTED at create) and the debug
+                                      flags other than the stall injection do not apply.
+                                      moe_tail_create returns MOE_TAIL_ERR_NOT_CORESIDENT when
+                                      no CTA of it fits an SM; a launch that cannot keep every
+                                      CTA resident fails with MOE_TAIL_ERR_CUDA instead of
+                                      waiting. */
 };
 
 /* Bits of the device status word read by moe_tail_get_status (sticky until cleared). */
@@ -142,8 +145,8 @@ typedef struct moe_tail moe_tail_t; /* opaque handle */
 
 typedef struct {
   int32_t max_rows;       /* 1..32: the largest `rows` any run will pass; above 16 only the
-                           * default expert form without attn_dim (the debug forms and the
-                           * persistent mode take 1..16; MOE_TAIL_ERR_UNSUPPORTED otherwise) */
+                           * default expert form and the persistent mode, without attn_dim
+                           * (the debug forms take 1..16; MOE_TAIL_ERR_UNSUPPORTED otherwise) */
   int32_t hidden;         /* H: multiple of 256 (of 512 above 2048), at most 32768 */
   int32_t n_experts;      /* E: 1..1024 */
   int32_t top_k;          /* k: 1..min(E, 32) */

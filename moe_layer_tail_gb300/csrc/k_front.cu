@@ -23,33 +23,6 @@
 
 namespace mtail {
 
-// Power-of-two exponent p such that amax * 2^-p lies in [2^14, 2^15) (0 for amax == 0).
-__device__ __forceinline__ int f16_block_exp(float amax) {
-  if (!(amax > 0.f)) return 0;
-  const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-  return max(-100, min(100, e - 14));
-}
-
-// 8 bf16 n values (one 16-byte group) -> f16 scaled by `down` (a power of two).
-__device__ __forceinline__ uint4 f16_group(uint4 nv, float down) {
-  const uint32_t w[4] = {nv.x, nv.y, nv.z, nv.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    __half2 h2 = __floats2half2_rn(bf16_lo(w[q]) * down, bf16_hi(w[q]) * down);
-    o[q] = *reinterpret_cast<uint32_t*>(&h2);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__device__ __forceinline__ float group_amax(uint4 nv) {
-  const uint32_t w[4] = {nv.x, nv.y, nv.z, nv.w};
-  float m = 0.f;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
-  return m;
-}
-
 // ---------------------------------------------------------------- add + RMSNorm ----
 // One CTA of 512 threads per row.  Thread i owns the 16-byte groups i, i + 512, ... of the
 // row (up to 8, H <= 32768) and keeps bf16(x + residual) in registers; gamma is staged in
@@ -59,16 +32,6 @@ __device__ __forceinline__ float group_amax(uint4 nv) {
 constexpr int kNormThreads = 512;
 constexpr int kNormGroups = 8;
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* part) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = is_max ? warp_max(v) : warp_sum(v);
-  __syncthreads();  // part[] may still be read by the previous reduction
-  if (lane == 0) part[warp] = v;
-  __syncthreads();
-  float r = 0.f;
-  for (int i = 0; i < kNormThreads / 32; ++i) r = is_max ? fmaxf(r, part[i]) : r + part[i];
-  return r;
-}
 
 __global__ void __launch_bounds__(kNormThreads)
 k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ residual,
@@ -82,136 +45,16 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   extern __shared__ uint4 s_gamma[];  // [H / 8]
   __shared__ float part[kNormThreads / 32];
   const int r = blockIdx.x;
-  const int ng = H / 8;
   const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
-  for (int c = threadIdx.x; c < ng; c += kNormThreads) s_gamma[c] = __ldg(g4 + c);
+  for (int c = threadIdx.x; c < H / 8; c += kNormThreads) s_gamma[c] = __ldg(g4 + c);
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) tl_first(tl, kTlNormStart);
   if (r == 0)  // work counters, tickets and per-expert progress of this call
     for (int i = threadIdx.x; i < kCtrWords; i += kNormThreads) counters[i] = 0u;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * H);
-  const uint4* rr = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
-  uint4 rn[kNormGroups];
-  float ss = 0.f;
-#pragma unroll
-  for (int q = 0; q < kNormGroups; ++q) {
-    const int c = threadIdx.x + q * kNormThreads;
-    if (c < ng) {
-      uint4 xv;
-      if (xpart) {  // x = bf16(the out_proj K parts added in part order)
-        const float* p0 = xpart + (size_t)r * H + 8 * (size_t)c;
-        float4 a = __ldcg(reinterpret_cast<const float4*>(p0));
-        float4 b = __ldcg(reinterpret_cast<const float4*>(p0) + 1);
-        for (int pp = 1; pp < Pk; ++pp) {
-          const float4* pq = reinterpret_cast<const float4*>(p0 + pp * part_stride);
-          const float4 a2 = __ldcg(pq), b2 = __ldcg(pq + 1);
-          a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
-          b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
-        }
-        xv = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                        pack_bf16x2(b.z, b.w));
-      } else {
-        xv = xr[c];
-      }
-      const uint4 rv = rr[c];
-      rn[q] = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y), add_bf16x2(xv.z, rv.z),
-                         add_bf16x2(xv.w, rv.w));
-    } else {
-      rn[q] = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < kNormGroups; ++q) {
-    const uint32_t o[4] = {rn[q].x, rn[q].y, rn[q].z, rn[q].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) ss += bf16_lo(o[i]) * bf16_lo(o[i]) + bf16_hi(o[i]) * bf16_hi(o[i]);
-  }
-  const float rstd = 1.0f / sqrtf(block_reduce(ss, false, part) / (float)H + eps);
-  float down = 1.f;
-  if (!np4) {
-    // the f16 copy of the CUDA-core expert form, with one power-of-two scale per row (row
-    // maximum in [2^14, 2^15)); the tensor-core form takes the E2M1 planes below instead
-    float amax = 0.f;
-#pragma unroll
-    for (int q = 0; q < kNormGroups; ++q) {
-      const int c = threadIdx.x + q * kNormThreads;
-      if (c < ng) {
-        const uint4 gv = s_gamma[c];
-        const uint4 nv = make_uint4(norm_bf16x2(rn[q].x, gv.x, rstd), norm_bf16x2(rn[q].y, gv.y, rstd),
-                                    norm_bf16x2(rn[q].z, gv.z, rstd), norm_bf16x2(rn[q].w, gv.w, rstd));
-        amax = fmaxf(amax, group_amax(nv));
-      }
-    }
-    const int p = f16_block_exp(block_reduce(amax, true, part));
-    down = __uint_as_float((uint32_t)(127 - p) << 23);
-    if (threadIdx.x == 0) n16s[r] = __uint_as_float((uint32_t)(127 + p) << 23);
-  }
-  uint4* rno = reinterpret_cast<uint4*>(rnew + (size_t)r * H);
-  uint4* no = reinterpret_cast<uint4*>(n_out + (size_t)r * H);
-  uint4* n16o = reinterpret_cast<uint4*>(n16 + (size_t)r * H);
-  const uint4* wg4 = reinterpret_cast<const uint4*>(wsg);
-  float zg = 0.f;  // this thread's part of the shared-expert gate logit n . wsg
-#pragma unroll
-  for (int q = 0; q < kNormGroups; ++q) {
-    const int c = threadIdx.x + q * kNormThreads;
-    if (c < ng) {
-      const uint4 gv = s_gamma[c];
-      const uint4 nv = make_uint4(norm_bf16x2(rn[q].x, gv.x, rstd), norm_bf16x2(rn[q].y, gv.y, rstd),
-                                  norm_bf16x2(rn[q].z, gv.z, rstd), norm_bf16x2(rn[q].w, gv.w, rstd));
-      rno[c] = rn[q];
-      no[c] = nv;
-      if (!np4) n16o[c] = f16_group(nv, down);
-      if (np4) {
-        // the four E2M1 planes of n for the tensor-core experts: a 32-element block is the
-        // groups of four adjacent threads (H / 8 is a multiple of 32, so a warp is either
-        // wholly inside the row or wholly past it)
-        const uint32_t ww[4] = {nv.x, nv.y, nv.z, nv.w};
-        float rv[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          rv[2 * i] = bf16_lo(ww[i]);
-          rv[2 * i + 1] = bf16_hi(ww[i]);
-        }
-#pragma unroll
-        for (int pl = 0; pl < 4; ++pl) {
-          float am = 0.f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(rv[i]));
-          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-          const int e = e2m1_plane_exp(am);
-          const float inv = exp2_int(-e), sc = exp2_int(e);
-          float xs[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) xs[i] = rv[i] * inv;
-          const uint32_t code = e2m1x8_pack(xs);
-          uint32_t h[4];
-          e2m1x8_to_f16x2(code, h[0], h[1], h[2], h[3]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
-            rv[2 * i] -= f.x * sc;
-            rv[2 * i + 1] -= f.y * sc;
-          }
-          const size_t prow = (size_t)(4 * r + pl);
-          reinterpret_cast<uint32_t*>(np4 + prow * (H / 2))[c] = code;
-          if ((c & 3) == 0) np4a[sf_atom_offset((int)prow, c / 4)] = (uint8_t)(e + 127);
-        }
-      }
-      if (wsg) {
-        const uint4 w = __ldg(wg4 + c);
-        const uint32_t nn[4] = {nv.x, nv.y, nv.z, nv.w}, ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          zg += bf16_lo(nn[i]) * bf16_lo(ww[i]) + bf16_hi(nn[i]) * bf16_hi(ww[i]);
-      }
-    }
-  }
-  if (wsg) {  // the gate of this row: sigmoid of the block-reduced logit
-    const float z = block_reduce(zg, false, part);
-    if (threadIdx.x == 0) sgate[r] = 1.0f / (1.0f + expf(-z));
-  }
+  add_rmsnorm_row<kNormThreads, kNormGroups>(r, x, residual, s_gamma, rnew, n_out, n16, n16s, H,
+                                             eps, wsg, sgate, xpart, Pk, part_stride, np4, np4a,
+                                             part);
   if (tl) {
     __syncthreads();
     if (threadIdx.x == 0) tl_last(tl, kTlNormEnd);
@@ -287,182 +130,56 @@ cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, 
 // count, sets the time an SM waits for instructions.
 constexpr int kRtWarps = 8;
 constexpr int kRtThreads = kRtWarps * 32;
-constexpr int kRtTile = 16;      // experts per CTA
-constexpr int kRtMaxPart = 2048; // K elements per part at most
-constexpr int kRtMaxParts = 16;
-
-struct RouterPlan {
-  int tiles, parts, plen;
-  size_t smem;
-};
 
 // Parts: enough CTAs to spread the router weights over the SMs (about 128), parts of at
-// most 2048 elements, each a multiple of 32.
-static RouterPlan router_plan(int R, int H, int E) {
+// most 2048 elements, each a multiple of 32; the shared memory of a part for `warps` warps
+// (staged weights and rows, or the logits of the last part, then the warps' tiles).
+RouterPlan router_plan(int R, int H, int E, int warps) {
   RouterPlan p;
   p.tiles = (E + kRtTile - 1) / kRtTile;
   int P = (128 + p.tiles - 1) / p.tiles;
   P = std::max(P, (H + kRtMaxPart - 1) / kRtMaxPart);
   P = std::min(P, kRtMaxParts);
+  const size_t nt = (R + 7) / 8;
   for (;; ++P) {  // more parts while the staged rows of many-row handles exceed 192 KB
     p.plen = ((H + P - 1) / P + 31) / 32 * 32;
     p.parts = (H + p.plen - 1) / p.plen;
     const size_t pitch = (size_t)p.plen * 2 + 16;
     const size_t tiles_bytes = (kRtTile + (size_t)R) * pitch;
     const size_t logit_bytes = (size_t)R * E * 4;
-    const size_t nt = (R + 7) / 8;
-    p.smem = ((std::max(tiles_bytes, logit_bytes) + 15) / 16) * 16 + kRtWarps * nt * 32 * 16;
+    p.red_off = (int)(((std::max(tiles_bytes, logit_bytes) + 15) / 16) * 16);
+    p.smem = (size_t)p.red_off + (size_t)warps * nt * 32 * 16;
     if (p.smem <= 192 * 1024 || P >= kRtMaxParts) break;
   }
   return p;
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   (uint32_t)__cvta_generic_to_shared(dst)),
-               "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
+// Grid (tiles, parts): one router part per CTA (router_stage_w before the wait on the norm
+// launch, router_part after it); the last part runs router_finish.  Loops stay rolled: every
+// CTA runs this code once, so its size, not its instruction count, sets the time an SM waits
+// for instructions.
 __global__ void __launch_bounds__(kRtThreads)
 k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, int E, int k,
               int plen, int red_off) {
   extern __shared__ __align__(16) uint8_t sm[];
   __shared__ int s_last;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int P = gridDim.y, p = blockIdx.y;
-  const int k0 = p * plen;
-  const int len = min(plen, H - k0);  // elements of this part (> 0, multiple of 32)
-  const int cpr = len / 8;            // 16-byte chunks per row in this part
-  const int pitch = plen * 2 + 16;    // bytes per staged row (16-byte pad: no bank conflicts)
-  const int e0 = blockIdx.x * kRtTile;
-  uint8_t* sw = sm;                             // [16][pitch] router weights
-  uint8_t* sn = sm + kRtTile * pitch;           // [R][pitch] n
-  float4* red = reinterpret_cast<float4*>(sm + red_off);  // [8 warps][NT][32 lanes]
-  for (int i = tid; i < kRtTile * cpr; i += kRtThreads) {
-    const int r = i / cpr, c = i % cpr;
-    cp_async16(sw + r * pitch + c * 16, w_r + (size_t)min(e0 + r, E - 1) * H + k0 + c * 8);
-  }
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  router_stage_w<kRtThreads>(sm, w_r, blockIdx.x, blockIdx.y, plen, H, E);
   pdl_wait();
-  if (tid == 0) tl_first(s.tl, kTlRouterStart);
+  if (threadIdx.x == 0) tl_first(s.tl, kTlRouterStart);
   // the expert launch may start as soon as every router CTA is past its wait: its
   // shared-expert items need only n (written by the norm launch, complete by now), and its
   // routed items wait for the kCtrRouted word this launch's last CTA sets
   pdl_trigger();
-  for (int i = tid; i < R * cpr; i += kRtThreads) {
-    const int r = i / cpr, c = i % cpr;
-    cp_async16(sn + r * pitch + c * 16, s.n + (size_t)r * H + k0 + c * 8);
-  }
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  __syncthreads();
-  // warp w: K steps [w * spw, ...) of 32 elements; lane (g, t) takes elements 8t .. 8t+7 of
-  // a step for weight rows g and g + 8 and for activation row g (+ 8 for the second tile)
-  const int NT = (R + 7) / 8;  // N-tiles of 8 rows (up to 4)
-  const int S = len / 32, spw = (S + kRtWarps - 1) / kRtWarps;
-  float acc[kMaxRows / 8][4];
-#pragma unroll
-  for (int nt = 0; nt < kMaxRows / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-  const uint8_t* wa = sw + g * pitch + 16 * t;
-  const uint8_t* wc = sw + (g + 8) * pitch + 16 * t;
-  const uint8_t* nb = sn + 16 * t;
-#pragma unroll 1
-  for (int st = warp * spw; st < min(S, (warp + 1) * spw); ++st) {
-    const uint4 a = *reinterpret_cast<const uint4*>(wa + st * 64);
-    const uint4 c = *reinterpret_cast<const uint4*>(wc + st * 64);
-#pragma unroll
-    for (int nt = 0; nt < kMaxRows / 8; ++nt) {
-      if (nt < NT) {
-        const uint4 b =
-            *reinterpret_cast<const uint4*>(nb + min(8 * nt + g, R - 1) * pitch + st * 64);
-        mma_bf16_16816(acc[nt], a.x, c.x, a.y, c.y, b.x, b.y);
-        mma_bf16_16816(acc[nt], a.z, c.z, a.w, c.w, b.z, b.w);
-      }
-    }
-  }
-#pragma unroll
-  for (int nt = 0; nt < kMaxRows / 8; ++nt)
-    if (nt < NT)
-      red[(warp * NT + nt) * 32 + lane] =
-          make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-  __syncthreads();
-  if (warp == 0) {
-    // lane (g, t): experts g and g + 8, rows 8 nt + 2t and 8 nt + 2t + 1
-    for (int nt = 0; nt < NT; ++nt) {
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int w2 = 0; w2 < kRtWarps; ++w2) {
-        const float4 x = red[(w2 * NT + nt) * 32 + lane];
-        v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
-      }
-      for (int q = 0; q < 4; ++q) {
-        const int e = e0 + g + 8 * (q >> 1), r = 8 * nt + 2 * t + (q & 1);
-        if (e < E && r < R) s.logit_parts[((size_t)p * R + r) * E + e] = v[q];
-      }
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0)
-    s_last = (atomicAdd(&s.counters[kCtrFrontTicket], 1u) == gridDim.x * gridDim.y - 1) ? 1 : 0;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // logits = the parts added in part order, into shared memory (the staged tiles are no
-  // longer needed); every part of four logits per thread is loaded before any is added
-  float* s_logits = reinterpret_cast<float*>(sm);
-  const int RE = R * E;
-  constexpr int kJ = 4;
-  for (int base = 0; base < RE; base += kJ * kRtThreads) {
-    float v[kRtMaxParts][kJ];
-#pragma unroll
-    for (int pp = 0; pp < kRtMaxParts; ++pp)
-#pragma unroll
-      for (int j = 0; j < kJ; ++j) {
-        const int i = base + tid + j * kRtThreads;
-        v[pp][j] = (pp < P && i < RE) ? __ldcg(s.logit_parts + (size_t)pp * RE + i) : 0.f;
-      }
-#pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-      float sum = v[0][j];
-#pragma unroll
-      for (int pp = 1; pp < kRtMaxParts; ++pp)
-        if (pp < P) sum += v[pp][j];
-      const int i = base + tid + j * kRtThreads;
-      if (i < RE) s_logits[i] = sum;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) tl_first(s.tl, kTlTopkStart);
-  topk_dedup_block<true>(s_logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
-                         s.user_list, s.status, R, E, k);
-  // publish the routing: every thread's table stores, then the word the expert launches
-  // wait for (release at GPU scope)
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    s.counters[kCtrFrontTicket] = 0u;
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&s.counters[kCtrRouted]), "r"(1u)
-                 : "memory");
-    tl_first(s.tl, kTlRouted);
-  }
+  if (router_part<kRtWarps>(sm, s, blockIdx.x, blockIdx.y, plen, red_off, R, H, E,
+                            gridDim.x * gridDim.y, &s_last))
+    router_finish<kRtThreads, false>(sm, s, gridDim.y, R, E, k);
 }
 
 cudaError_t launch_router_topk(const Dims& d, const Weights& w, const Scratch& s,
                                cudaStream_t st, bool pdl) {
-  const RouterPlan rp = router_plan(d.R, d.H, d.E);
-  const size_t nt = (d.R + 7) / 8;
-  const int red_off = (int)(rp.smem - kRtWarps * nt * 32 * 16);
+  const RouterPlan rp = router_plan(d.R, d.H, d.E, kRtWarps);
   return launch_k(k_router_topk, dim3(rp.tiles, rp.parts), dim3(kRtThreads), rp.smem, st, pdl,
-                  w.w_r, s, d.R, d.H, d.E, d.k, rp.plen, red_off);
+                  w.w_r, s, d.R, d.H, d.E, d.k, rp.plen, rp.red_off);
 }
 
 // Parts of the router's K at most: sizes the scratch of the partial logits.
@@ -475,7 +192,7 @@ cudaError_t prepare_front_kernels() {
                                        (1 << 15) * 2);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_router_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)router_plan(kMaxRows, 1 << 15, kMaxExperts).smem + 4096);
+                             (int)router_plan(kMaxRows, 1 << 15, kMaxExperts, kRtWarps).smem + 4096);
   return e;
 }
 

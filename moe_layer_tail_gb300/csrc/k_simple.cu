@@ -8,8 +8,8 @@
 // routed experts" (bf16 activations x MXFP4 weights, gate and up, SiLU, down) and "The
 // shared expert gate_up / SiLU and mul / down"; "glm53: Long-context indexer ..." page,
 // Modifications rows 16 and 20 (each distinct expert once, every using row against it).
+#include "k_combine.cuh"
 #include "k_front.cuh"
-#include "k_persist.cuh"
 #include "moe_tail_internal.cuh"
 
 namespace mtail {
@@ -32,10 +32,8 @@ __device__ __forceinline__ void dequant32(uint4 c, float* v) {
   }
 }
 
-// dot of 32 floats with 32 bf16 activations at p (64 bytes, 16-byte aligned).  Activations
-// are read with ordinary loads, not the read-only path: in the persistent launch they were
-// written earlier in the same kernel by other CTAs, and ordinary loads after the grid
-// barrier's acquire see those writes (the CTA's warps still share them through L1).
+// dot of 32 floats with 32 bf16 activations at p (64 bytes, 16-byte aligned); ordinary loads
+// (the CTA's warps share them through L1).
 __device__ __forceinline__ float dot32_bf16(const float* v, const __nv_bfloat16* p) {
   const uint4* p4 = reinterpret_cast<const uint4*>(p);
   float a = 0.f;
@@ -53,8 +51,7 @@ __device__ __forceinline__ float dot32_bf16(const float* v, const __nv_bfloat16*
 }
 
 // Each stage below is a warp-level loop: warp gw of nw (this warp's index among all warps
-// of the grid, and their number) takes items gw, gw + nw, ...; the __global__ wrappers and
-// the single persistent launch call the same functions.
+// of the grid, and their number) takes items gw, gw + nw, ...
 
 // Ask L2 for a weight row's lines before the lanes walk it, so that a warp has the whole row
 // in flight rather than one 16-byte block per lane at a time.
@@ -292,10 +289,6 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
 // are in flight together.  wait_tiles: instead of waiting for the previous launch as a
 // whole, each warp waits (bounded, acquire) until the down items of the two 128-output
 // tiles it covers (the shared expert's and one per distinct expert) are counted done.
-// One thread's 8 outputs: row r, outputs 8c .. 8c + 7.
-__device__ __forceinline__ void combine_one(const Dims& dm, const Scratch& s, int r, int c,
-                                            __nv_bfloat16* __restrict__ out,
-                                            __nv_bfloat16* __restrict__ residual, bool gated);
 
 __global__ void __launch_bounds__(256)
 k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
@@ -309,65 +302,9 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= dm.R * ng) return;
   const int r = idx / ng, c = idx % ng;
-  if (wait_tiles) {
-    const int lane = threadIdx.x & 31;
-    const uint32_t need = (uint32_t)min(max(*s.n_distinct, 1), kMaxPicks) + 1u;
-    bool ok = true;
-    if ((lane & 15) == 0) ok = wait_count(&s.counters[kCtrTileDone + c / 16], need, budget_ns);
-    if (__any_sync(0xffffffffu, !ok)) {
-      if (lane == 0) set_status(s.status, kStatusTimeout);
-      return;
-    }
-    __syncwarp();  // orders the other lanes' loads after lanes 0 and 16's acquires
-  }
+  if (wait_tiles && !combine_wait_tiles(s, c, budget_ns)) return;
   combine_one(dm, s, r, c, out, residual, gated);
   if ((threadIdx.x & 31) == 0) tl_last(s.tl, kTlCombineEnd);
-}
-
-__device__ __forceinline__ void combine_one(const Dims& dm, const Scratch& s, int r, int c,
-                                            __nv_bfloat16* __restrict__ out,
-                                            __nv_bfloat16* __restrict__ residual, bool gated) {
-  const int H = dm.H, k = dm.k;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int i0 = 0; i0 < k; i0 += 8) {
-    float4 ya[8], yb[8];
-    float wv[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = i0 + j;
-      if (i < k) {
-        const float4* yp = reinterpret_cast<const float4*>(s.y + (size_t)(r * k + i) * H) + 2 * c;
-        ya[j] = __ldcg(yp);
-        yb[j] = __ldcg(yp + 1);
-        wv[j] = s.wts[r * k + i];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (i0 + j < k) {
-        acc[0] += wv[j] * ya[j].x; acc[1] += wv[j] * ya[j].y;
-        acc[2] += wv[j] * ya[j].z; acc[3] += wv[j] * ya[j].w;
-        acc[4] += wv[j] * yb[j].x; acc[5] += wv[j] * yb[j].y;
-        acc[6] += wv[j] * yb[j].z; acc[7] += wv[j] * yb[j].w;
-      }
-    }
-  }
-  // + the shared expert's output, times its row's sigmoid gate when the layer has one
-  const float4* ysp = reinterpret_cast<const float4*>(s.ys + (size_t)r * H) + 2 * c;
-  const float4 s0 = __ldcg(ysp), s1 = __ldcg(ysp + 1);
-  const float gt = gated ? __ldcg(s.sgate + r) : 1.f;
-  acc[0] = fmaf(gt, s0.x, acc[0]); acc[1] = fmaf(gt, s0.y, acc[1]);
-  acc[2] = fmaf(gt, s0.z, acc[2]); acc[3] = fmaf(gt, s0.w, acc[3]);
-  acc[4] = fmaf(gt, s1.x, acc[4]); acc[5] = fmaf(gt, s1.y, acc[5]);
-  acc[6] = fmaf(gt, s1.z, acc[6]); acc[7] = fmaf(gt, s1.w, acc[7]);
-  uint32_t o[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    o[q] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q])) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q + 1])) << 16);
-  reinterpret_cast<uint4*>(out + (size_t)r * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
-  reinterpret_cast<uint4*>(residual + (size_t)r * H)[c] =
-      __ldcg(reinterpret_cast<const uint4*>(s.rnew + (size_t)r * H) + c);
 }
 
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
@@ -378,181 +315,5 @@ cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                   residual, wait_tiles, budget_ns, gated);
 }
 
-
-// ------------------------------------------------------- single persistent launch ----
-// The whole call in one launch whose CTAs are all resident (a cooperative launch): add +
-// RMSNorm (one warp per row), router logits (one warp per expert), top-k + dedup (CTA 0),
-// the shared and routed gate/up, the shared and routed down (the warp-level loops above),
-// and the combine with the residual update, separated by grid-wide barriers.  A barrier
-// is a count of arrivals and a generation word in the handle's counters: the last CTA to
-// arrive resets the count and advances the generation with a release store; the others
-// wait (bounded, acquire) until the generation differs from the one they read on arrival.
-// The generation only grows, so it tags every barrier of every call and nothing is reset
-// between calls or graph replays.  A CTA whose wait expires sets MOE_TAIL_STATUS_TIMEOUT
-// and leaves; the others then give up at the next barrier the same way.
-// Sources: "[AMD] integrate kimi k3 monokernel" page, Motivation and Kernel Replacement
-// (the layer tail as one resident launch whose stages hand over through in-kernel flags);
-// "Split the Kimi3 AttnRes mix across CTAs for decode rows" page (a tag per call instead of
-// a reset).
-constexpr int kPersistWarps = 8;
-constexpr int kCtrPersistArrive = 8;  // counters words outside every other use
-constexpr int kCtrPersistGen = 9;
-static_assert(kCtrOutProj < kCtrPersistArrive && kCtrPersistGen < kCtrGUDone &&
-                  kCtrPersistGen != kCtrSharedGUDone,
-              "the persistent launch's counter words are free");
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Grid-wide barrier; false when this CTA's wait expired (the status word says so).
-__device__ __forceinline__ bool grid_barrier(const Scratch& s, uint64_t budget_ns) {
-  __shared__ int s_ok;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t* arrive = &s.counters[kCtrPersistArrive];
-    uint32_t* gen = &s.counters[kCtrPersistGen];
-    const uint32_t g0 = ld_acquire_u32(gen);
-    __threadfence();  // this CTA's writes (seen by thread 0 through the CTA barrier) first
-    int ok = 1;
-    if (atomicAdd(arrive, 1u) == gridDim.x - 1) {
-      atomicExch(arrive, 0u);
-      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(gen), "r"(g0 + 1u) : "memory");
-    } else {
-      const uint64_t t0 = globaltimer();
-      for (uint32_t i = 1; ld_acquire_u32(gen) == g0; ++i) {
-        __nanosleep(32);
-        if ((i & 15) == 0 && globaltimer() - t0 > budget_ns) {
-          set_status(s.status, kStatusTimeout);
-          ok = 0;
-          break;
-        }
-      }
-    }
-    __threadfence();
-    s_ok = ok;
-  }
-  __syncthreads();
-  return s_ok != 0;
-}
-
-// Add + RMSNorm of row r by one warp: r_new = bf16(x + residual) to scratch, rstd from the
-// fp32 sum of squares of r_new (lane-strided, butterfly, lane 0's value for every lane),
-// n = bf16(r_new * rstd * gamma); with a shared-expert gate, its sigmoid of n . g.
-__device__ __forceinline__ void norm_row_warp(int r, int lane, const Dims& dm,
-                                              const __nv_bfloat16* __restrict__ x,
-                                              const __nv_bfloat16* __restrict__ residual,
-                                              const Weights& w, const Scratch& s) {
-  const int H = dm.H;
-  const uint4* x4 = reinterpret_cast<const uint4*>(x + (size_t)r * H);
-  const uint4* r4 = reinterpret_cast<const uint4*>(residual + (size_t)r * H);
-  const uint4* g4 = reinterpret_cast<const uint4*>(w.gamma);
-  uint4* rn4 = reinterpret_cast<uint4*>(s.rnew + (size_t)r * H);
-  uint4* n4 = reinterpret_cast<uint4*>(s.n + (size_t)r * H);
-  float ss = 0.f;
-  for (int c = lane; c < H / 8; c += 32) {
-    const uint4 xv = __ldg(x4 + c), rv = __ldcg(r4 + c);
-    const uint4 o = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
-                               add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w));
-    rn4[c] = o;
-    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      ss = fmaf(bf16_lo(ow[i]), bf16_lo(ow[i]), ss);
-      ss = fmaf(bf16_hi(ow[i]), bf16_hi(ow[i]), ss);
-    }
-  }
-  ss = __shfl_sync(0xffffffffu, warp_sum(ss), 0);
-  const float rstd = 1.0f / sqrtf(ss / (float)H + dm.eps);
-  const uint4* wg4 = reinterpret_cast<const uint4*>(w.wsg);
-  float zg = 0.f;
-  for (int c = lane; c < H / 8; c += 32) {
-    const uint4 xv = __ldg(x4 + c), rv = __ldcg(r4 + c), gv = __ldg(g4 + c);
-    const uint4 o = make_uint4(add_bf16x2(xv.x, rv.x), add_bf16x2(xv.y, rv.y),
-                               add_bf16x2(xv.z, rv.z), add_bf16x2(xv.w, rv.w));
-    const uint4 nv = make_uint4(norm_bf16x2(o.x, gv.x, rstd), norm_bf16x2(o.y, gv.y, rstd),
-                                norm_bf16x2(o.z, gv.z, rstd), norm_bf16x2(o.w, gv.w, rstd));
-    n4[c] = nv;
-    if (wg4) {
-      const uint4 wv = __ldg(wg4 + c);
-      const uint32_t nw[4] = {nv.x, nv.y, nv.z, nv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        zg = fmaf(bf16_lo(nw[i]), bf16_lo(ww[i]), zg);
-        zg = fmaf(bf16_hi(nw[i]), bf16_hi(ww[i]), zg);
-      }
-    }
-  }
-  if (wg4) {
-    const float z = __shfl_sync(0xffffffffu, warp_sum(zg), 0);
-    if (lane == 0) s.sgate[r] = 1.0f / (1.0f + expf(-z));
-  }
-}
-
-__global__ void __launch_bounds__(kPersistWarps * 32, 1)
-k_tail_persistent(Dims dm, Weights w, Scratch s, const __nv_bfloat16* __restrict__ x,
-                  const __nv_bfloat16* __restrict__ residual_in,
-                  __nv_bfloat16* __restrict__ residual, __nv_bfloat16* __restrict__ out,
-                  uint64_t budget_ns, int stall) {
-  // failure-injection switch: CTA 0 never arrives at a barrier, so the others' bounded
-  // waits expire (tests the timeout path; never set in production)
-  if (stall && blockIdx.x == 0) return;
-  const int lane = threadIdx.x & 31;
-  const long long gw = (long long)blockIdx.x * kPersistWarps + (threadIdx.x >> 5);
-  const long long nw = (long long)gridDim.x * kPersistWarps;
-  // 1. add + RMSNorm
-  for (long long r = gw; r < dm.R; r += nw) norm_row_warp((int)r, lane, dm, x, residual_in, w, s);
-  if (!grid_barrier(s, budget_ns)) return;
-  // 2. router logits
-  for (long long e = gw; e < dm.E; e += nw)
-    router_warp(s.n, w.w_r, s.logits, dm.R, dm.H, dm.E, (int)e, lane);
-  if (!grid_barrier(s, budget_ns)) return;
-  // 3. top-k and the dedup
-  if (blockIdx.x == 0)
-    topk_dedup_block<false>(s.logits, s.ids, s.wts, s.n_distinct, s.uniq, s.user_off,
-                            s.user_list, s.status, dm.R, dm.E, dm.k);
-  if (!grid_barrier(s, budget_ns)) return;
-  // 4. gate/up, 5. down
-  shared_gateup_work(gw, nw, dm, w, s);
-  routed_gateup_work(gw, nw, dm, w, s);
-  if (!grid_barrier(s, budget_ns)) return;
-  shared_down_work(gw, nw, dm, w, s);
-  routed_down_work(gw, nw, dm, w, s);
-  if (!grid_barrier(s, budget_ns)) return;
-  // 6. combine and the residual update
-  const int ng = dm.H / 8;
-  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < (long long)dm.R * ng;
-       t += (long long)gridDim.x * blockDim.x)
-    combine_one(dm, s, (int)(t / ng), (int)(t % ng), out, residual, w.wsg != nullptr);
-}
-
-cudaError_t persistent_reset(const Scratch& s) {
-  return cudaMemset(s.counters + kCtrPersistArrive, 0, 2 * sizeof(uint32_t));
-}
-
-cudaError_t persistent_blocks_per_sm(int* blocks) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, k_tail_persistent,
-                                                       kPersistWarps * 32, 0);
-}
-
-cudaError_t launch_persistent(const Dims& d, const __nv_bfloat16* x,
-                              const __nv_bfloat16* residual_in, __nv_bfloat16* residual,
-                              __nv_bfloat16* out, const Weights& w, const Scratch& s, int grid,
-                              uint64_t budget_ns, bool stall, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kPersistWarps * 32);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_tail_persistent, d, w, s, x, residual_in, residual, out,
-                            budget_ns, stall ? 1 : 0);
-}
 
 }  // namespace mtail

@@ -821,7 +821,7 @@ int make_stream_maps(StreamMaps* out, const Dims& d, const Weights& w, const Scr
 // travel as scale-factor atoms by plain bulk copies).  Returns 0,
 // -1 (no encoder) or -2 (encoding failed).
 int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights& w,
-                 const Scratch& s) {
+                 const Scratch& s, int smem_limit) {
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return -1;
   memset(out, 0, sizeof(*out));
@@ -829,7 +829,7 @@ int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights
   out->ws2 = sm.ws2;
   out->n = sm.n;
   out->ms = sm.ms;
-  out->lay = make_tc_layout(d.Rmax, d.k);
+  out->lay = make_tc_layout(d.Rmax, d.k, smem_limit);
   const uint32_t nmax = (uint32_t)out->lay.nmax;
   const uint64_t H = d.H, I = d.I, R4 = 4ull * d.Rmax, P4 = 4ull * d.Rmax * d.k;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;

@@ -14,7 +14,6 @@ constexpr int kStageW = 16384;    // 128 weight rows x 128 bytes
 constexpr int kWinK = 2048;       // K elements per scale window
 constexpr int kWinStages = kWinK / kChunkF4;
 constexpr int kWinW = 8192;       // weight scales of one window: 128 rows x 64 bytes
-constexpr int kSmemLimit = 232448;
 
 enum : int { kSharedGU = 0, kRoutedGU = 1, kSharedDN = 2, kRoutedDN = 3, kOutProj = 4 };
 

@@ -52,8 +52,12 @@
 //   * tensor memory (512 columns): two accumulator slots x two issuers x N columns, and a
 //     ring of per-stage scale-factor slots (16 columns each); every wait is bounded, and a
 //     CTA that gives up lets its copies and MMAs finish before it frees its tensor memory.
+#include <algorithm>
 #include <cstring>
 
+#include "k_combine.cuh"
+#include "k_front.cuh"
+#include "k_persist.cuh"
 #include "k_stream_common.cuh"
 
 namespace mtail {
@@ -206,14 +210,16 @@ struct TcPtrs {
   uint64_t* tables;  // [1] epilogue warps -> producer: routing tables copied (gate/up launch)
 };
 
-__device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L) {
+// set: which of the two barrier sets (the persistent launch's down roles take the second, so
+// that no arrival still landing on a barrier of its gate/up roles meets a new one)
+__device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L, int set) {
   TcPtrs p;
   p.stages = smem;
   p.xch = reinterpret_cast<float*>(smem + L.off_x);
   p.t_uniq = reinterpret_cast<int*>(smem + L.off_tab);
   p.t_off = p.t_uniq + L.tab_picks;
   p.t_users = p.t_off + L.tab_picks + 1;
-  p.full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
+  p.full = reinterpret_cast<uint64_t*>(smem + L.off_bar + set * L.bar_set_bytes);
   p.empty = p.full + kTcMaxStages;
   p.afull = p.empty + kTcMaxStages;
   p.aempty = p.afull + 2;
@@ -423,28 +429,118 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
 
 // ------------------------------------------------------------------------ kernel ----
 
-template <int PHASE, int NMAX>
+// The persistent launch's arguments (zero in the multi-kernel launches).
+struct PersistArgs {
+  const __nv_bfloat16* x;
+  __nv_bfloat16* residual;
+  __nv_bfloat16* out;
+  RouterPlan rp;
+  int stall;  // failure injection: CTA 0 leaves at once, the others' barrier waits expire
+};
+
+// The expert roles of one CTA over the items of launch phases PH0..PH1 (0 = gate/up, 1 =
+// down): one phase per launch in the multi-kernel form (PH0 == PH1); in the single persistent
+// launch (PH0 = 0, PH1 = 1) the gate/up roles and then, shared and tensor memory set up afresh
+// with a second barrier set, the down roles, between the front and the combine below.
+// --------------------------------------------------------- single persistent launch ----
+// The whole call in one cooperative launch of one CTA per SM (224 threads, the streaming
+// kernels' shared-memory plan): add + RMSNorm (CTA r takes row r), a grid barrier, the
+// router's parts as virtual CTAs spread over the grid (the last part ranks the experts,
+// builds the dedup tables and publishes them), then the expert roles of the streaming
+// kernels over the gate/up items and, once none is left, over the down items (a CTA starts on
+// its shared-expert items at once; routed items wait for the published routing, down items
+// for the gate/up items of their expert), then the combine (each warp waits for the down items
+// of its outputs).  Only the norm -> router hand-over is a grid barrier; every later one is
+// a count per expert or per output tile, as between the launches of the multi-kernel form.
+// Sources: "[AMD] integrate kimi k3 monokernel" page, Motivation and Kernel Replacement (the
+// layer tail as one resident launch whose stages hand over through in-kernel flags); "Split
+// the Kimi3 AttnRes mix across CTAs for decode rows" page (a tag per call instead of a
+// reset, here the barrier's generation word).
+template <int PH0, int PH1, int NMAX>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
-            uint64_t budget_ns, uint32_t debug) {
+            uint64_t budget_ns, uint32_t debug, PersistArgs pa) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const TcLayout& lay = maps.lay;
+  constexpr bool kPersist = PH0 != PH1;
+  // failure-injection switch of the persistent launch (never set in production)
+  if (kPersist && pa.stall && blockIdx.x == 0) return;
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) set_status(s.status, kStatusBadTile);
-    return;
+    return;  // (persistent launch: the other CTAs' barrier waits expire)
   }
-  const TcPtrs sp = tc_carve(smem, lay);
+  if constexpr (kPersist) {
+    __shared__ float part[kTcThreads / 32];
+    __shared__ int s_last;
+    if (threadIdx.x == 0) tl_first(s.tl, kTlNormStart);
+    // 1. the call's counter words (not the barrier's); this CTA's first router part's weights
+    //    (they depend on nothing); add + RMSNorm, each row split over P CTAs.  The residual is
+    //    read here and rewritten by the combine, after the barrier below.
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i < kCtrWords; i += kTcThreads)
+        if (i != kCtrPersistArrive && i != kCtrPersistGen) s.counters[i] = 0u;
+    const int nparts = pa.rp.tiles * pa.rp.parts;
+    if ((int)blockIdx.x < nparts)
+      router_stage_w<kTcThreads>(smem, w.w_r, blockIdx.x % pa.rp.tiles, blockIdx.x / pa.rp.tiles,
+                                 pa.rp.plen, dm.H, dm.E);
+    const int P = max(1, min((int)gridDim.x / dm.R, dm.H / 256));
+    for (int v = blockIdx.x; v < dm.R * P; v += gridDim.x)
+      add_rmsnorm_part<kTcThreads>(v % dm.R, v / dm.R, P, pa.x, pa.residual, w.gamma, s.rnew,
+                                   s.n, dm.H, dm.eps, w.wsg,
+                                   s.gate_part + (size_t)(v % dm.R) * kMaxNormParts, s.np4,
+                                   s.np4a, part);
+    if (threadIdx.x == 0 && (int)blockIdx.x < dm.R * P) tl_last(s.tl, kTlNormEnd);
+    if (!grid_barrier(s, budget_ns)) return;
+    // each row's gate from its parts' logits, added in part order (before this CTA's router
+    // ticket, which orders it before every later reader)
+    if (w.wsg && blockIdx.x == 0)
+      for (int r = threadIdx.x; r < dm.R; r += kTcThreads) {
+        float z = 0.f;
+        for (int q = 0; q < P; ++q) z += __ldcg(s.gate_part + (size_t)r * kMaxNormParts + q);
+        s.sgate[r] = 1.0f / (1.0f + expf(-z));
+      }
+    // 2. the router's parts (the first one's weights are already on their way)
+    if (threadIdx.x == 0) tl_first(s.tl, kTlRouterStart);
+    for (int v = blockIdx.x; v < nparts; v += gridDim.x) {
+      const int tile = v % pa.rp.tiles, p = v / pa.rp.tiles;
+      if (v != (int)blockIdx.x)
+        router_stage_w<kTcThreads>(smem, w.w_r, tile, p, pa.rp.plen, dm.H, dm.E);
+      if (router_part<kTcThreads / 32>(smem, s, tile, p, pa.rp.plen, pa.rp.red_off, dm.R, dm.H,
+                                       dm.E, (uint32_t)nparts, &s_last))
+        router_finish<kTcThreads, true>(smem, s, pa.rp.parts, dm.R, dm.E, dm.k);
+      __syncthreads();
+    }
+    // The expert roles' copies read activations written with ordinary stores earlier in this
+    // launch (n and its planes, before the barrier; the producer is thread 0, which took the
+    // barrier's acquire): order those writes first.
+    if (threadIdx.x == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      tl_first(s.tl, kTlGateUpStart);
+    }
+  } else {
+    if (threadIdx.x == 0) tl_first(s.tl, PH0 == 0 ? kTlGateUpStart : kTlDownStart);
+  }
+#pragma unroll
+  for (int PHASE = PH0; PHASE <= PH1; ++PHASE) {
+  if (kPersist && PHASE == 1 && threadIdx.x == 0) tl_first(s.tl, kTlDownStart);
+  // trigger: release the next launch once the barriers are set up (multi-kernel form);
+  // bar_set: the persistent launch's down roles take the second barrier set, so that no
+  // arrival still landing on a barrier of its gate/up roles meets a new one; last: the CTA
+  // allocates no tensor memory after this phase (it gives up its allocation permit)
+  const bool trigger = !kPersist;
+  const int bar_set = (kPersist && PHASE == 1) ? 1 : 0;
+  const bool last = PHASE == PH1;
+  const TcLayout& lay = maps.lay;
+  const TcPtrs sp = tc_carve(smem, lay, bar_set);
   const int S = lay.stages;
   constexpr uint32_t A = kAccSlots<NMAX>;
-  if (threadIdx.x == 0) tl_first(s.tl, PHASE == 0 ? kTlGateUpStart : kTlDownStart);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // The gate/up launch starts while the router still runs (its shared-expert items need only
-  // n, which the norm launch finished before the router's wait returned): it splits the
-  // shared items by the call's largest possible distinct count, and its routed items wait for
-  // the tables (copied to shared memory by the epilogue warps once the router's last CTA has
-  // published them).  The down launch starts after every gate/up CTA, and waits for the
-  // published routing once before it reads the tables.
+  // Gate/up items start while the router still runs (the shared-expert items need only n,
+  // complete before the router's wait returned): the shared items are split by the call's
+  // largest possible distinct count, and the routed items wait for the tables (copied to
+  // shared memory by the epilogue warps once the router's last CTA has published them).  A
+  // down-only launch starts after every gate/up CTA, and waits for the published routing once
+  // before it reads the tables.
   const int Dmax = min(dm.E, dm.R * dm.k);
   const int P = (PHASE == 0) ? shared_parts(dm, Dmax, (int)gridDim.x) : 1;
   const int n_shared = (PHASE == 0) ? (dm.Is / 64) * P : 0;  // items that need no routing
@@ -454,12 +550,12 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       set_status(s.status, kStatusTimeout);
     __syncthreads();
     D = min(max(__ldcg(s.n_distinct), 1), kMaxPicks);
-    n_items = items_of(PHASE, dm, D);
     for (int i = threadIdx.x; i < D; i += kTcThreads) sp.t_uniq[i] = __ldcg(s.uniq + i);
     for (int i = threadIdx.x; i <= D; i += kTcThreads) sp.t_off[i] = __ldcg(s.user_off + i);
     for (int i = threadIdx.x; i < dm.R * dm.k; i += kTcThreads)
       sp.t_users[i] = __ldcg(s.user_list + i);
     if (threadIdx.x == 0) *sp.sD = D;
+    n_items = items_of(1, dm, D);
   }
   Tables tb;
   tb.uniq = sp.t_uniq;
@@ -481,13 +577,13 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     if (PHASE == 0) *sp.sD = 1;  // until the routing is known (only routed items read it)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    pdl_trigger();  // the next launch may queue for SMs from now on (it waits on counts)
+    if (trigger) pdl_trigger();  // the next launch may queue for SMs (it waits on counts)
   }
   if (warp == kTcWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(sp.tbase)),
                  "n"(kTcCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    if (last) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
@@ -499,14 +595,18 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     // ---------------------------------------------------------------- producer ----
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      // scale atoms per weight tile: over H (gate/up) or I (down), two per stage
-      const int ga = sf_atoms_per_tile(PHASE == 0 ? dm.H : dm.I);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t pend = 0u, pend_par = 0u;
       bool skip_first = PHASE == 0 && (debug & kDebugStallFirstStage) && blockIdx.x == 0;
-      // a CTA's first item is its index; later ones come from the counter (from gridDim.x on)
-      int item = (int)blockIdx.x;
+      // scale atoms per weight tile: over H (gate/up) or I (down), two per stage
+      const int ga = sf_atoms_per_tile(PHASE == 0 ? dm.H : dm.I);
+      // a CTA's first item is its index, later ones come from the counter (from gridDim.x on);
+      // the persistent launch's gate/up items all come from the counter (its CTAs reach those
+      // roles at different times: the ones without a router part first)
+      const bool claim_all = kPersist && PHASE == 0;
+      const int base = claim_all ? 0 : (int)gridDim.x;
+      int item = claim_all ? (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u) : (int)blockIdx.x;
       bool have_tables = (PHASE == 1);
       while (ok) {
         if (!have_tables && item >= n_shared) {
@@ -517,7 +617,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
           n_items = n_shared + D * (dm.I / 64);
         }
         if (have_tables && item >= n_items) break;
-        const int next = (int)gridDim.x + (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
+        const int next = base + (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u);
         const Item it = decode_tc(PHASE, item, dm, tb, D, P);
         const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
         const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : (it.U <= 16) ? 2 : 3;
@@ -759,13 +859,101 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
                  "n"(kTcCols));
   }
+  }
+  if constexpr (kPersist) {
+    // 4. the combine: thread t of the grid takes 8-output groups t, t + grid threads, ...
+    if (threadIdx.x == 0) tl_first(s.tl, kTlCombineStart);
+    const int ng = dm.H / 8;  // a multiple of 32: a warp's groups lie in one row
+    for (int u = blockIdx.x * kTcThreads + threadIdx.x; u < dm.R * ng; u += gridDim.x * kTcThreads) {
+      const int r = u / ng, c = u % ng;
+      if (!combine_wait_tiles(s, c, budget_ns)) return;
+      combine_one(dm, s, r, c, pa.out, pa.residual, w.wsg != nullptr);
+    }
+    if ((threadIdx.x & 31) == 0) tl_last(s.tl, kTlCombineEnd);
+  }
+}
+
+template <int NMAX>
+static cudaError_t persist_prepare_one(int* blocks, int* smem_limit) {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, k_stream_tc<0, 1, NMAX>);
+  if (e != cudaSuccess) return e;
+  *smem_limit = kSmemLimit - (int)a.sharedSizeBytes;
+  e = cudaFuncSetAttribute(k_stream_tc<0, 1, NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           *smem_limit);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, k_stream_tc<0, 1, NMAX>, kTcThreads,
+                                                      *smem_limit);
+  return e;
+}
+
+cudaError_t persistent_smem_limit(int nmax, int* smem_limit) {
+  int blocks = 0;
+  if (nmax == 16) return persist_prepare_one<16>(&blocks, smem_limit);
+  if (nmax == 32) return persist_prepare_one<32>(&blocks, smem_limit);
+  if (nmax == 64) return persist_prepare_one<64>(&blocks, smem_limit);
+  return persist_prepare_one<128>(&blocks, smem_limit);
+}
+
+cudaError_t persistent_prepare(const TcMaps& maps, int* blocks_per_sm) {
+  int limit = 0;
+  const int nmax = maps.lay.nmax;
+  if (nmax == 16) return persist_prepare_one<16>(blocks_per_sm, &limit);
+  if (nmax == 32) return persist_prepare_one<32>(blocks_per_sm, &limit);
+  if (nmax == 64) return persist_prepare_one<64>(blocks_per_sm, &limit);
+  return persist_prepare_one<128>(blocks_per_sm, &limit);
+}
+
+template <int NMAX>
+static cudaError_t persist_launch(const TcMaps& maps, const Dims& d, const __nv_bfloat16* x,
+                                  __nv_bfloat16* residual, __nv_bfloat16* out, const Weights& w,
+                                  const Scratch& s, int grid, const RouterPlan& rp, size_t smem,
+                                  uint64_t budget_ns, int stall, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  PersistArgs pa;
+  pa.x = x;
+  pa.residual = residual;
+  pa.out = out;
+  pa.rp = rp;
+  pa.stall = stall;
+  return cudaLaunchKernelEx(&cfg, k_stream_tc<0, 1, NMAX>, maps, d, w, s, budget_ns, 0u, pa);
+}
+
+cudaError_t launch_persistent(const TcMaps& maps, const Dims& d, const __nv_bfloat16* x,
+                              __nv_bfloat16* residual, __nv_bfloat16* out, const Weights& w,
+                              const Scratch& s, int grid, uint64_t budget_ns, bool stall,
+                              cudaStream_t st) {
+  const RouterPlan rp = router_plan(d.R, d.H, d.E, kTcThreads / 32);
+  // the front's use of the same shared memory: gamma (2 H bytes), a router part, the last
+  // part's logits and top-k workspace
+  const size_t topk = (((size_t)d.R * d.E * 4 + 15) & ~(size_t)15) + kTopkWsBytes;
+  const size_t smem = std::max(std::max((size_t)maps.lay.smem_bytes, rp.smem),
+                               std::max((size_t)d.H * 2, topk));
+  const int nmax = maps.lay.nmax, st_ = stall ? 1 : 0;
+  if (nmax == 16) return persist_launch<16>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st);
+  if (nmax == 32) return persist_launch<32>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st);
+  if (nmax == 64) return persist_launch<64>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st);
+  return persist_launch<128>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st);
+}
+
+cudaError_t persistent_reset(const Scratch& s) {
+  return cudaMemset(s.counters + kCtrPersistArrive, 0, 2 * sizeof(uint32_t));
 }
 
 // -------------------------------------------------------------------- host side ----
 
 template <int PHASE, int NMAX>
 static cudaError_t tc_prepare_one() {
-  return cudaFuncSetAttribute(k_stream_tc<PHASE, NMAX>,
+  return cudaFuncSetAttribute(k_stream_tc<PHASE, PHASE, NMAX>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
@@ -786,8 +974,9 @@ template <int PHASE, int NMAX>
 static cudaError_t tc_launch(const TcMaps& maps, const Dims& d, const Weights& w,
                              const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                              bool pdl, uint32_t debug) {
-  return launch_k(k_stream_tc<PHASE, NMAX>, dim3(num_sms), dim3(kTcThreads),
-                  (size_t)maps.lay.smem_bytes, st, pdl, maps, d, w, s, budget_ns, debug);
+  return launch_k(k_stream_tc<PHASE, PHASE, NMAX>, dim3(num_sms), dim3(kTcThreads),
+                  (size_t)maps.lay.smem_bytes, st, pdl, maps, d, w, s, budget_ns, debug,
+                  PersistArgs{});
 }
 
 cudaError_t launch_stream_tc(int phase, const TcMaps& maps, const Dims& d, const Weights& w,
@@ -809,7 +998,7 @@ cudaError_t launch_stream_tc(int phase, const TcMaps& maps, const Dims& d, const
 // Shared-memory plan: stages of 16 KB weights + nmax x 128 B activations + 2 KB scale atoms,
 // as many as fit (up to kTcMaxStages, the tensor-memory scale ring), the epilogue exchange,
 // the dedup tables and the barriers.
-TcLayout make_tc_layout(int Rmax, int k) {
+TcLayout make_tc_layout(int Rmax, int k, int smem_limit) {
   TcLayout L;
   L.nmax = (Rmax <= 4) ? 16 : (Rmax <= 8) ? 32 : (Rmax <= 16) ? 64 : 128;
   L.aslots = (L.nmax <= 64) ? 2 : 1;
@@ -820,14 +1009,16 @@ TcLayout make_tc_layout(int Rmax, int k) {
   const int tab_bytes = ((3 * L.tab_picks + 1) * 4 + 127) & ~127;
   // mbarriers full, empty per stage + afull, aempty, drain (2 each) + tables; the stages'
   // item words; the accumulator slots' item words; tbase, eflag and sD
+  // (two sets of them)
   const int bar_bytes = (2 * kTcMaxStages + 7) * 8 + kTcMaxStages * 8 + 2 * 4 + 4 + 4 + 4;
-  const int fixed = x_bytes + tab_bytes + ((bar_bytes + 127) & ~127);
-  L.stages = (kSmemLimit - fixed) / L.stage_bytes;
+  L.bar_set_bytes = (bar_bytes + 127) & ~127;
+  const int fixed = x_bytes + tab_bytes + 2 * L.bar_set_bytes;
+  L.stages = (smem_limit - fixed) / L.stage_bytes;
   if (L.stages > kTcMaxStages) L.stages = kTcMaxStages;
   L.off_x = L.stages * L.stage_bytes;
   L.off_tab = L.off_x + x_bytes;
   L.off_bar = L.off_tab + tab_bytes;
-  L.smem_bytes = L.off_bar + ((bar_bytes + 127) & ~127);
+  L.smem_bytes = L.off_bar + 2 * L.bar_set_bytes;
   return L;
 }
 

@@ -84,8 +84,10 @@ static_assert(MOE_TAIL_TL_SLOTS == (int)kTlSlots, "timeline slots agree");
 
 // The expert stages run on the tcgen05 kernels unless a debug flag picks another form (the
 // mma.sync streaming kernels, the cross-checking CUDA-core kernels, or the fused front, which
-// writes no activation planes) or the handle is a persistent one.
+// writes no activation planes); the persistent launch runs them too (its debug flags other
+// than the stall injection do not apply).
 static bool uses_tc(const moe_tail_config_t* c) {
+  if (c->mode == MOE_TAIL_MODE_PERSISTENT) return true;
   return c->mode == MOE_TAIL_MODE_MULTI_KERNEL &&
          !(c->debug_flags & (MOE_TAIL_DEBUG_MMA_SYNC | MOE_TAIL_DEBUG_SIMPLE_KERNELS |
                              MOE_TAIL_DEBUG_FUSED_FRONT));
@@ -159,6 +161,7 @@ static size_t carve(const moe_tail_config_t* c, char* base, Scratch* s, size_t* 
   s->y = (float*)take(P * H * 4);
   s->ys = (float*)take(R * H * 4);
   s->sgate = (float*)take(R * 4);
+  s->gate_part = (float*)take(R * kMaxNormParts * 4);
   s->xproj = (__nv_bfloat16*)take(R * H * 2);
   s->xpart = (float*)take((size_t)kMaxOutProjParts * R * H * 4);
   s->gpart = (float*)take((size_t)std::min<size_t>(Is / 64, kMaxSharedSplitItems) *
@@ -214,13 +217,8 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   if (e == cudaSuccess) e = prepare_front_kernels();
   if (e == cudaSuccess && uses_tc(cfg)) e = prepare_stream_tc_kernels();
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
-  if (e == cudaSuccess && cfg->mode == MOE_TAIL_MODE_PERSISTENT) {
-    // one CTA per SM at most; the cooperative launch checks at run time that all fit
-    int per_sm = 0;
-    e = persistent_blocks_per_sm(&per_sm);
-    if (e == cudaSuccess && per_sm < 1) { delete h; return MOE_TAIL_ERR_NOT_CORESIDENT; }
-    h->persist_grid = h->num_sms;
-  }
+  if (e == cudaSuccess && cfg->mode == MOE_TAIL_MODE_PERSISTENT)
+    h->persist_grid = h->num_sms;  // one CTA per SM (checked once the layout is known)
   if (e != cudaSuccess) { delete h; return cuda_fail(e); }
   h->slab_bytes = carve(cfg, nullptr, &h->s, nullptr, nullptr);
   e = cudaMalloc(&h->slab, h->slab_bytes);
@@ -263,7 +261,19 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
       }
     }
     int mrc = make_stream_maps(&h->maps, d0, h->w, h->s);
-    if (mrc == 0 && uses_tc(cfg)) mrc = make_tc_maps(&h->tcmaps, h->maps, d0, h->w, h->s);
+    int limit = kSmemLimit;
+    if (mrc == 0 && cfg->mode == MOE_TAIL_MODE_PERSISTENT) {
+      const TcLayout l0 = make_tc_layout(d0.Rmax, d0.k, kSmemLimit);
+      if (persistent_smem_limit(l0.nmax, &limit) != cudaSuccess) mrc = -3;
+    }
+    if (mrc == 0 && uses_tc(cfg))
+      mrc = make_tc_maps(&h->tcmaps, h->maps, d0, h->w, h->s, limit);
+    if (mrc == 0 && cfg->mode == MOE_TAIL_MODE_PERSISTENT) {
+      // every CTA of the cooperative launch resident at once: one per SM
+      int per_sm = 0;
+      if (persistent_prepare(h->tcmaps, &per_sm) != cudaSuccess) mrc = -3;
+      else if (per_sm < 1) mrc = -4;
+    }
     if (mrc != 0) {
       cudaFree(h->slab);
       cudaFree(h->stage);
@@ -273,6 +283,8 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
         snprintf(g_cuda_err, sizeof(g_cuda_err), "no cuTensorMapEncodeTiled");
         return MOE_TAIL_ERR_CUDA;
       }
+      if (mrc == -3) return cuda_fail(cudaGetLastError());
+      if (mrc == -4) return MOE_TAIL_ERR_NOT_CORESIDENT;
       return MOE_TAIL_ERR_UNSUPPORTED;
     }
   }
@@ -338,9 +350,8 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   if (h->s.tl && (e = cudaMemsetAsync(h->s.tl, 0, kTlSlots * 8, st))) return cuda_fail(e);
   if (h->cfg.mode == MOE_TAIL_MODE_PERSISTENT) {
     // the whole call in one cooperative launch (such a handle has no out_proj stage)
-    MT_STAGE(launch_persistent(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
-                               (__nv_bfloat16*)residual, (__nv_bfloat16*)out, h->w, h->s,
-                               h->persist_grid, budget_ns,
+    MT_STAGE(launch_persistent(h->tcmaps, d, (const __nv_bfloat16*)x, (__nv_bfloat16*)residual,
+                               (__nv_bfloat16*)out, h->w, h->s, h->persist_grid, budget_ns,
                                (h->cfg.debug_flags & MOE_TAIL_DEBUG_STALL_FIRST_STAGE) != 0, st));
     h->last_rows = rows;
     return MOE_TAIL_OK;

@@ -20,6 +20,10 @@ constexpr int kMaxRows = 32;
 constexpr int kMaxRowsOther = 16;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxExperts = 1024;
+// dynamic shared memory a streaming CTA may take (the opt-in maximum per block)
+constexpr int kSmemLimit = 232448;
+// parts a row's add + RMSNorm may be split into (the persistent launch; H / 256 at most)
+constexpr int kMaxNormParts = 128;
 constexpr int kMaxPicks = kMaxRows * kMaxTopK;  // (row, slot) pairs of one call
 constexpr int kMaxOutProjParts = 8;  // K parts of an out_proj box at most
 // A shared-expert gate/up item (64 gate + 64 up rows over all of H) may be split along K into
@@ -87,6 +91,7 @@ struct Scratch {
   float* y;              // [Rmax*k, H] routed expert outputs
   float* ys;             // [Rmax, H] shared expert output
   float* sgate;          // [Rmax] sigmoid gate of the shared output (when a gate is given)
+  float* gate_part;      // [Rmax, kMaxNormParts] the persistent launch's per-part gate logits
   __nv_bfloat16* xproj;  // [Rmax, H] x = out_proj(attn) for moe_tail_run_attn (one K part)
   float* xpart;          // [kMaxOutProjParts, Rmax, H] fp32 sums of each out_proj K part
   float* gpart;          // [kMaxSharedSplitItems, kMaxSharedParts, 128, Rmax] fp32 sums of the
@@ -343,6 +348,7 @@ struct TcLayout {
   int stage_bytes;  // 16 KB weights + b_bytes + 2 KB scale-factor atoms
   int stages;
   int off_x, off_tab, off_bar, smem_bytes;
+  int bar_set_bytes;  // one set of barriers and item words (two sets follow off_bar)
   int tab_picks;    // entries of the dedup tables (rows x k of the handle)
 };
 
@@ -384,13 +390,23 @@ int router_max_parts();
 cudaError_t launch_stream(int phase, const StreamMaps& maps, const Dims& d, const Weights& w,
                           const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                           bool pdl, uint32_t debug);
-TcLayout make_tc_layout(int Rmax, int k);
+// smem_limit: the dynamic shared memory the kernel may take (less for the persistent one,
+// whose front keeps static shared memory)
+TcLayout make_tc_layout(int Rmax, int k, int smem_limit);
 int make_tc_maps(TcMaps* out, const StreamMaps& sm, const Dims& d, const Weights& w,
-                 const Scratch& s);
+                 const Scratch& s, int smem_limit);
 cudaError_t prepare_stream_tc_kernels();
 cudaError_t launch_stream_tc(int phase, const TcMaps& maps, const Dims& d, const Weights& w,
                              const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                              bool pdl, uint32_t debug);
+// The router's parts (k_front.cu): 16-expert tiles x K parts of plen elements, the shared
+// memory of one part for `warps` warps and the offset of its reduction tiles in it.
+struct RouterPlan {
+  int tiles, parts, plen, red_off;
+  size_t smem;
+};
+RouterPlan router_plan(int R, int H, int E, int warps);
+
 // bytes of the two atom copies (w13a then w2a) and the launch that writes them from w13s, w2s
 size_t scale_atom_bytes(const Dims& d);
 cudaError_t launch_scale_atoms(const Dims& d, const Weights& w, uint8_t* atoms, cudaStream_t st);

@@ -126,10 +126,10 @@ def test_unsupported_configs_refused_before_device(lib, field, value):
     assert h.value is None
 
 
-@pytest.mark.parametrize("flags,mode,attn", [(16, 0, 0), (1, 0, 0), (8, 0, 0), (0, 1, 0),
-                                             (0, 0, 64)])
-def test_more_than_16_rows_only_in_the_default_form(lib, flags, mode, attn):
-    # mma.sync, cross-checking kernels, fused front, persistent mode, out_proj: 16 rows at most
+@pytest.mark.parametrize("flags,mode,attn", [(16, 0, 0), (1, 0, 0), (8, 0, 0), (0, 0, 64)])
+def test_more_than_16_rows_only_in_the_tensor_core_forms(lib, flags, mode, attn):
+    # mma.sync, cross-checking kernels, fused front, out_proj: 16 rows at most (the default
+    # form and the persistent launch, both on the tensor-core kernels, take up to 32)
     cfg = mt.make_config(gen.TailShape(24, 256, 8, 2, 128, 128, Ha=attn), debug_flags=flags,
                          mode=mode)
     w = mt.WeightPtrs(*([16] * 8 + ([0, 16] if attn else [])))  # never dereferenced

@@ -408,11 +408,6 @@ from moe_layer_tail_gb300 import MODE_PERSISTENT  # noqa: E402
 @pytest.mark.parametrize("name", list(gen.WORKLOADS))
 def test_persistent_mode_parity_full_size(name):
     wl, d, dev, orc = workload_inputs(name)
-    if wl.shape.R > 16:  # the persistent launch takes 16 rows at most: refused at create
-        with pytest.raises(MoeTailError) as ei:
-            MoeTail(wl.shape, dev, max_rows=wl.shape.R, mode=MODE_PERSISTENT)
-        assert ei.value.code == ERR_UNSUPPORTED
-        return
     tail = MoeTail(wl.shape, dev, max_rows=wl.shape.R, mode=MODE_PERSISTENT)
     assert tail.launches_per_run(wl.shape.R) == 1
     got = run_gpu(tail, d)
@@ -425,6 +420,7 @@ def test_persistent_mode_parity_full_size(name):
     (5, 768, 20, 4, 384, 192, True),    # ragged rows, shared-expert gate
     (16, 512, 12, 3, 256, 64, False),   # maximum rows, repeated experts
     (3, 512, 4, 4, 256, 192, True),     # k = E
+    (32, 1024, 40, 6, 384, 128, True),  # 32 rows (128 plane columns), half last down stage
 ])
 def test_persistent_mode_small_shapes(R, H, E, k, I, Is, gated):
     shape = gen.TailShape(R, H, E, k, I, Is)
