@@ -214,15 +214,15 @@ int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* out, int32_
 int moe_tail_run_attn(moe_tail_t* h, const void* attn, void* residual, void* out, int32_t rows,
                       void* stream);
 
-/* The same call on HOST buffers: copies x and residual to the handle's device staging
- * buffers, runs, copies residual and out back, and synchronises `stream` before returning.
- * Pinned host memory gives asynchronous copies; pageable memory works too.  When the three
- * buffers are one block [x; residual; out] (residual_host = x_host + rows*H*2 bytes and
- * out_host = residual_host + rows*H*2), x and residual go in one copy and residual and out
- * come back in one copy; if that block is page-locked and `stream` is not a default stream,
- * the first such call for a row count captures [copy in, the call's launches, copy out] as a
- * CUDA graph on `stream` and every later one replays it with its copies pointed at the
- * call's block (so the first call must not run inside another capture). */
+/* The same call on HOST buffers; synchronises `stream` before returning.  Host memory the
+ * device reaches directly (16-byte aligned buffers: any host memory on a device that uses the
+ * host's page tables, as on a Grace-Blackwell node over NVLink-C2C; else page-locked memory,
+ * mapped into the device's address space) is read and written in place by the call's
+ * kernels: x and residual read, out and residual written, no copy step.  Otherwise x and
+ * residual are copied to the handle's
+ * device staging buffers, the call runs there, and residual and out are copied back (one copy
+ * each way when the buffers form one block [x; residual; out], residual_host = x_host +
+ * rows*H*2 bytes and out_host = residual_host + rows*H*2). */
 int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host, void* out_host,
                       int32_t rows, void* stream);
 

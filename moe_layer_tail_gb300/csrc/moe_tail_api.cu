@@ -37,6 +37,7 @@ struct moe_tail {
   size_t slab_bytes;
   void* stage;         // device staging for moe_tail_run_host: x, residual, out
   void* atoms;         // the tensor-core form's copy of w13s and w2s in scale-factor atoms
+  int host_direct;     // the device reads pageable host memory through the host's page tables
   int device;
   int num_sms;
   int persist_grid;    // CTAs of the single persistent launch (MOE_TAIL_MODE_PERSISTENT)
@@ -45,11 +46,6 @@ struct moe_tail {
   int n_ev;
   size_t canary_off[kMaxCanaries];  // slab offsets of the guard words after each buffer
   int n_canary;
-  // moe_tail_run_host on page-locked buffers: one graph per row count of [copy in, the
-  // call's launches, copy out], its two copy nodes re-pointed at every run's buffers
-  cudaGraph_t hgraph[kMaxRows + 1];
-  cudaGraphExec_t hexec[kMaxRows + 1];
-  cudaGraphNode_t hin[kMaxRows + 1], hout[kMaxRows + 1];
 };
 
 static thread_local char g_cuda_err[256];
@@ -217,6 +213,9 @@ extern "C" int moe_tail_create(const moe_tail_config_t* cfg, const moe_tail_weig
   if (e == cudaSuccess) e = prepare_front_kernels();
   if (e == cudaSuccess && uses_tc(cfg)) e = prepare_stream_tc_kernels();
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&h->host_direct, cudaDevAttrPageableMemoryAccessUsesHostPageTables,
+                               h->device);
   if (e == cudaSuccess && cfg->mode == MOE_TAIL_MODE_PERSISTENT)
     h->persist_grid = h->num_sms;  // one CTA per SM (checked once the layout is known)
   if (e != cudaSuccess) { delete h; return cuda_fail(e); }
@@ -433,60 +432,17 @@ extern "C" int moe_tail_run_attn(moe_tail_t* h, const void* attn, void* residual
   return run_impl(h, nullptr, attn, residual, out, rows, stream);
 }
 
-static bool page_locked(const void* p) {
+// The device address of a page-locked host buffer, or null (pageable memory).  Page-locked
+// memory is mapped into the device's address space (unified addressing), so kernels read and
+// write it in place: over NVLink-C2C on a Grace-Blackwell node.
+static void* mapped_host(const void* p) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();  // pageable memory may report an error on some drivers: not sticky
-    return false;
+    return nullptr;
   }
-  return a.type == cudaMemoryTypeHost;
-}
-
-// Capture [copy in, the call, copy out] on `st` for `rows` rows once, keeping the copy nodes.
-static cudaError_t build_host_graph(moe_tail_t* h, int rows, const void* in_host, void* out_host,
-                                    char* din, char* dout, size_t bytes2, cudaStream_t st) {
-  cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
-  if (e != cudaSuccess) return e;
-  cudaError_t e1 = cudaMemcpyAsync(din, in_host, bytes2, cudaMemcpyHostToDevice, st);
-  const int rc = (e1 == cudaSuccess)
-                     ? run_impl(h, din, nullptr, din + bytes2 / 2, din + bytes2, rows, st)
-                     : MOE_TAIL_ERR_CUDA;
-  cudaError_t e2 = cudaMemcpyAsync(out_host, dout, bytes2, cudaMemcpyDeviceToHost, st);
-  cudaGraph_t g = nullptr;
-  e = cudaStreamEndCapture(st, &g);
-  if (e == cudaSuccess && (e1 != cudaSuccess || rc != MOE_TAIL_OK || e2 != cudaSuccess))
-    e = cudaErrorUnknown;
-  if (e != cudaSuccess) {
-    if (g) cudaGraphDestroy(g);
-    return e;
-  }
-  // the two copy nodes: the one that writes device memory and the one that reads it
-  size_t n = 0;
-  cudaGraphGetNodes(g, nullptr, &n);
-  cudaGraphNode_t nodes[64];
-  if (n > 64) n = 64;
-  e = cudaGraphGetNodes(g, nodes, &n);
-  cudaGraphNode_t gin = nullptr, gout = nullptr;
-  for (size_t i = 0; e == cudaSuccess && i < n; ++i) {
-    cudaGraphNodeType t;
-    if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess || t != cudaGraphNodeTypeMemcpy) continue;
-    cudaMemcpy3DParms p = {};
-    if (cudaGraphMemcpyNodeGetParams(nodes[i], &p) != cudaSuccess) continue;
-    if (p.kind == cudaMemcpyHostToDevice) gin = nodes[i];
-    else if (p.kind == cudaMemcpyDeviceToHost) gout = nodes[i];
-  }
-  cudaGraphExec_t ex = nullptr;
-  if (e == cudaSuccess && (!gin || !gout)) e = cudaErrorUnknown;
-  if (e == cudaSuccess) e = cudaGraphInstantiate(&ex, g, 0);
-  if (e != cudaSuccess) {
-    cudaGraphDestroy(g);
-    return e;
-  }
-  h->hgraph[rows] = g;
-  h->hexec[rows] = ex;
-  h->hin[rows] = gin;
-  h->hout[rows] = gout;
-  return cudaSuccess;
+  if (a.type != cudaMemoryTypeHost) return nullptr;
+  return a.devicePointer;
 }
 
 extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host,
@@ -503,22 +459,19 @@ extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residu
   const bool in_block = (const char*)residual_host == (const char*)x_host + bytes;
   const bool out_block = (char*)out_host == (char*)residual_host + bytes;
   cudaError_t e;
-  if (in_block && out_block && st != nullptr && st != cudaStreamLegacy && st != cudaStreamPerThread &&
-      h->n_ev == 0 && page_locked(x_host)) {
-    // one [x; residual; out] block in page-locked memory: replay this row count's graph
-    if (!h->hexec[rows]) {
-      e = build_host_graph(h, rows, x_host, residual_host, dx, dres, 2 * bytes, st);
-      if (e != cudaSuccess) return cuda_fail(e);
+  {
+    // host memory the device reaches directly (any host memory where the device uses the
+    // host's page tables, else page-locked buffers): the call's kernels read x and the
+    // residual and write out and the residual in place, no copy step
+    void* mx = h->host_direct ? (void*)x_host : mapped_host(x_host);
+    void* mr = h->host_direct ? residual_host : mx ? mapped_host(residual_host) : nullptr;
+    void* mo = h->host_direct ? out_host : mr ? mapped_host(out_host) : nullptr;
+    if (mo && aligned16(mx) && aligned16(mr) && aligned16(mo)) {
+      const int rc = run_impl(h, mx, nullptr, mr, mo, rows, stream);
+      if (rc) return rc;
+      e = cudaStreamSynchronize(st);
+      return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
     }
-    e = cudaGraphExecMemcpyNodeSetParams1D(h->hexec[rows], h->hin[rows], dx, x_host, 2 * bytes,
-                                           cudaMemcpyHostToDevice);
-    if (e == cudaSuccess)
-      e = cudaGraphExecMemcpyNodeSetParams1D(h->hexec[rows], h->hout[rows], residual_host, dres,
-                                             2 * bytes, cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess) e = cudaGraphLaunch(h->hexec[rows], st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e == cudaSuccess) h->last_rows = rows;
-    return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
   }
   if (in_block) {
     e = cudaMemcpyAsync(dx, x_host, 2 * bytes, cudaMemcpyHostToDevice, st);
@@ -591,10 +544,6 @@ extern "C" void moe_tail_destroy(moe_tail_t* h) {
   cudaGetDevice(&cur);
   if (cur != h->device) cudaSetDevice(h->device);
   cudaDeviceSynchronize();
-  for (int r = 0; r <= kMaxRows; ++r) {
-    if (h->hexec[r]) cudaGraphExecDestroy(h->hexec[r]);
-    if (h->hgraph[r]) cudaGraphDestroy(h->hgraph[r]);
-  }
   cudaFree(h->slab);
   cudaFree(h->stage);
   if (h->atoms) cudaFree(h->atoms);

@@ -328,12 +328,20 @@ def test_run_host_matches_device_run():
     tail.run_host(x, res, out)
     assert np.array_equal(bf16_tensor_to_bits(out), out_d)
     assert np.array_equal(bf16_tensor_to_bits(res), res_d)
+    # pageable buffers: in place where the device uses the host's page tables, else copied
+    x2 = torch.from_numpy(d["x"].view(np.int16).copy()).view(torch.bfloat16)
+    res2 = torch.from_numpy(d["residual"].view(np.int16).copy()).view(torch.bfloat16)
+    out2 = torch.empty_like(x2)
+    assert not x2.is_pinned()
+    tail.run_host(x2, res2, out2)
+    assert np.array_equal(bf16_tensor_to_bits(out2), out_d)
+    assert np.array_equal(bf16_tensor_to_bits(res2), res_d)
 
 
-def test_run_host_block_graph_replays_match_device_runs():
-    """One page-locked [x; residual; out] block per call on a non-default stream: the entry
-    point replays a captured graph (one per row count) with its copies re-pointed at each
-    call's block; every call matches the device-buffer run bit for bit."""
+def test_run_host_page_locked_buffers_match_device_runs():
+    """Page-locked host buffers, read and written in place by the call's kernels, on a
+    non-default stream, over calls of two row counts (a block [x; residual; out] per call):
+    every call matches the device-buffer run bit for bit."""
     shape, d = _small(14, R=4, H=512, E=12, k=3, I=256, Is=128)
     dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
     tail = MoeTail(shape, dev, max_rows=4)
