@@ -214,15 +214,21 @@ int moe_tail_run(moe_tail_t* h, const void* x, void* residual, void* out, int32_
 int moe_tail_run_attn(moe_tail_t* h, const void* attn, void* residual, void* out, int32_t rows,
                       void* stream);
 
-/* The same call on HOST buffers; synchronises `stream` before returning.  Host memory the
- * device reaches directly (16-byte aligned buffers: any host memory on a device that uses the
- * host's page tables, as on a Grace-Blackwell node over NVLink-C2C; else page-locked memory,
- * mapped into the device's address space) is read and written in place by the call's
- * kernels: x and residual read, out and residual written, no copy step.  Otherwise x and
- * residual are copied to the handle's
- * device staging buffers, the call runs there, and residual and out are copied back (one copy
- * each way when the buffers form one block [x; residual; out], residual_host = x_host +
- * rows*H*2 bytes and out_host = residual_host + rows*H*2). */
+/* The same call on HOST buffers; returns once out and residual hold the call's results.
+ * Host memory the device reaches directly (16-byte aligned buffers: any host memory on a
+ * device that uses the host's page tables, as on a Grace-Blackwell node over NVLink-C2C; else
+ * page-locked memory, mapped into the device's address space) is read and written in place by
+ * the call's kernels: x and residual read, out and residual written, no copy step (on a
+ * non-default stream the first such call for a row count captures the call's launches as a
+ * CUDA graph, so it must not run inside another capture, and every later one replays it with
+ * its buffers passed through a page-locked argument block of the handle); the call's last
+ * kernel then sets a page-locked completion word of the handle that this function polls
+ * (the stream may still be retiring that kernel when it returns; if the call ends without
+ * setting the word, a device-side failure reported by moe_tail_get_status, it returns once
+ * the stream is idle).  Otherwise x and residual are copied to the handle's device staging
+ * buffers, the call runs there, residual and out are copied back (one copy each way when the
+ * buffers form one block [x; residual; out], residual_host = x_host + rows*H*2 bytes and
+ * out_host = residual_host + rows*H*2), and `stream` is synchronised. */
 int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residual_host, void* out_host,
                       int32_t rows, void* stream);
 

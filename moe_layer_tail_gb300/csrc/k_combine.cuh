@@ -76,4 +76,21 @@ __device__ __forceinline__ bool combine_wait_tiles(const Scratch& s, int c, uint
   return true;
 }
 
+// After a CTA's combine: when `done` is given, the last of the launch's nctas CTAs (a ticket
+// after a system-scope fence in every CTA) writes seq to the host-visible word done with a
+// system-scope release, so that a host thread that reads seq there (acquire) sees every
+// output of the call.  Every thread of the CTA calls it.
+__device__ __forceinline__ void signal_done(const Scratch& s, uint32_t* done, uint32_t seq,
+                                            uint32_t nctas) {
+  if (!done) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence_system();
+    if (atomicAdd(&s.counters[kCtrCombineTicket], 1u) == nctas - 1u) {
+      __threadfence_system();
+      asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(done), "r"(seq) : "memory");
+    }
+  }
+}
+
 }  // namespace mtail

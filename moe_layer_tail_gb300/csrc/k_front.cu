@@ -41,7 +41,7 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
               const __nv_bfloat16* __restrict__ wsg, float* __restrict__ sgate,
               const float* __restrict__ xpart, int Pk, size_t part_stride,
               uint8_t* __restrict__ np4, uint8_t* __restrict__ np4a,
-              unsigned long long* __restrict__ tl) {
+              unsigned long long* __restrict__ tl, const HostArgs* ha) {
   extern __shared__ uint4 s_gamma[];  // [H / 8]
   __shared__ float part[kNormThreads / 32];
   const int r = blockIdx.x;
@@ -49,6 +49,10 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   for (int c = threadIdx.x; c < H / 8; c += kNormThreads) s_gamma[c] = __ldg(g4 + c);
   pdl_wait();
   pdl_trigger();
+  if (ha) {  // a host-buffer call: its buffers (written before the launch)
+    x = reinterpret_cast<const __nv_bfloat16*>(ha_ptr(&ha->x));
+    residual = reinterpret_cast<const __nv_bfloat16*>(ha_ptr((const void* const*)&ha->residual));
+  }
   if (threadIdx.x == 0) tl_first(tl, kTlNormStart);
   if (r == 0)  // work counters, tickets and per-expert progress of this call
     for (int i = threadIdx.x; i < kCtrWords; i += kNormThreads) counters[i] = 0u;
@@ -64,11 +68,11 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
 cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
                                const __nv_bfloat16* residual, const Weights& w,
                                const Scratch& s, cudaStream_t st, bool pdl, const float* xpart,
-                               bool planes) {
+                               bool planes, const HostArgs* ha) {
   return launch_k(k_add_rmsnorm, dim3(d.R), dim3(kNormThreads), (size_t)d.H * 2, st, pdl, x,
                   residual, w.gamma, s.rnew, s.n, s.n16, s.n16s, s.counters, d.H, d.eps, w.wsg,
                   s.sgate, xpart, d.Pk, (size_t)d.Rmax * d.H, planes ? s.np4 : nullptr,
-                  planes ? s.np4a : nullptr, s.tl);
+                  planes ? s.np4a : nullptr, s.tl, ha);
 }
 
 // ------------------------------------------------------------------- router GEMV ----

@@ -66,11 +66,13 @@ cudaError_t persistent_smem_limit(int nmax, int* smem_limit);
 cudaError_t persistent_prepare(const TcMaps& maps, int* blocks_per_sm);
 
 // The whole call in one cooperative launch of `grid` CTAs (all resident at once); stall:
-// CTA 0 leaves at once (failure injection: the others' barrier waits expire).
+// CTA 0 leaves at once (failure injection: the others' barrier waits expire); done, seq, ha:
+// as for launch_combine (ha also gives x).
 cudaError_t launch_persistent(const TcMaps& maps, const Dims& d, const __nv_bfloat16* x,
                               __nv_bfloat16* residual, __nv_bfloat16* out, const Weights& w,
                               const Scratch& s, int grid, uint64_t budget_ns, bool stall,
-                              cudaStream_t st);
+                              cudaStream_t st, uint32_t* done = nullptr, uint32_t seq = 0u,
+                              const HostArgs* ha = nullptr);
 
 // Zero the barrier words of the persistent launch (after a call that gave up on a wait).
 cudaError_t persistent_reset(const Scratch& s);

@@ -293,26 +293,35 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
 __global__ void __launch_bounds__(256)
 k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
           __nv_bfloat16* __restrict__ residual, bool wait_tiles, uint64_t budget_ns,
-          bool gated) {
+          bool gated, uint32_t* done, uint32_t seq, const HostArgs* ha) {
   if (!wait_tiles) pdl_wait();
   pdl_trigger();
+  if (ha) {  // a host-buffer call: its buffers and number (written before the launch)
+    out = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(ha_ptr((const void* const*)&ha->out)));
+    residual = reinterpret_cast<__nv_bfloat16*>(
+        const_cast<void*>(ha_ptr((const void* const*)&ha->residual)));
+    seq = *reinterpret_cast<const volatile uint32_t*>(&ha->seq);
+  }
   if (threadIdx.x == 0) tl_first(s.tl, kTlCombineStart);
   const int H = dm.H;
   const int ng = H / 8;  // a multiple of 32: whole warps lie in one row
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= dm.R * ng) return;
-  const int r = idx / ng, c = idx % ng;
-  if (wait_tiles && !combine_wait_tiles(s, c, budget_ns)) return;
-  combine_one(dm, s, r, c, out, residual, gated);
-  if ((threadIdx.x & 31) == 0) tl_last(s.tl, kTlCombineEnd);
+  if (idx < dm.R * ng) {
+    const int r = idx / ng, c = idx % ng;
+    if (!wait_tiles || combine_wait_tiles(s, c, budget_ns))
+      combine_one(dm, s, r, c, out, residual, gated);
+    if ((threadIdx.x & 31) == 0) tl_last(s.tl, kTlCombineEnd);
+  }
+  signal_done(s, done, seq, gridDim.x);
 }
 
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
-                           uint64_t budget_ns, bool gated) {
+                           uint64_t budget_ns, bool gated, uint32_t* done, uint32_t seq,
+                           const HostArgs* ha) {
   const int n = d.R * d.H / 8;
   return launch_k(k_combine, dim3((n + 255) / 256), dim3(256), 0, st, pdl, d, s, out,
-                  residual, wait_tiles, budget_ns, gated);
+                  residual, wait_tiles, budget_ns, gated, done, seq, ha);
 }
 
 

@@ -436,6 +436,9 @@ struct PersistArgs {
   __nv_bfloat16* out;
   RouterPlan rp;
   int stall;  // failure injection: CTA 0 leaves at once, the others' barrier waits expire
+  uint32_t* done;  // host-visible completion word (signal_done), or null
+  uint32_t seq;
+  const HostArgs* ha;  // a host-buffer call: x, residual, out and seq from here instead
 };
 
 // The expert roles of one CTA over the items of launch phases PH0..PH1 (0 = gate/up, 1 =
@@ -464,6 +467,19 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   constexpr bool kPersist = PH0 != PH1;
   // failure-injection switch of the persistent launch (never set in production)
   if (kPersist && pa.stall && blockIdx.x == 0) return;
+  // the persistent launch's buffers (a host-buffer call's from its arguments)
+  const __nv_bfloat16* px = pa.x;
+  __nv_bfloat16* pres = pa.residual;
+  __nv_bfloat16* pout = pa.out;
+  uint32_t pseq = pa.seq;
+  if (kPersist && pa.ha) {
+    px = reinterpret_cast<const __nv_bfloat16*>(ha_ptr(&pa.ha->x));
+    pres = reinterpret_cast<__nv_bfloat16*>(
+        const_cast<void*>(ha_ptr((const void* const*)&pa.ha->residual)));
+    pout = reinterpret_cast<__nv_bfloat16*>(
+        const_cast<void*>(ha_ptr((const void* const*)&pa.ha->out)));
+    pseq = *reinterpret_cast<const volatile uint32_t*>(&pa.ha->seq);
+  }
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) set_status(s.status, kStatusBadTile);
     return;  // (persistent launch: the other CTAs' barrier waits expire)
@@ -484,7 +500,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
                                  pa.rp.plen, dm.H, dm.E);
     const int P = max(1, min((int)gridDim.x / dm.R, dm.H / 256));
     for (int v = blockIdx.x; v < dm.R * P; v += gridDim.x)
-      add_rmsnorm_part<kTcThreads>(v % dm.R, v / dm.R, P, pa.x, pa.residual, w.gamma, s.rnew,
+      add_rmsnorm_part<kTcThreads>(v % dm.R, v / dm.R, P, px, pres, w.gamma, s.rnew,
                                    s.n, dm.H, dm.eps, w.wsg,
                                    s.gate_part + (size_t)(v % dm.R) * kMaxNormParts, s.np4,
                                    s.np4a, part);
@@ -866,10 +882,11 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     const int ng = dm.H / 8;  // a multiple of 32: a warp's groups lie in one row
     for (int u = blockIdx.x * kTcThreads + threadIdx.x; u < dm.R * ng; u += gridDim.x * kTcThreads) {
       const int r = u / ng, c = u % ng;
-      if (!combine_wait_tiles(s, c, budget_ns)) return;
-      combine_one(dm, s, r, c, pa.out, pa.residual, w.wsg != nullptr);
+      if (!combine_wait_tiles(s, c, budget_ns)) break;  // whole warps
+      combine_one(dm, s, r, c, pout, pres, w.wsg != nullptr);
     }
     if ((threadIdx.x & 31) == 0) tl_last(s.tl, kTlCombineEnd);
+    signal_done(s, pa.done, pseq, gridDim.x);
   }
 }
 
@@ -908,7 +925,8 @@ template <int NMAX>
 static cudaError_t persist_launch(const TcMaps& maps, const Dims& d, const __nv_bfloat16* x,
                                   __nv_bfloat16* residual, __nv_bfloat16* out, const Weights& w,
                                   const Scratch& s, int grid, const RouterPlan& rp, size_t smem,
-                                  uint64_t budget_ns, int stall, cudaStream_t st) {
+                                  uint64_t budget_ns, int stall, cudaStream_t st, uint32_t* done,
+                                  uint32_t seq, const HostArgs* ha) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTcThreads);
@@ -925,13 +943,17 @@ static cudaError_t persist_launch(const TcMaps& maps, const Dims& d, const __nv_
   pa.out = out;
   pa.rp = rp;
   pa.stall = stall;
+  pa.done = done;
+  pa.seq = seq;
+  pa.ha = ha;
   return cudaLaunchKernelEx(&cfg, k_stream_tc<0, 1, NMAX>, maps, d, w, s, budget_ns, 0u, pa);
 }
 
 cudaError_t launch_persistent(const TcMaps& maps, const Dims& d, const __nv_bfloat16* x,
                               __nv_bfloat16* residual, __nv_bfloat16* out, const Weights& w,
                               const Scratch& s, int grid, uint64_t budget_ns, bool stall,
-                              cudaStream_t st) {
+                              cudaStream_t st, uint32_t* done, uint32_t seq,
+                              const HostArgs* ha) {
   const RouterPlan rp = router_plan(d.R, d.H, d.E, kTcThreads / 32);
   // the front's use of the same shared memory: gamma (2 H bytes), a router part, the last
   // part's logits and top-k workspace
@@ -939,10 +961,10 @@ cudaError_t launch_persistent(const TcMaps& maps, const Dims& d, const __nv_bflo
   const size_t smem = std::max(std::max((size_t)maps.lay.smem_bytes, rp.smem),
                                std::max((size_t)d.H * 2, topk));
   const int nmax = maps.lay.nmax, st_ = stall ? 1 : 0;
-  if (nmax == 16) return persist_launch<16>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st);
-  if (nmax == 32) return persist_launch<32>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st);
-  if (nmax == 64) return persist_launch<64>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st);
-  return persist_launch<128>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st);
+  if (nmax == 16) return persist_launch<16>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
+  if (nmax == 32) return persist_launch<32>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
+  if (nmax == 64) return persist_launch<64>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
+  return persist_launch<128>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
 }
 
 cudaError_t persistent_reset(const Scratch& s) {

@@ -38,6 +38,15 @@ struct moe_tail {
   void* stage;         // device staging for moe_tail_run_host: x, residual, out
   void* atoms;         // the tensor-core form's copy of w13s and w2s in scale-factor atoms
   int host_direct;     // the device reads pageable host memory through the host's page tables
+  uint32_t* hdone;     // page-locked completion word of moe_tail_run_host (mapped), or null
+  uint32_t* hdone_dev; // its device address
+  uint32_t hseq;       // the last value a call asked for in it
+  HostArgs* hargs;     // page-locked arguments of the host-buffer call (mapped, after hdone)
+  HostArgs* hargs_dev; // their device address
+  // moe_tail_run_host on a non-default stream: one graph per row count of the call's launches,
+  // which take the buffers from hargs
+  cudaGraph_t hgraph[kMaxRows + 1];
+  cudaGraphExec_t hexec[kMaxRows + 1];
   int device;
   int num_sms;
   int persist_grid;    // CTAs of the single persistent launch (MOE_TAIL_MODE_PERSISTENT)
@@ -311,9 +320,13 @@ extern "C" int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows) {
   return (h->cfg.debug_flags & MOE_TAIL_DEBUG_FUSED_FRONT) ? 4 : 5;
 }
 
-// One call: x is the tail's input, or null with attn the attention output to project first.
+// One call: x is the tail's input, or null with attn the attention output to project first;
+// done, seq: a host-visible word the call's last kernel sets to seq when its outputs are
+// visible to the host (null: none); ha: the tensor-core forms take x, residual, out and seq
+// from a host-buffer call's arguments at run time instead (null: as given).
 static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residual, void* out,
-                    int32_t rows, void* stream) {
+                    int32_t rows, void* stream, uint32_t* done = nullptr, uint32_t seq = 0u,
+                    const HostArgs* ha = nullptr) {
   cudaStream_t st = (cudaStream_t)stream;
   Dims d;
   d.R = rows;
@@ -351,7 +364,8 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
     // the whole call in one cooperative launch (such a handle has no out_proj stage)
     MT_STAGE(launch_persistent(h->tcmaps, d, (const __nv_bfloat16*)x, (__nv_bfloat16*)residual,
                                (__nv_bfloat16*)out, h->w, h->s, h->persist_grid, budget_ns,
-                               (h->cfg.debug_flags & MOE_TAIL_DEBUG_STALL_FIRST_STAGE) != 0, st));
+                               (h->cfg.debug_flags & MOE_TAIL_DEBUG_STALL_FIRST_STAGE) != 0, st,
+                               done, seq, ha));
     h->last_rows = rows;
     return MOE_TAIL_OK;
   }
@@ -393,7 +407,7 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
                                   h->w, h->s, st, pdl));
     } else {
       MT_STAGE(launch_add_rmsnorm(d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)residual,
-                                  h->w, h->s, st, pdl, xpart, tc));
+                                  h->w, h->s, st, pdl, xpart, tc, ha));
       MT_STAGE(launch_router_topk(d, h->w, h->s, st, pdl));
     }
     const uint32_t dbg = h->cfg.debug_flags;
@@ -408,7 +422,7 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   // after the streaming kernels the combine waits per 128 outputs for the down items that
   // write them; after the cross-checking kernels it waits for the previous launch
   MT_STAGE(launch_combine(d, h->s, (__nv_bfloat16*)out, (__nv_bfloat16*)residual, st, pdl,
-                          !simple, budget_ns, h->w.wsg != nullptr));
+                          !simple, budget_ns, h->w.wsg != nullptr, done, seq, ha));
 #undef MT_STAGE
   h->last_rows = rows;
   return MOE_TAIL_OK;
@@ -467,10 +481,68 @@ extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residu
     void* mr = h->host_direct ? residual_host : mx ? mapped_host(residual_host) : nullptr;
     void* mo = h->host_direct ? out_host : mr ? mapped_host(out_host) : nullptr;
     if (mo && aligned16(mx) && aligned16(mr) && aligned16(mo)) {
-      const int rc = run_impl(h, mx, nullptr, mr, mo, rows, stream);
-      if (rc) return rc;
-      e = cudaStreamSynchronize(st);
-      return e == cudaSuccess ? MOE_TAIL_OK : cuda_fail(e);
+      // the call's last kernel writes its number to a page-locked word once the outputs are
+      // visible to the host; the host polls that word (and, every few hundred polls, the
+      // stream, which ends the wait if the call finished without writing it: a device-side
+      // failure, reported by moe_tail_get_status)
+      if (!h->hdone) {
+        void* pg = nullptr;
+        e = cudaHostAlloc(&pg, 128, cudaHostAllocMapped);
+        void* dg = nullptr;
+        if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dg, pg, 0);
+        if (e != cudaSuccess) {
+          if (pg) cudaFreeHost(pg);
+          return cuda_fail(e);
+        }
+        h->hdone = (uint32_t*)pg;
+        h->hdone_dev = (uint32_t*)dg;
+        h->hargs = (HostArgs*)((char*)pg + 64);
+        h->hargs_dev = (HostArgs*)((char*)dg + 64);
+        __atomic_store_n(h->hdone, 0u, __ATOMIC_RELEASE);
+      }
+      const uint32_t seq = ++h->hseq ? h->hseq : ++h->hseq;  // never 0 (the initial value)
+      // the tensor-core forms on a non-default stream: a graph of the call's launches,
+      // captured once per row count, reads this call's buffers and number from hargs
+      const bool graph = uses_tc(&h->cfg) && h->n_ev == 0 && h->cfg.attn_dim == 0 &&
+                         st != nullptr && st != cudaStreamLegacy && st != cudaStreamPerThread;
+      if (graph) {
+        if (!h->hexec[rows]) {
+          e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+          if (e != cudaSuccess) return cuda_fail(e);
+          const int rc = run_impl(h, nullptr, nullptr, nullptr, nullptr, rows, stream,
+                                  h->hdone_dev, 0u, h->hargs_dev);
+          cudaGraph_t g = nullptr;
+          e = cudaStreamEndCapture(st, &g);
+          if (e == cudaSuccess && rc != MOE_TAIL_OK) e = cudaErrorUnknown;
+          cudaGraphExec_t ex = nullptr;
+          if (e == cudaSuccess) e = cudaGraphInstantiate(&ex, g, 0);
+          if (e != cudaSuccess) {
+            if (g) cudaGraphDestroy(g);
+            return rc != MOE_TAIL_OK ? rc : cuda_fail(e);
+          }
+          h->hgraph[rows] = g;
+          h->hexec[rows] = ex;
+        }
+        h->hargs->x = mx;
+        h->hargs->residual = mr;
+        h->hargs->out = mo;
+        h->hargs->seq = seq;
+        __atomic_thread_fence(__ATOMIC_SEQ_CST);  // the arguments before the launch
+        e = cudaGraphLaunch(h->hexec[rows], st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        h->last_rows = rows;
+      } else {
+        const int rc = run_impl(h, mx, nullptr, mr, mo, rows, stream, h->hdone_dev, seq);
+        if (rc) return rc;
+      }
+      for (uint32_t i = 1; __atomic_load_n(h->hdone, __ATOMIC_ACQUIRE) != seq; ++i) {
+        if ((i & 255) == 0) {
+          e = cudaStreamQuery(st);
+          if (e == cudaSuccess) break;
+          if (e != cudaErrorNotReady) return cuda_fail(e);
+        }
+      }
+      return MOE_TAIL_OK;
     }
   }
   if (in_block) {
@@ -547,6 +619,11 @@ extern "C" void moe_tail_destroy(moe_tail_t* h) {
   cudaFree(h->slab);
   cudaFree(h->stage);
   if (h->atoms) cudaFree(h->atoms);
+  for (int r = 0; r <= kMaxRows; ++r) {
+    if (h->hexec[r]) cudaGraphExecDestroy(h->hexec[r]);
+    if (h->hgraph[r]) cudaGraphDestroy(h->hgraph[r]);
+  }
+  if (h->hdone) cudaFreeHost(h->hdone);
   if (cur >= 0 && cur != h->device) cudaSetDevice(cur);
   delete h;
 }

@@ -50,6 +50,21 @@ struct Dims {
   float eps;
 };
 
+// The buffers and number of one host-buffer call (moe_tail_run_host), in page-locked memory
+// mapped into the device's address space: the kernels that read or write the call's buffers
+// take them from here at run time, so one captured graph serves every call.
+struct HostArgs {
+  const void* x;
+  void* residual;
+  void* out;
+  uint32_t seq;  // the value the call's last kernel writes to the completion word
+  uint32_t pad;
+};
+__device__ __forceinline__ const void* ha_ptr(const void* const* p) {
+  return reinterpret_cast<const void*>(
+      *reinterpret_cast<const volatile unsigned long long*>(p));
+}
+
 struct Weights {
   const __nv_bfloat16* gamma;
   const __nv_bfloat16* w_r;
@@ -140,6 +155,7 @@ enum : int {
   kCtrFrontTicket = 2,   // router CTAs done (the last one ranks the experts)
   kCtrRouted = 3,        // nonzero once the call's routing tables are written (release)
   kCtrSharedGUDone = 4,  // shared-expert gate/up items finished
+  kCtrCombineTicket = 10,  // combine CTAs done (the last one signals a host-visible word)
   kCtrGUDone = 16,       // [kMaxPicks] routed gate/up items finished, per distinct expert
   kCtrMidFlag = 16 + kMaxPicks,  // [kMaxPicks] nonzero: some 32-block of the expert's mid
                                  // carries a power-of-two scale
@@ -366,10 +382,12 @@ struct TcMaps {
 // ------------------------------------------------------------------ launchers ----
 // Each returns the cudaError_t of its launch.
 
+// ha: take x and residual from a host-buffer call's arguments instead (null: as given)
 cudaError_t launch_add_rmsnorm(const Dims& d, const __nv_bfloat16* x,
                                const __nv_bfloat16* residual, const Weights& w,
                                const Scratch& s, cudaStream_t st, bool pdl,
-                               const float* xpart = nullptr, bool planes = false);
+                               const float* xpart = nullptr, bool planes = false,
+                               const HostArgs* ha = nullptr);
 cudaError_t launch_router(const Dims& d, const Weights& w, const Scratch& s, cudaStream_t st,
                           bool pdl);
 cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, bool pdl);
@@ -410,8 +428,12 @@ RouterPlan router_plan(int R, int H, int E, int warps);
 // bytes of the two atom copies (w13a then w2a) and the launch that writes them from w13s, w2s
 size_t scale_atom_bytes(const Dims& d);
 cudaError_t launch_scale_atoms(const Dims& d, const Weights& w, uint8_t* atoms, cudaStream_t st);
+// done: a host-visible word the call's last combine CTA sets to seq once every output is
+// visible to the host (null: none); ha: take out, residual and seq from a host-buffer call's
+// arguments instead (null: as given)
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
-                           uint64_t budget_ns, bool gated);
+                           uint64_t budget_ns, bool gated, uint32_t* done = nullptr,
+                           uint32_t seq = 0u, const HostArgs* ha = nullptr);
 
 }  // namespace mtail

@@ -16,6 +16,7 @@ from moe_layer_tail_gb300 import (ERR_INVALID_ARG, ERR_UNSUPPORTED, STATUS_BAD_R
                                   MoeTailError, acts_to_device, bf16_tensor_to_bits,
                                   weights_to_device)
 from moe_layer_tail_gb300 import inputs as gen
+from moe_layer_tail_gb300 import MODE_PERSISTENT as MODE_PERSISTENT_ID
 from parity import bf16_step, check_parity, inject_near_ties
 
 torch = pytest.importorskip("torch")
@@ -360,6 +361,31 @@ def test_run_host_page_locked_buffers_match_device_runs():
         assert np.array_equal(bf16_tensor_to_bits(blk[1]), res_d), (rows, seed)
     ids, _, _ = tail.routing(2)
     assert ids.shape == (2, shape.k)
+    assert tail.status() == 0
+
+
+@pytest.mark.parametrize("mode", [0, MODE_PERSISTENT_ID])
+def test_run_host_returns_complete_results_back_to_back(mode):
+    """Twenty host-buffer calls in a row on one page-locked block each (the call returns when
+    the completion word its last kernel sets says so): every call's out and residual, read
+    right after it returns, match the device-buffer run of the same inputs bit for bit."""
+    shape, d = _small(19, R=3, H=512, E=12, k=3, I=256, Is=128)
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    tail = MoeTail(shape, dev, mode=mode)
+    stream = torch.cuda.Stream()
+    H = shape.H
+    for seed in range(20):
+        a = gen.make_activations(shape, 900 + seed, "plain")
+        dd = dict(d)
+        dd["x"], dd["residual"] = a["x"], a["residual"]
+        out_d, res_d, *_ = run_gpu(tail, dd)
+        blk = torch.empty((3, shape.R, H), dtype=torch.bfloat16).pin_memory()
+        blk[0].copy_(torch.from_numpy(a["x"].view(np.int16)).view(torch.bfloat16))
+        blk[1].copy_(torch.from_numpy(a["residual"].view(np.int16)).view(torch.bfloat16))
+        blk[2].fill_(0)
+        tail.run_host(blk[0], blk[1], blk[2], stream=stream)
+        assert np.array_equal(bf16_tensor_to_bits(blk[2]), out_d), seed
+        assert np.array_equal(bf16_tensor_to_bits(blk[1]), res_d), seed
     assert tail.status() == 0
 
 
