@@ -615,6 +615,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       uint32_t phase = 0;
       uint32_t pend = 0u, pend_par = 0u;
       bool skip_first = PHASE == 0 && (debug & kDebugStallFirstStage) && blockIdx.x == 0;
+      bool stamped = false, stamped_routed = false;  // timeline stamps taken (tracing only)
       // scale atoms per weight tile: over H (gate/up) or I (down), two per stage
       const int ga = sf_atoms_per_tile(PHASE == 0 ? dm.H : dm.I);
       // a CTA's first item is its index, later ones come from the counter (from gridDim.x on);
@@ -676,8 +677,14 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
           sp.info[stage] = make_int2(item, 0);
           mbar_expect_tx(&sp.full[stage], bytes);
-          tl_first(s.tl, PHASE == 0 ? kTlGateUpFirstCopy : kTlDownFirstCopy);
-          if (PHASE == 0 && it.kind == kRoutedGU) tl_first(s.tl, kTlGateUpRouted);
+          if (s.tl) {  // each CTA's first copy, and its first of a routed gate/up item
+            if (!stamped) tl_first(s.tl, PHASE == 0 ? kTlGateUpFirstCopy : kTlDownFirstCopy);
+            if (!stamped_routed && PHASE == 0 && it.kind == kRoutedGU) {
+              tl_first(s.tl, kTlGateUpRouted);
+              stamped_routed = true;
+            }
+            stamped = true;
+          }
           if (it.kind == kRoutedGU) {
             // the 64 gate and 64 up rows in one copy (3-D box over [2E][I][H/2])
             const int x = kc * (kChunkF4 / 2);
