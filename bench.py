@@ -90,6 +90,9 @@ def parse_args():
     p.add_argument("--no-pdl", action="store_true",
                    help="with --attnres-mix: plain launches instead of programmatic "
                         "dependent ones")
+    p.add_argument("--no-extras", action="store_true",
+                   help="the default line without its 'also_measured' entries (the AttnRes "
+                        "mix at 8 rows and the workload with the attention out_proj in front)")
     return p.parse_args()
 
 
@@ -767,6 +770,32 @@ def run_reference_mix(args, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def extras(args):
+    """Two more workloads of the same build, measured in the same run and reported beside the
+    headline line (not part of its value): the AttnRes mix at 8 rows (one step = one graph
+    replay of the 187-call sequence) and the headline workload with the attention output
+    projection (Ha 16384) in front of the tail, 100 calls."""
+    import copy
+    out = {}
+    a = copy.copy(args)
+    a.attnres_mix, a.steps, a.warmup, a.no_cpu_baseline = 8, 50, 5, True
+    m = run_mix(a, 0, 1, 0)
+    out["attnres_mix_8_rows"] = {
+        "metric": m["metric"], "value": m["value"], "unit": m["unit"], "steps": a.steps,
+        "roofline_frac": (m.get("roofline") or {}).get("frac"),
+        "e2e_value": (m.get("e2e") or {}).get("value"), "clocks": m.get("clocks"),
+        "config": m.get("config")}
+    b = copy.copy(args)
+    b.out_proj, b.steps, b.warmup = 16384, 100, 5
+    b.no_cpu_baseline, b.no_e2e, b.no_protocol, b.timeline = True, True, True, False
+    o = run_ours(b, 0, 1, 0)
+    out["out_proj_16384_in_front"] = {
+        "metric": o["metric"], "value": o["value"], "unit": o["unit"], "steps": b.steps,
+        "stages_us": o.get("stages_us"), "roofline": o.get("roofline"),
+        "clocks": o.get("clocks")}
+    return out
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -784,6 +813,10 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     res = (run_mix if args.attnres_mix else run_ours)(args, rank, world, local_rank)
+    if (rank == 0 and world == 1 and not args.no_extras and not args.attnres_mix
+            and not args.out_proj and not args.persistent and not args.mma_sync
+            and not args.experts and args.workload == gen.BENCH_WORKLOAD):
+        res["also_measured"] = extras(args)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

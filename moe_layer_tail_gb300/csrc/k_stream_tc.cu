@@ -328,9 +328,11 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
   constexpr int NSH = kSharedCols<NMAX>;  // bf16 (shared-expert) columns: the rows
   if (it.kind == kRoutedGU || it.kind == kSharedGU) {
     const int R = dm.Rmax;
-    float* xg = xch;            // [64][R] gate sums
-    float* xu = xch + 64 * R;   // [64][R] up sums
-    float* dst = (m < 64) ? xg + m * R : xu + (m - 64) * R;
+    // [R][64] gate sums, then [R][64] up sums: a warp's 32 lanes (weight rows) store, and the
+    // SiLU tasks' lanes (outputs) load, 32 consecutive words
+    float* xg = xch;
+    float* xu = xch + 64 * R;
+    float* dst = (m < 64) ? xg + m : xu + (m - 64);
     if (it.kind == kSharedGU && P > 1) {
       // one K part: its sums to scratch; the CTA whose part completes the item adds all parts
       // in part order (whichever CTAs ran them) and finishes it
@@ -354,7 +356,7 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
         if (c < R) {
           float a = __ldcg(g0 + c);
           for (int pp = 1; pp < P; ++pp) a += __ldcg(g0 + (size_t)pp * 128 * R + c);
-          dst[c] = a;
+          dst[c * 64] = a;
         }
       }
     } else if (it.kind == kRoutedGU) {
@@ -367,7 +369,7 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
           acc_chunk<C>(acc0, acc1, two, c0, v);
 #pragma unroll
           for (int c = 0; c < C / 4; ++c)
-            if (c0 / 4 + c < R) dst[c0 / 4 + c] = plane_sum<C>(v, c);
+            if (c0 / 4 + c < R) dst[(c0 / 4 + c) * 64] = plane_sum<C>(v, c);
         }
       }
     } else {
@@ -375,7 +377,7 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
       acc_chunk<NSH>(acc0, acc1, two, 0, v);
 #pragma unroll
       for (int c = 0; c < NSH; ++c)
-        if (c < R) dst[c] = v[c];
+        if (c < R) dst[c * 64] = v[c];
     }
     bar_epi();
     if (it.kind == kRoutedGU) {
@@ -385,7 +387,7 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
         const int slot = it.u0 + u;
         const int r = tb.users[slot] / dm.k;
         const int j = 32 * blk + lane;
-        const float g = xg[j * R + r], up = xu[j * R + r];
+        const float g = xg[r * 64 + j], up = xu[r * 64 + j];
         const float mv = __bfloat162float(__float2bfloat16_rn(silu_f(g) * up));
         const size_t cp = (size_t)dm.I / 2;
         // scales: atoms of this expert's down items, column 4 u + p (the planes of a user
@@ -399,7 +401,7 @@ __device__ __forceinline__ bool tc_finish(const Item& it, int item, int P, uint3
       for (int e = 32 * ew + lane; e < 64 * dm.R; e += 128) {
         const int j = e & 63, r = e >> 6;
         s.ms[(size_t)r * dm.Is + it.out0 + j] =
-            __float2bfloat16_rn(silu_f(xg[j * R + r]) * xu[j * R + r]);
+            __float2bfloat16_rn(silu_f(xg[r * 64 + j]) * xu[r * 64 + j]);
       }
     }
   } else if (it.kind == kRoutedDN) {
