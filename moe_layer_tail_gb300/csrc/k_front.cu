@@ -49,9 +49,15 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   for (int c = threadIdx.x; c < H / 8; c += kNormThreads) s_gamma[c] = __ldg(g4 + c);
   pdl_wait();
   pdl_trigger();
-  if (ha) {  // a host-buffer call: its buffers (written before the launch)
-    x = reinterpret_cast<const __nv_bfloat16*>(ha_ptr(&ha->x));
-    residual = reinterpret_cast<const __nv_bfloat16*>(ha_ptr((const void* const*)&ha->residual));
+  if (ha) {  // a host-buffer call: its buffers (written before the launch), read once per CTA
+    __shared__ const void* s_buf[2];
+    if (threadIdx.x == 0) {
+      s_buf[0] = ha_ptr(&ha->x);
+      s_buf[1] = ha_ptr((const void* const*)&ha->residual);
+    }
+    __syncthreads();
+    x = reinterpret_cast<const __nv_bfloat16*>(s_buf[0]);
+    residual = reinterpret_cast<const __nv_bfloat16*>(s_buf[1]);
   }
   if (threadIdx.x == 0) tl_first(tl, kTlNormStart);
   if (r == 0)  // work counters, tickets and per-expert progress of this call

@@ -296,11 +296,19 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
           bool gated, uint32_t* done, uint32_t seq, const HostArgs* ha) {
   if (!wait_tiles) pdl_wait();
   pdl_trigger();
-  if (ha) {  // a host-buffer call: its buffers and number (written before the launch)
-    out = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(ha_ptr((const void* const*)&ha->out)));
-    residual = reinterpret_cast<__nv_bfloat16*>(
-        const_cast<void*>(ha_ptr((const void* const*)&ha->residual)));
-    seq = *reinterpret_cast<const volatile uint32_t*>(&ha->seq);
+  if (ha) {  // a host-buffer call: its buffers and number (written before the launch), read
+             // once per CTA
+    __shared__ const void* s_buf[2];
+    __shared__ uint32_t s_seq;
+    if (threadIdx.x == 0) {
+      s_buf[0] = ha_ptr((const void* const*)&ha->out);
+      s_buf[1] = ha_ptr((const void* const*)&ha->residual);
+      s_seq = *reinterpret_cast<const volatile uint32_t*>(&ha->seq);
+    }
+    __syncthreads();
+    out = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(s_buf[0]));
+    residual = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(s_buf[1]));
+    seq = s_seq;
   }
   if (threadIdx.x == 0) tl_first(s.tl, kTlCombineStart);
   const int H = dm.H;

@@ -475,13 +475,20 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   __nv_bfloat16* pres = pa.residual;
   __nv_bfloat16* pout = pa.out;
   uint32_t pseq = pa.seq;
-  if (kPersist && pa.ha) {
-    px = reinterpret_cast<const __nv_bfloat16*>(ha_ptr(&pa.ha->x));
-    pres = reinterpret_cast<__nv_bfloat16*>(
-        const_cast<void*>(ha_ptr((const void* const*)&pa.ha->residual)));
-    pout = reinterpret_cast<__nv_bfloat16*>(
-        const_cast<void*>(ha_ptr((const void* const*)&pa.ha->out)));
-    pseq = *reinterpret_cast<const volatile uint32_t*>(&pa.ha->seq);
+  if (kPersist && pa.ha) {  // read once per CTA (host memory: every access crosses the link)
+    __shared__ const void* s_buf[3];
+    __shared__ uint32_t s_seq;
+    if (threadIdx.x == 0) {
+      s_buf[0] = ha_ptr(&pa.ha->x);
+      s_buf[1] = ha_ptr((const void* const*)&pa.ha->residual);
+      s_buf[2] = ha_ptr((const void* const*)&pa.ha->out);
+      s_seq = *reinterpret_cast<const volatile uint32_t*>(&pa.ha->seq);
+    }
+    __syncthreads();
+    px = reinterpret_cast<const __nv_bfloat16*>(s_buf[0]);
+    pres = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(s_buf[1]));
+    pout = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(s_buf[2]));
+    pseq = s_seq;
   }
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) set_status(s.status, kStatusBadTile);
@@ -501,7 +508,9 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
     if ((int)blockIdx.x < nparts)
       router_stage_w<kTcThreads>(smem, w.w_r, blockIdx.x % pa.rp.tiles, blockIdx.x / pa.rp.tiles,
                                  pa.rp.plen, dm.H, dm.E);
-    const int P = max(1, min((int)gridDim.x / dm.R, dm.H / 256));
+    // (a host-buffer call reads x and residual over the host link: at most 4 CTAs per row
+    // read each row, so that the whole-row reads for rstd stay small there)
+    const int P = max(1, min(min((int)gridDim.x / dm.R, dm.H / 256), pa.ha ? 4 : kMaxNormParts));
     for (int v = blockIdx.x; v < dm.R * P; v += gridDim.x)
       add_rmsnorm_part<kTcThreads>(v % dm.R, v / dm.R, P, px, pres, w.gamma, s.rnew,
                                    s.n, dm.H, dm.eps, w.wsg,

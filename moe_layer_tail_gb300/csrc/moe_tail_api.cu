@@ -523,16 +523,21 @@ extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residu
           h->hgraph[rows] = g;
           h->hexec[rows] = ex;
         }
-        h->hargs->x = mx;
-        h->hargs->residual = mr;
-        h->hargs->out = mo;
-        h->hargs->seq = seq;
-        __atomic_thread_fence(__ATOMIC_SEQ_CST);  // the arguments before the launch
+      }
+      // the kernels take the buffers and the call number from the argument block (written
+      // before the launch; the previous call has finished reading it)
+      h->hargs->x = mx;
+      h->hargs->residual = mr;
+      h->hargs->out = mo;
+      h->hargs->seq = seq;
+      __atomic_thread_fence(__ATOMIC_SEQ_CST);
+      if (graph) {
         e = cudaGraphLaunch(h->hexec[rows], st);
         if (e != cudaSuccess) return cuda_fail(e);
         h->last_rows = rows;
       } else {
-        const int rc = run_impl(h, mx, nullptr, mr, mo, rows, stream, h->hdone_dev, seq);
+        const int rc = run_impl(h, mx, nullptr, mr, mo, rows, stream, h->hdone_dev, seq,
+                                uses_tc(&h->cfg) && h->cfg.attn_dim == 0 ? h->hargs_dev : nullptr);
         if (rc) return rc;
       }
       for (uint32_t i = 1; __atomic_load_n(h->hdone, __ATOMIC_ACQUIRE) != seq; ++i) {
