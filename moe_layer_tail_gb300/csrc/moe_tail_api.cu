@@ -105,7 +105,7 @@ static int check_config(const moe_tail_config_t* c) {
   if (c->max_rows > kMaxRowsOther && (!uses_tc(c) || c->attn_dim != 0))
     return MOE_TAIL_ERR_UNSUPPORTED;
   // hidden: whole 256-element stages; above 2048 the E8M0 rows (hidden/32 bytes) must be
-  // whole 16-byte units for the scale-window tensor maps
+  // whole 16-byte units for the scale-window tensor maps of the CUDA-core form
   if (c->hidden < 256 || c->hidden % 256) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->hidden > 2048 && c->hidden % 512) return MOE_TAIL_ERR_UNSUPPORTED;
   if (c->hidden > (1 << 15)) return MOE_TAIL_ERR_UNSUPPORTED;

@@ -136,13 +136,19 @@ def test_mid_outside_f16_range_takes_block_scales(shift):
     _check_small(shape, d)
 
 
-def test_refresh_scales_follows_in_place_scale_changes():
-    """The default form reads the routed experts' E8M0 scales from a copy the handle makes at
-    create (scale-factor atoms).  After the caller rewrites w13_scales and w2_scales in place,
-    moe_tail_refresh_scales makes the next run follow the new scales: checked against the
-    oracle on the changed weights, with I = 384 (a half stage at the end of every down item)."""
+@pytest.mark.parametrize("mode", [0, MODE_PERSISTENT_ID])
+def test_refresh_scales_follows_in_place_scale_changes(mode):
+    """The tensor-core forms read the routed experts' E8M0 scales from a copy the handle makes
+    at create (scale-factor atoms).  After the caller rewrites w13_scales and w2_scales in
+    place, moe_tail_refresh_scales makes the next run follow the new scales: checked against
+    the oracle on the changed weights, with I = 384 (a half stage at the end of every down
+    item), in the multi-kernel form and the persistent launch."""
     shape, d = _small(23, R=5, H=768, E=9, k=3, I=384, Is=128)
-    tail, dev, _, _ = _check_small(shape, d)
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    orc = oracle.moe_tail(d, shape.k, shape.eps, nthreads=NTHREADS)
+    tail = MoeTail(shape, dev, mode=mode)
+    out, res, ids, _, _ = run_gpu(tail, d)
+    check_parity(out, res, ids, orc, shape.k)
     rng = np.random.default_rng(231)
     d2 = dict(d)
     for key in ("w13_scales", "w2_scales"):

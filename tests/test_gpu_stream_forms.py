@@ -174,3 +174,29 @@ def test_timeline_milestones_in_order():
                  ("combine_start", "combine_end"), ("down_end", "combine_end")]:
         assert t[a] <= t[b], (a, b, t)
     assert t["combine_end"] < 1e4  # microseconds: one call
+
+
+def test_timeline_milestones_in_order_persistent():
+    """The same milestones recorded by the single persistent launch, in causal order (its
+    combine starts once a CTA has left its down roles)."""
+    from moe_layer_tail_gb300 import DEBUG_TIMELINE, MODE_PERSISTENT
+    shape, d = _small(26, R=8, H=1024, E=32, k=4, I=512, Is=256, kind="similar")
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    orc = oracle.moe_tail(d, shape.k, shape.eps, nthreads=NTHREADS)
+    tail = MoeTail(shape, dev, mode=MODE_PERSISTENT, debug_flags=DEBUG_TIMELINE)
+    x = acts_to_device(d["x"])
+    res = acts_to_device(d["residual"])
+    out = torch.empty_like(x)
+    tail.run(x, res, out)
+    torch.cuda.synchronize()
+    ids, _, _ = tail.routing(shape.R)
+    check_parity(bf16_tensor_to_bits(out), bf16_tensor_to_bits(res), ids, orc, shape.k)
+    t = tail.timeline()
+    assert all(v is not None for v in t.values()), t
+    for a, b in [("norm_start", "norm_end"), ("norm_end", "router_start"),
+                 ("router_start", "topk_start"), ("topk_start", "routed"),
+                 ("gate_up_start", "gate_up_first_copy"), ("routed", "gate_up_routed"),
+                 ("down_start", "down_first_copy"), ("down_first_copy", "down_end"),
+                 ("combine_start", "combine_end"), ("down_end", "combine_end")]:
+        assert t[a] <= t[b], (a, b, t)
+    assert tail.status() == 0
