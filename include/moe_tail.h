@@ -138,7 +138,9 @@ enum {
   MOE_TAIL_TL_DOWN_END = 11,         /* down launch: last CTA done */
   MOE_TAIL_TL_COMBINE_START = 12,    /* combine launch: first CTA entered */
   MOE_TAIL_TL_COMBINE_END = 13,      /* combine launch: last output written */
-  MOE_TAIL_TL_SLOTS = 14
+  MOE_TAIL_TL_ROUTER_ALL_STARTED = 14, /* router launch: last CTA past its wait */
+  MOE_TAIL_TL_GATE_UP_ALL_COPYING = 15,/* gate/up launch: last CTA's first weight copy issued */
+  MOE_TAIL_TL_SLOTS = 16
 };
 
 typedef struct moe_tail moe_tail_t; /* opaque handle */

@@ -43,7 +43,8 @@ DEBUG_TIMELINE = 32
 # timeline slots (moe_tail_debug_timeline)
 TL_NAMES = ("norm_start", "norm_end", "router_start", "topk_start", "routed", "gate_up_start",
             "gate_up_first_copy", "gate_up_routed", "gate_up_end", "down_start",
-            "down_first_copy", "down_end", "combine_start", "combine_end")
+            "down_first_copy", "down_end", "combine_start", "combine_end",
+            "router_all_started", "gate_up_all_copying")
 
 # moe_attnres_mix launch flags (attnres_mix.h)
 ATTNRES_MIX_PDL = 1

@@ -175,7 +175,10 @@ k_router_topk(const __nv_bfloat16* __restrict__ w_r, Scratch s, int R, int H, in
   __shared__ int s_last;
   router_stage_w<kRtThreads>(sm, w_r, blockIdx.x, blockIdx.y, plen, H, E);
   pdl_wait();
-  if (threadIdx.x == 0) tl_first(s.tl, kTlRouterStart);
+  if (threadIdx.x == 0) {
+    tl_first(s.tl, kTlRouterStart);
+    tl_last(s.tl, kTlRouterAllStarted);
+  }
   // the expert launch may start as soon as every router CTA is past its wait: its
   // shared-expert items need only n (written by the norm launch, complete by now), and its
   // routed items wait for the kCtrRouted word this launch's last CTA sets

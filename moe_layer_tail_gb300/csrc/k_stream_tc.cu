@@ -234,8 +234,10 @@ __device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L, int
 }
 
 // K parts of every shared-expert gate/up item of this call: the fewest (1, 2 or 4, dividing
-// H / 64) that bring an item down to an SM's share of the launch's bytes, so that at one or a
-// few rows the shared items do not outlast the routed ones.  Every CTA computes the same.
+// H / 64) that bring an item down to an SM's share of the launch's bytes (so that at one or a
+// few rows the shared items do not outlast the routed ones) and give three quarters of the
+// CTAs a shared part to stream until the routing is known (a CTA whose first item is routed
+// waits for the router's tables).  Every CTA computes the same.
 __device__ __forceinline__ int shared_parts(const Dims& dm, int D, int nsm) {
   const int ns = dm.Is / 64;
   if (ns > kMaxSharedSplitItems) return 1;
@@ -244,7 +246,8 @@ __device__ __forceinline__ int shared_parts(const Dims& dm, int D, int nsm) {
   const uint64_t total = (uint64_t)ns * item_b + (uint64_t)D * (uint64_t)(dm.I / 64) * routed_b;
   const uint64_t share = total / (uint64_t)nsm;
   int p = 1;
-  while (p < kMaxSharedParts && item_b / (uint64_t)p > share && (dm.H / 64) % (2 * p) == 0)
+  while (p < kMaxSharedParts && (dm.H / 64) % (2 * p) == 0 &&
+         (item_b / (uint64_t)p > share || 4 * ns * p < 3 * nsm))
     p *= 2;
   return p;
 }
@@ -527,7 +530,10 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
         s.sgate[r] = 1.0f / (1.0f + expf(-z));
       }
     // 2. the router's parts (the first one's weights are already on their way)
-    if (threadIdx.x == 0) tl_first(s.tl, kTlRouterStart);
+    if (threadIdx.x == 0) {
+      tl_first(s.tl, kTlRouterStart);
+      if ((int)blockIdx.x < nparts) tl_last(s.tl, kTlRouterAllStarted);
+    }
     for (int v = blockIdx.x; v < nparts; v += gridDim.x) {
       const int tile = v % pa.rp.tiles, p = v / pa.rp.tiles;
       if (v != (int)blockIdx.x)
@@ -637,6 +643,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       const int base = claim_all ? 0 : (int)gridDim.x;
       int item = claim_all ? (int)atomicAdd(&s.counters[work_counter(PHASE)], 1u) : (int)blockIdx.x;
       bool have_tables = (PHASE == 1);
+      bool gu_all = false;  // every gate/up item of the call counted (down roles)
       while (ok) {
         if (!have_tables && item >= n_shared) {
           // the first routed item: the routing tables must be in shared memory
@@ -651,10 +658,18 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
         const bool routed = (it.kind == kRoutedGU || it.kind == kRoutedDN);
         const int hsel = (it.U <= 4) ? 0 : (it.U <= 8) ? 1 : (it.U <= 16) ? 2 : 3;
         const int nb = (it.kind == kRoutedGU) ? NMAX : (it.kind == kRoutedDN) ? (16 << hsel) : 0;
-        if (PHASE == 1) {
+        if (PHASE == 1 && !gu_all) {
+          // the item's inputs (the shared expert's or its expert's mid): wait for their gate/up
+          // items, then order the async proxy's reads after them; once every gate/up item of
+          // the call is counted, one such fence covers all later items
           const bool sh = (it.kind == kSharedDN);
-          if (!wait_count(&s.counters[sh ? kCtrSharedGUDone : kCtrGUDone + it.d],
-                          (uint32_t)(sh ? dm.Is / 64 : dm.I / 64), budget_ns)) {
+          uint32_t v;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v)
+                       : "l"(&s.counters[kCtrGUAllDone]) : "memory");
+          if (v >= (uint32_t)(D * (dm.I / 64) + dm.Is / 64)) {
+            gu_all = true;
+          } else if (!wait_count(&s.counters[sh ? kCtrSharedGUDone : kCtrGUDone + it.d],
+                                 (uint32_t)(sh ? dm.Is / 64 : dm.I / 64), budget_ns)) {
             ok = false;
             break;
           }
@@ -690,7 +705,10 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
           sp.info[stage] = make_int2(item, 0);
           mbar_expect_tx(&sp.full[stage], bytes);
           if (s.tl) {  // each CTA's first copy, and its first of a routed gate/up item
-            if (!stamped) tl_first(s.tl, PHASE == 0 ? kTlGateUpFirstCopy : kTlDownFirstCopy);
+            if (!stamped) {
+              tl_first(s.tl, PHASE == 0 ? kTlGateUpFirstCopy : kTlDownFirstCopy);
+              if (PHASE == 0) tl_last(s.tl, kTlGateUpAllCopying);
+            }
             if (!stamped_routed && PHASE == 0 && it.kind == kRoutedGU) {
               tl_first(s.tl, kTlGateUpRouted);
               stamped_routed = true;
@@ -870,15 +888,19 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
       float* xch = sp.xch;  // one buffer: the item-end barrier orders its reuse
       const bool done = tc_finish<NMAX>(it, item, P, acc0, acc1, xch, sp.eflag, ew, q, lane, dm,
                                         tb, s);
-      // every epilogue thread's stores before the count the next launch waits for
-      __threadfence();
+      // every epilogue thread's stores before the count the next launch waits for: the
+      // epilogue barrier orders them before the counting thread's fence and release
       tc_fence_before();
       bar_epi();
       if (done && ew == 0 && lane == 0) {
         uint32_t* c = &s.counters[PHASE == 1 ? kCtrTileDone + it.out0 / 128
                                   : it.kind == kSharedGU ? kCtrSharedGUDone
                                                          : kCtrGUDone + it.d];
+        __threadfence();
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
+        if (PHASE == 0)
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&s.counters[kCtrGUAllDone])
+                       : "memory");
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sp.aempty[as]);

@@ -27,8 +27,9 @@ constexpr int kMaxNormParts = 128;
 constexpr int kMaxPicks = kMaxRows * kMaxTopK;  // (row, slot) pairs of one call
 constexpr int kMaxOutProjParts = 8;  // K parts of an out_proj box at most
 // A shared-expert gate/up item (64 gate + 64 up rows over all of H) may be split along K into
-// up to kMaxSharedParts parts when it is larger than an SM's share of the launch (the tensor-
-// core form), for shared experts of at most kMaxSharedSplitItems items.
+// up to kMaxSharedParts parts when it is larger than an SM's share of the launch or when the
+// shared items are too few to keep most SMs streaming before the routing is known (the
+// tensor-core form), for shared experts of at most kMaxSharedSplitItems items.
 constexpr int kMaxSharedParts = 4;
 constexpr int kMaxSharedSplitItems = 256;
 
@@ -145,6 +146,8 @@ enum : int {
   kTlDownEnd,         // down launch: last CTA done
   kTlCombineStart,    // combine launch: first CTA entered
   kTlCombineEnd,      // combine launch: last output written
+  kTlRouterAllStarted,  // router launch: last CTA past its wait
+  kTlGateUpAllCopying,  // gate/up launch: last CTA's first weight copy issued
   kTlSlots
 };
 
@@ -155,6 +158,7 @@ enum : int {
   kCtrFrontTicket = 2,   // router CTAs done (the last one ranks the experts)
   kCtrRouted = 3,        // nonzero once the call's routing tables are written (release)
   kCtrSharedGUDone = 4,  // shared-expert gate/up items finished
+  kCtrGUAllDone = 5,     // gate/up items finished, shared and routed together (release)
   kCtrCombineTicket = 10,  // combine CTAs done (the last one signals a host-visible word)
   kCtrGUDone = 16,       // [kMaxPicks] routed gate/up items finished, per distinct expert
   kCtrMidFlag = 16 + kMaxPicks,  // [kMaxPicks] nonzero: some 32-block of the expert's mid

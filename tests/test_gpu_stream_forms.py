@@ -167,8 +167,11 @@ def test_timeline_milestones_in_order():
     t = tail.timeline()
     assert all(v is not None for v in t.values()), t
     assert t["norm_start"] == 0.0
-    for a, b in [("norm_start", "norm_end"), ("router_start", "topk_start"),
+    for a, b in [("norm_start", "norm_end"), ("router_start", "router_all_started"),
+                 ("router_all_started", "topk_start"),
                  ("topk_start", "routed"), ("gate_up_start", "gate_up_first_copy"),
+                 ("gate_up_first_copy", "gate_up_all_copying"),
+                 ("gate_up_all_copying", "gate_up_end"),
                  ("routed", "gate_up_routed"), ("gate_up_routed", "gate_up_end"),
                  ("down_start", "down_first_copy"), ("down_first_copy", "down_end"),
                  ("combine_start", "combine_end"), ("down_end", "combine_end")]:
@@ -194,8 +197,10 @@ def test_timeline_milestones_in_order_persistent():
     t = tail.timeline()
     assert all(v is not None for v in t.values()), t
     for a, b in [("norm_start", "norm_end"), ("norm_end", "router_start"),
-                 ("router_start", "topk_start"), ("topk_start", "routed"),
+                 ("router_start", "router_all_started"), ("router_all_started", "topk_start"),
+                 ("topk_start", "routed"),
                  ("gate_up_start", "gate_up_first_copy"), ("routed", "gate_up_routed"),
+                 ("gate_up_first_copy", "gate_up_all_copying"),
                  ("down_start", "down_first_copy"), ("down_first_copy", "down_end"),
                  ("combine_start", "combine_end"), ("down_end", "combine_end")]:
         assert t[a] <= t[b], (a, b, t)
