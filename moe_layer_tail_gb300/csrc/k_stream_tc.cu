@@ -237,8 +237,8 @@ __device__ __forceinline__ TcPtrs tc_carve(uint8_t* smem, const TcLayout& L, int
 // H / 64) that bring an item down to an SM's share of the launch's bytes (so that at one or a
 // few rows the shared items do not outlast the routed ones) and give three quarters of the
 // CTAs a shared part to stream until the routing is known (a CTA whose first item is routed
-// waits for the router's tables).  Every CTA computes the same.
-__device__ __forceinline__ int shared_parts(const Dims& dm, int D, int nsm) {
+// waits for the router's tables).  Computed on the host at launch (64-bit divisions).
+static int shared_parts(const Dims& dm, int D, int nsm) {
   const int ns = dm.Is / 64;
   if (ns > kMaxSharedSplitItems) return 1;
   const uint64_t item_b = 128ull * (uint64_t)dm.H * 2;
@@ -473,6 +473,16 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   constexpr bool kBoth = PH0 != PH1;  // gate/up roles, then down roles, in the same CTA
   // failure-injection switch of the persistent launch (never set in production)
   if (kPersist && pa.stall && blockIdx.x == 0) return;
+  // the tensor maps this CTA's copies will use (all encoded at create; mid4[i] for boxes of
+  // at most NMAX rows), fetched while the rest of the set-up runs
+  if (threadIdx.x < 32) {
+    const CUtensorMap* m = nullptr;
+    const int l = threadIdx.x;
+    if (PH0 == 0 && l < 4) m = l == 0 ? &maps.w13 : l == 1 ? &maps.np4 : l == 2 ? &maps.ws13 : &maps.n;
+    if (PH1 == 1 && l >= 4 && l < 8 && (16 << (l - 4)) <= NMAX) m = &maps.mid4[l - 4];
+    if (PH1 == 1 && l >= 8 && l < 11) m = l == 8 ? &maps.w2 : l == 9 ? &maps.ws2 : &maps.ms;
+    if (m) asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
+  }
   // the persistent launch's buffers (a host-buffer call's from its arguments)
   const __nv_bfloat16* px = pa.x;
   __nv_bfloat16* pres = pa.residual;
@@ -575,8 +585,7 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
   // shared memory by the epilogue warps once the router's last CTA has published them).  A
   // down-only launch starts after every gate/up CTA, and waits for the published routing once
   // before it reads the tables.
-  const int Dmax = min(dm.E, dm.R * dm.k);
-  const int P = (PHASE == 0) ? shared_parts(dm, Dmax, (int)gridDim.x) : 1;
+  const int P = (PHASE == 0) ? dm.sparts : 1;
   const int n_shared = (PHASE == 0) ? (dm.Is / 64) * P : 0;  // items that need no routing
   int D = 1, n_items = 0;
   if (PHASE == 1) {
@@ -661,18 +670,22 @@ k_stream_tc(const __grid_constant__ TcMaps maps, Dims dm, Weights w, Scratch s,
         if (PHASE == 1 && !gu_all) {
           // the item's inputs (the shared expert's or its expert's mid): wait for their gate/up
           // items, then order the async proxy's reads after them; once every gate/up item of
-          // the call is counted, one such fence covers all later items
+          // the call is counted, one such fence covers all later items.  Both counts are read
+          // together (relaxed), the fence after them takes the acquire side of their releases.
           const bool sh = (it.kind == kSharedDN);
-          uint32_t v;
-          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v)
+          const uint32_t* cd = &s.counters[sh ? kCtrSharedGUDone : kCtrGUDone + it.d];
+          const uint32_t need = (uint32_t)(sh ? dm.Is / 64 : dm.I / 64);
+          uint32_t va, vd;
+          asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(va)
                        : "l"(&s.counters[kCtrGUAllDone]) : "memory");
-          if (v >= (uint32_t)(D * (dm.I / 64) + dm.Is / 64)) {
+          asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(vd) : "l"(cd) : "memory");
+          if (va >= (uint32_t)(D * (dm.I / 64) + dm.Is / 64)) {
             gu_all = true;
-          } else if (!wait_count(&s.counters[sh ? kCtrSharedGUDone : kCtrGUDone + it.d],
-                                 (uint32_t)(sh ? dm.Is / 64 : dm.I / 64), budget_ns)) {
+          } else if (vd < need && !wait_count(cd, need, budget_ns)) {
             ok = false;
             break;
           }
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         // the item's scale atoms: its weight tile's (expert e, tile t) and its activations'
@@ -1002,10 +1015,12 @@ cudaError_t launch_persistent(const TcMaps& maps, const Dims& d, const __nv_bflo
   const size_t smem = std::max(std::max((size_t)maps.lay.smem_bytes, rp.smem),
                                std::max((size_t)d.H * 2, topk));
   const int nmax = maps.lay.nmax, st_ = stall ? 1 : 0;
-  if (nmax == 16) return persist_launch<16>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
-  if (nmax == 32) return persist_launch<32>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
-  if (nmax == 64) return persist_launch<64>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
-  return persist_launch<128>(maps, d, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
+  Dims dd = d;
+  dd.sparts = shared_parts(d, std::min(d.E, d.R * d.k), grid);
+  if (nmax == 16) return persist_launch<16>(maps, dd, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
+  if (nmax == 32) return persist_launch<32>(maps, dd, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
+  if (nmax == 64) return persist_launch<64>(maps, dd, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
+  return persist_launch<128>(maps, dd, x, residual, out, w, s, grid, rp, smem, budget_ns, st_, st, done, seq, ha);
 }
 
 cudaError_t persistent_reset(const Scratch& s) {
@@ -1061,7 +1076,11 @@ static cudaError_t tc_launch_n(const TcMaps& maps, const Dims& d, const Weights&
 cudaError_t launch_stream_tc(int phase, const TcMaps& maps, const Dims& d, const Weights& w,
                              const Scratch& s, int num_sms, uint64_t budget_ns, cudaStream_t st,
                              bool pdl, uint32_t debug) {
-  if (phase == 0) return tc_launch_n<0, 0>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
+  if (phase == 0) {
+    Dims dd = d;
+    dd.sparts = shared_parts(d, std::min(d.E, d.R * d.k), num_sms);
+    return tc_launch_n<0, 0>(maps, dd, w, s, num_sms, budget_ns, st, pdl, debug);
+  }
   return tc_launch_n<1, 1>(maps, d, w, s, num_sms, budget_ns, st, pdl, debug);
 }
 

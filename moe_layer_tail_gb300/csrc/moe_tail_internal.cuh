@@ -49,6 +49,7 @@ struct Dims {
   int Ha;       // attention out_proj K (0: none)
   int Pk;       // K parts of an out_proj box (1: the launch writes x itself)
   float eps;
+  int sparts = 1;  // K parts of a shared-expert gate/up item (tensor-core gate/up roles)
 };
 
 // The buffers and number of one host-buffer call (moe_tail_run_host), in page-locked memory

@@ -579,3 +579,32 @@ def test_graph_of_mixed_widths_replays_bitwise():
                 assert np.array_equal(bf16_tensor_to_bits(o), eo)
                 assert np.array_equal(bf16_tensor_to_bits(r), er)
     assert tail.status() == 0
+
+
+def test_back_to_back_mixed_widths_match_one_at_a_time():
+    """Calls of widths 8, 1, 5, 8, 2, 8, 3 issued back to back on one stream (each launch
+    may start while the previous one still runs) equal the same calls run one at a time."""
+    shape, d = _small(17, R=8, H=512, E=24, k=4, I=256, Is=192, kind="similar")
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    tail = MoeTail(shape, dev, max_rows=8)
+    widths = [8, 1, 5, 8, 2, 8, 3]
+    acts = [gen.make_activations(shape, 800 + i, rows=w) for i, w in enumerate(widths)]
+    xs = [acts_to_device(a["x"]) for a in acts]
+    r0 = [acts_to_device(a["residual"]) for a in acts]
+    single = []
+    for x, r in zip(xs, r0):
+        res, out = r.clone(), torch.empty_like(x)
+        tail.run(x, res, out)
+        torch.cuda.synchronize()
+        single.append((bf16_tensor_to_bits(out), bf16_tensor_to_bits(res)))
+    for _ in range(3):
+        res = [r.clone() for r in r0]
+        outs = [torch.empty_like(x) for x in xs]
+        torch.cuda.synchronize()
+        for x, r, o in zip(xs, res, outs):
+            tail.run(x, r, o)
+        torch.cuda.synchronize()
+        for (so, sr), o, r in zip(single, outs, res):
+            assert np.array_equal(bf16_tensor_to_bits(o), so)
+            assert np.array_equal(bf16_tensor_to_bits(r), sr)
+    assert tail.status() == 0
