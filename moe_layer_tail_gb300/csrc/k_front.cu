@@ -45,15 +45,23 @@ k_add_rmsnorm(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restri
   extern __shared__ uint4 s_gamma[];  // [H / 8]
   __shared__ float part[kNormThreads / 32];
   const int r = blockIdx.x;
+  // a host-buffer call: its buffers (written before the launch), read once per CTA, over the
+  // link while gamma is staged
+  const void* hx = nullptr;
+  const void* hr = nullptr;
+  if (ha && threadIdx.x == 0) {
+    hx = ha_ptr(&ha->x);
+    hr = ha_ptr((const void* const*)&ha->residual);
+  }
   const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
   for (int c = threadIdx.x; c < H / 8; c += kNormThreads) s_gamma[c] = __ldg(g4 + c);
   pdl_wait();
   pdl_trigger();
-  if (ha) {  // a host-buffer call: its buffers (written before the launch), read once per CTA
+  if (ha) {
     __shared__ const void* s_buf[2];
     if (threadIdx.x == 0) {
-      s_buf[0] = ha_ptr(&ha->x);
-      s_buf[1] = ha_ptr((const void* const*)&ha->residual);
+      s_buf[0] = hx;
+      s_buf[1] = hr;
     }
     __syncthreads();
     x = reinterpret_cast<const __nv_bfloat16*>(s_buf[0]);

@@ -9,6 +9,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <chrono>
 #include <new>
 
 #include <math.h>
@@ -482,9 +483,10 @@ extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residu
     void* mo = h->host_direct ? out_host : mr ? mapped_host(out_host) : nullptr;
     if (mo && aligned16(mx) && aligned16(mr) && aligned16(mo)) {
       // the call's last kernel writes its number to a page-locked word once the outputs are
-      // visible to the host; the host polls that word (and, every few hundred polls, the
-      // stream, which ends the wait if the call finished without writing it: a device-side
-      // failure, reported by moe_tail_get_status)
+      // visible to the host; the host polls that word (and, every 20 us or so, the stream,
+      // which ends the wait if the call finished without writing it: a device-side failure,
+      // reported by moe_tail_get_status).  The stream is queried rarely: a query costs the
+      // polling thread about a microsecond, during which the word's arrival goes unseen.
       if (!h->hdone) {
         void* pg = nullptr;
         e = cudaHostAlloc(&pg, 128, cudaHostAllocMapped);
@@ -540,8 +542,12 @@ extern "C" int moe_tail_run_host(moe_tail_t* h, const void* x_host, void* residu
                                 uses_tc(&h->cfg) && h->cfg.attn_dim == 0 ? h->hargs_dev : nullptr);
         if (rc) return rc;
       }
+      auto last = std::chrono::steady_clock::now();
       for (uint32_t i = 1; __atomic_load_n(h->hdone, __ATOMIC_ACQUIRE) != seq; ++i) {
-        if ((i & 255) == 0) {
+        if ((i & 63) == 0) {
+          const auto now = std::chrono::steady_clock::now();
+          if (now - last < std::chrono::microseconds(20)) continue;
+          last = now;
           e = cudaStreamQuery(st);
           if (e == cudaSuccess) break;
           if (e != cudaErrorNotReady) return cuda_fail(e);
