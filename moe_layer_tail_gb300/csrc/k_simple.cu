@@ -288,12 +288,16 @@ cudaError_t launch_experts_simple(const Dims& d, const Weights& w, const Scratch
 // One thread per 8 consecutive outputs of a row; the slots' loads are unrolled so that they
 // are in flight together.  wait_tiles: instead of waiting for the previous launch as a
 // whole, each warp waits (bounded, acquire) until the down items of the two 128-output
-// tiles it covers (the shared expert's and one per distinct expert) are counted done.
+// tiles it covers (the shared expert's and one per distinct expert) are counted done.  Before
+// that (down_grid > 0, the tensor-core down launch) one thread per CTA waits, polling every
+// 2 us, until the down launch's items are all claimed (each of its CTAs then streams its last
+// one): the per-tile polls of the whole combine grid, started as soon as the down launch
+// begins, had cost the streaming launches up to 18 us a call at 32 rows.
 
 __global__ void __launch_bounds__(256)
 k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
           __nv_bfloat16* __restrict__ residual, bool wait_tiles, uint64_t budget_ns,
-          bool gated, uint32_t* done, uint32_t seq, const HostArgs* ha) {
+          bool gated, uint32_t* done, uint32_t seq, const HostArgs* ha, int down_grid) {
   if (!wait_tiles) pdl_wait();
   pdl_trigger();
   if (ha) {  // a host-buffer call: its buffers and number (written before the launch), read
@@ -312,11 +316,24 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
   }
   if (threadIdx.x == 0) tl_first(s.tl, kTlCombineStart);
   const int H = dm.H;
+  bool claimed = true;
+  if (wait_tiles && down_grid > 0) {
+    __shared__ int s_claimed;
+    if (threadIdx.x == 0) {
+      const int D = min(max(__ldcg(s.n_distinct), 1), kMaxPicks);
+      const int n_items = (D + 1) * (H / 128);  // the down launch's items
+      const uint32_t need = (uint32_t)max(n_items - down_grid, 0);
+      s_claimed = wait_count(&s.counters[kCtrDown], need, budget_ns, 2000u) ? 1 : 0;
+      if (!s_claimed) set_status(s.status, kStatusTimeout);
+    }
+    __syncthreads();
+    claimed = s_claimed != 0;
+  }
   const int ng = H / 8;  // a multiple of 32: whole warps lie in one row
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx < dm.R * ng) {
     const int r = idx / ng, c = idx % ng;
-    if (!wait_tiles || combine_wait_tiles(s, c, budget_ns))
+    if (!wait_tiles || (claimed && combine_wait_tiles(s, c, budget_ns)))
       combine_one(dm, s, r, c, out, residual, gated);
     if ((threadIdx.x & 31) == 0) tl_last(s.tl, kTlCombineEnd);
   }
@@ -326,10 +343,10 @@ k_combine(Dims dm, Scratch s, __nv_bfloat16* __restrict__ out,
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
                            uint64_t budget_ns, bool gated, uint32_t* done, uint32_t seq,
-                           const HostArgs* ha) {
+                           const HostArgs* ha, int down_grid) {
   const int n = d.R * d.H / 8;
   return launch_k(k_combine, dim3((n + 255) / 256), dim3(256), 0, st, pdl, d, s, out,
-                  residual, wait_tiles, budget_ns, gated, done, seq, ha);
+                  residual, wait_tiles, budget_ns, gated, done, seq, ha, down_grid);
 }
 
 

@@ -423,7 +423,8 @@ static int run_impl(moe_tail_t* h, const void* x, const void* attn, void* residu
   // after the streaming kernels the combine waits per 128 outputs for the down items that
   // write them; after the cross-checking kernels it waits for the previous launch
   MT_STAGE(launch_combine(d, h->s, (__nv_bfloat16*)out, (__nv_bfloat16*)residual, st, pdl,
-                          !simple, budget_ns, h->w.wsg != nullptr, done, seq, ha));
+                          !simple, budget_ns, h->w.wsg != nullptr, done, seq, ha,
+                          tc ? h->num_sms : 0));
 #undef MT_STAGE
   h->last_rows = rows;
   return MOE_TAIL_OK;

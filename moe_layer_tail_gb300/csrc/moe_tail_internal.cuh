@@ -199,13 +199,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 
 // Bounded wait until *p >= need (acquire at GPU scope): false when the budget ran out.
-__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t need, uint64_t budget_ns) {
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t need, uint64_t budget_ns,
+                                           uint32_t sleep_ns = 64) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   if (v >= need) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    __nanosleep(64);
+    __nanosleep(sleep_ns);
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     if (v >= need) return true;
     if ((i & 15) == 0 && globaltimer() - t0 > budget_ns) return false;
@@ -435,10 +436,11 @@ size_t scale_atom_bytes(const Dims& d);
 cudaError_t launch_scale_atoms(const Dims& d, const Weights& w, uint8_t* atoms, cudaStream_t st);
 // done: a host-visible word the call's last combine CTA sets to seq once every output is
 // visible to the host (null: none); ha: take out, residual and seq from a host-buffer call's
-// arguments instead (null: as given)
+// arguments instead (null: as given); down_grid: the tensor-core down launch's grid, whose
+// items the combine waits to see all claimed before its per-tile waits (0: no such wait)
 cudaError_t launch_combine(const Dims& d, const Scratch& s, __nv_bfloat16* out,
                            __nv_bfloat16* residual, cudaStream_t st, bool pdl, bool wait_tiles,
                            uint64_t budget_ns, bool gated, uint32_t* done = nullptr,
-                           uint32_t seq = 0u, const HostArgs* ha = nullptr);
+                           uint32_t seq = 0u, const HostArgs* ha = nullptr, int down_grid = 0);
 
 }  // namespace mtail
