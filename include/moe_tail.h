@@ -267,8 +267,8 @@ int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows);
 
 /* Routing of one call with no device allocation at all, for callers that cannot call
  * cudaMalloc: a host framework that owns every device allocation and hands a plugin only
- * its input and output tensors, or a decode step replayed from a memory pool that is
- * frozen once warm-up is over.  It runs add + RMSNorm, the router GEMV and the top-k with
+ * its input and output tensors, or a decode step run from a memory pool that is frozen
+ * once warm-up is over.  It runs add + RMSNorm, the router GEMV and the top-k with
  * renormalised weights on `stream`, with the arithmetic of the fused front
  * (MOE_TAIL_DEBUG_FUSED_FRONT): its logits are summed in another order than the default
  * front of moe_tail_run (which runs the router on the tensor cores), so they may differ in
@@ -285,7 +285,7 @@ int moe_tail_launches_per_run(const moe_tail_t* h, int32_t rows);
  * exits).  The array bounds the call: rows <= 16, n_experts <= 1024, top_k <= 32 (and
  * hidden a multiple of 128); anything larger returns MOE_TAIL_ERR_UNSUPPORTED.  The first
  * call on a device looks up the array's device address with that device current (once,
- * safe from several host threads), so make that first call before any stream capture.
+ * safe from several host threads).
  * Every call shares the array and it keeps the last call's contents (each call clears its
  * status word and counter first): calls that overlap on the same GPU race, so issue them
  * in one stream or otherwise ordered.  Nothing is allocated or freed.  The pages have no

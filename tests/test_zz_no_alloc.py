@@ -1,6 +1,6 @@
 """moe_tail_route_noalloc: routing for callers that cannot allocate device memory (a host
 framework that owns every allocation and passes a plugin only its tensors, or a decode
-step replayed from a memory pool frozen after warm-up).  Its scratch is a fixed array
+step run from a memory pool frozen after warm-up).  Its scratch is a fixed array
 inside the library, so this file runs last: if it fails, every other test has already run.
 
 The entry point is checked against the CPU oracle with the parity rule of the other tests
