@@ -140,18 +140,21 @@ cudaError_t launch_topk_dedup(const Dims& d, const Scratch& s, cudaStream_t st, 
 // experts are the M rows, the call's rows the N columns).  The CTA's router weights are
 // copied into shared memory with cp.async before the wait on the norm launch (they depend
 // on nothing), then the rows' n for the part (up to 32 rows: four N-tiles of 8); each of
-// the 8 warps takes a slice of the part's 32-element K steps and the warps' partial tiles
+// the 16 warps takes a slice of the part's 32-element K steps and the warps' partial tiles
 // are added in warp order.  The
 // partial logits of each part go to scratch; the last CTA to finish (atomic ticket after a
-// fence) adds the parts in part order into shared memory, then runs top-k and the dedup.
+// fence) adds the parts in part order into shared memory, then runs top-k (one warp per row,
+// so 16 warps take up to 16 rows at once: a row's selection is a chain of dependent warp
+// reductions, ~1.5 us whatever else runs) and the dedup.
 // Loops stay rolled: every CTA runs this code once, so its size, not its instruction
 // count, sets the time an SM waits for instructions.
-constexpr int kRtWarps = 8;
+constexpr int kRtWarps = 16;
 constexpr int kRtThreads = kRtWarps * 32;
 
 // Parts: enough CTAs to spread the router weights over the SMs (about 128), parts of at
 // most 2048 elements, each a multiple of 32; the shared memory of a part for `warps` warps
-// (staged weights and rows, or the logits of the last part, then the warps' tiles).
+// (the largest of the staged weights and rows, the logits of the last part and the warps'
+// tiles: each overlays the one before).
 RouterPlan router_plan(int R, int H, int E, int warps) {
   RouterPlan p;
   p.tiles = (E + kRtTile - 1) / kRtTile;
@@ -165,8 +168,10 @@ RouterPlan router_plan(int R, int H, int E, int warps) {
     const size_t pitch = (size_t)p.plen * 2 + 16;
     const size_t tiles_bytes = (kRtTile + (size_t)R) * pitch;
     const size_t logit_bytes = (size_t)R * E * 4;
-    p.red_off = (int)(((std::max(tiles_bytes, logit_bytes) + 15) / 16) * 16);
-    p.smem = (size_t)p.red_off + (size_t)warps * nt * 32 * 16;
+    // the warps' reduction tiles overlay the staged tiles once every warp's MMAs are done
+    const size_t red_bytes = (size_t)warps * nt * 32 * 16;
+    p.red_off = 0;
+    p.smem = ((std::max(std::max(tiles_bytes, logit_bytes), red_bytes) + 15) / 16) * 16;
     if (p.smem <= 192 * 1024 || P >= kRtMaxParts) break;
   }
   return p;

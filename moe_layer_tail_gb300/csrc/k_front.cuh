@@ -626,6 +626,7 @@ __device__ __forceinline__ bool router_part(uint8_t* sm, const Scratch& s, int t
       }
     }
   }
+  __syncthreads();  // the reduction tiles may overlay the staged tiles every warp has read
 #pragma unroll
   for (int nt = 0; nt < kMaxRows / 8; ++nt)
     if (nt < NT)
