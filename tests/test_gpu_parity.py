@@ -288,6 +288,23 @@ def test_rows_below_max_and_batch_invariance():
     assert np.array_equal(sub[0], full[0][2:5])
 
 
+def test_batch_invariance_above_eight_rows():
+    """Twelve rows in one call equal each row alone and a 9-row subset, bit for bit: the
+    router's split over its warps, the expert stages' columns and the combine are the same
+    whatever the call's row count."""
+    shape, d = _small(18, R=12, H=512, E=20, k=4, I=256, Is=128, kind="similar")
+    dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
+    tail = MoeTail(shape, dev, max_rows=16)
+    full = run_gpu(tail, d)
+    for r in (0, 5, 11):
+        one = run_gpu(tail, {"x": d["x"][r:r + 1], "residual": d["residual"][r:r + 1]})
+        assert np.array_equal(one[0][0], full[0][r]), "row %d differs alone vs batched" % r
+        assert np.array_equal(one[1][0], full[1][r])
+    sub = run_gpu(tail, {"x": d["x"][1:10], "residual": d["residual"][1:10]})
+    assert np.array_equal(sub[0], full[0][1:10])
+    assert np.array_equal(sub[1], full[1][1:10])
+
+
 def test_determinism_and_graph_replay():
     shape, d = _small(11, R=4, H=512, E=24, k=4, I=256, Is=192)
     dev = weights_to_device({k: v for k, v in d.items() if k not in ("x", "residual")})
